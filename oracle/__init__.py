@@ -1,0 +1,216 @@
+"""NumPy front end of the plain CPU oracle (``moe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the GPU library and never imports it.
+
+Arrays: bf16 tensors travel as ``numpy.uint16`` holding the bf16 bit
+patterns; f32 as ``numpy.float32``; indices as ``numpy.int32``.  Every
+function mirrors one entry point of the GPU C-ABI, with host arrays and
+without stream or workspace.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+F32, BF16, F16 = 0, 1, 2
+OK, ERR_ARG, ERR_DTYPE, ERR_UNSUPPORTED = 0, -1, -2, -3
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        _lib = ctypes.CDLL(path)
+        _declare(_lib)
+    return _lib
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+
+
+def _declare(L: ctypes.CDLL) -> None:
+    sig = {
+        "oracle_abi_version": ([], _I),
+        "oracle_set_threads": ([_I], None),
+        "oracle_max_threads": ([], _I),
+        "oracle_bf16_to_f32": ([ctypes.c_uint16], _F),
+        "oracle_f32_to_bf16": ([_F], ctypes.c_uint16),
+        "oracle_f32_to_bf16_array": ([_P, _P, _I64], None),
+        "oracle_exp_f32": ([_F], _F),
+        "oracle_exp_f32_array": ([_P, _P, _I64], None),
+        "oracle_sigmoid_f32": ([_F], _F),
+        "oracle_route_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+        "oracle_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+        "oracle_gateup_silu": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I], _I),
+        "oracle_down": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P], _I),
+        "oracle_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I], _I),
+        "oracle_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I], _I),
+        "oracle_shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I], _I),
+        "oracle_moe_layer_tokens": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
+                                     _P, _I, _P, _P, _P], _I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dt(a) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float16:
+        return F16
+    raise TypeError(f"unsupported dtype {a.dtype}")
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        raise ValueError(f"oracle {what} refused its arguments (code {rc})")
+
+
+def set_threads(n: int) -> None:
+    lib().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+# ---------------------------------------------------------------- scalars
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening: the bf16 bits become the upper half of an f32."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_f32_to_bf16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def exp_f32(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    lib().oracle_exp_f32_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def sigmoid_f32(g: float) -> np.float32:
+    return np.float32(lib().oracle_sigmoid_f32(float(g)))
+
+
+# ---------------------------------------------------------------- steps
+def route_topk(x=None, w_router=None, logit_bias=None, w_shared_gate=None, logits_in=None, *,
+               T, H, E, K, renormalize=1, scoring=0, n_group=1, want_logits=False):
+    ids = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float32)
+    logits = np.zeros((T, E), np.float32) if want_logits else None
+    gl = np.zeros((T,), np.float32) if w_shared_gate is not None else None
+    rc = lib().oracle_route_topk(_ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(w_shared_gate),
+                                 _ptr(logits_in), T, H, E, K, renormalize, scoring, n_group,
+                                 _ptr(ids), _ptr(w), _ptr(logits), _ptr(gl))
+    _check(rc, "route_topk")
+    return ids, w, logits, gl
+
+
+def permute(topk_ids, x=None, *, T, K, E, H=0):
+    P = T * K
+    off = np.zeros((E + 1,), np.int32)
+    sp = np.zeros((P,), np.int32)
+    p2r = np.zeros((P,), np.int32)
+    xp = np.zeros((P, H), np.uint16) if x is not None else None
+    rc = lib().oracle_permute(_ptr(np.ascontiguousarray(topk_ids, np.int32)), _ptr(x), T, K, E, H,
+                              _ptr(off), _ptr(sp), _ptr(p2r), _ptr(xp))
+    _check(rc, "permute")
+    return off, sp, p2r, xp
+
+
+def gateup_silu(a, w13, group_offsets, *, P, H, I, G, a_row_gather=None, rows=None, narrow=1,
+                act=None):
+    if act is None:
+        act = np.zeros((P, I), np.uint16)
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    rc = lib().oracle_gateup_silu(_ptr(a), _ptr(a_row_gather), _ptr(w13), _ptr(group_offsets),
+                                  P, H, I, G, _ptr(r), 0 if r is None else r.size, _ptr(act),
+                                  narrow)
+    _check(rc, "gateup_silu")
+    return act
+
+
+def down(act, w2, group_offsets, *, P, I, H, G, pair_weight=None, row_to_pair=None, rows=None,
+         out=None):
+    if out is None:
+        out = np.zeros((P, H), np.uint16)
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    rc = lib().oracle_down(_ptr(act), _ptr(w2), _ptr(group_offsets), _ptr(pair_weight),
+                           _ptr(row_to_pair), P, I, H, G, _ptr(r), 0 if r is None else r.size,
+                           _ptr(out))
+    _check(rc, "down")
+    return out
+
+
+def combine(expert_out, w=None, shared=None, *, routed_scale=1.0, T, K, H, out_dtype=BF16):
+    out = np.zeros((T, H), np.float32 if out_dtype == F32 else np.uint16)
+    rc = lib().oracle_combine(_ptr(expert_out), _dt(expert_out), _ptr(w), _ptr(shared),
+                              _dt(shared) if shared is not None else BF16, routed_scale, T, K, H,
+                              _ptr(out), out_dtype)
+    _check(rc, "combine")
+    return out
+
+
+def combine_gate(expert_out, w, sd, gl, *, routed_scale=1.0, T, K, H, out_dtype=BF16):
+    out = np.zeros((T, H), np.float32 if out_dtype == F32 else np.uint16)
+    rc = lib().oracle_combine_gate(_ptr(expert_out), _dt(expert_out), _ptr(w), _ptr(sd), _dt(sd),
+                                   _ptr(gl), routed_scale, T, K, H, _ptr(out), out_dtype)
+    _check(rc, "combine_gate")
+    return out
+
+
+def shared_expert_gate(sd, gl, *, T, H, out_dtype=BF16):
+    out = np.zeros((T, H), np.float32 if out_dtype == F32 else np.uint16)
+    rc = lib().oracle_shared_expert_gate(_ptr(sd), _dt(sd), _ptr(gl), T, H, _ptr(out), out_dtype)
+    _check(rc, "shared_expert_gate")
+    return out
+
+
+def moe_layer_tokens(x, w_router, logit_bias, w13, w2, w_shared_gate, w13_shared, w2_shared, *,
+                     H, I, E, K, I_shared=0, routed_scale=1.0, tokens):
+    tok = np.ascontiguousarray(tokens, np.int32)
+    n = tok.size
+    ids = np.zeros((n, K), np.int32)
+    w = np.zeros((n, K), np.float32)
+    out = np.zeros((n, H), np.uint16)
+    rc = lib().oracle_moe_layer_tokens(_ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(w13),
+                                       _ptr(w2), _ptr(w_shared_gate), _ptr(w13_shared),
+                                       _ptr(w2_shared), H, I, E, K, I_shared, routed_scale,
+                                       _ptr(tok), n, _ptr(ids), _ptr(w), _ptr(out))
+    _check(rc, "moe_layer_tokens")
+    return out, ids, w
+
+
+def abi_version() -> int:
+    return int(lib().oracle_abi_version())
+
+
+__all__ = [n for n in dir() if not n.startswith("_")]
