@@ -1,0 +1,373 @@
+"""Benchmark of the BF16 MoE expert block on GB300.
+
+Default workload: the prefill MoE layer (T=8192 tokens, H=2048, I=768, E=128
+experts, top-8 renormalised softmax router with Zipf(1.1)-skewed expert load,
+no shared expert).  One step = one full forward of the block: router (logits
+GEMM + top-k), permute, grouped gate/up GEMM + SiLU-mul, grouped down GEMM
+with routing weight and scatter, combine.  Inputs are synthetic and seeded;
+the weights (1.21 GB) exceed the 126 MB L2, so no step finds the previous
+step's operands in cache.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config prefill|decode|large] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+tokens of a batch are independent: weak scaling, no collective on the data
+path); rank 0 prints one JSON line with value = all ranks' tokens / max time.
+--impl reference times the CPU oracle (the plain sequential definition of the
+block) on this host's cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM TFLOP/s and combine GB/s vs peak"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = {}
+            for k in FALLBACK:
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                out[k] = float(v) if v is not None else FALLBACK[k]
+            return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def layer_config(name):
+    from mixture_experts_ffn_renorm_gb300 import workloads as W
+
+    return {"prefill": W.PREFILL, "decode": W.DECODE, "large": W.LARGE, "tiny": W.TINY}[name]
+
+
+def config_dict(cfg, ws):
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K,
+            "I_shared": cfg.I_shared, "zipf_s": cfg.zipf_s, "tokens_per_gpu": cfg.T,
+            "global_batch": cfg.T * ws, "parallelism": f"dp{ws} (independent replicas)",
+            "l2": "operands larger than L2 (weights 1.21 GB > 126 MB), no flush needed"
+            if cfg.T >= 8192 else "L2 flushed between steps (256 MB write)"}
+
+
+def oracle_tokens_per_s(cfg, d, seconds=10.0):
+    """Time the CPU oracle on a bounded sample of the workload's tokens."""
+    import oracle as O
+
+    def run(tokens):
+        t0 = time.perf_counter()
+        O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
+                           d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H, I=cfg.I,
+                           E=cfg.E, K=cfg.K, I_shared=cfg.I_shared,
+                           tokens=np.asarray(tokens, np.int32))
+        return time.perf_counter() - t0
+
+    cores = O.max_threads()
+    t1 = run(np.arange(min(cores, cfg.T)))
+    per_tok = t1 / min(cores, cfg.T)
+    n = int(max(min(cores, cfg.T), min(cfg.T, seconds / max(per_tok, 1e-9))))
+    dt = run(np.arange(n))
+    return n / dt, cores, n, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    cfg = layer_config(args.config)
+    from mixture_experts_ffn_renorm_gb300 import workloads as W
+    from oracle import build as ob
+
+    ob.build()
+    d = W.layer_inputs(cfg)
+    import oracle as O
+
+    cores = O.max_threads()
+    n = max(cores, 8) if cfg.T >= 64 else cfg.T
+    tokens = np.arange(n, dtype=np.int32)
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
+                           d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H, I=cfg.I,
+                           E=cfg.E, K=cfg.K, I_shared=cfg.I_shared, tokens=tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
+                           d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H, I=cfg.I,
+                           E=cfg.E, K=cfg.K, I_shared=cfg.I_shared, tokens=tokens)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_dict(cfg, 1),
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "tokens/s",
+                         "sample": f"{n} of {cfg.T} tokens per step, full block per token"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    ws, rank, local = dist_setup(args)
+    import __graft_entry__ as ge
+
+    if rank == 0 or ws == 1:
+        ge.build()
+    barrier(ws)
+    import mixture_experts_ffn_renorm_gb300 as m
+    from mixture_experts_ffn_renorm_gb300 import workloads as W
+    from mixture_experts_ffn_renorm_gb300.layer import MoeBlock
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = layer_config(args.config)
+    d = W.layer_inputs(cfg)
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
+                   I_shared=cfg.I_shared)
+    x_host = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    x_dev = x_host.to(dev)
+    out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    flush = None
+    if cfg.T < 8192:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        blk.forward(x_dev)
+    torch.cuda.synchronize()
+
+    # ---------------- timed: device-resident inputs
+    counts0 = m.moe_launch_counts()
+    step_marks = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        t_start.record()
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            marks = []
+            blk.forward(x_dev, marks=marks)
+            step_marks.append(marks)
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+    counts1 = m.moe_launch_counts()
+    launches = sum(b - a for a, b in zip(counts0, counts1))
+    if flush is None:
+        step_ms = t_start.elapsed_time(t_end) / args.steps
+    else:  # the L2 flush between steps is not part of a step
+        step_ms = sum(mk[0][1].elapsed_time(mk[-1][1]) for mk in step_marks) / args.steps
+    ms = max_over_ranks(step_ms, ws, dev)
+    value = ws * cfg.T / (ms / 1000.0)
+
+    stage_ms = {}
+    for marks in step_marks:
+        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
+            stage_ms.setdefault(name, []).append(a.elapsed_time(b))
+    stage_avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+
+    # ---------------- end to end through the public API with host buffers
+    e2e_steps = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        o = blk.forward(x_dev)
+        out_host.copy_(o, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    e2e_value = ws * cfg.T / (e2e_ms / 1000.0)
+
+    # ---------------- roofline of the dominant kernel (the gate/up GEMM)
+    pk, pk_src = peaks()
+    P = cfg.T * cfg.K
+    flop_gateup = 2.0 * P * cfg.H * 2 * cfg.I
+    flop_down = 2.0 * P * cfg.I * cfg.H
+    t_gu = stage_avg["gemm_gateup"] / 1000.0
+    t_dn = stage_avg["gemm_down"] / 1000.0
+    achieved = flop_gateup / t_gu / 1e12
+    comb_bytes = P * cfg.H * 2 + cfg.T * cfg.H * 2
+    if cfg.I_shared:
+        comb_bytes += cfg.T * cfg.H * 2 + cfg.T * 4
+    roofline = {"kernel": "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)",
+                "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                "peak_source": f"{pk_src} bf16 dense (burst)", "traffic": None,
+                "algorithmic_flop_per_launch": flop_gateup}
+    components = {
+        "ms": stage_avg,
+        "gemm_gateup_tflops": achieved,
+        "gemm_down_tflops": flop_down / t_dn / 1e12,
+        "gemm_down_frac": flop_down / t_dn / 1e12 / pk["bf16_tflops"],
+        "combine_gbs": comb_bytes / (stage_avg["combine"] / 1000.0) / 1e9,
+        "combine_frac_hbm": comb_bytes / (stage_avg["combine"] / 1000.0) / 1e9 / pk["hbm_gbs"],
+        "route_gbs": (cfg.T * cfg.H * 2 + cfg.E * cfg.H * 2) / (stage_avg["route"] / 1000.0) / 1e9,
+        "permute_gbs": (2 * P * cfg.H * 2 + P * 16) / (stage_avg["permute"] / 1000.0) / 1e9,
+        "hbm_peak_gbs": pk["hbm_gbs"],
+    }
+    counts = np.diff(blk.expert_offsets.cpu().numpy())
+    components["expert_load"] = {"max": int(counts.max()), "mean": float(counts.mean()),
+                                 "min": int(counts.min())}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, cores, n, dt = oracle_tokens_per_s(cfg, d, seconds=args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} of {cfg.T} tokens, whole block per token, {dt:.1f} s"}
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded normal inputs and weights, Zipf-skewed router bias)",
+            "config": config_dict(cfg, ws),
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(cfg.T * cfg.H * 2),
+                    "d2h_bytes_per_step": int(cfg.T * cfg.H * 2)},
+            "gpu_launches": launches,
+            "roofline": roofline,
+            "components": components,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="prefill", choices=["prefill", "decode", "large", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,266 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the BF16 Mixture-of-Experts expert block of an
+ * LLM forward pass on one GB300 (sm_103a).
+ *
+ *   moe_route_topk                     ungrouped softmax router, top-k, renormalise
+ *   moe_permute                        tokens -> expert-contiguous rows
+ *   moe_grouped_gemm_gateup_silu_bf16  grouped gate/up GEMM fused with SiLU-and-mul
+ *   moe_grouped_gemm_down_bf16         grouped down GEMM, routing weight, scatter
+ *   moe_combine                        weighted top-k sum (+ optional shared term)
+ *   moe_combine_gate                   combine with the shared-expert sigmoid gate
+ *   shared_expert_gate                 out = sigmoid(gl) * sd
+ *
+ * Sources (vllm.cpp pages):
+ *   [I3094]  issue #3094 "Row: BACKEND-ROCM-BF16-MOE": names the two grouped
+ *            BF16 GEMM ops and the numeric contract -- BF16 narrowing of the
+ *            gate/up result before activation, routing weight applied before
+ *            the down result is stored, reduction without applying the
+ *            weights twice.
+ *   [PR509]  PR #509 "MoE combine/gate ops -- SharedExpertGate, MoeCombine,
+ *            MoeCombineGate": "What changed" (the three formulas), the review
+ *            (dtype refusals, production dtype arms, bit-exactness), the
+ *            rework commits (sequential K order, single store rounding, no
+ *            contraction; routed_scale on the routed sum before the shared
+ *            term), "Honest gaps" (the covered router is ungrouped softmax).
+ *   [PR523]  PR #509's stacked follow-up #523, "What changed": the expert GEMM
+ *            is grouped over expert ids; activation scratch is capture-safe
+ *            and never reallocated during reuse.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or synchronises inside a call.  Scratch memory is
+ *     a caller-provided workspace sized by the matching *_workspace_size query.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it and returns.
+ *   - Row-major layouts.  bf16 = IEEE binary32 rounded to nearest even and
+ *     truncated to its upper 16 bits.  T tokens, H hidden, I per-expert
+ *     intermediate, E experts, K experts per token, P = T*K routed rows.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code; nothing is
+ *     enqueued when a call fails its argument checks.  moe_last_error()
+ *     returns a thread-local message naming what was refused.
+ *   - T = 0 (P = 0) is a legal no-op.  Data pointers must be 16-byte aligned
+ *     and H, I multiples of 8 (MOE_ERR_ALIGN otherwise).
+ *   - Bit-exact ops (router selection and weights, permute, combine, gate)
+ *     give the same bits as the plain sequential definitions in their
+ *     comments; the grouped GEMMs accumulate in f32 in tensor-core order.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 /* always refused, see [PR509] review */ };
+
+/* return codes */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,         /* a size, count or pointer argument is invalid */
+  MOE_ERR_DTYPE = -2,       /* dtype other than f32/bf16 (f16 is refused by name) */
+  MOE_ERR_UNSUPPORTED = -3, /* a router form outside ungrouped softmax */
+  MOE_ERR_ALIGN = -4,       /* pointer not 16-byte aligned or H/I not a multiple of 8 */
+  MOE_ERR_WORKSPACE = -5,   /* workspace missing or smaller than the size query */
+  MOE_ERR_CUDA = -6,        /* launch or runtime error (message from the CUDA runtime) */
+  MOE_ERR_TIMEOUT = -7      /* a device-side wait hit its iteration cap (see moe_device_status) */
+};
+
+/* Thread-local message for the last failing call on this thread. */
+const char* moe_last_error(void);
+
+/* Library ABI version (bumped on any signature change). */
+int moe_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
+ * covered router path is ungrouped softmax; grouped / bias-corrected forms
+ * are refused).
+ *
+ *   l[t,e] = sum_h f32(x[t,h]) * f32(w_router[e,h])  (+ logit_bias[e])
+ *            f32 accumulation in tensor-core order (not bit-exact vs a
+ *            sequential sum; within the dot-product error bound).
+ *   Selection: the K largest l[t,:] in descending order; equal logits go to
+ *            the lower expert id; NaN ranks below every number.
+ *   Weights (renormalize=1): m = l of rank 0, e_j = expf_cr(l_j - m),
+ *            S = ((e_0 + e_1) + ...) + e_{K-1} from +0, w_j = e_j / S.
+ *            (renormalize=0: S sums expf_cr(l_e - m) over all e in id order.)
+ *            expf_cr is the binary32 rounding of a fixed double-precision
+ *            evaluation (Cody-Waite reduction with ln2 split in a 32-bit head
+ *            and a tail, Taylor series through r^13, scaling by 2^n); its
+ *            result is the correctly rounded exp on every input tested.
+ *   Given the same logits (logits_in), ids and weights are bit-exact.
+ *
+ *   x            bf16 [T,H]        (ignored when logits_in != NULL)
+ *   w_router     bf16 [E,H]        (ignored when logits_in != NULL)
+ *   logit_bias   f32  [E] or NULL  added to every logit before selection and weights
+ *   w_shared_gate bf16 [H] or NULL if set, gate_logit_out[t] = sum_h x[t,h]*wsg[h]
+ *   logits_in    f32  [T,E] or NULL: use these logits instead of the GEMM
+ *   T >= 0, H > 0 (multiple of 8), 1 <= K <= min(E, 32), E <= 1024
+ *   renormalize  1 (the block's path) or 0
+ *   scoring      0 = softmax (anything else: MOE_ERR_UNSUPPORTED)
+ *   n_group      1 (anything else: MOE_ERR_UNSUPPORTED)
+ *   topk_ids     int32 [T,K] out, rank order
+ *   topk_w       f32   [T,K] out
+ *   logits_out   f32   [T,E] out or NULL
+ *   gate_logit_out f32 [T] out; required when w_shared_gate != NULL
+ *   workspace    >= moe_route_topk_workspace_size(T, E, K) bytes (may be 0)
+ * ---------------------------------------------------------------------- */
+int moe_route_topk(const void* x_bf16, const void* w_router_bf16, const float* logit_bias,
+                   const void* w_shared_gate_bf16, const float* logits_in, int T, int H, int E,
+                   int K, int renormalize, int scoring, int n_group, int32_t* topk_ids,
+                   float* topk_w, float* logits_out, float* gate_logit_out, void* workspace,
+                   size_t ws_bytes, void* stream);
+size_t moe_route_topk_workspace_size(int T, int E, int K);
+
+/* ------------------------------------------------------------------------
+ * moe_permute -- stable counting sort of the P = T*K (token, slot) pairs by
+ * expert, so each expert's rows are contiguous for the grouped GEMMs ([PR509]
+ * review: the expert path stores P permuted rows, "ddown {P, H}"; [PR523]:
+ * grouped over expert ids).  Rows of one expert keep ascending pair order
+ * p = t*K + j.  Bit-exact.
+ *
+ *   topk_ids       int32 [T,K] in, each in [0,E) (checked on the device:
+ *                  out-of-range ids are counted nowhere and raise the device
+ *                  status flag MOE_STATUS_BAD_ID)
+ *   x              bf16 [T,H] or NULL (indices only)
+ *   expert_offsets int32 [E+1] out: exclusive scan of the per-expert counts
+ *   sorted_pair    int32 [P] out: sorted_pair[row] = p
+ *   pair_to_row    int32 [P] out: inverse of sorted_pair
+ *   x_perm         bf16 [P,H] out or NULL: x_perm[row] = x[sorted_pair[row] / K]
+ *   T >= 0, 1 <= K <= 32, 1 <= E <= 1024, H multiple of 8 when x != NULL
+ *   workspace      >= moe_permute_workspace_size(T, K, E) bytes
+ * ---------------------------------------------------------------------- */
+int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, int K, int E, int H,
+                int32_t* expert_offsets, int32_t* sorted_pair, int32_t* pair_to_row,
+                void* x_perm_bf16, void* workspace, size_t ws_bytes, void* stream);
+size_t moe_permute_workspace_size(int T, int K, int E);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_gemm_gateup_silu_bf16 -- kMoeGroupedGemmBf16GateUpSilu of
+ * [I3094].  For every group g and row r in [group_offsets[g], group_offsets[g+1]):
+ *   gate[n] = bf16( sum_h A[r,h] * w13[g, n, h] )        n in [0, I)
+ *   up[n]   = bf16( sum_h A[r,h] * w13[g, I + n, h] )
+ *   act[r,n] = bf16( silu(f32 gate[n]) * f32 up[n] ),  silu(z) = z / (1 + exp(-z))
+ * f32 accumulation on tcgen05 tensor cores; both halves are narrowed to bf16
+ * BEFORE the activation ([I3094] "BF16 result narrowing before activation").
+ *
+ *   a            bf16 [P,H] (rows in group order), or, when a_row_gather is
+ *                set, bf16 [n_src,H] read through a_row_gather
+ *   a_row_gather int32 [P] or NULL: row r of the product uses A row a_row_gather[r]
+ *                (e.g. sorted_pair[r] / K to read x [T,H] without x_perm)
+ *   w13          bf16 [G, 2I, H]: gate rows first, then up rows, per group
+ *   group_offsets int32 [G+1], non-decreasing, group_offsets[G] <= P;
+ *                read on the device (no host round trip); may be NULL when G == 1
+ *                (one group of P rows)
+ *   act          bf16 [P,I] out; rows outside every group are not written
+ *   P >= 0, H > 0 and I > 0 multiples of 64, 1 <= G <= 1024
+ *   workspace    >= moe_grouped_gemm_workspace_size(...) bytes (currently 0)
+ * ---------------------------------------------------------------------- */
+int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, const int32_t* a_row_gather,
+                                      const void* w13_bf16, const int32_t* group_offsets,
+                                      int P, int H, int I, int G, void* act_bf16,
+                                      void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_gemm_down_bf16 -- kMoeGroupedGemmBf16 of [I3094].  For every
+ * group g and row r in it:
+ *   y[n] = sum_i act[r,i] * w2[g, n, i]   (f32, tensor cores)
+ *   out[dst, n] = bf16( y[n] * pair_weight[dst] )   dst = row_to_pair ? row_to_pair[r] : r
+ * The routing weight is applied exactly once, as one f32 multiply before the
+ * one bf16 rounding of the store ([I3094] "routing-weight placement before the
+ * down-projection result is stored"); a combine after it must not apply it again.
+ *
+ *   act          bf16 [P,I]
+ *   w2           bf16 [G,H,I]
+ *   group_offsets int32 [G+1] (as above; NULL allowed when G == 1)
+ *   pair_weight  f32 [P] indexed by dst, or NULL (no weight: the shared expert)
+ *   row_to_pair  int32 [P] or NULL (store in row order)
+ *   out          bf16 [P,H] out (pair order when row_to_pair is set, i.e. [T,K,H])
+ *   P >= 0, H > 0 and I > 0 multiples of 64, 1 <= G <= 1024
+ * ---------------------------------------------------------------------- */
+int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
+                               const int32_t* group_offsets, const float* pair_weight,
+                               const int32_t* row_to_pair, int P, int I, int H, int G,
+                               void* out_bf16, void* workspace, size_t ws_bytes, void* stream);
+size_t moe_grouped_gemm_workspace_size(int P, int H, int I, int G);
+
+/* ------------------------------------------------------------------------
+ * moe_combine -- kMoeCombine of [PR509].  Per output element, sequentially:
+ *   acc = +0.0f
+ *   for k = 0 .. K-1:  acc = acc + (w ? f32(eo[t,k,c]) * w[t,k] : f32(eo[t,k,c]))
+ *   acc = acc * routed_scale
+ *   if shared: acc = acc + f32(shared[t,c])
+ *   out[t,c] = acc rounded once to out_dtype
+ * Every operation is a separately rounded binary32 op (no fused multiply-add),
+ * so the result is bit-exact against the sequential definition.  In the
+ * expert block the down GEMM already applied the weights: pass w = NULL.
+ *
+ *   expert_out  [T,K,H] f32 or bf16 (eo_dtype)
+ *   w           f32 [T,K] or NULL
+ *   shared      [T,H] f32 or bf16 (sh_dtype) or NULL
+ *   out         [T,H] f32 or bf16 (out_dtype)
+ *   T >= 0, 1 <= K <= 64, H > 0 multiple of 8
+ * ---------------------------------------------------------------------- */
+int moe_combine(const void* expert_out, int eo_dtype, const float* w, const void* shared,
+                int sh_dtype, float routed_scale, int T, int K, int H, void* out, int out_dtype,
+                void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_combine_gate -- kMoeCombineGate of [PR509]: the combine with the shared
+ * expert's sigmoid gate folded in and the gated shared term rounded through
+ * bf16 before it is added:
+ *   s   = sigmoid(gl[t]) = 1 / (1 + expf_cr(-gl[t]))
+ *   sv  = f32( bf16( s * f32(sd[t,c]) ) )
+ *   acc = the routed sum of moe_combine (w optional), acc = acc * routed_scale
+ *   out[t,c] = (acc + sv) rounded once to out_dtype
+ * Bit-exact.  sd f32 or bf16; out f32 or bf16; gl f32 [T].
+ * ---------------------------------------------------------------------- */
+int moe_combine_gate(const void* expert_out, int eo_dtype, const float* w, const void* sd,
+                     int sd_dtype, const float* gl, float routed_scale, int T, int K, int H,
+                     void* out, int out_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * shared_expert_gate -- kSharedExpertGate of [PR509]:
+ *   out[t,c] = sigmoid(gl[t]) * sd[t,c], one rounding to out_dtype.
+ * Four dtype arms: sd f32/bf16 x out f32/bf16.  Bit-exact.
+ * ---------------------------------------------------------------------- */
+int shared_expert_gate(const void* sd, int sd_dtype, const float* gl, int T, int H, void* out,
+                       int out_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Introspection (not on the hot path; these synchronise the device).
+ *
+ * moe_device_status: reads and optionally clears the library's device status
+ * word, a bit set of MOE_STATUS_* raised by kernels (a bounded wait that ran
+ * out, an out-of-range expert id).  Returns MOE_OK or MOE_ERR_CUDA.
+ *
+ * moe_launch_counts: copies the per-kernel launch counters (incremented by
+ * each kernel on the device, so they count kernels that actually ran) into
+ * counts[0 .. n-1], indexed by MOE_KID_*; returns the number of counters.
+ * ---------------------------------------------------------------------- */
+enum { MOE_STATUS_TIMEOUT = 1, MOE_STATUS_BAD_ID = 2 };
+enum {
+  MOE_KID_ROUTE_LOGITS = 0,
+  MOE_KID_ROUTE_TOPK = 1,
+  MOE_KID_PERMUTE_COUNT = 2,
+  MOE_KID_PERMUTE_SCAN = 3,
+  MOE_KID_PERMUTE_PLACE = 4,
+  MOE_KID_PERMUTE_GATHER = 5,
+  MOE_KID_GEMM_GATEUP = 6,
+  MOE_KID_GEMM_DOWN = 7,
+  MOE_KID_COMBINE = 8,
+  MOE_KID_COMBINE_GATE = 9,
+  MOE_KID_SHARED_GATE = 10,
+  MOE_KID_COUNT = 16
+};
+int moe_device_status(int* status_out, int clear);
+int moe_launch_counts(unsigned long long* counts, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

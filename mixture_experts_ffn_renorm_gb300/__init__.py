@@ -1,0 +1,197 @@
+"""Python binding of libmoe.so: the BF16 MoE expert block on one GB300.
+
+Argument marshalling only.  Every function here has the name, argument order
+and meaning of the C entry point declared in ``include/moe.h``; tensors are
+passed as raw device pointers (``tensor.data_ptr()``), the stream defaults to
+PyTorch's current stream, and a negative return code raises ``MoeError`` with
+the library's message.  All compute runs in the library's CUDA kernels: there
+is no fallback of any kind, and calling into a missing or unbuilt library
+raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe.so")
+
+F32, BF16, F16 = 0, 1, 2
+OK = 0
+ERR_ARG, ERR_DTYPE, ERR_UNSUPPORTED, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = (
+    -1, -2, -3, -4, -5, -6, -7)
+STATUS_TIMEOUT, STATUS_BAD_ID = 1, 2
+KID = {
+    "route_logits": 0, "route_topk": 1, "permute_count": 2, "permute_scan": 3,
+    "permute_place": 4, "permute_gather": 5, "gemm_gateup": 6, "gemm_down": 7, "combine": 8,
+    "combine_gate": 9, "shared_gate": 10,
+}
+KID_COUNT = 16
+
+EXPORTS = (
+    "moe_last_error", "moe_abi_version", "moe_route_topk", "moe_route_topk_workspace_size",
+    "moe_permute", "moe_permute_workspace_size", "moe_grouped_gemm_gateup_silu_bf16",
+    "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
+    "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "moe_last_error": ([], ctypes.c_char_p),
+    "moe_abi_version": ([], _I),
+    "moe_route_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ,
+                        _P], _I),
+    "moe_route_topk_workspace_size": ([_I, _I, _I], _SZ),
+    "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
+    "moe_grouped_gemm_gateup_silu_bf16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
+    "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
+    "moe_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I, _P], _I),
+    "shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I, _P], _I),
+    "moe_device_status": ([ctypes.POINTER(_I), _I], _I),
+    "moe_launch_counts": ([ctypes.POINTER(ctypes.c_ulonglong), _I], _I),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmoe.so.  Raises if it has not been built (see build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"libmoe.so is not built at {LIB_PATH}; run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise MoeError(rc, lib().moe_last_error().decode(errors="replace"))
+    return rc
+
+
+def last_error() -> str:
+    return lib().moe_last_error().decode(errors="replace")
+
+
+def abi_version() -> int:
+    return lib().moe_abi_version()
+
+
+# ------------------------------------------------------------------ entry points
+def moe_route_topk(x, w_router, logit_bias, w_shared_gate, logits_in, T, H, E, K, renormalize,
+                   scoring, n_group, topk_ids, topk_w, logits_out, gate_logit_out, workspace,
+                   ws_bytes, stream=None, check=True):
+    rc = lib().moe_route_topk(_ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(w_shared_gate),
+                              _ptr(logits_in), T, H, E, K, renormalize, scoring, n_group,
+                              _ptr(topk_ids), _ptr(topk_w), _ptr(logits_out),
+                              _ptr(gate_logit_out), _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_route_topk_workspace_size(T, E, K) -> int:
+    return lib().moe_route_topk_workspace_size(T, E, K)
+
+
+def moe_permute(topk_ids, x, T, K, E, H, expert_offsets, sorted_pair, pair_to_row, x_perm,
+                workspace, ws_bytes, stream=None, check=True):
+    rc = lib().moe_permute(_ptr(topk_ids), _ptr(x), T, K, E, H, _ptr(expert_offsets),
+                           _ptr(sorted_pair), _ptr(pair_to_row), _ptr(x_perm), _ptr(workspace),
+                           ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_permute_workspace_size(T, K, E) -> int:
+    return lib().moe_permute_workspace_size(T, K, E)
+
+
+def moe_grouped_gemm_gateup_silu_bf16(a, a_row_gather, w13, group_offsets, P, H, I, G, act,
+                                      workspace=None, ws_bytes=0, stream=None, check=True):
+    rc = lib().moe_grouped_gemm_gateup_silu_bf16(_ptr(a), _ptr(a_row_gather), _ptr(w13),
+                                                 _ptr(group_offsets), P, H, I, G, _ptr(act),
+                                                 _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_down_bf16(act, w2, group_offsets, pair_weight, row_to_pair, P, I, H, G, out,
+                               workspace=None, ws_bytes=0, stream=None, check=True):
+    rc = lib().moe_grouped_gemm_down_bf16(_ptr(act), _ptr(w2), _ptr(group_offsets),
+                                          _ptr(pair_weight), _ptr(row_to_pair), P, I, H, G,
+                                          _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_workspace_size(P, H, I, G) -> int:
+    return lib().moe_grouped_gemm_workspace_size(P, H, I, G)
+
+
+def moe_combine(expert_out, eo_dtype, w, shared, sh_dtype, routed_scale, T, K, H, out, out_dtype,
+                stream=None, check=True):
+    rc = lib().moe_combine(_ptr(expert_out), eo_dtype, _ptr(w), _ptr(shared), sh_dtype,
+                           float(routed_scale), T, K, H, _ptr(out), out_dtype, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_combine_gate(expert_out, eo_dtype, w, sd, sd_dtype, gl, routed_scale, T, K, H, out,
+                     out_dtype, stream=None, check=True):
+    rc = lib().moe_combine_gate(_ptr(expert_out), eo_dtype, _ptr(w), _ptr(sd), sd_dtype, _ptr(gl),
+                                float(routed_scale), T, K, H, _ptr(out), out_dtype,
+                                _stream(stream))
+    return _check(rc) if check else rc
+
+
+def shared_expert_gate(sd, sd_dtype, gl, T, H, out, out_dtype, stream=None, check=True):
+    rc = lib().shared_expert_gate(_ptr(sd), sd_dtype, _ptr(gl), T, H, _ptr(out), out_dtype,
+                                  _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_device_status(clear: bool = False) -> int:
+    v = _I(0)
+    _check(lib().moe_device_status(ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
+def moe_launch_counts() -> list[int]:
+    buf = (ctypes.c_ulonglong * KID_COUNT)()
+    n = _check(lib().moe_launch_counts(buf, KID_COUNT))
+    return [int(buf[i]) for i in range(n)]

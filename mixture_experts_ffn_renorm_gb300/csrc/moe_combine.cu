@@ -1,0 +1,269 @@
+// moe_combine.cu -- kMoeCombine, kMoeCombineGate and kSharedExpertGate
+// (vllm.cpp PR #509 "MoE combine/gate ops -- SharedExpertGate, MoeCombine,
+// MoeCombineGate": "What changed" gives the formulas; the review rework makes
+// them bit-exact: sequential K order, one store rounding, no contraction; the
+// routed_scale rework scales the finished routed sum before the shared term).
+//
+// Design: a pure HBM stream.  One thread owns 8 consecutive channels of one
+// token, so every expert row, shared row and output row moves as one 16-byte
+// vector per thread (two for f32) and a warp touches 512 contiguous bytes per
+// load.  All K expert vectors of a thread are in flight at once.  The sigmoid
+// of the gate is evaluated once per token per block (it costs a short chain of
+// double-precision operations, which GB300 runs at a low rate), by as many
+// threads as the block has tokens, overlapped with the loads.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVec = 8;       // channels per thread
+constexpr int kChunkK = 8;    // expert rows loaded per batch of loads
+
+enum Mode { kCombine = 0, kCombineGate = 1, kGateOnly = 2 };
+
+template <typename T>
+struct Vec8;
+template <>
+struct Vec8<float> {
+  __device__ __forceinline__ static void load(const void* base, size_t idx, float* v) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  __device__ __forceinline__ static void store(void* base, size_t idx, const float* v) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + idx);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+template <>
+struct Vec8<__nv_bfloat16> {
+  __device__ __forceinline__ static void load(const void* base, size_t idx, float* v) {
+    uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx));
+    uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ static void store(void* base, size_t idx, const float* v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(v[2 * i])) |
+             (static_cast<uint32_t>(f32_to_bf16_bits(v[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + idx) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+__device__ __forceinline__ float round_through_bf16(float v) {
+  return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(v)) << 16);
+}
+
+template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
+               const void* __restrict__ sh, const float* __restrict__ gl, float rs, int T, int K,
+               int H, void* __restrict__ out, unsigned long long* launches, int kid) {
+  count_launch(launches, kid);
+  __shared__ float s_gate[kThreads];
+  const int ipr = H / kVec;                         // items per token row
+  const long long first = static_cast<long long>(blockIdx.x) * kThreads;
+  const long long item = first + threadIdx.x;
+  const long long n_items = static_cast<long long>(T) * ipr;
+  const bool live = item < n_items;
+  const int t = live ? static_cast<int>(item / ipr) : 0;
+  const int c0 = live ? static_cast<int>(item % ipr) * kVec : 0;
+
+  float shv[kVec];
+  if (kMode != kCombine || kHasShared) {
+    if (live) Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
+  }
+
+  float acc[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
+
+  if (kMode != kGateOnly && live) {
+    const size_t row0 = static_cast<size_t>(t) * K;
+    for (int k0 = 0; k0 < K; k0 += kChunkK) {
+      float v[kChunkK][kVec];
+      const int kn = min(kChunkK, K - k0);
+#pragma unroll
+      for (int j = 0; j < kChunkK; ++j)
+        if (j < kn) Vec8<EoT>::load(eo, (row0 + k0 + j) * H + c0, v[j]);
+#pragma unroll
+      for (int j = 0; j < kChunkK; ++j) {
+        if (j < kn) {
+          float wk = kHasW ? __ldg(w + row0 + k0 + j) : 1.0f;
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) {
+            float term = kHasW ? __fmul_rn(v[j][i], wk) : v[j][i];
+            acc[i] = __fadd_rn(acc[i], term);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = __fmul_rn(acc[i], rs);
+  }
+
+  if (kMode != kCombine) {
+    // one sigmoid per token of this block
+    const int t_first = static_cast<int>(first / ipr);
+    long long last_item = first + kThreads - 1;
+    if (last_item >= n_items) last_item = n_items - 1;
+    const int n_rows = static_cast<int>(last_item / ipr) - t_first + 1;
+    if (static_cast<int>(threadIdx.x) < n_rows) s_gate[threadIdx.x] = sigmoid_cr(__ldg(gl + t_first + threadIdx.x));
+    __syncthreads();
+    if (!live) return;
+    const float s = s_gate[t - t_first];
+    float o[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      float g = __fmul_rn(s, shv[i]);
+      o[i] = (kMode == kGateOnly) ? g : __fadd_rn(acc[i], round_through_bf16(g));
+    }
+    Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, o);
+    return;
+  }
+  if (!live) return;
+  if (kHasShared) {
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = __fadd_rn(acc[i], shv[i]);
+  }
+  Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, acc);
+}
+
+using KernelFn = void (*)(const void*, const float*, const void*, const float*, float, int, int,
+                          int, void*, unsigned long long*, int);
+
+template <int kMode, typename EoT, typename ShT, typename OutT>
+KernelFn pick_w_sh(bool has_w, bool has_sh) {
+  if (has_w) return has_sh ? combine_kernel<kMode, EoT, ShT, OutT, true, true>
+                           : combine_kernel<kMode, EoT, ShT, OutT, true, false>;
+  return has_sh ? combine_kernel<kMode, EoT, ShT, OutT, false, true>
+                : combine_kernel<kMode, EoT, ShT, OutT, false, false>;
+}
+
+template <int kMode, typename EoT, typename ShT>
+KernelFn pick_out(int out_dt, bool has_w, bool has_sh) {
+  return out_dt == MOE_F32 ? pick_w_sh<kMode, EoT, ShT, float>(has_w, has_sh)
+                           : pick_w_sh<kMode, EoT, ShT, __nv_bfloat16>(has_w, has_sh);
+}
+
+template <int kMode, typename EoT>
+KernelFn pick_sh(int sh_dt, int out_dt, bool has_w, bool has_sh) {
+  return sh_dt == MOE_F32 ? pick_out<kMode, EoT, float>(out_dt, has_w, has_sh)
+                          : pick_out<kMode, EoT, __nv_bfloat16>(out_dt, has_w, has_sh);
+}
+
+template <int kMode>
+KernelFn pick(int eo_dt, int sh_dt, int out_dt, bool has_w, bool has_sh) {
+  return eo_dt == MOE_F32 ? pick_sh<kMode, float>(sh_dt, out_dt, has_w, has_sh)
+                          : pick_sh<kMode, __nv_bfloat16>(sh_dt, out_dt, has_w, has_sh);
+}
+
+const char* dt_name(int dt) {
+  switch (dt) {
+    case MOE_F32: return "f32";
+    case MOE_BF16: return "bf16";
+    case MOE_F16: return "f16";
+    default: return "unknown";
+  }
+}
+
+// dtype refusal: only the f32 and bf16 arms exist; f16 is named in the message
+int check_dtype(const char* op, const char* arg, int dt) {
+  if (dt == MOE_F32 || dt == MOE_BF16) return MOE_OK;
+  return set_error(MOE_ERR_DTYPE,
+                   "%s: %s dtype %s (%d) is not implemented; only f32 and bf16 arms exist",
+                   op, arg, dt_name(dt), dt);
+}
+
+int common_checks(const char* op, int T, int K, int H, bool need_k) {
+  if (T < 0) return set_error(MOE_ERR_ARG, "%s: T=%d < 0", op, T);
+  if (need_k && (K < 1 || K > 64)) return set_error(MOE_ERR_ARG, "%s: K=%d outside [1, 64]", op, K);
+  if (H <= 0) return set_error(MOE_ERR_ARG, "%s: H=%d <= 0", op, H);
+  if (H % kVec != 0) return set_error(MOE_ERR_ALIGN, "%s: H=%d is not a multiple of 8", op, H);
+  return MOE_OK;
+}
+
+int launch(const char* op, KernelFn fn, const void* eo, const float* w, const void* sh,
+           const float* gl, float rs, int T, int K, int H, void* out, void* stream, int kid) {
+  if (T == 0) return MOE_OK;
+  DeviceDiag diag = device_diag();
+  const long long items = static_cast<long long>(T) * (H / kVec);
+  const long long blocks = (items + kThreads - 1) / kThreads;
+  if (blocks > 0x7fffffffLL) return set_error(MOE_ERR_ARG, "%s: T*H too large", op);
+  fn<<<static_cast<unsigned>(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      eo, w, sh, gl, rs, T, K, H, out, diag.launches, kid);
+  return check_launch(op);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_combine(const void* expert_out, int eo_dtype, const float* w,
+                           const void* shared, int sh_dtype, float routed_scale, int T, int K,
+                           int H, void* out, int out_dtype, void* stream) {
+  clear_error();
+  const char* op = "moe_combine";
+  int rc;
+  if ((rc = check_dtype(op, "expert_out", eo_dtype)) != MOE_OK) return rc;
+  if ((rc = check_dtype(op, "out", out_dtype)) != MOE_OK) return rc;
+  if (shared && (rc = check_dtype(op, "shared", sh_dtype)) != MOE_OK) return rc;
+  if ((rc = common_checks(op, T, K, H, true)) != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!expert_out || !out) return set_error(MOE_ERR_ARG, "%s: expert_out/out is NULL", op);
+  if (!aligned16(expert_out) || !aligned16(out) || (shared && !aligned16(shared)) ||
+      (w && (reinterpret_cast<uintptr_t>(w) & 3u)))
+    return set_error(MOE_ERR_ALIGN, "%s: expert_out/shared/out must be 16-byte aligned", op);
+  KernelFn fn = pick<kCombine>(eo_dtype, shared ? sh_dtype : MOE_BF16, out_dtype, w != nullptr,
+                               shared != nullptr);
+  return launch(op, fn, expert_out, w, shared, nullptr, routed_scale, T, K, H, out, stream,
+                MOE_KID_COMBINE);
+}
+
+extern "C" int moe_combine_gate(const void* expert_out, int eo_dtype, const float* w,
+                                const void* sd, int sd_dtype, const float* gl, float routed_scale,
+                                int T, int K, int H, void* out, int out_dtype, void* stream) {
+  clear_error();
+  const char* op = "moe_combine_gate";
+  int rc;
+  if ((rc = check_dtype(op, "expert_out", eo_dtype)) != MOE_OK) return rc;
+  if ((rc = check_dtype(op, "sd", sd_dtype)) != MOE_OK) return rc;
+  if ((rc = check_dtype(op, "out", out_dtype)) != MOE_OK) return rc;
+  if ((rc = common_checks(op, T, K, H, true)) != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!expert_out || !sd || !gl || !out)
+    return set_error(MOE_ERR_ARG, "%s: expert_out/sd/gl/out is NULL", op);
+  if (!aligned16(expert_out) || !aligned16(out) || !aligned16(sd) ||
+      (reinterpret_cast<uintptr_t>(gl) & 3u) || (w && (reinterpret_cast<uintptr_t>(w) & 3u)))
+    return set_error(MOE_ERR_ALIGN, "%s: expert_out/sd/out must be 16-byte aligned", op);
+  KernelFn fn = pick<kCombineGate>(eo_dtype, sd_dtype, out_dtype, w != nullptr, true);
+  return launch(op, fn, expert_out, w, sd, gl, routed_scale, T, K, H, out, stream,
+                MOE_KID_COMBINE_GATE);
+}
+
+extern "C" int shared_expert_gate(const void* sd, int sd_dtype, const float* gl, int T, int H,
+                                  void* out, int out_dtype, void* stream) {
+  clear_error();
+  const char* op = "shared_expert_gate";
+  int rc;
+  if ((rc = check_dtype(op, "sd", sd_dtype)) != MOE_OK) return rc;
+  if ((rc = check_dtype(op, "out", out_dtype)) != MOE_OK) return rc;
+  if ((rc = common_checks(op, T, 1, H, false)) != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!sd || !gl || !out) return set_error(MOE_ERR_ARG, "%s: sd/gl/out is NULL", op);
+  if (!aligned16(sd) || !aligned16(out) || (reinterpret_cast<uintptr_t>(gl) & 3u))
+    return set_error(MOE_ERR_ALIGN, "%s: sd/out must be 16-byte aligned", op);
+  KernelFn fn = pick<kGateOnly>(MOE_BF16, sd_dtype, out_dtype, false, true);
+  return launch(op, fn, nullptr, nullptr, sd, gl, 1.0f, T, 1, H, out, stream,
+                MOE_KID_SHARED_GATE);
+}

@@ -1,0 +1,606 @@
+// moe_gemm.cu -- grouped BF16 GEMMs of the MoE expert block on tcgen05 tensor
+// cores: kMoeGroupedGemmBf16GateUpSilu and kMoeGroupedGemmBf16 (vllm.cpp issue
+// #3094 "Row: BACKEND-ROCM-BF16-MOE", which also fixes their numeric contract:
+// BF16 narrowing of the gate/up result before activation, routing weight
+// applied before the down result is stored), plus the router-logit GEMM.
+//
+// One persistent, warp-specialised kernel template:
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [kN x 64] bf16 per
+//               stage, 128-byte swizzle, into a kStages-deep shared-memory ring
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//               (M = 128, N = kN, K = 16 per instruction, f32 accumulators in
+//               TMEM, double-buffered so the epilogue overlaps the next tile)
+//   warps 2-5   epilogue: tcgen05.ld of one accumulator row per thread, the
+//               fused op (bf16 narrowing + SiLU-mul, or routing weight +
+//               scatter, or bias + f32 store) and 16-byte stores
+// The tile schedule is built on the device from the group offsets (the
+// routing histogram): every CTA scans ceil(rows_g / 128) * n_tiles over the
+// groups in shared memory and walks tiles blockIdx.x, blockIdx.x + gridDim.x,
+// ...  All tiles cost the same, so the static stride balances any skew of the
+// expert load to within one tile per CTA.  No host round trip, no scratch.
+//
+// Every wait on an mbarrier is bounded (about one second of device time); on
+// expiry the kernel raises MOE_STATUS_TIMEOUT in the library's status word,
+// every role stops, in-flight copies and MMAs are drained (again bounded) and
+// the TMEM is freed before the CTA exits.
+#include <stdio.h>
+
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+namespace gemm {
+
+constexpr int BM = 128;           // rows per tile (MMA M)
+constexpr int BK = 64;            // bf16 per 128-byte swizzled row: K per stage
+constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 1024;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int BOX_ROWS = 128;     // rows per TMA box
+constexpr int BOX_BYTES = BOX_ROWS * BK * 2;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+enum Epi { EPI_GATEUP = 0, EPI_DOWN = 1, EPI_F32 = 2 };
+
+struct Params {
+  const int32_t* group_offsets;  // [G+1] device, or null: one group [0, P)
+  int P;                         // rows of the product
+  int Kdim;                      // contraction length
+  int N;                         // output columns
+  int G;                         // groups
+  int b_rows_per_group;          // rows of the 2-D view of B per group
+  int half_off;                  // gate/up: row offset of the up half inside a group
+  void* out;
+  const float* pair_weight;      // down: [P] by destination row, or null
+  const int32_t* row_to_pair;    // down: destination row, or null
+  const float* bias;             // f32 epilogue: per output column, or null
+  unsigned int* status;
+  unsigned long long* launches;
+  int kid;
+};
+
+template <int kN>
+struct Smem {
+  static constexpr int B_BYTES = kN * BK * 2;
+  static constexpr int STAGE_A = 0;
+  static constexpr int STAGE_B = kStages * A_BYTES;
+  static constexpr int BARS = STAGE_B + kStages * B_BYTES;
+  // full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  static constexpr int NBARS = 2 * kStages + 5;
+  static constexpr int MISC = BARS + NBARS * 8;           // tmem slot, abort flag, scan scratch
+  static constexpr int TILE_START = MISC + 64;            // int[kMaxGroups + 1]
+  static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
+  static constexpr int BYTES = GOFF + (kMaxGroups + 1) * 4;
+  static constexpr int ALLOC = BYTES + 1024;              // slack to align the base to 1024
+};
+
+struct Tile {
+  int g, row0, row_end, n0;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, const int* goff,
+                                            int G, int n_tiles, int bn_out) {
+  int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  int local = tile - tile_start[lo];
+  int m = local / n_tiles, n = local - m * n_tiles;
+  Tile t;
+  t.g = lo;
+  t.row0 = goff[lo] + m * BM;
+  t.row_end = goff[lo + 1];
+  t.n0 = n * bn_out;
+  return t;
+}
+
+// Bounded mbarrier wait.  Returns false when this CTA is aborting.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned int* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 128; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicOr(status, static_cast<unsigned int>(MOE_STATUS_TIMEOUT));
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(v)) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16_bits(lo)) |
+         (static_cast<uint32_t>(f32_to_bf16_bits(hi)) << 16);
+}
+
+template <int kN, int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using S = Smem<kN>;
+  constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;
+  constexpr int kTmemCols = 2 * kN;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, kN);
+  constexpr uint32_t kStageTx = A_BYTES + S::B_BYTES;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC + 4);
+  int* scan_tmp = reinterpret_cast<int*>(smem + S::MISC + 8);   // 8 ints
+  int* tile_start = reinterpret_cast<int*>(smem + S::TILE_START);
+  int* goff = reinterpret_cast<int*>(smem + S::GOFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar_full = [&](int s) { return ptx::smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return ptx::smem_u32(bars + kStages + s); };
+  auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + a); };
+  auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 + a); };
+  const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kStages + 4);
+
+  count_launch(p.launches, p.kid);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar_full(s), 1);
+      ptx::mbar_init(bar_empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar_tfull(a), 1);
+      ptx::mbar_init(bar_tempty(a), 128);
+    }
+    ptx::mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+
+  // ---- device-side tile schedule from the group offsets
+  const int G = p.G;
+  for (int g = threadIdx.x; g <= G; g += kThreads)
+    goff[g] = p.group_offsets ? __ldg(p.group_offsets + g) : (g == 0 ? 0 : p.P);
+  __syncthreads();
+  const int n_tiles = (p.N + kBnOut - 1) / kBnOut;
+  const int chunk = (G + kThreads - 1) / kThreads;
+  const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
+  const int g_hi = min(G, g_lo + chunk);
+  int local = 0;
+  for (int g = g_lo; g < g_hi; ++g) {
+    int rows = goff[g + 1] - goff[g];
+    local += rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scan_tmp[warp] = incl;
+  __syncthreads();
+  int warp_base = 0, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    int v = scan_tmp[w];
+    if (w < warp) warp_base += v;
+    total += v;
+  }
+  int run = warp_base + incl - local;
+  for (int g = g_lo; g < g_hi; ++g) {
+    tile_start[g] = run;
+    int rows = goff[g + 1] - goff[g];
+    run += rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+  }
+  if (threadIdx.x == 0) tile_start[G] = total;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nk = (p.Kdim + BK - 1) / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
+        const int brow = t.g * p.b_rows_per_group + t.n0;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t fb = bar_full(stage);
+          ptx::mbar_arrive_expect_tx(fb, kStageTx);
+          const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
+          const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
+          ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0, fb);
+          if (kEpi == EPI_GATEUP) {
+            ptx::tma_load_2d(sb, &tmB, kb * BK, brow, fb);
+            ptx::tma_load_2d(sb + BOX_BYTES, &tmB, kb * BK, brow + p.half_off, fb);
+          } else {
+#pragma unroll
+            for (int h = 0; h < kN / BOX_ROWS; ++h)
+              ptx::tma_load_2d(sb + h * BOX_BYTES, &tmB, kb * BK, brow + h * BOX_ROWS, fb);
+          }
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: the last min(issued, kStages) copies may still be landing
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < min(issued, kStages); ++i) {
+          if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(bar_full(s), ph) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true, any = false;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
+        if (!wait_bar(bar_tempty(acc), aphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * A_BYTES);
+          const uint64_t db = ptx::desc_kmajor_sw128(sbase + S::STAGE_B + stage * S::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
+            ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          any = true;
+          ptx::mma_commit(bar_empty(stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar_tfull(acc));
+      }
+      if (!ok && any) {
+        ptx::mma_commit(bar_drain);
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar_drain, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
+      const int acc = it & 1;
+      const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
+      if (!wait_bar(bar_tfull(acc), aphase, abort_flag, p.status)) break;
+      ptx::tc_fence_after();
+      const int row = t.row0 + r_in_tile;
+      const bool valid = row < t.row_end;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * kN);
+      if (kEpi == EPI_GATEUP) {
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < kBnOut / 32; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
+          ptx::tmem_ld_32x32b_x32(taddr + kBnOut + c * 32, u);
+          ptx::tmem_ld_wait();
+          const int col = t.n0 + c * 32;
+          if (valid && col < p.N) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float a2[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                // narrowing before the activation: gate and up are rounded to bf16 first
+                const float gz = bf16_round(__uint_as_float(g[j + h]));
+                const float uz = bf16_round(__uint_as_float(u[j + h]));
+                const float s = gz / (1.0f + __expf(-gz));
+                a2[h] = s * uz;
+              }
+              packed[j / 2] = pack_bf16x2(a2[0], a2[1]);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * p.N + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              if (col + v * 8 < p.N)
+                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                    packed[4 * v + 3]);
+          }
+        }
+      } else if (kEpi == EPI_DOWN) {
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+        int dst_row = row;
+        float wgt = 1.0f;
+        if (valid) {
+          if (p.row_to_pair) dst_row = __ldg(p.row_to_pair + row);
+          if (p.pair_weight) wgt = __ldg(p.pair_weight + dst_row);
+        }
+#pragma unroll 1
+        for (int c = 0; c < kBnOut / 32; ++c) {
+          uint32_t y[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, y);
+          ptx::tmem_ld_wait();
+          const int col = t.n0 + c * 32;
+          if (valid && col < p.N) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              // the routing weight: one f32 multiply, then the one bf16 rounding
+              const float a = p.pair_weight ? __fmul_rn(__uint_as_float(y[j]), wgt) : __uint_as_float(y[j]);
+              const float b = p.pair_weight ? __fmul_rn(__uint_as_float(y[j + 1]), wgt) : __uint_as_float(y[j + 1]);
+              packed[j / 2] = pack_bf16x2(a, b);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(dst_row) * p.N + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              if (col + v * 8 < p.N)
+                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                    packed[4 * v + 3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < kBnOut / 32; ++c) {
+          uint32_t y[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, y);
+          ptx::tmem_ld_wait();
+          const int col = t.n0 + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col + j < p.N) {
+                float v = __uint_as_float(y[j]);
+                if (p.bias) v = __fadd_rn(v, __ldg(p.bias + col + j));
+                out[static_cast<size_t>(row) * p.N + col + j] = v;
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_tempty(acc));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// rows x cols bf16 matrix (row-major, cols contiguous), box of 64 cols x 128 rows
+int make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, const char* op,
+              const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(MOE_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", op);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {BK, BOX_ROWS};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(MOE_ERR_CUDA, "%s: tensor map for %s rejected (CUresult %d)", op, what,
+                     static_cast<int>(r));
+  return MOE_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+template <int kN, int kEpi>
+int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
+           long long tile_bound, cudaStream_t stream) {
+  auto kern = grouped_gemm_kernel<kN, kEpi>;
+  const int smem = Smem<kN>::ALLOC;
+  static int configured_dev[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured_dev[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "%s: cannot reserve %d bytes of shared memory: %s", op, smem,
+                       cudaGetErrorString(cudaGetLastError()));
+    configured_dev[dev] = 1;
+  }
+  long long grid = tile_bound;
+  const int sms = num_sms();
+  if (grid > sms) grid = sms;
+  if (grid < 1) grid = 1;
+  DeviceDiag diag = device_diag();
+  p.status = diag.status;
+  p.launches = diag.launches;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(ta, tb, p);
+  return check_launch(op);
+}
+
+int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, const void* b,
+                 const void* out) {
+  if (P < 0) return set_error(MOE_ERR_ARG, "%s: P=%d < 0", op, P);
+  if (Kdim <= 0 || N <= 0) return set_error(MOE_ERR_ARG, "%s: dimensions must be positive", op);
+  if (G < 1 || G > kMaxGroups)
+    return set_error(MOE_ERR_ARG, "%s: G=%d outside [1, %d]", op, G, kMaxGroups);
+  if (Kdim % 8 != 0 || N % 8 != 0)
+    return set_error(MOE_ERR_ALIGN, "%s: H and I must be multiples of 8", op);
+  if (P > 0 && (!a || !b || !out)) return set_error(MOE_ERR_ARG, "%s: NULL operand", op);
+  if (!aligned16(a) || !aligned16(b) || !aligned16(out))
+    return set_error(MOE_ERR_ALIGN, "%s: operands must be 16-byte aligned", op);
+  return MOE_OK;
+}
+
+long long tile_bound(int P, int G, int N, int bn_out) {
+  long long mt = (P + BM - 1) / BM + (G < P ? G : P);
+  return mt * ((N + bn_out - 1) / bn_out);
+}
+
+}  // namespace gemm
+
+// router logits l[t, e] = x[t,:] . w_router[e,:] (+ bias[e]) in f32 (used by moe_route.cu)
+int launch_router_logits(const void* x, const void* w_router, const float* bias, int T, int H,
+                         int E, float* logits, cudaStream_t stream) {
+  using namespace gemm;
+  const char* op = "moe_route_topk";
+  if (T == 0) return MOE_OK;
+  CUtensorMap ta, tb;
+  int rc;
+  if ((rc = make_tmap(&ta, x, T, H, op, "x")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tb, w_router, E, H, op, "w_router")) != MOE_OK) return rc;
+  Params p{};
+  p.group_offsets = nullptr;
+  p.P = T;
+  p.Kdim = H;
+  p.N = E;
+  p.G = 1;
+  p.b_rows_per_group = E;
+  p.half_off = 0;
+  p.out = logits;
+  p.bias = bias;
+  p.kid = MOE_KID_ROUTE_LOGITS;
+  if (E <= 128) return launch<128, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 128), stream);
+  return launch<256, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 256), stream);
+}
+
+}  // namespace moe
+
+using namespace moe;
+using namespace moe::gemm;
+
+extern "C" size_t moe_grouped_gemm_workspace_size(int, int, int, int) { return 0; }
+
+extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, const int32_t* a_row_gather,
+                                                 const void* w13_bf16,
+                                                 const int32_t* group_offsets, int P, int H,
+                                                 int I, int G, void* act_bf16, void* workspace,
+                                                 size_t ws_bytes, void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  clear_error();
+  const char* op = "moe_grouped_gemm_gateup_silu_bf16";
+  int rc;
+  if ((rc = check_common(op, P, H, I, G, a_bf16, w13_bf16, act_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if (a_row_gather)
+    return set_error(MOE_ERR_UNSUPPORTED, "%s: a_row_gather is not implemented yet", op);
+  if (P == 0) return MOE_OK;
+  CUtensorMap ta, tb;
+  if ((rc = make_tmap(&ta, a_bf16, P, H, op, "a")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, op, "w13")) != MOE_OK)
+    return rc;
+  Params p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = H;
+  p.N = I;
+  p.G = G;
+  p.b_rows_per_group = 2 * I;
+  p.half_off = I;
+  p.out = act_bf16;
+  p.kid = MOE_KID_GEMM_GATEUP;
+  return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128),
+                                 static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
+                                          const int32_t* group_offsets, const float* pair_weight,
+                                          const int32_t* row_to_pair, int P, int I, int H, int G,
+                                          void* out_bf16, void* workspace, size_t ws_bytes,
+                                          void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  clear_error();
+  const char* op = "moe_grouped_gemm_down_bf16";
+  int rc;
+  if ((rc = check_common(op, P, I, H, G, act_bf16, w2_bf16, out_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if (P == 0) return MOE_OK;
+  CUtensorMap ta, tb;
+  if ((rc = make_tmap(&ta, act_bf16, P, I, op, "act")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, op, "w2")) != MOE_OK)
+    return rc;
+  Params p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = I;
+  p.N = H;
+  p.G = G;
+  p.b_rows_per_group = H;
+  p.half_off = 0;
+  p.out = out_bf16;
+  p.pair_weight = pair_weight;
+  p.row_to_pair = row_to_pair;
+  p.kid = MOE_KID_GEMM_DOWN;
+  return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256),
+                               static_cast<cudaStream_t>(stream));
+}

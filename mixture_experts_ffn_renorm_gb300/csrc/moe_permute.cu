@@ -1,0 +1,207 @@
+// moe_permute.cu -- tokens into expert-contiguous order: a deterministic,
+// stable counting sort of the P = T*K (token, slot) pairs by expert.  The
+// expert path stores P permuted rows (vllm.cpp PR #509 review, finding 2:
+// "DBuf ddown(d, DType::kBF16, {P, H})") and the expert GEMM is grouped over
+// expert ids (PR #523, "What changed").
+//
+//   count   one warp per chunk of 512 pairs: per-chunk expert histogram in
+//           shared memory (bad ids raise MOE_STATUS_BAD_ID and are skipped)
+//   scan    one block: per expert, exclusive scan of the chunk counts in chunk
+//           order; then the exclusive scan over experts -> expert_offsets
+//   place   one warp per chunk again, 32 pairs at a time in pair order: the
+//           rank of a pair among equal experts of its step comes from
+//           __match_any_sync, so rows inside an expert ascend with p
+//   gather  (optional) x_perm[row] = x[sorted_pair[row] / K], 16 bytes a thread
+// Everything is a function of the ids alone: no atomics decide an order.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 512;  // pairs per warp
+constexpr int kWarps = 8;    // warps (chunks) per block
+
+__global__ void __launch_bounds__(kWarps * 32)
+permute_count(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
+              int32_t* __restrict__ hist, unsigned int* status, unsigned long long* launches) {
+  count_launch(launches, MOE_KID_PERMUTE_COUNT);
+  extern __shared__ int32_t sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  int32_t* h = sh + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (c < n_chunks) {
+    const int p0 = c * kChunk, p1 = min(P, p0 + kChunk);
+    bool bad = false;
+    for (int p = p0 + lane; p < p1; p += 32) {
+      const int e = __ldg(ids + p);
+      if (e >= 0 && e < E) atomicAdd(h + e, 1);
+      else bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
+      atomicOr(status, static_cast<unsigned int>(MOE_STATUS_BAD_ID));
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(c) * E + e] = h[e];
+  }
+}
+
+__global__ void __launch_bounds__(1024)
+permute_scan(int32_t* __restrict__ hist, int E, int n_chunks, int32_t* __restrict__ offsets,
+             unsigned long long* launches) {
+  count_launch(launches, MOE_KID_PERMUTE_SCAN);
+  __shared__ int32_t warp_sum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int run = 0;
+  if (tid < E) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + tid;
+      const int v = hist[i];
+      hist[i] = run;
+      run += v;
+    }
+  }
+  // block-wide exclusive scan of the per-expert totals (E <= 1024)
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = warp_sum[lane];
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sum[lane] = wi - ws;
+  }
+  __syncthreads();
+  const int excl = warp_sum[warp] + incl - run;
+  if (tid < E) offsets[tid] = excl;
+  if (tid == E - 1) offsets[E] = excl + run;
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+permute_place(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
+              const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets,
+              int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_to_row,
+              unsigned long long* launches) {
+  count_launch(launches, MOE_KID_PERMUTE_PLACE);
+  extern __shared__ int32_t sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  if (c >= n_chunks) return;
+  int32_t* cnt = sh + warp * E;
+  for (int e = lane; e < E; e += 32)
+    cnt[e] = hist[static_cast<size_t>(c) * E + e] + __ldg(offsets + e);
+  __syncwarp();
+  const int p0 = c * kChunk, p1 = min(P, p0 + kChunk);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    const int e = p < p1 ? __ldg(ids + p) : -1;
+    const bool valid = e >= 0 && e < E;
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+    int row = 0;
+    uint32_t peers = 0;
+    if (valid) {
+      peers = __match_any_sync(vmask, e);
+      row = cnt[e] + __popc(peers & lt_mask);
+    }
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) cnt[e] += __popc(peers);  // lowest lane of the group
+    __syncwarp();
+    if (valid) {
+      sorted_pair[row] = p;
+      pair_to_row[p] = row;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair, int P,
+               int K, int H, uint16_t* __restrict__ x_perm, unsigned long long* launches) {
+  count_launch(launches, MOE_KID_PERMUTE_GATHER);
+  const int vpr = H / 8;
+  const long long n = static_cast<long long>(P) * vpr;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(i / vpr);
+    const int v = static_cast<int>(i - static_cast<long long>(row) * vpr);
+    const int src = __ldg(sorted_pair + row) / K;
+    const uint4 d = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(src) * H) + v);
+    reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(row) * H)[v] = d;
+  }
+}
+
+int n_chunks_of(long long P) { return static_cast<int>((P + kChunk - 1) / kChunk); }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
+  if (T <= 0 || K <= 0 || E <= 0) return 0;
+  const long long P = static_cast<long long>(T) * K;
+  return ((static_cast<size_t>(n_chunks_of(P)) * E * sizeof(int32_t)) + 255) &
+         ~static_cast<size_t>(255);
+}
+
+extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, int K, int E,
+                           int H, int32_t* expert_offsets, int32_t* sorted_pair,
+                           int32_t* pair_to_row, void* x_perm_bf16, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_permute";
+  if (T < 0) return set_error(MOE_ERR_ARG, "%s: T=%d < 0", op, T);
+  if (K < 1 || K > 32) return set_error(MOE_ERR_ARG, "%s: K=%d outside [1, 32]", op, K);
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_ARG, "%s: E=%d outside [1, 1024]", op, E);
+  if (!expert_offsets) return set_error(MOE_ERR_ARG, "%s: expert_offsets is NULL", op);
+  if (x_perm_bf16 && (!x_bf16 || H <= 0))
+    return set_error(MOE_ERR_ARG, "%s: x_perm needs x and H > 0", op);
+  if (x_perm_bf16 && (H % 8 != 0 || !aligned16(x_bf16) || !aligned16(x_perm_bf16)))
+    return set_error(MOE_ERR_ALIGN, "%s: x/x_perm need 16-byte alignment and H %% 8 == 0", op);
+  const long long P = static_cast<long long>(T) * K;
+  if (P > 0x7fffffffLL) return set_error(MOE_ERR_ARG, "%s: T*K too large", op);
+  if (P > 0 && (!topk_ids || !sorted_pair || !pair_to_row))
+    return set_error(MOE_ERR_ARG, "%s: ids/sorted_pair/pair_to_row is NULL", op);
+  const size_t need = moe_permute_workspace_size(T, K, E);
+  if (need > 0 && (!workspace || ws_bytes < need))
+    return set_error(MOE_ERR_WORKSPACE, "%s: workspace of %zu bytes is smaller than %zu", op,
+                     ws_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceDiag diag = device_diag();
+  const int n_chunks = n_chunks_of(P);
+  int32_t* hist = static_cast<int32_t*>(workspace);
+  const int blocks = (n_chunks + kWarps - 1) / kWarps;
+  const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(int32_t);
+  if (n_chunks > 0) {
+    permute_count<<<blocks, kWarps * 32, smem, s>>>(topk_ids, static_cast<int>(P), E, n_chunks,
+                                                    hist, diag.status, diag.launches);
+    int rc = check_launch(op);
+    if (rc != MOE_OK) return rc;
+  }
+  permute_scan<<<1, 1024, 0, s>>>(hist, E, n_chunks, expert_offsets, diag.launches);
+  int rc = check_launch(op);
+  if (rc != MOE_OK || n_chunks == 0) return rc;
+  permute_place<<<blocks, kWarps * 32, smem, s>>>(topk_ids, static_cast<int>(P), E, n_chunks,
+                                                  hist, expert_offsets, sorted_pair, pair_to_row,
+                                                  diag.launches);
+  if ((rc = check_launch(op)) != MOE_OK) return rc;
+  if (x_perm_bf16) {
+    const long long items = P * (H / 8);
+    long long g = (items + 255) / 256;
+    if (g > 152LL * 16) g = 152LL * 16;
+    permute_gather<<<static_cast<unsigned>(g), 256, 0, s>>>(
+        static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P), K, H,
+        static_cast<uint16_t*>(x_perm_bf16), diag.launches);
+    rc = check_launch(op);
+  }
+  return rc;
+}

@@ -1,0 +1,215 @@
+// moe_route.cu -- the ungrouped softmax router with top-k and renormalisation
+// (vllm.cpp PR #509, "Honest gaps": the covered router path is ungrouped
+// softmax; grouped, bias-corrected (noaux_tc) and sigmoid forms are refused).
+//
+// Two kernels: the logits GEMM on tcgen05 tensor cores (moe_gemm.cu, f32
+// epilogue with the optional per-expert bias) and a warp-per-token selection
+// kernel.  Selection runs on the f32 logits themselves (softmax is monotone),
+// so the chosen ids do not depend on exp; the weights use the bit-exact
+// binary32 exp and are summed in rank order, so they are bit-identical to the
+// sequential definition for the same logits.
+#include <math.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+int launch_router_logits(const void* x, const void* w_router, const float* bias, int T, int H,
+                         int E, float* logits, cudaStream_t stream);
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+// does (a, ia) rank above (b, ib)?  descending value, ties to the lower id,
+// NaN below every number; ib < 0 means "no candidate yet"
+__device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
+  if (ib < 0) return true;
+  const bool na = a != a, nb = b != b;
+  if (na || nb) {
+    if (na && nb) return ia < ib;
+    return nb;
+  }
+  if (a > b) return true;
+  if (a < b) return false;
+  return ia < ib;
+}
+
+template <int kPerLane>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormalize,
+            const uint16_t* __restrict__ x, const uint16_t* __restrict__ wsg, int H,
+            int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ gl_out,
+            unsigned long long* launches) {
+  count_launch(launches, MOE_KID_ROUTE_TOPK);
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + static_cast<size_t>(t) * E;
+  float v[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(row + e) : 0.0f;
+  }
+  uint32_t taken = 0;
+  float my_sel = 0.0f;
+  int my_id = 0;
+  for (int j = 0; j < K; ++j) {
+    float bv = 0.0f;
+    int be = -1;
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, be)) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (oe >= 0 && ranks_above(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_sel = bv;
+      my_id = be;
+    }
+  }
+  // weights: e_j = exp(l_j - l_0), S summed in rank order from +0, w_j = e_j / S
+  const float m = __shfl_sync(0xffffffffu, my_sel, 0);
+  const float ex = exp_cr(__fsub_rn(my_sel, m));
+  float S = 0.0f;
+  if (renormalize) {
+    for (int j = 0; j < K; ++j) S = __fadd_rn(S, __shfl_sync(0xffffffffu, ex, j));
+  } else {
+    float ev[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) ev[i] = exp_cr(__fsub_rn(v[i], m));
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i)
+      for (int l = 0; l < 32; ++l) {
+        const float term = __shfl_sync(0xffffffffu, ev[i], l);
+        if (l + 32 * i < E) S = __fadd_rn(S, term);
+      }
+  }
+  if (lane < K) {
+    ids[static_cast<size_t>(t) * K + lane] = my_id;
+    w[static_cast<size_t>(t) * K + lane] = __fdiv_rn(ex, S);
+  }
+  if (wsg != nullptr) {
+    // shared-expert gate logit: a plain f32 dot product of x[t] and wsg
+    const uint16_t* xr = x + static_cast<size_t>(t) * H;
+    float acc = 0.0f;
+    for (int h = lane * 8; h < H; h += 256) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(xr + h));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(wsg + h));
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc += __uint_as_float(aw[q] << 16) * __uint_as_float(bw[q] << 16);
+        acc += __uint_as_float(aw[q] & 0xFFFF0000u) * __uint_as_float(bw[q] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) gl_out[t] = acc;
+  }
+}
+
+using TopkFn = void (*)(const float*, int, int, int, int, const uint16_t*, const uint16_t*, int,
+                        int32_t*, float*, float*, unsigned long long*);
+
+TopkFn pick_topk(int E) {
+  if (E <= 32) return topk_kernel<1>;
+  if (E <= 64) return topk_kernel<2>;
+  if (E <= 128) return topk_kernel<4>;
+  if (E <= 256) return topk_kernel<8>;
+  if (E <= 512) return topk_kernel<16>;
+  return topk_kernel<32>;
+}
+
+size_t logits_bytes(int T, int E) {
+  return ((static_cast<size_t>(T) * E * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_route_topk_workspace_size(int T, int E, int K) {
+  (void)K;
+  if (T <= 0 || E <= 0) return 0;
+  return logits_bytes(T, E);
+}
+
+extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
+                              const float* logit_bias, const void* w_shared_gate_bf16,
+                              const float* logits_in, int T, int H, int E, int K, int renormalize,
+                              int scoring, int n_group, int32_t* topk_ids, float* topk_w,
+                              float* logits_out, float* gate_logit_out, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_route_topk";
+  if (scoring != 0)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "%s: scoring=%d is not implemented; only ungrouped softmax (0) is", op,
+                     scoring);
+  if (n_group != 1)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "%s: grouped routing (n_group=%d) is not implemented; only n_group=1 is", op,
+                     n_group);
+  if (T < 0) return set_error(MOE_ERR_ARG, "%s: T=%d < 0", op, T);
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_ARG, "%s: E=%d outside [1, 1024]", op, E);
+  if (K < 1 || K > E || K > 32)
+    return set_error(MOE_ERR_ARG, "%s: K=%d outside [1, min(E, 32)]", op, K);
+  if (renormalize != 0 && renormalize != 1)
+    return set_error(MOE_ERR_ARG, "%s: renormalize must be 0 or 1", op);
+  const bool need_x = logits_in == nullptr || w_shared_gate_bf16 != nullptr;
+  if (need_x && (H <= 0 || H % 8 != 0))
+    return set_error(MOE_ERR_ALIGN, "%s: H=%d must be a positive multiple of 8", op, H);
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !topk_w) return set_error(MOE_ERR_ARG, "%s: topk_ids/topk_w is NULL", op);
+  if (!logits_in && (!x_bf16 || !w_router_bf16))
+    return set_error(MOE_ERR_ARG, "%s: x/w_router is NULL and no logits_in given", op);
+  if (w_shared_gate_bf16 && (!x_bf16 || !gate_logit_out))
+    return set_error(MOE_ERR_ARG, "%s: w_shared_gate needs x and gate_logit_out", op);
+  if ((x_bf16 && !aligned16(x_bf16)) || (w_router_bf16 && !aligned16(w_router_bf16)) ||
+      (w_shared_gate_bf16 && !aligned16(w_shared_gate_bf16)))
+    return set_error(MOE_ERR_ALIGN, "%s: x/w_router/w_shared_gate must be 16-byte aligned", op);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float* logits = logits_in;
+  if (!logits) {
+    float* dst = logits_out;
+    if (!dst) {
+      if (!workspace || ws_bytes < logits_bytes(T, E))
+        return set_error(MOE_ERR_WORKSPACE,
+                         "%s: workspace of %zu bytes is smaller than the %zu bytes of logits", op,
+                         ws_bytes, logits_bytes(T, E));
+      if (!aligned16(workspace))
+        return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
+      dst = static_cast<float*>(workspace);
+    }
+    int rc = launch_router_logits(x_bf16, w_router_bf16, logit_bias, T, H, E, dst, s);
+    if (rc != MOE_OK) return rc;
+    logits = dst;
+  } else if (logits_out && logits_out != logits_in) {
+    if (cudaMemcpyAsync(logits_out, logits_in, static_cast<size_t>(T) * E * sizeof(float),
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "%s: copy of logits failed: %s", op,
+                       cudaGetErrorString(cudaGetLastError()));
+  }
+  DeviceDiag diag = device_diag();
+  const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  pick_topk(E)<<<blocks, kWarpsPerBlock * 32, 0, s>>>(
+      logits, T, E, K, renormalize, static_cast<const uint16_t*>(x_bf16),
+      static_cast<const uint16_t*>(w_shared_gate_bf16), H, topk_ids, topk_w, gate_logit_out,
+      diag.launches);
+  return check_launch(op);
+}

@@ -114,8 +114,27 @@ def to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
 
 def normal_bf16(seed: int, tag: int, shape, std: float) -> np.ndarray:
+    """Same values as to_bf16_bits(normal_f32(...)), converted chunk by chunk."""
     n = int(np.prod(shape))
-    return to_bf16_bits(normal_f32(seed, tag, n, std)).reshape(shape)
+    out = np.empty(n, np.uint16)
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def fill(c: int) -> None:
+        lo = c * CHUNK
+        hi = min(n, lo + CHUNK)
+        tmp = np.empty(hi - lo, np.float32)
+        np.random.default_rng([seed, tag, c]).standard_normal(hi - lo, dtype=np.float32, out=tmp)
+        if std != 1.0:
+            tmp *= np.float32(std)
+        out[lo:hi] = to_bf16_bits(tmp)
+
+    if nchunks <= 1:
+        for c in range(nchunks):
+            fill(c)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out.reshape(shape)
 
 
 def zipf_logit_bias(cfg: LayerConfig) -> np.ndarray | None:

@@ -1,0 +1,73 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every
+entry point include/moe.h declares; argument checks that fail before any CUDA
+call are exercised here (no compute without a GPU)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_ffn_renorm_gb300 as m
+from mixture_experts_ffn_renorm_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            for mt in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                                  src, flags=re.M):
+                names.add(mt.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return m.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert {"moe_route_topk", "moe_permute", "moe_grouped_gemm_gateup_silu_bf16",
+            "moe_grouped_gemm_down_bf16", "moe_combine", "moe_combine_gate",
+            "shared_expert_gate", "moe_last_error"} <= declared
+    raw = ctypes.CDLL(m.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+    assert set(m.EXPORTS) <= declared
+
+
+def test_abi_version_and_refusals_without_gpu(lib):
+    assert m.abi_version() == 1
+    # dtype refusals name the missing arm and return before touching the device
+    rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
+    assert rc == m.ERR_DTYPE and "f16" in m.last_error()
+    rc = lib.shared_expert_gate(None, m.BF16, None, 1, 8, None, 7, None)
+    assert rc == m.ERR_DTYPE
+    rc = lib.moe_route_topk(None, None, None, None, None, 1, 8, 8, 2, 1, 1, 1, None, None, None,
+                            None, None, 0, None)
+    assert rc == m.ERR_UNSUPPORTED and "softmax" in m.last_error()
+    rc = lib.moe_route_topk(None, None, None, None, None, 1, 8, 8, 2, 1, 0, 4, None, None, None,
+                            None, None, 0, None)
+    assert rc == m.ERR_UNSUPPORTED
+    rc = lib.moe_permute(None, None, 1, 0, 8, 8, None, None, None, None, None, 0, None)
+    assert rc == m.ERR_ARG
+    rc = lib.moe_grouped_gemm_down_bf16(None, None, None, None, None, 4, 60, 64, 1, None, None, 0,
+                                        None)
+    assert rc == m.ERR_ALIGN
+    # T = 0 is a legal no-op for the stream ops
+    assert lib.moe_combine(None, m.BF16, None, None, m.BF16, 1.0, 0, 2, 8, None, m.BF16, None) == 0
+
+
+def test_workspace_queries(lib):
+    assert m.moe_route_topk_workspace_size(8192, 128, 8) >= 8192 * 128 * 4
+    assert m.moe_permute_workspace_size(8192, 8, 128) >= (65536 // 512) * 128 * 4
+    assert m.moe_permute_workspace_size(0, 8, 128) == 0
+    assert m.moe_grouped_gemm_workspace_size(65536, 2048, 768, 128) == 0

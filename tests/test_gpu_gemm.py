@@ -1,0 +1,130 @@
+"""GPU parity of the grouped BF16 GEMMs (tcgen05) against the CPU oracle.
+
+kMoeGroupedGemmBf16GateUpSilu and kMoeGroupedGemmBf16 (vllm.cpp issue #3094
+"Row: BACKEND-ROCM-BF16-MOE"): stage-wise, the oracle consumes the same A, and
+the outputs must have NMSE <= 1e-5 and max relative error <= 2e-2 against the
+oracle's f32-accumulated bf16 result.  Shapes span several M, N and K tiles,
+ragged tails in every dimension, empty and one-row groups."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_renorm_gb300 as m
+import oracle as O
+from mixture_experts_ffn_renorm_gb300 import workloads as W
+
+from .gpu_util import assert_gemm_close, empty, launched_since, launches, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    m.lib()
+    m.moe_device_status(clear=True)
+    yield
+    assert m.moe_device_status() == 0
+
+
+def _case(sizes, H, I, seed):
+    rng = np.random.default_rng(seed)
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(off[-1])
+    A = W.to_bf16_bits(rng.standard_normal((P, H)).astype(np.float32))
+    W13 = W.to_bf16_bits((0.02 * rng.standard_normal((G, 2 * I, H))).astype(np.float32))
+    W2 = W.to_bf16_bits((0.02 * rng.standard_normal((G, H, I))).astype(np.float32))
+    return off, P, G, A, W13, W2
+
+
+SHAPES = [
+    # group sizes, H, I
+    ([4], 64, 32),
+    ([0, 1, 130, 129, 40], 256, 192),
+    ([300], 512, 128),
+    ([1, 1, 1, 1, 1, 1, 1, 1], 2048, 768),
+    ([257, 0, 0, 3], 136, 72),
+    ([128, 128, 255, 1], 1024, 256),
+]
+
+
+@pytest.mark.parametrize("sizes,H,I", SHAPES)
+def test_gateup_silu(sizes, H, I):
+    off, P, G, A, W13, _ = _case(sizes, H, I, sum(sizes) + H)
+    want = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G)
+    act = empty((P, I), torch.bfloat16)
+    act.fill_(0)
+    before = launches()
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), None, to_dev(W13), to_dev(off), P, H, I, G, act)
+    assert launched_since(before, "gemm_gateup") == 1
+    assert m.moe_device_status() == 0
+    assert_gemm_close(to_host(act), want, "gate/up")
+
+
+@pytest.mark.parametrize("sizes,H,I", SHAPES)
+def test_down_weight_scatter(sizes, H, I):
+    off, P, G, _, _, W2 = _case(sizes, H, I, sum(sizes) + I)
+    rng = np.random.default_rng(1)
+    act = W.to_bf16_bits(rng.standard_normal((P, I)).astype(np.float32))
+    wts = rng.uniform(0.05, 1.0, P).astype(np.float32)
+    r2p = rng.permutation(P).astype(np.int32)
+    for pw, rp in ((wts, r2p), (None, None), (wts, None)):
+        want = O.down(act, W2, off, P=P, I=I, H=H, G=G, pair_weight=pw, row_to_pair=rp)
+        out = empty((P, H), torch.bfloat16)
+        out.fill_(0)
+        before = launches()
+        m.moe_grouped_gemm_down_bf16(to_dev(act), to_dev(W2), to_dev(off),
+                                     None if pw is None else to_dev(pw),
+                                     None if rp is None else to_dev(rp), P, I, H, G, out)
+        assert launched_since(before, "gemm_down") == 1
+        assert m.moe_device_status() == 0
+        assert_gemm_close(to_host(out), want, "down")
+
+
+def test_gateup_narrowing_is_visible_on_the_gpu():
+    # g = u = 1 + 2^-9 exactly: narrowing before the activation gives
+    # bf16(silu(1) * 1) = 0x3F3B; without it the result would be 0x3F3C
+    H, I = 64, 32
+    A = np.zeros((1, H), np.float32)
+    A[0, 0], A[0, 1] = 1.0, 2.0**-9
+    Wt = np.zeros((1, 2 * I, H), np.float32)
+    Wt[0, :, 0] = 1.0
+    Wt[0, :, 1] = 1.0
+    act = empty((1, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(W.to_bf16_bits(A)), None,
+                                        to_dev(W.to_bf16_bits(Wt)), to_dev(np.array([0, 1], np.int32)),
+                                        1, H, I, 1, act)
+    assert np.all(to_host(act) == 0x3F3B)
+
+
+def test_single_group_without_offsets_and_rows_outside_groups():
+    H, I, P = 128, 64, 200
+    rng = np.random.default_rng(2)
+    A = W.to_bf16_bits(rng.standard_normal((P, H)).astype(np.float32))
+    W13 = W.to_bf16_bits((0.05 * rng.standard_normal((1, 2 * I, H))).astype(np.float32))
+    act = empty((P, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), None, to_dev(W13), None, P, H, I, 1, act)
+    want = O.gateup_silu(A, W13, np.array([0, P], np.int32), P=P, H=H, I=I, G=1)
+    assert_gemm_close(to_host(act), want, "single group")
+    # rows past group_offsets[G] are not written
+    off = np.array([0, 150], np.int32)
+    act.fill_(0)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), None, to_dev(W13), to_dev(off), P, H, I, 1, act)
+    h = to_host(act)
+    assert np.all(h[150:] == 0)
+    assert_gemm_close(h[:150], want[:150], "partial group")
+
+
+def test_gemm_refusals_and_empty():
+    act = empty((4, 64), torch.bfloat16)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_grouped_gemm_gateup_silu_bf16(act, None, act, None, 4, 64, 60, 1, act)
+    assert ei.value.code == m.ERR_ALIGN
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_grouped_gemm_gateup_silu_bf16(act, None, act, None, 4, 64, 32, 2, act)
+    assert ei.value.code == m.ERR_ARG
+    before = launches()
+    assert m.moe_grouped_gemm_down_bf16(act, act, None, None, None, 0, 64, 64, 1, act) == 0
+    assert launches() == before

@@ -1,0 +1,172 @@
+"""The whole MoE expert block on the GPU against the CPU oracle.
+
+Tiny layer: every output element.  Full-size workloads (decode T=16, prefill
+T=8192 with Zipf-skewed load, large T=2048 with a shared expert), in the same
+launch configuration the benchmark times: stage by stage, each stage fed the
+GPU's own inputs so that it is checked on its own --
+  router   logits within the dot-product bound on sampled tokens; ids and
+           weights bit-exact given the GPU logits
+  permute  bit-exact (all rows)
+  gate/up  sampled rows, NMSE <= 1e-5 and max rel <= 2e-2
+  down     sampled rows, same tolerance
+  combine  sampled tokens, bit-exact given the GPU's expert outputs
+and end to end on sampled tokens (oracle from the raw inputs), excluding the
+few tokens whose top-k set sits on a near-tie the logit bound cannot decide.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_renorm_gb300 as m
+import oracle as O
+from mixture_experts_ffn_renorm_gb300 import workloads as W
+from mixture_experts_ffn_renorm_gb300.layer import MoeBlock
+
+from .gpu_util import (GEMM_MAXREL, GEMM_NMSE, assert_gemm_close, bf16_to_f64, launched_since,
+                       launches, nmse_maxrel, to_dev, to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    m.lib()
+    m.moe_device_status(clear=True)
+    yield
+    assert m.moe_device_status() == 0
+
+
+def _block(cfg, d):
+    return MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                    I_shared=cfg.I_shared)
+
+
+def _oracle_tokens(cfg, d, tokens):
+    return O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
+                              d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H,
+                              I=cfg.I, E=cfg.E, K=cfg.K, I_shared=cfg.I_shared,
+                              tokens=np.asarray(tokens, np.int32))
+
+
+def test_tiny_layer_every_element():
+    cfg = W.TINY
+    d = W.layer_inputs(cfg)
+    blk = _block(cfg, d)
+    before = launches()
+    out = to_host(blk.forward(to_dev(d["x"])))
+    for k in ("route_logits", "route_topk", "permute_place", "combine_gate"):
+        assert launched_since(before, k) == 1, k
+    assert launched_since(before, "gemm_gateup") == 2 and launched_since(before, "gemm_down") == 2
+    want, ids, w = _oracle_tokens(cfg, d, range(cfg.T))
+    assert np.array_equal(to_host(blk.topk_ids), ids)
+    nmse, rel = nmse_maxrel(bf16_to_f64(out), bf16_to_f64(want))
+    assert nmse <= GEMM_NMSE and rel <= GEMM_MAXREL, (nmse, rel)
+
+
+def _stagewise(cfg, n_tok_sample, n_row_sample):
+    d = W.layer_inputs(cfg)
+    T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
+    P = T * K
+    blk = _block(cfg, d)
+    x_dev = to_dev(d["x"])
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    out = to_host(blk.forward(x_dev))
+    torch.cuda.synchronize()
+    ids = to_host(blk.topk_ids)
+    wts = to_host(blk.topk_w)
+    rng = np.random.default_rng(99)
+    toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, min(T, n_tok_sample), replace=False)]))
+
+    # router: logits (re-run with logits_out) within the bound; ids/w exact from them
+    ws = blk.workspace
+    m.moe_route_topk(x_dev, blk.w_router, blk.logit_bias, None, None, T, H, E, K, 1, 0, 1,
+                     blk.topk_ids, blk.topk_w, logits, None, ws, ws.numel())
+    lo = to_host(logits)
+    want_ids, want_w, _, _ = O.route_topk(logits_in=lo, T=T, H=1, E=E, K=K)
+    assert np.array_equal(ids, want_ids) and np.array_equal(wts.view(np.uint32), want_w.view(np.uint32))
+    _, _, lo_ora, _ = O.route_topk(d["x"][toks], d["w_router"], d["logit_bias"], T=len(toks), H=H,
+                                   E=E, K=K, want_logits=True)
+    xf, wf = bf16_to_f64(d["x"][toks]), bf16_to_f64(d["w_router"])
+    bound = (H + 2) * 2.0**-23 * (np.abs(xf) @ np.abs(wf).T + (0 if d["logit_bias"] is None else np.abs(d["logit_bias"])))
+    assert np.all(np.abs(lo[toks].astype(np.float64) - lo_ora) <= 2 * bound)
+
+    # permute: bit-exact over all rows
+    off, sp, p2r, _ = O.permute(ids, None, T=T, K=K, E=E)
+    assert np.array_equal(to_host(blk.expert_offsets), off)
+    assert np.array_equal(to_host(blk.sorted_pair)[:P], sp)
+    assert np.array_equal(to_host(blk.pair_to_row)[:P], p2r)
+    rows = np.unique(np.concatenate([
+        [0, P - 1], rng.choice(P, min(P, n_row_sample), replace=False),
+        off[1:-1][off[1:-1] < P],            # first row of every expert (tile starts)
+    ])).astype(np.int32)
+    xp = to_host(blk.x_perm)
+    assert np.array_equal(xp[rows], d["x"][sp[rows] // K])
+
+    # gate/up on sampled rows, fed the GPU's own x_perm
+    act = to_host(blk.act)
+    want_act = O.gateup_silu(xp, d["w13"], off, P=P, H=H, I=I, G=E, rows=rows)
+    assert_gemm_close(act[rows], want_act[rows], "gate/up rows")
+
+    # down on sampled rows, fed the GPU's own act
+    eo = to_host(blk.expert_out)
+    want_eo = O.down(act, d["w2"], off, P=P, I=I, H=H, G=E, pair_weight=wts.ravel(),
+                     row_to_pair=sp, rows=rows)
+    assert_gemm_close(eo[sp[rows]], want_eo[sp[rows]], "down rows")
+
+    # combine on sampled tokens: bit-exact given the GPU's expert outputs
+    eo3 = eo.reshape(T, K, H)
+    if cfg.I_shared:
+        sd = to_host(blk.sd)
+        gl = to_host(blk.gate_logit)
+        want_out = O.combine_gate(np.ascontiguousarray(eo3[toks]), None,
+                                  np.ascontiguousarray(sd[toks]), np.ascontiguousarray(gl[toks]),
+                                  T=len(toks), K=K, H=H)
+        # the shared expert's two GEMMs, fed the GPU's own x and act
+        Is = cfg.I_shared
+        one = np.array([0, T], np.int32)
+        sact = to_host(blk.act_shared)
+        want_sact = O.gateup_silu(d["x"], d["w13_shared"], one, P=T, H=H, I=Is, G=1, rows=toks)
+        assert_gemm_close(sact[toks], want_sact[toks], "shared gate/up")
+        want_sd = O.down(sact, d["w2_shared"], one, P=T, I=Is, H=H, G=1, rows=toks)
+        assert_gemm_close(sd[toks], want_sd[toks], "shared down")
+    else:
+        want_out = O.combine(np.ascontiguousarray(eo3[toks]), None, T=len(toks), K=K, H=H)
+    assert np.array_equal(out[toks], want_out)
+
+    # end to end from the raw inputs on sampled tokens
+    want_tok, ora_ids, _ = _oracle_tokens(cfg, d, toks)
+    same = np.all(np.sort(ora_ids, 1) == np.sort(ids[toks], 1), axis=1)
+    assert same.mean() >= 0.95, f"routing differs on {np.sum(~same)} of {len(toks)} tokens"
+    nmse, rel = nmse_maxrel(bf16_to_f64(out[toks][same]), bf16_to_f64(want_tok[same]))
+    assert nmse <= 1e-4 and rel <= 5e-2, (nmse, rel)
+    return blk
+
+
+def test_decode_layer_stagewise():
+    _stagewise(W.DECODE, 16, 128)
+
+
+@pytest.mark.slow
+def test_prefill_zipf_layer_stagewise():
+    blk = _stagewise(W.PREFILL, 48, 160)
+    counts = np.diff(to_host(blk.expert_offsets))
+    assert counts.max() > 4 * counts.mean()      # the load really is skewed
+
+
+@pytest.mark.slow
+def test_large_shared_layer_stagewise():
+    _stagewise(W.LARGE, 32, 96)
+
+
+def test_graph_replay_matches_eager():
+    cfg = W.DECODE
+    d = W.layer_inputs(cfg)
+    blk = _block(cfg, d)
+    x = to_dev(d["x"])
+    eager = to_host(blk.forward(x)).copy()
+    blk.capture(x)
+    for _ in range(3):
+        got = to_host(blk.replay())
+        assert np.array_equal(got, eager)

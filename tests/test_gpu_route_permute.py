@@ -1,0 +1,156 @@
+"""GPU parity of moe_route_topk and moe_permute against the CPU oracle.
+
+Router (vllm.cpp PR #509 "Honest gaps": ungrouped softmax only): given the
+same f32 logits, ids and weights are bit-exact; the tensor-core logits are
+checked against the dot-product error bound.  Permute: bit-exact."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_renorm_gb300 as m
+import oracle as O
+from mixture_experts_ffn_renorm_gb300 import workloads as W
+
+from .gpu_util import bf16_to_f64, empty, launched_since, launches, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    m.lib()
+    m.moe_device_status(clear=True)
+    yield
+    assert m.moe_device_status() == 0
+
+
+def gpu_route(x, wr, bias, wsg, logits_in, T, H, E, K, renorm=1, want_logits=False):
+    ids = empty((T, K), torch.int32)
+    w = empty((T, K), torch.float32)
+    lo = empty((T, E), torch.float32) if want_logits else None
+    gl = empty((T,), torch.float32) if wsg is not None else None
+    wsz = m.moe_route_topk_workspace_size(T, E, K)
+    ws = empty((max(wsz, 16),), torch.uint8)
+    m.moe_route_topk(None if x is None else to_dev(x), None if wr is None else to_dev(wr),
+                     None if bias is None else to_dev(bias), None if wsg is None else to_dev(wsg),
+                     None if logits_in is None else to_dev(logits_in), T, H, E, K, renorm, 0, 1,
+                     ids, w, lo, gl, ws, wsz)
+    return (to_host(ids), to_host(w), None if lo is None else to_host(lo),
+            None if gl is None else to_host(gl))
+
+
+@pytest.mark.parametrize("E,K", [(8, 2), (128, 8), (256, 8), (1000, 32), (5, 5), (64, 1)])
+@pytest.mark.parametrize("renorm", [1, 0])
+def test_topk_bit_exact_from_logits(E, K, renorm):
+    rng = np.random.default_rng(E * 7 + K)
+    T = 301
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    # ties, signed zeros, NaN and infinities in a few rows
+    logits[0, :] = 0.5
+    logits[1, ::2] = -0.0
+    logits[1, 1::2] = 0.0
+    logits[2, 0] = np.nan
+    logits[3, E - 1] = np.inf
+    logits[4, : E // 2] = -np.inf
+    want_ids, want_w, _, _ = O.route_topk(logits_in=logits, T=T, H=1, E=E, K=K,
+                                          renormalize=renorm)
+    before = launches()
+    ids, w, _, _ = gpu_route(None, None, None, None, logits, T, 8, E, K, renorm)
+    assert launched_since(before, "route_topk") == 1
+    assert np.array_equal(ids, want_ids)
+    ok = ~np.isnan(want_w)
+    assert np.array_equal(np.isnan(w), ~ok)
+    assert np.array_equal(w[ok].view(np.uint32), want_w[ok].view(np.uint32))
+
+
+@pytest.mark.parametrize("T,H,E,K", [(4, 64, 8, 2), (300, 256, 128, 8), (131, 512, 256, 8),
+                                     (16, 2048, 128, 8), (2, 72, 40, 3)])
+def test_router_gemm_logits_within_bound_and_selection_exact(T, H, E, K):
+    rng = np.random.default_rng(T + H + E)
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = W.to_bf16_bits((0.02 * rng.standard_normal((E, H))).astype(np.float32))
+    bias = (0.5 * rng.standard_normal(E)).astype(np.float32)
+    wsg = W.to_bf16_bits((0.02 * rng.standard_normal(H)).astype(np.float32))
+    before = launches()
+    ids, w, lo, gl = gpu_route(x, wr, bias, wsg, None, T, H, E, K, want_logits=True)
+    assert launched_since(before, "route_logits") == 1
+    xf, wf = bf16_to_f64(x), bf16_to_f64(wr)
+    exact = xf @ wf.T + bias
+    # tensor-core f32 accumulation: allow 2^-23 per addition (truncating adders)
+    bound = (H + 2) * 2.0**-23 * (np.abs(xf) @ np.abs(wf).T + np.abs(bias))
+    assert np.all(np.abs(lo - exact) <= bound), float(np.max(np.abs(lo - exact) / bound))
+    # selection and weights are bit-exact functions of the GPU's logits
+    want_ids, want_w, _, _ = O.route_topk(logits_in=lo, T=T, H=1, E=E, K=K)
+    assert np.array_equal(ids, want_ids)
+    assert np.array_equal(w.view(np.uint32), want_w.view(np.uint32))
+    gl_exact = xf @ bf16_to_f64(wsg)
+    gl_bound = (H + 2) * 2.0**-23 * (np.abs(xf) @ np.abs(bf16_to_f64(wsg)))
+    assert np.all(np.abs(gl - gl_exact) <= gl_bound)
+    # without logits_out the logits go to the workspace and the ids are the same
+    ids2, w2, _, _ = gpu_route(x, wr, bias, None, None, T, H, E, K)
+    assert np.array_equal(ids2, ids) and np.array_equal(w2, w)
+
+
+def test_router_refusals():
+    T, E, K = 4, 8, 2
+    logits = np.zeros((T, E), np.float32)
+    ids = empty((T, K), torch.int32)
+    w = empty((T, K), torch.float32)
+    for scoring, n_group, k, code in ((1, 1, K, m.ERR_UNSUPPORTED), (0, 2, K, m.ERR_UNSUPPORTED),
+                                      (0, 1, 9, m.ERR_ARG), (0, 1, 0, m.ERR_ARG)):
+        with pytest.raises(m.MoeError) as ei:
+            m.moe_route_topk(None, None, None, None, to_dev(logits), T, 8, E, k, 1, scoring,
+                             n_group, ids, w, None, None, None, 0)
+        assert ei.value.code == code
+
+
+def gpu_permute(ids, x, T, K, E, H):
+    P = T * K
+    off = empty((E + 1,), torch.int32)
+    sp = empty((max(P, 1),), torch.int32)
+    p2r = empty((max(P, 1),), torch.int32)
+    xp = empty((max(P, 1), H), torch.bfloat16) if x is not None else None
+    wsz = m.moe_permute_workspace_size(T, K, E)
+    ws = empty((max(wsz, 16),), torch.uint8)
+    m.moe_permute(to_dev(ids) if P else None, None if x is None else to_dev(x), T, K, E, H, off,
+                  sp, p2r, xp, ws, wsz)
+    return (to_host(off), to_host(sp)[:P], to_host(p2r)[:P],
+            None if xp is None else to_host(xp)[:P])
+
+
+def _ids(T, K, E, seed, skew=False):
+    rng = np.random.default_rng(seed)
+    if skew:
+        p = 1.0 / np.arange(1, E + 1) ** 1.1
+        p /= p.sum()
+        return np.stack([rng.choice(E, K, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    return np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,K,E,H", [(4, 2, 8, 64), (16, 8, 128, 2048), (1000, 8, 128, 64),
+                                     (2048, 8, 256, 128), (77, 3, 1000, 16), (1, 1, 1, 8),
+                                     (8192, 8, 128, 8)])
+def test_permute_bit_exact(T, K, E, H):
+    ids = _ids(T, K, E, T + E, skew=(T >= 1000))
+    rng = np.random.default_rng(5)
+    x = rng.integers(0, 65535, (T, H), dtype=np.uint16)
+    want = O.permute(ids, x, T=T, K=K, E=E, H=H)
+    before = launches()
+    got = gpu_permute(ids, x, T, K, E, H)
+    assert launched_since(before, "permute_place") == 1
+    for g, w_, name in zip(got, want, ("expert_offsets", "sorted_pair", "pair_to_row", "x_perm")):
+        assert np.array_equal(g, w_), name
+
+
+def test_permute_empty_batch_zeroes_offsets():
+    off, _, _, _ = gpu_permute(np.zeros((0, 2), np.int32), None, 0, 2, 8, 8)
+    assert np.array_equal(off, np.zeros(9, np.int32))
+
+
+def test_permute_flags_out_of_range_ids():
+    ids = np.array([[0, 1], [2, 9]], np.int32)
+    m.moe_device_status(clear=True)
+    gpu_permute(ids, None, 2, 2, 4, 8)
+    assert m.moe_device_status(clear=True) & m.STATUS_BAD_ID
