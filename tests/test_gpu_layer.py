@@ -139,8 +139,14 @@ def _stagewise(cfg, n_tok_sample, n_row_sample):
     want_tok, ora_ids, _ = _oracle_tokens(cfg, d, toks)
     same = np.all(np.sort(ora_ids, 1) == np.sort(ids[toks], 1), axis=1)
     assert same.mean() >= 0.95, f"routing differs on {np.sum(~same)} of {len(toks)} tokens"
-    nmse, rel = nmse_maxrel(bf16_to_f64(out[toks][same]), bf16_to_f64(want_tok[same]))
-    assert nmse <= 1e-4 and rel <= 5e-2, (nmse, rel)
+    # end to end the two sides round each of the K expert rows to bf16 independently
+    # (one-ulp flips of 2^-8 relative), so elements are compared against the
+    # output's rms as well as their own size
+    g, r = bf16_to_f64(out[toks][same]), bf16_to_f64(want_tok[same])
+    nmse, _ = nmse_maxrel(g, r)
+    rms = float(np.sqrt(np.mean(r * r)))
+    worst = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), rms)))
+    assert nmse <= GEMM_NMSE and worst <= GEMM_MAXREL, (nmse, worst)
     return blk
 
 
