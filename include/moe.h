@@ -140,6 +140,29 @@ int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, int K, int E
 size_t moe_permute_workspace_size(int T, int K, int E);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_noalloc -- moe_permute without a caller-provided workspace, for
+ * callers that cannot allocate device memory (no reachable allocator at the
+ * call site, or allocation forbidden after start-up).  The pages have no
+ * counterpart of this entry point; it exists for those callers only.
+ *
+ * Same arguments, outputs and bit-exact results as moe_permute, minus the
+ * workspace.  The scratch is a fixed array of MOE_PERMUTE_NOALLOC_MAX_SCRATCH
+ * bytes inside the library's device memory (held by every GPU that loads the
+ * library until the process exits); calls whose moe_permute_workspace_size
+ * exceeds it are refused with MOE_ERR_WORKSPACE (e.g. P = T*K up to 65536
+ * pairs with E up to 1024, or up to 262144 pairs with E up to 256).  The call
+ * allocates nothing.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current, so make it
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents (no state carries over: every entry read is written first);
+ * calls whose kernels may overlap on the GPU race on it.
+ * ---------------------------------------------------------------------- */
+#define MOE_PERMUTE_NOALLOC_MAX_SCRATCH (1 << 20)
+int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int K, int E, int H,
+                        int32_t* expert_offsets, int32_t* sorted_pair, int32_t* pair_to_row,
+                        void* x_perm_bf16, void* stream);
+
+/* ------------------------------------------------------------------------
  * moe_grouped_gemm_gateup_silu_bf16 -- kMoeGroupedGemmBf16GateUpSilu of
  * [I3094].  For every group g and row r in [group_offsets[g], group_offsets[g+1]):
  *   gate[n] = bf16( sum_h A[r,h] * w13[g, n, h] )        n in [0, I)

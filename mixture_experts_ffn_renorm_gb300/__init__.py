@@ -30,7 +30,8 @@ KID_COUNT = 16
 
 EXPORTS = (
     "moe_last_error", "moe_abi_version", "moe_route_topk", "moe_route_topk_workspace_size",
-    "moe_permute", "moe_permute_workspace_size", "moe_grouped_gemm_gateup_silu_bf16",
+    "moe_permute", "moe_permute_workspace_size", "moe_permute_noalloc",
+    "moe_grouped_gemm_gateup_silu_bf16",
     "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
 )
@@ -57,6 +58,7 @@ _SIGS = {
     "moe_route_topk_workspace_size": ([_I, _I, _I], _SZ),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
+    "moe_permute_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_silu_bf16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
@@ -142,6 +144,19 @@ def moe_permute(topk_ids, x, T, K, E, H, expert_offsets, sorted_pair, pair_to_ro
 
 def moe_permute_workspace_size(T, K, E) -> int:
     return lib().moe_permute_workspace_size(T, K, E)
+
+
+PERMUTE_NOALLOC_MAX_SCRATCH = 1 << 20
+
+
+def moe_permute_noalloc(topk_ids, x, T, K, E, H, expert_offsets, sorted_pair, pair_to_row, x_perm,
+                        stream=None, check=True):
+    """moe_permute without a workspace: for callers that cannot allocate device
+    memory.  Uses the library's fixed 1 MiB scratch array (see include/moe.h)."""
+    rc = lib().moe_permute_noalloc(_ptr(topk_ids), _ptr(x), T, K, E, H, _ptr(expert_offsets),
+                                   _ptr(sorted_pair), _ptr(pair_to_row), _ptr(x_perm),
+                                   _stream(stream))
+    return _check(rc) if check else rc
 
 
 def moe_grouped_gemm_gateup_silu_bf16(a, a_row_gather, w13, group_offsets, P, H, I, G, act,
