@@ -73,7 +73,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);
+int moe_abi_version(void);  /* 2 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -172,9 +172,14 @@ int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int 
  * BEFORE the activation ([I3094] "BF16 result narrowing before activation").
  *
  *   a            bf16 [P,H] (rows in group order), or, when a_row_gather is
- *                set, bf16 [n_src,H] read through a_row_gather
- *   a_row_gather int32 [P] or NULL: row r of the product uses A row a_row_gather[r]
- *                (e.g. sorted_pair[r] / K to read x [T,H] without x_perm)
+ *                set, bf16 [a_rows,H] read through a_row_gather
+ *   a_rows       rows of `a` when gathering (ignored otherwise)
+ *   a_row_gather int32 [P] or NULL: row r of the product reads A row
+ *                a_row_gather[r] / gather_div.  With sorted_pair and gather_div = K
+ *                this reads every routed row straight from x [T,H] (no x_perm);
+ *                rows are fetched by TMA tile::gather4.  An index outside
+ *                [0, a_rows) reads zeros.
+ *   gather_div   >= 1 when gathering (ignored otherwise)
  *   w13          bf16 [G, 2I, H]: gate rows first, then up rows, per group
  *   group_offsets int32 [G+1], non-decreasing, group_offsets[G] <= P;
  *                read on the device (no host round trip); may be NULL when G == 1
@@ -183,10 +188,11 @@ int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int 
  *   P >= 0, H > 0 and I > 0 multiples of 64, 1 <= G <= 1024
  *   workspace    >= moe_grouped_gemm_workspace_size(...) bytes (currently 0)
  * ---------------------------------------------------------------------- */
-int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, const int32_t* a_row_gather,
-                                      const void* w13_bf16, const int32_t* group_offsets,
-                                      int P, int H, int I, int G, void* act_bf16,
-                                      void* workspace, size_t ws_bytes, void* stream);
+int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows, const int32_t* a_row_gather,
+                                      int gather_div, const void* w13_bf16,
+                                      const int32_t* group_offsets, int P, int H, int I, int G,
+                                      void* act_bf16, void* workspace, size_t ws_bytes,
+                                      void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_grouped_gemm_down_bf16 -- kMoeGroupedGemmBf16 of [I3094].  For every

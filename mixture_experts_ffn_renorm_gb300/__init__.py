@@ -59,7 +59,8 @@ _SIGS = {
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
     "moe_permute_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
-    "moe_grouped_gemm_gateup_silu_bf16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_grouped_gemm_gateup_silu_bf16": ([_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _SZ,
+                                           _P], _I),
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
@@ -159,11 +160,13 @@ def moe_permute_noalloc(topk_ids, x, T, K, E, H, expert_offsets, sorted_pair, pa
     return _check(rc) if check else rc
 
 
-def moe_grouped_gemm_gateup_silu_bf16(a, a_row_gather, w13, group_offsets, P, H, I, G, act,
-                                      workspace=None, ws_bytes=0, stream=None, check=True):
-    rc = lib().moe_grouped_gemm_gateup_silu_bf16(_ptr(a), _ptr(a_row_gather), _ptr(w13),
-                                                 _ptr(group_offsets), P, H, I, G, _ptr(act),
-                                                 _ptr(workspace), ws_bytes, _stream(stream))
+def moe_grouped_gemm_gateup_silu_bf16(a, a_rows, a_row_gather, gather_div, w13, group_offsets, P,
+                                      H, I, G, act, workspace=None, ws_bytes=0, stream=None,
+                                      check=True):
+    rc = lib().moe_grouped_gemm_gateup_silu_bf16(_ptr(a), a_rows, _ptr(a_row_gather), gather_div,
+                                                 _ptr(w13), _ptr(group_offsets), P, H, I, G,
+                                                 _ptr(act), _ptr(workspace), ws_bytes,
+                                                 _stream(stream))
     return _check(rc) if check else rc
 
 

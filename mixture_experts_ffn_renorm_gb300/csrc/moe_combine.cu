@@ -90,18 +90,24 @@ combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
   if (kMode != kGateOnly && live) {
     const size_t row0 = static_cast<size_t>(t) * K;
     for (int k0 = 0; k0 < K; k0 += kChunkK) {
+      // all kChunkK loads are issued before any arithmetic: rows past K load
+      // row K-1 again (a cache hit) instead of being predicated off, so the
+      // compiler keeps every load in flight at once
       float v[kChunkK][kVec];
-      const int kn = min(kChunkK, K - k0);
+      float wk[kChunkK];
 #pragma unroll
-      for (int j = 0; j < kChunkK; ++j)
-        if (j < kn) Vec8<EoT>::load(eo, (row0 + k0 + j) * H + c0, v[j]);
+      for (int j = 0; j < kChunkK; ++j) {
+        const int kk = min(k0 + j, K - 1);
+        Vec8<EoT>::load(eo, (row0 + kk) * H + c0, v[j]);
+        wk[j] = kHasW ? __ldg(w + row0 + kk) : 1.0f;
+      }
+      const int kn = min(kChunkK, K - k0);
 #pragma unroll
       for (int j = 0; j < kChunkK; ++j) {
         if (j < kn) {
-          float wk = kHasW ? __ldg(w + row0 + k0 + j) : 1.0f;
 #pragma unroll
           for (int i = 0; i < kVec; ++i) {
-            float term = kHasW ? __fmul_rn(v[j][i], wk) : v[j][i];
+            float term = kHasW ? __fmul_rn(v[j][i], wk[j]) : v[j][i];
             acc[i] = __fadd_rn(acc[i], term);
           }
         }

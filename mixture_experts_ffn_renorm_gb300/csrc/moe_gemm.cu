@@ -36,12 +36,12 @@ namespace gemm {
 constexpr int BM = 128;           // rows per tile (MMA M)
 constexpr int BK = 64;            // bf16 per 128-byte swizzled row: K per stage
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int BOX_ROWS = 128;     // rows per TMA box
-constexpr int BOX_BYTES = BOX_ROWS * BK * 2;
+// bytes of the 227 KB per-block shared memory left for the stage ring after the
+// barriers, the schedule tables (2 x 4 KB) and the 1 KB alignment slack
+constexpr int kSmemBudget = 227 * 1024 - 11 * 1024;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 enum Epi { EPI_GATEUP = 0, EPI_DOWN = 1, EPI_F32 = 2 };
@@ -54,6 +54,8 @@ struct Params {
   int G;                         // groups
   int b_rows_per_group;          // rows of the 2-D view of B per group
   int half_off;                  // gate/up: row offset of the up half inside a group
+  const int32_t* row_gather;     // gate/up: A row of product row r is row_gather[r] / gather_div
+  int gather_div;
   void* out;
   const float* pair_weight;      // down: [P] by destination row, or null
   const int32_t* row_to_pair;    // down: destination row, or null
@@ -63,8 +65,15 @@ struct Params {
   int kid;
 };
 
+// Stage ring depth: as many stages as fit the budget, at most 8.
 template <int kN>
+__host__ __device__ constexpr int stages_for() {
+  return kSmemBudget / (A_BYTES + kN * BK * 2) > 8 ? 8 : kSmemBudget / (A_BYTES + kN * BK * 2);
+}
+
+template <int kN, int kStages>
 struct Smem {
+  static_assert(kStages >= 2, "stage ring too shallow");
   static constexpr int B_BYTES = kN * BK * 2;
   static constexpr int STAGE_A = 0;
   static constexpr int STAGE_B = kStages * A_BYTES;
@@ -130,7 +139,11 @@ template <int kN, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using S = Smem<kN>;
+  constexpr int kStages = stages_for<kN>();
+  using S = Smem<kN, kStages>;
+  // B arrives in boxes of kBoxB rows (the tensor map's box height)
+  constexpr int kBoxB = (kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128);
+  constexpr int kBoxBytes = kBoxB * BK * 2;
   constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;
   constexpr int kTmemCols = 2 * kN;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, kN);
@@ -220,7 +233,60 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
 
-  if (warp == 0) {
+  if (warp == 0 && p.row_gather != nullptr) {
+    // ------------------------------------------------------------ TMA producer, gathered A
+    // The whole warp loads: lane l fetches rows 4l..4l+3 of the A tile with one
+    // tile::gather4 per stage (row indices read once per tile); lane 0 owns the
+    // barrier and the B boxes.
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
+      const int brow = t.g * p.b_rows_per_group + t.n0;
+      int src[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = min(t.row0 + 4 * lane + q, p.P - 1);  // rows past the group are masked later
+        src[q] = __ldg(p.row_gather + r) / p.gather_div;
+      }
+      for (int kb = 0; kb < nk; ++kb) {
+        int go = 1;
+        if (lane == 0) go = wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status) ? 1 : 0;
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) { ok = false; break; }
+        const uint32_t fb = bar_full(stage);
+        const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
+        const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kStageTx);
+        __syncwarp();
+        ptx::tma_gather4(sa + lane * 4 * 128, &tmA, kb * BK, src[0], src[1], src[2], src[3], fb);
+        if (lane == 0) {
+          if (kEpi == EPI_GATEUP) {
+            ptx::tma_load_2d(sb, &tmB, kb * BK, brow, fb);
+            ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow + p.half_off, fb);
+          } else {
+#pragma unroll
+            for (int h = 0; h < kN / kBoxB; ++h)
+              ptx::tma_load_2d(sb + h * kBoxBytes, &tmB, kb * BK, brow + h * kBoxB, fb);
+          }
+        }
+        ++issued;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < min(issued, kStages); ++i) {
+        if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar_full(s), ph) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -239,11 +305,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0, fb);
           if (kEpi == EPI_GATEUP) {
             ptx::tma_load_2d(sb, &tmB, kb * BK, brow, fb);
-            ptx::tma_load_2d(sb + BOX_BYTES, &tmB, kb * BK, brow + p.half_off, fb);
+            ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow + p.half_off, fb);
           } else {
 #pragma unroll
-            for (int h = 0; h < kN / BOX_ROWS; ++h)
-              ptx::tma_load_2d(sb + h * BOX_BYTES, &tmB, kb * BK, brow + h * BOX_ROWS, fb);
+            for (int h = 0; h < kN / kBoxB; ++h)
+              ptx::tma_load_2d(sb + h * kBoxBytes, &tmB, kb * BK, brow + h * kBoxB, fb);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -384,14 +450,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::tmem_ld_32x32b_x32(taddr + c * 32, y);
           ptx::tmem_ld_wait();
           const int col = t.n0 + c * 32;
-          if (valid) {
+          if (valid && col < p.N) {
+            float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (col + j < p.N) {
-                float v = __uint_as_float(y[j]);
-                if (p.bias) v = __fadd_rn(v, __ldg(p.bias + col + j));
-                out[static_cast<size_t>(row) * p.N + col + j] = v;
-              }
+              v[j] = __uint_as_float(y[j]);
+              if (p.bias && col + j < p.N) v[j] = __fadd_rn(v[j], __ldg(p.bias + col + j));
+            }
+            float* dst = out + static_cast<size_t>(row) * p.N + col;
+            if ((p.N & 3) == 0) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                if (col + 4 * q < p.N)
+                  reinterpret_cast<float4*>(dst)[q] =
+                      make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col + j < p.N) dst[j] = v[j];
             }
           }
         }
@@ -430,14 +506,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// rows x cols bf16 matrix (row-major, cols contiguous), box of 64 cols x 128 rows
-int make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, const char* op,
-              const char* what) {
+// rows x cols bf16 matrix (row-major, cols contiguous), box of 64 cols x box_rows rows
+int make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows,
+              const char* op, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return set_error(MOE_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", op);
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {BK, BOX_ROWS};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -462,7 +538,7 @@ template <int kN, int kEpi>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<kN, kEpi>;
-  const int smem = Smem<kN>::ALLOC;
+  const int smem = Smem<kN, stages_for<kN>()>::ALLOC;
   static int configured_dev[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -513,8 +589,9 @@ int launch_router_logits(const void* x, const void* w_router, const float* bias,
   if (T == 0) return MOE_OK;
   CUtensorMap ta, tb;
   int rc;
-  if ((rc = make_tmap(&ta, x, T, H, op, "x")) != MOE_OK) return rc;
-  if ((rc = make_tmap(&tb, w_router, E, H, op, "w_router")) != MOE_OK) return rc;
+  // 128 x 64 tiles: twice the CTAs of a full-width tile, so more SMs stream x
+  if ((rc = make_tmap(&ta, x, T, H, BM, op, "x")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tb, w_router, E, H, 64, op, "w_router")) != MOE_OK) return rc;
   Params p{};
   p.group_offsets = nullptr;
   p.P = T;
@@ -526,8 +603,7 @@ int launch_router_logits(const void* x, const void* w_router, const float* bias,
   p.out = logits;
   p.bias = bias;
   p.kid = MOE_KID_ROUTE_LOGITS;
-  if (E <= 128) return launch<128, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 128), stream);
-  return launch<256, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 256), stream);
+  return launch<64, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 64), stream);
 }
 
 }  // namespace moe
@@ -537,7 +613,8 @@ using namespace moe::gemm;
 
 extern "C" size_t moe_grouped_gemm_workspace_size(int, int, int, int) { return 0; }
 
-extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, const int32_t* a_row_gather,
+extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
+                                                 const int32_t* a_row_gather, int gather_div,
                                                  const void* w13_bf16,
                                                  const int32_t* group_offsets, int P, int H,
                                                  int I, int G, void* act_bf16, void* workspace,
@@ -550,12 +627,18 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, const int32
   if ((rc = check_common(op, P, H, I, G, a_bf16, w13_bf16, act_bf16)) != MOE_OK) return rc;
   if (!group_offsets && G != 1)
     return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
-  if (a_row_gather)
-    return set_error(MOE_ERR_UNSUPPORTED, "%s: a_row_gather is not implemented yet", op);
+  if (a_row_gather && (a_rows < 1 || gather_div < 1))
+    return set_error(MOE_ERR_ARG, "%s: gathering needs a_rows >= 1 and gather_div >= 1", op);
   if (P == 0) return MOE_OK;
   CUtensorMap ta, tb;
-  if ((rc = make_tmap(&ta, a_bf16, P, H, op, "a")) != MOE_OK) return rc;
-  if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, op, "w13")) != MOE_OK)
+  if (a_row_gather) {
+    // one-row boxes for tile::gather4
+    if ((rc = make_tmap(&ta, a_bf16, a_rows, H, 1, op, "a (gathered)")) != MOE_OK) return rc;
+  } else if ((rc = make_tmap(&ta, a_bf16, P, H, BM, op, "a")) != MOE_OK) {
+    return rc;
+  }
+  if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, 128, op, "w13")) !=
+      MOE_OK)
     return rc;
   Params p{};
   p.group_offsets = group_offsets;
@@ -565,6 +648,8 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, const int32
   p.G = G;
   p.b_rows_per_group = 2 * I;
   p.half_off = I;
+  p.row_gather = a_row_gather;
+  p.gather_div = gather_div;
   p.out = act_bf16;
   p.kid = MOE_KID_GEMM_GATEUP;
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128),
@@ -586,8 +671,8 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
     return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
   if (P == 0) return MOE_OK;
   CUtensorMap ta, tb;
-  if ((rc = make_tmap(&ta, act_bf16, P, I, op, "act")) != MOE_OK) return rc;
-  if ((rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, op, "w2")) != MOE_OK)
+  if ((rc = make_tmap(&ta, act_bf16, P, I, BM, op, "act")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) != MOE_OK)
     return rc;
   Params p{};
   p.group_offsets = group_offsets;

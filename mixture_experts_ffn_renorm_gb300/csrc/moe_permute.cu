@@ -6,8 +6,9 @@
 //
 //   count   one warp per chunk of 512 pairs: per-chunk expert histogram in
 //           shared memory (bad ids raise MOE_STATUS_BAD_ID and are skipped)
-//   scan    one block: per expert, exclusive scan of the chunk counts in chunk
-//           order; then the exclusive scan over experts -> expert_offsets
+//   scan    one block: per expert (one warp each), exclusive scan of the chunk
+//           counts in chunk order; then the exclusive scan over experts ->
+//           expert_offsets
 //   place   one warp per chunk again, 32 pairs at a time in pair order: the
 //           rank of a pair among equal experts of its step comes from
 //           __match_any_sync, so rows inside an expert ascend with p
@@ -42,31 +43,54 @@ permute_count(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
     if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
       atomicOr(status, static_cast<unsigned int>(MOE_STATUS_BAD_ID));
     __syncwarp();
-    for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(c) * E + e] = h[e];
+    for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(e) * n_chunks + c] = h[e];
   }
 }
 
+// hist is laid out [E][n_chunks]: one warp scans one expert's chunk counts
+// (coalesced, all loads of a batch in flight), then the block scans the
+// per-expert totals into expert_offsets.
 __global__ void __launch_bounds__(1024)
 permute_scan(int32_t* __restrict__ hist, int E, int n_chunks, int32_t* __restrict__ offsets,
              unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_SCAN);
+  __shared__ int32_t tot[1024];
   __shared__ int32_t warp_sum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int run = 0;
-  if (tid < E) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const size_t i = static_cast<size_t>(c) * E + tid;
-      const int v = hist[i];
-      hist[i] = run;
-      run += v;
+  constexpr int kBatch = 8;
+  for (int e = warp; e < E; e += 32) {
+    int32_t* row = hist + static_cast<size_t>(e) * n_chunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32 * kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int c = c0 + b * 32 + lane;
+        v[b] = c < n_chunks ? row[c] : 0;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        int incl = v[b];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const int c = c0 + b * 32 + lane;
+        if (c < n_chunks) row[c] = carry + incl - v[b];
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
+    if (lane == 0) tot[e] = carry;
   }
+  __syncthreads();
   // block-wide exclusive scan of the per-expert totals (E <= 1024)
+  const int run = tid < E ? tot[tid] : 0;
   int incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
   }
   if (lane == 31) warp_sum[warp] = incl;
   __syncthreads();
@@ -75,8 +99,8 @@ permute_scan(int32_t* __restrict__ hist, int E, int n_chunks, int32_t* __restric
     int wi = ws;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += v;
+      const int u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
     }
     warp_sum[lane] = wi - ws;
   }
@@ -98,7 +122,7 @@ permute_place(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   if (c >= n_chunks) return;
   int32_t* cnt = sh + warp * E;
   for (int e = lane; e < E; e += 32)
-    cnt[e] = hist[static_cast<size_t>(c) * E + e] + __ldg(offsets + e);
+    cnt[e] = hist[static_cast<size_t>(e) * n_chunks + c] + __ldg(offsets + e);
   __syncwarp();
   const int p0 = c * kChunk, p1 = min(P, p0 + kChunk);
   const uint32_t lt_mask = (1u << lane) - 1u;

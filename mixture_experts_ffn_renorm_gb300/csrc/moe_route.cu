@@ -35,6 +35,10 @@ __device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
   return ia < ib;
 }
 
+// One warp selects the top-K of one token.  The weights' exps are then
+// evaluated by the whole block, one (token, rank) pair per thread, so that the
+// double-precision chain of exp_cr runs on full warps (GB300's FP64 rate is
+// low, and a warp instruction costs the same with 8 or 32 lanes active).
 template <int kPerLane>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormalize,
@@ -42,51 +46,66 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormali
             int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ gl_out,
             unsigned long long* launches) {
   count_launch(launches, MOE_KID_ROUTE_TOPK);
+  __shared__ float s_sel[kWarpsPerBlock][32];
+  __shared__ float s_ex[kWarpsPerBlock][32];
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
+  const int wib = threadIdx.x >> 5;
+  const int t = blockIdx.x * kWarpsPerBlock + wib;
+  const bool live = t < T;
   float v[kPerLane];
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? __ldg(row + e) : 0.0f;
-  }
-  uint32_t taken = 0;
   float my_sel = 0.0f;
   int my_id = 0;
-  for (int j = 0; j < K; ++j) {
-    float bv = 0.0f;
-    int be = -1;
+  if (live) {
+    const float* row = logits + static_cast<size_t>(t) * E;
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, be)) {
-        bv = v[i];
-        be = e;
-      }
+      v[i] = e < E ? __ldg(row + e) : 0.0f;
     }
+    uint32_t taken = 0;
+    for (int j = 0; j < K; ++j) {
+      float bv = 0.0f;
+      int be = -1;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (oe >= 0 && ranks_above(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
+      for (int i = 0; i < kPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, be)) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe >= 0 && ranks_above(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) {
+        my_sel = bv;
+        my_id = be;
       }
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) {
-      my_sel = bv;
-      my_id = be;
-    }
+    s_sel[wib][lane] = my_sel;
   }
-  // weights: e_j = exp(l_j - l_0), S summed in rank order from +0, w_j = e_j / S
-  const float m = __shfl_sync(0xffffffffu, my_sel, 0);
-  const float ex = exp_cr(__fsub_rn(my_sel, m));
+  __syncthreads();
+  // e_j = exp(l_j - l_0) for every (token, rank) pair of the block
+  const int n_live = min(kWarpsPerBlock, T - static_cast<int>(blockIdx.x) * kWarpsPerBlock);
+  for (int q = threadIdx.x; q < n_live * K; q += blockDim.x) {
+    const int tt = q / K, j = q - tt * K;
+    s_ex[tt][j] = exp_cr(__fsub_rn(s_sel[tt][j], s_sel[tt][0]));
+  }
+  __syncthreads();
+  if (!live) return;
+  const float m = s_sel[wib][0];
   float S = 0.0f;
+  float ex = 0.0f;
   if (renormalize) {
-    for (int j = 0; j < K; ++j) S = __fadd_rn(S, __shfl_sync(0xffffffffu, ex, j));
+    for (int j = 0; j < K; ++j) S = __fadd_rn(S, s_ex[wib][j]);
+    if (lane < K) ex = s_ex[wib][lane];
   } else {
     float ev[kPerLane];
 #pragma unroll
@@ -97,6 +116,7 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormali
         const float term = __shfl_sync(0xffffffffu, ev[i], l);
         if (l + 32 * i < E) S = __fadd_rn(S, term);
       }
+    if (lane < K) ex = s_ex[wib][lane];
   }
   if (lane < K) {
     ids[static_cast<size_t>(t) * K + lane] = my_id;

@@ -37,9 +37,13 @@ class MoeBlock:
     """
 
     def __init__(self, H, I, E, K, weights, max_tokens, device="cuda", I_shared=0,
-                 routed_scale=1.0):
+                 routed_scale=1.0, gather=False):
         self.H, self.I, self.E, self.K, self.Is = H, I, E, K, I_shared
         self.max_tokens = max_tokens
+        # gather=True: the gate/up GEMM reads each routed row straight from x
+        # (through sorted_pair / K); False: permute materialises x_perm and the
+        # GEMM streams it with tiled TMA loads
+        self.gather = gather
         self.routed_scale = float(routed_scale)
         self.device = torch.device(device)
         dv = self.device
@@ -61,7 +65,7 @@ class MoeBlock:
         self.expert_offsets = torch.empty((E + 1,), dtype=i32, device=dv)
         self.sorted_pair = torch.empty((P,), dtype=i32, device=dv)
         self.pair_to_row = torch.empty((P,), dtype=i32, device=dv)
-        self.x_perm = torch.empty((P, H), dtype=bf, device=dv)
+        self.x_perm = None if gather else torch.empty((P, H), dtype=bf, device=dv)
         self.act = torch.empty((P, I), dtype=bf, device=dv)
         self.expert_out = torch.empty((P, H), dtype=bf, device=dv)
         self.out = torch.empty((T, H), dtype=bf, device=dv)
@@ -100,16 +104,22 @@ class MoeBlock:
         moe_permute(self.topk_ids, x, T, K, E, H, self.expert_offsets, self.sorted_pair,
                     self.pair_to_row, self.x_perm, ws, ws.numel(), stream)
         mark("permute")
-        moe_grouped_gemm_gateup_silu_bf16(self.x_perm, None, self.w13, self.expert_offsets, P, H,
-                                          I, E, self.act, None, 0, stream)
+        if self.gather:
+            moe_grouped_gemm_gateup_silu_bf16(x, T, self.sorted_pair, K, self.w13,
+                                              self.expert_offsets, P, H, I, E, self.act, None, 0,
+                                              stream)
+        else:
+            moe_grouped_gemm_gateup_silu_bf16(self.x_perm, P, None, 1, self.w13,
+                                              self.expert_offsets, P, H, I, E, self.act, None, 0,
+                                              stream)
         mark("gemm_gateup")
         moe_grouped_gemm_down_bf16(self.act, self.w2, self.expert_offsets, self.topk_w,
                                    self.sorted_pair, P, I, H, E, self.expert_out, None, 0, stream)
         mark("gemm_down")
         out = self.out[:T]
         if self.has_shared:
-            moe_grouped_gemm_gateup_silu_bf16(x, None, self.w13_shared, None, T, H, self.Is, 1,
-                                              self.act_shared, None, 0, stream)
+            moe_grouped_gemm_gateup_silu_bf16(x, T, None, 1, self.w13_shared, None, T, H, self.Is,
+                                              1, self.act_shared, None, 0, stream)
             moe_grouped_gemm_down_bf16(self.act_shared, self.w2_shared, None, None, None, T,
                                        self.Is, H, 1, self.sd, None, 0, stream)
             mark("shared_expert")
@@ -125,7 +135,7 @@ class MoeBlock:
 
     # launches per forward (for the bench's gpu_launches claim)
     def kernels_per_forward(self) -> int:
-        n = 2 + 4 + 1 + 1 + 1   # route (logits, top-k), permute (4), gate/up, down, combine
+        n = 2 + (3 if self.gather else 4) + 3  # route (2), permute (3 or 4), 2 GEMMs, combine
         if self.has_shared:
             n += 2
         return n

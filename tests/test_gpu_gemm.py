@@ -57,10 +57,32 @@ def test_gateup_silu(sizes, H, I):
     act = empty((P, I), torch.bfloat16)
     act.fill_(0)
     before = launches()
-    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), None, to_dev(W13), to_dev(off), P, H, I, G, act)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I, G,
+                                        act)
     assert launched_since(before, "gemm_gateup") == 1
     assert m.moe_device_status() == 0
     assert_gemm_close(to_host(act), want, "gate/up")
+
+
+@pytest.mark.parametrize("sizes,H,I", SHAPES)
+@pytest.mark.parametrize("K", [1, 3, 8])
+def test_gateup_silu_gathered_rows(sizes, H, I, K):
+    # product row r reads x[pair[r] // K]: the routed rows come straight from the
+    # token matrix through TMA gather4 (no x_perm)
+    off, P, G, _, W13, _ = _case(sizes, H, I, sum(sizes) + 7 * H + K)
+    rng = np.random.default_rng(P + K)
+    T = max(1, (P + K - 1) // K) + 3
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    pair = rng.integers(0, T * K, P).astype(np.int32)
+    want = O.gateup_silu(x, W13, off, P=P, H=H, I=I, G=G, a_row_gather=(pair // K).astype(np.int32))
+    act = empty((P, I), torch.bfloat16)
+    act.fill_(0)
+    before = launches()
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(x), T, to_dev(pair), K, to_dev(W13), to_dev(off), P,
+                                        H, I, G, act)
+    assert launched_since(before, "gemm_gateup") == 1
+    assert m.moe_device_status() == 0
+    assert_gemm_close(to_host(act), want, "gathered gate/up")
 
 
 @pytest.mark.parametrize("sizes,H,I", SHAPES)
@@ -93,7 +115,7 @@ def test_gateup_narrowing_is_visible_on_the_gpu():
     Wt[0, :, 0] = 1.0
     Wt[0, :, 1] = 1.0
     act = empty((1, I), torch.bfloat16)
-    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(W.to_bf16_bits(A)), None,
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(W.to_bf16_bits(A)), 1, None, 1,
                                         to_dev(W.to_bf16_bits(Wt)), to_dev(np.array([0, 1], np.int32)),
                                         1, H, I, 1, act)
     assert np.all(to_host(act) == 0x3F3B)
@@ -105,13 +127,14 @@ def test_single_group_without_offsets_and_rows_outside_groups():
     A = W.to_bf16_bits(rng.standard_normal((P, H)).astype(np.float32))
     W13 = W.to_bf16_bits((0.05 * rng.standard_normal((1, 2 * I, H))).astype(np.float32))
     act = empty((P, I), torch.bfloat16)
-    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), None, to_dev(W13), None, P, H, I, 1, act)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), None, P, H, I, 1, act)
     want = O.gateup_silu(A, W13, np.array([0, P], np.int32), P=P, H=H, I=I, G=1)
     assert_gemm_close(to_host(act), want, "single group")
     # rows past group_offsets[G] are not written
     off = np.array([0, 150], np.int32)
     act.fill_(0)
-    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), None, to_dev(W13), to_dev(off), P, H, I, 1, act)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I, 1,
+                                        act)
     h = to_host(act)
     assert np.all(h[150:] == 0)
     assert_gemm_close(h[:150], want[:150], "partial group")
@@ -120,10 +143,10 @@ def test_single_group_without_offsets_and_rows_outside_groups():
 def test_gemm_refusals_and_empty():
     act = empty((4, 64), torch.bfloat16)
     with pytest.raises(m.MoeError) as ei:
-        m.moe_grouped_gemm_gateup_silu_bf16(act, None, act, None, 4, 64, 60, 1, act)
+        m.moe_grouped_gemm_gateup_silu_bf16(act, 4, None, 1, act, None, 4, 64, 60, 1, act)
     assert ei.value.code == m.ERR_ALIGN
     with pytest.raises(m.MoeError) as ei:
-        m.moe_grouped_gemm_gateup_silu_bf16(act, None, act, None, 4, 64, 32, 2, act)
+        m.moe_grouped_gemm_gateup_silu_bf16(act, 4, None, 1, act, None, 4, 64, 32, 2, act)
     assert ei.value.code == m.ERR_ARG
     before = launches()
     assert m.moe_grouped_gemm_down_bf16(act, act, None, None, None, 0, 64, 64, 1, act) == 0

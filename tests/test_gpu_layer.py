@@ -101,12 +101,12 @@ def _stagewise(cfg, n_tok_sample, n_row_sample):
         [0, P - 1], rng.choice(P, min(P, n_row_sample), replace=False),
         off[1:-1][off[1:-1] < P],            # first row of every expert (tile starts)
     ])).astype(np.int32)
-    xp = to_host(blk.x_perm)
-    assert np.array_equal(xp[rows], d["x"][sp[rows] // K])
-
-    # gate/up on sampled rows, fed the GPU's own x_perm
+    # gate/up on sampled rows, fed the same routed rows of x the GPU used
     act = to_host(blk.act)
-    want_act = O.gateup_silu(xp, d["w13"], off, P=P, H=H, I=I, G=E, rows=rows)
+    if blk.x_perm is not None:
+        assert np.array_equal(to_host(blk.x_perm)[rows], d["x"][sp[rows] // K])
+    want_act = O.gateup_silu(d["x"], d["w13"], off, P=P, H=H, I=I, G=E, rows=rows,
+                             a_row_gather=(sp // K).astype(np.int32))
     assert_gemm_close(act[rows], want_act[rows], "gate/up rows")
 
     # down on sampled rows, fed the GPU's own act
@@ -164,6 +164,19 @@ def test_prefill_zipf_layer_stagewise():
 @pytest.mark.slow
 def test_large_shared_layer_stagewise():
     _stagewise(W.LARGE, 32, 96)
+
+
+def test_materialised_x_perm_path_matches_gather_path():
+    cfg = W.DECODE
+    d = W.layer_inputs(cfg)
+    x = to_dev(d["x"])
+    a = to_host(MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                         gather=True).forward(x))
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda", gather=False)
+    b = to_host(blk.forward(x))
+    assert np.array_equal(a, b)
+    sp = to_host(blk.sorted_pair)
+    assert np.array_equal(to_host(blk.x_perm), d["x"][sp // cfg.K])
 
 
 def test_graph_replay_matches_eager():
