@@ -13,6 +13,8 @@
 //   warps 2-5   epilogue: tcgen05.ld of one accumulator row per thread, the
 //               fused op (bf16 narrowing + SiLU-mul, or routing weight +
 //               scatter, or bias + f32 store) and 16-byte stores
+//   warps 6-9   (gathered A only) cp.async copies of the routed rows of x into
+//               the swizzled A stage, so no permuted copy of x is needed
 // The tile schedule is built on the device from the group offsets (the
 // routing histogram): every CTA scans ceil(rows_g / 128) * n_tiles over the
 // groups in shared memory and walks tiles blockIdx.x, blockIdx.x + gridDim.x,
@@ -36,7 +38,8 @@ namespace gemm {
 constexpr int BM = 128;           // rows per tile (MMA M)
 constexpr int BK = 64;            // bf16 per 128-byte swizzled row: K per stage
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;        // producer, MMA, 4 epilogue warps
+constexpr int kThreadsGather = 320;  // + 4 warps that gather A rows
 constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK * 2;
 // bytes of the 227 KB per-block shared memory left for the stage ring after the
@@ -54,7 +57,9 @@ struct Params {
   int G;                         // groups
   int b_rows_per_group;          // rows of the 2-D view of B per group
   int half_off;                  // gate/up: row offset of the up half inside a group
-  const int32_t* row_gather;     // gate/up: A row of product row r is row_gather[r] / gather_div
+  const uint16_t* a;             // gathered A: row-major [a_rows, Kdim] bf16
+  int a_rows;
+  const int32_t* row_gather;     // gathered A: product row r reads row row_gather[r] / gather_div
   int gather_div;
   void* out;
   const float* pair_weight;      // down: [P] by destination row, or null
@@ -135,11 +140,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(f32_to_bf16_bits(hi)) << 16);
 }
 
-template <int kN, int kEpi>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kN, int kEpi, bool kGatherA>
+__global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
   constexpr int kStages = stages_for<kN>();
+  constexpr int kNThreads = kGatherA ? kThreadsGather : kThreads;
+  // gathered A: each row-thread keeps kDepth stages of copies in flight before
+  // it must retire the oldest one (kDepth < kStages keeps the ring deadlock-free)
+  constexpr int kDepth = kStages - 1;
   using S = Smem<kN, kStages>;
   // B arrives in boxes of kBoxB rows (the tensor map's box height)
   constexpr int kBoxB = (kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128);
@@ -147,7 +156,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;
   constexpr int kTmemCols = 2 * kN;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, kN);
-  constexpr uint32_t kStageTx = A_BYTES + S::B_BYTES;
+  constexpr uint32_t kStageTx = (kGatherA ? 0 : A_BYTES) + S::B_BYTES;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -156,7 +165,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC + 4);
-  int* scan_tmp = reinterpret_cast<int*>(smem + S::MISC + 8);   // 8 ints
+  int* scan_tmp = reinterpret_cast<int*>(smem + S::MISC + 8);   // 10 ints
   int* tile_start = reinterpret_cast<int*>(smem + S::TILE_START);
   int* goff = reinterpret_cast<int*>(smem + S::GOFF);
 
@@ -172,7 +181,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(bar_full(s), 1);
+      ptx::mbar_init(bar_full(s), kGatherA ? 1 + BM : 1);
       ptx::mbar_init(bar_empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -194,11 +203,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   // ---- device-side tile schedule from the group offsets
   const int G = p.G;
-  for (int g = threadIdx.x; g <= G; g += kThreads)
+  for (int g = threadIdx.x; g <= G; g += kNThreads)
     goff[g] = p.group_offsets ? __ldg(p.group_offsets + g) : (g == 0 ? 0 : p.P);
   __syncthreads();
   const int n_tiles = (p.N + kBnOut - 1) / kBnOut;
-  const int chunk = (G + kThreads - 1) / kThreads;
+  const int chunk = (G + kNThreads - 1) / kNThreads;
   const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
   const int g_hi = min(G, g_lo + chunk);
   int local = 0;
@@ -215,7 +224,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (lane == 31) scan_tmp[warp] = incl;
   __syncthreads();
   int warp_base = 0, total = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < kNThreads / 32; ++w) {
     int v = scan_tmp[w];
     if (w < warp) warp_base += v;
     total += v;
@@ -233,61 +242,57 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
 
-  if (warp == 0 && p.row_gather != nullptr) {
-    // ------------------------------------------------------------ TMA producer, gathered A
-    // The whole warp loads: lane l fetches rows 4l..4l+3 of the A tile with one
-    // tile::gather4 per stage (row indices read once per tile); lane 0 owns the
-    // barrier and the B boxes.
+  if (kGatherA && warp >= 6) {
+    // ------------------------------------------------------------ A-row gatherers
+    // Thread i owns row i of every A tile: row_gather[row0 + i] / gather_div
+    // picks the source row, and each stage copies its 64 columns (8 x 16 B)
+    // with cp.async into the 128-byte-swizzled layout a TMA SWIZZLE_128B box
+    // would produce (16-byte chunk c of row i lands at chunk c ^ (i % 8)).
+    // Indices outside [0, a_rows) read zeros, like a TMA out-of-bounds box.
+    const int i = static_cast<int>(threadIdx.x) - kThreads;
     int stage = 0;
     uint32_t phase = 0;
-    int issued = 0;
+    int pending = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
-      const int brow = t.g * p.b_rows_per_group + t.n0;
-      int src[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = min(t.row0 + 4 * lane + q, p.P - 1);  // rows past the group are masked later
-        src[q] = __ldg(p.row_gather + r) / p.gather_div;
-      }
+      const int r = min(t.row0 + i, p.P - 1);  // rows past the group are masked later
+      const int srow = __ldg(p.row_gather + r) / p.gather_div;
+      const bool in = srow >= 0 && srow < p.a_rows;
+      const uint16_t* src = p.a + static_cast<size_t>(in ? srow : 0) * p.Kdim;
       for (int kb = 0; kb < nk; ++kb) {
-        int go = 1;
-        if (lane == 0) go = wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status) ? 1 : 0;
-        go = __shfl_sync(0xffffffffu, go, 0);
-        if (!go) { ok = false; break; }
-        const uint32_t fb = bar_full(stage);
-        const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
-        const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kStageTx);
-        __syncwarp();
-        ptx::tma_gather4(sa + lane * 4 * 128, &tmA, kb * BK, src[0], src[1], src[2], src[3], fb);
-        if (lane == 0) {
-          if (kEpi == EPI_GATEUP) {
-            ptx::tma_load_2d(sb, &tmB, kb * BK, brow, fb);
-            ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow + p.half_off, fb);
-          } else {
+        if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t dst = sbase + S::STAGE_A + stage * A_BYTES + i * 128;
 #pragma unroll
-            for (int h = 0; h < kN / kBoxB; ++h)
-              ptx::tma_load_2d(sb + h * kBoxBytes, &tmB, kb * BK, brow + h * kBoxB, fb);
-          }
+        for (int c = 0; c < 8; ++c) {
+          const int col = kb * BK + c * 8;
+          const bool live = in && col < p.Kdim;    // Kdim % 8 == 0: a chunk is all in or out
+          ptx::cp_async_16(dst + ((c ^ (i & 7)) << 4), src + (live ? col : 0), live ? 16u : 0u);
         }
-        ++issued;
+        ptx::cp_async_commit();
+        if (++pending == kDepth) {
+          ptx::cp_async_wait<kDepth - 1>();
+          ptx::fence_proxy_async_smem();
+          int old = stage - (kDepth - 1);
+          if (old < 0) old += kStages;
+          ptx::mbar_arrive(bar_full(old));
+          --pending;
+        }
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok && lane == 0) {
-      int s = stage;
-      uint32_t ph = phase;
-      for (int i = 0; i < min(issued, kStages); ++i) {
-        if (--s < 0) { s = kStages - 1; ph ^= 1u; }
-        const uint64_t t0 = ptx::globaltimer_ns();
-        while (!ptx::mbar_try_wait(bar_full(s), ph) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
-        }
+    ptx::cp_async_wait<0>();
+    if (ok) {
+      ptx::fence_proxy_async_smem();
+      for (int q = pending; q > 0; --q) {
+        int old = stage - q;
+        if (old < 0) old += kStages;
+        ptx::mbar_arrive(bar_full(old));
       }
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // (A and B boxes; only B when the gatherer warps fill A)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -302,7 +307,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::mbar_arrive_expect_tx(fb, kStageTx);
           const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
           const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
-          ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0, fb);
+          if (!kGatherA) ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0, fb);
           if (kEpi == EPI_GATEUP) {
             ptx::tma_load_2d(sb, &tmB, kb * BK, brow, fb);
             ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow + p.half_off, fb);
@@ -364,7 +369,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int r_in_tile = q * 32 + lane;
@@ -534,10 +539,10 @@ int num_sms() {
   return n;
 }
 
-template <int kN, int kEpi>
+template <int kN, int kEpi, bool kGatherA = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<kN, kEpi>;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA>;
   const int smem = Smem<kN, stages_for<kN>()>::ALLOC;
   static int configured_dev[64] = {};
   int dev = 0;
@@ -556,7 +561,8 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
   DeviceDiag diag = device_diag();
   p.status = diag.status;
   p.launches = diag.launches;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(ta, tb, p);
+  kern<<<static_cast<unsigned>(grid), kGatherA ? kThreadsGather : kThreads, smem, stream>>>(ta, tb,
+                                                                                             p);
   return check_launch(op);
 }
 
@@ -631,15 +637,14 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
     return set_error(MOE_ERR_ARG, "%s: gathering needs a_rows >= 1 and gather_div >= 1", op);
   if (P == 0) return MOE_OK;
   CUtensorMap ta, tb;
-  if (a_row_gather) {
-    // one-row boxes for tile::gather4
-    if ((rc = make_tmap(&ta, a_bf16, a_rows, H, 1, op, "a (gathered)")) != MOE_OK) return rc;
-  } else if ((rc = make_tmap(&ta, a_bf16, P, H, BM, op, "a")) != MOE_OK) {
-    return rc;
-  }
   if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, 128, op, "w13")) !=
       MOE_OK)
     return rc;
+  if (a_row_gather) {
+    ta = tb;  // unused: the gatherer warps read A rows directly
+  } else if ((rc = make_tmap(&ta, a_bf16, P, H, BM, op, "a")) != MOE_OK) {
+    return rc;
+  }
   Params p{};
   p.group_offsets = group_offsets;
   p.P = P;
@@ -648,10 +653,15 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   p.G = G;
   p.b_rows_per_group = 2 * I;
   p.half_off = I;
+  p.a = static_cast<const uint16_t*>(a_bf16);
+  p.a_rows = a_rows;
   p.row_gather = a_row_gather;
   p.gather_div = gather_div;
   p.out = act_bf16;
   p.kid = MOE_KID_GEMM_GATEUP;
+  if (a_row_gather)
+    return launch<256, EPI_GATEUP, true>(op, ta, tb, p, tile_bound(P, G, I, 128),
+                                         static_cast<cudaStream_t>(stream));
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128),
                                  static_cast<cudaStream_t>(stream));
 }

@@ -1,6 +1,6 @@
 // sm100_ptx.cuh -- thin inline-PTX wrappers for the Blackwell (sm_100a /
 // sm_103a) data-movement and tensor-core instructions the GEMMs use:
-// mbarrier, TMA tiled loads (cp.async.bulk.tensor), tcgen05 TMEM allocation,
+// mbarrier, TMA tiled loads (cp.async.bulk.tensor), cp.async, tcgen05 TMEM allocation,
 // MMA, commit and loads.  Written from the PTX ISA's instruction descriptions.
 #pragma once
 
@@ -65,15 +65,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// 4 rows (y0..y3) x one box of columns starting at x, into 4 consecutive
-// 128-byte rows of shared memory (tensor map box: 64 bf16 wide, 1 row high)
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int x, int y0,
-                                            int y1, int y2, int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes instead
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// orders this thread's generic-proxy shared-memory writes before later
+// async-proxy accesses (the tensor core reads its operands through the async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
