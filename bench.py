@@ -140,9 +140,9 @@ class ClockSampler:
 
 
 def dist_setup(args):
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from mixture_experts_ffn_renorm_gb300 import dp
+
+    ws, rank, local = dp.world()
     if ws > 1:
         import torch.distributed as dist
 
@@ -152,21 +152,15 @@ def dist_setup(args):
 
 
 def barrier(ws):
-    if ws > 1:
-        import torch.distributed as dist
+    from mixture_experts_ffn_renorm_gb300 import dp
 
-        dist.barrier()
+    dp.barrier(ws)
 
 
 def max_over_ranks(v, ws, device):
-    if ws == 1:
-        return v
-    import torch
-    import torch.distributed as dist
+    from mixture_experts_ffn_renorm_gb300 import dp
 
-    t = torch.tensor([v], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return dp.max_over_ranks(v, ws, device)
 
 
 def layer_config(name):
@@ -261,6 +255,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     cfg = layer_config(args.config)
     d = W.layer_inputs(cfg)
+    if rank > 0:  # each replica gets its own tokens of the global batch
+        d["x"] = W.rank_tokens(cfg, rank)
     blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
                    I_shared=cfg.I_shared)
     x_host = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
@@ -299,7 +295,9 @@ def run_ours(args):
     else:  # the L2 flush between steps is not part of a step
         step_ms = sum(mk[0][1].elapsed_time(mk[-1][1]) for mk in step_marks) / args.steps
     ms = max_over_ranks(step_ms, ws, dev)
-    value = ws * cfg.T / (ms / 1000.0)
+    from mixture_experts_ffn_renorm_gb300 import dp
+
+    value = dp.aggregate_tokens_per_s(cfg.T, ws, ms)
 
     stage_ms = {}
     for marks in step_marks:

@@ -36,6 +36,7 @@ CHUNK = 1 << 22
 # stream tags: one per tensor, fixed forever so that inputs never change
 TAG_X, TAG_WR, TAG_W13, TAG_W2, TAG_WSG, TAG_W13S, TAG_W2S, TAG_RANK = 1, 2, 3, 4, 5, 6, 7, 8
 TAG_EO, TAG_LOGITS, TAG_SD, TAG_GL = 11, 12, 13, 14
+TAG_X_RANK = 1000  # + rank: the tokens of data-parallel replica `rank`
 
 
 @dataclasses.dataclass(frozen=True)
@@ -173,6 +174,13 @@ def layer_inputs(cfg: LayerConfig, with_weights: bool = True) -> dict:
         d["w13_shared"] = normal_bf16(s, TAG_W13S, (1, 2 * Is, H), 0.02)
         d["w2_shared"] = normal_bf16(s, TAG_W2S, (1, H, Is), 0.02)
     return d
+
+
+def rank_tokens(cfg: LayerConfig, rank: int) -> np.ndarray:
+    """Tokens of data-parallel replica `rank` (rank 0 has the workload's own x)."""
+    if rank == 0:
+        return normal_bf16(cfg.seed, TAG_X, (cfg.T, cfg.H), 1.0)
+    return normal_bf16(cfg.seed, TAG_X_RANK + rank, (cfg.T, cfg.H), 1.0)
 
 
 def combine_inputs(cfg: CombineConfig) -> dict:
