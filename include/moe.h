@@ -217,6 +217,17 @@ int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
                                void* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 size_t moe_grouped_gemm_workspace_size(int P, int H, int I, int G);
 
+/* moe_set_gemm_pairing -- tile shape of the two grouped GEMMs above (not of
+ * the gathered-A gate/up, which always runs single-CTA tiles).
+ *   on != 0: CTA pairs (2-SM tcgen05.mma.cta_group::2, 256-row tiles; each SM
+ *            of the pair stages 128 A rows and half of the weight tile)
+ *   on == 0 (default): one CTA per 128-row tile (less padding on skewed
+ *            expert loads, where most groups hold well under 256 rows)
+ * Results are identical up to f32 accumulation order.  Process-wide, takes
+ * effect at the next launch; returns the previous setting.  Not for use while
+ * another thread is launching these GEMMs. */
+int moe_set_gemm_pairing(int on);
+
 /* ------------------------------------------------------------------------
  * moe_combine -- kMoeCombine of [PR509].  Per output element, sequentially:
  *   acc = +0.0f

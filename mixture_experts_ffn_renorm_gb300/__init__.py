@@ -34,6 +34,7 @@ EXPORTS = (
     "moe_grouped_gemm_gateup_silu_bf16",
     "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
+    "moe_set_gemm_pairing",
 )
 
 
@@ -63,6 +64,7 @@ _SIGS = {
                                            _P], _I),
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
+    "moe_set_gemm_pairing": ([_I], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
     "moe_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I, _P], _I),
     "shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I, _P], _I),
@@ -180,6 +182,11 @@ def moe_grouped_gemm_down_bf16(act, w2, group_offsets, pair_weight, row_to_pair,
 
 def moe_grouped_gemm_workspace_size(P, H, I, G) -> int:
     return lib().moe_grouped_gemm_workspace_size(P, H, I, G)
+
+
+def moe_set_gemm_pairing(on: bool) -> bool:
+    """CTA-pair (2-SM) tiles for the grouped GEMMs on/off; returns the previous setting."""
+    return bool(lib().moe_set_gemm_pairing(1 if on else 0))
 
 
 def moe_combine(expert_out, eo_dtype, w, shared, sh_dtype, routed_scale, T, K, H, out, out_dtype,

@@ -27,6 +27,7 @@
 // the TMEM is freed before the CTA exits.
 #include <stdio.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe_common.cuh"
@@ -70,16 +71,15 @@ struct Params {
   int kid;
 };
 
-// Stage ring depth: as many stages as fit the budget, at most 8.
-template <int kN>
-__host__ __device__ constexpr int stages_for() {
-  return kSmemBudget / (A_BYTES + kN * BK * 2) > 8 ? 8 : kSmemBudget / (A_BYTES + kN * BK * 2);
+// Stage ring depth: as many stages of `stage_bytes` as fit the budget, at most 8.
+__host__ __device__ constexpr int stages_for_bytes(int stage_bytes) {
+  return kSmemBudget / stage_bytes > 8 ? 8 : kSmemBudget / stage_bytes;
 }
 
-template <int kN, int kStages>
+template <int kStages, int kBBytes>
 struct Smem {
   static_assert(kStages >= 2, "stage ring too shallow");
-  static constexpr int B_BYTES = kN * BK * 2;
+  static constexpr int B_BYTES = kBBytes;
   static constexpr int STAGE_A = 0;
   static constexpr int STAGE_B = kStages * A_BYTES;
   static constexpr int BARS = STAGE_B + kStages * B_BYTES;
@@ -92,12 +92,30 @@ struct Smem {
   static constexpr int ALLOC = BYTES + 1024;              // slack to align the base to 1024
 };
 
+// Compile-time shape of one kernel instantiation.
+//   kN      MMA N (accumulator columns per tile)
+//   kPair   CTA pair (cta_group::2): M = 256 per tile, each CTA holds 128 A rows
+//           and half of B, and one thread of the even CTA issues the MMAs
+template <int kN, int kEpi, bool kGatherA, bool kPair>
+struct Cfg {
+  static constexpr int kTileM = kPair ? 2 * BM : BM;              // product rows per tile
+  static constexpr int kBRowsCta = kPair ? kN / 2 : kN;           // B rows held per CTA
+  static constexpr int kBBytes = kBRowsCta * BK * 2;
+  static constexpr int kStages = stages_for_bytes(A_BYTES + kBBytes);
+  // B boxes: gate/up loads its gate and up halves separately (per CTA when paired)
+  static constexpr int kBoxB = kPair ? kBRowsCta
+                                     : ((kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128));
+  static constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;  // output columns per tile
+  static constexpr int kThreadsT = kGatherA ? kThreadsGather : kThreads;
+  using S = Smem<kStages, kBBytes>;
+};
+
 struct Tile {
   int g, row0, row_end, n0;
 };
 
 __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, const int* goff,
-                                            int G, int n_tiles, int bn_out) {
+                                            int G, int n_tiles, int bn_out, int tile_m) {
   int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -107,27 +125,41 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, con
   int m = local / n_tiles, n = local - m * n_tiles;
   Tile t;
   t.g = lo;
-  t.row0 = goff[lo] + m * BM;
+  t.row0 = goff[lo] + m * tile_m;
   t.row_end = goff[lo + 1];
   t.n0 = n * bn_out;
   return t;
 }
 
-// Bounded mbarrier wait.  Returns false when this CTA is aborting.
+// Bounded mbarrier wait.  Returns false when this CTA is aborting.  kCluster:
+// acquire at cluster scope (the barrier is arrived on by the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned int* status) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    if (!kCluster) return ptx::mbar_try_wait(bar, parity);
+    if (!ptx::mbar_try_wait_cluster(bar, parity)) return false;
+    ptx::fence_acquire_cluster();
+    return true;
+  };
+  if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (probe()) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
       if (status) atomicOr(status, static_cast<unsigned int>(MOE_STATUS_TIMEOUT));
       *abort_flag = 1;
       return false;
     }
+  }
+}
+
+__device__ __forceinline__ void spin_bounded(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
   }
 }
 
@@ -140,22 +172,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(f32_to_bf16_bits(hi)) << 16);
 }
 
-template <int kN, int kEpi, bool kGatherA>
-__global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
+template <int kN, int kEpi, bool kGatherA, bool kPair>
+__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair>::kThreadsT, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
-  constexpr int kStages = stages_for<kN>();
-  constexpr int kNThreads = kGatherA ? kThreadsGather : kThreads;
+  using C = Cfg<kN, kEpi, kGatherA, kPair>;
+  using S = typename C::S;
+  constexpr int kStages = C::kStages;
+  constexpr int kNThreads = C::kThreadsT;
+  constexpr int kTileM = C::kTileM;
+  constexpr int kBnOut = C::kBnOut;
+  constexpr int kBoxB = C::kBoxB;
+  constexpr int kBoxBytes = kBoxB * BK * 2;
   // gathered A: each row-thread keeps kDepth stages of copies in flight before
   // it must retire the oldest one (kDepth < kStages keeps the ring deadlock-free)
   constexpr int kDepth = kStages - 1;
-  using S = Smem<kN, kStages>;
-  // B arrives in boxes of kBoxB rows (the tensor map's box height)
-  constexpr int kBoxB = (kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128);
-  constexpr int kBoxBytes = kBoxB * BK * 2;
-  constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;
   constexpr int kTmemCols = 2 * kN;
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, kN);
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kN);
   constexpr uint32_t kStageTx = (kGatherA ? 0 : A_BYTES) + S::B_BYTES;
 
   extern __shared__ uint8_t smem_raw[];
@@ -171,6 +204,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // pair: rank 0 (even CTA) issues the MMAs and owns the stage barriers; both load
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto bar_full = [&](int s) { return ptx::smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return ptx::smem_u32(bars + kStages + s); };
   auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + a); };
@@ -186,7 +224,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_tfull(a), 1);
-      ptx::mbar_init(bar_tempty(a), 128);
+      ptx::mbar_init(bar_tempty(a), kPair ? 2 * BM : BM);
     }
     ptx::mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -197,8 +235,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    if (kPair) {
+      ptx::tmem_alloc2(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish2();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
 
   // ---- device-side tile schedule from the group offsets
@@ -213,7 +256,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   int local = 0;
   for (int g = g_lo; g < g_hi; ++g) {
     int rows = goff[g + 1] - goff[g];
-    local += rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+    local += rows > 0 ? ((rows + kTileM - 1) / kTileM) * n_tiles : 0;
   }
   int incl = local;
 #pragma unroll
@@ -233,18 +276,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   for (int g = g_lo; g < g_hi; ++g) {
     tile_start[g] = run;
     int rows = goff[g + 1] - goff[g];
-    run += rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+    run += rows > 0 ? ((rows + kTileM - 1) / kTileM) * n_tiles : 0;
   }
   if (threadIdx.x == 0) tile_start[G] = total;
   ptx::tc_fence_before();
   __syncthreads();
+  if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
+  const int row_off = static_cast<int>(rank) * BM;  // this CTA's A rows inside a tile
 
   if (kGatherA && warp >= 6) {
     // ------------------------------------------------------------ A-row gatherers
-    // Thread i owns row i of every A tile: row_gather[row0 + i] / gather_div
+    // Thread i owns row i of this CTA's A tile: row_gather[row] / gather_div
     // picks the source row, and each stage copies its 64 columns (8 x 16 B)
     // with cp.async into the 128-byte-swizzled layout a TMA SWIZZLE_128B box
     // would produce (16-byte chunk c of row i lands at chunk c ^ (i % 8)).
@@ -254,9 +299,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     int pending = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
-      const int r = min(t.row0 + i, p.P - 1);  // rows past the group are masked later
+    for (int tile = unit; ok && tile < total; tile += n_units) {
+      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
+      const int r = min(t.row0 + row_off + i, p.P - 1);  // rows past the group are masked later
       const int srow = __ldg(p.row_gather + r) / p.gather_div;
       const bool in = srow >= 0 && srow < p.a_rows;
       const uint16_t* src = p.a + static_cast<size_t>(in ? srow : 0) * p.Kdim;
@@ -292,57 +337,81 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // (A and B boxes; only B when the gatherer warps fill A)
+    // A box (unless gathered) and B boxes of this CTA, completion on its own barrier
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
-        const int brow = t.g * p.b_rows_per_group + t.n0;
+      for (int tile = unit; ok && tile < total; tile += n_units) {
+        Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
+        // B rows of this CTA: unpaired, the whole tile (gate/up: gate half, then
+        // up half); paired, rank 0 holds the first half of the N columns
+        // (gate rows) and rank 1 the second (up rows)
+        int brow0, brow1;
+        if (kPair) {
+          brow0 = t.g * p.b_rows_per_group + t.n0 +
+                  static_cast<int>(rank) * ((kEpi == EPI_GATEUP) ? p.half_off : kN / 2);
+          brow1 = brow0;
+        } else {
+          brow0 = t.g * p.b_rows_per_group + t.n0;
+          brow1 = brow0 + p.half_off;
+        }
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          const uint32_t fb = bar_full(stage);
-          ptx::mbar_arrive_expect_tx(fb, kStageTx);
           const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
           const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
-          if (!kGatherA) ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0, fb);
+          if (kPair) {
+            // both CTAs' boxes are counted on the even CTA's barrier, which
+            // expects the bytes of both halves
+            const uint32_t fb = ptx::mapa_shared(bar_full(stage), 0);
+            if (leader) ptx::mbar_arrive_expect_tx(bar_full(stage), 2 * kStageTx);
+            ptx::tma_load_2d_pair(sa, &tmA, kb * BK, t.row0 + row_off, fb);
+            ptx::tma_load_2d_pair(sb, &tmB, kb * BK, brow0, fb);
+            ++issued;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
+          const uint32_t fb = bar_full(stage);
+          ptx::mbar_arrive_expect_tx(fb, kStageTx);
+          if (!kGatherA) ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0 + row_off, fb);
           if (kEpi == EPI_GATEUP) {
-            ptx::tma_load_2d(sb, &tmB, kb * BK, brow, fb);
-            ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow + p.half_off, fb);
+            ptx::tma_load_2d(sb, &tmB, kb * BK, brow0, fb);
+            ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow1, fb);
           } else {
 #pragma unroll
             for (int h = 0; h < kN / kBoxB; ++h)
-              ptx::tma_load_2d(sb + h * kBoxBytes, &tmB, kb * BK, brow + h * kBoxB, fb);
+              ptx::tma_load_2d(sb + h * kBoxBytes, &tmB, kb * BK, brow0 + h * kBoxB, fb);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok && (!kPair || leader)) {
         // drain: the last min(issued, kStages) copies may still be landing
         int s = stage;
         uint32_t ph = phase;
         for (int i = 0; i < min(issued, kStages); ++i) {
           if (--s < 0) { s = kStages - 1; ph ^= 1u; }
-          const uint64_t t0 = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(bar_full(s), ph) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
+          spin_bounded(bar_full(s), ph);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (paired: the even CTA's thread issues for both; the odd CTA's warp 1 idles)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true, any = false;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
+      for (int tile = unit; ok && tile < total; tile += n_units, ++it) {
         const int acc = it & 1;
         const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
-        if (!wait_bar(bar_tempty(acc), aphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_bar<kPair>(bar_tempty(acc), aphase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kN);
         for (int kb = 0; kb < nk; ++kb) {
@@ -353,29 +422,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
-            ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            if (kPair)
+              ptx::mma_bf16_pair(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
           any = true;
-          ptx::mma_commit(bar_empty(stage));
+          if (kPair) ptx::mma_commit_pair(bar_empty(stage), 3);
+          else ptx::mma_commit(bar_empty(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        ptx::mma_commit(bar_tfull(acc));
+        if (kPair) ptx::mma_commit_pair(bar_tfull(acc), 3);
+        else ptx::mma_commit(bar_tfull(acc));
       }
       if (!ok && any) {
-        ptx::mma_commit(bar_drain);
-        const uint64_t t0 = ptx::globaltimer_ns();
-        while (!ptx::mbar_try_wait(bar_drain, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
-        }
+        if (kPair) ptx::mma_commit_pair(bar_drain, 1);
+        else ptx::mma_commit(bar_drain);
+        spin_bounded(bar_drain, 0);
       }
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int r_in_tile = q * 32 + lane;
+    const int r_in_tile = row_off + q * 32 + lane;
+    const uint32_t tempty_leader =
+        kPair ? ptx::mapa_shared(bar_tempty(0), 0) : 0u;  // + 8 * acc for buffer acc
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut);
+    for (int tile = unit; tile < total; tile += n_units, ++it) {
+      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
       const int acc = it & 1;
       const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
       if (!wait_bar(bar_tfull(acc), aphase, abort_flag, p.status)) break;
@@ -465,10 +540,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             float* dst = out + static_cast<size_t>(row) * p.N + col;
             if ((p.N & 3) == 0) {
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                if (col + 4 * q < p.N)
-                  reinterpret_cast<float4*>(dst)[q] =
-                      make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              for (int q4 = 0; q4 < 8; ++q4)
+                if (col + 4 * q4 < p.N)
+                  reinterpret_cast<float4*>(dst)[q4] =
+                      make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -478,14 +553,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_tempty(acc));
+      if (kPair && !leader) ptx::mbar_arrive_remote(tempty_leader + 8u * acc);
+      else ptx::mbar_arrive(bar_tempty(acc));
     }
   }
 
   __syncthreads();
+  if (kPair) ptx::cluster_sync();  // the peer may still read this CTA's smem or TMEM until here
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    if (kPair) ptx::tmem_dealloc2(tmem_base, kTmemCols);
+    else ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -539,11 +617,14 @@ int num_sms() {
   return n;
 }
 
-template <int kN, int kEpi, bool kGatherA = false>
+// tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
+// grid is that many CTAs (pairs when paired), capped at the SM count
+template <int kN, int kEpi, bool kGatherA = false, bool kPair = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA>;
-  const int smem = Smem<kN, stages_for<kN>()>::ALLOC;
+  using C = Cfg<kN, kEpi, kGatherA, kPair>;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair>;
+  const int smem = C::S::ALLOC;
   static int configured_dev[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -554,15 +635,46 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
                        cudaGetErrorString(cudaGetLastError()));
     configured_dev[dev] = 1;
   }
-  long long grid = tile_bound;
-  const int sms = num_sms();
-  if (grid > sms) grid = sms;
-  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::kThreadsT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent grid: as many CTAs (pairs) as can be resident at once.  A pair
+  // must sit in one GPC, so with an odd SM count per GPC fewer than SMs / 2
+  // pairs fit; launching more would leave a second, mostly idle wave.
+  static int max_units_dev[64] = {};
+  int max_units = (dev >= 0 && dev < 64) ? max_units_dev[dev] : 0;
+  if (max_units <= 0) {
+    max_units = kPair ? num_sms() / 2 : num_sms();
+    if (kPair) {
+      int clusters = 0;
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * max_units), 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0)
+        max_units = clusters < max_units ? clusters : max_units;
+      else
+        cudaGetLastError();
+    }
+    if (dev >= 0 && dev < 64) max_units_dev[dev] = max_units;
+  }
+  long long units = tile_bound;
+  if (units > max_units) units = max_units;
+  if (units < 1) units = 1;
   DeviceDiag diag = device_diag();
   p.status = diag.status;
   p.launches = diag.launches;
-  kern<<<static_cast<unsigned>(grid), kGatherA ? kThreadsGather : kThreads, smem, stream>>>(ta, tb,
-                                                                                             p);
+  cfg.gridDim = dim3(static_cast<unsigned>(kPair ? 2 * units : units), 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(MOE_ERR_CUDA, "%s: kernel launch failed: %s", op, cudaGetErrorString(e));
+  }
   return check_launch(op);
 }
 
@@ -580,10 +692,13 @@ int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, c
   return MOE_OK;
 }
 
-long long tile_bound(int P, int G, int N, int bn_out) {
-  long long mt = (P + BM - 1) / BM + (G < P ? G : P);
+long long tile_bound(int P, int G, int N, int bn_out, int tile_m = BM) {
+  long long mt = (P + tile_m - 1) / tile_m + (G < P ? G : P);
   return mt * ((N + bn_out - 1) / bn_out);
 }
+
+// CTA-pair tiles for the grouped GEMMs (process-wide; see moe_set_gemm_pairing)
+std::atomic<int> g_pairing{0};
 
 }  // namespace gemm
 
@@ -618,6 +733,11 @@ using namespace moe;
 using namespace moe::gemm;
 
 extern "C" size_t moe_grouped_gemm_workspace_size(int, int, int, int) { return 0; }
+
+extern "C" int moe_set_gemm_pairing(int on) {
+  clear_error();
+  return g_pairing.exchange(on ? 1 : 0);
+}
 
 extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
                                                  const int32_t* a_row_gather, int gather_div,
@@ -659,11 +779,12 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   p.gather_div = gather_div;
   p.out = act_bf16;
   p.kid = MOE_KID_GEMM_GATEUP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a_row_gather)
-    return launch<256, EPI_GATEUP, true>(op, ta, tb, p, tile_bound(P, G, I, 128),
-                                         static_cast<cudaStream_t>(stream));
-  return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128),
-                                 static_cast<cudaStream_t>(stream));
+    return launch<256, EPI_GATEUP, true>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
+  if (g_pairing.load(std::memory_order_relaxed))
+    return launch<256, EPI_GATEUP, false, true>(op, ta, tb, p, tile_bound(P, G, I, 128, 2 * BM), s);
+  return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
 extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
@@ -696,6 +817,8 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   p.pair_weight = pair_weight;
   p.row_to_pair = row_to_pair;
   p.kid = MOE_KID_GEMM_DOWN;
-  return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256),
-                               static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g_pairing.load(std::memory_order_relaxed))
+    return launch<256, EPI_DOWN, false, true>(op, ta, tb, p, tile_bound(P, G, H, 256, 2 * BM), s);
+  return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
 }

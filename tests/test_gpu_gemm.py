@@ -28,6 +28,14 @@ def _lib():
     assert m.moe_device_status() == 0
 
 
+@pytest.fixture(params=[True, False], ids=["pair", "single"])
+def pairing(request):
+    """Both tilings of the grouped GEMMs: CTA pairs (2-SM, 256-row tiles) and single CTAs."""
+    prev = m.moe_set_gemm_pairing(request.param)
+    yield request.param
+    m.moe_set_gemm_pairing(prev)
+
+
 def _case(sizes, H, I, seed):
     rng = np.random.default_rng(seed)
     G = len(sizes)
@@ -50,8 +58,8 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("sizes,H,I", SHAPES)
-def test_gateup_silu(sizes, H, I):
+@pytest.mark.parametrize("sizes,H,I", SHAPES + [([300, 0, 520], 2048, 768)])
+def test_gateup_silu(sizes, H, I, pairing):
     off, P, G, A, W13, _ = _case(sizes, H, I, sum(sizes) + H)
     want = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G)
     act = empty((P, I), torch.bfloat16)
@@ -85,8 +93,8 @@ def test_gateup_silu_gathered_rows(sizes, H, I, K):
     assert_gemm_close(to_host(act), want, "gathered gate/up")
 
 
-@pytest.mark.parametrize("sizes,H,I", SHAPES)
-def test_down_weight_scatter(sizes, H, I):
+@pytest.mark.parametrize("sizes,H,I", SHAPES + [([300, 0, 520], 2048, 768)])
+def test_down_weight_scatter(sizes, H, I, pairing):
     off, P, G, _, _, W2 = _case(sizes, H, I, sum(sizes) + I)
     rng = np.random.default_rng(1)
     act = W.to_bf16_bits(rng.standard_normal((P, I)).astype(np.float32))
@@ -105,7 +113,7 @@ def test_down_weight_scatter(sizes, H, I):
         assert_gemm_close(to_host(out), want, "down")
 
 
-def test_gateup_narrowing_is_visible_on_the_gpu():
+def test_gateup_narrowing_is_visible_on_the_gpu(pairing):
     # g = u = 1 + 2^-9 exactly: narrowing before the activation gives
     # bf16(silu(1) * 1) = 0x3F3B; without it the result would be 0x3F3C
     H, I = 64, 32
@@ -121,7 +129,7 @@ def test_gateup_narrowing_is_visible_on_the_gpu():
     assert np.all(to_host(act) == 0x3F3B)
 
 
-def test_single_group_without_offsets_and_rows_outside_groups():
+def test_single_group_without_offsets_and_rows_outside_groups(pairing):
     H, I, P = 128, 64, 200
     rng = np.random.default_rng(2)
     A = W.to_bf16_bits(rng.standard_normal((P, H)).astype(np.float32))

@@ -179,6 +179,27 @@ def test_materialised_x_perm_path_matches_gather_path():
     assert np.array_equal(to_host(blk.x_perm), d["x"][sp // cfg.K])
 
 
+def test_pair_and_single_cta_tiles_agree_on_prefill():
+    # the two GEMM tilings differ only in f32 accumulation order
+    cfg = W.PREFILL
+    d = W.layer_inputs(cfg)
+    blk = _block(cfg, d)
+    x = to_dev(d["x"])
+    prev = m.moe_set_gemm_pairing(True)
+    try:
+        a = to_host(blk.forward(x)).copy()
+        act_a = to_host(blk.act).copy()
+        m.moe_set_gemm_pairing(False)
+        b = to_host(blk.forward(x))
+        act_b = to_host(blk.act)
+    finally:
+        m.moe_set_gemm_pairing(prev)
+    nmse, _ = nmse_maxrel(bf16_to_f64(act_a), bf16_to_f64(act_b))
+    assert nmse <= 1e-6, nmse
+    nmse, _ = nmse_maxrel(bf16_to_f64(a), bf16_to_f64(b))
+    assert nmse <= 1e-6, nmse
+
+
 def test_graph_replay_matches_eager():
     cfg = W.DECODE
     d = W.layer_inputs(cfg)
