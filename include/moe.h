@@ -73,7 +73,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 2 */
+int moe_abi_version(void);  /* 3 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -258,18 +258,24 @@ int moe_combine(const void* expert_out, int eo_dtype, const float* w, const void
  *   acc = the routed sum of moe_combine (w optional), acc = acc * routed_scale
  *   out[t,c] = (acc + sv) rounded once to out_dtype
  * Bit-exact.  sd f32 or bf16; out f32 or bf16; gl f32 [T].
+ * workspace: NULL, or >= moe_gate_workspace_size(T) bytes.  With a workspace
+ * the T sigmoids are evaluated first by a small kernel and the stream reads
+ * them (faster: the sigmoid is a chain of double-precision operations); without
+ * one each block evaluates the sigmoids of its tokens itself.  Same bits.
  * ---------------------------------------------------------------------- */
 int moe_combine_gate(const void* expert_out, int eo_dtype, const float* w, const void* sd,
                      int sd_dtype, const float* gl, float routed_scale, int T, int K, int H,
-                     void* out, int out_dtype, void* stream);
+                     void* out, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * shared_expert_gate -- kSharedExpertGate of [PR509]:
  *   out[t,c] = sigmoid(gl[t]) * sd[t,c], one rounding to out_dtype.
- * Four dtype arms: sd f32/bf16 x out f32/bf16.  Bit-exact.
+ * Four dtype arms: sd f32/bf16 x out f32/bf16.  Bit-exact.  workspace as
+ * for moe_combine_gate (NULL allowed).
  * ---------------------------------------------------------------------- */
 int shared_expert_gate(const void* sd, int sd_dtype, const float* gl, int T, int H, void* out,
-                       int out_dtype, void* stream);
+                       int out_dtype, void* workspace, size_t ws_bytes, void* stream);
+size_t moe_gate_workspace_size(int T); /* for moe_combine_gate and shared_expert_gate */
 
 /* ------------------------------------------------------------------------
  * Introspection (not on the hot path; these synchronise the device).

@@ -34,7 +34,7 @@ EXPORTS = (
     "moe_grouped_gemm_gateup_silu_bf16",
     "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
-    "moe_set_gemm_pairing",
+    "moe_set_gemm_pairing", "moe_gate_workspace_size",
 )
 
 
@@ -66,8 +66,9 @@ _SIGS = {
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
     "moe_set_gemm_pairing": ([_I], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
-    "moe_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I, _P], _I),
-    "shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I, _P], _I),
+    "moe_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I, _P, _SZ, _P], _I),
+    "shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I, _P, _SZ, _P], _I),
+    "moe_gate_workspace_size": ([_I], _SZ),
     "moe_device_status": ([ctypes.POINTER(_I), _I], _I),
     "moe_launch_counts": ([ctypes.POINTER(ctypes.c_ulonglong), _I], _I),
 }
@@ -197,17 +198,22 @@ def moe_combine(expert_out, eo_dtype, w, shared, sh_dtype, routed_scale, T, K, H
 
 
 def moe_combine_gate(expert_out, eo_dtype, w, sd, sd_dtype, gl, routed_scale, T, K, H, out,
-                     out_dtype, stream=None, check=True):
+                     out_dtype, workspace=None, ws_bytes=0, stream=None, check=True):
     rc = lib().moe_combine_gate(_ptr(expert_out), eo_dtype, _ptr(w), _ptr(sd), sd_dtype, _ptr(gl),
                                 float(routed_scale), T, K, H, _ptr(out), out_dtype,
-                                _stream(stream))
+                                _ptr(workspace), ws_bytes, _stream(stream))
     return _check(rc) if check else rc
 
 
-def shared_expert_gate(sd, sd_dtype, gl, T, H, out, out_dtype, stream=None, check=True):
+def shared_expert_gate(sd, sd_dtype, gl, T, H, out, out_dtype, workspace=None, ws_bytes=0,
+                       stream=None, check=True):
     rc = lib().shared_expert_gate(_ptr(sd), sd_dtype, _ptr(gl), T, H, _ptr(out), out_dtype,
-                                  _stream(stream))
+                                  _ptr(workspace), ws_bytes, _stream(stream))
     return _check(rc) if check else rc
+
+
+def moe_gate_workspace_size(T) -> int:
+    return lib().moe_gate_workspace_size(T)
 
 
 def moe_device_status(clear: bool = False) -> int:

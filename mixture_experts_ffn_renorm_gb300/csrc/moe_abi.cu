@@ -65,7 +65,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_msg; }
 
-int moe_abi_version(void) { return 2; }
+int moe_abi_version(void) { return 3; }
 
 int moe_device_status(int* status_out, int clear) {
   moe::clear_error();

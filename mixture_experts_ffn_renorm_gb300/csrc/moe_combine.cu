@@ -8,9 +8,9 @@
 // token, so every expert row, shared row and output row moves as one 16-byte
 // vector per thread (two for f32) and a warp touches 512 contiguous bytes per
 // load.  All K expert vectors of a thread are in flight at once.  The sigmoid
-// of the gate is evaluated once per token per block (it costs a short chain of
-// double-precision operations, which GB300 runs at a low rate), by as many
-// threads as the block has tokens, overlapped with the loads.
+// of the gate is evaluated once per token per block (it costs a chain of
+// double-precision operations, which GB300 runs at a low rate); a gate block
+// streams several slices so that chain is amortised and overlaps the loads.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -19,18 +19,28 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kVec = 8;       // channels per thread
 constexpr int kChunkK = 8;    // expert rows loaded per batch of loads
+constexpr int kGateIters = 4; // slices per block in the fused-sigmoid gate kernels
 
 enum Mode { kCombine = 0, kCombineGate = 1, kGateOnly = 2 };
 
+// 8 consecutive channels of one row: `Raw` is what a load brings in (one
+// 16-byte vector of bf16, two of f32); widening to f32 is deferred to the
+// arithmetic so that loads in flight hold packed data.
 template <typename T>
 struct Vec8;
 template <>
 struct Vec8<float> {
-  __device__ __forceinline__ static void load(const void* base, size_t idx, float* v) {
+  struct Raw { float4 a, b; };
+  __device__ __forceinline__ static Raw load_raw(const void* base, size_t idx) {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
-    float4 a = __ldg(p), b = __ldg(p + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    return Raw{__ldg(p), __ldg(p + 1)};
+  }
+  __device__ __forceinline__ static void widen(const Raw& r, float* v) {
+    v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+    v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+  }
+  __device__ __forceinline__ static void load(const void* base, size_t idx, float* v) {
+    widen(load_raw(base, idx), v);
   }
   __device__ __forceinline__ static void store(void* base, size_t idx, const float* v) {
     float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + idx);
@@ -40,14 +50,20 @@ struct Vec8<float> {
 };
 template <>
 struct Vec8<__nv_bfloat16> {
-  __device__ __forceinline__ static void load(const void* base, size_t idx, float* v) {
-    uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx));
-    uint32_t w[4] = {a.x, a.y, a.z, a.w};
+  using Raw = uint4;
+  __device__ __forceinline__ static Raw load_raw(const void* base, size_t idx) {
+    return __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx));
+  }
+  __device__ __forceinline__ static void widen(const Raw& a, float* v) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       v[2 * i] = __uint_as_float(w[i] << 16);
       v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
+  }
+  __device__ __forceinline__ static void load(const void* base, size_t idx, float* v) {
+    widen(load_raw(base, idx), v);
   }
   __device__ __forceinline__ static void store(void* base, size_t idx, const float* v) {
     uint32_t w[4];
@@ -63,80 +79,62 @@ __device__ __forceinline__ float round_through_bf16(float v) {
   return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(v)) << 16);
 }
 
+// The routed sum of one 8-channel item: acc = (sum_k eo[t,k,c] (* w[t,k])) * rs,
+// sequential in k from +0, every operation separately rounded.  All of a
+// batch's expert rows are loaded before any arithmetic: rows past K load row
+// K-1 again (a cache hit) instead of being predicated off, so the compiler
+// keeps every load in flight at once.
+template <typename EoT, bool kHasW>
+__device__ __forceinline__ void routed_sum(const void* __restrict__ eo,
+                                           const float* __restrict__ w, float rs, int t, int c0,
+                                           int K, int H, float (&acc)[kVec]) {
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
+  const size_t row0 = static_cast<size_t>(t) * K;
+  for (int k0 = 0; k0 < K; k0 += kChunkK) {
+    typename Vec8<EoT>::Raw raw[kChunkK];
+    float wk[kChunkK];
+#pragma unroll
+    for (int j = 0; j < kChunkK; ++j) {
+      const int kk = min(k0 + j, K - 1);
+      raw[j] = Vec8<EoT>::load_raw(eo, (row0 + kk) * H + c0);
+      wk[j] = kHasW ? __ldg(w + row0 + kk) : 1.0f;
+    }
+    const int kn = min(kChunkK, K - k0);
+#pragma unroll
+    for (int j = 0; j < kChunkK; ++j) {
+      if (j < kn) {
+        float v[kVec];
+        Vec8<EoT>::widen(raw[j], v);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) {
+          float term = kHasW ? __fmul_rn(v[i], wk[j]) : v[i];
+          acc[i] = __fadd_rn(acc[i], term);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) acc[i] = __fmul_rn(acc[i], rs);
+}
+
+// kMoeCombine: one 8-channel item per thread
 template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
                const void* __restrict__ sh, const float* __restrict__ gl, float rs, int T, int K,
                int H, void* __restrict__ out, unsigned long long* launches, int kid) {
+  (void)gl;
   count_launch(launches, kid);
-  __shared__ float s_gate[kThreads];
   const int ipr = H / kVec;                         // items per token row
-  const long long first = static_cast<long long>(blockIdx.x) * kThreads;
-  const long long item = first + threadIdx.x;
-  const long long n_items = static_cast<long long>(T) * ipr;
-  const bool live = item < n_items;
-  const int t = live ? static_cast<int>(item / ipr) : 0;
-  const int c0 = live ? static_cast<int>(item % ipr) * kVec : 0;
-
+  const long long item = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+  if (item >= static_cast<long long>(T) * ipr) return;
+  const int t = static_cast<int>(item / ipr);
+  const int c0 = static_cast<int>(item % ipr) * kVec;
   float shv[kVec];
-  if (kMode != kCombine || kHasShared) {
-    if (live) Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
-  }
-
+  if (kHasShared) Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
   float acc[kVec];
-#pragma unroll
-  for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
-
-  if (kMode != kGateOnly && live) {
-    const size_t row0 = static_cast<size_t>(t) * K;
-    for (int k0 = 0; k0 < K; k0 += kChunkK) {
-      // all kChunkK loads are issued before any arithmetic: rows past K load
-      // row K-1 again (a cache hit) instead of being predicated off, so the
-      // compiler keeps every load in flight at once
-      float v[kChunkK][kVec];
-      float wk[kChunkK];
-#pragma unroll
-      for (int j = 0; j < kChunkK; ++j) {
-        const int kk = min(k0 + j, K - 1);
-        Vec8<EoT>::load(eo, (row0 + kk) * H + c0, v[j]);
-        wk[j] = kHasW ? __ldg(w + row0 + kk) : 1.0f;
-      }
-      const int kn = min(kChunkK, K - k0);
-#pragma unroll
-      for (int j = 0; j < kChunkK; ++j) {
-        if (j < kn) {
-#pragma unroll
-          for (int i = 0; i < kVec; ++i) {
-            float term = kHasW ? __fmul_rn(v[j][i], wk[j]) : v[j][i];
-            acc[i] = __fadd_rn(acc[i], term);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) acc[i] = __fmul_rn(acc[i], rs);
-  }
-
-  if (kMode != kCombine) {
-    // one sigmoid per token of this block
-    const int t_first = static_cast<int>(first / ipr);
-    long long last_item = first + kThreads - 1;
-    if (last_item >= n_items) last_item = n_items - 1;
-    const int n_rows = static_cast<int>(last_item / ipr) - t_first + 1;
-    if (static_cast<int>(threadIdx.x) < n_rows) s_gate[threadIdx.x] = sigmoid_cr(__ldg(gl + t_first + threadIdx.x));
-    __syncthreads();
-    if (!live) return;
-    const float s = s_gate[t - t_first];
-    float o[kVec];
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) {
-      float g = __fmul_rn(s, shv[i]);
-      o[i] = (kMode == kGateOnly) ? g : __fadd_rn(acc[i], round_through_bf16(g));
-    }
-    Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, o);
-    return;
-  }
-  if (!live) return;
+  routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
   if (kHasShared) {
 #pragma unroll
     for (int i = 0; i < kVec; ++i) acc[i] = __fadd_rn(acc[i], shv[i]);
@@ -144,15 +142,116 @@ combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
   Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, acc);
 }
 
+// kMoeCombineGate / kSharedExpertGate: a block streams kGateIters consecutive
+// slices of kThreads items, so the sigmoid of each of its tokens (a chain of
+// double-precision operations, slow on GB300) is evaluated once per block, by
+// full warps, while the first slice's loads are in flight.
+// sigma(gl[t]) for every token, one per thread (full warps), into s_out[T]
+__global__ void __launch_bounds__(kThreads)
+gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_out) {
+  const int t = blockIdx.x * kThreads + threadIdx.x;
+  if (t < T) s_out[t] = sigmoid_cr(__ldg(gl + t));
+}
+
+// The gate ops with the sigmoids already in `sig` (gate_sigmoid_kernel): a
+// plain stream, one 8-channel item per thread, no double precision.
+template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
+__global__ void __launch_bounds__(kThreads)
+gate_stream_kernel(const void* __restrict__ eo, const float* __restrict__ w,
+                   const void* __restrict__ sh, const float* __restrict__ sig, float rs, int T,
+                   int K, int H, void* __restrict__ out, unsigned long long* launches, int kid) {
+  count_launch(launches, kid);
+  const int ipr = H / kVec;
+  const long long item = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+  if (item >= static_cast<long long>(T) * ipr) return;
+  const int t = static_cast<int>(item / ipr);
+  const int c0 = static_cast<int>(item % ipr) * kVec;
+  float shv[kVec], acc[kVec];
+  Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
+  if (kMode == kCombineGate) routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
+  const float sg = __ldg(sig + t);
+  float o[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const float g = __fmul_rn(sg, shv[i]);
+    o[i] = (kMode == kGateOnly) ? g : __fadd_rn(acc[i], round_through_bf16(g));
+  }
+  Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, o);
+}
+
+template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
+__global__ void __launch_bounds__(kThreads)
+gate_kernel(const void* __restrict__ eo, const float* __restrict__ w,
+            const void* __restrict__ sh, const float* __restrict__ gl, float rs, int T, int K,
+            int H, void* __restrict__ out, unsigned long long* launches, int kid) {
+  count_launch(launches, kid);
+  __shared__ float s_gate[kThreads * kGateIters + 1];
+  const int ipr = H / kVec;
+  const long long n_items = static_cast<long long>(T) * ipr;
+  const long long base = static_cast<long long>(blockIdx.x) * kThreads * kGateIters;
+  long long last = base + static_cast<long long>(kThreads) * kGateIters - 1;
+  if (last >= n_items) last = n_items - 1;
+  const int t_first = static_cast<int>(base / ipr);
+  const int n_rows = static_cast<int>(last / ipr) - t_first + 1;
+
+  // first slice: loads issued before the sigmoids are evaluated
+  long long item = base + threadIdx.x;
+  bool live = item < n_items;
+  int t = live ? static_cast<int>(item / ipr) : 0;
+  int c0 = live ? static_cast<int>(item % ipr) * kVec : 0;
+  float shv[kVec], acc[kVec];
+  if (live) {
+    Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
+    if (kMode == kCombineGate) routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
+  }
+  for (int r = threadIdx.x; r < n_rows; r += kThreads)
+    s_gate[r] = sigmoid_cr(__ldg(gl + t_first + r));
+  __syncthreads();
+  for (int it = 0; it < kGateIters; ++it) {
+    if (it > 0) {
+      item = base + static_cast<long long>(it) * kThreads + threadIdx.x;
+      live = item < n_items;
+      if (!live) break;
+      t = static_cast<int>(item / ipr);
+      c0 = static_cast<int>(item % ipr) * kVec;
+      Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
+      if (kMode == kCombineGate) routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
+    }
+    if (!live) break;
+    const float sg = s_gate[t - t_first];
+    float o[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const float g = __fmul_rn(sg, shv[i]);
+      // combine-gate: the gated shared term is rounded through bf16 before the add
+      o[i] = (kMode == kGateOnly) ? g : __fadd_rn(acc[i], round_through_bf16(g));
+    }
+    Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, o);
+  }
+}
+
 using KernelFn = void (*)(const void*, const float*, const void*, const float*, float, int, int,
                           int, void*, unsigned long long*, int);
 
+// kMode 3 / 4: kCombineGate / kGateOnly reading precomputed sigmoids
 template <int kMode, typename EoT, typename ShT, typename OutT>
 KernelFn pick_w_sh(bool has_w, bool has_sh) {
-  if (has_w) return has_sh ? combine_kernel<kMode, EoT, ShT, OutT, true, true>
-                           : combine_kernel<kMode, EoT, ShT, OutT, true, false>;
-  return has_sh ? combine_kernel<kMode, EoT, ShT, OutT, false, true>
-                : combine_kernel<kMode, EoT, ShT, OutT, false, false>;
+  if constexpr (kMode == kGateOnly) {
+    return gate_kernel<kMode, EoT, ShT, OutT, false, true>;
+  } else if constexpr (kMode == kCombineGate) {
+    return has_w ? gate_kernel<kMode, EoT, ShT, OutT, true, true>
+                 : gate_kernel<kMode, EoT, ShT, OutT, false, true>;
+  } else if constexpr (kMode == kGateOnly + 2) {
+    return gate_stream_kernel<kGateOnly, EoT, ShT, OutT, false, true>;
+  } else if constexpr (kMode == kCombineGate + 2) {
+    return has_w ? gate_stream_kernel<kCombineGate, EoT, ShT, OutT, true, true>
+                 : gate_stream_kernel<kCombineGate, EoT, ShT, OutT, false, true>;
+  } else {
+    if (has_w) return has_sh ? combine_kernel<kMode, EoT, ShT, OutT, true, true>
+                             : combine_kernel<kMode, EoT, ShT, OutT, true, false>;
+    return has_sh ? combine_kernel<kMode, EoT, ShT, OutT, false, true>
+                  : combine_kernel<kMode, EoT, ShT, OutT, false, false>;
+  }
 }
 
 template <int kMode, typename EoT, typename ShT>
@@ -199,21 +298,47 @@ int common_checks(const char* op, int T, int K, int H, bool need_k) {
 }
 
 int launch(const char* op, KernelFn fn, const void* eo, const float* w, const void* sh,
-           const float* gl, float rs, int T, int K, int H, void* out, void* stream, int kid) {
+           const float* gl, float rs, int T, int K, int H, void* out, void* stream, int kid,
+           bool fused_sigmoid) {
   if (T == 0) return MOE_OK;
   DeviceDiag diag = device_diag();
   const long long items = static_cast<long long>(T) * (H / kVec);
-  const long long blocks = (items + kThreads - 1) / kThreads;
+  const long long per_block =
+      fused_sigmoid ? static_cast<long long>(kThreads) * kGateIters : kThreads;
+  const long long blocks = (items + per_block - 1) / per_block;
   if (blocks > 0x7fffffffLL) return set_error(MOE_ERR_ARG, "%s: T*H too large", op);
   fn<<<static_cast<unsigned>(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       eo, w, sh, gl, rs, T, K, H, out, diag.launches, kid);
   return check_launch(op);
 }
 
+// sigmoids of all T tokens into the workspace (then the stream reads them)
+int precompute_sigmoids(const char* op, const float* gl, int T, void* workspace, size_t ws_bytes,
+                        void* stream, const float** sig) {
+  *sig = nullptr;
+  if (workspace == nullptr) return MOE_OK;  // fused path: sigmoids inside the gate kernel
+  if (ws_bytes < moe_gate_workspace_size(T))
+    return set_error(MOE_ERR_WORKSPACE, "%s: workspace of %zu bytes is smaller than %zu", op,
+                     ws_bytes, moe_gate_workspace_size(T));
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u)
+    return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
+  float* s_out = static_cast<float*>(workspace);
+  gate_sigmoid_kernel<<<(T + kThreads - 1) / kThreads, kThreads, 0,
+                        static_cast<cudaStream_t>(stream)>>>(gl, T, s_out);
+  int rc = check_launch(op);
+  if (rc == MOE_OK) *sig = s_out;
+  return rc;
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" size_t moe_gate_workspace_size(int T) {
+  if (T <= 0) return 0;
+  return ((static_cast<size_t>(T) * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+}
 
 extern "C" int moe_combine(const void* expert_out, int eo_dtype, const float* w,
                            const void* shared, int sh_dtype, float routed_scale, int T, int K,
@@ -233,12 +358,13 @@ extern "C" int moe_combine(const void* expert_out, int eo_dtype, const float* w,
   KernelFn fn = pick<kCombine>(eo_dtype, shared ? sh_dtype : MOE_BF16, out_dtype, w != nullptr,
                                shared != nullptr);
   return launch(op, fn, expert_out, w, shared, nullptr, routed_scale, T, K, H, out, stream,
-                MOE_KID_COMBINE);
+                MOE_KID_COMBINE, false);
 }
 
 extern "C" int moe_combine_gate(const void* expert_out, int eo_dtype, const float* w,
                                 const void* sd, int sd_dtype, const float* gl, float routed_scale,
-                                int T, int K, int H, void* out, int out_dtype, void* stream) {
+                                int T, int K, int H, void* out, int out_dtype, void* workspace,
+                                size_t ws_bytes, void* stream) {
   clear_error();
   const char* op = "moe_combine_gate";
   int rc;
@@ -252,13 +378,22 @@ extern "C" int moe_combine_gate(const void* expert_out, int eo_dtype, const floa
   if (!aligned16(expert_out) || !aligned16(out) || !aligned16(sd) ||
       (reinterpret_cast<uintptr_t>(gl) & 3u) || (w && (reinterpret_cast<uintptr_t>(w) & 3u)))
     return set_error(MOE_ERR_ALIGN, "%s: expert_out/sd/out must be 16-byte aligned", op);
+  const float* sig = nullptr;
+  if ((rc = precompute_sigmoids(op, gl, T, workspace, ws_bytes, stream, &sig)) != MOE_OK)
+    return rc;
+  if (sig) {
+    KernelFn fn = pick<kCombineGate + 2>(eo_dtype, sd_dtype, out_dtype, w != nullptr, true);
+    return launch(op, fn, expert_out, w, sd, sig, routed_scale, T, K, H, out, stream,
+                  MOE_KID_COMBINE_GATE, false);
+  }
   KernelFn fn = pick<kCombineGate>(eo_dtype, sd_dtype, out_dtype, w != nullptr, true);
   return launch(op, fn, expert_out, w, sd, gl, routed_scale, T, K, H, out, stream,
-                MOE_KID_COMBINE_GATE);
+                MOE_KID_COMBINE_GATE, true);
 }
 
 extern "C" int shared_expert_gate(const void* sd, int sd_dtype, const float* gl, int T, int H,
-                                  void* out, int out_dtype, void* stream) {
+                                  void* out, int out_dtype, void* workspace, size_t ws_bytes,
+                                  void* stream) {
   clear_error();
   const char* op = "shared_expert_gate";
   int rc;
@@ -269,7 +404,15 @@ extern "C" int shared_expert_gate(const void* sd, int sd_dtype, const float* gl,
   if (!sd || !gl || !out) return set_error(MOE_ERR_ARG, "%s: sd/gl/out is NULL", op);
   if (!aligned16(sd) || !aligned16(out) || (reinterpret_cast<uintptr_t>(gl) & 3u))
     return set_error(MOE_ERR_ALIGN, "%s: sd/out must be 16-byte aligned", op);
+  const float* sig = nullptr;
+  if ((rc = precompute_sigmoids(op, gl, T, workspace, ws_bytes, stream, &sig)) != MOE_OK)
+    return rc;
+  if (sig) {
+    KernelFn fn = pick<kGateOnly + 2>(MOE_BF16, sd_dtype, out_dtype, false, true);
+    return launch(op, fn, nullptr, nullptr, sd, sig, 1.0f, T, 1, H, out, stream,
+                  MOE_KID_SHARED_GATE, false);
+  }
   KernelFn fn = pick<kGateOnly>(MOE_BF16, sd_dtype, out_dtype, false, true);
   return launch(op, fn, nullptr, nullptr, sd, gl, 1.0f, T, 1, H, out, stream,
-                MOE_KID_SHARED_GATE);
+                MOE_KID_SHARED_GATE, true);
 }

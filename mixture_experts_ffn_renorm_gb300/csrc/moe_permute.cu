@@ -147,19 +147,32 @@ permute_place(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   }
 }
 
+// One warp per permuted row; each lane keeps up to 8 16-byte vectors of the
+// row in flight before it stores any of them.
 __global__ void __launch_bounds__(256)
 permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair, int P,
                int K, int H, uint16_t* __restrict__ x_perm, unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_GATHER);
+  const int lane = threadIdx.x & 31;
   const int vpr = H / 8;
-  const long long n = static_cast<long long>(P) * vpr;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int row = static_cast<int>(i / vpr);
-    const int v = static_cast<int>(i - static_cast<long long>(row) * vpr);
+  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       row < P; row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
     const int src = __ldg(sorted_pair + row) / K;
-    const uint4 d = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(src) * H) + v);
-    reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(row) * H)[v] = d;
+    const uint4* s = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src) * H);
+    uint4* d = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(row) * H);
+    for (int v0 = 0; v0 < vpr; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < vpr) buf[i] = __ldg(s + v);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < vpr) d[v] = buf[i];
+      }
+    }
   }
 }
 
@@ -219,9 +232,8 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
                                                   diag.launches);
   if ((rc = check_launch(op)) != MOE_OK) return rc;
   if (x_perm_bf16) {
-    const long long items = P * (H / 8);
-    long long g = (items + 255) / 256;
-    if (g > 152LL * 16) g = 152LL * 16;
+    long long g = (P + 7) / 8;  // 8 rows (warps) per block
+    if (g > 152LL * 32) g = 152LL * 32;
     permute_gather<<<static_cast<unsigned>(g), 256, 0, s>>>(
         static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P), K, H,
         static_cast<uint16_t*>(x_perm_bf16), diag.launches);

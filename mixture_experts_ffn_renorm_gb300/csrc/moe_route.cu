@@ -21,18 +21,15 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-// does (a, ia) rank above (b, ib)?  descending value, ties to the lower id,
-// NaN below every number; ib < 0 means "no candidate yet"
-__device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
-  if (ib < 0) return true;
-  const bool na = a != a, nb = b != b;
-  if (na || nb) {
-    if (na && nb) return ia < ib;
-    return nb;
-  }
-  if (a > b) return true;
-  if (a < b) return false;
-  return ia < ib;
+// Order-preserving 32-bit key of a logit for the selection: larger key = ranks
+// higher.  -0 and +0 share a key (they compare equal), every NaN gets key 0
+// (below -inf, whose key is 0x007FFFFF), and equal keys go to the lower expert
+// id -- the order "descending value, ties to the lower id, NaN last".
+__device__ __forceinline__ uint32_t rank_key(float v) {
+  if (v != v) return 0u;
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // One warp selects the top-K of one token.  The weights' exps are then
@@ -62,31 +59,33 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormali
       const int e = lane + 32 * i;
       v[i] = e < E ? __ldg(row + e) : 0.0f;
     }
+    uint32_t key[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) key[i] = rank_key(v[i]);
     uint32_t taken = 0;
     for (int j = 0; j < K; ++j) {
+      // this lane's best untaken entry (ascending id, so ties keep the lower id)
+      uint32_t bk = 0u, bid = 0xFFFFFFFFu;
       float bv = 0.0f;
-      int be = -1;
 #pragma unroll
       for (int i = 0; i < kPerLane; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && ranks_above(v[i], e, bv, be)) {
+        if (e < E && !((taken >> i) & 1u) && (bid == 0xFFFFFFFFu || key[i] > bk)) {
+          bk = key[i];
+          bid = static_cast<uint32_t>(e);
           bv = v[i];
-          be = e;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe >= 0 && ranks_above(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      // the warp's best: highest key, then lowest id among the lanes holding it
+      const uint32_t top = __reduce_max_sync(0xffffffffu, bid == 0xFFFFFFFFu ? 0u : bk);
+      const uint32_t cand = (bid != 0xFFFFFFFFu && bk == top) ? bid : 0xFFFFFFFFu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      const int owner = static_cast<int>(win & 31u);
+      const float wv = __shfl_sync(0xffffffffu, bv, owner);
+      if (owner == lane) taken |= 1u << (win >> 5);
       if (lane == j) {
-        my_sel = bv;
-        my_id = be;
+        my_sel = wv;
+        my_id = static_cast<int>(win);
       }
     }
     s_sel[wib][lane] = my_sel;

@@ -13,9 +13,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, moe_combine, moe_combine_gate, moe_grouped_gemm_down_bf16,
-               moe_grouped_gemm_gateup_silu_bf16, moe_permute, moe_permute_workspace_size,
-               moe_route_topk, moe_route_topk_workspace_size)
+from . import (BF16, moe_combine, moe_combine_gate, moe_gate_workspace_size,
+               moe_grouped_gemm_down_bf16, moe_grouped_gemm_gateup_silu_bf16, moe_permute,
+               moe_permute_workspace_size, moe_route_topk, moe_route_topk_workspace_size)
 
 
 def _dev_bf16(a, device):
@@ -74,15 +74,17 @@ class MoeBlock:
             self.sd = torch.empty((T, H), dtype=bf, device=dv)
         self.ws_route = moe_route_topk_workspace_size(T, E, K)
         self.ws_perm = moe_permute_workspace_size(T, K, E)
-        self.workspace = torch.empty((max(self.ws_route, self.ws_perm, 256),), dtype=torch.uint8,
-                                     device=dv)
+        self.ws_gate = moe_gate_workspace_size(T)
+        self.workspace = torch.empty((max(self.ws_route, self.ws_perm, self.ws_gate, 256),),
+                                     dtype=torch.uint8, device=dv)
         self.graph = None
         self.graph_x = None
+        self._pipe = None
 
     # one forward over x [T, H] bf16 (device); returns a view of the output buffer.
     # marks: optional list; a CUDA event is recorded after each stage and
     # appended as (stage name, event), for per-kernel timing on the stream.
-    def forward(self, x, stream=None, marks=None):
+    def forward(self, x, stream=None, marks=None, out=None):
         T = x.shape[0]
         assert T <= self.max_tokens and x.dtype == torch.bfloat16 and x.is_contiguous()
         H, I, E, K = self.H, self.I, self.E, self.K
@@ -116,7 +118,7 @@ class MoeBlock:
         moe_grouped_gemm_down_bf16(self.act, self.w2, self.expert_offsets, self.topk_w,
                                    self.sorted_pair, P, I, H, E, self.expert_out, None, 0, stream)
         mark("gemm_down")
-        out = self.out[:T]
+        out = self.out[:T] if out is None else out
         if self.has_shared:
             moe_grouped_gemm_gateup_silu_bf16(x, T, None, 1, self.w13_shared, None, T, H, self.Is,
                                               1, self.act_shared, None, 0, stream)
@@ -124,7 +126,7 @@ class MoeBlock:
                                        self.Is, H, 1, self.sd, None, 0, stream)
             mark("shared_expert")
             moe_combine_gate(self.expert_out, BF16, None, self.sd, BF16, self.gate_logit,
-                             self.routed_scale, T, K, H, out, BF16, stream)
+                             self.routed_scale, T, K, H, out, BF16, ws, ws.numel(), stream)
             mark("combine")
             return out
         else:
@@ -136,6 +138,8 @@ class MoeBlock:
     # launches per forward (for the bench's gpu_launches claim)
     def kernels_per_forward(self) -> int:
         n = 2 + (3 if self.gather else 4) + 3  # route (2), permute (3 or 4), 2 GEMMs, combine
+        if self.has_shared:
+            n += 1  # the combine-gate's sigmoid pass
         if self.has_shared:
             n += 2
         return n
@@ -156,3 +160,59 @@ class MoeBlock:
     def replay(self):
         self.graph.replay()
         return self.out[: self.graph_x.shape[0]]
+
+    def run_host_batches(self, x_hosts, out_hosts):
+        """End to end over pinned host batches: out_hosts[i] <- block(x_hosts[i]).
+
+        Batch i computes on the current stream while batch i+1 is copied in
+        on an upload stream and batch i-1 is copied out on a download stream;
+        device input and output buffers are double-buffered and every reuse
+        waits on the event that frees it.  Returns when all work is enqueued;
+        synchronise the current stream (or the device) before reading
+        out_hosts.  Batches may have different token counts up to max_tokens.
+        """
+        dev = self.device
+        H = self.H
+        if self._pipe is None:
+            mk = lambda: torch.empty((self.max_tokens, H), dtype=torch.bfloat16, device=dev)
+            ev = lambda: torch.cuda.Event()
+            self._pipe = {
+                "up": torch.cuda.Stream(device=dev), "down": torch.cuda.Stream(device=dev),
+                "x": [mk(), mk()], "o": [mk(), mk()],
+                "h2d": [ev(), ev()], "fwd": [ev(), ev()], "d2h": [ev(), ev()],
+            }
+        pp = self._pipe
+        cs = torch.cuda.current_stream(dev)
+        up, down = pp["up"], pp["down"]
+        n = len(x_hosts)
+        up.wait_stream(cs)
+        down.wait_stream(cs)
+
+        def upload(i):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(pp["fwd"][b])      # batch i-2 no longer reads x[b]
+                T = x_hosts[i].shape[0]
+                pp["x"][b][:T].copy_(x_hosts[i], non_blocking=True)
+                pp["h2d"][b].record(up)
+
+        if n:
+            upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            T = x_hosts[i].shape[0]
+            cs.wait_event(pp["h2d"][b])
+            if i >= 2:
+                cs.wait_event(pp["d2h"][b])          # batch i-2's output has left o[b]
+            self.forward(pp["x"][b][:T], out=pp["o"][b][:T])
+            pp["fwd"][b].record(cs)
+            with torch.cuda.stream(down):
+                down.wait_event(pp["fwd"][b])
+                out_hosts[i].copy_(pp["o"][b][:T], non_blocking=True)
+                pp["d2h"][b].record(down)
+        cs.wait_stream(up)
+        cs.wait_stream(down)
+        return out_hosts

@@ -45,11 +45,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_refusals_without_gpu(lib):
-    assert m.abi_version() == 2
+    assert m.abi_version() == 3
     # dtype refusals name the missing arm and return before touching the device
     rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
     assert rc == m.ERR_DTYPE and "f16" in m.last_error()
-    rc = lib.shared_expert_gate(None, m.BF16, None, 1, 8, None, 7, None)
+    rc = lib.shared_expert_gate(None, m.BF16, None, 1, 8, None, 7, None, 0, None)
     assert rc == m.ERR_DTYPE
     rc = lib.moe_route_topk(None, None, None, None, None, 1, 8, 8, 2, 1, 1, 1, None, None, None,
                             None, None, 0, None)

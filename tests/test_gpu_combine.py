@@ -69,14 +69,17 @@ def test_combine_gate_bit_exact(eo_dt, sd_dt, out_dt, T, K, H, rs):
     gl = rng.normal(0, 2, T).astype(np.float32)
     gl[0] = 0.0
     w = rng.uniform(0, 1, (T, K)).astype(np.float32)
+    ws = empty((m.moe_gate_workspace_size(T),), torch.uint8)
     for ww in (w, None):
         want = O.combine_gate(eo, ww, sd, gl, routed_scale=rs, T=T, K=K, H=H, out_dtype=out_dt)
-        out = _out(T, H, out_dt)
-        before = launches()
-        m.moe_combine_gate(to_dev(eo), eo_dt, None if ww is None else to_dev(ww), to_dev(sd),
-                           sd_dt, to_dev(gl), rs, T, K, H, out, out_dt)
-        assert launched_since(before, "combine_gate") == 1
-        assert np.array_equal(to_host(out), want)
+        for wsp in (None, ws):   # sigmoids inside the stream, or precomputed into the workspace
+            out = _out(T, H, out_dt)
+            before = launches()
+            m.moe_combine_gate(to_dev(eo), eo_dt, None if ww is None else to_dev(ww), to_dev(sd),
+                               sd_dt, to_dev(gl), rs, T, K, H, out, out_dt, wsp,
+                               0 if wsp is None else wsp.numel())
+            assert launched_since(before, "combine_gate") == 1
+            assert np.array_equal(to_host(out), want)
 
 
 @pytest.mark.parametrize("sd_dt", [F32, BF16])
@@ -88,11 +91,14 @@ def test_shared_expert_gate_four_arms(sd_dt, out_dt):
     gl = rng.normal(0, 4, T).astype(np.float32)
     gl[:6] = [0.0, -0.0, 100.0, -100.0, 17.0, -89.0]
     want = O.shared_expert_gate(sd, gl, T=T, H=H, out_dtype=out_dt)
-    out = _out(T, H, out_dt)
-    before = launches()
-    m.shared_expert_gate(to_dev(sd), sd_dt, to_dev(gl), T, H, out, out_dt)
-    assert launched_since(before, "shared_gate") == 1
-    assert np.array_equal(to_host(out), want)
+    ws = empty((m.moe_gate_workspace_size(T),), torch.uint8)
+    for wsp in (None, ws):
+        out = _out(T, H, out_dt)
+        before = launches()
+        m.shared_expert_gate(to_dev(sd), sd_dt, to_dev(gl), T, H, out, out_dt, wsp,
+                             0 if wsp is None else wsp.numel())
+        assert launched_since(before, "shared_gate") == 1
+        assert np.array_equal(to_host(out), want)
 
 
 def test_sigmoid_bit_exact_on_a_wide_sweep():
@@ -108,11 +114,14 @@ def test_sigmoid_bit_exact_on_a_wide_sweep():
     g = np.concatenate([edges, g, rng.uniform(-110, 110, 1 << 20).astype(np.float32)])
     T, H = g.size, 8
     sd = np.ones((T, H), np.float32)
-    out = _out(T, H, F32)
-    m.shared_expert_gate(to_dev(sd), F32, to_dev(g), T, H, out, F32)
-    got = to_host(out)[:, 0]
     want = O.shared_expert_gate(sd[:, :1].copy(), g, T=T, H=1, out_dtype=F32)[:, 0]
-    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    ws = empty((m.moe_gate_workspace_size(T),), torch.uint8)
+    for wsp in (None, ws):
+        out = _out(T, H, F32)
+        m.shared_expert_gate(to_dev(sd), F32, to_dev(g), T, H, out, F32, wsp,
+                             0 if wsp is None else wsp.numel())
+        got = to_host(out)[:, 0]
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
 def test_combine_gate_full_size_workload():
@@ -123,10 +132,13 @@ def test_combine_gate_full_size_workload():
     T, K, H = cfg.T, cfg.K, cfg.H
     _, w, _, _ = O.route_topk(logits_in=d["logits"], T=T, H=1, E=cfg.E_logits, K=K)
     want = O.combine_gate(d["expert_out"], w, d["sd"], d["gl"], T=T, K=K, H=H, out_dtype=BF16)
-    out = _out(T, H, BF16)
-    m.moe_combine_gate(to_dev(d["expert_out"]), BF16, to_dev(w), to_dev(d["sd"]), BF16,
-                       to_dev(d["gl"]), 1.0, T, K, H, out, BF16)
-    assert np.array_equal(to_host(out), want)
+    ws = empty((m.moe_gate_workspace_size(T),), torch.uint8)
+    for wsp in (None, ws):
+        out = _out(T, H, BF16)
+        m.moe_combine_gate(to_dev(d["expert_out"]), BF16, to_dev(w), to_dev(d["sd"]), BF16,
+                           to_dev(d["gl"]), 1.0, T, K, H, out, BF16, wsp,
+                           0 if wsp is None else wsp.numel())
+        assert np.array_equal(to_host(out), want)
 
 
 def test_refusals_enqueue_nothing():
@@ -140,6 +152,11 @@ def test_refusals_enqueue_nothing():
     with pytest.raises(m.MoeError) as ei:
         m.shared_expert_gate(eo, m.F16, to_dev(np.zeros(T, np.float32)), T, H, out, BF16)
     assert ei.value.code == m.ERR_DTYPE
+    small = empty((16,), torch.uint8)
+    with pytest.raises(m.MoeError) as ei:
+        m.shared_expert_gate(out, BF16, to_dev(np.zeros(T, np.float32)), 4096, H, out, BF16, small,
+                             16)
+    assert ei.value.code == m.ERR_WORKSPACE
     with pytest.raises(m.MoeError) as ei:
         m.moe_combine(out, BF16, None, None, BF16, 1.0, T, 0, H, out, BF16)
     assert ei.value.code == m.ERR_ARG
