@@ -35,6 +35,28 @@ METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM TFLOP/s and combine GB/s v
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def recorded_traffic():
+    """DRAM traffic of one gate/up GEMM launch from the committed ncu summary,
+    or None when the kernel sources have changed since it was captured."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "gemm_gateup_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for ln in open(path):
+        if "=" in ln and not ln.startswith("#"):
+            k, v = ln.strip().split("=", 1)
+            kv[k] = v
+    h = hashlib.sha256()
+    for f in ("moe_gemm.cu", "sm100_ptx.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_ffn_renorm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if kv.get("sources_sha256") != h.hexdigest():
+        return None
+    return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -177,6 +199,55 @@ def config_dict(cfg, ws):
             if cfg.T >= 8192 else "L2 flushed between steps (256 MB write)"}
 
 
+def combine_gate_workload(dev, iters=20):
+    """The combine/gate bandwidth workload (T=4096, K=8, H=2048): weighted top-8
+    sum of bf16 expert rows plus the sigmoid-gated shared term.  `iters`
+    back-to-back launches between two CUDA events, alternating between two
+    copies of the inputs (2 x 168 MB > L2), so no launch finds its operands in
+    L2."""
+    import torch
+
+    import mixture_experts_ffn_renorm_gb300 as m
+    from mixture_experts_ffn_renorm_gb300 import workloads as W
+
+    cfg = W.COMBINE
+    d = W.combine_inputs(cfg)
+    T, K, H, E = cfg.T, cfg.K, cfg.H, cfg.E_logits
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    eo, sd = dev_bf16(d["expert_out"]), dev_bf16(d["sd"])
+    eo2, sd2 = eo.clone(), sd.clone()
+    gl = torch.from_numpy(d["gl"]).to(dev)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    m.moe_route_topk(None, None, None, None, logits, T, 8, E, K, 1, 0, 1, ids, w, None, None, None,
+                     0)
+    outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    ws = torch.empty((m.moe_gate_workspace_size(T),), dtype=torch.uint8, device=dev)
+    sets = [(eo, sd, outs[0]), (eo2, sd2, outs[1])]
+
+    def launch(i):
+        e, s_, o = sets[i % 2]
+        m.moe_combine_gate(e, m.BF16, w, s_, m.BF16, gl, 1.0, T, K, H, o, m.BF16, ws, ws.numel())
+
+    for i in range(4):
+        launch(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        launch(i)
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1000.0 * e0.elapsed_time(e1) / iters
+    nbytes = T * K * H * 2 + 2 * T * H * 2 + T * K * 4 + T * 4
+    return {"workload": cfg.name, "us": us, "gbs": nbytes / us / 1e3, "bytes": nbytes}
+
+
 def oracle_tokens_per_s(cfg, d, seconds=10.0):
     """Time the CPU oracle on a bounded sample of the workload's tokens."""
     import oracle as O
@@ -238,9 +309,32 @@ def run_reference(args):
     return 0
 
 
+def run_combine_only(args):
+    import torch
+
+    import __graft_entry__ as ge
+
+    ge.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk, pk_src = peaks()
+    cg = combine_gate_workload(dev, iters=args.steps)
+    line = {"metric": "combine/gate GB/s (bandwidth workload)", "value": cg["gbs"], "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": 3, "ms_per_step": cg["us"] / 1000.0,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": cg["workload"]},
+            "roofline": {"bound": "hbm", "achieved": cg["gbs"], "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": cg["gbs"] / pk["hbm_gbs"],
+                         "peak_source": pk_src, "traffic": None}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
 
+    if args.config == "combine":
+        return run_combine_only(args)
     ws, rank, local = dist_setup(args)
     import __graft_entry__ as ge
 
@@ -337,7 +431,8 @@ def run_ours(args):
     roofline = {"kernel": "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)",
                 "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                "peak_source": f"{pk_src} bf16 dense (burst)", "traffic": None,
+                "peak_source": f"{pk_src} bf16 dense (burst)", "traffic": recorded_traffic(),
+                "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "algorithmic_flop_per_launch": flop_gateup}
     components = {
         "ms": stage_avg,
@@ -350,6 +445,9 @@ def run_ours(args):
         "permute_gbs": (2 * P * cfg.H * 2 + P * 16) / (stage_avg["permute"] / 1000.0) / 1e9,
         "hbm_peak_gbs": pk["hbm_gbs"],
     }
+    cg = combine_gate_workload(dev)
+    cg["frac_hbm"] = cg["gbs"] / pk["hbm_gbs"]
+    components["combine_gate_workload"] = cg
     counts = np.diff(blk.expert_offsets.cpu().numpy())
     components["expert_load"] = {"max": int(counts.max()), "mean": float(counts.mean()),
                                  "min": int(counts.min())}
@@ -391,7 +489,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="prefill", choices=["prefill", "decode", "large", "tiny"])
+    ap.add_argument("--config", default="prefill",
+                    choices=["prefill", "decode", "large", "tiny", "combine"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

@@ -119,8 +119,12 @@ __device__ __forceinline__ void routed_sum(const void* __restrict__ eo,
 }
 
 // kMoeCombine: one 8-channel item per thread
+// bf16 expert rows: <= 64 registers, 4 blocks (32 warps) per SM keep more loads in flight
+template <typename EoT>
+constexpr int min_blocks() { return sizeof(EoT) == 2 ? 4 : 2; }
+
 template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, min_blocks<EoT>())
 combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
                const void* __restrict__ sh, const float* __restrict__ gl, float rs, int T, int K,
                int H, void* __restrict__ out, unsigned long long* launches, int kid) {
@@ -156,7 +160,7 @@ gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_o
 // The gate ops with the sigmoids already in `sig` (gate_sigmoid_kernel): a
 // plain stream, one 8-channel item per thread, no double precision.
 template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, min_blocks<EoT>())
 gate_stream_kernel(const void* __restrict__ eo, const float* __restrict__ w,
                    const void* __restrict__ sh, const float* __restrict__ sig, float rs, int T,
                    int K, int H, void* __restrict__ out, unsigned long long* launches, int kid) {
