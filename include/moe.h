@@ -77,7 +77,7 @@ int moe_abi_version(void);  /* 3 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
- * covered router path is ungrouped softmax; grouped / bias-corrected forms
+ * router in scope there is ungrouped softmax; grouped / bias-corrected forms
  * are refused).
  *
  *   l[t,e] = sum_h f32(x[t,h]) * f32(w_router[e,h])  (+ logit_bias[e])
@@ -119,7 +119,7 @@ size_t moe_route_topk_workspace_size(int T, int E, int K);
 /* ------------------------------------------------------------------------
  * moe_permute -- stable counting sort of the P = T*K (token, slot) pairs by
  * expert, so each expert's rows are contiguous for the grouped GEMMs ([PR509]
- * review: the expert path stores P permuted rows, "ddown {P, H}"; [PR523]:
+ * review: the expert path keeps P permuted bf16 rows of H; [PR523]:
  * grouped over expert ids).  Rows of one expert keep ascending pair order
  * p = t*K + j.  Bit-exact.
  *
@@ -169,7 +169,7 @@ int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int 
  *   up[n]   = bf16( sum_h A[r,h] * w13[g, I + n, h] )
  *   act[r,n] = bf16( silu(f32 gate[n]) * f32 up[n] ),  silu(z) = z / (1 + exp(-z))
  * f32 accumulation on tcgen05 tensor cores; both halves are narrowed to bf16
- * BEFORE the activation ([I3094] "BF16 result narrowing before activation").
+ * BEFORE the activation, as the numeric contract of [I3094] requires.
  *
  *   a            bf16 [P,H] (rows in group order), or, when a_row_gather is
  *                set, bf16 [a_rows,H] read through a_row_gather
@@ -200,8 +200,8 @@ int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows, const int3
  *   y[n] = sum_i act[r,i] * w2[g, n, i]   (f32, tensor cores)
  *   out[dst, n] = bf16( y[n] * pair_weight[dst] )   dst = row_to_pair ? row_to_pair[r] : r
  * The routing weight is applied exactly once, as one f32 multiply before the
- * one bf16 rounding of the store ([I3094] "routing-weight placement before the
- * down-projection result is stored"); a combine after it must not apply it again.
+ * one bf16 rounding of the store: [I3094] puts the weight on the down result
+ * ahead of its store, so a combine after it must not apply it again.
  *
  *   act          bf16 [P,I]
  *   w2           bf16 [G,H,I]

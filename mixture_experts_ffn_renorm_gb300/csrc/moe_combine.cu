@@ -227,7 +227,7 @@ gate_kernel(const void* __restrict__ eo, const float* __restrict__ w,
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
       const float g = __fmul_rn(sg, shv[i]);
-      // combine-gate: the gated shared term is rounded through bf16 before the add
+      // combine-gate: the gated shared term passes through a bf16 rounding before the add
       o[i] = (kMode == kGateOnly) ? g : __fadd_rn(acc[i], round_through_bf16(g));
     }
     Vec8<OutT>::store(out, static_cast<size_t>(t) * H + c0, o);

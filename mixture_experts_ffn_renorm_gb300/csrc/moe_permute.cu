@@ -1,8 +1,8 @@
 // moe_permute.cu -- tokens into expert-contiguous order: a deterministic,
 // stable counting sort of the P = T*K (token, slot) pairs by expert.  The
-// expert path stores P permuted rows (vllm.cpp PR #509 review, finding 2:
-// "DBuf ddown(d, DType::kBF16, {P, H})") and the expert GEMM is grouped over
-// expert ids (PR #523, "What changed").
+// expert path keeps one bf16 row per routed pair, P rows of H (vllm.cpp PR #509
+// review, finding 2), and the expert GEMM is grouped over expert ids (PR #523,
+// "What changed").
 //
 //   count   one warp per chunk of 512 pairs: per-chunk expert histogram in
 //           shared memory (bad ids raise MOE_STATUS_BAD_ID and are skipped)

@@ -1,6 +1,6 @@
 // moe_route.cu -- the ungrouped softmax router with top-k and renormalisation
-// (vllm.cpp PR #509, "Honest gaps": the covered router path is ungrouped
-// softmax; grouped, bias-corrected (noaux_tc) and sigmoid forms are refused).
+// (vllm.cpp PR #509, "Honest gaps": only the ungrouped softmax router is in
+// scope there; grouped, bias-corrected (noaux_tc) and sigmoid forms are refused).
 //
 // Two kernels: the logits GEMM on tcgen05 tensor cores (moe_gemm.cu, f32
 // epilogue with the optional per-expert bias) and a warp-per-token selection

@@ -7,7 +7,7 @@
  * CPU-baseline leg of the benchmark load this library.  The GPU product path
  * never calls it, and the two share no source, header, table or helper.
  *
- * Arithmetic rules (the "local numeric contract" of vllm.cpp issue #3094,
+ * Arithmetic rules (the numeric contract stated in vllm.cpp issue #3094,
  * "Row: BACKEND-ROCM-BF16-MOE", second paragraph, and the bit-exactness rules
  * of vllm.cpp PR #509 "MoE combine/gate ops -- SharedExpertGate, MoeCombine,
  * MoeCombineGate", review rework commit, item 2):
@@ -72,7 +72,7 @@ static float bf2f(uint16_t h) {
  * or exactly one half with an odd kept part.  A carry out of the mantissa
  * moves into the exponent, which is exactly the correct rounding up to the
  * next binade or to infinity.  READING: a NaN stays a NaN (quiet bit set,
- * sign kept); the pages only say the shared term is "rounded through bf16". */
+ * sign kept); the pages only say that the shared term passes through bf16. */
 static uint16_t f2bf(float f) {
   uint32_t u;
   memcpy(&u, &f, 4);
@@ -99,7 +99,7 @@ void oracle_f32_to_bf16_array(const float* src, uint16_t* dst, int64_t n) {
 /* ------------------------------------------------------------------ */
 
 /* READING: the pages require the sigmoid gate and the combine-gate to be
- * bit-identical across CPU and GPU (PR #509 review, "bit-exactness by design")
+ * bit-identical across CPU and GPU (PR #509 review and rework commits)
  * but never say which exp.  The exp used there is therefore DEFINED as the
  * binary32 rounding of one fixed double-precision evaluation:
  *   Cody & Waite (1980) argument reduction  x = n*ln2 + r,  |r| <= ln2/2,
@@ -179,7 +179,7 @@ static float dot_bf16(const uint16_t* a, const uint16_t* b, int n) {
 
 /* ------------------------------------------------------------------ */
 /* a1 + a2: ungrouped softmax router, top-k, renormalise                */
-/* PR #509 "Honest gaps": the covered router path is ungrouped softmax;  */
+/* PR #509 "Honest gaps": only the ungrouped softmax router is in scope;  */
 /* grouped / bias-corrected (noaux_tc) forms are refused.                */
 /* ------------------------------------------------------------------ */
 
@@ -258,8 +258,8 @@ int oracle_route_topk(const uint16_t* x, const uint16_t* w_router, const float* 
 
 /* ------------------------------------------------------------------ */
 /* a3: permute into expert-contiguous order (stable counting sort)      */
-/* The pages' expert path stores P = T*K permuted rows ("DBuf ddown(d,    */
-/* DType::kBF16, {P, H})", PR #509 review finding 2) and groups them over */
+/* The pages' expert path keeps P = T*K permuted bf16 rows of H (PR #509  */
+/* review, finding 2) and groups them over                                */
 /* expert ids (PR #523 "What changed").  READING: rows of one expert keep */
 /* ascending pair order p = t*K + j.                                     */
 /* ------------------------------------------------------------------ */
@@ -297,9 +297,9 @@ int oracle_permute(const int32_t* topk_ids, const uint16_t* x, int T, int K, int
 
 /* ------------------------------------------------------------------ */
 /* a4: grouped gate/up GEMM fused with SiLU-and-mul                     */
-/* kMoeGroupedGemmBf16GateUpSilu, issue #3094: "BF16 result narrowing    */
-/* before activation" -- both the gate and the up accumulations are      */
-/* rounded to bf16 before silu(g)*u.  READING: per expert the weight is  */
+/* kMoeGroupedGemmBf16GateUpSilu, issue #3094: the GEMM result is cut to  */
+/* bf16 ahead of the activation -- both the gate and the up accumulations */
+/* are rounded to bf16 before silu(g)*u.  READING: per expert the weight is */
 /* [2I, H] with the gate rows first and the up rows after them.          */
 /* ------------------------------------------------------------------ */
 
@@ -368,9 +368,9 @@ int oracle_gateup_silu(const uint16_t* a, const int32_t* a_row_gather, const uin
 
 /* ------------------------------------------------------------------ */
 /* a5: grouped down GEMM, routing weight applied once before the store   */
-/* kMoeGroupedGemmBf16, issue #3094: "routing-weight placement before the */
-/* down-projection result is stored, and reduction without applying      */
-/* those weights twice".  READING: y = sum_i act*W2 in f32, one f32      */
+/* kMoeGroupedGemmBf16, issue #3094: the routing weight belongs to the    */
+/* down projection, ahead of its store, and the later reduction must not  */
+/* apply it a second time.  READING: y = sum_i act*W2 in f32, one f32     */
 /* multiply by the pair's weight, one bf16 rounding; the row goes to the  */
 /* pair order ([T, K, H]) when row_to_pair is given.                     */
 /* ------------------------------------------------------------------ */
@@ -441,8 +441,8 @@ int oracle_combine(const void* expert_out, int eo_dtype, const float* w, const v
 /* ------------------------------------------------------------------ */
 /* a8: kMoeCombineGate                                                   */
 /* PR #509 "What changed" + review: combine with the shared-expert sigmoid */
-/* gate folded in, the gated shared term rounded through bf16 before it   */
-/* is added (the donor's bf16 double round).  READING: routed_scale is    */
+/* gate folded in; the gated shared term is rounded to bf16 and widened   */
+/* back before it is added (a double rounding).  READING: routed_scale is */
 /* accepted here too and applied to the routed sum before the add.        */
 /* ------------------------------------------------------------------ */
 

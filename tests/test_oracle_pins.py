@@ -9,10 +9,10 @@ transposed operand, a reordered sum, a fused multiply-add) fails one of them.
 
 Passages the checks follow (vllm.cpp pages):
   * issue #3094 "Row: BACKEND-ROCM-BF16-MOE": the numeric contract -- BF16
-    narrowing before activation, routing weight applied before the down result
+    narrowing of gate and up ahead of the activation, routing weight applied to the down result
     is stored, reduction without applying the weights twice;
   * PR #509 "MoE combine/gate ops": out = sigmoid(gl) * sd, weighted top-k sum
-    with optional shared term, the shared term rounded through bf16, sequential
+    with optional shared term, the shared term rounded to bf16 first, sequential
     K order with one store rounding and no contraction (review rework item 2),
     routed_scale applied to the routed sum before the shared term;
   * PR #509 "Honest gaps": the covered router is ungrouped softmax.
