@@ -44,9 +44,11 @@ constexpr int kThreadsGather = 320;  // + 4 warps that gather A rows
 constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK * 2;
 // bytes of the 227 KB per-block shared memory left for the stage ring after the
-// barriers, the schedule tables (2 x 4 KB) and the 1 KB alignment slack
-constexpr int kSmemBudget = 227 * 1024 - 11 * 1024;
+// barriers, the schedule tables (2 x 4 KB), the epilogue staging buffers
+// (4 x 4 KB) and the 1 KB alignment slack
+constexpr int kSmemBudget = 227 * 1024 - 11 * 1024 - 16 * 1024;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr int kStgBytes = 32 * 128;  // epilogue staging: 32 rows x 64 bf16 per warp
 
 enum Epi { EPI_GATEUP = 0, EPI_DOWN = 1, EPI_F32 = 2 };
 
@@ -82,7 +84,8 @@ struct Smem {
   static constexpr int B_BYTES = kBBytes;
   static constexpr int STAGE_A = 0;
   static constexpr int STAGE_B = kStages * A_BYTES;
-  static constexpr int BARS = STAGE_B + kStages * B_BYTES;
+  static constexpr int STAGE_EPI = STAGE_B + kStages * B_BYTES;   // 4 epilogue staging buffers
+  static constexpr int BARS = STAGE_EPI + 4 * kStgBytes;
   // full[kStages], empty[kStages], tfull[2], tempty[2], drain
   static constexpr int NBARS = 2 * kStages + 5;
   static constexpr int MISC = BARS + NBARS * 8;           // tmem slot, abort flag, scan scratch
@@ -459,68 +462,76 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const bool valid = row < t.row_end;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kN);
-      if (kEpi == EPI_GATEUP) {
+      if (kEpi == EPI_GATEUP || kEpi == EPI_DOWN) {
+        // bf16 outputs go out through a per-warp staging buffer: the warp's 32
+        // rows x 64 columns (128 B a row) are written to shared memory by row
+        // (16-byte pieces XOR-swizzled by row to spread the banks), then read
+        // back so that eight lanes store one row's 128 contiguous bytes: full
+        // 128-byte lines instead of 32 scattered 16-byte pieces per store.
         uint16_t* out = static_cast<uint16_t*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < kBnOut / 32; ++c) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
-          ptx::tmem_ld_32x32b_x32(taddr + kBnOut + c * 32, u);
-          ptx::tmem_ld_wait();
-          const int col = t.n0 + c * 32;
-          if (valid && col < p.N) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float a2[2];
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                // narrowing before the activation: gate and up are rounded to bf16 first
-                const float gz = bf16_round(__uint_as_float(g[j + h]));
-                const float uz = bf16_round(__uint_as_float(u[j + h]));
-                const float s = gz / (1.0f + __expf(-gz));
-                a2[h] = s * uz;
-              }
-              packed[j / 2] = pack_bf16x2(a2[0], a2[1]);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * p.N + col);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              if (col + v * 8 < p.N)
-                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                    packed[4 * v + 3]);
-          }
-        }
-      } else if (kEpi == EPI_DOWN) {
-        uint16_t* out = static_cast<uint16_t*>(p.out);
+        const uint32_t stg = sbase + S::STAGE_EPI + static_cast<uint32_t>(warp - 2) * kStgBytes;
         int dst_row = row;
         float wgt = 1.0f;
-        if (valid) {
+        if (kEpi == EPI_DOWN && valid) {
           if (p.row_to_pair) dst_row = __ldg(p.row_to_pair + row);
           if (p.pair_weight) wgt = __ldg(p.pair_weight + dst_row);
         }
 #pragma unroll 1
-        for (int c = 0; c < kBnOut / 32; ++c) {
-          uint32_t y[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, y);
-          ptx::tmem_ld_wait();
-          const int col = t.n0 + c * 32;
-          if (valid && col < p.N) {
-            uint32_t packed[16];
+        for (int c = 0; c < kBnOut / 64; ++c) {
+          uint32_t packed[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              // the routing weight: one f32 multiply, then the one bf16 rounding
-              const float a = p.pair_weight ? __fmul_rn(__uint_as_float(y[j]), wgt) : __uint_as_float(y[j]);
-              const float b = p.pair_weight ? __fmul_rn(__uint_as_float(y[j + 1]), wgt) : __uint_as_float(y[j + 1]);
-              packed[j / 2] = pack_bf16x2(a, b);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t g[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c * 64 + h * 32, g);
+            if (kEpi == EPI_GATEUP) {
+              uint32_t u[32];
+              ptx::tmem_ld_32x32b_x32(taddr + kBnOut + c * 64 + h * 32, u);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float a2[2];
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                  // narrowing before the activation: gate and up are rounded to bf16 first
+                  const float gz = bf16_round(__uint_as_float(g[j + q2]));
+                  const float uz = bf16_round(__uint_as_float(u[j + q2]));
+                  const float sl = gz / (1.0f + __expf(-gz));
+                  a2[q2] = sl * uz;
+                }
+                packed[h * 16 + j / 2] = pack_bf16x2(a2[0], a2[1]);
+              }
+            } else {
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                // the routing weight: one f32 multiply, then the one bf16 rounding
+                const float a = p.pair_weight ? __fmul_rn(__uint_as_float(g[j]), wgt)
+                                              : __uint_as_float(g[j]);
+                const float b = p.pair_weight ? __fmul_rn(__uint_as_float(g[j + 1]), wgt)
+                                              : __uint_as_float(g[j + 1]);
+                packed[h * 16 + j / 2] = pack_bf16x2(a, b);
+              }
             }
-            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(dst_row) * p.N + col);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              if (col + v * 8 < p.N)
-                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                    packed[4 * v + 3]);
           }
+          // row `lane` of the staging buffer, piece k at slot k ^ (lane & 7)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            ptx::st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4), packed[4 * k],
+                              packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+          __syncwarp();
+          const int col0 = t.n0 + c * 64;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {           // 4 rows per store instruction
+            const int r = i * 4 + (lane >> 3);     // row of the warp this lane stores
+            const int k = lane & 7;                // its 16-byte piece of that row
+            const int drow = __shfl_sync(0xffffffffu, dst_row, r);
+            const int rvalid = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
+            const uint4 v = ptx::ld_shared_v4(stg + r * 128 + ((k ^ (r & 7)) << 4));
+            const int col = col0 + k * 8;
+            if (rvalid && col < p.N)
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(drow) * p.N + col) = v;
+          }
+          __syncwarp();
         }
       } else {
         float* out = static_cast<float*>(p.out);
