@@ -217,16 +217,27 @@ int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
                                void* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 size_t moe_grouped_gemm_workspace_size(int P, int H, int I, int G);
 
-/* moe_set_gemm_pairing -- tile shape of the two grouped GEMMs above (not of
- * the gathered-A gate/up, which always runs single-CTA tiles).
- *   on != 0: CTA pairs (2-SM tcgen05.mma.cta_group::2, 256-row tiles; each SM
- *            of the pair stages 128 A rows and half of the weight tile)
- *   on == 0 (default): one CTA per 128-row tile (less padding on skewed
- *            expert loads, where most groups hold well under 256 rows)
- * Results are identical up to f32 accumulation order.  Process-wide, takes
- * effect at the next launch; returns the previous setting.  Not for use while
- * another thread is launching these GEMMs. */
-int moe_set_gemm_pairing(int on);
+/* moe_set_gemm_pairing -- tiling of the two grouped GEMMs above (the
+ * gathered-A gate/up always runs single-CTA tiles):
+ *   MOE_GEMM_SINGLE (default): one CTA per 128-row x N tile
+ *   MOE_GEMM_PAIR:   CTA pairs on 256-row tiles (2-SM tcgen05.mma.cta_group::2;
+ *                    each SM stages 128 A rows and half of the weight tile)
+ *   MOE_GEMM_MCAST:  clusters of two CTAs on the same 128 rows and two
+ *                    neighbouring N tiles; each loads half of the shared A tile
+ *                    and multicasts it to both (used when the GEMM has an even
+ *                    number of N tiles, otherwise single-CTA tiles)
+ *   MOE_GEMM_SPLIT:  two launches per call -- the whole 256-row
+ *                    blocks of every group on CTA pairs (no padding rows), then
+ *                    the remaining rows of each group on MCAST/single tiles
+ * Results are identical up to f32 accumulation order.  On a skewed expert load
+ * the single-CTA tiles are the fastest: their random mix of weight-bound and
+ * tensor-bound tiles keeps both HBM and the tensor cores busy, which the
+ * padding (PAIR) or the phase separation (SPLIT) of the others gives up.
+ * Process-wide, takes effect at the next launch; returns the previous mode
+ * (MOE_ERR_ARG for an unknown mode).  Not for use while another thread is
+ * launching these GEMMs. */
+enum { MOE_GEMM_SINGLE = 0, MOE_GEMM_PAIR = 1, MOE_GEMM_MCAST = 2, MOE_GEMM_SPLIT = 3 };
+int moe_set_gemm_pairing(int mode);
 
 /* ------------------------------------------------------------------------
  * moe_combine -- kMoeCombine of [PR509].  Per output element, sequentially:

@@ -185,9 +185,13 @@ def moe_grouped_gemm_workspace_size(P, H, I, G) -> int:
     return lib().moe_grouped_gemm_workspace_size(P, H, I, G)
 
 
-def moe_set_gemm_pairing(on: bool) -> bool:
-    """CTA-pair (2-SM) tiles for the grouped GEMMs on/off; returns the previous setting."""
-    return bool(lib().moe_set_gemm_pairing(1 if on else 0))
+GEMM_SINGLE, GEMM_PAIR, GEMM_MCAST, GEMM_SPLIT = 0, 1, 2, 3
+
+
+def moe_set_gemm_pairing(mode: int) -> int:
+    """Tiling of the grouped GEMMs (GEMM_SINGLE / GEMM_PAIR / GEMM_MCAST / GEMM_SPLIT);
+    returns the previous mode."""
+    return _check(lib().moe_set_gemm_pairing(int(mode)))
 
 
 def moe_combine(expert_out, eo_dtype, w, shared, sh_dtype, routed_scale, T, K, H, out, out_dtype,

@@ -64,6 +64,7 @@ struct Params {
   int a_rows;
   const int32_t* row_gather;     // gathered A: product row r reads row row_gather[r] / gather_div
   int gather_div;
+  int split;                     // 0 whole groups; 1 their leading 256-row blocks; 2 the rest
   void* out;
   const float* pair_weight;      // down: [P] by destination row, or null
   const int32_t* row_to_pair;    // down: destination row, or null
@@ -99,7 +100,7 @@ struct Smem {
 //   kN      MMA N (accumulator columns per tile)
 //   kPair   CTA pair (cta_group::2): M = 256 per tile, each CTA holds 128 A rows
 //           and half of B, and one thread of the even CTA issues the MMAs
-template <int kN, int kEpi, bool kGatherA, bool kPair>
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false>
 struct Cfg {
   static constexpr int kTileM = kPair ? 2 * BM : BM;              // product rows per tile
   static constexpr int kBRowsCta = kPair ? kN / 2 : kN;           // B rows held per CTA
@@ -117,8 +118,19 @@ struct Tile {
   int g, row0, row_end, n0;
 };
 
+// rows of group g this launch covers: all of them, the leading whole 256-row
+// blocks (split 1) or the remainder after them (split 2)
+__device__ __forceinline__ void group_range(const int* goff, int g, int split, int& lo, int& hi) {
+  lo = goff[g];
+  hi = goff[g + 1];
+  const int head = ((hi - lo) / 256) * 256;
+  if (split == 1) hi = lo + head;
+  else if (split == 2) lo += head;
+}
+
 __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, const int* goff,
-                                            int G, int n_tiles, int bn_out, int tile_m) {
+                                            int G, int n_tiles, int bn_out, int tile_m,
+                                            int split) {
   int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -126,10 +138,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, con
   }
   int local = tile - tile_start[lo];
   int m = local / n_tiles, n = local - m * n_tiles;
+  int r0, r1;
+  group_range(goff, lo, split, r0, r1);
   Tile t;
   t.g = lo;
-  t.row0 = goff[lo] + m * tile_m;
-  t.row_end = goff[lo + 1];
+  t.row0 = r0 + m * tile_m;
+  t.row_end = r1;
   t.n0 = n * bn_out;
   return t;
 }
@@ -175,11 +189,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(f32_to_bf16_bits(hi)) << 16);
 }
 
-template <int kN, int kEpi, bool kGatherA, bool kPair>
-__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair>::kThreadsT, 1)
+// kMcastA: a cluster of two CTAs computes the same 128 A rows against two
+// neighbouring N tiles; each CTA loads half of the A tile and multicasts it to
+// both, and each stage is released only when both MMAs are done with it.
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA>
+__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA>::kThreadsT, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA>;
+  constexpr bool kCluster = kPair || kMcastA;
   using S = typename C::S;
   constexpr int kStages = C::kStages;
   constexpr int kNThreads = C::kThreadsT;
@@ -208,10 +226,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // pair: rank 0 (even CTA) issues the MMAs and owns the stage barriers; both load
-  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
-  const bool leader = rank == 0;
-  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int n_units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const uint32_t rank = kCluster ? ptx::cluster_ctarank() : 0u;
+  const bool leader = !kPair || rank == 0;
+  const int unit = kCluster ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = kCluster ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto bar_full = [&](int s) { return ptx::smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return ptx::smem_u32(bars + kStages + s); };
   auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + a); };
@@ -223,7 +241,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar_full(s), kGatherA ? 1 + BM : 1);
-      ptx::mbar_init(bar_empty(s), 1);
+      ptx::mbar_init(bar_empty(s), kMcastA ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_tfull(a), 1);
@@ -252,13 +270,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   for (int g = threadIdx.x; g <= G; g += kNThreads)
     goff[g] = p.group_offsets ? __ldg(p.group_offsets + g) : (g == 0 ? 0 : p.P);
   __syncthreads();
-  const int n_tiles = (p.N + kBnOut - 1) / kBnOut;
+  // schedule units along N: one tile, or (multicast) a pair of neighbouring tiles
+  const int n_tiles = ((p.N + kBnOut - 1) / kBnOut) / (kMcastA ? 2 : 1);
+  constexpr int kBnSched = kMcastA ? 2 * kBnOut : kBnOut;
   const int chunk = (G + kNThreads - 1) / kNThreads;
   const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
   const int g_hi = min(G, g_lo + chunk);
   int local = 0;
   for (int g = g_lo; g < g_hi; ++g) {
-    int rows = goff[g + 1] - goff[g];
+    int r0, r1;
+    group_range(goff, g, p.split, r0, r1);
+    const int rows = r1 - r0;
     local += rows > 0 ? ((rows + kTileM - 1) / kTileM) * n_tiles : 0;
   }
   int incl = local;
@@ -278,17 +300,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   int run = warp_base + incl - local;
   for (int g = g_lo; g < g_hi; ++g) {
     tile_start[g] = run;
-    int rows = goff[g + 1] - goff[g];
+    int r0, r1;
+    group_range(goff, g, p.split, r0, r1);
+    const int rows = r1 - r0;
     run += rows > 0 ? ((rows + kTileM - 1) / kTileM) * n_tiles : 0;
   }
   if (threadIdx.x == 0) tile_start[G] = total;
   ptx::tc_fence_before();
   __syncthreads();
-  if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
+  if (kCluster) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
-  const int row_off = static_cast<int>(rank) * BM;  // this CTA's A rows inside a tile
+  const int row_off = kPair ? static_cast<int>(rank) * BM : 0;  // this CTA's A rows in a tile
+  const int n_off = kMcastA ? static_cast<int>(rank) * kBnOut : 0;  // this CTA's N tile in a unit
 
   if (kGatherA && warp >= 6) {
     // ------------------------------------------------------------ A-row gatherers
@@ -303,7 +328,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int pending = 0;
     bool ok = true;
     for (int tile = unit; ok && tile < total; tile += n_units) {
-      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
+      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split);
+      t.n0 += n_off;
       const int r = min(t.row0 + row_off + i, p.P - 1);  // rows past the group are masked later
       const int srow = __ldg(p.row_gather + r) / p.gather_div;
       const bool in = srow >= 0 && srow < p.a_rows;
@@ -347,7 +373,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int issued = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
+        Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split);
+        t.n0 += n_off;
         // B rows of this CTA: unpaired, the whole tile (gate/up: gate half, then
         // up half); paired, rank 0 holds the first half of the N columns
         // (gate rows) and rank 1 the second (up rows)
@@ -377,7 +404,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           const uint32_t fb = bar_full(stage);
           ptx::mbar_arrive_expect_tx(fb, kStageTx);
-          if (!kGatherA) ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0 + row_off, fb);
+          if (kMcastA) {
+            // this CTA's half of the A tile (64 rows), into both CTAs of the pair
+            ptx::tma_load_2d_mcast(sa + rank * (A_BYTES / 2), &tmA, kb * BK,
+                                   t.row0 + static_cast<int>(rank) * (BM / 2), fb, 3);
+          } else if (!kGatherA) {
+            ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0 + row_off, fb);
+          }
           if (kEpi == EPI_GATEUP) {
             ptx::tma_load_2d(sb, &tmB, kb * BK, brow0, fb);
             ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow1, fb);
@@ -432,6 +465,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           any = true;
           if (kPair) ptx::mma_commit_pair(bar_empty(stage), 3);
+          else if (kMcastA) ptx::mma_commit_mcast(bar_empty(stage), 3);  // frees it in both CTAs
           else ptx::mma_commit(bar_empty(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -453,7 +487,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         kPair ? ptx::mapa_shared(bar_tempty(0), 0) : 0u;  // + 8 * acc for buffer acc
     int it = 0;
     for (int tile = unit; tile < total; tile += n_units, ++it) {
-      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
+      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split);
+      t.n0 += n_off;
       const int acc = it & 1;
       const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
       if (!wait_bar(bar_tfull(acc), aphase, abort_flag, p.status)) break;
@@ -570,7 +605,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 
   __syncthreads();
-  if (kPair) ptx::cluster_sync();  // the peer may still read this CTA's smem or TMEM until here
+  if (kCluster) ptx::cluster_sync();  // the peer may still use this CTA's smem or TMEM until here
   if (warp == 1) {
     ptx::tc_fence_after();
     if (kPair) ptx::tmem_dealloc2(tmem_base, kTmemCols);
@@ -630,11 +665,12 @@ int num_sms() {
 
 // tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
 // grid is that many CTAs (pairs when paired), capped at the SM count
-template <int kN, int kEpi, bool kGatherA = false, bool kPair = false>
+template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair>;
-  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA>;
+  constexpr bool kCluster = kPair || kMcastA;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA>;
   const int smem = C::S::ALLOC;
   static int configured_dev[64] = {};
   int dev = 0;
@@ -652,7 +688,7 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.x = kCluster ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -663,8 +699,8 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
   static int max_units_dev[64] = {};
   int max_units = (dev >= 0 && dev < 64) ? max_units_dev[dev] : 0;
   if (max_units <= 0) {
-    max_units = kPair ? num_sms() / 2 : num_sms();
-    if (kPair) {
+    max_units = kCluster ? num_sms() / 2 : num_sms();
+    if (kCluster) {
       int clusters = 0;
       cfg.gridDim = dim3(static_cast<unsigned>(2 * max_units), 1, 1);
       if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0)
@@ -680,7 +716,7 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
   DeviceDiag diag = device_diag();
   p.status = diag.status;
   p.launches = diag.launches;
-  cfg.gridDim = dim3(static_cast<unsigned>(kPair ? 2 * units : units), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(kCluster ? 2 * units : units), 1, 1);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -708,8 +744,8 @@ long long tile_bound(int P, int G, int N, int bn_out, int tile_m = BM) {
   return mt * ((N + bn_out - 1) / bn_out);
 }
 
-// CTA-pair tiles for the grouped GEMMs (process-wide; see moe_set_gemm_pairing)
-std::atomic<int> g_pairing{0};
+// tiling of the grouped GEMMs (process-wide; see moe_set_gemm_pairing)
+std::atomic<int> g_pairing{MOE_GEMM_SINGLE};
 
 }  // namespace gemm
 
@@ -745,9 +781,11 @@ using namespace moe::gemm;
 
 extern "C" size_t moe_grouped_gemm_workspace_size(int, int, int, int) { return 0; }
 
-extern "C" int moe_set_gemm_pairing(int on) {
+extern "C" int moe_set_gemm_pairing(int mode) {
   clear_error();
-  return g_pairing.exchange(on ? 1 : 0);
+  if (mode < MOE_GEMM_SINGLE || mode > MOE_GEMM_SPLIT)
+    return set_error(MOE_ERR_ARG, "moe_set_gemm_pairing: mode %d is not 0, 1, 2 or 3", mode);
+  return g_pairing.exchange(mode);
 }
 
 extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
@@ -767,13 +805,16 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   if (a_row_gather && (a_rows < 1 || gather_div < 1))
     return set_error(MOE_ERR_ARG, "%s: gathering needs a_rows >= 1 and gather_div >= 1", op);
   if (P == 0) return MOE_OK;
+  const int mode = g_pairing.load(std::memory_order_relaxed);
+  const bool mcast = !a_row_gather && (mode == MOE_GEMM_MCAST || mode == MOE_GEMM_SPLIT) &&
+                     ((I + 127) / 128) % 2 == 0;
   CUtensorMap ta, tb;
   if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, 128, op, "w13")) !=
       MOE_OK)
     return rc;
   if (a_row_gather) {
     ta = tb;  // unused: the gatherer warps read A rows directly
-  } else if ((rc = make_tmap(&ta, a_bf16, P, H, BM, op, "a")) != MOE_OK) {
+  } else if ((rc = make_tmap(&ta, a_bf16, P, H, mcast ? BM / 2 : BM, op, "a")) != MOE_OK) {
     return rc;
   }
   Params p{};
@@ -793,8 +834,19 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a_row_gather)
     return launch<256, EPI_GATEUP, true>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
-  if (g_pairing.load(std::memory_order_relaxed))
+  if (mode == MOE_GEMM_PAIR)
     return launch<256, EPI_GATEUP, false, true>(op, ta, tb, p, tile_bound(P, G, I, 128, 2 * BM), s);
+  if (mode == MOE_GEMM_SPLIT) {
+    // whole 256-row blocks on CTA pairs (no padding), the rest on 128-row tiles
+    CUtensorMap ta_pair;
+    if ((rc = make_tmap(&ta_pair, a_bf16, P, H, BM, op, "a")) != MOE_OK) return rc;
+    p.split = 1;
+    rc = launch<256, EPI_GATEUP, false, true>(op, ta_pair, tb, p, tile_bound(P, G, I, 128, 2 * BM), s);
+    if (rc != MOE_OK) return rc;
+    p.split = 2;
+  }
+  if (mcast)
+    return launch<256, EPI_GATEUP, false, false, true>(op, ta, tb, p, tile_bound(P, G, I, 256), s);
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
@@ -812,8 +864,11 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   if (!group_offsets && G != 1)
     return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
   if (P == 0) return MOE_OK;
+  const int mode = g_pairing.load(std::memory_order_relaxed);
+  const bool mcast =
+      (mode == MOE_GEMM_MCAST || mode == MOE_GEMM_SPLIT) && ((H + 255) / 256) % 2 == 0;
   CUtensorMap ta, tb;
-  if ((rc = make_tmap(&ta, act_bf16, P, I, BM, op, "act")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&ta, act_bf16, P, I, mcast ? BM / 2 : BM, op, "act")) != MOE_OK) return rc;
   if ((rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) != MOE_OK)
     return rc;
   Params p{};
@@ -829,7 +884,17 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   p.row_to_pair = row_to_pair;
   p.kid = MOE_KID_GEMM_DOWN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (g_pairing.load(std::memory_order_relaxed))
+  if (mode == MOE_GEMM_PAIR)
     return launch<256, EPI_DOWN, false, true>(op, ta, tb, p, tile_bound(P, G, H, 256, 2 * BM), s);
+  if (mode == MOE_GEMM_SPLIT) {
+    CUtensorMap ta_pair;
+    if ((rc = make_tmap(&ta_pair, act_bf16, P, I, BM, op, "act")) != MOE_OK) return rc;
+    p.split = 1;
+    rc = launch<256, EPI_DOWN, false, true>(op, ta_pair, tb, p, tile_bound(P, G, H, 256, 2 * BM), s);
+    if (rc != MOE_OK) return rc;
+    p.split = 2;
+  }
+  if (mcast)
+    return launch<256, EPI_DOWN, false, false, true>(op, ta, tb, p, tile_bound(P, G, H, 512), s);
   return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
 }

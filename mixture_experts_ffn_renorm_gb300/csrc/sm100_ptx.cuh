@@ -121,6 +121,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// multicast form: the box lands at offset `dst` in the shared memory of every
+// CTA in cta_mask, and each of them counts the bytes on its barrier at `bar`
+__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                                  uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
 // CTA-pair form: the box lands in this CTA's shared memory and its bytes are
 // counted on `bar`, which may be the peer CTA's barrier (a shared::cluster
 // address, e.g. from mapa), so one barrier can collect both halves of a stage
@@ -217,6 +228,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// the mbarrier at this offset in every CTA of cta_mask arrives once every
+// previously issued (single-CTA) tcgen05 op of this thread is done
+__device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 

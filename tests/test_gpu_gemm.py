@@ -28,9 +28,12 @@ def _lib():
     assert m.moe_device_status() == 0
 
 
-@pytest.fixture(params=[True, False], ids=["pair", "single"])
+@pytest.fixture(params=[m.GEMM_SINGLE, m.GEMM_MCAST, m.GEMM_PAIR, m.GEMM_SPLIT],
+                ids=["single", "mcast", "pair", "split"])
 def pairing(request):
-    """Both tilings of the grouped GEMMs: CTA pairs (2-SM, 256-row tiles) and single CTAs."""
+    """Every tiling of the grouped GEMMs: single CTAs (the default), A-multicast
+    clusters, CTA pairs (2-SM, 256-row tiles), and whole 256-row blocks on CTA
+    pairs with the rest on A-multicast clusters."""
     prev = m.moe_set_gemm_pairing(request.param)
     yield request.param
     m.moe_set_gemm_pairing(prev)
@@ -48,8 +51,10 @@ def _case(sizes, H, I, seed):
 
 
 SHAPES = [
-    # group sizes, H, I
+    # group sizes, H, I  (I / 128 and H / 256 even or odd: multicast or its fallback)
     ([4], 64, 32),
+    ([3, 200, 0, 77], 512, 256),
+    ([600, 5, 256, 255, 513], 256, 256),
     ([0, 1, 130, 129, 40], 256, 192),
     ([300], 512, 128),
     ([1, 1, 1, 1, 1, 1, 1, 1], 2048, 768),
@@ -67,7 +72,7 @@ def test_gateup_silu(sizes, H, I, pairing):
     before = launches()
     m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I, G,
                                         act)
-    assert launched_since(before, "gemm_gateup") == 1
+    assert launched_since(before, "gemm_gateup") == (2 if pairing == m.GEMM_SPLIT else 1)
     assert m.moe_device_status() == 0
     assert_gemm_close(to_host(act), want, "gate/up")
 
@@ -108,7 +113,7 @@ def test_down_weight_scatter(sizes, H, I, pairing):
         m.moe_grouped_gemm_down_bf16(to_dev(act), to_dev(W2), to_dev(off),
                                      None if pw is None else to_dev(pw),
                                      None if rp is None else to_dev(rp), P, I, H, G, out)
-        assert launched_since(before, "gemm_down") == 1
+        assert launched_since(before, "gemm_down") == (2 if pairing == m.GEMM_SPLIT else 1)
         assert m.moe_device_status() == 0
         assert_gemm_close(to_host(out), want, "down")
 

@@ -58,7 +58,7 @@ def test_tiny_layer_every_element():
     out = to_host(blk.forward(to_dev(d["x"])))
     for k in ("route_logits", "route_topk", "permute_place", "combine_gate"):
         assert launched_since(before, k) == 1, k
-    assert launched_since(before, "gemm_gateup") == 2 and launched_since(before, "gemm_down") == 2
+    assert launched_since(before, "gemm_gateup") >= 2 and launched_since(before, "gemm_down") >= 2
     want, ids, w = _oracle_tokens(cfg, d, range(cfg.T))
     assert np.array_equal(to_host(blk.topk_ids), ids)
     nmse, rel = nmse_maxrel(bf16_to_f64(out), bf16_to_f64(want))
@@ -179,25 +179,25 @@ def test_materialised_x_perm_path_matches_gather_path():
     assert np.array_equal(to_host(blk.x_perm), d["x"][sp // cfg.K])
 
 
-def test_pair_and_single_cta_tiles_agree_on_prefill():
-    # the two GEMM tilings differ only in f32 accumulation order
+def test_gemm_tilings_agree_on_prefill():
+    # the GEMM tilings differ only in f32 accumulation order
     cfg = W.PREFILL
     d = W.layer_inputs(cfg)
     blk = _block(cfg, d)
     x = to_dev(d["x"])
-    prev = m.moe_set_gemm_pairing(True)
+    res = {}
+    prev = m.moe_set_gemm_pairing(m.GEMM_SINGLE)
     try:
-        a = to_host(blk.forward(x)).copy()
-        act_a = to_host(blk.act).copy()
-        m.moe_set_gemm_pairing(False)
-        b = to_host(blk.forward(x))
-        act_b = to_host(blk.act)
+        for mode in (m.GEMM_SINGLE, m.GEMM_PAIR, m.GEMM_MCAST, m.GEMM_SPLIT):
+            m.moe_set_gemm_pairing(mode)
+            res[mode] = (to_host(blk.forward(x)).copy(), to_host(blk.act).copy())
     finally:
         m.moe_set_gemm_pairing(prev)
-    nmse, _ = nmse_maxrel(bf16_to_f64(act_a), bf16_to_f64(act_b))
-    assert nmse <= 1e-6, nmse
-    nmse, _ = nmse_maxrel(bf16_to_f64(a), bf16_to_f64(b))
-    assert nmse <= 1e-6, nmse
+    ref_out, ref_act = res[m.GEMM_SINGLE]
+    for mode in (m.GEMM_PAIR, m.GEMM_MCAST, m.GEMM_SPLIT):
+        out, act = res[mode]
+        assert nmse_maxrel(bf16_to_f64(act), bf16_to_f64(ref_act))[0] <= 1e-6
+        assert nmse_maxrel(bf16_to_f64(out), bf16_to_f64(ref_out))[0] <= 1e-6
 
 
 def test_host_batches_pipeline_matches_eager():
