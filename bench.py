@@ -35,9 +35,10 @@ METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM TFLOP/s and combine GB/s v
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def recorded_traffic():
-    """DRAM traffic of one gate/up GEMM launch from the committed ncu summary,
-    or None when the kernel sources have changed since it was captured."""
+def recorded_traffic(workload):
+    """DRAM traffic of one gate/up GEMM launch on `workload` from the committed
+    ncu summary, or None when it covers another workload or the kernel
+    sources have changed since it was captured."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "gemm_gateup_traffic.txt")
@@ -52,7 +53,7 @@ def recorded_traffic():
     for f in ("moe_gemm.cu", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "mixture_experts_ffn_renorm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    if kv.get("sources_sha256") != h.hexdigest():
+    if kv.get("sources_sha256") != h.hexdigest() or kv.get("workload") != workload:
         return None
     return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
 
@@ -364,7 +365,9 @@ def run_ours(args):
         blk.forward(x_dev)
     torch.cuda.synchronize()
 
-    # ---------------- timed: device-resident inputs
+    # ---------------- timed: device-resident inputs, whole steps (no events
+    # between the kernels of a step, so each may start under programmatic
+    # dependent launch while its predecessor drains)
     counts0 = m.moe_launch_counts()
     step_marks = []
     t_start = torch.cuda.Event(enable_timing=True)
@@ -376,9 +379,11 @@ def run_ours(args):
         for _ in range(args.steps):
             if flush is not None:
                 flush.zero_()
-            marks = []
-            blk.forward(x_dev, marks=marks)
-            step_marks.append(marks)
+                marks = []
+                blk.forward(x_dev, marks=marks, stages=False)
+                step_marks.append(marks)
+            else:
+                blk.forward(x_dev)
         t_end.record()
         torch.cuda.synchronize()
         barrier(ws)
@@ -393,11 +398,18 @@ def run_ours(args):
 
     value = dp.aggregate_tokens_per_s(cfg.T, ws, ms)
 
+    # ---------------- per-stage breakdown: the same steps with an event after
+    # every stage (reported as components; not the headline)
     stage_ms = {}
-    for marks in step_marks:
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        marks = []
+        blk.forward(x_dev, marks=marks)
         for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
-            stage_ms.setdefault(name, []).append(a.elapsed_time(b))
-    stage_avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+            stage_ms.setdefault(name, []).append((a, b))
+    torch.cuda.synchronize()
+    stage_avg = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in stage_ms.items()}
 
     # ---------------- end to end through the public API with host buffers:
     # every step copies its tokens in from pinned host memory and its output
@@ -417,40 +429,62 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
     e2e_value = ws * cfg.T / (e2e_ms / 1000.0)
 
-    # ---------------- roofline of the dominant kernel (the gate/up GEMM)
+    # ---------------- roofline of the dominant kernel (the gate/up GEMM):
+    # tensor-bound when its FLOPs take longer at peak than its bytes at HBM
+    # peak (the prefill layer), HBM-bound otherwise (decode, the large layer)
     pk, pk_src = peaks()
     P = cfg.T * cfg.K
+    counts = np.diff(blk.expert_offsets.cpu().numpy())
+    touched = int((counts > 0).sum())
     flop_gateup = 2.0 * P * cfg.H * 2 * cfg.I
     flop_down = 2.0 * P * cfg.I * cfg.H
+    bytes_gateup = touched * 2 * cfg.I * cfg.H * 2 + P * cfg.H * 2 + P * cfg.I * 2
+    bytes_down = touched * cfg.H * cfg.I * 2 + P * cfg.I * 2 + P * cfg.H * 2 + P * 4
     t_gu = stage_avg["gemm_gateup"] / 1000.0
     t_dn = stage_avg["gemm_down"] / 1000.0
-    achieved = flop_gateup / t_gu / 1e12
+    tensor_bound = flop_gateup / (pk["bf16_tflops"] * 1e12) >= bytes_gateup / (pk["hbm_gbs"] * 1e9)
+    kname = "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)"
+    if tensor_bound:
+        achieved = flop_gateup / t_gu / 1e12
+        roofline = {"kernel": kname, "bound": "tensor", "achieved": achieved,
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / pk["bf16_tflops"],
+                    "peak_source": f"{pk_src} bf16 dense (burst)",
+                    "traffic": recorded_traffic(cfg.name),
+                    "traffic_unit": "bytes per launch (ncu dram read + write)",
+                    "algorithmic_flop_per_launch": flop_gateup}
+    else:
+        achieved = bytes_gateup / t_gu / 1e9
+        roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
+                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                    "peak_source": f"{pk_src} HBM copy bandwidth",
+                    "traffic": recorded_traffic(cfg.name),
+                    "traffic_unit": "bytes per launch (ncu dram read + write)",
+                    "algorithmic_bytes_per_launch": bytes_gateup,
+                    "touched_experts": touched}
     comb_bytes = P * cfg.H * 2 + cfg.T * cfg.H * 2
     if cfg.I_shared:
         comb_bytes += cfg.T * cfg.H * 2 + cfg.T * 4
-    roofline = {"kernel": "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)",
-                "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                "peak_source": f"{pk_src} bf16 dense (burst)", "traffic": recorded_traffic(),
-                "traffic_unit": "bytes per launch (ncu dram read + write)",
-                "algorithmic_flop_per_launch": flop_gateup}
     components = {
         "ms": stage_avg,
-        "gemm_gateup_tflops": achieved,
+        "gemm_gateup_tflops": flop_gateup / t_gu / 1e12,
+        "gemm_gateup_gbs": bytes_gateup / t_gu / 1e9,
         "gemm_down_tflops": flop_down / t_dn / 1e12,
-        "gemm_down_frac": flop_down / t_dn / 1e12 / pk["bf16_tflops"],
+        "gemm_down_gbs": bytes_down / t_dn / 1e9,
+        "gemm_down_frac": (flop_down / t_dn / 1e12 / pk["bf16_tflops"] if tensor_bound
+                           else bytes_down / t_dn / 1e9 / pk["hbm_gbs"]),
         "combine_gbs": comb_bytes / (stage_avg["combine"] / 1000.0) / 1e9,
         "combine_frac_hbm": comb_bytes / (stage_avg["combine"] / 1000.0) / 1e9 / pk["hbm_gbs"],
         "route_gbs": (cfg.T * cfg.H * 2 + cfg.E * cfg.H * 2) / (stage_avg["route"] / 1000.0) / 1e9,
         "permute_gbs": (2 * P * cfg.H * 2 + P * 16) / (stage_avg["permute"] / 1000.0) / 1e9,
         "hbm_peak_gbs": pk["hbm_gbs"],
+        "stages_sum_ms": sum(stage_avg.values()),
     }
     cg = combine_gate_workload(dev)
     cg["frac_hbm"] = cg["gbs"] / pk["hbm_gbs"]
     components["combine_gate_workload"] = cg
-    counts = np.diff(blk.expert_offsets.cpu().numpy())
     components["expert_load"] = {"max": int(counts.max()), "mean": float(counts.mean()),
-                                 "min": int(counts.min())}
+                                 "min": int(counts.min()), "touched": touched}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -464,7 +498,9 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded normal inputs and weights, Zipf-skewed router bias)",
+            "data": "synthetic (seeded normal inputs and weights, "
+                    + (f"Zipf({cfg.zipf_s})-skewed router bias)" if cfg.zipf_s
+                       else "unbiased router)"),
             "config": config_dict(cfg, ws),
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": int(cfg.T * cfg.H * 2),

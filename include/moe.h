@@ -73,7 +73,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 3 */
+int moe_abi_version(void);  /* 4 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -239,6 +239,17 @@ size_t moe_grouped_gemm_workspace_size(int P, int H, int I, int G);
 enum { MOE_GEMM_SINGLE = 0, MOE_GEMM_PAIR = 1, MOE_GEMM_MCAST = 2, MOE_GEMM_SPLIT = 3 };
 int moe_set_gemm_pairing(int mode);
 
+/* moe_set_pdl -- programmatic dependent launch for every kernel of the
+ * library (enable = 1, the default) or plain stream order (0).  With it on,
+ * each kernel is allowed to start while the previous kernel in the same
+ * stream is still running: its CTAs do their set-up (barrier init, TMEM
+ * allocation, descriptor prefetch) early and then wait, on the device, until
+ * that kernel has completed before they read or write global memory, so the
+ * results are the same either way and only the gaps between kernels shrink.
+ * Process-wide, takes effect at the next launch; returns the previous
+ * setting (MOE_ERR_ARG unless enable is 0 or 1). */
+int moe_set_pdl(int enable);
+
 /* ------------------------------------------------------------------------
  * moe_combine -- kMoeCombine of [PR509].  Per output element, sequentially:
  *   acc = +0.0f
@@ -312,6 +323,7 @@ enum {
   MOE_KID_COMBINE = 8,
   MOE_KID_COMBINE_GATE = 9,
   MOE_KID_SHARED_GATE = 10,
+  MOE_KID_GATE_SIGMOID = 11,  /* the sigmoid pre-pass of the gate ops (workspace given) */
   MOE_KID_COUNT = 16
 };
 int moe_device_status(int* status_out, int clear);

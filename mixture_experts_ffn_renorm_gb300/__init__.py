@@ -24,7 +24,7 @@ STATUS_TIMEOUT, STATUS_BAD_ID = 1, 2
 KID = {
     "route_logits": 0, "route_topk": 1, "permute_count": 2, "permute_scan": 3,
     "permute_place": 4, "permute_gather": 5, "gemm_gateup": 6, "gemm_down": 7, "combine": 8,
-    "combine_gate": 9, "shared_gate": 10,
+    "combine_gate": 9, "shared_gate": 10, "gate_sigmoid": 11,
 }
 KID_COUNT = 16
 
@@ -34,7 +34,7 @@ EXPORTS = (
     "moe_grouped_gemm_gateup_silu_bf16",
     "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
-    "moe_set_gemm_pairing", "moe_gate_workspace_size",
+    "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl",
 )
 
 
@@ -65,6 +65,7 @@ _SIGS = {
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
     "moe_set_gemm_pairing": ([_I], _I),
+    "moe_set_pdl": ([_I], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
     "moe_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I, _P, _SZ, _P], _I),
     "shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I, _P, _SZ, _P], _I),
@@ -192,6 +193,12 @@ def moe_set_gemm_pairing(mode: int) -> int:
     """Tiling of the grouped GEMMs (GEMM_SINGLE / GEMM_PAIR / GEMM_MCAST / GEMM_SPLIT);
     returns the previous mode."""
     return _check(lib().moe_set_gemm_pairing(int(mode)))
+
+
+def moe_set_pdl(enable: bool) -> bool:
+    """Programmatic dependent launch on (default) or off for every kernel;
+    returns the previous setting."""
+    return bool(_check(lib().moe_set_pdl(1 if enable else 0)))
 
 
 def moe_combine(expert_out, eo_dtype, w, shared, sh_dtype, routed_scale, T, K, H, out, out_dtype,

@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe_common.cuh"
@@ -16,6 +17,7 @@ __device__ unsigned long long g_launches[MOE_KID_COUNT];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_diag_mu;
+std::atomic<int> g_pdl{1};
 moe::DeviceDiag g_diag[kMaxDevices];
 bool g_diag_ready[kMaxDevices] = {};
 }  // namespace
@@ -52,6 +54,8 @@ DeviceDiag device_diag() {
   return g_diag[dev];
 }
 
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
 int check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
@@ -65,7 +69,14 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_msg; }
 
-int moe_abi_version(void) { return 3; }
+int moe_abi_version(void) { return 4; }
+
+int moe_set_pdl(int enable) {
+  moe::clear_error();
+  if (enable != 0 && enable != 1)
+    return moe::set_error(MOE_ERR_ARG, "moe_set_pdl: enable must be 0 or 1, got %d", enable);
+  return g_pdl.exchange(enable);
+}
 
 int moe_device_status(int* status_out, int clear) {
   moe::clear_error();

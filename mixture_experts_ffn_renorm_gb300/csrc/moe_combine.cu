@@ -130,6 +130,8 @@ combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
                int H, void* __restrict__ out, unsigned long long* launches, int kid) {
   (void)gl;
   count_launch(launches, kid);
+  grid_dep_wait();
+  grid_dep_launch();
   const int ipr = H / kVec;                         // items per token row
   const long long item = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   if (item >= static_cast<long long>(T) * ipr) return;
@@ -152,7 +154,11 @@ combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
 // full warps, while the first slice's loads are in flight.
 // sigma(gl[t]) for every token, one per thread (full warps), into s_out[T]
 __global__ void __launch_bounds__(kThreads)
-gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_out) {
+gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_out,
+                    unsigned long long* launches) {
+  count_launch(launches, MOE_KID_GATE_SIGMOID);
+  grid_dep_wait();
+  grid_dep_launch();
   const int t = blockIdx.x * kThreads + threadIdx.x;
   if (t < T) s_out[t] = sigmoid_cr(__ldg(gl + t));
 }
@@ -165,6 +171,8 @@ gate_stream_kernel(const void* __restrict__ eo, const float* __restrict__ w,
                    const void* __restrict__ sh, const float* __restrict__ sig, float rs, int T,
                    int K, int H, void* __restrict__ out, unsigned long long* launches, int kid) {
   count_launch(launches, kid);
+  grid_dep_wait();
+  grid_dep_launch();
   const int ipr = H / kVec;
   const long long item = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   if (item >= static_cast<long long>(T) * ipr) return;
@@ -189,6 +197,8 @@ gate_kernel(const void* __restrict__ eo, const float* __restrict__ w,
             const void* __restrict__ sh, const float* __restrict__ gl, float rs, int T, int K,
             int H, void* __restrict__ out, unsigned long long* launches, int kid) {
   count_launch(launches, kid);
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float s_gate[kThreads * kGateIters + 1];
   const int ipr = H / kVec;
   const long long n_items = static_cast<long long>(T) * ipr;
@@ -311,9 +321,10 @@ int launch(const char* op, KernelFn fn, const void* eo, const float* w, const vo
       fused_sigmoid ? static_cast<long long>(kThreads) * kGateIters : kThreads;
   const long long blocks = (items + per_block - 1) / per_block;
   if (blocks > 0x7fffffffLL) return set_error(MOE_ERR_ARG, "%s: T*H too large", op);
-  fn<<<static_cast<unsigned>(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      eo, w, sh, gl, rs, T, K, H, out, diag.launches, kid);
-  return check_launch(op);
+  return launch_status(launch_kernel(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                                     static_cast<cudaStream_t>(stream), nullptr, 0, eo, w, sh,
+                                     gl, rs, T, K, H, out, diag.launches, kid),
+                       op);
 }
 
 // sigmoids of all T tokens into the workspace (then the stream reads them)
@@ -327,9 +338,10 @@ int precompute_sigmoids(const char* op, const float* gl, int T, void* workspace,
   if (reinterpret_cast<uintptr_t>(workspace) & 15u)
     return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
   float* s_out = static_cast<float*>(workspace);
-  gate_sigmoid_kernel<<<(T + kThreads - 1) / kThreads, kThreads, 0,
-                        static_cast<cudaStream_t>(stream)>>>(gl, T, s_out);
-  int rc = check_launch(op);
+  int rc = launch_status(launch_kernel(gate_sigmoid_kernel, dim3((T + kThreads - 1) / kThreads),
+                                       dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+                                       nullptr, 0, gl, T, s_out, device_diag().launches),
+                         op);
   if (rc == MOE_OK) *sig = s_out;
   return rc;
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -22,10 +24,61 @@ struct DeviceDiag {
 };
 DeviceDiag device_diag();  // resolves the symbols on first use per device
 int check_launch(const char* what);  // cudaGetLastError -> MOE_ERR_CUDA
+// result of a cudaLaunchKernelEx -> MOE_OK or MOE_ERR_CUDA (sticky error cleared)
+inline int launch_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MOE_OK;
+  cudaGetLastError();
+  return set_error(MOE_ERR_CUDA, "%s: kernel launch failed: %s", what, cudaGetErrorString(e));
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Programmatic dependent launch (process-wide switch, moe_set_pdl; on by default).
+bool pdl_enabled();
+
+// Every kernel of the library goes through this launch: with PDL on it carries
+// the programmatic-stream-serialisation attribute, so the kernel may be
+// scheduled while the previous kernel in the stream is still running; its
+// CTAs then do their set-up (barrier init, TMEM allocation, descriptor
+// prefetch) and block in grid_dep_wait() until the predecessor has completed.
+// `extra` are further launch attributes (a cluster shape).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, const cudaLaunchAttribute* extra, int n_extra,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[4];
+  int n = 0;
+  for (int i = 0; i < n_extra && n < 3; ++i) attr[n++] = extra[i];
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = static_cast<unsigned>(n);
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------------ device side
+// Ordering against the previous kernel in the stream under programmatic
+// dependent launch.  grid_dep_wait() returns once every grid this one depends
+// on has completed and its memory is visible (at once without PDL); each
+// kernel calls it in every CTA before its first global read of another
+// kernel's output and before its first global write, so a chain of launches
+// keeps full stream order.  grid_dep_launch() then lets the next kernel in
+// the stream be scheduled while this one runs.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void count_launch(unsigned long long* launches, int kid) {
   if (launches != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
       threadIdx.x == 0)

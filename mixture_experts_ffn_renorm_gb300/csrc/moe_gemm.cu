@@ -265,6 +265,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
 
+  // the set-up above touches no global data; from here on this kernel reads
+  // what the previous kernel in the stream wrote (group offsets, A rows)
+  grid_dep_wait();
+  grid_dep_launch();
+
   // ---- device-side tile schedule from the group offsets
   const int G = p.G;
   for (int g = threadIdx.x; g <= G; g += kNThreads)
@@ -717,12 +722,9 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
   p.status = diag.status;
   p.launches = diag.launches;
   cfg.gridDim = dim3(static_cast<unsigned>(kCluster ? 2 * units : units), 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return set_error(MOE_ERR_CUDA, "%s: kernel launch failed: %s", op, cudaGetErrorString(e));
-  }
-  return check_launch(op);
+  return launch_status(launch_kernel(kern, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes,
+                                     stream, attr, 1, ta, tb, p),
+                       op);
 }
 
 int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, const void* b,

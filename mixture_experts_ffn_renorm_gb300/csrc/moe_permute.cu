@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 permute_count(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
               int32_t* __restrict__ hist, unsigned int* status, unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_COUNT);
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(1024)
 permute_scan(int32_t* __restrict__ hist, int E, int n_chunks, int32_t* __restrict__ offsets,
              unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_SCAN);
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int32_t tot[1024];
   __shared__ int32_t warp_sum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -116,6 +120,8 @@ permute_place(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
               int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_to_row,
               unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_PLACE);
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
@@ -153,6 +159,8 @@ __global__ void __launch_bounds__(256)
 permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair, int P,
                int K, int H, uint16_t* __restrict__ x_perm, unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_GATHER);
+  grid_dep_wait();
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const int vpr = H / 8;
   for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -219,25 +227,29 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
   const int blocks = (n_chunks + kWarps - 1) / kWarps;
   const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(int32_t);
   if (n_chunks > 0) {
-    permute_count<<<blocks, kWarps * 32, smem, s>>>(topk_ids, static_cast<int>(P), E, n_chunks,
-                                                    hist, diag.status, diag.launches);
-    int rc = check_launch(op);
+    int rc = launch_status(launch_kernel(permute_count, dim3(blocks), dim3(kWarps * 32), smem, s,
+                                         nullptr, 0, topk_ids, static_cast<int>(P), E, n_chunks,
+                                         hist, diag.status, diag.launches),
+                           op);
     if (rc != MOE_OK) return rc;
   }
-  permute_scan<<<1, 1024, 0, s>>>(hist, E, n_chunks, expert_offsets, diag.launches);
-  int rc = check_launch(op);
+  int rc = launch_status(launch_kernel(permute_scan, dim3(1), dim3(1024), 0, s, nullptr, 0, hist,
+                                       E, n_chunks, expert_offsets, diag.launches),
+                         op);
   if (rc != MOE_OK || n_chunks == 0) return rc;
-  permute_place<<<blocks, kWarps * 32, smem, s>>>(topk_ids, static_cast<int>(P), E, n_chunks,
-                                                  hist, expert_offsets, sorted_pair, pair_to_row,
-                                                  diag.launches);
-  if ((rc = check_launch(op)) != MOE_OK) return rc;
+  rc = launch_status(launch_kernel(permute_place, dim3(blocks), dim3(kWarps * 32), smem, s,
+                                   nullptr, 0, topk_ids, static_cast<int>(P), E, n_chunks, hist,
+                                   expert_offsets, sorted_pair, pair_to_row, diag.launches),
+                     op);
+  if (rc != MOE_OK) return rc;
   if (x_perm_bf16) {
     long long g = (P + 7) / 8;  // 8 rows (warps) per block
     if (g > 152LL * 32) g = 152LL * 32;
-    permute_gather<<<static_cast<unsigned>(g), 256, 0, s>>>(
-        static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P), K, H,
-        static_cast<uint16_t*>(x_perm_bf16), diag.launches);
-    rc = check_launch(op);
+    rc = launch_status(
+        launch_kernel(permute_gather, dim3(static_cast<unsigned>(g)), dim3(256), 0, s, nullptr,
+                      0, static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P),
+                      K, H, static_cast<uint16_t*>(x_perm_bf16), diag.launches),
+        op);
   }
   return rc;
 }

@@ -43,6 +43,8 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormali
             int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ gl_out,
             unsigned long long* launches) {
   count_launch(launches, MOE_KID_ROUTE_TOPK);
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float s_sel[kWarpsPerBlock][32];
   __shared__ float s_ex[kWarpsPerBlock][32];
   const int lane = threadIdx.x & 31;
@@ -226,9 +228,10 @@ extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
   }
   DeviceDiag diag = device_diag();
   const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  pick_topk(E)<<<blocks, kWarpsPerBlock * 32, 0, s>>>(
-      logits, T, E, K, renormalize, static_cast<const uint16_t*>(x_bf16),
-      static_cast<const uint16_t*>(w_shared_gate_bf16), H, topk_ids, topk_w, gate_logit_out,
-      diag.launches);
-  return check_launch(op);
+  return launch_status(
+      launch_kernel(pick_topk(E), dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, nullptr, 0,
+                    logits, T, E, K, renormalize, static_cast<const uint16_t*>(x_bf16),
+                    static_cast<const uint16_t*>(w_shared_gate_bf16), H, topk_ids, topk_w,
+                    gate_logit_out, diag.launches),
+      op);
 }

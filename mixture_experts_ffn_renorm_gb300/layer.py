@@ -84,20 +84,23 @@ class MoeBlock:
     # one forward over x [T, H] bf16 (device); returns a view of the output buffer.
     # marks: optional list; a CUDA event is recorded after each stage and
     # appended as (stage name, event), for per-kernel timing on the stream.
-    def forward(self, x, stream=None, marks=None, out=None):
+    # stages=False records only the first ("start") and the last event: an
+    # event between two kernels keeps the second from starting early under
+    # programmatic dependent launch, so whole-step timings leave them out.
+    def forward(self, x, stream=None, marks=None, out=None, stages=True):
         T = x.shape[0]
         assert T <= self.max_tokens and x.dtype == torch.bfloat16 and x.is_contiguous()
         H, I, E, K = self.H, self.I, self.E, self.K
         P = T * K
         ws = self.workspace
 
-        def mark(name):
-            if marks is not None:
+        def mark(name, edge=False):
+            if marks is not None and (stages or edge):
                 ev = torch.cuda.Event(enable_timing=True)
                 ev.record(torch.cuda.current_stream(self.device) if stream is None else stream)
                 marks.append((name, ev))
 
-        mark("start")
+        mark("start", edge=True)
         moe_route_topk(x, self.w_router, self.logit_bias,
                        self.w_shared_gate if self.has_shared else None, None, T, H, E, K, 1, 0, 1,
                        self.topk_ids, self.topk_w, None,
@@ -127,12 +130,12 @@ class MoeBlock:
             mark("shared_expert")
             moe_combine_gate(self.expert_out, BF16, None, self.sd, BF16, self.gate_logit,
                              self.routed_scale, T, K, H, out, BF16, ws, ws.numel(), stream)
-            mark("combine")
+            mark("combine", edge=True)
             return out
         else:
             moe_combine(self.expert_out, BF16, None, None, BF16, self.routed_scale, T, K, H, out,
                         BF16, stream)
-        mark("combine")
+        mark("combine", edge=True)
         return out
 
     # launches per forward (for the bench's gpu_launches claim)

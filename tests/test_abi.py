@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_refusals_without_gpu(lib):
-    assert m.abi_version() == 3
+    assert m.abi_version() == 4
     # dtype refusals name the missing arm and return before touching the device
     rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
     assert rc == m.ERR_DTYPE and "f16" in m.last_error()
@@ -64,6 +64,17 @@ def test_abi_version_and_refusals_without_gpu(lib):
     assert rc == m.ERR_ALIGN
     # T = 0 is a legal no-op for the stream ops
     assert lib.moe_combine(None, m.BF16, None, None, m.BF16, 1.0, 0, 2, 8, None, m.BF16, None) == 0
+
+
+def test_process_switches(lib):
+    # launch-mode switches are host-side state: they return the previous value
+    # and refuse values outside their range without touching the device
+    prev = m.moe_set_pdl(False)
+    assert prev is True                       # on by default
+    assert m.moe_set_pdl(True) is False
+    assert lib.moe_set_pdl(2) == m.ERR_ARG and "enable" in m.last_error()
+    assert m.moe_set_gemm_pairing(m.GEMM_SINGLE) == m.GEMM_SINGLE
+    assert lib.moe_set_gemm_pairing(7) == m.ERR_ARG
 
 
 def test_workspace_queries(lib):

@@ -226,3 +226,30 @@ def test_graph_replay_matches_eager():
     for _ in range(3):
         got = to_host(blk.replay())
         assert np.array_equal(got, eager)
+
+
+def test_dependent_launch_keeps_stream_order():
+    # Back-to-back forwards of two different batches with no host sync in
+    # between, under programmatic dependent launch: every kernel starts while
+    # its predecessor may still run and must wait for it before touching
+    # global memory (the next batch's router writes the workspace the previous
+    # combine-gate reads its sigmoids from).  The results must equal plain
+    # stream order, bit for bit, for every batch.
+    cfg = W.LayerConfig("pdl_T512_H1024_I512_E32_K4_Is512", T=512, H=1024, I=512, E=32, K=4,
+                        I_shared=512, zipf_s=1.1)
+    d = W.layer_inputs(cfg)
+    blk = _block(cfg, d)
+    x1 = to_dev(d["x"])
+    x2 = to_dev(d["x"][::-1].copy())
+    outs = [torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    prev = m.moe_set_pdl(False)
+    try:
+        want = [to_host(blk.forward(x, out=torch.empty_like(outs[0]))).copy() for x in (x1, x2)]
+        m.moe_set_pdl(True)
+        for i, o in enumerate(outs):
+            blk.forward(x1 if i % 2 == 0 else x2, out=o)
+        torch.cuda.synchronize()
+    finally:
+        m.moe_set_pdl(prev)
+    for i, o in enumerate(outs):
+        assert np.array_equal(to_host(o), want[i % 2]), f"batch {i}"
