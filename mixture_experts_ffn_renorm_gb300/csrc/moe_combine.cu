@@ -152,36 +152,48 @@ combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
 // slices of kThreads items, so the sigmoid of each of its tokens (a chain of
 // double-precision operations, slow on GB300) is evaluated once per block, by
 // full warps, while the first slice's loads are in flight.
-// sigma(gl[t]) for every token, one per thread (full warps), into s_out[T]
-__global__ void __launch_bounds__(kThreads)
+// sigma(gl[t]) for every token, one per thread, into s_out[T].  One warp per
+// block: the double-precision chain of each sigmoid is throughput-bound on an
+// SM's few FP64 units, so the tokens are spread over as many SMs as possible.
+constexpr int kSigThreads = 32;
+__global__ void __launch_bounds__(kSigThreads)
 gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_out,
                     unsigned long long* launches) {
   count_launch(launches, MOE_KID_GATE_SIGMOID);
   grid_dep_wait();
   grid_dep_launch();
-  const int t = blockIdx.x * kThreads + threadIdx.x;
+  const int t = blockIdx.x * kSigThreads + threadIdx.x;
   if (t < T) s_out[t] = sigmoid_cr(__ldg(gl + t));
 }
 
 // The gate ops with the sigmoids already in `sig` (gate_sigmoid_kernel): a
 // plain stream, one 8-channel item per thread, no double precision.
+// This kernel is always launched right after gate_sigmoid_kernel, which waits
+// for all earlier work in the stream before it lets this one start; so under
+// programmatic dependent launch everything this kernel reads except `sig` is
+// final from its first instruction, and every earlier reader of `out` is done.
+// It streams its expert and shared rows first and waits only before it reads
+// the sigmoids, which overlaps the two kernels.
 template <int kMode, typename EoT, typename ShT, typename OutT, bool kHasW, bool kHasShared>
 __global__ void __launch_bounds__(kThreads, min_blocks<EoT>())
 gate_stream_kernel(const void* __restrict__ eo, const float* __restrict__ w,
                    const void* __restrict__ sh, const float* __restrict__ sig, float rs, int T,
                    int K, int H, void* __restrict__ out, unsigned long long* launches, int kid) {
   count_launch(launches, kid);
-  grid_dep_wait();
-  grid_dep_launch();
   const int ipr = H / kVec;
   const long long item = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
-  if (item >= static_cast<long long>(T) * ipr) return;
-  const int t = static_cast<int>(item / ipr);
-  const int c0 = static_cast<int>(item % ipr) * kVec;
+  const bool live = item < static_cast<long long>(T) * ipr;
+  const int t = live ? static_cast<int>(item / ipr) : 0;
+  const int c0 = live ? static_cast<int>(item % ipr) * kVec : 0;
   float shv[kVec], acc[kVec];
-  Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
-  if (kMode == kCombineGate) routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
-  const float sg = __ldg(sig + t);
+  if (live) {
+    Vec8<ShT>::load(sh, static_cast<size_t>(t) * H + c0, shv);
+    if (kMode == kCombineGate) routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
+  }
+  grid_dep_wait();     // the sigmoid pass has completed
+  grid_dep_launch();
+  if (!live) return;
+  const float sg = sig[t];
   float o[kVec];
 #pragma unroll
   for (int i = 0; i < kVec; ++i) {
@@ -338,8 +350,9 @@ int precompute_sigmoids(const char* op, const float* gl, int T, void* workspace,
   if (reinterpret_cast<uintptr_t>(workspace) & 15u)
     return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
   float* s_out = static_cast<float*>(workspace);
-  int rc = launch_status(launch_kernel(gate_sigmoid_kernel, dim3((T + kThreads - 1) / kThreads),
-                                       dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+  int rc = launch_status(launch_kernel(gate_sigmoid_kernel,
+                                       dim3((T + kSigThreads - 1) / kSigThreads),
+                                       dim3(kSigThreads), 0, static_cast<cudaStream_t>(stream),
                                        nullptr, 0, gl, T, s_out, device_diag().launches),
                          op);
   if (rc == MOE_OK) *sig = s_out;

@@ -553,6 +553,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               }
             }
           }
+          if (c == kBnOut / 64 - 1) {   // the accumulator is in registers: free it now
+            ptx::tc_fence_before();
+            if (kPair && !leader) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
+            else ptx::mbar_arrive(bar_tempty(acc));
+          }
           // row `lane` of the staging buffer, piece k at slot k ^ (lane & 7)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -603,9 +608,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       }
-      ptx::tc_fence_before();
-      if (kPair && !leader) ptx::mbar_arrive_remote(tempty_leader + 8u * acc);
-      else ptx::mbar_arrive(bar_tempty(acc));
+      if (!(kEpi == EPI_GATEUP || kEpi == EPI_DOWN)) {
+        ptx::tc_fence_before();
+        if (kPair && !leader) ptx::mbar_arrive_remote(tempty_leader + 8u * acc);
+        else ptx::mbar_arrive(bar_tempty(acc));
+      }
     }
   }
 
