@@ -73,7 +73,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 4 */
+int moe_abi_version(void);  /* 5 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -216,6 +216,40 @@ int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
                                const int32_t* row_to_pair, int P, int I, int H, int G,
                                void* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 size_t moe_grouped_gemm_workspace_size(int P, int H, int I, int G);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_gemm_gateup_silu_bf16_shared / moe_grouped_gemm_down_bf16_shared
+ * -- the routed expert GEMM and the shared expert's GEMM in ONE launch.
+ *
+ * The routed half is exactly moe_grouped_gemm_gateup_silu_bf16 over x_perm
+ * (no row gather), resp. moe_grouped_gemm_down_bf16 with its routing weight
+ * and scatter.  The shared half is the same GEMM over all Ts token rows with
+ * the single shared weight matrix and no routing weight: the shared expert of
+ * [PR509] (its output sd feeds moe_combine_gate), run as one more group.
+ * The shared expert's tiles follow the routed tiles in the one persistent
+ * grid's round-robin schedule, so its tensor-bound work fills the ragged last
+ * round of the weight-streaming routed tiles instead of a launch of its own.  Every output element
+ * is computed by the same tile and K order as in the separate calls, so the
+ * results are bit-identical to them.  Always single-CTA tiles (the
+ * moe_set_gemm_pairing mode applies only when one half is empty, in which
+ * case the call is the plain single-problem one).
+ *
+ *   gate/up:  xs bf16 [Ts,H], w13s bf16 [1,2Is,H] (gate rows first), acts bf16 [Ts,Is]
+ *   down:     acts bf16 [Ts,Is], w2s bf16 [1,H,Is], sd bf16 [Ts,H]
+ *   the routed arguments as in the single-problem calls; Is a multiple of 8
+ * Errors as the single-problem calls; MOE_ERR_ARG/ALIGN for the shared operands.
+ * ---------------------------------------------------------------------- */
+int moe_grouped_gemm_gateup_silu_bf16_shared(const void* a_bf16, const void* w13_bf16,
+                                             const int32_t* group_offsets, int P, int H, int I,
+                                             int G, void* act_bf16, const void* xs_bf16, int Ts,
+                                             const void* w13s_bf16, int Is, void* acts_bf16,
+                                             void* workspace, size_t ws_bytes, void* stream);
+int moe_grouped_gemm_down_bf16_shared(const void* act_bf16, const void* w2_bf16,
+                                      const int32_t* group_offsets, const float* pair_weight,
+                                      const int32_t* row_to_pair, int P, int I, int H, int G,
+                                      void* out_bf16, const void* acts_bf16, int Ts,
+                                      const void* w2s_bf16, int Is, void* sd_bf16,
+                                      void* workspace, size_t ws_bytes, void* stream);
 
 /* moe_set_gemm_pairing -- tiling of the two grouped GEMMs above (the
  * gathered-A gate/up always runs single-CTA tiles):

@@ -35,6 +35,7 @@ EXPORTS = (
     "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
     "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl",
+    "moe_grouped_gemm_gateup_silu_bf16_shared", "moe_grouped_gemm_down_bf16_shared",
 )
 
 
@@ -64,6 +65,10 @@ _SIGS = {
                                            _P], _I),
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
+    "moe_grouped_gemm_gateup_silu_bf16_shared": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P,
+                                                  _I, _P, _P, _SZ, _P], _I),
+    "moe_grouped_gemm_down_bf16_shared": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P,
+                                           _I, _P, _P, _SZ, _P], _I),
     "moe_set_gemm_pairing": ([_I], _I),
     "moe_set_pdl": ([_I], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
@@ -179,6 +184,27 @@ def moe_grouped_gemm_down_bf16(act, w2, group_offsets, pair_weight, row_to_pair,
     rc = lib().moe_grouped_gemm_down_bf16(_ptr(act), _ptr(w2), _ptr(group_offsets),
                                           _ptr(pair_weight), _ptr(row_to_pair), P, I, H, G,
                                           _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_gateup_silu_bf16_shared(a, w13, group_offsets, P, H, I, G, act, xs, Ts,
+                                             w13s, Is, acts, workspace=None, ws_bytes=0,
+                                             stream=None, check=True):
+    """Routed gate/up over x_perm plus the shared expert's gate/up over xs, one launch."""
+    rc = lib().moe_grouped_gemm_gateup_silu_bf16_shared(
+        _ptr(a), _ptr(w13), _ptr(group_offsets), P, H, I, G, _ptr(act), _ptr(xs), Ts, _ptr(w13s),
+        Is, _ptr(acts), _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_down_bf16_shared(act, w2, group_offsets, pair_weight, row_to_pair, P, I, H,
+                                      G, out, acts, Ts, w2s, Is, sd, workspace=None, ws_bytes=0,
+                                      stream=None, check=True):
+    """Routed down (weight, scatter) plus the shared expert's down into sd, one launch."""
+    rc = lib().moe_grouped_gemm_down_bf16_shared(
+        _ptr(act), _ptr(w2), _ptr(group_offsets), _ptr(pair_weight), _ptr(row_to_pair), P, I, H,
+        G, _ptr(out), _ptr(acts), Ts, _ptr(w2s), Is, _ptr(sd), _ptr(workspace), ws_bytes,
+        _stream(stream))
     return _check(rc) if check else rc
 
 

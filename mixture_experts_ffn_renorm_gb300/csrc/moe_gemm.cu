@@ -69,6 +69,15 @@ struct Params {
   const float* pair_weight;      // down: [P] by destination row, or null
   const int32_t* row_to_pair;    // down: destination row, or null
   const float* bias;             // f32 epilogue: per output column, or null
+  // A second, dense problem in the same launch (single-CTA tiles only): rows
+  // [0, P2) of the A matrix behind the second A tensor map times the one weight
+  // matrix behind the second B map, into out2 [P2, N2] (no weight, no scatter).
+  // Its tiles come after the grouped ones in the schedule.  P2 == 0: none.
+  int P2;
+  int N2;
+  int Kdim2;
+  int half_off2;                 // gate/up: row offset of the up half in its weight
+  void* out2;
   unsigned int* status;
   unsigned long long* launches;
   int kid;
@@ -116,6 +125,7 @@ struct Cfg {
 
 struct Tile {
   int g, row0, row_end, n0;
+  int pb;  // 0: the grouped problem, 1: the second (dense) problem
 };
 
 // rows of group g this launch covers: all of them, the leading whole 256-row
@@ -145,7 +155,37 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, con
   t.row0 = r0 + m * tile_m;
   t.row_end = r1;
   t.n0 = n * bn_out;
+  t.pb = 0;
   return t;
+}
+
+// Placement of the second problem's `extra` tiles: after the `routed` grouped
+// tiles (schedule indices routed .. routed + extra - 1).  The persistent CTAs
+// take tiles round-robin, so the second problem's tiles fill the ragged last
+// round of the grouped ones.  On the large layer (all routed tiles streaming
+// weights from HBM, shared-expert tiles bound by the tensor pipe) this beats
+// interleaving them evenly, which leaves the CTAs that drew one late on their
+// share of the HBM stream (gate/up 683 us at the end, 720 us interleaved, 711 us
+// as two launches).
+struct Sched2 {
+  int routed, extra, n2_tiles, P2;
+};
+
+__device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const int* goff, int G,
+                                            int n_tiles, int bn_out, int tile_m, int split,
+                                            const Sched2& s2) {
+  if (s2.extra > 0 && i >= s2.routed) {
+    const int q = i - s2.routed;
+    const int m = q / s2.n2_tiles;
+    Tile t;
+    t.g = 0;
+    t.row0 = m * tile_m;
+    t.row_end = s2.P2;
+    t.n0 = (q - m * s2.n2_tiles) * bn_out;
+    t.pb = 1;
+    return t;
+  }
+  return decode_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split);
 }
 
 // Bounded mbarrier wait.  Returns false when this CTA is aborting.  kCluster:
@@ -195,7 +235,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA>
 __global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA>::kThreadsT, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB2, const Params p) {
   using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA>;
   constexpr bool kCluster = kPair || kMcastA;
   using S = typename C::S;
@@ -254,6 +296,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (p.P2 > 0) {
+      ptx::tma_prefetch_desc(&tmA2);
+      ptx::tma_prefetch_desc(&tmB2);
+    }
   }
   if (warp == 1) {
     if (kPair) {
@@ -317,6 +363,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
+  constexpr bool kCan2 = !kPair && !kMcastA && !kGatherA;
+  Sched2 s2{total, 0, 1, 0};
+  if (kCan2 && p.P2 > 0) {
+    s2.n2_tiles = (p.N2 + kBnOut - 1) / kBnOut;
+    s2.extra = ((p.P2 + kTileM - 1) / kTileM) * s2.n2_tiles;
+    s2.P2 = p.P2;
+    total += s2.extra;
+  }
+  const int nk2 = (p.Kdim2 + BK - 1) / BK;
   const int row_off = kPair ? static_cast<int>(rank) * BM : 0;  // this CTA's A rows in a tile
   const int n_off = kMcastA ? static_cast<int>(rank) * kBnOut : 0;  // this CTA's N tile in a unit
 
@@ -378,13 +433,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int issued = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split);
+        Tile t = locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2);
         t.n0 += n_off;
+        const bool second = kCan2 && t.pb == 1;
+        const CUtensorMap* mA = second ? &tmA2 : &tmA;
+        const CUtensorMap* mB = second ? &tmB2 : &tmB;
+        const int nk_t = second ? nk2 : nk;
         // B rows of this CTA: unpaired, the whole tile (gate/up: gate half, then
         // up half); paired, rank 0 holds the first half of the N columns
         // (gate rows) and rank 1 the second (up rows)
         int brow0, brow1;
-        if (kPair) {
+        if (second) {
+          brow0 = t.n0;
+          brow1 = brow0 + p.half_off2;
+        } else if (kPair) {
           brow0 = t.g * p.b_rows_per_group + t.n0 +
                   static_cast<int>(rank) * ((kEpi == EPI_GATEUP) ? p.half_off : kN / 2);
           brow1 = brow0;
@@ -392,7 +454,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           brow0 = t.g * p.b_rows_per_group + t.n0;
           brow1 = brow0 + p.half_off;
         }
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = 0; kb < nk_t; ++kb) {
           if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
           const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
@@ -414,15 +476,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             ptx::tma_load_2d_mcast(sa + rank * (A_BYTES / 2), &tmA, kb * BK,
                                    t.row0 + static_cast<int>(rank) * (BM / 2), fb, 3);
           } else if (!kGatherA) {
-            ptx::tma_load_2d(sa, &tmA, kb * BK, t.row0 + row_off, fb);
+            ptx::tma_load_2d(sa, mA, kb * BK, t.row0 + row_off, fb);
           }
           if (kEpi == EPI_GATEUP) {
-            ptx::tma_load_2d(sb, &tmB, kb * BK, brow0, fb);
-            ptx::tma_load_2d(sb + kBoxBytes, &tmB, kb * BK, brow1, fb);
+            ptx::tma_load_2d(sb, mB, kb * BK, brow0, fb);
+            ptx::tma_load_2d(sb + kBoxBytes, mB, kb * BK, brow1, fb);
           } else {
 #pragma unroll
             for (int h = 0; h < kN / kBoxB; ++h)
-              ptx::tma_load_2d(sb + h * kBoxBytes, &tmB, kb * BK, brow0 + h * kBoxB, fb);
+              ptx::tma_load_2d(sb + h * kBoxBytes, mB, kb * BK, brow0 + h * kBoxB, fb);
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -455,7 +517,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kN);
-        for (int kb = 0; kb < nk; ++kb) {
+        int nk_t = nk;
+        if (kCan2 && s2.extra > 0 &&
+            locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2).pb)
+          nk_t = nk2;
+        for (int kb = 0; kb < nk_t; ++kb) {
           if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * A_BYTES);
@@ -492,8 +558,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         kPair ? ptx::mapa_shared(bar_tempty(0), 0) : 0u;  // + 8 * acc for buffer acc
     int it = 0;
     for (int tile = unit; tile < total; tile += n_units, ++it) {
-      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split);
+      Tile t = locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2);
       t.n0 += n_off;
+      const bool second = kCan2 && t.pb == 1;
+      const int n_out = second ? p.N2 : p.N;
       const int acc = it & 1;
       const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
       if (!wait_bar(bar_tfull(acc), aphase, abort_flag, p.status)) break;
@@ -508,11 +576,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // (16-byte pieces XOR-swizzled by row to spread the banks), then read
         // back so that eight lanes store one row's 128 contiguous bytes: full
         // 128-byte lines instead of 32 scattered 16-byte pieces per store.
-        uint16_t* out = static_cast<uint16_t*>(p.out);
+        uint16_t* out = static_cast<uint16_t*>(second ? p.out2 : p.out);
         const uint32_t stg = sbase + S::STAGE_EPI + static_cast<uint32_t>(warp - 2) * kStgBytes;
         int dst_row = row;
         float wgt = 1.0f;
-        if (kEpi == EPI_DOWN && valid) {
+        if (kEpi == EPI_DOWN && valid && !second) {
           if (p.row_to_pair) dst_row = __ldg(p.row_to_pair + row);
           if (p.pair_weight) wgt = __ldg(p.pair_weight + dst_row);
         }
@@ -545,10 +613,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int j = 0; j < 32; j += 2) {
                 // the routing weight: one f32 multiply, then the one bf16 rounding
-                const float a = p.pair_weight ? __fmul_rn(__uint_as_float(g[j]), wgt)
-                                              : __uint_as_float(g[j]);
-                const float b = p.pair_weight ? __fmul_rn(__uint_as_float(g[j + 1]), wgt)
-                                              : __uint_as_float(g[j + 1]);
+                const bool wt = p.pair_weight && !second;
+                const float a = wt ? __fmul_rn(__uint_as_float(g[j]), wgt) : __uint_as_float(g[j]);
+                const float b = wt ? __fmul_rn(__uint_as_float(g[j + 1]), wgt)
+                                   : __uint_as_float(g[j + 1]);
                 packed[h * 16 + j / 2] = pack_bf16x2(a, b);
               }
             }
@@ -573,8 +641,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             const int rvalid = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
             const uint4 v = ptx::ld_shared_v4(stg + r * 128 + ((k ^ (r & 7)) << 4));
             const int col = col0 + k * 8;
-            if (rvalid && col < p.N)
-              *reinterpret_cast<uint4*>(out + static_cast<size_t>(drow) * p.N + col) = v;
+            if (rvalid && col < n_out)
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(drow) * n_out + col) = v;
           }
           __syncwarp();
         }
@@ -678,8 +746,8 @@ int num_sms() {
 // tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
 // grid is that many CTAs (pairs when paired), capped at the SM count
 template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false>
-int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
-           long long tile_bound, cudaStream_t stream) {
+int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta2,
+           const CUtensorMap& tb2, Params p, long long tile_bound, cudaStream_t stream) {
   using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA>;
   constexpr bool kCluster = kPair || kMcastA;
   auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA>;
@@ -730,8 +798,15 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params 
   p.launches = diag.launches;
   cfg.gridDim = dim3(static_cast<unsigned>(kCluster ? 2 * units : units), 1, 1);
   return launch_status(launch_kernel(kern, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes,
-                                     stream, attr, 1, ta, tb, p),
+                                     stream, attr, 1, ta, tb, ta2, tb2, p),
                        op);
+}
+
+// one grouped problem (the second-problem maps are unused copies)
+template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false>
+int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
+           long long tile_bound, cudaStream_t stream) {
+  return launch<kN, kEpi, kGatherA, kPair, kMcastA>(op, ta, tb, ta, tb, p, tile_bound, stream);
 }
 
 int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, const void* b,
@@ -906,4 +981,117 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   if (mcast)
     return launch<256, EPI_DOWN, false, false, true>(op, ta, tb, p, tile_bound(P, G, H, 512), s);
   return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
+}
+
+namespace {
+
+// arguments of the shared expert's half of a fused launch
+int check_shared(const char* op, int Ts, int Kdim2, int N2, const void* a2, const void* b2,
+                 const void* out2) {
+  if (Ts < 0) return set_error(MOE_ERR_ARG, "%s: Ts=%d < 0", op, Ts);
+  if (Kdim2 <= 0 || N2 <= 0)
+    return set_error(MOE_ERR_ARG, "%s: shared-expert dimensions must be positive", op);
+  if (Kdim2 % 8 != 0 || N2 % 8 != 0)
+    return set_error(MOE_ERR_ALIGN, "%s: H and I_shared must be multiples of 8", op);
+  if (Ts > 0 && (!a2 || !b2 || !out2))
+    return set_error(MOE_ERR_ARG, "%s: NULL shared-expert operand", op);
+  if (!aligned16(a2) || !aligned16(b2) || !aligned16(out2))
+    return set_error(MOE_ERR_ALIGN, "%s: shared-expert operands must be 16-byte aligned", op);
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_grouped_gemm_gateup_silu_bf16_shared(
+    const void* a_bf16, const void* w13_bf16, const int32_t* group_offsets, int P, int H, int I,
+    int G, void* act_bf16, const void* xs_bf16, int Ts, const void* w13s_bf16, int Is,
+    void* acts_bf16, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_grouped_gemm_gateup_silu_bf16_shared";
+  int rc;
+  if ((rc = check_common(op, P, H, I, G, a_bf16, w13_bf16, act_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if ((rc = check_shared(op, Ts, H, Is, xs_bf16, w13s_bf16, acts_bf16)) != MOE_OK) return rc;
+  // one side empty: the plain single-problem launches (the same tiles either way)
+  if (Ts == 0)
+    return moe_grouped_gemm_gateup_silu_bf16(a_bf16, P, nullptr, 1, w13_bf16, group_offsets, P, H,
+                                             I, G, act_bf16, workspace, ws_bytes, stream);
+  if (P == 0)
+    return moe_grouped_gemm_gateup_silu_bf16(xs_bf16, Ts, nullptr, 1, w13s_bf16, nullptr, Ts, H,
+                                             Is, 1, acts_bf16, workspace, ws_bytes, stream);
+  clear_error();
+  CUtensorMap ta, tb, ta2, tb2;
+  if ((rc = make_tmap(&ta, a_bf16, P, H, BM, op, "a")) != MOE_OK ||
+      (rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, 128, op, "w13")) !=
+          MOE_OK ||
+      (rc = make_tmap(&ta2, xs_bf16, Ts, H, BM, op, "xs")) != MOE_OK ||
+      (rc = make_tmap(&tb2, w13s_bf16, 2LL * Is, H, 128, op, "w13s")) != MOE_OK)
+    return rc;
+  Params p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = H;
+  p.N = I;
+  p.G = G;
+  p.b_rows_per_group = 2 * I;
+  p.half_off = I;
+  p.out = act_bf16;
+  p.P2 = Ts;
+  p.N2 = Is;
+  p.Kdim2 = H;
+  p.half_off2 = Is;
+  p.out2 = acts_bf16;
+  p.kid = MOE_KID_GEMM_GATEUP;
+  const long long extra = ((Ts + BM - 1) / BM) * static_cast<long long>((Is + 127) / 128);
+  return launch<256, EPI_GATEUP>(op, ta, tb, ta2, tb2, p, tile_bound(P, G, I, 128) + extra,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_grouped_gemm_down_bf16_shared(
+    const void* act_bf16, const void* w2_bf16, const int32_t* group_offsets,
+    const float* pair_weight, const int32_t* row_to_pair, int P, int I, int H, int G,
+    void* out_bf16, const void* acts_bf16, int Ts, const void* w2s_bf16, int Is, void* sd_bf16,
+    void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_grouped_gemm_down_bf16_shared";
+  int rc;
+  if ((rc = check_common(op, P, I, H, G, act_bf16, w2_bf16, out_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if ((rc = check_shared(op, Ts, Is, H, acts_bf16, w2s_bf16, sd_bf16)) != MOE_OK) return rc;
+  if (Ts == 0)
+    return moe_grouped_gemm_down_bf16(act_bf16, w2_bf16, group_offsets, pair_weight, row_to_pair,
+                                      P, I, H, G, out_bf16, workspace, ws_bytes, stream);
+  if (P == 0)
+    return moe_grouped_gemm_down_bf16(acts_bf16, w2s_bf16, nullptr, nullptr, nullptr, Ts, Is, H,
+                                      1, sd_bf16, workspace, ws_bytes, stream);
+  clear_error();
+  CUtensorMap ta, tb, ta2, tb2;
+  if ((rc = make_tmap(&ta, act_bf16, P, I, BM, op, "act")) != MOE_OK ||
+      (rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) !=
+          MOE_OK ||
+      (rc = make_tmap(&ta2, acts_bf16, Ts, Is, BM, op, "acts")) != MOE_OK ||
+      (rc = make_tmap(&tb2, w2s_bf16, H, Is, 128, op, "w2s")) != MOE_OK)
+    return rc;
+  Params p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = I;
+  p.N = H;
+  p.G = G;
+  p.b_rows_per_group = H;
+  p.half_off = 0;
+  p.out = out_bf16;
+  p.pair_weight = pair_weight;
+  p.row_to_pair = row_to_pair;
+  p.P2 = Ts;
+  p.N2 = H;
+  p.Kdim2 = Is;
+  p.half_off2 = 0;
+  p.out2 = sd_bf16;
+  p.kid = MOE_KID_GEMM_DOWN;
+  const long long extra = ((Ts + BM - 1) / BM) * static_cast<long long>((H + 255) / 256);
+  return launch<256, EPI_DOWN>(op, ta, tb, ta2, tb2, p, tile_bound(P, G, H, 256) + extra,
+                               static_cast<cudaStream_t>(stream));
 }

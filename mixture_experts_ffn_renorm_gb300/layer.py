@@ -14,8 +14,10 @@ from __future__ import annotations
 import torch
 
 from . import (BF16, moe_combine, moe_combine_gate, moe_gate_workspace_size,
-               moe_grouped_gemm_down_bf16, moe_grouped_gemm_gateup_silu_bf16, moe_permute,
-               moe_permute_workspace_size, moe_route_topk, moe_route_topk_workspace_size)
+               moe_grouped_gemm_down_bf16, moe_grouped_gemm_down_bf16_shared,
+               moe_grouped_gemm_gateup_silu_bf16, moe_grouped_gemm_gateup_silu_bf16_shared,
+               moe_permute, moe_permute_workspace_size, moe_route_topk,
+               moe_route_topk_workspace_size)
 
 
 def _dev_bf16(a, device):
@@ -37,13 +39,16 @@ class MoeBlock:
     """
 
     def __init__(self, H, I, E, K, weights, max_tokens, device="cuda", I_shared=0,
-                 routed_scale=1.0, gather=False):
+                 routed_scale=1.0, gather=False, fuse_shared=True):
         self.H, self.I, self.E, self.K, self.Is = H, I, E, K, I_shared
         self.max_tokens = max_tokens
         # gather=True: the gate/up GEMM reads each routed row straight from x
         # (through sorted_pair / K); False: permute materialises x_perm and the
         # GEMM streams it with tiled TMA loads
         self.gather = gather
+        # fuse_shared: the shared expert's GEMMs run inside the routed GEMM
+        # launches (one launch each for gate/up and down); False: own launches
+        self.fuse_shared = fuse_shared and not gather
         self.routed_scale = float(routed_scale)
         self.device = torch.device(device)
         dv = self.device
@@ -109,7 +114,12 @@ class MoeBlock:
         moe_permute(self.topk_ids, x, T, K, E, H, self.expert_offsets, self.sorted_pair,
                     self.pair_to_row, self.x_perm, ws, ws.numel(), stream)
         mark("permute")
-        if self.gather:
+        fused = self.has_shared and self.fuse_shared
+        if fused:
+            moe_grouped_gemm_gateup_silu_bf16_shared(self.x_perm, self.w13, self.expert_offsets,
+                                                     P, H, I, E, self.act, x, T, self.w13_shared,
+                                                     self.Is, self.act_shared, None, 0, stream)
+        elif self.gather:
             moe_grouped_gemm_gateup_silu_bf16(x, T, self.sorted_pair, K, self.w13,
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,
                                               stream)
@@ -118,16 +128,24 @@ class MoeBlock:
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,
                                               stream)
         mark("gemm_gateup")
-        moe_grouped_gemm_down_bf16(self.act, self.w2, self.expert_offsets, self.topk_w,
-                                   self.sorted_pair, P, I, H, E, self.expert_out, None, 0, stream)
+        if fused:
+            moe_grouped_gemm_down_bf16_shared(self.act, self.w2, self.expert_offsets, self.topk_w,
+                                              self.sorted_pair, P, I, H, E, self.expert_out,
+                                              self.act_shared, T, self.w2_shared, self.Is, self.sd,
+                                              None, 0, stream)
+        else:
+            moe_grouped_gemm_down_bf16(self.act, self.w2, self.expert_offsets, self.topk_w,
+                                       self.sorted_pair, P, I, H, E, self.expert_out, None, 0,
+                                       stream)
         mark("gemm_down")
         out = self.out[:T] if out is None else out
         if self.has_shared:
-            moe_grouped_gemm_gateup_silu_bf16(x, T, None, 1, self.w13_shared, None, T, H, self.Is,
-                                              1, self.act_shared, None, 0, stream)
-            moe_grouped_gemm_down_bf16(self.act_shared, self.w2_shared, None, None, None, T,
-                                       self.Is, H, 1, self.sd, None, 0, stream)
-            mark("shared_expert")
+            if not fused:
+                moe_grouped_gemm_gateup_silu_bf16(x, T, None, 1, self.w13_shared, None, T, H,
+                                                  self.Is, 1, self.act_shared, None, 0, stream)
+                moe_grouped_gemm_down_bf16(self.act_shared, self.w2_shared, None, None, None, T,
+                                           self.Is, H, 1, self.sd, None, 0, stream)
+                mark("shared_expert")
             moe_combine_gate(self.expert_out, BF16, None, self.sd, BF16, self.gate_logit,
                              self.routed_scale, T, K, H, out, BF16, ws, ws.numel(), stream)
             mark("combine", edge=True)
@@ -143,7 +161,7 @@ class MoeBlock:
         n = 2 + (3 if self.gather else 4) + 3  # route (2), permute (3 or 4), 2 GEMMs, combine
         if self.has_shared:
             n += 1  # the combine-gate's sigmoid pass
-        if self.has_shared:
+        if self.has_shared and not self.fuse_shared:
             n += 2
         return n
 

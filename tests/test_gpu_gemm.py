@@ -118,6 +118,79 @@ def test_down_weight_scatter(sizes, H, I, pairing):
         assert_gemm_close(to_host(out), want, "down")
 
 
+FUSED = [
+    # routed group sizes, H, I, shared rows Ts, shared I_s (ragged tiles on both sides)
+    ([3, 200, 0, 77], 512, 256, 130, 192),
+    ([600, 5, 256, 255, 513], 256, 256, 1, 64),
+    ([1, 1, 1, 1, 1, 1, 1, 1], 2048, 768, 16, 256),
+    ([0, 0], 256, 128, 300, 128),          # no routed rows: the shared GEMM alone
+    ([40, 9], 256, 128, 0, 128),           # no shared rows: the routed GEMM alone
+    ([4, 3], 64, 32, 4, 32),               # narrower than one tile everywhere
+    ([257, 0, 0, 3], 136, 72, 70, 40),     # K and N not multiples of the tile
+]
+
+
+@pytest.mark.parametrize("sizes,H,I,Ts,Is", FUSED)
+def test_fused_shared_expert_launch(sizes, H, I, Ts, Is):
+    # the routed GEMM and the shared expert's GEMM in one launch: bit-identical
+    # to the two separate launches (same tiles, same K order), and the shared
+    # half within tolerance of the oracle
+    off, P, G, A, W13, W2 = _case(sizes, H, I, sum(sizes) + Ts + Is)
+    rng = np.random.default_rng(Ts + 3 * Is)
+    xs = W.to_bf16_bits(rng.standard_normal((Ts, H)).astype(np.float32))
+    w13s = W.to_bf16_bits((0.02 * rng.standard_normal((1, 2 * Is, H))).astype(np.float32))
+    w2s = W.to_bf16_bits((0.02 * rng.standard_normal((1, H, Is))).astype(np.float32))
+    wts = rng.uniform(0.05, 1.0, P).astype(np.float32)
+    r2p = rng.permutation(P).astype(np.int32)
+    dA, dW13, dW2, doff = to_dev(A), to_dev(W13), to_dev(W2), to_dev(off)
+    dxs, dw13s, dw2s, dwts, dr2p = to_dev(xs), to_dev(w13s), to_dev(w2s), to_dev(wts), to_dev(r2p)
+
+    def bufs(rows, cols):
+        t = empty((rows, cols), torch.bfloat16)
+        t.fill_(0)
+        return t
+
+    act_a, acts_a, out_a, sd_a = bufs(P, I), bufs(Ts, Is), bufs(P, H), bufs(Ts, H)
+    m.moe_grouped_gemm_gateup_silu_bf16(dA, P, None, 1, dW13, doff, P, H, I, G, act_a)
+    m.moe_grouped_gemm_gateup_silu_bf16(dxs, Ts, None, 1, dw13s, None, Ts, H, Is, 1, acts_a)
+    m.moe_grouped_gemm_down_bf16(act_a, dW2, doff, dwts, dr2p, P, I, H, G, out_a)
+    m.moe_grouped_gemm_down_bf16(acts_a, dw2s, None, None, None, Ts, Is, H, 1, sd_a)
+
+    act_b, acts_b, out_b, sd_b = bufs(P, I), bufs(Ts, Is), bufs(P, H), bufs(Ts, H)
+    before = launches()
+    m.moe_grouped_gemm_gateup_silu_bf16_shared(dA, dW13, doff, P, H, I, G, act_b, dxs, Ts, dw13s,
+                                               Is, acts_b)
+    m.moe_grouped_gemm_down_bf16_shared(act_b, dW2, doff, dwts, dr2p, P, I, H, G, out_b, acts_b,
+                                        Ts, dw2s, Is, sd_b)
+    assert launched_since(before, "gemm_gateup") == 1
+    assert launched_since(before, "gemm_down") == 1
+    assert m.moe_device_status() == 0
+    for a, b in ((act_a, act_b), (acts_a, acts_b), (out_a, out_b), (sd_a, sd_b)):
+        assert np.array_equal(to_host(a), to_host(b))
+    if Ts:
+        one = np.array([0, Ts], np.int32)
+        want_acts = O.gateup_silu(xs, w13s, one, P=Ts, H=H, I=Is, G=1)
+        assert_gemm_close(to_host(acts_b), want_acts, "fused shared gate/up")
+        want_sd = O.down(to_host(acts_b), w2s, one, P=Ts, I=Is, H=H, G=1)
+        assert_gemm_close(to_host(sd_b), want_sd, "fused shared down")
+    if P:
+        want_act = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G)
+        assert_gemm_close(to_host(act_b), want_act, "fused routed gate/up")
+
+
+def test_fused_shared_refusals():
+    x = empty((4, 64), torch.bfloat16)
+    before = launches()
+    with pytest.raises(m.MoeError) as ei:   # I_shared not a multiple of 8
+        m.moe_grouped_gemm_gateup_silu_bf16_shared(x, x, None, 4, 64, 64, 1, x, x, 4, x, 36, x)
+    assert ei.value.code == m.ERR_ALIGN
+    with pytest.raises(m.MoeError) as ei:   # shared rows without operands
+        m.moe_grouped_gemm_down_bf16_shared(x, x, None, None, None, 4, 64, 64, 1, x, None, 4,
+                                            None, 64, None)
+    assert ei.value.code == m.ERR_ARG
+    assert launches() == before
+
+
 def test_gateup_narrowing_is_visible_on_the_gpu(pairing):
     # g = u = 1 + 2^-9 exactly: narrowing before the activation gives
     # bf16(silu(1) * 1) = 0x3F3B; without it the result would be 0x3F3C
