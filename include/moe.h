@@ -107,7 +107,13 @@ int moe_abi_version(void);  /* 5 */
  *   topk_w       f32   [T,K] out
  *   logits_out   f32   [T,E] out or NULL
  *   gate_logit_out f32 [T] out; required when w_shared_gate != NULL
- *   workspace    >= moe_route_topk_workspace_size(T, E, K) bytes (may be 0)
+ *   workspace    >= moe_route_topk_workspace_size(T, E, K) bytes (may be 0
+ *                when logits_in or logits_out is given).  When T*E gives the
+ *                logits GEMM fewer tiles than SMs (decode), it splits K into up
+ *                to 16 ranges whose partial sums go to the workspace; the
+ *                selection adds them in range order, then the bias.  It uses as
+ *                many ranges as the workspace holds (one: no split), so a
+ *                smaller workspace only costs speed.
  * ---------------------------------------------------------------------- */
 int moe_route_topk(const void* x_bf16, const void* w_router_bf16, const float* logit_bias,
                    const void* w_shared_gate_bf16, const float* logits_in, int T, int H, int E,
@@ -358,6 +364,7 @@ enum {
   MOE_KID_COMBINE_GATE = 9,
   MOE_KID_SHARED_GATE = 10,
   MOE_KID_GATE_SIGMOID = 11,  /* the sigmoid pre-pass of the gate ops (workspace given) */
+  MOE_KID_PERMUTE_SMALL = 12, /* count + scan + place in one block (P <= 4096) */
   MOE_KID_COUNT = 16
 };
 int moe_device_status(int* status_out, int clear);

@@ -24,7 +24,7 @@ STATUS_TIMEOUT, STATUS_BAD_ID = 1, 2
 KID = {
     "route_logits": 0, "route_topk": 1, "permute_count": 2, "permute_scan": 3,
     "permute_place": 4, "permute_gather": 5, "gemm_gateup": 6, "gemm_down": 7, "combine": 8,
-    "combine_gate": 9, "shared_gate": 10, "gate_sigmoid": 11,
+    "combine_gate": 9, "shared_gate": 10, "gate_sigmoid": 11, "permute_small": 12,
 }
 KID_COUNT = 16
 

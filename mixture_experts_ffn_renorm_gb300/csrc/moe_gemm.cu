@@ -78,6 +78,10 @@ struct Params {
   int Kdim2;
   int half_off2;                 // gate/up: row offset of the up half in its weight
   void* out2;
+  // f32 epilogue only: split K into ksplit ranges of ceil(nk / ksplit) k-blocks;
+  // each (tile, range) is a unit of its own and stores its partial sum, without
+  // the bias, at out + range * P * N.  ksplit == 1: the whole K, bias added.
+  int ksplit;
   unsigned int* status;
   unsigned long long* launches;
   int kid;
@@ -126,6 +130,7 @@ struct Cfg {
 struct Tile {
   int g, row0, row_end, n0;
   int pb;  // 0: the grouped problem, 1: the second (dense) problem
+  int ks;  // K range of a split-K unit (0 without split)
 };
 
 // rows of group g this launch covers: all of them, the leading whole 256-row
@@ -156,6 +161,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, con
   t.row_end = r1;
   t.n0 = n * bn_out;
   t.pb = 0;
+  t.ks = 0;
   return t;
 }
 
@@ -183,9 +189,21 @@ __device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const 
     t.row_end = s2.P2;
     t.n0 = (q - m * s2.n2_tiles) * bn_out;
     t.pb = 1;
+    t.ks = 0;
     return t;
   }
   return decode_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split);
+}
+
+// split-K units (f32 epilogue): schedule index i is K range i % ksplit of tile i / ksplit
+__device__ __forceinline__ Tile locate_unit(int i, int ksplit, const int* tile_start,
+                                            const int* goff, int G, int n_tiles, int bn_out,
+                                            int tile_m, int split, const Sched2& s2) {
+  if (ksplit <= 1) return locate_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2);
+  const int q = i / ksplit;
+  Tile t = locate_tile(q, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2);
+  t.ks = i - q * ksplit;
+  return t;
 }
 
 // Bounded mbarrier wait.  Returns false when this CTA is aborting.  kCluster:
@@ -364,6 +382,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
   constexpr bool kCan2 = !kPair && !kMcastA && !kGatherA;
+  const int ksplit = (kEpi == EPI_F32 && p.ksplit > 1) ? p.ksplit : 1;
+  const int nk_split = (nk + ksplit - 1) / ksplit;   // k-blocks per K range
   Sched2 s2{total, 0, 1, 0};
   if (kCan2 && p.P2 > 0) {
     s2.n2_tiles = (p.N2 + kBnOut - 1) / kBnOut;
@@ -371,6 +391,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     s2.P2 = p.P2;
     total += s2.extra;
   }
+  total *= ksplit;
   const int nk2 = (p.Kdim2 + BK - 1) / BK;
   const int row_off = kPair ? static_cast<int>(rank) * BM : 0;  // this CTA's A rows in a tile
   const int n_off = kMcastA ? static_cast<int>(rank) * kBnOut : 0;  // this CTA's N tile in a unit
@@ -433,12 +454,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int issued = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        Tile t = locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2);
+        Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
+                             p.split, s2);
         t.n0 += n_off;
         const bool second = kCan2 && t.pb == 1;
         const CUtensorMap* mA = second ? &tmA2 : &tmA;
         const CUtensorMap* mB = second ? &tmB2 : &tmB;
-        const int nk_t = second ? nk2 : nk;
+        const int kb_lo = t.ks * nk_split;
+        const int nk_t = second ? nk2 : min(nk, kb_lo + nk_split);
         // B rows of this CTA: unpaired, the whole tile (gate/up: gate half, then
         // up half); paired, rank 0 holds the first half of the N columns
         // (gate rows) and rank 1 the second (up rows)
@@ -454,7 +477,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           brow0 = t.g * p.b_rows_per_group + t.n0;
           brow1 = brow0 + p.half_off;
         }
-        for (int kb = 0; kb < nk_t; ++kb) {
+        for (int kb = second ? 0 : kb_lo; kb < nk_t; ++kb) {
           if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
           const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
@@ -518,9 +541,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kN);
         int nk_t = nk;
-        if (kCan2 && s2.extra > 0 &&
-            locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2).pb)
+        if (ksplit > 1) {
+          const int kb_lo = (tile % ksplit) * nk_split;
+          nk_t = min(nk, kb_lo + nk_split) - kb_lo;
+        } else if (kCan2 && s2.extra > 0 &&
+                   locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2)
+                       .pb) {
           nk_t = nk2;
+        }
         for (int kb = 0; kb < nk_t; ++kb) {
           if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
           ptx::tc_fence_after();
@@ -558,7 +586,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         kPair ? ptx::mapa_shared(bar_tempty(0), 0) : 0u;  // + 8 * acc for buffer acc
     int it = 0;
     for (int tile = unit; tile < total; tile += n_units, ++it) {
-      Tile t = locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2);
+      Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split,
+                           s2);
       t.n0 += n_off;
       const bool second = kCan2 && t.pb == 1;
       const int n_out = second ? p.N2 : p.N;
@@ -647,7 +676,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           __syncwarp();
         }
       } else {
-        float* out = static_cast<float*>(p.out);
+        // a split-K unit stores its partial sum, without the bias, in its own slab
+        float* out = static_cast<float*>(p.out) +
+                     static_cast<size_t>(t.ks) * static_cast<size_t>(p.P) * p.N;
+        const float* bias = ksplit > 1 ? nullptr : p.bias;
 #pragma unroll 1
         for (int c = 0; c < kBnOut / 32; ++c) {
           uint32_t y[32];
@@ -659,7 +691,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               v[j] = __uint_as_float(y[j]);
-              if (p.bias && col + j < p.N) v[j] = __fadd_rn(v[j], __ldg(p.bias + col + j));
+              if (bias && col + j < p.N) v[j] = __fadd_rn(v[j], __ldg(bias + col + j));
             }
             float* dst = out + static_cast<size_t>(row) * p.N + col;
             if ((p.N & 3) == 0) {
@@ -834,8 +866,23 @@ std::atomic<int> g_pairing{MOE_GEMM_SINGLE};
 }  // namespace gemm
 
 // router logits l[t, e] = x[t,:] . w_router[e,:] (+ bias[e]) in f32 (used by moe_route.cu)
+// K ranges for the router logits GEMM: enough (tile, range) units to give every
+// SM one when T x E alone makes few tiles (decode), at most 16, every range
+// non-empty.  ranges * T * E floats of partial sums.
+int router_splits(int T, int H, int E) {
+  using namespace gemm;
+  const long long tiles = static_cast<long long>((T + BM - 1) / BM) * ((E + 63) / 64);
+  long long want = tiles > 0 ? num_sms() / tiles : 1;
+  if (want > 16) want = 16;
+  if (want < 1) want = 1;
+  const int nk = (H + BK - 1) / BK;
+  if (want > nk) want = nk;
+  const int per = static_cast<int>((nk + want - 1) / want);
+  return (nk + per - 1) / per;
+}
+
 int launch_router_logits(const void* x, const void* w_router, const float* bias, int T, int H,
-                         int E, float* logits, cudaStream_t stream) {
+                         int E, float* logits, int ksplit, cudaStream_t stream) {
   using namespace gemm;
   const char* op = "moe_route_topk";
   if (T == 0) return MOE_OK;
@@ -854,8 +901,9 @@ int launch_router_logits(const void* x, const void* w_router, const float* bias,
   p.half_off = 0;
   p.out = logits;
   p.bias = bias;
+  p.ksplit = ksplit < 1 ? 1 : ksplit;
   p.kid = MOE_KID_ROUTE_LOGITS;
-  return launch<64, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 64), stream);
+  return launch<64, EPI_F32>(op, ta, tb, p, tile_bound(T, 1, E, 64) * p.ksplit, stream);
 }
 
 }  // namespace moe

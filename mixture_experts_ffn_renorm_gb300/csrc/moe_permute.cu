@@ -13,6 +13,9 @@
 //           rank of a pair among equal experts of its step comes from
 //           __match_any_sync, so rows inside an expert ascend with p
 //   gather  (optional) x_perm[row] = x[sorted_pair[row] / K], 16 bytes a thread
+// Up to kSmallChunks chunks (decode-sized batches) count, scan and place run in
+// one block (permute_small) with the histogram in shared memory: the same
+// steps, one launch instead of three.
 // Everything is a function of the ids alone: no atomics decide an order.
 #include "moe_common.cuh"
 
@@ -184,7 +187,128 @@ permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorte
   }
 }
 
+// Count, scan and place for n_chunks <= kSmallChunks in one block: warp c owns
+// chunk c as in permute_count / permute_place; the chunk histograms and the
+// expert offsets stay in shared memory ([kSmallChunks][E] + [E] ints).
+constexpr int kSmallChunks = 8;
+__global__ void __launch_bounds__(kSmallChunks * 32)
+permute_small(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
+              int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair,
+              int32_t* __restrict__ pair_to_row, unsigned int* status,
+              unsigned long long* launches) {
+  count_launch(launches, MOE_KID_PERMUTE_SMALL);
+  grid_dep_wait();
+  grid_dep_launch();
+  extern __shared__ int32_t sh[];
+  __shared__ int32_t warp_sum[kSmallChunks];
+  int32_t* hist = sh;                         // [kSmallChunks][E]
+  int32_t* base = sh + kSmallChunks * E;      // [E]: first row of each expert
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int kT = kSmallChunks * 32;
+  // 1. per-chunk histograms
+  int32_t* h = hist + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (warp < n_chunks) {
+    const int p0 = warp * kChunk, p1 = min(P, p0 + kChunk);
+    bool bad = false;
+    for (int p = p0 + lane; p < p1; p += 32) {
+      const int e = __ldg(ids + p);
+      if (e >= 0 && e < E) atomicAdd(h + e, 1);
+      else bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
+      atomicOr(status, static_cast<unsigned int>(MOE_STATUS_BAD_ID));
+  }
+  __syncthreads();
+  // 2. per expert: exclusive prefix over the chunks (in chunk order), total in base[e]
+  for (int e = tid; e < E; e += kT) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int v = hist[c * E + e];
+      hist[c * E + e] = run;
+      run += v;
+    }
+    base[e] = run;
+  }
+  __syncthreads();
+  // 3. exclusive scan of the totals over experts: thread tid owns experts
+  //    [tid * per, tid * per + per), a warp scan, then a scan of the warp sums
+  const int per = (E + kT - 1) / kT;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += base[e];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kSmallChunks; ++w) {
+    const int v = warp_sum[w];
+    if (w < warp) before += v;
+    total += v;
+  }
+  int run = before + incl - local;
+  for (int e = e0; e < e1; ++e) {
+    const int v = base[e];
+    base[e] = run;
+    offsets[e] = run;
+    run += v;
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+  // 4. place chunk `warp`, 32 pairs at a time in pair order
+  if (warp >= n_chunks) return;
+  for (int e = lane; e < E; e += 32) h[e] += base[e];
+  __syncwarp();
+  const int p0 = warp * kChunk, p1 = min(P, p0 + kChunk);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int b = p0; b < p1; b += 32) {
+    const int p = b + lane;
+    const int e = p < p1 ? __ldg(ids + p) : -1;
+    const bool valid = e >= 0 && e < E;
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+    int row = 0;
+    uint32_t peers = 0;
+    if (valid) {
+      peers = __match_any_sync(vmask, e);
+      row = h[e] + __popc(peers & lt_mask);
+    }
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) h[e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      sorted_pair[row] = p;
+      pair_to_row[p] = row;
+    }
+  }
+}
+
 int n_chunks_of(long long P) { return static_cast<int>((P + kChunk - 1) / kChunk); }
+
+}  // namespace
+}  // namespace moe
+
+namespace moe {
+namespace {
+
+// the optional x_perm gather after the sort
+int gather(const char* op, const void* x_bf16, void* x_perm_bf16, const int32_t* sorted_pair,
+           long long P, int K, int H, cudaStream_t s, const DeviceDiag& diag) {
+  if (!x_perm_bf16) return MOE_OK;
+  long long g = (P + 7) / 8;  // 8 rows (warps) per block
+  if (g > 152LL * 32) g = 152LL * 32;
+  return launch_status(
+      launch_kernel(permute_gather, dim3(static_cast<unsigned>(g)), dim3(256), 0, s, nullptr, 0,
+                    static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P), K, H,
+                    static_cast<uint16_t*>(x_perm_bf16), diag.launches),
+      op);
+}
 
 }  // namespace
 }  // namespace moe
@@ -226,6 +350,16 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
   int32_t* hist = static_cast<int32_t*>(workspace);
   const int blocks = (n_chunks + kWarps - 1) / kWarps;
   const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(int32_t);
+  if (n_chunks > 0 && n_chunks <= kSmallChunks) {
+    const size_t smem_small = static_cast<size_t>(kSmallChunks + 1) * E * sizeof(int32_t);
+    int rc = launch_status(launch_kernel(permute_small, dim3(1), dim3(kSmallChunks * 32),
+                                         smem_small, s, nullptr, 0, topk_ids,
+                                         static_cast<int>(P), E, n_chunks, expert_offsets,
+                                         sorted_pair, pair_to_row, diag.status, diag.launches),
+                           op);
+    if (rc != MOE_OK) return rc;
+    return gather(op, x_bf16, x_perm_bf16, sorted_pair, P, K, H, s, diag);
+  }
   if (n_chunks > 0) {
     int rc = launch_status(launch_kernel(permute_count, dim3(blocks), dim3(kWarps * 32), smem, s,
                                          nullptr, 0, topk_ids, static_cast<int>(P), E, n_chunks,
@@ -242,14 +376,5 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
                                    expert_offsets, sorted_pair, pair_to_row, diag.launches),
                      op);
   if (rc != MOE_OK) return rc;
-  if (x_perm_bf16) {
-    long long g = (P + 7) / 8;  // 8 rows (warps) per block
-    if (g > 152LL * 32) g = 152LL * 32;
-    rc = launch_status(
-        launch_kernel(permute_gather, dim3(static_cast<unsigned>(g)), dim3(256), 0, s, nullptr,
-                      0, static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P),
-                      K, H, static_cast<uint16_t*>(x_perm_bf16), diag.launches),
-        op);
-  }
-  return rc;
+  return gather(op, x_bf16, x_perm_bf16, sorted_pair, P, K, H, s, diag);
 }

@@ -4,7 +4,9 @@
 //
 // Two kernels: the logits GEMM on tcgen05 tensor cores (moe_gemm.cu, f32
 // epilogue with the optional per-expert bias) and a warp-per-token selection
-// kernel.  Selection runs on the f32 logits themselves (softmax is monotone),
+// kernel.  When T x E makes few GEMM tiles (decode), the GEMM splits K into up
+// to 16 ranges that store partial sums in the workspace, and the selection
+// kernel adds them in range order (then the bias) before it selects.  Selection runs on the f32 logits themselves (softmax is monotone),
 // so the chosen ids do not depend on exp; the weights use the bit-exact
 // binary32 exp and are summed in rank order, so they are bit-identical to the
 // sequential definition for the same logits.
@@ -14,8 +16,9 @@
 
 namespace moe {
 
+int router_splits(int T, int H, int E);
 int launch_router_logits(const void* x, const void* w_router, const float* bias, int T, int H,
-                         int E, float* logits, cudaStream_t stream);
+                         int E, float* logits, int ksplit, cudaStream_t stream);
 
 namespace {
 
@@ -38,7 +41,8 @@ __device__ __forceinline__ uint32_t rank_key(float v) {
 // low, and a warp instruction costs the same with 8 or 32 lanes active).
 template <int kPerLane>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormalize,
+topk_kernel(const float* __restrict__ logits, int n_part, const float* __restrict__ bias,
+            float* __restrict__ logits_out, int T, int E, int K, int renormalize,
             const uint16_t* __restrict__ x, const uint16_t* __restrict__ wsg, int H,
             int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ gl_out,
             unsigned long long* launches) {
@@ -55,11 +59,20 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormali
   float my_sel = 0.0f;
   int my_id = 0;
   if (live) {
+    // n_part K-range partial sums of each logit, added in range order, then the bias
     const float* row = logits + static_cast<size_t>(t) * E;
+    const size_t slab = static_cast<size_t>(T) * E;
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < E ? __ldg(row + e) : 0.0f;
+      float a = 0.0f;
+      if (e < E) {
+        a = __ldg(row + e);
+        for (int q = 1; q < n_part; ++q) a = __fadd_rn(a, __ldg(row + q * slab + e));
+        if (bias) a = __fadd_rn(a, __ldg(bias + e));
+        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = a;
+      }
+      v[i] = a;
     }
     uint32_t key[kPerLane];
 #pragma unroll
@@ -143,8 +156,9 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renormali
   }
 }
 
-using TopkFn = void (*)(const float*, int, int, int, int, const uint16_t*, const uint16_t*, int,
-                        int32_t*, float*, float*, unsigned long long*);
+using TopkFn = void (*)(const float*, int, const float*, float*, int, int, int, int,
+                        const uint16_t*, const uint16_t*, int, int32_t*, float*, float*,
+                        unsigned long long*);
 
 TopkFn pick_topk(int E) {
   if (E <= 32) return topk_kernel<1>;
@@ -167,7 +181,8 @@ using namespace moe;
 extern "C" size_t moe_route_topk_workspace_size(int T, int E, int K) {
   (void)K;
   if (T <= 0 || E <= 0) return 0;
-  return logits_bytes(T, E);
+  // the largest K split any H allows (the split never exceeds H / 64 ranges)
+  return logits_bytes(T, E) * static_cast<size_t>(router_splits(T, 1 << 20, E));
 }
 
 extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
@@ -206,18 +221,32 @@ extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
     return set_error(MOE_ERR_ALIGN, "%s: x/w_router/w_shared_gate must be 16-byte aligned", op);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float* logits = logits_in;
+  int n_part = 1;
+  const float* part_bias = nullptr;   // added by the selection kernel after a K split
+  float* sel_logits_out = nullptr;    // written by the selection kernel after a K split
   if (!logits) {
+    if (workspace && !aligned16(workspace))
+      return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
+    // K split into ranges of partial sums in the workspace, as many as it holds
+    const size_t slab = static_cast<size_t>(T) * E * sizeof(float);
+    int splits = router_splits(T, H, E);
+    const size_t fit = workspace ? ws_bytes / slab : 0;
+    if (static_cast<size_t>(splits) > fit) splits = static_cast<int>(fit);
     float* dst = logits_out;
-    if (!dst) {
+    if (splits > 1) {
+      dst = static_cast<float*>(workspace);
+      n_part = splits;
+      part_bias = logit_bias;
+      sel_logits_out = logits_out;
+    } else if (!dst) {
       if (!workspace || ws_bytes < logits_bytes(T, E))
         return set_error(MOE_ERR_WORKSPACE,
                          "%s: workspace of %zu bytes is smaller than the %zu bytes of logits", op,
                          ws_bytes, logits_bytes(T, E));
-      if (!aligned16(workspace))
-        return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
       dst = static_cast<float*>(workspace);
     }
-    int rc = launch_router_logits(x_bf16, w_router_bf16, logit_bias, T, H, E, dst, s);
+    int rc = launch_router_logits(x_bf16, w_router_bf16, logit_bias, T, H, E, dst,
+                                  n_part, s);
     if (rc != MOE_OK) return rc;
     logits = dst;
   } else if (logits_out && logits_out != logits_in) {
@@ -230,7 +259,8 @@ extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
   const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   return launch_status(
       launch_kernel(pick_topk(E), dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, nullptr, 0,
-                    logits, T, E, K, renormalize, static_cast<const uint16_t*>(x_bf16),
+                    logits, n_part, part_bias, sel_logits_out, T, E, K, renormalize,
+                    static_cast<const uint16_t*>(x_bf16),
                     static_cast<const uint16_t*>(w_shared_gate_bf16), H, topk_ids, topk_w,
                     gate_logit_out, diag.launches),
       op);

@@ -56,7 +56,7 @@ def test_tiny_layer_every_element():
     blk = _block(cfg, d)
     before = launches()
     out = to_host(blk.forward(to_dev(d["x"])))
-    for k in ("route_logits", "route_topk", "permute_place", "combine_gate"):
+    for k in ("route_logits", "route_topk", "permute_small", "combine_gate"):
         assert launched_since(before, k) == 1, k
     # the shared expert runs inside the routed GEMM launches
     assert launched_since(before, "gemm_gateup") == 1 and launched_since(before, "gemm_down") == 1

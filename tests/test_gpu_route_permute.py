@@ -93,6 +93,40 @@ def test_router_gemm_logits_within_bound_and_selection_exact(T, H, E, K):
     assert np.array_equal(ids2, ids) and np.array_equal(w2, w)
 
 
+@pytest.mark.parametrize("T,H,E", [(16, 2048, 128), (1, 4096, 256), (2048, 4096, 256),
+                                   (40, 200, 96)])
+def test_router_k_split_matches_unsplit_within_bound(T, H, E):
+    # with a workspace the logits GEMM splits K into ranges whose partial sums
+    # the selection adds in range order (then the bias); without one it runs
+    # whole.  Both logits are within the dot-product bound, and each side's ids
+    # and weights are the exact functions of its own logits.
+    K = 8
+    rng = np.random.default_rng(T * 3 + H + E)
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = W.to_bf16_bits((0.02 * rng.standard_normal((E, H))).astype(np.float32))
+    bias = (0.5 * rng.standard_normal(E)).astype(np.float32)
+    xf, wf = bf16_to_f64(x), bf16_to_f64(wr)
+    exact = xf @ wf.T + bias
+    bound = (H + 2) * 2.0**-23 * (np.abs(xf) @ np.abs(wf).T + np.abs(bias))
+    wsz = m.moe_route_topk_workspace_size(T, E, K)
+    res = []
+    for ws in (empty((max(wsz, 16),), torch.uint8), None):
+        ids = empty((T, K), torch.int32)
+        w = empty((T, K), torch.float32)
+        lo = empty((T, E), torch.float32)
+        m.moe_route_topk(to_dev(x), to_dev(wr), to_dev(bias), None, None, T, H, E, K, 1, 0, 1,
+                         ids, w, lo, None, ws, 0 if ws is None else ws.numel())
+        lo_h, ids_h, w_h = to_host(lo), to_host(ids), to_host(w)
+        assert np.all(np.abs(lo_h - exact) <= bound), float(np.max(np.abs(lo_h - exact) / bound))
+        want_ids, want_w, _, _ = O.route_topk(logits_in=lo_h, T=T, H=1, E=E, K=K)
+        assert np.array_equal(ids_h, want_ids)
+        assert np.array_equal(w_h.view(np.uint32), want_w.view(np.uint32))
+        res.append(ids_h)
+    # the two orders round differently; the chosen sets agree except on near-ties
+    same = np.all(np.sort(res[0], 1) == np.sort(res[1], 1), axis=1)
+    assert same.mean() >= 0.95
+
+
 def test_router_refusals():
     T, E, K = 4, 8, 2
     logits = np.zeros((T, E), np.float32)
@@ -131,7 +165,8 @@ def _ids(T, K, E, seed, skew=False):
 
 @pytest.mark.parametrize("T,K,E,H", [(4, 2, 8, 64), (16, 8, 128, 2048), (1000, 8, 128, 64),
                                      (2048, 8, 256, 128), (77, 3, 1000, 16), (1, 1, 1, 8),
-                                     (8192, 8, 128, 8)])
+                                     (8192, 8, 128, 8), (512, 8, 128, 64), (513, 8, 128, 64),
+                                     (1365, 3, 1024, 8)])
 def test_permute_bit_exact(T, K, E, H):
     ids = _ids(T, K, E, T + E, skew=(T >= 1000))
     rng = np.random.default_rng(5)
@@ -139,7 +174,10 @@ def test_permute_bit_exact(T, K, E, H):
     want = O.permute(ids, x, T=T, K=K, E=E, H=H)
     before = launches()
     got = gpu_permute(ids, x, T, K, E, H)
-    assert launched_since(before, "permute_place") == 1
+    # up to 8 chunks of 512 pairs: count, scan and place in one block
+    small = T * K <= 8 * 512
+    assert launched_since(before, "permute_small") == (1 if small else 0)
+    assert launched_since(before, "permute_place") == (0 if small else 1)
     for g, w_, name in zip(got, want, ("expert_offsets", "sorted_pair", "pair_to_row", "x_perm")):
         assert np.array_equal(g, w_), name
 
@@ -149,8 +187,15 @@ def test_permute_empty_batch_zeroes_offsets():
     assert np.array_equal(off, np.zeros(9, np.int32))
 
 
-def test_permute_flags_out_of_range_ids():
-    ids = np.array([[0, 1], [2, 9]], np.int32)
+@pytest.mark.parametrize("T", [2, 3000])
+def test_permute_flags_out_of_range_ids(T):
+    # bad ids are flagged and skipped on both the one-block and the chunked path
+    K, E = 2, 4
+    ids = _ids(T, K, E, 11)
+    ids[1, 1] = 9
+    ids[T - 1, 0] = -1
     m.moe_device_status(clear=True)
-    gpu_permute(ids, None, 2, 2, 4, 8)
+    off, sp, p2r, _ = gpu_permute(ids, None, T, K, E, 8)
     assert m.moe_device_status(clear=True) & m.STATUS_BAD_ID
+    counts = np.bincount(ids[(ids >= 0) & (ids < E)], minlength=E)
+    assert np.array_equal(np.diff(off), counts) and off[E] == T * K - 2
