@@ -940,9 +940,15 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   const int mode = g_pairing.load(std::memory_order_relaxed);
   const bool mcast = !a_row_gather && (mode == MOE_GEMM_MCAST || mode == MOE_GEMM_SPLIT) &&
                      ((I + 127) / 128) % 2 == 0;
+  // Few rows per expert (decode): each tile streams its weight rows from HBM
+  // and the tile count decides the balance; 128-wide tiles (64 gate + 64 up
+  // rows) double it, which cuts the idle tail of the last round (decode layer,
+  // 82 of 128 experts touched: 127 -> 115 us).  Tensor-bound loads keep 256.
+  const bool narrow = !a_row_gather && mode == MOE_GEMM_SINGLE &&
+                      static_cast<long long>(P) <= 16LL * G;
   CUtensorMap ta, tb;
-  if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, 128, op, "w13")) !=
-      MOE_OK)
+  if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, narrow ? 64 : 128, op,
+                      "w13")) != MOE_OK)
     return rc;
   if (a_row_gather) {
     ta = tb;  // unused: the gatherer warps read A rows directly
@@ -979,6 +985,7 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   }
   if (mcast)
     return launch<256, EPI_GATEUP, false, false, true>(op, ta, tb, p, tile_bound(P, G, I, 256), s);
+  if (narrow) return launch<128, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 64), s);
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
