@@ -73,7 +73,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 5 */
+int moe_abi_version(void);  /* 6 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -121,6 +121,41 @@ int moe_route_topk(const void* x_bf16, const void* w_router_bf16, const float* l
                    float* topk_w, float* logits_out, float* gate_logit_out, void* workspace,
                    size_t ws_bytes, void* stream);
 size_t moe_route_topk_workspace_size(int T, int E, int K);
+
+/* ------------------------------------------------------------------------
+ * moe_route_topk_ex -- the router forms the pages leave open: [I3094] keeps
+ * the grouped and sigmoid routers of DeepSeek-V2 and Dots3 out of its scope,
+ * and [PR509] "Honest gaps" says its grouped / bias / noaux_tc forms still
+ * throw.  The pages do not define them; this follows the published
+ * DeepSeek-V2 (softmax, groups scored by their best expert) and DeepSeek-V3
+ * (sigmoid scores, selection bias, groups scored by their two best experts)
+ * routers.  Logits as in moe_route_topk (GEMM, K split, logit_bias), then:
+ *   s_e   = l_e (scoring 0, softmax) or sigmoid(l_e) (scoring 1; the same
+ *           binary32 sigmoid as the shared-expert gate)
+ *   k_e   = s_e + select_bias[e] (sigmoid only; steers the choice, never
+ *           enters a weight), else s_e
+ *   groups: E / n_group contiguous experts each; score = best k (group_score
+ *           0) or best + second best k (1); the topk_group best groups stay
+ *           eligible (descending, ties to the lower group, NaN last)
+ *   choice: the K best k among eligible experts (descending, ties to the
+ *           lower id, NaN last)
+ *   weights: sigmoid: w_j = s_j / ((s_0 + s_1) + ... + s_{K-1}) from +0
+ *           (renormalize 1) or s_j (0); softmax: as moe_route_topk
+ * Given the same logits, ids and weights are bit-exact.  scoring 0 with
+ * n_group 1 and no select_bias is exactly moe_route_topk.
+ *   select_bias  f32 [E] or NULL (sigmoid scoring only)
+ *   n_group      1..64, divides E; topk_group 1..n_group; group_score 0 or 1
+ *                (1 needs groups of at least two experts)
+ *   K            <= topk_group * E / n_group (and the limits of moe_route_topk)
+ *   the other arguments, outputs, workspace and errors as moe_route_topk;
+ *   MOE_ERR_UNSUPPORTED for scoring > 1 or a select_bias with softmax.
+ * ---------------------------------------------------------------------- */
+int moe_route_topk_ex(const void* x_bf16, const void* w_router_bf16, const float* logit_bias,
+                      const float* select_bias, const void* w_shared_gate_bf16,
+                      const float* logits_in, int T, int H, int E, int K, int renormalize,
+                      int scoring, int n_group, int topk_group, int group_score,
+                      int32_t* topk_ids, float* topk_w, float* logits_out,
+                      float* gate_logit_out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_permute -- stable counting sort of the P = T*K (token, slot) pairs by

@@ -36,6 +36,7 @@ EXPORTS = (
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
     "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl",
     "moe_grouped_gemm_gateup_silu_bf16_shared", "moe_grouped_gemm_down_bf16_shared",
+    "moe_route_topk_ex",
 )
 
 
@@ -58,6 +59,8 @@ _SIGS = {
     "moe_route_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ,
                         _P], _I),
     "moe_route_topk_workspace_size": ([_I, _I, _I], _SZ),
+    "moe_route_topk_ex": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                           _P, _P, _P, _SZ, _P], _I),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
     "moe_permute_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
@@ -137,6 +140,18 @@ def moe_route_topk(x, w_router, logit_bias, w_shared_gate, logits_in, T, H, E, K
                               _ptr(logits_in), T, H, E, K, renormalize, scoring, n_group,
                               _ptr(topk_ids), _ptr(topk_w), _ptr(logits_out),
                               _ptr(gate_logit_out), _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_route_topk_ex(x, w_router, logit_bias, select_bias, w_shared_gate, logits_in, T, H, E,
+                      K, renormalize, scoring, n_group, topk_group, group_score, topk_ids, topk_w,
+                      logits_out, gate_logit_out, workspace, ws_bytes, stream=None, check=True):
+    """Grouped / sigmoid / bias-corrected router (see moe.h)."""
+    rc = lib().moe_route_topk_ex(_ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(select_bias),
+                                 _ptr(w_shared_gate), _ptr(logits_in), T, H, E, K, renormalize,
+                                 scoring, n_group, topk_group, group_score, _ptr(topk_ids),
+                                 _ptr(topk_w), _ptr(logits_out), _ptr(gate_logit_out),
+                                 _ptr(workspace), ws_bytes, _stream(stream))
     return _check(rc) if check else rc
 
 

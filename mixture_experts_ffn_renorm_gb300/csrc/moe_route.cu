@@ -23,6 +23,17 @@ int launch_router_logits(const void* x, const void* w_router, const float* bias,
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kMaxGroups = 64;   // n_group limit of the grouped router
+
+// The router forms beyond ungrouped softmax (selection bias, sigmoid scores,
+// expert groups); all off: the plain router.
+struct RouteEx {
+  const float* select_bias;  // [E] or null: added to the scores for the choice only
+  int scoring;               // 0 softmax (choice on the logits), 1 sigmoid
+  int n_group;               // contiguous expert groups (1: none)
+  int topk_group;            // groups that stay eligible
+  int group_score;           // 0: a group's best key; 1: its two best keys added
+};
 
 // Order-preserving 32-bit key of a logit for the selection: larger key = ranks
 // higher.  -0 and +0 share a key (they compare equal), every NaN gets key 0
@@ -35,17 +46,50 @@ __device__ __forceinline__ uint32_t rank_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// shared-expert gate logit of token t: a plain f32 dot product of x[t] and wsg
+// (one warp; the result from lane 0)
+__device__ __forceinline__ void shared_gate_logit(const uint16_t* __restrict__ x,
+                                                  const uint16_t* __restrict__ wsg, int H, int t,
+                                                  int lane, float* __restrict__ gl_out) {
+  const uint16_t* xr = x + static_cast<size_t>(t) * H;
+  float acc = 0.0f;
+  for (int h = lane * 8; h < H; h += 256) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(xr + h));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(wsg + h));
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc += __uint_as_float(aw[q] << 16) * __uint_as_float(bw[q] << 16);
+      acc += __uint_as_float(aw[q] & 0xFFFF0000u) * __uint_as_float(bw[q] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) gl_out[t] = acc;
+}
+
+// Does key a (expert ia) rank above key b (expert ib): larger first, ties to
+// the lower index, NaN last (the order of rank_key).
+__device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
+  const uint32_t ka = rank_key(a), kb = rank_key(b);
+  return ka > kb || (ka == kb && ia < ib);
+}
+
 // One warp selects the top-K of one token.  The weights' exps are then
 // evaluated by the whole block, one (token, rank) pair per thread, so that the
 // double-precision chain of exp_cr runs on full warps (GB300's FP64 rate is
 // low, and a warp instruction costs the same with 8 or 32 lanes active).
-template <int kPerLane>
+// kEx: the extended forms of RouteEx.  Each lane turns its logits into scores
+// (sigmoid_cr for sigmoid scoring) and keys (score + selection bias); the keys
+// go to shared memory, where lane g scores expert group g; the warp picks the
+// topk_group best groups, and the expert choice skips experts of the others.
+template <int kPerLane, bool kEx>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 topk_kernel(const float* __restrict__ logits, int n_part, const float* __restrict__ bias,
             float* __restrict__ logits_out, int T, int E, int K, int renormalize,
             const uint16_t* __restrict__ x, const uint16_t* __restrict__ wsg, int H,
             int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ gl_out,
-            unsigned long long* launches) {
+            unsigned long long* launches, RouteEx rx) {
   count_launch(launches, MOE_KID_ROUTE_TOPK);
   grid_dep_wait();
   grid_dep_launch();
@@ -75,9 +119,82 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
       v[i] = a;
     }
     uint32_t key[kPerLane];
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) key[i] = rank_key(v[i]);
+    float sc[kPerLane];      // what a chosen expert reports: its logit, or its sigmoid score
     uint32_t taken = 0;
+    if (!kEx) {
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        key[i] = rank_key(v[i]);
+        sc[i] = v[i];
+      }
+    } else {
+      extern __shared__ float s_dyn[];
+      float* s_key = s_dyn + static_cast<size_t>(wib) * E;
+      float* s_gsc = s_dyn + static_cast<size_t>(kWarpsPerBlock) * E + wib * kMaxGroups;
+      unsigned char* s_gok = reinterpret_cast<unsigned char*>(
+                                 s_dyn + static_cast<size_t>(kWarpsPerBlock) * (E + kMaxGroups)) +
+                             wib * kMaxGroups;
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        const int e = lane + 32 * i;
+        sc[i] = 0.0f;
+        float kv = 0.0f;
+        if (e < E) {
+          sc[i] = rx.scoring == 1 ? sigmoid_cr(v[i]) : v[i];
+          kv = rx.select_bias ? __fadd_rn(sc[i], __ldg(rx.select_bias + e)) : sc[i];
+          s_key[e] = kv;
+        }
+        key[i] = rank_key(kv);
+      }
+      __syncwarp();
+      // group scores: lane g scans group g in expert order
+      const int gs = E / rx.n_group;
+      for (int g = lane; g < rx.n_group; g += 32) {
+        int b0 = -1, b1 = -1;
+        for (int e = g * gs; e < g * gs + gs; ++e) {
+          if (b0 < 0 || ranks_above(s_key[e], e, s_key[b0], b0)) {
+            b1 = b0;
+            b0 = e;
+          } else if (b1 < 0 || ranks_above(s_key[e], e, s_key[b1], b1)) {
+            b1 = e;
+          }
+        }
+        s_gsc[g] = rx.group_score == 0 ? s_key[b0] : __fadd_rn(s_key[b0], s_key[b1]);
+        s_gok[g] = 0;
+      }
+      __syncwarp();
+      // the topk_group best groups (descending score, ties to the lower group)
+      constexpr int kGroupsPerLane = kMaxGroups / 32;
+      uint32_t gtaken = 0;
+      for (int j = 0; j < rx.topk_group; ++j) {
+        uint32_t bk = 0u, bid = 0xFFFFFFFFu;
+#pragma unroll
+        for (int q = 0; q < kGroupsPerLane; ++q) {
+          const int g = lane + 32 * q;
+          if (g < rx.n_group && !((gtaken >> q) & 1u)) {
+            const uint32_t k = rank_key(s_gsc[g]);
+            if (bid == 0xFFFFFFFFu || k > bk) {
+              bk = k;
+              bid = static_cast<uint32_t>(g);
+            }
+          }
+        }
+        const uint32_t top = __reduce_max_sync(0xffffffffu, bid == 0xFFFFFFFFu ? 0u : bk);
+        const uint32_t cand = (bid != 0xFFFFFFFFu && bk == top) ? bid : 0xFFFFFFFFu;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+        if (win != 0xFFFFFFFFu && static_cast<int>(win & 31u) == lane) {
+          gtaken |= 1u << (win >> 5);
+          s_gok[win] = 1;
+        }
+        __syncwarp();
+      }
+      // experts of the other groups are never chosen
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !s_gok[e / gs]) taken |= 1u << i;
+      }
+    }
     for (int j = 0; j < K; ++j) {
       // this lane's best untaken entry (ascending id, so ties keep the lower id)
       uint32_t bk = 0u, bid = 0xFFFFFFFFu;
@@ -88,7 +205,7 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
         if (e < E && !((taken >> i) & 1u) && (bid == 0xFFFFFFFFu || key[i] > bk)) {
           bk = key[i];
           bid = static_cast<uint32_t>(e);
-          bv = v[i];
+          bv = sc[i];
         }
       }
       // the warp's best: highest key, then lowest id among the lanes holding it
@@ -106,6 +223,18 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
     s_sel[wib][lane] = my_sel;
   }
   __syncthreads();
+  if (kEx && rx.scoring == 1) {
+    // sigmoid scores: w_j = s_j / ((s_0 + s_1) + ...) or s_j
+    if (!live) return;
+    float den = 0.0f;
+    for (int j = 0; j < K; ++j) den = __fadd_rn(den, s_sel[wib][j]);
+    if (lane < K) {
+      ids[static_cast<size_t>(t) * K + lane] = my_id;
+      w[static_cast<size_t>(t) * K + lane] = renormalize ? __fdiv_rn(my_sel, den) : my_sel;
+    }
+    if (wsg != nullptr) shared_gate_logit(x, wsg, H, t, lane, gl_out);
+    return;
+  }
   // e_j = exp(l_j - l_0) for every (token, rank) pair of the block
   const int n_live = min(kWarpsPerBlock, T - static_cast<int>(blockIdx.x) * kWarpsPerBlock);
   for (int q = threadIdx.x; q < n_live * K; q += blockDim.x) {
@@ -136,37 +265,21 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
     ids[static_cast<size_t>(t) * K + lane] = my_id;
     w[static_cast<size_t>(t) * K + lane] = __fdiv_rn(ex, S);
   }
-  if (wsg != nullptr) {
-    // shared-expert gate logit: a plain f32 dot product of x[t] and wsg
-    const uint16_t* xr = x + static_cast<size_t>(t) * H;
-    float acc = 0.0f;
-    for (int h = lane * 8; h < H; h += 256) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(xr + h));
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(wsg + h));
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc += __uint_as_float(aw[q] << 16) * __uint_as_float(bw[q] << 16);
-        acc += __uint_as_float(aw[q] & 0xFFFF0000u) * __uint_as_float(bw[q] & 0xFFFF0000u);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) gl_out[t] = acc;
-  }
+  if (wsg != nullptr) shared_gate_logit(x, wsg, H, t, lane, gl_out);
 }
 
 using TopkFn = void (*)(const float*, int, const float*, float*, int, int, int, int,
                         const uint16_t*, const uint16_t*, int, int32_t*, float*, float*,
-                        unsigned long long*);
+                        unsigned long long*, RouteEx);
 
+template <bool kEx>
 TopkFn pick_topk(int E) {
-  if (E <= 32) return topk_kernel<1>;
-  if (E <= 64) return topk_kernel<2>;
-  if (E <= 128) return topk_kernel<4>;
-  if (E <= 256) return topk_kernel<8>;
-  if (E <= 512) return topk_kernel<16>;
-  return topk_kernel<32>;
+  if (E <= 32) return topk_kernel<1, kEx>;
+  if (E <= 64) return topk_kernel<2, kEx>;
+  if (E <= 128) return topk_kernel<4, kEx>;
+  if (E <= 256) return topk_kernel<8, kEx>;
+  if (E <= 512) return topk_kernel<16, kEx>;
+  return topk_kernel<32, kEx>;
 }
 
 size_t logits_bytes(int T, int E) {
@@ -185,22 +298,14 @@ extern "C" size_t moe_route_topk_workspace_size(int T, int E, int K) {
   return logits_bytes(T, E) * static_cast<size_t>(router_splits(T, 1 << 20, E));
 }
 
-extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
-                              const float* logit_bias, const void* w_shared_gate_bf16,
-                              const float* logits_in, int T, int H, int E, int K, int renormalize,
-                              int scoring, int n_group, int32_t* topk_ids, float* topk_w,
-                              float* logits_out, float* gate_logit_out, void* workspace,
-                              size_t ws_bytes, void* stream) {
-  clear_error();
-  const char* op = "moe_route_topk";
-  if (scoring != 0)
-    return set_error(MOE_ERR_UNSUPPORTED,
-                     "%s: scoring=%d is not implemented; only ungrouped softmax (0) is", op,
-                     scoring);
-  if (n_group != 1)
-    return set_error(MOE_ERR_UNSUPPORTED,
-                     "%s: grouped routing (n_group=%d) is not implemented; only n_group=1 is", op,
-                     n_group);
+namespace moe {
+namespace {
+
+int route_impl(const char* op, const void* x_bf16, const void* w_router_bf16,
+               const float* logit_bias, const void* w_shared_gate_bf16, const float* logits_in,
+               int T, int H, int E, int K, int renormalize, const RouteEx& ex,
+               int32_t* topk_ids, float* topk_w, float* logits_out, float* gate_logit_out,
+               void* workspace, size_t ws_bytes, void* stream) {
   if (T < 0) return set_error(MOE_ERR_ARG, "%s: T=%d < 0", op, T);
   if (E < 1 || E > 1024) return set_error(MOE_ERR_ARG, "%s: E=%d outside [1, 1024]", op, E);
   if (K < 1 || K > E || K > 32)
@@ -257,11 +362,78 @@ extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
   }
   DeviceDiag diag = device_diag();
   const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const bool extended = ex.scoring != 0 || ex.n_group != 1 || ex.select_bias != nullptr;
+  const size_t smem = extended ? static_cast<size_t>(kWarpsPerBlock) *
+                                     ((E + kMaxGroups) * sizeof(float) + kMaxGroups)
+                               : 0;
   return launch_status(
-      launch_kernel(pick_topk(E), dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, nullptr, 0,
-                    logits, n_part, part_bias, sel_logits_out, T, E, K, renormalize,
-                    static_cast<const uint16_t*>(x_bf16),
+      launch_kernel(extended ? pick_topk<true>(E) : pick_topk<false>(E), dim3(blocks),
+                    dim3(kWarpsPerBlock * 32), smem, s, nullptr, 0, logits, n_part, part_bias,
+                    sel_logits_out, T, E, K, renormalize, static_cast<const uint16_t*>(x_bf16),
                     static_cast<const uint16_t*>(w_shared_gate_bf16), H, topk_ids, topk_w,
-                    gate_logit_out, diag.launches),
+                    gate_logit_out, diag.launches, ex),
       op);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_route_topk(const void* x_bf16, const void* w_router_bf16,
+                              const float* logit_bias, const void* w_shared_gate_bf16,
+                              const float* logits_in, int T, int H, int E, int K, int renormalize,
+                              int scoring, int n_group, int32_t* topk_ids, float* topk_w,
+                              float* logits_out, float* gate_logit_out, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_route_topk";
+  if (scoring != 0)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "%s: scoring=%d is not implemented here; only ungrouped softmax (0) is "
+                     "(sigmoid scores: moe_route_topk_ex)", op, scoring);
+  if (n_group != 1)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "%s: grouped routing (n_group=%d) is not implemented here; only n_group=1 "
+                     "is (expert groups: moe_route_topk_ex)", op, n_group);
+  const RouteEx ex{nullptr, 0, 1, 1, 0};
+  return route_impl(op, x_bf16, w_router_bf16, logit_bias, w_shared_gate_bf16, logits_in, T, H,
+                    E, K, renormalize, ex, topk_ids, topk_w, logits_out, gate_logit_out,
+                    workspace, ws_bytes, stream);
+}
+
+extern "C" int moe_route_topk_ex(const void* x_bf16, const void* w_router_bf16,
+                                 const float* logit_bias, const float* select_bias,
+                                 const void* w_shared_gate_bf16, const float* logits_in, int T,
+                                 int H, int E, int K, int renormalize, int scoring, int n_group,
+                                 int topk_group, int group_score, int32_t* topk_ids,
+                                 float* topk_w, float* logits_out, float* gate_logit_out,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_route_topk_ex";
+  if (scoring != 0 && scoring != 1)
+    return set_error(MOE_ERR_UNSUPPORTED, "%s: scoring=%d is not 0 (softmax) or 1 (sigmoid)", op,
+                     scoring);
+  if (select_bias && scoring != 1)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "%s: a selection bias is implemented for sigmoid scores only", op);
+  if (E < 1 || E > 1024) return set_error(MOE_ERR_ARG, "%s: E=%d outside [1, 1024]", op, E);
+  if (n_group < 1 || n_group > kMaxGroups || E % n_group != 0)
+    return set_error(MOE_ERR_ARG, "%s: n_group=%d must divide E=%d and be at most %d", op,
+                     n_group, E, kMaxGroups);
+  if (topk_group < 1 || topk_group > n_group)
+    return set_error(MOE_ERR_ARG, "%s: topk_group=%d outside [1, n_group=%d]", op, topk_group,
+                     n_group);
+  if (group_score != 0 && group_score != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_score=%d is not 0 (best) or 1 (two best)", op,
+                     group_score);
+  if (group_score == 1 && E / n_group < 2)
+    return set_error(MOE_ERR_ARG, "%s: two-best group scores need groups of two experts", op);
+  if (K > topk_group * (E / n_group))
+    return set_error(MOE_ERR_ARG, "%s: K=%d exceeds the %d experts of the eligible groups", op,
+                     K, topk_group * (E / n_group));
+  if (select_bias && (reinterpret_cast<uintptr_t>(select_bias) & 3u))
+    return set_error(MOE_ERR_ALIGN, "%s: select_bias must be 4-byte aligned", op);
+  const RouteEx ex{select_bias, scoring, n_group, topk_group, group_score};
+  return route_impl(op, x_bf16, w_router_bf16, logit_bias, w_shared_gate_bf16, logits_in, T, H,
+                    E, K, renormalize, ex, topk_ids, topk_w, logits_out, gate_logit_out,
+                    workspace, ws_bytes, stream);
 }

@@ -50,6 +50,7 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_exp_f32_array": ([_P, _P, _I64], None),
         "oracle_sigmoid_f32": ([_F], _F),
         "oracle_route_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+        "oracle_route_topk_ex": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
         "oracle_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
         "oracle_gateup_silu": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I], _I),
         "oracle_down": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P], _I),
@@ -132,6 +133,18 @@ def route_topk(x=None, w_router=None, logit_bias=None, w_shared_gate=None, logit
                                  _ptr(ids), _ptr(w), _ptr(logits), _ptr(gl))
     _check(rc, "route_topk")
     return ids, w, logits, gl
+
+
+def route_topk_ex(logits, select_bias=None, *, T, E, K, renormalize=1, scoring=0, n_group=1,
+                  topk_group=1, group_score=0):
+    """The grouped / sigmoid / bias-corrected router forms on given f32 logits [T, E]."""
+    ids = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float32)
+    rc = lib().oracle_route_topk_ex(_ptr(np.ascontiguousarray(logits, np.float32)),
+                                    _ptr(select_bias), T, E, K, renormalize, scoring, n_group,
+                                    topk_group, group_score, _ptr(ids), _ptr(w))
+    _check(rc, "route_topk_ex")
+    return ids, w
 
 
 def permute(topk_ids, x=None, *, T, K, E, H=0):

@@ -257,6 +257,125 @@ int oracle_route_topk(const uint16_t* x, const uint16_t* w_router, const float* 
 }
 
 /* ------------------------------------------------------------------ */
+/* Router forms the pages name as open gaps (issue #3094 leaves the grouped */
+/* and sigmoid routers of DeepSeek-V2 and Dots3 to separate work; PR #509    */
+/* "Honest gaps" says its grouped / bias / noaux_tc forms still throw).  The */
+/* pages do not define them; READING, after the published DeepSeek-V2 and    */
+/* DeepSeek-V3 routers:                                                      */
+/*   scores   softmax (scoring 0): selection on the logits, weights as in    */
+/*            topk_row; sigmoid (scoring 1): s_e = sigmoid(l_e), the same    */
+/*            sigmoid as the shared-expert gate                              */
+/*   keys     k_e = s_e + select_bias[e] (sigmoid only; the bias steers the  */
+/*            choice, never the weights), else the scores (logits for softmax)*/
+/*   groups   E experts in n_group contiguous groups of E / n_group; a       */
+/*            group's score is its largest key (group_score 0) or its two    */
+/*            largest keys added, largest first (group_score 1); the          */
+/*            topk_group best groups (descending, ties to the lower group,   */
+/*            NaN last) stay eligible                                        */
+/*   choice   the K best keys among eligible experts (descending, ties to     */
+/*            the lower id, NaN last)                                        */
+/*   weights  sigmoid: w_j = s_j / ((s_0 + s_1) + ... + s_{K-1}) from +0      */
+/*            (renormalize 1) or s_j (renormalize 0); softmax: as topk_row    */
+/* ------------------------------------------------------------------ */
+
+/* the k-th best (k = 0, 1) key of experts [e0, e1) in ranks_above order */
+static float group_score(const float* key, int e0, int e1, int mode) {
+  int b0 = -1, b1 = -1;
+  for (int e = e0; e < e1; ++e) {
+    if (b0 < 0 || ranks_above(key[e], e, key[b0], b0)) {
+      b1 = b0;
+      b0 = e;
+    } else if (b1 < 0 || ranks_above(key[e], e, key[b1], b1)) {
+      b1 = e;
+    }
+  }
+  if (mode == 0) return key[b0];
+  return key[b0] + key[b1];
+}
+
+static void topk_row_ex(const float* l, const float* select_bias, int E, int K, int renormalize,
+                        int scoring, int n_group, int topk_group, int gmode, int32_t* ids,
+                        float* w) {
+  float* key = (float*)malloc(sizeof(float) * (size_t)E);
+  float* sc = (float*)malloc(sizeof(float) * (size_t)E);
+  unsigned char* ok = (unsigned char*)calloc((size_t)E, 1);
+  for (int e = 0; e < E; ++e) {
+    sc[e] = scoring == 1 ? oracle_sigmoid_f32(l[e]) : l[e];
+    key[e] = select_bias ? sc[e] + select_bias[e] : sc[e];
+  }
+  /* eligible groups: the topk_group best by group score */
+  const int gs = E / n_group;
+  float gsc[1024];
+  int gchosen[1024];
+  for (int g = 0; g < n_group; ++g) gsc[g] = group_score(key, g * gs, g * gs + gs, gmode);
+  for (int j = 0; j < topk_group; ++j) {
+    int best = -1;
+    for (int g = 0; g < n_group; ++g) {
+      int taken = 0;
+      for (int q = 0; q < j; ++q)
+        if (gchosen[q] == g) taken = 1;
+      if (taken) continue;
+      if (best < 0 || ranks_above(gsc[g], g, gsc[best], best)) best = g;
+    }
+    gchosen[j] = best;
+    for (int e = best * gs; e < best * gs + gs; ++e) ok[e] = 1;
+  }
+  /* the K best eligible experts */
+  int32_t chosen[32] = {0};
+  for (int j = 0; j < K; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (!ok[e]) continue;
+      int taken = 0;
+      for (int q = 0; q < j; ++q)
+        if (chosen[q] == e) taken = 1;
+      if (taken) continue;
+      if (best < 0 || ranks_above(key[e], e, key[best], best)) best = e;
+    }
+    chosen[j] = best;
+    ids[j] = best;
+  }
+  if (scoring == 1) {
+    float den = 0.0f;
+    for (int j = 0; j < K; ++j) den = den + sc[chosen[j]];
+    for (int j = 0; j < K; ++j) w[j] = renormalize ? sc[chosen[j]] / den : sc[chosen[j]];
+  } else {
+    float m = l[chosen[0]];
+    float ex[32];
+    for (int j = 0; j < K; ++j) ex[j] = oracle_exp_f32(l[chosen[j]] - m);
+    float den = 0.0f;
+    if (renormalize) {
+      for (int j = 0; j < K; ++j) den = den + ex[j];
+    } else {
+      for (int e = 0; e < E; ++e) den = den + oracle_exp_f32(l[e] - m);
+    }
+    for (int j = 0; j < K; ++j) w[j] = ex[j] / den;
+  }
+  free(key);
+  free(sc);
+  free(ok);
+}
+
+/* the extended router on given logits (the GEMM part is oracle_route_topk's) */
+int oracle_route_topk_ex(const float* logits, const float* select_bias, int T, int E, int K,
+                         int renormalize, int scoring, int n_group, int topk_group,
+                         int group_score_mode, int32_t* topk_ids, float* topk_w) {
+  if (T < 0 || E <= 0 || E > 1024 || K < 1 || K > 32) return ORA_ERR_ARG;
+  if (scoring != 0 && scoring != 1) return ORA_ERR_UNSUPPORTED;
+  if (select_bias && scoring != 1) return ORA_ERR_UNSUPPORTED;
+  if (n_group < 1 || E % n_group != 0 || topk_group < 1 || topk_group > n_group)
+    return ORA_ERR_ARG;
+  if (group_score_mode != 0 && group_score_mode != 1) return ORA_ERR_ARG;
+  if (group_score_mode == 1 && E / n_group < 2) return ORA_ERR_ARG;
+  if (K > topk_group * (E / n_group)) return ORA_ERR_ARG;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    topk_row_ex(logits + (int64_t)t * E, select_bias, E, K, renormalize, scoring, n_group,
+                topk_group, group_score_mode, topk_ids + (int64_t)t * K, topk_w + (int64_t)t * K);
+  return ORA_OK;
+}
+
+/* ------------------------------------------------------------------ */
 /* a3: permute into expert-contiguous order (stable counting sort)      */
 /* The pages' expert path keeps P = T*K permuted bf16 rows of H (PR #509  */
 /* review, finding 2) and groups them over                                */

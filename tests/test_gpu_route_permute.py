@@ -127,6 +127,90 @@ def test_router_k_split_matches_unsplit_within_bound(T, H, E):
     assert same.mean() >= 0.95
 
 
+EX_CASES = [
+    # E, K, scoring, n_group, topk_group, group_score, select bias
+    (256, 8, 1, 8, 4, 1, True),      # DeepSeek-V3 shape
+    (160, 6, 0, 8, 3, 0, False),     # DeepSeek-V2 shape
+    (64, 4, 1, 4, 2, 1, False),
+    (128, 8, 1, 1, 1, 0, True),      # sigmoid + bias, no groups
+    (1024, 8, 1, 64, 8, 1, True),    # widest rows and most groups
+    (12, 3, 0, 6, 2, 1, False),      # two experts per group
+]
+
+
+@pytest.mark.parametrize("E,K,scoring,n_group,topk_group,gscore,with_bias", EX_CASES)
+@pytest.mark.parametrize("renorm", [1, 0])
+def test_router_ex_bit_exact_from_logits(E, K, scoring, n_group, topk_group, gscore, with_bias,
+                                         renorm):
+    rng = np.random.default_rng(E + 13 * K + n_group)
+    T = 133
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[0, : E // 2] = l[0, E // 2:]      # ties between groups and between experts
+    l[1, :] = 0.0
+    l[2, 3] = np.nan
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32) if with_bias else None
+    want_ids, want_w = O.route_topk_ex(l, bias, T=T, E=E, K=K, renormalize=renorm,
+                                       scoring=scoring, n_group=n_group, topk_group=topk_group,
+                                       group_score=gscore)
+    ids = empty((T, K), torch.int32)
+    w = empty((T, K), torch.float32)
+    before = launches()
+    m.moe_route_topk_ex(None, None, None, None if bias is None else to_dev(bias), None, to_dev(l),
+                        T, 8, E, K, renorm, scoring, n_group, topk_group, gscore, ids, w, None,
+                        None, None, 0)
+    assert launched_since(before, "route_topk") == 1
+    assert np.array_equal(to_host(ids), want_ids)
+    # a NaN logit makes a full-softmax row NaN (renormalize 0): positions must
+    # agree; NaN payloads are not part of the contract
+    got = to_host(w)
+    ok = ~np.isnan(want_w)
+    assert np.array_equal(np.isnan(got), ~ok)
+    assert np.array_equal(got[ok].view(np.uint32), want_w[ok].view(np.uint32))
+
+
+def test_router_ex_through_the_logits_gemm():
+    # DeepSeek-V3-like routing of 16 and 300 tokens: logits from the tensor-core
+    # GEMM (with the K split), ids and weights exact given those logits
+    E, K, H = 256, 8, 1024
+    rng = np.random.default_rng(8)
+    wr = W.to_bf16_bits((0.02 * rng.standard_normal((E, H))).astype(np.float32))
+    bias = (0.05 * rng.standard_normal(E)).astype(np.float32)
+    for T in (16, 300):
+        x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+        ids = empty((T, K), torch.int32)
+        w = empty((T, K), torch.float32)
+        lo = empty((T, E), torch.float32)
+        wsz = m.moe_route_topk_workspace_size(T, E, K)
+        ws = empty((max(wsz, 16),), torch.uint8)
+        m.moe_route_topk_ex(to_dev(x), to_dev(wr), None, to_dev(bias), None, None, T, H, E, K, 1,
+                            1, 8, 4, 1, ids, w, lo, None, ws, wsz)
+        want_ids, want_w = O.route_topk_ex(to_host(lo), bias, T=T, E=E, K=K, scoring=1,
+                                           n_group=8, topk_group=4, group_score=1)
+        assert np.array_equal(to_host(ids), want_ids)
+        assert np.array_equal(to_host(w).view(np.uint32), want_w.view(np.uint32))
+
+
+def test_router_ex_refusals():
+    T, E = 4, 16
+    logits = to_dev(np.zeros((T, E), np.float32))
+    ids = empty((T, 8), torch.int32)
+    w = empty((T, 8), torch.float32)
+    bias = to_dev(np.zeros(E, np.float32))
+    before = launches()
+    for args, code in (((2, 1, 1, 0, 2, None), m.ERR_UNSUPPORTED),     # scoring 2
+                       ((0, 1, 1, 0, 2, bias), m.ERR_UNSUPPORTED),     # bias with softmax
+                       ((1, 3, 1, 0, 2, None), m.ERR_ARG),             # 3 does not divide 16
+                       ((1, 4, 5, 0, 2, None), m.ERR_ARG),             # topk_group > n_group
+                       ((1, 16, 2, 1, 2, None), m.ERR_ARG),            # two-best of one expert
+                       ((1, 8, 1, 0, 3, None), m.ERR_ARG)):            # K > eligible experts
+        scoring, n_group, topk_group, gscore, k, b = args
+        with pytest.raises(m.MoeError) as ei:
+            m.moe_route_topk_ex(None, None, None, b, None, logits, T, 8, E, k, 1, scoring, n_group,
+                                topk_group, gscore, ids, w, None, None, None, 0)
+        assert ei.value.code == code
+    assert launches() == before
+
+
 def test_router_refusals():
     T, E, K = 4, 8, 2
     logits = np.zeros((T, E), np.float32)

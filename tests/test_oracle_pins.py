@@ -247,6 +247,126 @@ def test_router_refuses_grouped_and_sigmoid_scoring():
         O.route_topk(logits_in=logits, T=2, H=1, E=8, K=9)
 
 
+# ------------------------------------------------------------------ router forms beyond
+# the pages' ungrouped softmax (grouped, sigmoid, bias-corrected): pinned by a
+# sort-based NumPy formulation and by the cases that reduce to the plain router
+def _np_route_ex(l, bias, K, scoring, n_group, topk_group, gmode, renorm):
+    """Sort-based restatement: group scores by np.sort, group and expert choice
+    by np.lexsort (descending key, then lower index), NaN keys last."""
+    T, E = l.shape
+    ids = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float32)
+    gs = E // n_group
+    for t in range(T):
+        if scoring == 1:
+            sc = np.array([O.lib().oracle_sigmoid_f32(float(v)) for v in l[t]], np.float32)
+        else:
+            sc = l[t].copy()
+        key = (sc + bias).astype(np.float32) if bias is not None else sc
+        kk = np.where(np.isnan(key), -np.inf, key).astype(np.float64)
+        nanr = np.isnan(key).astype(np.int64)
+        g_score = []
+        for g in range(n_group):
+            blk = key[g * gs:(g + 1) * gs]
+            order = np.lexsort((np.arange(gs), -np.where(np.isnan(blk), -np.inf, blk), np.isnan(blk)))
+            top = blk[order]
+            g_score.append(top[0] if gmode == 0 else np.float32(top[0] + top[1]))
+        g_score = np.array(g_score, np.float32)
+        gorder = np.lexsort((np.arange(n_group), -np.where(np.isnan(g_score), -np.inf, g_score),
+                             np.isnan(g_score)))
+        eligible = np.zeros(E, bool)
+        for g in gorder[:topk_group]:
+            eligible[g * gs:(g + 1) * gs] = True
+        cand = np.nonzero(eligible)[0]
+        order = np.lexsort((cand, -kk[cand], nanr[cand]))
+        sel = cand[order[:K]]
+        ids[t] = sel
+        if scoring == 1:
+            den = np.float32(0.0)
+            for j in range(K):
+                den = np.float32(den + sc[sel[j]])
+            w[t] = [np.float32(sc[j] / den) if renorm else sc[j] for j in sel]
+        else:
+            m = sc[sel[0]]
+            ex = [O.lib().oracle_exp_f32(float(np.float32(sc[j] - m))) for j in sel]
+            den = np.float32(0.0)
+            for e in ex:
+                den = np.float32(den + np.float32(e))
+            w[t] = [np.float32(np.float32(e) / den) for e in ex]
+    return ids, w
+
+
+@pytest.mark.parametrize("E,K,n_group,topk_group,gmode,scoring,with_bias", [
+    (256, 8, 8, 4, 1, 1, True),     # DeepSeek-V3 shape: sigmoid, bias, sum-of-top-2 groups
+    (160, 6, 8, 3, 0, 0, False),    # DeepSeek-V2 shape: softmax, max-of-group
+    (64, 4, 4, 2, 1, 1, False),
+    (64, 4, 16, 16, 0, 1, True),    # every group eligible: the plain top-k of the keys
+    (8, 2, 8, 2, 0, 0, False),      # one expert per group
+])
+def test_router_ex_matches_sort_based_restatement(E, K, n_group, topk_group, gmode, scoring,
+                                                  with_bias):
+    rng = np.random.default_rng(E + K + n_group)
+    T = 23
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[0, : E // 2] = l[0, E // 2:]           # exact ties between groups and experts
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32) if with_bias else None
+    ids, w = O.route_topk_ex(l, bias, T=T, E=E, K=K, scoring=scoring, n_group=n_group,
+                             topk_group=topk_group, group_score=gmode)
+    want_ids, want_w = _np_route_ex(l, bias, K, scoring, n_group, topk_group, gmode, 1)
+    assert np.array_equal(ids, want_ids)
+    assert np.array_equal(w.view(np.uint32), want_w.view(np.uint32))
+    # the chosen experts lie in at most topk_group groups
+    assert np.all([len(set((r // (E // n_group)).tolist())) <= topk_group for r in ids])
+    # renormalised weights sum to one within K roundings
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= K * 2.0**-23)
+
+
+def test_router_ex_reduces_to_the_plain_router():
+    rng = np.random.default_rng(4)
+    T, E, K = 31, 64, 6
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    plain_ids, plain_w, _, _ = O.route_topk(logits_in=l, T=T, H=1, E=E, K=K)
+    # softmax, one group
+    ids, w = O.route_topk_ex(l, T=T, E=E, K=K)
+    assert np.array_equal(ids, plain_ids) and np.array_equal(w, plain_w)
+    # softmax, every group eligible
+    ids, w = O.route_topk_ex(l, T=T, E=E, K=K, n_group=8, topk_group=8)
+    assert np.array_equal(ids, plain_ids) and np.array_equal(w, plain_w)
+    # sigmoid is monotone: without a bias it chooses what softmax chooses, and
+    # its weights are the chosen sigmoids over their sum
+    ids, w = O.route_topk_ex(l, T=T, E=E, K=K, scoring=1)
+    assert np.array_equal(ids, plain_ids)
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(l, ids, 1).astype(np.float64)))
+    assert np.allclose(w, s / s.sum(1, keepdims=True), rtol=1e-6, atol=0)
+
+
+def test_router_ex_bias_steers_choice_not_weights():
+    T, E, K = 3, 16, 2
+    l = np.zeros((T, E), np.float32)
+    l[:, 5] = 2.0
+    bias = np.zeros(E, np.float32)
+    bias[11] = 10.0                       # expert 11 is always chosen first ...
+    ids, w = O.route_topk_ex(l, bias, T=T, E=E, K=K, scoring=1)
+    assert np.all(ids[:, 0] == 11) and np.all(ids[:, 1] == 5)
+    # ... but weighs by its own score sigmoid(0) = 0.5 exactly, not by the bias
+    s5 = np.float32(1.0) / np.float32(1.0 + np.float32(math.exp(-2.0)))
+    den = np.float32(np.float32(0.5) + s5)
+    assert np.all(w[:, 0] == np.float32(np.float32(0.5) / den))
+    ids, w = O.route_topk_ex(l, bias, T=T, E=E, K=K, scoring=1, renormalize=0)
+    assert np.all(w[:, 0] == np.float32(0.5))
+
+
+def test_router_ex_refusals():
+    l = np.zeros((2, 16), np.float32)
+    for kw in (dict(scoring=2), dict(n_group=3, topk_group=1), dict(n_group=4, topk_group=5),
+               dict(n_group=16, topk_group=1, group_score=1), dict(n_group=8, topk_group=1, K=3)):
+        k = kw.pop("K", 2)
+        with pytest.raises(ValueError):
+            O.route_topk_ex(l, T=2, E=16, K=k, **kw)
+    with pytest.raises(ValueError):           # a selection bias only with sigmoid scores
+        O.route_topk_ex(l, np.zeros(16, np.float32), T=2, E=16, K=2, scoring=0)
+
+
 def test_shared_gate_logit_is_a_dot_product():
     T, H, E = 5, 64, 8
     x, wr, _ = _tiny_router_case(T, H, E)
