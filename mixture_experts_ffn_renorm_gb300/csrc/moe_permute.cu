@@ -13,9 +13,10 @@
 //           rank of a pair among equal experts of its step comes from
 //           __match_any_sync, so rows inside an expert ascend with p
 //   gather  (optional) x_perm[row] = x[sorted_pair[row] / K], 16 bytes a thread
-// Up to kSmallChunks chunks (decode-sized batches) count, scan and place run in
-// one block (permute_small) with the histogram in shared memory: the same
-// steps, one launch instead of three.
+// Up to kSmallChunks chunks whose histograms fit in 48 KB of shared memory
+// (decode batches; the large layer's 16384 pairs over 256 experts) count, scan
+// and place run in one block (permute_small): the same steps, one launch
+// instead of three.
 // Everything is a function of the ids alone: no atomics decide an order.
 #include "moe_common.cuh"
 
@@ -189,8 +190,8 @@ permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorte
 
 // Count, scan and place for n_chunks <= kSmallChunks in one block: warp c owns
 // chunk c as in permute_count / permute_place; the chunk histograms and the
-// expert offsets stay in shared memory ([kSmallChunks][E] + [E] ints).
-constexpr int kSmallChunks = 8;
+// expert offsets stay in shared memory ([n_chunks][E] + [E] ints).
+constexpr int kSmallChunks = 32;
 __global__ void __launch_bounds__(kSmallChunks * 32)
 permute_small(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
               int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair,
@@ -200,16 +201,16 @@ permute_small(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   grid_dep_wait();
   grid_dep_launch();
   extern __shared__ int32_t sh[];
-  __shared__ int32_t warp_sum[kSmallChunks];
-  int32_t* hist = sh;                         // [kSmallChunks][E]
-  int32_t* base = sh + kSmallChunks * E;      // [E]: first row of each expert
+  __shared__ int32_t warp_sum[kSmallChunks];   // one per warp
+  int32_t* hist = sh;                         // [n_chunks][E]
+  int32_t* base = sh + n_chunks * E;          // [E]: first row of each expert
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kT = kSmallChunks * 32;
   // 1. per-chunk histograms
   int32_t* h = hist + warp * E;
-  for (int e = lane; e < E; e += 32) h[e] = 0;
-  __syncwarp();
   if (warp < n_chunks) {
+    for (int e = lane; e < E; e += 32) h[e] = 0;
+    __syncwarp();
     const int p0 = warp * kChunk, p1 = min(P, p0 + kChunk);
     bool bad = false;
     for (int p = p0 + lane; p < p1; p += 32) {
@@ -350,8 +351,8 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
   int32_t* hist = static_cast<int32_t*>(workspace);
   const int blocks = (n_chunks + kWarps - 1) / kWarps;
   const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(int32_t);
-  if (n_chunks > 0 && n_chunks <= kSmallChunks) {
-    const size_t smem_small = static_cast<size_t>(kSmallChunks + 1) * E * sizeof(int32_t);
+  const size_t smem_small = static_cast<size_t>(n_chunks + 1) * E * sizeof(int32_t);
+  if (n_chunks > 0 && n_chunks <= kSmallChunks && smem_small <= 48 * 1024) {
     int rc = launch_status(launch_kernel(permute_small, dim3(1), dim3(kSmallChunks * 32),
                                          smem_small, s, nullptr, 0, topk_ids,
                                          static_cast<int>(P), E, n_chunks, expert_offsets,

@@ -250,7 +250,8 @@ def _ids(T, K, E, seed, skew=False):
 @pytest.mark.parametrize("T,K,E,H", [(4, 2, 8, 64), (16, 8, 128, 2048), (1000, 8, 128, 64),
                                      (2048, 8, 256, 128), (77, 3, 1000, 16), (1, 1, 1, 8),
                                      (8192, 8, 128, 8), (512, 8, 128, 64), (513, 8, 128, 64),
-                                     (1365, 3, 1024, 8)])
+                                     (1365, 3, 1024, 8), (2048, 8, 256, 64), (2049, 8, 256, 8),
+                                     (2048, 8, 512, 8)])
 def test_permute_bit_exact(T, K, E, H):
     ids = _ids(T, K, E, T + E, skew=(T >= 1000))
     rng = np.random.default_rng(5)
@@ -258,8 +259,9 @@ def test_permute_bit_exact(T, K, E, H):
     want = O.permute(ids, x, T=T, K=K, E=E, H=H)
     before = launches()
     got = gpu_permute(ids, x, T, K, E, H)
-    # up to 8 chunks of 512 pairs: count, scan and place in one block
-    small = T * K <= 8 * 512
+    # up to 32 chunks of 512 pairs whose histograms fit in 48 KB: one block
+    chunks = (T * K + 511) // 512
+    small = chunks <= 32 and (chunks + 1) * E * 4 <= 48 * 1024
     assert launched_since(before, "permute_small") == (1 if small else 0)
     assert launched_since(before, "permute_place") == (0 if small else 1)
     for g, w_, name in zip(got, want, ("expert_offsets", "sorted_pair", "pair_to_row", "x_perm")):
