@@ -249,6 +249,61 @@ def combine_gate_workload(dev, iters=20):
     return {"workload": cfg.name, "us": us, "gbs": nbytes / us / 1e3, "bytes": nbytes}
 
 
+def combine_arms(dev, iters=20):
+    """Every dtype arm of the combine/gate and combine ops on the bandwidth
+    workload's shape (T=4096, K=8, H=2048, weighted): microseconds and GB/s per
+    call, back to back over two input copies (more than L2)."""
+    import torch
+
+    import mixture_experts_ffn_renorm_gb300 as m
+
+    T, K, H = 4096, 8, 2048
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    tdt = {m.F32: torch.float32, m.BF16: torch.bfloat16}
+    size = {m.F32: 4, m.BF16: 2}
+    w = torch.rand((T, K), device=dev, generator=g)
+    gl = torch.randn((T,), device=dev, generator=g)
+    ws = torch.empty((m.moe_gate_workspace_size(T),), dtype=torch.uint8, device=dev)
+    out = {}
+    arms = [(m.BF16, m.BF16, m.BF16), (m.F32, m.F32, m.F32), (m.BF16, m.F32, m.F32),
+            (m.F32, m.BF16, m.BF16), (m.BF16, m.BF16, m.F32), (m.F32, m.F32, m.BF16)]
+    name = {m.F32: "f32", m.BF16: "bf16"}
+    for eo_dt, sd_dt, o_dt in arms:
+        sets = []
+        for _ in range(2):
+            eo = torch.randn((T, K, H), device=dev, generator=g).to(tdt[eo_dt])
+            sd = torch.randn((T, H), device=dev, generator=g).to(tdt[sd_dt])
+            o = torch.empty((T, H), dtype=tdt[o_dt], device=dev)
+            sets.append((eo, sd, o))
+        for op in ("combine_gate", "combine"):
+            def call(i):
+                eo, sd, o = sets[i % 2]
+                if op == "combine_gate":
+                    m.moe_combine_gate(eo, eo_dt, w, sd, sd_dt, gl, 1.0, T, K, H, o, o_dt, ws,
+                                       ws.numel())
+                else:
+                    m.moe_combine(eo, eo_dt, w, sd, sd_dt, 1.0, T, K, H, o, o_dt)
+            for i in range(4):
+                call(i)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(iters):
+                call(i)
+            e1.record()
+            torch.cuda.synchronize()
+            us = 1000.0 * e0.elapsed_time(e1) / iters
+            nbytes = T * K * H * size[eo_dt] + T * H * (size[sd_dt] + size[o_dt]) + T * K * 4
+            if op == "combine_gate":
+                nbytes += T * 4
+            out[f"{op} eo={name[eo_dt]} sd={name[sd_dt]} out={name[o_dt]}"] = {
+                "us": us, "gbs": nbytes / us / 1e3, "bytes": nbytes}
+        del sets
+    return out
+
+
 def oracle_tokens_per_s(cfg, d, seconds=10.0):
     """Time the CPU oracle on a bounded sample of the workload's tokens."""
     import oracle as O
@@ -320,13 +375,17 @@ def run_combine_only(args):
     torch.cuda.set_device(dev)
     pk, pk_src = peaks()
     cg = combine_gate_workload(dev, iters=args.steps)
+    arms = combine_arms(dev, iters=args.steps)
+    for v in arms.values():
+        v["frac_hbm"] = v["gbs"] / pk["hbm_gbs"]
     line = {"metric": "combine/gate GB/s (bandwidth workload)", "value": cg["gbs"], "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": 3, "ms_per_step": cg["us"] / 1000.0,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": cg["workload"]},
             "roofline": {"bound": "hbm", "achieved": cg["gbs"], "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": cg["gbs"] / pk["hbm_gbs"],
-                         "peak_source": pk_src, "traffic": None}}
+                         "peak_source": pk_src, "traffic": None},
+            "components": {"dtype_arms": arms}}
     print(json.dumps(line), flush=True)
     return 0
 

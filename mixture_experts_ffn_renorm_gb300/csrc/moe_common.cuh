@@ -24,6 +24,7 @@ struct DeviceDiag {
 };
 DeviceDiag device_diag();  // resolves the symbols on first use per device
 int check_launch(const char* what);  // cudaGetLastError -> MOE_ERR_CUDA
+int sm_count();                      // SMs of the current device (cached per device)
 // result of a cudaLaunchKernelEx -> MOE_OK or MOE_ERR_CUDA (sticky error cleared)
 inline int launch_status(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return MOE_OK;

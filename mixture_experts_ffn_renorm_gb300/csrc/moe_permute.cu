@@ -302,8 +302,9 @@ namespace {
 int gather(const char* op, const void* x_bf16, void* x_perm_bf16, const int32_t* sorted_pair,
            long long P, int K, int H, cudaStream_t s, const DeviceDiag& diag) {
   if (!x_perm_bf16) return MOE_OK;
-  long long g = (P + 7) / 8;  // 8 rows (warps) per block
-  if (g > 152LL * 32) g = 152LL * 32;
+  long long g = (P + 7) / 8;  // 8 rows (warps) per block, at most 32 blocks per SM
+  const long long cap = 32LL * sm_count();
+  if (g > cap) g = cap;
   return launch_status(
       launch_kernel(permute_gather, dim3(static_cast<unsigned>(g)), dim3(256), 0, s, nullptr, 0,
                     static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P), K, H,
