@@ -49,6 +49,7 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int kSmemBudget = 227 * 1024 - 11 * 1024 - 16 * 1024;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr int kStgBytes = 32 * 128;  // epilogue staging: 32 rows x 64 bf16 per warp
+constexpr int kNarrowRows = 32;      // rows per tile when experts hold few rows
 
 enum Epi { EPI_GATEUP = 0, EPI_DOWN = 1, EPI_F32 = 2 };
 
@@ -87,17 +88,17 @@ struct Params {
   int kid;
 };
 
-// Stage ring depth: as many stages of `stage_bytes` as fit the budget, at most 8.
+// Stage ring depth: as many stages of `stage_bytes` as fit the budget, at most 12.
 __host__ __device__ constexpr int stages_for_bytes(int stage_bytes) {
-  return kSmemBudget / stage_bytes > 8 ? 8 : kSmemBudget / stage_bytes;
+  return kSmemBudget / stage_bytes > 12 ? 12 : kSmemBudget / stage_bytes;
 }
 
-template <int kStages, int kBBytes>
+template <int kStages, int kBBytes, int kABytes = A_BYTES>
 struct Smem {
   static_assert(kStages >= 2, "stage ring too shallow");
   static constexpr int B_BYTES = kBBytes;
   static constexpr int STAGE_A = 0;
-  static constexpr int STAGE_B = kStages * A_BYTES;
+  static constexpr int STAGE_B = kStages * kABytes;
   static constexpr int STAGE_EPI = STAGE_B + kStages * B_BYTES;   // 4 epilogue staging buffers
   static constexpr int BARS = STAGE_EPI + 4 * kStgBytes;
   // full[kStages], empty[kStages], tfull[2], tempty[2], drain
@@ -113,18 +114,27 @@ struct Smem {
 //   kN      MMA N (accumulator columns per tile)
 //   kPair   CTA pair (cta_group::2): M = 256 per tile, each CTA holds 128 A rows
 //           and half of B, and one thread of the even CTA issues the MMAs
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false>
+//   kARows  rows per tile and per A box (single CTAs): 128, or 32 when experts
+//           hold few rows.  The MMA is still M = 128; with 32-row tiles it reads
+//           the 96 rows after the stage's A box from whatever shared memory follows
+//           (a later stage), and those accumulator rows are never stored.  A
+//           stage then holds 4 KB of A instead of 16, so the same shared memory
+//           keeps about twice as many weight bytes in flight.
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false, int kARows = BM>
 struct Cfg {
-  static constexpr int kTileM = kPair ? 2 * BM : BM;              // product rows per tile
+  static_assert(kARows == BM || (!kPair && !kMcastA && !kGatherA && kARows % 8 == 0),
+                "short A tiles are single-CTA TMA tiles only");
+  static constexpr int kTileM = kPair ? 2 * BM : kARows;          // product rows per tile
+  static constexpr int kABytes = kARows * BK * 2;                  // A bytes per stage
   static constexpr int kBRowsCta = kPair ? kN / 2 : kN;           // B rows held per CTA
   static constexpr int kBBytes = kBRowsCta * BK * 2;
-  static constexpr int kStages = stages_for_bytes(A_BYTES + kBBytes);
+  static constexpr int kStages = stages_for_bytes(kABytes + kBBytes);
   // B boxes: gate/up loads its gate and up halves separately (per CTA when paired)
   static constexpr int kBoxB = kPair ? kBRowsCta
                                      : ((kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128));
   static constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;  // output columns per tile
   static constexpr int kThreadsT = kGatherA ? kThreadsGather : kThreads;
-  using S = Smem<kStages, kBBytes>;
+  using S = Smem<kStages, kBBytes, kABytes>;
 };
 
 struct Tile {
@@ -158,7 +168,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, con
   Tile t;
   t.g = lo;
   t.row0 = r0 + m * tile_m;
-  t.row_end = r1;
+  t.row_end = min(r1, t.row0 + tile_m);
   t.n0 = n * bn_out;
   t.pb = 0;
   t.ks = 0;
@@ -186,7 +196,7 @@ __device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const 
     Tile t;
     t.g = 0;
     t.row0 = m * tile_m;
-    t.row_end = s2.P2;
+    t.row_end = min(s2.P2, t.row0 + tile_m);
     t.n0 = (q - m * s2.n2_tiles) * bn_out;
     t.pb = 1;
     t.ks = 0;
@@ -250,15 +260,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kMcastA: a cluster of two CTAs computes the same 128 A rows against two
 // neighbouring N tiles; each CTA loads half of the A tile and multicasts it to
 // both, and each stage is released only when both MMAs are done with it.
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA>
-__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA>::kThreadsT, 1)
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA, int kARows>
+__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows>::kThreadsT, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
   constexpr bool kCluster = kPair || kMcastA;
   using S = typename C::S;
+  constexpr int kABytes = C::kABytes;
   constexpr int kStages = C::kStages;
   constexpr int kNThreads = C::kThreadsT;
   constexpr int kTileM = C::kTileM;
@@ -269,8 +280,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   // it must retire the oldest one (kDepth < kStages keeps the ring deadlock-free)
   constexpr int kDepth = kStages - 1;
   constexpr int kTmemCols = 2 * kN;
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kN);
-  constexpr uint32_t kStageTx = (kGatherA ? 0 : A_BYTES) + S::B_BYTES;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPair ? 2 * BM : BM, kN);
+  constexpr uint32_t kStageTx = (kGatherA ? 0 : kABytes) + S::B_BYTES;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -417,7 +428,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint16_t* src = p.a + static_cast<size_t>(in ? srow : 0) * p.Kdim;
       for (int kb = 0; kb < nk; ++kb) {
         if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        const uint32_t dst = sbase + S::STAGE_A + stage * A_BYTES + i * 128;
+        const uint32_t dst = sbase + S::STAGE_A + stage * kABytes + i * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int col = kb * BK + c * 8;
@@ -479,7 +490,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         for (int kb = second ? 0 : kb_lo; kb < nk_t; ++kb) {
           if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          const uint32_t sa = sbase + S::STAGE_A + stage * A_BYTES;
+          const uint32_t sa = sbase + S::STAGE_A + stage * kABytes;
           const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
           if (kPair) {
             // both CTAs' boxes are counted on the even CTA's barrier, which
@@ -496,7 +507,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::mbar_arrive_expect_tx(fb, kStageTx);
           if (kMcastA) {
             // this CTA's half of the A tile (64 rows), into both CTAs of the pair
-            ptx::tma_load_2d_mcast(sa + rank * (A_BYTES / 2), &tmA, kb * BK,
+            ptx::tma_load_2d_mcast(sa + rank * (kABytes / 2), &tmA, kb * BK,
                                    t.row0 + static_cast<int>(rank) * (BM / 2), fb, 3);
           } else if (!kGatherA) {
             ptx::tma_load_2d(sa, mA, kb * BK, t.row0 + row_off, fb);
@@ -552,7 +563,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int kb = 0; kb < nk_t; ++kb) {
           if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * A_BYTES);
+          const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * kABytes);
           const uint64_t db = ptx::desc_kmajor_sw128(sbase + S::STAGE_B + stage * S::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -777,12 +788,13 @@ int num_sms() {
 
 // tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
 // grid is that many CTAs (pairs when paired), capped at the SM count
-template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false>
+template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
+          int kARows = BM>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta2,
            const CUtensorMap& tb2, Params p, long long tile_bound, cudaStream_t stream) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
   constexpr bool kCluster = kPair || kMcastA;
-  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA>;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
   const int smem = C::S::ALLOC;
   static int configured_dev[64] = {};
   int dev = 0;
@@ -835,10 +847,12 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const C
 }
 
 // one grouped problem (the second-problem maps are unused copies)
-template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false>
+template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
+          int kARows = BM>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
-  return launch<kN, kEpi, kGatherA, kPair, kMcastA>(op, ta, tb, ta, tb, p, tile_bound, stream);
+  return launch<kN, kEpi, kGatherA, kPair, kMcastA, kARows>(op, ta, tb, ta, tb, p, tile_bound,
+                                                           stream);
 }
 
 int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, const void* b,
@@ -943,7 +957,9 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   // Few rows per expert (decode): each tile streams its weight rows from HBM
   // and the tile count decides the balance; 128-wide tiles (64 gate + 64 up
   // rows) double it, which cuts the idle tail of the last round (decode layer,
-  // 82 of 128 experts touched: 127 -> 115 us).  Tensor-bound loads keep 256.
+  // 82 of 128 experts touched: 127 -> 115 us).  32-row tiles load 4 KB of A per
+  // stage instead of 16, so the ring keeps more weight bytes in flight.
+  // Tensor-bound loads keep 128 x 256.
   const bool narrow = !a_row_gather && mode == MOE_GEMM_SINGLE &&
                       static_cast<long long>(P) <= 16LL * G;
   CUtensorMap ta, tb;
@@ -952,7 +968,8 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
     return rc;
   if (a_row_gather) {
     ta = tb;  // unused: the gatherer warps read A rows directly
-  } else if ((rc = make_tmap(&ta, a_bf16, P, H, mcast ? BM / 2 : BM, op, "a")) != MOE_OK) {
+  } else if ((rc = make_tmap(&ta, a_bf16, P, H, narrow ? kNarrowRows : (mcast ? BM / 2 : BM), op,
+                             "a")) != MOE_OK) {
     return rc;
   }
   Params p{};
@@ -985,7 +1002,9 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   }
   if (mcast)
     return launch<256, EPI_GATEUP, false, false, true>(op, ta, tb, p, tile_bound(P, G, I, 256), s);
-  if (narrow) return launch<128, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 64), s);
+  if (narrow)
+    return launch<128, EPI_GATEUP, false, false, false, kNarrowRows>(
+        op, ta, tb, p, tile_bound(P, G, I, 64, kNarrowRows), s);
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
@@ -1006,8 +1025,12 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   const int mode = g_pairing.load(std::memory_order_relaxed);
   const bool mcast =
       (mode == MOE_GEMM_MCAST || mode == MOE_GEMM_SPLIT) && ((H + 255) / 256) % 2 == 0;
+  // few rows per expert: 32-row tiles, as in the gate/up GEMM
+  const bool narrow = mode == MOE_GEMM_SINGLE && static_cast<long long>(P) <= 16LL * G;
   CUtensorMap ta, tb;
-  if ((rc = make_tmap(&ta, act_bf16, P, I, mcast ? BM / 2 : BM, op, "act")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&ta, act_bf16, P, I, narrow ? kNarrowRows : (mcast ? BM / 2 : BM), op,
+                      "act")) != MOE_OK)
+    return rc;
   if ((rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) != MOE_OK)
     return rc;
   Params p{};
@@ -1035,6 +1058,9 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   }
   if (mcast)
     return launch<256, EPI_DOWN, false, false, true>(op, ta, tb, p, tile_bound(P, G, H, 512), s);
+  if (narrow)
+    return launch<256, EPI_DOWN, false, false, false, kNarrowRows>(
+        op, ta, tb, p, tile_bound(P, G, H, 256, kNarrowRows), s);
   return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
 }
 

@@ -60,6 +60,9 @@ SHAPES = [
     ([1, 1, 1, 1, 1, 1, 1, 1], 2048, 768),
     ([257, 0, 0, 3], 136, 72),
     ([128, 128, 255, 1], 1024, 256),
+    # few rows per expert (P <= 16 G): 32-row tiles, experts spanning several of them
+    ([40, 0, 70, 1, 33] + [0] * 11, 256, 192),
+    ([2, 1, 0, 3] * 16 + [97], 512, 128),
 ]
 
 
