@@ -796,15 +796,19 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const C
   constexpr bool kCluster = kPair || kMcastA;
   auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
   const int smem = C::S::ALLOC;
-  static int configured_dev[64] = {};
+  // per instantiation and device, set once (racing threads set the same value)
+  static std::atomic<int> configured_dev[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured_dev[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  if (dev < 0 || dev >= 64 || !configured_dev[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return set_error(MOE_ERR_CUDA, "%s: cannot reserve %d bytes of shared memory: %s", op, smem,
                        cudaGetErrorString(cudaGetLastError()));
-    configured_dev[dev] = 1;
+    if (dev >= 0 && dev < 64) configured_dev[dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreadsT, 1, 1);
@@ -820,8 +824,8 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const C
   // Persistent grid: as many CTAs (pairs) as can be resident at once.  A pair
   // must sit in one GPC, so with an odd SM count per GPC fewer than SMs / 2
   // pairs fit; launching more would leave a second, mostly idle wave.
-  static int max_units_dev[64] = {};
-  int max_units = (dev >= 0 && dev < 64) ? max_units_dev[dev] : 0;
+  static std::atomic<int> max_units_dev[64] = {};
+  int max_units = (dev >= 0 && dev < 64) ? max_units_dev[dev].load(std::memory_order_relaxed) : 0;
   if (max_units <= 0) {
     max_units = kCluster ? num_sms() / 2 : num_sms();
     if (kCluster) {
@@ -832,7 +836,7 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const C
       else
         cudaGetLastError();
     }
-    if (dev >= 0 && dev < 64) max_units_dev[dev] = max_units;
+    if (dev >= 0 && dev < 64) max_units_dev[dev].store(max_units, std::memory_order_relaxed);
   }
   long long units = tile_bound;
   if (units > max_units) units = max_units;
