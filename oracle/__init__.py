@@ -51,6 +51,8 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_sigmoid_f32": ([_F], _F),
         "oracle_route_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
         "oracle_route_topk_ex": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+        "oracle_e4m3_to_f32": ([ctypes.c_uint8], _F),
+        "oracle_dequant_fp8_block": ([_P, _P, _I, _I, _I, _P], _I),
         "oracle_permute": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
         "oracle_gateup_silu": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I], _I),
         "oracle_down": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P], _I),
@@ -145,6 +147,23 @@ def route_topk_ex(logits, select_bias=None, *, T, E, K, renormalize=1, scoring=0
                                     topk_group, group_score, _ptr(ids), _ptr(w))
     _check(rc, "route_topk_ex")
     return ids, w
+
+
+def e4m3_to_f32(codes):
+    """f32 values of FP8 E4M3 codes (uint8 array)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    return np.array([lib().oracle_e4m3_to_f32(int(c)) for c in codes.ravel()],
+                    np.float32).reshape(codes.shape)
+
+
+def dequant_fp8_block(q, scale, *, G, R, C):
+    """bf16 bits [G, R, C] of block-scaled FP8 weights (scale [G, ceil(R/128), ceil(C/128)])."""
+    w = np.zeros((G, R, C), np.uint16)
+    rc = lib().oracle_dequant_fp8_block(_ptr(np.ascontiguousarray(q, np.uint8)),
+                                        _ptr(np.ascontiguousarray(scale, np.float32)), G, R, C,
+                                        _ptr(w))
+    _check(rc, "dequant_fp8_block")
+    return w
 
 
 def permute(topk_ids, x=None, *, T, K, E, H=0):

@@ -415,6 +415,47 @@ int oracle_permute(const int32_t* topk_ids, const uint16_t* x, int T, int K, int
 }
 
 /* ------------------------------------------------------------------ */
+/* Block-scaled FP8 expert weights (the pages only name                 */
+/* kMatmulFp8BlockScaled and kQuantFp8Group as ops of the engine).      */
+/* READING, after the published DeepSeek-V3 FP8 weights: each expert's  */
+/* weight matrix is stored as FP8 E4M3 codes (the "fn" variant: no      */
+/* infinities, S.1111.111 is NaN, largest finite 448) with one f32      */
+/* scale per 128 x 128 block of its own rows and columns.  The expert   */
+/* GEMMs use w = bf16(f32(code) * scale), one f32 multiply and one RNE  */
+/* rounding to bf16, and then the bf16 contract above; activations stay */
+/* bf16.                                                                */
+/* ------------------------------------------------------------------ */
+
+float oracle_e4m3_to_f32(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  float v;
+  if (e == 15 && m == 7) return sign ? -NAN : NAN;
+  if (e == 0)
+    v = ldexpf((float)m, -9);           /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexpf((float)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  return sign ? -v : v;
+}
+
+/* w[g, r, c] = bf16(f32(q[g, r, c]) * scale[g, r / 128, c / 128]) for G matrices
+ * of R x C; scale is [G][ceil(R/128)][ceil(C/128)] */
+int oracle_dequant_fp8_block(const uint8_t* q, const float* scale, int G, int R, int C,
+                             uint16_t* w) {
+  if (G < 1 || R < 1 || C < 1 || !q || !scale || !w) return ORA_ERR_ARG;
+  const int64_t rb = (R + 127) / 128, cb = (C + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t gr = 0; gr < (int64_t)G * R; ++gr) {
+    const int64_t g = gr / R, r = gr % R;
+    const float* srow = scale + (g * rb + r / 128) * cb;
+    for (int64_t c = 0; c < C; ++c) {
+      float v = oracle_e4m3_to_f32(q[gr * C + c]) * srow[c / 128];
+      w[gr * C + c] = f2bf(v);
+    }
+  }
+  return ORA_OK;
+}
+
+/* ------------------------------------------------------------------ */
 /* a4: grouped gate/up GEMM fused with SiLU-and-mul                     */
 /* kMoeGroupedGemmBf16GateUpSilu, issue #3094: the GEMM result is cut to  */
 /* bf16 ahead of the activation -- both the gate and the up accumulations */

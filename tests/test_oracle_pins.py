@@ -715,3 +715,46 @@ def test_oracle_threads_do_not_change_bits():
     O.set_threads(n)
     b = O.moe_layer_tokens(*args, **kw)[0]
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ block-scaled FP8 weights
+def test_e4m3_decode_matches_torch_float8_on_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.e4m3_to_f32(codes)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok].view(np.uint32), want[ok].view(np.uint32))
+    # hand values: smallest subnormal, smallest normal, one, largest finite, NaN
+    assert got[0x01] == 2.0**-9 and got[0x08] == 2.0**-6 and got[0x38] == 1.0
+    assert got[0x7E] == 448.0 and np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def test_fp8_block_dequant_uses_each_block_scale_once():
+    # code 0x38 is 1.0 everywhere; block (g, i, j) gets scale 2^(g + 2i - j), so
+    # every weight is exactly that power of two in bf16 and the block map shows
+    G, R, C = 2, 300, 200
+    q = np.full((G, R, C), 0x38, np.uint8)
+    rb, cb = (R + 127) // 128, (C + 127) // 128
+    scale = np.zeros((G, rb, cb), np.float32)
+    for g in range(G):
+        for i in range(rb):
+            for j in range(cb):
+                scale[g, i, j] = 2.0 ** (g + 2 * i - j)
+    w = bits_to_f32(O.dequant_fp8_block(q, scale, G=G, R=R, C=C))
+    r = np.arange(R)[None, :, None] // 128
+    c = np.arange(C)[None, None, :] // 128
+    g = np.arange(G)[:, None, None]
+    assert np.array_equal(w, (2.0 ** (g + 2 * r - c)).astype(np.float32))
+
+
+def test_fp8_block_dequant_rounds_the_product_once_to_bf16():
+    rng = np.random.default_rng(12)
+    G, R, C = 1, 128, 128
+    q = rng.integers(0, 256, (G, R, C), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x30                     # no NaN codes
+    scale = np.array([[[0.013]]], np.float32)
+    w = O.dequant_fp8_block(q, scale, G=G, R=R, C=C)
+    prod = (O.e4m3_to_f32(q).astype(np.float32) * np.float32(0.013)).astype(np.float32)
+    assert np.array_equal(w.ravel(), f64_to_nearest_bf16_bits(prod.astype(np.float64)))
