@@ -411,8 +411,12 @@ def run_ours(args):
     d = W.layer_inputs(cfg)
     if rank > 0:  # each replica gets its own tokens of the global batch
         d["x"] = W.rank_tokens(cfg, rank)
+    fp8 = args.weights == "fp8"
+    if fp8:
+        d["w13_e4m3"], d["w13_scale"] = W.quantize_fp8_block(d["w13"])
+        d["w2_e4m3"], d["w2_scale"] = W.quantize_fp8_block(d["w2"])
     blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
-                   I_shared=cfg.I_shared)
+                   I_shared=cfg.I_shared, fp8_weights=fp8)
     x_host = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     x_dev = x_host.to(dev)
     out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
@@ -497,19 +501,22 @@ def run_ours(args):
     touched = int((counts > 0).sum())
     flop_gateup = 2.0 * P * cfg.H * 2 * cfg.I
     flop_down = 2.0 * P * cfg.I * cfg.H
-    bytes_gateup = touched * 2 * cfg.I * cfg.H * 2 + P * cfg.H * 2 + P * cfg.I * 2
-    bytes_down = touched * cfg.H * cfg.I * 2 + P * cfg.I * 2 + P * cfg.H * 2 + P * 4
+    wb = 1 if fp8 else 2          # bytes per expert weight (FP8 adds one f32 per 128x128 block)
+    sc = 4.0 / (128 * 128) if fp8 else 0.0
+    bytes_gateup = touched * 2 * cfg.I * cfg.H * (wb + sc) + P * cfg.H * 2 + P * cfg.I * 2
+    bytes_down = touched * cfg.H * cfg.I * (wb + sc) + P * cfg.I * 2 + P * cfg.H * 2 + P * 4
     t_gu = stage_avg["gemm_gateup"] / 1000.0
     t_dn = stage_avg["gemm_down"] / 1000.0
     tensor_bound = flop_gateup / (pk["bf16_tflops"] * 1e12) >= bytes_gateup / (pk["hbm_gbs"] * 1e9)
-    kname = "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)"
+    kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
+             "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)")
     if tensor_bound:
         achieved = flop_gateup / t_gu / 1e12
         roofline = {"kernel": kname, "bound": "tensor", "achieved": achieved,
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / pk["bf16_tflops"],
                     "peak_source": f"{pk_src} bf16 dense (burst)",
-                    "traffic": recorded_traffic(cfg.name),
+                    "traffic": None if fp8 else recorded_traffic(cfg.name),
                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "algorithmic_flop_per_launch": flop_gateup}
     else:
@@ -517,7 +524,7 @@ def run_ours(args):
         roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                     "peak_source": f"{pk_src} HBM copy bandwidth",
-                    "traffic": recorded_traffic(cfg.name),
+                    "traffic": None if fp8 else recorded_traffic(cfg.name),
                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "algorithmic_bytes_per_launch": bytes_gateup,
                     "touched_experts": touched}
@@ -547,7 +554,16 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, cores, n, dt = oracle_tokens_per_s(cfg, d, seconds=args.cpu_seconds)
+        do = d
+        if fp8:  # the oracle runs the layer on the dequantised FP8 weights
+            import oracle as O
+
+            do = dict(d)
+            do["w13"] = O.dequant_fp8_block(d["w13_e4m3"], d["w13_scale"], G=cfg.E,
+                                            R=2 * cfg.I, C=cfg.H)
+            do["w2"] = O.dequant_fp8_block(d["w2_e4m3"], d["w2_scale"], G=cfg.E, R=cfg.H,
+                                           C=cfg.I)
+        v, cores, n, dt = oracle_tokens_per_s(cfg, do, seconds=args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} of {cfg.T} tokens, whole block per token, {dt:.1f} s"}
 
@@ -558,9 +574,11 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded normal inputs and weights, "
-                    + (f"Zipf({cfg.zipf_s})-skewed router bias)" if cfg.zipf_s
-                       else "unbiased router)"),
-            "config": config_dict(cfg, ws),
+                    + (f"Zipf({cfg.zipf_s})-skewed router bias" if cfg.zipf_s
+                       else "unbiased router")
+                    + ("; routed expert weights FP8 E4M3 with 128x128 block scales, "
+                       "quantised from the same bf16 weights)" if fp8 else ")"),
+            "config": dict(config_dict(cfg, ws), weights=args.weights),
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": int(cfg.T * cfg.H * 2),
                     "d2h_bytes_per_step": int(cfg.T * cfg.H * 2)},
@@ -587,6 +605,8 @@ def main():
     ap.add_argument("--config", default="prefill",
                     choices=["prefill", "decode", "large", "tiny", "combine"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                    help="routed expert weights: bf16, or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -73,7 +73,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 6 */
+int moe_abi_version(void);  /* 7 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -291,6 +291,35 @@ int moe_grouped_gemm_down_bf16_shared(const void* act_bf16, const void* w2_bf16,
                                       void* out_bf16, const void* acts_bf16, int Ts,
                                       const void* w2s_bf16, int Is, void* sd_bf16,
                                       void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_gemm_gateup_silu_fp8w / moe_grouped_gemm_down_fp8w -- the two
+ * expert GEMMs with block-scaled FP8 weights.  The pages name FP8 block-scaled
+ * matmul and FP8 group quantisation only as ops of the engine; the format here
+ * follows the published DeepSeek-V3 weights: each group's weight matrix is FP8
+ * E4M3 codes ("fn" variant: no infinities, largest finite 448) with one f32
+ * scale per 128 x 128 block of its own rows and columns.  The GEMM uses
+ *   w = bf16( f32(code) * scale )      (one f32 multiply, one RNE rounding)
+ * and is then exactly the bf16 call above (same narrowing, weight, scatter,
+ * tolerance); activations stay bf16.  Four converter warps per CTA turn the
+ * codes into bf16 tiles in shared memory between the TMA loads and the MMA,
+ * so the weights cross HBM at one byte each.
+ *   w13_e4m3  uint8 [G, 2I, H] (gate rows first), w13_scale f32 [G, ceil(2I/128), ceil(H/128)]
+ *   w2_e4m3   uint8 [G, H, I],                     w2_scale f32 [G, ceil(H/128), ceil(I/128)]
+ *   the other arguments as moe_grouped_gemm_gateup_silu_bf16 (x_perm rows, no gather) and
+ *   moe_grouped_gemm_down_bf16; the contraction length (H, resp. I) a multiple of 16;
+ *   codes 16-byte aligned, scales 4-byte aligned.  Single-CTA tiles (128-wide,
+ *   32-row ones when P <= 16 G).  Errors as those calls.
+ * ---------------------------------------------------------------------- */
+int moe_grouped_gemm_gateup_silu_fp8w(const void* a_bf16, const uint8_t* w13_e4m3,
+                                      const float* w13_scale, const int32_t* group_offsets,
+                                      int P, int H, int I, int G, void* act_bf16,
+                                      void* workspace, size_t ws_bytes, void* stream);
+int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
+                               const float* w2_scale, const int32_t* group_offsets,
+                               const float* pair_weight, const int32_t* row_to_pair, int P,
+                               int I, int H, int G, void* out_bf16, void* workspace,
+                               size_t ws_bytes, void* stream);
 
 /* moe_set_gemm_pairing -- tiling of the two grouped GEMMs above (the
  * gathered-A gate/up always runs single-CTA tiles):

@@ -36,7 +36,7 @@ EXPORTS = (
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
     "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl",
     "moe_grouped_gemm_gateup_silu_bf16_shared", "moe_grouped_gemm_down_bf16_shared",
-    "moe_route_topk_ex",
+    "moe_route_topk_ex", "moe_grouped_gemm_gateup_silu_fp8w", "moe_grouped_gemm_down_fp8w",
 )
 
 
@@ -68,6 +68,9 @@ _SIGS = {
                                            _P], _I),
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
+    "moe_grouped_gemm_gateup_silu_fp8w": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "moe_grouped_gemm_down_fp8w": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P],
+                                   _I),
     "moe_grouped_gemm_gateup_silu_bf16_shared": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P,
                                                   _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_down_bf16_shared": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P,
@@ -220,6 +223,26 @@ def moe_grouped_gemm_down_bf16_shared(act, w2, group_offsets, pair_weight, row_t
         _ptr(act), _ptr(w2), _ptr(group_offsets), _ptr(pair_weight), _ptr(row_to_pair), P, I, H,
         G, _ptr(out), _ptr(acts), Ts, _ptr(w2s), Is, _ptr(sd), _ptr(workspace), ws_bytes,
         _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_gateup_silu_fp8w(a, w13_e4m3, w13_scale, group_offsets, P, H, I, G, act,
+                                      workspace=None, ws_bytes=0, stream=None, check=True):
+    """Gate/up GEMM + SiLU-mul with block-scaled FP8 weights (see moe.h)."""
+    rc = lib().moe_grouped_gemm_gateup_silu_fp8w(_ptr(a), _ptr(w13_e4m3), _ptr(w13_scale),
+                                                 _ptr(group_offsets), P, H, I, G, _ptr(act),
+                                                 _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_down_fp8w(act, w2_e4m3, w2_scale, group_offsets, pair_weight, row_to_pair,
+                               P, I, H, G, out, workspace=None, ws_bytes=0, stream=None,
+                               check=True):
+    """Down GEMM (routing weight, scatter) with block-scaled FP8 weights (see moe.h)."""
+    rc = lib().moe_grouped_gemm_down_fp8w(_ptr(act), _ptr(w2_e4m3), _ptr(w2_scale),
+                                          _ptr(group_offsets), _ptr(pair_weight),
+                                          _ptr(row_to_pair), P, I, H, G, _ptr(out),
+                                          _ptr(workspace), ws_bytes, _stream(stream))
     return _check(rc) if check else rc
 
 

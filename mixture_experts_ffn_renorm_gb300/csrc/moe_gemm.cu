@@ -30,6 +30,9 @@
 #include <atomic>
 #include <mutex>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "moe_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -41,6 +44,8 @@ constexpr int BK = 64;            // bf16 per 128-byte swizzled row: K per stage
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;        // producer, MMA, 4 epilogue warps
 constexpr int kThreadsGather = 320;  // + 4 warps that gather A rows
+constexpr int kConverters = 256;     // FP8 weights: 8 warps that dequantise B
+constexpr int kThreadsFp8 = kThreads + kConverters;
 constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK * 2;
 // bytes of the 227 KB per-block shared memory left for the stage ring after the
@@ -79,6 +84,12 @@ struct Params {
   int Kdim2;
   int half_off2;                 // gate/up: row offset of the up half in its weight
   void* out2;
+  // FP8 weights (kFp8B): E4M3 codes behind the B tensor map, one f32 scale per
+  // 128 x 128 block of each group's weight matrix, b_scale[g][row/128][col/128]
+  // with scale_rb = ceil(b_rows_per_group / 128) and scale_cb = ceil(Kdim / 128)
+  const float* b_scale;
+  int scale_rb;
+  int scale_cb;
   // f32 epilogue only: split K into ksplit ranges of ceil(nk / ksplit) k-blocks;
   // each (tile, range) is a unit of its own and stores its partial sum, without
   // the bias, at out + range * P * N.  ksplit == 1: the whole K, bias added.
@@ -89,20 +100,28 @@ struct Params {
 };
 
 // Stage ring depth: as many stages of `stage_bytes` as fit the budget, at most 12.
+__host__ __device__ constexpr int stages_for_bytes_with(int stage_bytes, int budget) {
+  return budget / stage_bytes > 12 ? 12 : budget / stage_bytes;
+}
 __host__ __device__ constexpr int stages_for_bytes(int stage_bytes) {
-  return kSmemBudget / stage_bytes > 12 ? 12 : kSmemBudget / stage_bytes;
+  return stages_for_bytes_with(stage_bytes, kSmemBudget);
 }
 
-template <int kStages, int kBBytes, int kABytes = A_BYTES>
+// kConv > 0 (FP8 weights): the stage ring holds A and the raw weight codes
+// (kRawBytes a stage); the bf16 B tiles the MMA reads live in a second ring of
+// kConv stages, written by the converter warps.
+template <int kStages, int kBBytes, int kABytes = A_BYTES, int kConv = 0, int kRawBytes = 0>
 struct Smem {
   static_assert(kStages >= 2, "stage ring too shallow");
   static constexpr int B_BYTES = kBBytes;
+  static constexpr int RAW_BYTES = kRawBytes;
   static constexpr int STAGE_A = 0;
-  static constexpr int STAGE_B = kStages * kABytes;
-  static constexpr int STAGE_EPI = STAGE_B + kStages * B_BYTES;   // 4 epilogue staging buffers
+  static constexpr int STAGE_RAW = kStages * kABytes;
+  static constexpr int STAGE_B = STAGE_RAW + kStages * kRawBytes;
+  static constexpr int STAGE_EPI = STAGE_B + (kConv ? kConv : kStages) * B_BYTES;  // 4 staging buffers
   static constexpr int BARS = STAGE_EPI + 4 * kStgBytes;
-  // full[kStages], empty[kStages], tfull[2], tempty[2], drain
-  static constexpr int NBARS = 2 * kStages + 5;
+  // full[kStages], empty[kStages], conv_full[kConv], conv_empty[kConv], tfull[2], tempty[2], drain
+  static constexpr int NBARS = 2 * kStages + 2 * kConv + 5;
   static constexpr int MISC = BARS + NBARS * 8;           // tmem slot, abort flag, scan scratch
   static constexpr int TILE_START = MISC + 64;            // int[kMaxGroups + 1]
   static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
@@ -120,21 +139,30 @@ struct Smem {
 //           (a later stage), and those accumulator rows are never stored.  A
 //           stage then holds 4 KB of A instead of 16, so the same shared memory
 //           keeps about twice as many weight bytes in flight.
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false, int kARows = BM>
+//   kFp8B   B holds FP8 E4M3 weight codes with block scales: TMA brings A and the
+//           codes into the stage ring, four converter warps write the scaled
+//           bf16 B tiles into a second ring, and the MMA reads A and that
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false, int kARows = BM,
+          bool kFp8B = false>
 struct Cfg {
   static_assert(kARows == BM || (!kPair && !kMcastA && !kGatherA && kARows % 8 == 0),
                 "short A tiles are single-CTA TMA tiles only");
+  static_assert(!kFp8B || (!kPair && !kMcastA && !kGatherA), "FP8 weights: single-CTA tiles");
   static constexpr int kTileM = kPair ? 2 * BM : kARows;          // product rows per tile
   static constexpr int kABytes = kARows * BK * 2;                  // A bytes per stage
   static constexpr int kBRowsCta = kPair ? kN / 2 : kN;           // B rows held per CTA
   static constexpr int kBBytes = kBRowsCta * BK * 2;
-  static constexpr int kStages = stages_for_bytes(kABytes + kBBytes);
+  static constexpr int kRawBytes = kFp8B ? kBRowsCta * BK : 0;    // FP8 codes per stage
+  static constexpr int kConv = kFp8B ? (kBBytes >= 32 * 1024 ? 2 : 4) : 0;
+  static constexpr int kStages =
+      kFp8B ? stages_for_bytes_with(kABytes + kRawBytes, kSmemBudget - kConv * kBBytes)
+            : stages_for_bytes(kABytes + kBBytes);
   // B boxes: gate/up loads its gate and up halves separately (per CTA when paired)
   static constexpr int kBoxB = kPair ? kBRowsCta
                                      : ((kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128));
   static constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;  // output columns per tile
-  static constexpr int kThreadsT = kGatherA ? kThreadsGather : kThreads;
-  using S = Smem<kStages, kBBytes, kABytes>;
+  static constexpr int kThreadsT = kFp8B ? kThreadsFp8 : (kGatherA ? kThreadsGather : kThreads);
+  using S = Smem<kStages, kBBytes, kABytes, kConv, kRawBytes>;
 };
 
 struct Tile {
@@ -260,28 +288,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kMcastA: a cluster of two CTAs computes the same 128 A rows against two
 // neighbouring N tiles; each CTA loads half of the A tile and multicasts it to
 // both, and each stage is released only when both MMAs are done with it.
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA, int kARows>
-__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows>::kThreadsT, 1)
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA, int kARows, bool kFp8B>
+__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>::kThreadsT,
+                                  1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>;
   constexpr bool kCluster = kPair || kMcastA;
   using S = typename C::S;
   constexpr int kABytes = C::kABytes;
+  constexpr int kConv = C::kConv;
   constexpr int kStages = C::kStages;
   constexpr int kNThreads = C::kThreadsT;
   constexpr int kTileM = C::kTileM;
   constexpr int kBnOut = C::kBnOut;
   constexpr int kBoxB = C::kBoxB;
-  constexpr int kBoxBytes = kBoxB * BK * 2;
+  constexpr int kBoxBytes = kBoxB * BK * (kFp8B ? 1 : 2);   // one B box as loaded
   // gathered A: each row-thread keeps kDepth stages of copies in flight before
   // it must retire the oldest one (kDepth < kStages keeps the ring deadlock-free)
   constexpr int kDepth = kStages - 1;
   constexpr int kTmemCols = 2 * kN;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPair ? 2 * BM : BM, kN);
-  constexpr uint32_t kStageTx = (kGatherA ? 0 : kABytes) + S::B_BYTES;
+  constexpr uint32_t kStageTx = (kGatherA ? 0 : kABytes) + (kFp8B ? S::RAW_BYTES : S::B_BYTES);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -303,16 +333,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int n_units = kCluster ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto bar_full = [&](int s) { return ptx::smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return ptx::smem_u32(bars + kStages + s); };
-  auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + a); };
-  auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 + a); };
-  const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kStages + 4);
+  auto bar_cfull = [&](int s) { return ptx::smem_u32(bars + 2 * kStages + s); };
+  auto bar_cempty = [&](int s) { return ptx::smem_u32(bars + 2 * kStages + kConv + s); };
+  auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 * kConv + a); };
+  auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 2 + a); };
+  const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 4);
 
   count_launch(p.launches, p.kid);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar_full(s), kGatherA ? 1 + BM : 1);
-      ptx::mbar_init(bar_empty(s), kMcastA ? 2 : 1);
+      // FP8 weights: a stage is free once the MMA and every converter are done with it
+      ptx::mbar_init(bar_empty(s), kFp8B ? 1 + kConverters : (kMcastA ? 2 : 1));
+    }
+    for (int s = 0; s < kConv; ++s) {
+      ptx::mbar_init(bar_cfull(s), kConverters);
+      ptx::mbar_init(bar_cempty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_tfull(a), 1);
@@ -491,7 +528,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int kb = second ? 0 : kb_lo; kb < nk_t; ++kb) {
           if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const uint32_t sa = sbase + S::STAGE_A + stage * kABytes;
-          const uint32_t sb = sbase + S::STAGE_B + stage * S::B_BYTES;
+          const uint32_t sb = kFp8B ? sbase + S::STAGE_RAW + stage * S::RAW_BYTES
+                                    : sbase + S::STAGE_B + stage * S::B_BYTES;
           if (kPair) {
             // both CTAs' boxes are counted on the even CTA's barrier, which
             // expects the bytes of both halves
@@ -540,6 +578,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
+      int cst = 0;             // FP8 weights: stage of the converted ring
+      uint32_t cphase = 0;
       int it = 0;
       bool ok = true, any = false;
       for (int tile = unit; ok && tile < total; tile += n_units, ++it) {
@@ -562,9 +602,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         for (int kb = 0; kb < nk_t; ++kb) {
           if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
+          if (kFp8B && !wait_bar(bar_cfull(cst), cphase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
           const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * kABytes);
-          const uint64_t db = ptx::desc_kmajor_sw128(sbase + S::STAGE_B + stage * S::B_BYTES);
+          const uint64_t db = ptx::desc_kmajor_sw128(sbase + S::STAGE_B +
+                                                     (kFp8B ? cst : stage) * S::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
@@ -577,6 +622,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (kPair) ptx::mma_commit_pair(bar_empty(stage), 3);
           else if (kMcastA) ptx::mma_commit_mcast(bar_empty(stage), 3);  // frees it in both CTAs
           else ptx::mma_commit(bar_empty(stage));
+          if (kFp8B) {
+            ptx::mma_commit(bar_cempty(cst));
+            if (++cst == kConv) { cst = 0; cphase ^= 1u; }
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -725,6 +774,69 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         else ptx::mbar_arrive(bar_tempty(acc));
       }
     }
+  } else if (kFp8B) {
+    // ------------------------------------------------------------ FP8 converters
+    // Thread ct of warps 6-13 handles 16-byte pieces q = ct + 256 j of the B tile:
+    // row q / 8, codes 8 (q % 8) .. 8 (q % 8) + 7 of the stage's 64 columns.  Each
+    // weight becomes bf16(f32(code) * scale) with the scale of its 128 x 128
+    // block, written where a TMA SWIZZLE_128B box would put it (16-byte piece c
+    // of row r at piece c ^ (r % 8)), so the MMA reads it like any bf16 B tile.
+    const int ct = static_cast<int>(threadIdx.x) - kThreads;
+    int stage = 0, cst = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int tile = unit; ok && tile < total; tile += n_units) {
+      const Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
+                                 p.split, s2);
+      // weight rows (within the group) of tile rows [0, kN/2) and [kN/2, kN)
+      const int wrow0 = t.n0;
+      const int wrow1 = (kEpi == EPI_GATEUP) ? t.n0 + p.half_off : t.n0 + kN / 2;
+      const float* scale_g =
+          p.b_scale + static_cast<size_t>(t.g) * static_cast<size_t>(p.scale_rb) * p.scale_cb;
+      const int kb_lo = t.ks * nk_split;
+      const int kb_hi = min(nk, kb_lo + nk_split);
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_bar(bar_cempty(cst), cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        const uint8_t* raw = smem + S::STAGE_RAW + stage * S::RAW_BYTES;
+        const uint32_t dst = sbase + S::STAGE_B + cst * S::B_BYTES;
+        const int cblk = (kb * BK) / 128;
+        // the scale of a row's block is reloaded only when the block changes
+        int sc_blk = -1;
+        float sc = 0.0f;
+#pragma unroll 4
+        for (int j = 0; j < kN * 8 / kConverters; ++j) {
+          const int q = ct + kConverters * j;
+          const int r = q >> 3, c = q & 7;
+          const int wr = r < kN / 2 ? wrow0 + r : wrow1 + (r - kN / 2);
+          // rows past the group's own (a ragged last N tile) are never stored
+          const int rblk = min(wr / 128, p.scale_rb - 1);
+          if (rblk != sc_blk) {
+            sc = __ldg(scale_g + static_cast<size_t>(rblk) * p.scale_cb + cblk);
+            sc_blk = rblk;
+          }
+          const uint2 codes = *reinterpret_cast<const uint2*>(raw + r * BK + c * 8);
+          const uint32_t cw[2] = {codes.x, codes.y};
+          uint32_t packed[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const __nv_fp8x2_storage_t two =
+                static_cast<__nv_fp8x2_storage_t>((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);  // exact
+            const float lo = __fmul_rn(__half2float(__ushort_as_half(hr.x)), sc);
+            const float hi = __fmul_rn(__half2float(__ushort_as_half(hr.y)), sc);
+            packed[h] = pack_bf16x2(lo, hi);
+          }
+          ptx::st_shared_v4(dst + r * 128 + ((c ^ (r & 7)) << 4), packed[0], packed[1], packed[2],
+                            packed[3]);
+        }
+        ptx::fence_proxy_async_smem();     // the tensor core reads these through the async proxy
+        ptx::mbar_arrive(bar_cfull(cst));
+        ptx::mbar_arrive(bar_empty(stage));
+        if (++cst == kConv) { cst = 0; cphase ^= 1u; }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
   }
 
   __syncthreads();
@@ -776,6 +888,25 @@ int make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, int bo
   return MOE_OK;
 }
 
+// rows x cols FP8 codes (one byte each, cols contiguous), box of 64 cols x box_rows
+// rows, unswizzled (the converter warps read it as plain rows of 64 bytes)
+int make_tmap_u8(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows,
+                 const char* op, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(MOE_ERR_CUDA, "%s: cuTensorMapEncodeTiled is unavailable", op);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(MOE_ERR_CUDA, "%s: tensor map for %s rejected (CUresult %d)", op, what,
+                     static_cast<int>(r));
+  return MOE_OK;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -789,12 +920,12 @@ int num_sms() {
 // tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
 // grid is that many CTAs (pairs when paired), capped at the SM count
 template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
-          int kARows = BM>
+          int kARows = BM, bool kFp8B = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta2,
            const CUtensorMap& tb2, Params p, long long tile_bound, cudaStream_t stream) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>;
   constexpr bool kCluster = kPair || kMcastA;
-  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows>;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>;
   const int smem = C::S::ALLOC;
   // per instantiation and device, set once (racing threads set the same value)
   static std::atomic<int> configured_dev[64] = {};
@@ -852,11 +983,11 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const C
 
 // one grouped problem (the second-problem maps are unused copies)
 template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
-          int kARows = BM>
+          int kARows = BM, bool kFp8B = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
-  return launch<kN, kEpi, kGatherA, kPair, kMcastA, kARows>(op, ta, tb, ta, tb, p, tile_bound,
-                                                           stream);
+  return launch<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>(op, ta, tb, ta, tb, p,
+                                                                  tile_bound, stream);
 }
 
 int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, const void* b,
@@ -1179,4 +1310,106 @@ extern "C" int moe_grouped_gemm_down_bf16_shared(
   const long long extra = ((Ts + BM - 1) / BM) * static_cast<long long>((H + 255) / 256);
   return launch<256, EPI_DOWN>(op, ta, tb, ta2, tb2, p, tile_bound(P, G, H, 256) + extra,
                                static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+// FP8 weights: codes and scales present and aligned, dimensions whole 16-byte rows
+int check_fp8(const char* op, int rows_per_group, int Kdim, const void* q, const float* scale) {
+  if (!q || !scale) return set_error(MOE_ERR_ARG, "%s: FP8 weight codes or scales are NULL", op);
+  if (Kdim % 16 != 0)
+    return set_error(MOE_ERR_ALIGN, "%s: K=%d of the FP8 weights must be a multiple of 16", op,
+                     Kdim);
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return set_error(MOE_ERR_ALIGN, "%s: FP8 codes must be 16-byte, scales 4-byte aligned", op);
+  (void)rows_per_group;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_grouped_gemm_gateup_silu_fp8w(const void* a_bf16, const uint8_t* w13_e4m3,
+                                                 const float* w13_scale,
+                                                 const int32_t* group_offsets, int P, int H,
+                                                 int I, int G, void* act_bf16, void* workspace,
+                                                 size_t ws_bytes, void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  clear_error();
+  const char* op = "moe_grouped_gemm_gateup_silu_fp8w";
+  int rc;
+  if ((rc = check_common(op, P, H, I, G, a_bf16, w13_e4m3, act_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if (P == 0) return MOE_OK;
+  if ((rc = check_fp8(op, 2 * I, H, w13_e4m3, w13_scale)) != MOE_OK) return rc;
+  const bool narrow = static_cast<long long>(P) <= 16LL * G;
+  CUtensorMap ta, tb;
+  if ((rc = make_tmap(&ta, a_bf16, P, H, narrow ? kNarrowRows : BM, op, "a")) != MOE_OK ||
+      (rc = make_tmap_u8(&tb, w13_e4m3, static_cast<long long>(G) * 2 * I, H, narrow ? 64 : 128,
+                         op, "w13")) != MOE_OK)
+    return rc;
+  Params p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = H;
+  p.N = I;
+  p.G = G;
+  p.b_rows_per_group = 2 * I;
+  p.half_off = I;
+  p.out = act_bf16;
+  p.b_scale = w13_scale;
+  p.scale_rb = (2 * I + 127) / 128;
+  p.scale_cb = (H + 127) / 128;
+  p.kid = MOE_KID_GEMM_GATEUP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (narrow)
+    return launch<128, EPI_GATEUP, false, false, false, kNarrowRows, true>(
+        op, ta, tb, p, tile_bound(P, G, I, 64, kNarrowRows), s);
+  return launch<256, EPI_GATEUP, false, false, false, BM, true>(op, ta, tb, p,
+                                                                tile_bound(P, G, I, 128), s);
+}
+
+extern "C" int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
+                                          const float* w2_scale, const int32_t* group_offsets,
+                                          const float* pair_weight, const int32_t* row_to_pair,
+                                          int P, int I, int H, int G, void* out_bf16,
+                                          void* workspace, size_t ws_bytes, void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  clear_error();
+  const char* op = "moe_grouped_gemm_down_fp8w";
+  int rc;
+  if ((rc = check_common(op, P, I, H, G, act_bf16, w2_e4m3, out_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if (P == 0) return MOE_OK;
+  if ((rc = check_fp8(op, H, I, w2_e4m3, w2_scale)) != MOE_OK) return rc;
+  const bool narrow = static_cast<long long>(P) <= 16LL * G;
+  CUtensorMap ta, tb;
+  if ((rc = make_tmap(&ta, act_bf16, P, I, narrow ? kNarrowRows : BM, op, "act")) != MOE_OK ||
+      (rc = make_tmap_u8(&tb, w2_e4m3, static_cast<long long>(G) * H, I, 128, op, "w2")) !=
+          MOE_OK)
+    return rc;
+  Params p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = I;
+  p.N = H;
+  p.G = G;
+  p.b_rows_per_group = H;
+  p.half_off = 0;
+  p.out = out_bf16;
+  p.pair_weight = pair_weight;
+  p.row_to_pair = row_to_pair;
+  p.b_scale = w2_scale;
+  p.scale_rb = (H + 127) / 128;
+  p.scale_cb = (I + 127) / 128;
+  p.kid = MOE_KID_GEMM_DOWN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (narrow)
+    return launch<256, EPI_DOWN, false, false, false, kNarrowRows, true>(
+        op, ta, tb, p, tile_bound(P, G, H, 256, kNarrowRows), s);
+  return launch<256, EPI_DOWN, false, false, false, BM, true>(op, ta, tb, p,
+                                                              tile_bound(P, G, H, 256), s);
 }

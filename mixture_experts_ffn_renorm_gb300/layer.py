@@ -15,7 +15,8 @@ import torch
 
 from . import (BF16, moe_combine, moe_combine_gate, moe_gate_workspace_size,
                moe_grouped_gemm_down_bf16, moe_grouped_gemm_down_bf16_shared,
-               moe_grouped_gemm_gateup_silu_bf16, moe_grouped_gemm_gateup_silu_bf16_shared,
+               moe_grouped_gemm_down_fp8w, moe_grouped_gemm_gateup_silu_bf16,
+               moe_grouped_gemm_gateup_silu_bf16_shared, moe_grouped_gemm_gateup_silu_fp8w,
                moe_permute, moe_permute_workspace_size, moe_route_topk,
                moe_route_topk_workspace_size)
 
@@ -36,10 +37,14 @@ class MoeBlock:
     weights: dict with ``w_router`` [E,H], ``w13`` [E,2I,H], ``w2`` [E,H,I] (bf16),
     optional ``logit_bias`` [E] f32, and for a shared expert ``w_shared_gate``
     [H], ``w13_shared`` [1,2Is,H], ``w2_shared`` [1,H,Is].
+    fp8_weights=True: the routed experts' weights are block-scaled FP8 instead,
+    ``w13_e4m3`` / ``w13_scale`` and ``w2_e4m3`` / ``w2_scale`` (codes uint8 of
+    the same shapes, f32 scales per 128 x 128 block); the shared expert stays
+    bf16 and runs in launches of its own.
     """
 
     def __init__(self, H, I, E, K, weights, max_tokens, device="cuda", I_shared=0,
-                 routed_scale=1.0, gather=False, fuse_shared=True):
+                 routed_scale=1.0, gather=False, fuse_shared=True, fp8_weights=False):
         self.H, self.I, self.E, self.K, self.Is = H, I, E, K, I_shared
         self.max_tokens = max_tokens
         # gather=True: the gate/up GEMM reads each routed row straight from x
@@ -48,13 +53,25 @@ class MoeBlock:
         self.gather = gather
         # fuse_shared: the shared expert's GEMMs run inside the routed GEMM
         # launches (one launch each for gate/up and down); False: own launches
-        self.fuse_shared = fuse_shared and not gather
+        self.fp8 = fp8_weights
+        self.fuse_shared = fuse_shared and not gather and not fp8_weights
+        if fp8_weights and gather:
+            raise ValueError("FP8 expert weights read x_perm rows (gather=False)")
         self.routed_scale = float(routed_scale)
         self.device = torch.device(device)
         dv = self.device
         self.w_router = _dev_bf16(weights["w_router"], dv)
-        self.w13 = _dev_bf16(weights["w13"], dv)
-        self.w2 = _dev_bf16(weights["w2"], dv)
+        if fp8_weights:
+            def dev(a, dt):
+                return torch.as_tensor(a).to(dtype=dt).to(dv).contiguous()
+            self.w13_q = dev(weights["w13_e4m3"], torch.uint8)
+            self.w13_s = dev(weights["w13_scale"], torch.float32)
+            self.w2_q = dev(weights["w2_e4m3"], torch.uint8)
+            self.w2_s = dev(weights["w2_scale"], torch.float32)
+            self.w13 = self.w2 = None
+        else:
+            self.w13 = _dev_bf16(weights["w13"], dv)
+            self.w2 = _dev_bf16(weights["w2"], dv)
         lb = weights.get("logit_bias")
         self.logit_bias = None if lb is None else torch.as_tensor(lb, dtype=torch.float32).to(dv)
         self.has_shared = I_shared > 0
@@ -115,7 +132,11 @@ class MoeBlock:
                     self.pair_to_row, self.x_perm, ws, ws.numel(), stream)
         mark("permute")
         fused = self.has_shared and self.fuse_shared
-        if fused:
+        if self.fp8:
+            moe_grouped_gemm_gateup_silu_fp8w(self.x_perm, self.w13_q, self.w13_s,
+                                              self.expert_offsets, P, H, I, E, self.act, None, 0,
+                                              stream)
+        elif fused:
             moe_grouped_gemm_gateup_silu_bf16_shared(self.x_perm, self.w13, self.expert_offsets,
                                                      P, H, I, E, self.act, x, T, self.w13_shared,
                                                      self.Is, self.act_shared, None, 0, stream)
@@ -128,7 +149,11 @@ class MoeBlock:
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,
                                               stream)
         mark("gemm_gateup")
-        if fused:
+        if self.fp8:
+            moe_grouped_gemm_down_fp8w(self.act, self.w2_q, self.w2_s, self.expert_offsets,
+                                       self.topk_w, self.sorted_pair, P, I, H, E, self.expert_out,
+                                       None, 0, stream)
+        elif fused:
             moe_grouped_gemm_down_bf16_shared(self.act, self.w2, self.expert_offsets, self.topk_w,
                                               self.sorted_pair, P, I, H, E, self.expert_out,
                                               self.act_shared, T, self.w2_shared, self.Is, self.sd,

@@ -176,6 +176,27 @@ def layer_inputs(cfg: LayerConfig, with_weights: bool = True) -> dict:
     return d
 
 
+def quantize_fp8_block(w_bits: np.ndarray):
+    """Block-scaled FP8 copy of bf16 weights [G, R, C] (input preparation for the
+    FP8-weight workloads): per 128 x 128 block, scale = max|w| / 448 (1 for an
+    all-zero block) and code = E4M3(w / scale), rounded to nearest even by
+    torch's float8_e4m3fn cast.  Returns (codes uint8 [G, R, C], scales f32
+    [G, ceil(R/128), ceil(C/128)])."""
+    import torch
+
+    G, R, C = w_bits.shape
+    rb, cb = (R + 127) // 128, (C + 127) // 128
+    w = torch.from_numpy(bf16_bits_to_f32(w_bits))
+    pad = torch.zeros((G, rb * 128, cb * 128), dtype=torch.float32)
+    pad[:, :R, :C] = w
+    blocks = pad.view(G, rb, 128, cb, 128)
+    amax = blocks.abs().amax(dim=(2, 4))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (blocks / scale[:, :, None, :, None]).to(torch.float8_e4m3fn)
+    codes = q.view(torch.uint8).view(G, rb * 128, cb * 128)[:, :R, :C].contiguous()
+    return codes.numpy(), scale.numpy().astype(np.float32)
+
+
 def rank_tokens(cfg: LayerConfig, rank: int) -> np.ndarray:
     """Tokens of data-parallel replica `rank` (rank 0 has the workload's own x)."""
     if rank == 0:

@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_refusals_without_gpu(lib):
-    assert m.abi_version() == 6
+    assert m.abi_version() == 7
     # dtype refusals name the missing arm and return before touching the device
     rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
     assert rc == m.ERR_DTYPE and "f16" in m.last_error()

@@ -194,6 +194,84 @@ def test_fused_shared_refusals():
     assert launches() == before
 
 
+FP8_SHAPES = [
+    # group sizes, H, I (few-row histograms take the 32-row tiles)
+    ([3, 200, 0, 77], 512, 256),
+    ([1, 1, 1, 1, 1, 1, 1, 1], 2048, 768),
+    ([40, 0, 70, 1, 33] + [0] * 11, 256, 192),
+    ([600, 5, 256, 255, 513], 256, 256),
+    ([257, 0, 0, 3], 144, 80),
+]
+
+
+def _fp8_weights(rng, G, R, C):
+    q = rng.integers(0, 256, (G, R, C), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x40                      # no NaN codes
+    scale = rng.uniform(1e-4, 3e-3, (G, (R + 127) // 128, (C + 127) // 128)).astype(np.float32)
+    return q, scale
+
+
+@pytest.mark.parametrize("sizes,H,I", FP8_SHAPES)
+def test_fp8_weight_gemms_against_the_oracle(sizes, H, I):
+    # block-scaled FP8 weights: the GPU dequantises in shared memory exactly as
+    # the oracle does (bf16(f32(code) * scale)), then the bf16 GEMM contract
+    off, P, G, A, _, _ = _case(sizes, H, I, sum(sizes) + 3 * H + I)
+    rng = np.random.default_rng(P + H)
+    q13, s13 = _fp8_weights(rng, G, 2 * I, H)
+    q2, s2 = _fp8_weights(rng, G, H, I)
+    W13 = O.dequant_fp8_block(q13, s13, G=G, R=2 * I, C=H)
+    W2 = O.dequant_fp8_block(q2, s2, G=G, R=H, C=I)
+    want_act = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G)
+    act = empty((P, I), torch.bfloat16)
+    act.fill_(0)
+    before = launches()
+    m.moe_grouped_gemm_gateup_silu_fp8w(to_dev(A), to_dev(q13), to_dev(s13), to_dev(off), P, H, I,
+                                        G, act)
+    assert launched_since(before, "gemm_gateup") == 1
+    assert m.moe_device_status() == 0
+    got_act = to_host(act)
+    assert_gemm_close(got_act, want_act, "fp8 gate/up")
+    wts = rng.uniform(0.05, 1.0, P).astype(np.float32)
+    r2p = rng.permutation(P).astype(np.int32)
+    want = O.down(got_act, W2, off, P=P, I=I, H=H, G=G, pair_weight=wts, row_to_pair=r2p)
+    out = empty((P, H), torch.bfloat16)
+    out.fill_(0)
+    m.moe_grouped_gemm_down_fp8w(act, to_dev(q2), to_dev(s2), to_dev(off), to_dev(wts),
+                                 to_dev(r2p), P, I, H, G, out)
+    assert m.moe_device_status() == 0
+    assert_gemm_close(to_host(out), want, "fp8 down")
+
+
+def test_fp8_weights_equal_their_bf16_dequantisation_on_the_gpu():
+    # the FP8 path against the bf16 path fed the oracle's dequantised weights:
+    # same tiles, same K order, so the results are bit-identical
+    sizes, H, I = [300, 0, 520, 7], 512, 256
+    off, P, G, A, _, _ = _case(sizes, H, I, 77)
+    rng = np.random.default_rng(78)
+    q13, s13 = _fp8_weights(rng, G, 2 * I, H)
+    W13 = O.dequant_fp8_block(q13, s13, G=G, R=2 * I, C=H)
+    a, b = empty((P, I), torch.bfloat16), empty((P, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_fp8w(to_dev(A), to_dev(q13), to_dev(s13), to_dev(off), P, H, I,
+                                        G, a)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I,
+                                        G, b)
+    assert np.array_equal(to_host(a), to_host(b))
+
+
+def test_fp8_refusals():
+    x = empty((4, 64), torch.bfloat16)
+    q = empty((1, 128, 64), torch.uint8)
+    before = launches()
+    with pytest.raises(m.MoeError) as ei:      # scales missing
+        m.moe_grouped_gemm_gateup_silu_fp8w(x, q, None, None, 4, 64, 64, 1, x)
+    assert ei.value.code == m.ERR_ARG
+    with pytest.raises(m.MoeError) as ei:      # contraction length not a multiple of 16
+        m.moe_grouped_gemm_down_fp8w(x, q, empty((1,), torch.float32), None, None, None, 4, 72,
+                                     64, 1, x)
+    assert ei.value.code == m.ERR_ALIGN
+    assert launches() == before
+
+
 def test_gateup_narrowing_is_visible_on_the_gpu(pairing):
     # g = u = 1 + 2^-9 exactly: narrowing before the activation gives
     # bf16(silu(1) * 1) = 0x3F3B; without it the result would be 0x3F3C

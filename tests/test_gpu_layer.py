@@ -270,3 +270,33 @@ def test_fused_shared_expert_matches_separate_launches(cfg):
         outs.append((o, to_host(blk.sd).copy(), to_host(blk.act_shared).copy()))
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("cfg", [W.DECODE, W.LayerConfig("fp8_T300_H512_I256_E16_K4_Is256",
+                                                           T=300, H=512, I=256, E=16, K=4,
+                                                           I_shared=256, zipf_s=1.1)],
+                         ids=lambda c: c.name)
+def test_fp8_expert_weights_layer_against_the_oracle(cfg):
+    # routed experts with block-scaled FP8 weights: the whole block against the
+    # oracle run on the dequantised weights, on sampled tokens
+    d = W.layer_inputs(cfg)
+    d["w13_e4m3"], d["w13_scale"] = W.quantize_fp8_block(d["w13"])
+    d["w2_e4m3"], d["w2_scale"] = W.quantize_fp8_block(d["w2"])
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                   I_shared=cfg.I_shared, fp8_weights=True)
+    out = to_host(blk.forward(to_dev(d["x"])))
+    do = dict(d)
+    do["w13"] = O.dequant_fp8_block(d["w13_e4m3"], d["w13_scale"], G=cfg.E, R=2 * cfg.I, C=cfg.H)
+    do["w2"] = O.dequant_fp8_block(d["w2_e4m3"], d["w2_scale"], G=cfg.E, R=cfg.H, C=cfg.I)
+    toks = np.unique(np.concatenate([[0, cfg.T - 1],
+                                     np.random.default_rng(3).choice(cfg.T, min(cfg.T, 24),
+                                                                      replace=False)]))
+    want, ora_ids, _ = _oracle_tokens(cfg, do, toks)
+    ids = to_host(blk.topk_ids)
+    same = np.all(np.sort(ora_ids, 1) == np.sort(ids[toks], 1), axis=1)
+    assert same.mean() >= 0.95
+    g, r = bf16_to_f64(out[toks][same]), bf16_to_f64(want[same])
+    nmse, _ = nmse_maxrel(g, r)
+    rms = float(np.sqrt(np.mean(r * r)))
+    worst = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), rms)))
+    assert nmse <= GEMM_NMSE and worst <= GEMM_MAXREL, (nmse, worst)
