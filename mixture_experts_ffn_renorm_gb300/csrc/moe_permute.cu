@@ -10,8 +10,8 @@
 //           counts in chunk order; then the exclusive scan over experts ->
 //           expert_offsets
 //   place   one warp per chunk again, 32 pairs at a time in pair order: the
-//           rank of a pair among equal experts of its step comes from
-//           __match_any_sync, so rows inside an expert ascend with p
+//           rank of a pair among equal experts of its step comes from one
+//           ballot per id bit, so rows inside an expert ascend with p
 //   gather  (optional) x_perm[row] = x[sorted_pair[row] / K], 16 bytes a thread
 // Up to kSmallChunks chunks whose histograms fit in 48 KB of shared memory
 // (decode batches; the large layer's 16384 pairs over 256 experts) count, scan
@@ -24,7 +24,78 @@ namespace moe {
 namespace {
 
 constexpr int kChunk = 512;  // pairs per warp
-constexpr int kWarps = 8;    // warps (chunks) per block
+constexpr int kWarps = 2;    // warps (chunks) per block: many small blocks spread the sort
+constexpr int kIdsPerLane = kChunk / 32;
+
+// A chunk's ids into registers, lane-strided (pair p0 + lane + 32 k in slot k),
+// every load in flight at once; pairs at or past p1 read as -1.
+__device__ __forceinline__ void load_chunk_ids(const int32_t* __restrict__ ids, int p0, int p1,
+                                               int lane, int (&v)[kIdsPerLane]) {
+#pragma unroll
+  for (int k = 0; k < kIdsPerLane; ++k) {
+    const int p = p0 + lane + 32 * k;
+    v[k] = p < p1 ? __ldg(ids + p) : -1;
+  }
+}
+
+// Histogram of a chunk's ids into the warp's shared counts; out-of-range ids
+// are skipped and reported through the status word.
+__device__ __forceinline__ void count_chunk_ids(const int (&v)[kIdsPerLane], int p0, int p1,
+                                                int E, int lane, int32_t* h,
+                                                unsigned int* status) {
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kIdsPerLane; ++k) {
+    const int e = v[k];
+    if (p0 + lane + 32 * k >= p1) continue;
+    if (e >= 0 && e < E) atomicAdd(h + e, 1);
+    else bad = true;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
+    atomicOr(status, static_cast<unsigned int>(MOE_STATUS_BAD_ID));
+}
+
+// The lanes of the warp holding the same expert id as this lane (among the
+// valid ones): one ballot per bit of the id, each narrowing the set to the
+// lanes that agree on that bit.  A fixed ceil(log2 E) ballots, where
+// __match_any_sync slows down with the number of distinct ids in the warp.
+__device__ __forceinline__ uint32_t same_expert_lanes(int e, bool valid, int id_bits) {
+  uint32_t peers = __ballot_sync(0xffffffffu, valid);
+  for (int b = 0; b < id_bits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const uint32_t m = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? m : ~m;
+  }
+  return peers;
+}
+
+// Stable placement of a chunk: cnt[e] holds the first row of expert e still
+// free for this chunk; 32 pairs at a time in pair order, the rank of a pair
+// among equal experts of its step from the lanes that share its id.
+__device__ __forceinline__ void place_chunk_ids(const int (&v)[kIdsPerLane], int p0, int p1,
+                                                int E, int lane, int32_t* cnt,
+                                                int32_t* __restrict__ sorted_pair,
+                                                int32_t* __restrict__ pair_to_row) {
+  const int id_bits = E > 1 ? 32 - __clz(E - 1) : 0;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int k = 0; k < kIdsPerLane; ++k) {
+    if (p0 + 32 * k >= p1) break;                // uniform across the warp
+    const int p = p0 + lane + 32 * k;
+    const int e = v[k];
+    const bool valid = p < p1 && e >= 0 && e < E;
+    const uint32_t peers = same_expert_lanes(e, valid, id_bits);
+    int row = 0;
+    if (valid) row = cnt[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) cnt[e] += __popc(peers);  // lowest lane of the group
+    __syncwarp();
+    if (valid) {
+      sorted_pair[row] = p;
+      pair_to_row[p] = row;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kWarps * 32)
 permute_count(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
@@ -40,14 +111,9 @@ permute_count(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   __syncwarp();
   if (c < n_chunks) {
     const int p0 = c * kChunk, p1 = min(P, p0 + kChunk);
-    bool bad = false;
-    for (int p = p0 + lane; p < p1; p += 32) {
-      const int e = __ldg(ids + p);
-      if (e >= 0 && e < E) atomicAdd(h + e, 1);
-      else bad = true;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
-      atomicOr(status, static_cast<unsigned int>(MOE_STATUS_BAD_ID));
+    int v[kIdsPerLane];
+    load_chunk_ids(ids, p0, p1, lane, v);
+    count_chunk_ids(v, p0, p1, E, lane, h, status);
     __syncwarp();
     for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(e) * n_chunks + c] = h[e];
   }
@@ -130,31 +196,14 @@ permute_place(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
   if (c >= n_chunks) return;
+  const int p0 = c * kChunk, p1 = min(P, p0 + kChunk);
+  int v[kIdsPerLane];
+  load_chunk_ids(ids, p0, p1, lane, v);          // in flight while the counts load
   int32_t* cnt = sh + warp * E;
   for (int e = lane; e < E; e += 32)
     cnt[e] = hist[static_cast<size_t>(e) * n_chunks + c] + __ldg(offsets + e);
   __syncwarp();
-  const int p0 = c * kChunk, p1 = min(P, p0 + kChunk);
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = p0; base < p1; base += 32) {
-    const int p = base + lane;
-    const int e = p < p1 ? __ldg(ids + p) : -1;
-    const bool valid = e >= 0 && e < E;
-    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-    int row = 0;
-    uint32_t peers = 0;
-    if (valid) {
-      peers = __match_any_sync(vmask, e);
-      row = cnt[e] + __popc(peers & lt_mask);
-    }
-    __syncwarp();
-    if (valid && (peers & lt_mask) == 0) cnt[e] += __popc(peers);  // lowest lane of the group
-    __syncwarp();
-    if (valid) {
-      sorted_pair[row] = p;
-      pair_to_row[p] = row;
-    }
-  }
+  place_chunk_ids(v, p0, p1, E, lane, cnt, sorted_pair, pair_to_row);
 }
 
 // One warp per permuted row; each lane keeps up to 8 16-byte vectors of the
@@ -206,20 +255,15 @@ permute_small(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   int32_t* base = sh + n_chunks * E;          // [E]: first row of each expert
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kT = kSmallChunks * 32;
-  // 1. per-chunk histograms
+  // 1. per-chunk histograms; the chunk's ids stay in registers for step 4
   int32_t* h = hist + warp * E;
+  const int p0 = warp * kChunk, p1 = min(P, p0 + kChunk);
+  int v[kIdsPerLane];
   if (warp < n_chunks) {
+    load_chunk_ids(ids, p0, p1, lane, v);
     for (int e = lane; e < E; e += 32) h[e] = 0;
     __syncwarp();
-    const int p0 = warp * kChunk, p1 = min(P, p0 + kChunk);
-    bool bad = false;
-    for (int p = p0 + lane; p < p1; p += 32) {
-      const int e = __ldg(ids + p);
-      if (e >= 0 && e < E) atomicAdd(h + e, 1);
-      else bad = true;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0 && status)
-      atomicOr(status, static_cast<unsigned int>(MOE_STATUS_BAD_ID));
+    count_chunk_ids(v, p0, p1, E, lane, h, status);
   }
   __syncthreads();
   // 2. per expert: exclusive prefix over the chunks (in chunk order), total in base[e]
@@ -267,27 +311,7 @@ permute_small(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
   if (warp >= n_chunks) return;
   for (int e = lane; e < E; e += 32) h[e] += base[e];
   __syncwarp();
-  const int p0 = warp * kChunk, p1 = min(P, p0 + kChunk);
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int b = p0; b < p1; b += 32) {
-    const int p = b + lane;
-    const int e = p < p1 ? __ldg(ids + p) : -1;
-    const bool valid = e >= 0 && e < E;
-    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-    int row = 0;
-    uint32_t peers = 0;
-    if (valid) {
-      peers = __match_any_sync(vmask, e);
-      row = h[e] + __popc(peers & lt_mask);
-    }
-    __syncwarp();
-    if (valid && (peers & lt_mask) == 0) h[e] += __popc(peers);
-    __syncwarp();
-    if (valid) {
-      sorted_pair[row] = p;
-      pair_to_row[p] = row;
-    }
-  }
+  place_chunk_ids(v, p0, p1, E, lane, h, sorted_pair, pair_to_row);
 }
 
 int n_chunks_of(long long P) { return static_cast<int>((P + kChunk - 1) / kChunk); }
