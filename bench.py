@@ -336,6 +336,10 @@ def run_reference(args):
     d = W.layer_inputs(cfg)
     import oracle as O
 
+    if getattr(args, "weights", "bf16") == "fp8":  # the layer on the dequantised FP8 weights
+        for key, R, C in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
+            q, sc = W.quantize_fp8_block(d[key])
+            d[key] = O.dequant_fp8_block(q, sc, G=cfg.E, R=R, C=C)
     cores = O.max_threads()
     n = max(cores, 8) if cfg.T >= 64 else cfg.T
     tokens = np.arange(n, dtype=np.int32)
@@ -355,7 +359,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_dict(cfg, 1),
+        "config": dict(config_dict(cfg, 1), weights=getattr(args, "weights", "bf16")),
         "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "tokens/s",
                          "sample": f"{n} of {cfg.T} tokens per step, full block per token"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
