@@ -82,3 +82,40 @@ def test_workspace_queries(lib):
     assert m.moe_permute_workspace_size(8192, 8, 128) >= (65536 // 512) * 128 * 4
     assert m.moe_permute_workspace_size(0, 8, 128) == 0
     assert m.moe_grouped_gemm_workspace_size(65536, 2048, 768, 128) == 0
+
+
+def test_newer_entry_points_refuse_without_touching_the_device(lib):
+    # argument checks of the fused shared-expert GEMMs, the extended router and
+    # the FP8-weight GEMMs all fail before any CUDA call
+    import ctypes
+    I, Z = ctypes.c_int, ctypes.c_size_t(0)
+    # fused shared expert: I_shared not a multiple of 8
+    rc = lib.moe_grouped_gemm_gateup_silu_bf16_shared(None, None, None, 0, 64, 64, 1, None, None,
+                                                      4, None, 36, None, None, Z, None)
+    assert rc == m.ERR_ALIGN and "I_shared" in m.last_error()
+    # fused shared expert: shared rows without operands
+    rc = lib.moe_grouped_gemm_down_bf16_shared(None, None, None, None, None, 0, 64, 64, 1, None,
+                                               None, 4, None, 64, None, None, Z, None)
+    assert rc == m.ERR_ARG
+    # extended router: scoring 2, a bias with softmax, a group count that does not divide E
+    rc = lib.moe_route_topk_ex(None, None, None, None, None, None, 1, 8, 16, 2, 1, 2, 1, 1, 0,
+                               None, None, None, None, None, Z, None)
+    assert rc == m.ERR_UNSUPPORTED and "scoring" in m.last_error()
+    bias = (ctypes.c_float * 16)()
+    rc = lib.moe_route_topk_ex(None, None, None, bias, None, None, 1, 8, 16, 2, 1, 0, 1, 1, 0,
+                               None, None, None, None, None, Z, None)
+    assert rc == m.ERR_UNSUPPORTED and "sigmoid" in m.last_error()
+    rc = lib.moe_route_topk_ex(None, None, None, None, None, None, 1, 8, 16, 2, 1, 1, 3, 1, 0,
+                               None, None, None, None, None, Z, None)
+    assert rc == m.ERR_ARG and "n_group" in m.last_error()
+    # plain router points at the extended entry for grouped routing
+    rc = lib.moe_route_topk(None, None, None, None, None, 1, 8, 16, 2, 1, 0, 4, None, None, None,
+                            None, None, Z, None)
+    assert rc == m.ERR_UNSUPPORTED and "moe_route_topk_ex" in m.last_error()
+    # FP8 weights: missing scales
+    buf = (ctypes.c_uint8 * 4096)()
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    rc = lib.moe_grouped_gemm_gateup_silu_fp8w(ctypes.c_void_p(addr), ctypes.c_void_p(addr), None,
+                                               None, 4, 64, 64, 1, ctypes.c_void_p(addr), None, Z,
+                                               None)
+    assert rc == m.ERR_ARG and "scales" in m.last_error()
