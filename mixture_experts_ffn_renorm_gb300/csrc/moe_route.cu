@@ -239,7 +239,9 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
   const int n_live = min(kWarpsPerBlock, T - static_cast<int>(blockIdx.x) * kWarpsPerBlock);
   for (int q = threadIdx.x; q < n_live * K; q += blockDim.x) {
     const int tt = q / K, j = q - tt * K;
-    s_ex[tt][j] = exp_cr(__fsub_rn(s_sel[tt][j], s_sel[tt][0]));
+    const float d = __fsub_rn(s_sel[tt][j], s_sel[tt][0]);
+    // rank 0: d is +0 for a finite top logit and exp_cr(+0) is exactly 1
+    s_ex[tt][j] = (j == 0 && d == 0.0f) ? 1.0f : exp_cr(d);
   }
   __syncthreads();
   if (!live) return;
