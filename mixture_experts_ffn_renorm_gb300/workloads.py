@@ -37,6 +37,13 @@ CHUNK = 1 << 22
 TAG_X, TAG_WR, TAG_W13, TAG_W2, TAG_WSG, TAG_W13S, TAG_W2S, TAG_RANK = 1, 2, 3, 4, 5, 6, 7, 8
 TAG_EO, TAG_LOGITS, TAG_SD, TAG_GL = 11, 12, 13, 14
 TAG_X_RANK = 1000  # + rank: the tokens of data-parallel replica `rank`
+TAG_W13Q, TAG_W2Q, TAG_W13S_Q = 21, 22, 23  # keep-quant expert weights (random valid blocks)
+
+# keep-quant weight formats: (weights per block, bytes per block, bytes of
+# fp16 scale fields at the block's start); the remaining bytes of a block
+# (int8 codes, resp. packed 6-bit scales/mins and 4-bit codes) are free bits
+# in which every pattern is a valid block
+Q_FORMATS = {"q8_0": (1, 32, 34, 1), "q4_k": (2, 256, 144, 2)}  # name: (id, block, bytes, fp16s)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -195,6 +202,54 @@ def quantize_fp8_block(w_bits: np.ndarray):
     q = (blocks / scale[:, :, None, :, None]).to(torch.float8_e4m3fn)
     codes = q.view(torch.uint8).view(G, rb * 128, cb * 128)[:, :R, :C].contiguous()
     return codes.numpy(), scale.numpy().astype(np.float32)
+
+
+def q_weights(seed: int, tag: int, G: int, R: int, K: int, fmt: str, std: float) -> np.ndarray:
+    """Random valid keep-quant weight blocks, uint8 [G, R, (K / block) * bytes].
+
+    Each block's free bytes are uniform random bytes.  Its fp16 scale fields
+    are drawn so that the weights have a standard deviation near `std`:
+    Q8_0 d = std/74 * U(0.8, 1.2) (uniform int8 codes have sd ~74); Q4_K
+    d = std/240 * U(0.8, 1.2) and dmin = 7.5 d * U(0.8, 1.2), which centres
+    d*sc*q - dmin*m for uniform 6-bit sc, m and 4-bit q.  The stream is
+    chunked by 2**20 blocks, (seed, tag, chunk), like the bf16 tensors.
+    """
+    _, blk, bb, n16 = Q_FORMATS[fmt]
+    if K % blk:
+        raise ValueError(f"K={K} is not a multiple of the {fmt} block ({blk})")
+    nblk = G * R * (K // blk)
+    out = np.empty((nblk, bb), np.uint8)
+    step = 1 << 20
+
+    def fill(c: int) -> None:
+        lo, hi = c * step, min(nblk, (c + 1) * step)
+        rng = np.random.default_rng([seed, tag, c])
+        out[lo:hi] = rng.integers(0, 256, size=(hi - lo, bb), dtype=np.uint8)
+        u = rng.uniform(0.8, 1.2, size=(hi - lo, 2))
+        if fmt == "q8_0":
+            d = (std / 74.0) * u[:, 0]
+            scales = d[:, None]
+        else:
+            d = (std / 240.0) * u[:, 0]
+            scales = np.stack([d, 7.5 * d * u[:, 1]], axis=1)
+        out[lo:hi, :2 * n16] = scales.astype(np.float16).view(np.uint8).reshape(hi - lo, 2 * n16)
+
+    n = (nblk + step - 1) // step
+    if n <= 1:
+        for c in range(n):
+            fill(c)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(fill, range(n)))
+    return out.reshape(G, R, (K // blk) * bb)
+
+
+def layer_q_weights(cfg: LayerConfig, fmt: str) -> dict:
+    """Keep-quant expert weights of a layer: w13q [E, 2I, H/blk*bytes], w2q [E, H, I/blk*bytes]."""
+    return {
+        "w13q": q_weights(cfg.seed, TAG_W13Q, cfg.E, 2 * cfg.I, cfg.H, fmt, 0.02),
+        "w2q": q_weights(cfg.seed, TAG_W2Q, cfg.E, cfg.H, cfg.I, fmt, 0.02),
+    }
 
 
 def rank_tokens(cfg: LayerConfig, rank: int) -> np.ndarray:

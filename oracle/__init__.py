@@ -61,6 +61,16 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I], _I),
         "oracle_moe_layer_tokens": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
                                      _P, _I, _P, _P, _P], _I),
+        "oracle_f16_to_f32": ([ctypes.c_uint16], _F),
+        "oracle_f32_to_f16": ([_F], ctypes.c_uint16),
+        "oracle_q4k_scale_min": ([_P, _I, _P], _I),
+        "oracle_dequant_q": ([_P, _I, _I64, _I, _P], _I),
+        "oracle_quantize_act_q8": ([_P, _I64, _I, _I, _P, _P], _I),
+        "oracle_gemm_q": ([_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
+        "oracle_gateup_silu_q": ([_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P], _I),
+        "oracle_down_q": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P], _I),
+        "oracle_moe_layer_tokens_q": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I,
+                                       _F, _P, _I, _P, _P, _P], _I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -238,6 +248,102 @@ def moe_layer_tokens(x, w_router, logit_bias, w13, w2, w_shared_gate, w13_shared
                                        _ptr(w2_shared), H, I, E, K, I_shared, routed_scale,
                                        _ptr(tok), n, _ptr(ids), _ptr(w), _ptr(out))
     _check(rc, "moe_layer_tokens")
+    return out, ids, w
+
+
+# ---------------------------------------------------------------- keep-quant
+Q8_0, Q4_K = 1, 2
+Q_BLOCK = {Q8_0: 32, Q4_K: 256}          # weights per block
+Q_BLOCK_BYTES = {Q8_0: 34, Q4_K: 144}    # bytes per block
+
+
+def f16_to_f32(bits):
+    """f32 values of fp16 bit patterns (uint16 array)."""
+    bits = np.ascontiguousarray(bits, np.uint16)
+    return np.array([lib().oracle_f16_to_f32(int(b)) for b in bits.ravel()],
+                    np.float32).reshape(bits.shape)
+
+
+def f32_to_f16(x):
+    """fp16 bit patterns (round to nearest even) of f32 values."""
+    x = np.ascontiguousarray(x, np.float32)
+    return np.array([lib().oracle_f32_to_f16(float(v)) for v in x.ravel()],
+                    np.uint16).reshape(x.shape)
+
+
+def q4k_scale_min(scales12, j):
+    """(scale, min) of Q4_K sub-block j from the 12 packed scale bytes."""
+    out = np.zeros(2, np.int32)
+    _check(lib().oracle_q4k_scale_min(_ptr(np.ascontiguousarray(scales12, np.uint8)), int(j),
+                                      _ptr(out)), "q4k_scale_min")
+    return int(out[0]), int(out[1])
+
+
+def dequant_q(w, fmt, *, rows, K):
+    """exact values (float64 [rows, K]) of `rows` weight rows stored in `fmt` blocks."""
+    out = np.zeros((rows, K), np.float64)
+    rc = lib().oracle_dequant_q(_ptr(np.ascontiguousarray(w, np.uint8)), fmt, rows, K, _ptr(out))
+    _check(rc, "dequant_q")
+    return out
+
+
+def quantize_act_q8(x, fmt, *, R, K):
+    """8-bit activation blocks of bf16 rows x [R, K]: (codes int8 [R, K], scales f32 [R, K/blk])."""
+    q = np.zeros((R, K), np.int8)
+    d = np.zeros((R, K // Q_BLOCK[fmt]), np.float32)
+    rc = lib().oracle_quantize_act_q8(_ptr(np.ascontiguousarray(x, np.uint16)), R, K, fmt,
+                                      _ptr(q), _ptr(d))
+    _check(rc, "quantize_act_q8")
+    return q, d
+
+
+def gemm_q(aq, ad, w, fmt, group_offsets, *, P, K, N, G, a_row_gather=None, gather_div=1,
+           rows=None):
+    """plain grouped keep-quant matmul: (y float64 [P, N], yabs float64 [P, N])."""
+    y = np.zeros((P, N), np.float64)
+    ya = np.zeros((P, N), np.float64)
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    rc = lib().oracle_gemm_q(_ptr(aq), _ptr(ad), _ptr(a_row_gather), gather_div, _ptr(w), fmt,
+                             _ptr(group_offsets), P, K, N, G, _ptr(r), 0 if r is None else r.size,
+                             _ptr(y), _ptr(ya))
+    _check(rc, "gemm_q")
+    return y, ya
+
+
+def gateup_silu_q(aq, ad, w13, fmt, group_offsets, *, P, H, I, G, a_row_gather=None,
+                  gather_div=1, rows=None):
+    act = np.zeros((P, I), np.uint16)
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    rc = lib().oracle_gateup_silu_q(_ptr(aq), _ptr(ad), _ptr(a_row_gather), gather_div, _ptr(w13),
+                                    fmt, _ptr(group_offsets), P, H, I, G, _ptr(r),
+                                    0 if r is None else r.size, _ptr(act))
+    _check(rc, "gateup_silu_q")
+    return act
+
+
+def down_q(aq, ad, w2, fmt, group_offsets, *, P, I, H, G, pair_weight=None, row_to_pair=None,
+           rows=None):
+    out = np.zeros((P, H), np.uint16)
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    rc = lib().oracle_down_q(_ptr(aq), _ptr(ad), _ptr(w2), fmt, _ptr(group_offsets),
+                             _ptr(pair_weight), _ptr(row_to_pair), P, I, H, G, _ptr(r),
+                             0 if r is None else r.size, _ptr(out))
+    _check(rc, "down_q")
+    return out
+
+
+def moe_layer_tokens_q(x, w_router, logit_bias, w13q, w2q, fmt, w_shared_gate, w13_shared,
+                       w2_shared, *, H, I, E, K, I_shared=0, routed_scale=1.0, tokens):
+    tok = np.ascontiguousarray(tokens, np.int32)
+    n = tok.size
+    ids = np.zeros((n, K), np.int32)
+    w = np.zeros((n, K), np.float32)
+    out = np.zeros((n, H), np.uint16)
+    rc = lib().oracle_moe_layer_tokens_q(_ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(w13q),
+                                         _ptr(w2q), fmt, _ptr(w_shared_gate), _ptr(w13_shared),
+                                         _ptr(w2_shared), H, I, E, K, I_shared, routed_scale,
+                                         _ptr(tok), n, _ptr(ids), _ptr(w), _ptr(out))
+    _check(rc, "moe_layer_tokens_q")
     return out, ids, w
 
 

@@ -38,7 +38,7 @@
 #define ORA_BF16 1
 #define ORA_F16 2
 
-int oracle_abi_version(void) { return 3; }
+int oracle_abi_version(void) { return 4; }
 
 void oracle_set_threads(int n) {
 #ifdef _OPENMP
@@ -469,19 +469,25 @@ static float silu_f32(float z) {
   return z / d;
 }
 
-/* one output row; narrow = 0 is a planted mutation used only by tests */
+/* act = bf16(silu(g) * u) with g and u narrowed to bf16 first; narrow = 0 is
+ * a planted mutation used only by tests */
+static uint16_t gateup_out(float g, float u, int narrow) {
+  if (narrow) {
+    g = bf16_round(g);
+    u = bf16_round(u);
+  }
+  float s = silu_f32(g);
+  float v = s * u;
+  return f2bf(v);
+}
+
+/* one output row */
 static void gateup_row(const uint16_t* a_row, const uint16_t* w13_g, int H, int I,
                        uint16_t* act_row, int narrow) {
   for (int n = 0; n < I; ++n) {
     float g = dot_bf16(a_row, w13_g + (int64_t)n * H, H);
     float u = dot_bf16(a_row, w13_g + (int64_t)(I + n) * H, H);
-    if (narrow) {
-      g = bf16_round(g);
-      u = bf16_round(u);
-    }
-    float s = silu_f32(g);
-    float v = s * u;
-    act_row[n] = f2bf(v);
+    act_row[n] = gateup_out(g, u, narrow);
   }
 }
 
@@ -698,6 +704,386 @@ int oracle_moe_layer_tokens(const uint16_t* x, const uint16_t* w_router, const f
     }
     if (ids_out) memcpy(ids_out + (int64_t)i * K, ids, sizeof(int32_t) * (size_t)K);
     if (w_out) memcpy(w_out + (int64_t)i * K, wts, sizeof(float) * (size_t)K);
+    free(act);
+    free(eo);
+  }
+  return ORA_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Keep-quant expert GEMM: kMatmulBTQuant / kMatmulBTQuantGrouped of    */
+/* vllm.cpp PR #523 ("What changed"): the expert matmul runs on the     */
+/* quantized weights as stored, grouped over the expert ids.  Activations */
+/* are quantized to 8-bit blocks (a Q8_0 quantizer for Q8_0 weights, a   */
+/* Q8_K one for the K-quant formats) and each block's dot product is an  */
+/* exact integer sum.  PR #523 "Evidence" checks it at NMSE <= 5e-4      */
+/* against a CPU keep-quant reference.                                   */
+/*                                                                      */
+/* Weight formats (the GGUF block layouts, stored little-endian):        */
+/*   Q8_0: 32 weights in 34 bytes -- fp16 d, int8 q[32]; w = d * q.       */
+/*   Q4_K: 256 weights in 144 bytes -- fp16 d, fp16 dmin, 12 bytes of    */
+/*         packed 6-bit sub-block scales and mins, 128 bytes of 4-bit    */
+/*         codes; sub-block j (32 weights) has w = d*sc_j*q - dmin*m_j.  */
+/* READING (activation quantizer; the pages name it but do not define    */
+/* it): per block of 32 (Q8_0) or 256 (Q8_K) values,                     */
+/*   amax = max |x|,  d = amax / 127,  id = d != 0 ? 1 / d : 0,           */
+/*   q = round-half-away(x * id), NaN -> 0, clamped to [-127, 127],      */
+/* every operation one binary32 rounding; the Q8_0 block stores d rounded */
+/* to fp16 (the Q8_0 format), the Q8_K block keeps the f32 d.  Codes go  */
+/* to an int8 [R, K] plane and scales to an f32 [R, K/block] plane.       */
+/* READING (float combination): the integer block sums are exact; the    */
+/* oracle combines them in double precision, block after block, and     */
+/* rounds the row result to binary32 once.                              */
+/* ------------------------------------------------------------------ */
+
+#define ORA_Q8_0 1
+#define ORA_Q4_K 2
+
+/* fp16 bits -> f32, exact */
+static float h2f(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+  float v;
+  if (e == 31)
+    v = m ? NAN : INFINITY;
+  else if (e == 0)
+    v = ldexpf((float)m, -24);
+  else
+    v = ldexpf((float)(1024 + m), e - 25);
+  return sign ? -v : v;
+}
+
+/* f32 -> fp16 bits, round to nearest, ties to even, from the definition:
+ * keep the top 11 significant bits (fewer below 2^-14, where the spacing is
+ * fixed at 2^-24), then round up when the dropped part is above one half or
+ * exactly one half with an odd kept part; a carry moves into the exponent,
+ * up to infinity.  NaN gives the quiet NaN 0x7e00 with the sign kept. */
+static uint16_t f2h(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return sign | 0x7E00u;
+  if (a == 0x7F800000u) return sign | 0x7C00u;
+  const int e = (int)(a >> 23) - 127; /* unbiased exponent (-127 for f32 subnormals) */
+  if (e >= 16) return sign | 0x7C00u;
+  uint32_t sig; /* significand with the implicit bit */
+  int shift;    /* bits dropped to reach the fp16 spacing */
+  if (e >= -14) {
+    sig = (a & 0x7FFFFFu) | 0x800000u;
+    shift = 13;
+  } else {
+    sig = (e == -127) ? (a & 0x7FFFFFu) : ((a & 0x7FFFFFu) | 0x800000u);
+    const int e_eff = (e == -127) ? -126 : e;
+    shift = 13 + (-14 - e_eff); /* value = sig * 2^(e_eff-23); fp16 unit 2^-24 */
+    if (shift > 31) return sign;
+  }
+  uint32_t kept = sig >> shift;
+  const uint32_t dropped = sig & ((1u << shift) - 1u);
+  const uint32_t half = 1u << (shift - 1);
+  if (dropped > half || (dropped == half && (kept & 1u))) kept += 1u;
+  uint32_t bits;
+  if (e >= -14)
+    bits = ((uint32_t)(e + 15) << 10) + (kept - 1024u); /* carry reaches the exponent */
+  else
+    bits = kept; /* subnormal, or 0x400 = the smallest normal after a carry */
+  return sign | (uint16_t)bits;
+}
+
+float oracle_f16_to_f32(uint16_t h) { return h2f(h); }
+uint16_t oracle_f32_to_f16(float f) { return f2h(f); }
+
+static uint16_t le16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+static int q_block(int fmt) { return fmt == ORA_Q8_0 ? 32 : (fmt == ORA_Q4_K ? 256 : 0); }
+static int q_block_bytes(int fmt) { return fmt == ORA_Q8_0 ? 34 : (fmt == ORA_Q4_K ? 144 : 0); }
+
+/* Q4_K: the 6-bit scale and min of sub-block j (0..7) from the 12 packed
+ * bytes.  Sub-blocks 0-3 keep theirs in the low six bits of bytes j
+ * (scale) and j+4 (min); sub-blocks 4-7 take their low four bits from the
+ * two nibbles of byte j+4 and their top two bits from the top bits of
+ * bytes j-4 (scale) and j (min). */
+static void q4k_scale_min(const uint8_t* s, int j, int* sc, int* m) {
+  if (j < 4) {
+    *sc = s[j] & 63;
+    *m = s[j + 4] & 63;
+  } else {
+    *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+    *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+  }
+}
+
+int oracle_q4k_scale_min(const uint8_t* scales12, int j, int32_t* sc_m) {
+  if (!scales12 || !sc_m || j < 0 || j > 7) return ORA_ERR_ARG;
+  int sc, m;
+  q4k_scale_min(scales12, j, &sc, &m);
+  sc_m[0] = sc;
+  sc_m[1] = m;
+  return ORA_OK;
+}
+
+/* Q4_K: the 4-bit code of weight k (0..255) of a super-block.  Each group of
+ * 64 weights owns 32 bytes of codes: the low nibble of byte i is weight i of
+ * the group's first sub-block, the high nibble weight i of its second. */
+static int q4k_code(const uint8_t* qs, int k) {
+  const int c = k / 64, o = k % 64;
+  const uint8_t b = qs[32 * c + (o % 32)];
+  return o < 32 ? (b & 15) : (b >> 4);
+}
+
+/* rows x K weights in `fmt` blocks -> exact values (double) */
+int oracle_dequant_q(const uint8_t* w, int fmt, int64_t rows, int K, double* out) {
+  const int blk = q_block(fmt), bb = q_block_bytes(fmt);
+  if (!blk || !w || !out || rows < 0 || K <= 0 || K % blk) return ORA_ERR_ARG;
+  const int64_t nb = K / blk;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* p = w + (r * nb + b) * bb;
+      double* o = out + r * K + b * blk;
+      if (fmt == ORA_Q8_0) {
+        const double d = h2f(le16(p));
+        for (int i = 0; i < 32; ++i) o[i] = d * (double)(int8_t)p[2 + i];
+      } else {
+        const double d = h2f(le16(p)), dmin = h2f(le16(p + 2));
+        for (int k = 0; k < 256; ++k) {
+          int sc, m;
+          q4k_scale_min(p + 4, k / 32, &sc, &m);
+          o[k] = d * sc * q4k_code(p + 16, k) - dmin * m;
+        }
+      }
+    }
+  return ORA_OK;
+}
+
+/* activation quantizer (READING above): x bf16 [R, K] -> q int8 [R, K],
+ * d f32 [R, K / block] with block 32 (fmt Q8_0) or 256 (fmt Q4_K) */
+int oracle_quantize_act_q8(const uint16_t* x, int64_t R, int K, int fmt, int8_t* q, float* d) {
+  const int blk = q_block(fmt);
+  if (!blk || !x || !q || !d || R < 0 || K <= 0 || K % blk) return ORA_ERR_ARG;
+  const int64_t nb = K / blk;
+#pragma omp parallel for schedule(static)
+  for (int64_t rb = 0; rb < R * nb; ++rb) {
+    const uint16_t* xb = x + rb * blk;
+    float amax = 0.0f;
+    for (int i = 0; i < blk; ++i) {
+      const float a = fabsf(bf2f(xb[i]));
+      if (a > amax) amax = a;
+    }
+    const float dd = amax / 127.0f;
+    const float id = dd != 0.0f ? 1.0f / dd : 0.0f;
+    for (int i = 0; i < blk; ++i) {
+      float r = roundf(bf2f(xb[i]) * id);
+      if (r != r) r = 0.0f;
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      q[rb * blk + i] = (int8_t)r;
+    }
+    d[rb] = fmt == ORA_Q8_0 ? h2f(f2h(dd)) : dd;
+  }
+  return ORA_OK;
+}
+
+/* one keep-quant dot product: activation row (codes aq, scales ad) with one
+ * weight row of K weights; *abs_out = the sum of the block terms' magnitudes */
+static double qdot(const int8_t* aq, const float* ad, const uint8_t* wrow, int fmt, int K,
+                   double* abs_out) {
+  double y = 0.0, ya = 0.0;
+  if (fmt == ORA_Q8_0) {
+    for (int b = 0; b < K / 32; ++b) {
+      const uint8_t* p = wrow + (int64_t)b * 34;
+      int64_t isum = 0;
+      for (int i = 0; i < 32; ++i) isum += (int64_t)(int8_t)p[2 + i] * aq[b * 32 + i];
+      const double t = (double)h2f(le16(p)) * (double)ad[b] * (double)isum;
+      y += t;
+      ya += fabs(t);
+    }
+  } else {
+    for (int b = 0; b < K / 256; ++b) {
+      const uint8_t* p = wrow + (int64_t)b * 144;
+      const int8_t* a = aq + b * 256;
+      int64_t s1 = 0, s2 = 0;
+      for (int j = 0; j < 8; ++j) {
+        int sc, m;
+        q4k_scale_min(p + 4, j, &sc, &m);
+        int64_t isum = 0, asum = 0;
+        for (int i = 0; i < 32; ++i) {
+          isum += (int64_t)q4k_code(p + 16, 32 * j + i) * a[32 * j + i];
+          asum += a[32 * j + i];
+        }
+        s1 += sc * isum;
+        s2 += m * asum;
+      }
+      const double dx = ad[b], t1 = (double)h2f(le16(p)) * (double)s1,
+                   t2 = (double)h2f(le16(p + 2)) * (double)s2;
+      y += dx * (t1 - t2);
+      ya += fabs(dx) * (fabs(t1) + fabs(t2));
+    }
+  }
+  if (abs_out) *abs_out = ya;
+  return y;
+}
+
+static int q_args_ok(int fmt, int K, const int32_t* off, int G, int P) {
+  if (!q_block(fmt) || K <= 0 || K % q_block(fmt) || G <= 0 || P < 0) return 0;
+  if (!off && G != 1) return 0;
+  return offsets_ok(off, G, P);
+}
+
+/* plain grouped keep-quant matmul: y[r, n] = sum_k A[src(r), k] * W[g, n, k]
+ * for rows r of group g, src(r) = a_row_gather ? a_row_gather[r] / gather_div : r;
+ * y (and yabs, the per-element sum of block-term magnitudes) in double */
+int oracle_gemm_q(const int8_t* aq, const float* ad, const int32_t* a_row_gather, int gather_div,
+                  const uint8_t* w, int fmt, const int32_t* group_offsets, int P, int K, int N,
+                  int G, const int32_t* rows, int n_rows, double* y, double* yabs) {
+  if (!q_args_ok(fmt, K, group_offsets, G, P) || N <= 0 || !aq || !ad || !w || !y)
+    return ORA_ERR_ARG;
+  if (a_row_gather && gather_div < 1) return ORA_ERR_ARG;
+  int32_t single[2] = {0, P};
+  const int32_t* off = group_offsets ? group_offsets : single;
+  const int64_t nb = K / q_block(fmt), row_bytes = nb * q_block_bytes(fmt);
+  const int64_t n = rows ? n_rows : (int64_t)off[G] - off[0];
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t r = rows ? rows[i] : off[0] + i;
+    const int g = group_of_row(off, G, r);
+    if (g < 0) continue;
+    const int64_t src = a_row_gather ? a_row_gather[r] / gather_div : r;
+    for (int64_t c = 0; c < N; ++c) {
+      double ya;
+      y[r * N + c] = qdot(aq + src * K, ad + src * nb, w + ((int64_t)g * N + c) * row_bytes, fmt,
+                          K, &ya);
+      if (yabs) yabs[r * N + c] = ya;
+    }
+  }
+  return ORA_OK;
+}
+
+static void gateup_q_row(const int8_t* aq, const float* ad, const uint8_t* w13_g, int fmt, int H,
+                         int I, uint16_t* act_row) {
+  const int64_t row_bytes = (int64_t)(H / q_block(fmt)) * q_block_bytes(fmt);
+  for (int n = 0; n < I; ++n) {
+    const float g = (float)qdot(aq, ad, w13_g + n * row_bytes, fmt, H, NULL);
+    const float u = (float)qdot(aq, ad, w13_g + (int64_t)(I + n) * row_bytes, fmt, H, NULL);
+    act_row[n] = gateup_out(g, u, 1);
+  }
+}
+
+static void down_q_row(const int8_t* aq, const float* ad, const uint8_t* w2_g, int fmt, int I,
+                       int H, const float* weight, uint16_t* out_row) {
+  const int64_t row_bytes = (int64_t)(I / q_block(fmt)) * q_block_bytes(fmt);
+  for (int n = 0; n < H; ++n) {
+    float y = (float)qdot(aq, ad, w2_g + n * row_bytes, fmt, I, NULL);
+    if (weight) y = y * (*weight);
+    out_row[n] = f2bf(y);
+  }
+}
+
+/* gate/up with SiLU-and-mul on keep-quant weights: the bf16 gate/up contract
+ * (narrowing before the activation) on top of the keep-quant dot products;
+ * w13 [G, 2I, H/block] blocks, gate rows first */
+int oracle_gateup_silu_q(const int8_t* aq, const float* ad, const int32_t* a_row_gather,
+                         int gather_div, const uint8_t* w13, int fmt,
+                         const int32_t* group_offsets, int P, int H, int I, int G,
+                         const int32_t* rows, int n_rows, uint16_t* act) {
+  if (!q_args_ok(fmt, H, group_offsets, G, P) || I <= 0 || !aq || !ad || !w13 || !act)
+    return ORA_ERR_ARG;
+  if (a_row_gather && gather_div < 1) return ORA_ERR_ARG;
+  int32_t single[2] = {0, P};
+  const int32_t* off = group_offsets ? group_offsets : single;
+  const int64_t nb = H / q_block(fmt), row_bytes = nb * q_block_bytes(fmt);
+  const int64_t n = rows ? n_rows : (int64_t)off[G] - off[0];
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t r = rows ? rows[i] : off[0] + i;
+    const int g = group_of_row(off, G, r);
+    if (g < 0) continue;
+    const int64_t src = a_row_gather ? a_row_gather[r] / gather_div : r;
+    gateup_q_row(aq + src * H, ad + src * nb, w13 + (int64_t)g * 2 * I * row_bytes, fmt, H, I,
+                 act + r * I);
+  }
+  return ORA_OK;
+}
+
+/* down on keep-quant weights: the bf16 down contract (one f32 weight
+ * multiply, one bf16 rounding, scatter to pair order); w2 [G, H, I/block] */
+int oracle_down_q(const int8_t* aq, const float* ad, const uint8_t* w2, int fmt,
+                  const int32_t* group_offsets, const float* pair_weight,
+                  const int32_t* row_to_pair, int P, int I, int H, int G, const int32_t* rows,
+                  int n_rows, uint16_t* out) {
+  if (!q_args_ok(fmt, I, group_offsets, G, P) || H <= 0 || !aq || !ad || !w2 || !out)
+    return ORA_ERR_ARG;
+  int32_t single[2] = {0, P};
+  const int32_t* off = group_offsets ? group_offsets : single;
+  const int64_t nb = I / q_block(fmt), row_bytes = nb * q_block_bytes(fmt);
+  const int64_t n = rows ? n_rows : (int64_t)off[G] - off[0];
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t r = rows ? rows[i] : off[0] + i;
+    const int g = group_of_row(off, G, r);
+    if (g < 0) continue;
+    const int64_t dst = row_to_pair ? row_to_pair[r] : r;
+    down_q_row(aq + r * I, ad + r * nb, w2 + (int64_t)g * H * row_bytes, fmt, I, H,
+               pair_weight ? pair_weight + dst : NULL, out + dst * H);
+  }
+  return ORA_OK;
+}
+
+/* The whole block with keep-quant expert weights, token by token: the bf16
+ * router, then per selected expert the token's row quantized (fmt's
+ * activation quantizer), keep-quant gate/up + SiLU-mul, the bf16 act row
+ * quantized again, keep-quant down with the routing weight; the shared
+ * expert stays bf16; then the combine (or the combine-gate).  The quantizer
+ * works on blocks inside one row, so a row's result does not depend on the
+ * batch it is computed in. */
+int oracle_moe_layer_tokens_q(const uint16_t* x, const uint16_t* w_router,
+                              const float* logit_bias, const uint8_t* w13q, const uint8_t* w2q,
+                              int fmt, const uint16_t* w_shared_gate, const uint16_t* w13_shared,
+                              const uint16_t* w2_shared, int H, int I, int E, int K, int I_shared,
+                              float routed_scale, const int32_t* tokens, int n_tokens,
+                              int32_t* ids_out, float* w_out, uint16_t* out) {
+  if (H <= 0 || I <= 0 || E <= 0 || K < 1 || K > E || K > 32 || n_tokens < 0) return ORA_ERR_ARG;
+  const int blk = q_block(fmt);
+  if (!blk || H % blk || I % blk) return ORA_ERR_ARG;
+  const int has_shared = (w_shared_gate && w13_shared && w2_shared && I_shared > 0);
+  const int64_t rb13 = (int64_t)(H / blk) * q_block_bytes(fmt);
+  const int64_t rb2 = (int64_t)(I / blk) * q_block_bytes(fmt);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n_tokens; ++i) {
+    const uint16_t* xt = x + (int64_t)tokens[i] * H;
+    int32_t ids[32];
+    float wts[32];
+    float gl = 0.0f;
+    oracle_route_topk(xt, w_router, logit_bias, has_shared ? w_shared_gate : NULL, NULL, 1, H, E,
+                      K, 1, 0, 1, ids, wts, NULL, has_shared ? &gl : NULL);
+    int8_t* xq = (int8_t*)malloc((size_t)H);
+    float* xd = (float*)malloc(sizeof(float) * (size_t)(H / blk));
+    int8_t* aq = (int8_t*)malloc((size_t)I);
+    float* adv = (float*)malloc(sizeof(float) * (size_t)(I / blk));
+    uint16_t* act = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(I > I_shared ? I : I_shared));
+    uint16_t* eo = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)K * H);
+    oracle_quantize_act_q8(xt, 1, H, fmt, xq, xd);
+    for (int j = 0; j < K; ++j) {
+      gateup_q_row(xq, xd, w13q + (int64_t)ids[j] * 2 * I * rb13, fmt, H, I, act);
+      oracle_quantize_act_q8(act, 1, I, fmt, aq, adv);
+      down_q_row(aq, adv, w2q + (int64_t)ids[j] * H * rb2, fmt, I, H, &wts[j],
+                 eo + (int64_t)j * H);
+    }
+    uint16_t* o = out + (int64_t)i * H;
+    if (has_shared) {
+      uint16_t* sd = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+      gateup_row(xt, w13_shared, H, I_shared, act, 1);
+      down_row(act, w2_shared, I_shared, H, NULL, sd);
+      oracle_combine_gate(eo, ORA_BF16, NULL, sd, ORA_BF16, &gl, routed_scale, 1, K, H, o,
+                          ORA_BF16);
+      free(sd);
+    } else {
+      oracle_combine(eo, ORA_BF16, NULL, NULL, ORA_BF16, routed_scale, 1, K, H, o, ORA_BF16);
+    }
+    if (ids_out) memcpy(ids_out + (int64_t)i * K, ids, sizeof(int32_t) * (size_t)K);
+    if (w_out) memcpy(w_out + (int64_t)i * K, wts, sizeof(float) * (size_t)K);
+    free(xq);
+    free(xd);
+    free(aq);
+    free(adv);
     free(act);
     free(eo);
   }
