@@ -35,13 +35,19 @@ METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM TFLOP/s and combine GB/s v
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, weights="bf16"):
     """DRAM traffic of one gate/up GEMM launch on `workload` from the committed
     ncu summary, or None when it covers another workload or the kernel
     sources have changed since it was captured."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "gemm_gateup_traffic.txt")
+    if weights == "bf16":
+        name, srcs = "gemm_gateup_traffic.txt", ("moe_gemm.cu", "sm100_ptx.cuh")
+    elif weights in Q_WEIGHTS:
+        name, srcs = f"qgemm_gateup_{weights}_traffic.txt", ("moe_qgemm.cu", "sm100_ptx.cuh")
+    else:
+        return None
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     kv = {}
@@ -50,12 +56,16 @@ def recorded_traffic(workload):
             k, v = ln.strip().split("=", 1)
             kv[k] = v
     h = hashlib.sha256()
-    for f in ("moe_gemm.cu", "sm100_ptx.cuh"):
+    for f in srcs:
         with open(os.path.join(ROOT, "mixture_experts_ffn_renorm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     if kv.get("sources_sha256") != h.hexdigest() or kv.get("workload") != workload:
         return None
     return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
+
+
+# keep-quant weight formats: name -> (oracle format id, weights per block, bytes per block)
+Q_WEIGHTS = {"q8_0": (1, 32, 34), "q4_k": (2, 256, 144)}
 
 
 def peaks():
@@ -304,16 +314,26 @@ def combine_arms(dev, iters=20):
     return out
 
 
+def layer_oracle(O, cfg, d, tokens):
+    """The oracle's whole block on `tokens`: keep-quant experts when `d` holds
+    GGUF blocks (w13q / w2q, format d["qfmt"]), bf16 experts otherwise."""
+    if "w13q" in d:
+        return O.moe_layer_tokens_q(d["x"], d["w_router"], d["logit_bias"], d["w13q"], d["w2q"],
+                                    Q_WEIGHTS[d["qfmt"]][0], d["w_shared_gate"], d["w13_shared"],
+                                    d["w2_shared"], H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K,
+                                    I_shared=cfg.I_shared, tokens=tokens)
+    return O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
+                              d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H,
+                              I=cfg.I, E=cfg.E, K=cfg.K, I_shared=cfg.I_shared, tokens=tokens)
+
+
 def oracle_tokens_per_s(cfg, d, seconds=10.0):
     """Time the CPU oracle on a bounded sample of the workload's tokens."""
     import oracle as O
 
     def run(tokens):
         t0 = time.perf_counter()
-        O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
-                           d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H, I=cfg.I,
-                           E=cfg.E, K=cfg.K, I_shared=cfg.I_shared,
-                           tokens=np.asarray(tokens, np.int32))
+        layer_oracle(O, cfg, d, np.asarray(tokens, np.int32))
         return time.perf_counter() - t0
 
     cores = O.max_threads()
@@ -333,10 +353,14 @@ def run_reference(args):
     from oracle import build as ob
 
     ob.build()
-    d = W.layer_inputs(cfg)
+    weights = getattr(args, "weights", "bf16")
+    d = W.layer_inputs(cfg, with_weights=weights not in Q_WEIGHTS)
     import oracle as O
 
-    if getattr(args, "weights", "bf16") == "fp8":  # the layer on the dequantised FP8 weights
+    if weights in Q_WEIGHTS:  # the keep-quant layer on the same GGUF blocks
+        d.update(W.layer_q_weights(cfg, weights))
+        d["qfmt"] = weights
+    if weights == "fp8":  # the layer on the dequantised FP8 weights
         for key, R, C in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
             q, sc = W.quantize_fp8_block(d[key])
             d[key] = O.dequant_fp8_block(q, sc, G=cfg.E, R=R, C=C)
@@ -344,14 +368,10 @@ def run_reference(args):
     n = max(cores, 8) if cfg.T >= 64 else cfg.T
     tokens = np.arange(n, dtype=np.int32)
     for _ in range(args.warmup if args.warmup < 2 else 1):
-        O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
-                           d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H, I=cfg.I,
-                           E=cfg.E, K=cfg.K, I_shared=cfg.I_shared, tokens=tokens)
+        layer_oracle(O, cfg, d, tokens)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        O.moe_layer_tokens(d["x"], d["w_router"], d["logit_bias"], d["w13"], d["w2"],
-                           d["w_shared_gate"], d["w13_shared"], d["w2_shared"], H=cfg.H, I=cfg.I,
-                           E=cfg.E, K=cfg.K, I_shared=cfg.I_shared, tokens=tokens)
+        layer_oracle(O, cfg, d, tokens)
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
     line = {
@@ -359,7 +379,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_dict(cfg, 1), weights=getattr(args, "weights", "bf16")),
+        "config": dict(config_dict(cfg, 1), weights=weights),
         "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "tokens/s",
                          "sample": f"{n} of {cfg.T} tokens per step, full block per token"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -412,7 +432,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = layer_config(args.config)
-    d = W.layer_inputs(cfg)
+    qw = args.weights if args.weights in Q_WEIGHTS else None
+    d = W.layer_inputs(cfg, with_weights=qw is None)
+    if qw:
+        d.update(W.layer_q_weights(cfg, qw))
+        d["qfmt"] = qw
     if rank > 0:  # each replica gets its own tokens of the global batch
         d["x"] = W.rank_tokens(cfg, rank)
     fp8 = args.weights == "fp8"
@@ -420,7 +444,7 @@ def run_ours(args):
         d["w13_e4m3"], d["w13_scale"] = W.quantize_fp8_block(d["w13"])
         d["w2_e4m3"], d["w2_scale"] = W.quantize_fp8_block(d["w2"])
     blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
-                   I_shared=cfg.I_shared, fp8_weights=fp8)
+                   I_shared=cfg.I_shared, fp8_weights=fp8, qweights=qw)
     x_host = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     x_dev = x_host.to(dev)
     out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
@@ -507,12 +531,19 @@ def run_ours(args):
     flop_down = 2.0 * P * cfg.I * cfg.H
     wb = 1 if fp8 else 2          # bytes per expert weight (FP8 adds one f32 per 128x128 block)
     sc = 4.0 / (128 * 128) if fp8 else 0.0
-    bytes_gateup = touched * 2 * cfg.I * cfg.H * (wb + sc) + P * cfg.H * 2 + P * cfg.I * 2
-    bytes_down = touched * cfg.H * cfg.I * (wb + sc) + P * cfg.I * 2 + P * cfg.H * 2 + P * 4
+    a_in = 2.0                    # bytes per activation element read by a GEMM
+    if qw:                        # GGUF blocks; 8-bit activation codes plus one f32 per block
+        _, qblk, qbytes = Q_WEIGHTS[qw]
+        wb, sc, a_in = qbytes / qblk, 0.0, 1.0 + 4.0 / qblk
+    bytes_gateup = touched * 2 * cfg.I * cfg.H * (wb + sc) + P * cfg.H * a_in + P * cfg.I * 2
+    bytes_down = touched * cfg.H * cfg.I * (wb + sc) + P * cfg.I * a_in + P * cfg.H * 2 + P * 4
     t_gu = stage_avg["gemm_gateup"] / 1000.0
     t_dn = stage_avg["gemm_down"] / 1000.0
-    tensor_bound = flop_gateup / (pk["bf16_tflops"] * 1e12) >= bytes_gateup / (pk["hbm_gbs"] * 1e9)
+    # the keep-quant kernels run on the CUDA cores and are reported against HBM
+    tensor_bound = (not qw and flop_gateup / (pk["bf16_tflops"] * 1e12)
+                    >= bytes_gateup / (pk["hbm_gbs"] * 1e9))
     kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
+             f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qw else
              "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)")
     if tensor_bound:
         achieved = flop_gateup / t_gu / 1e12
@@ -520,7 +551,7 @@ def run_ours(args):
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / pk["bf16_tflops"],
                     "peak_source": f"{pk_src} bf16 dense (burst)",
-                    "traffic": None if fp8 else recorded_traffic(cfg.name),
+                    "traffic": recorded_traffic(cfg.name, args.weights),
                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "algorithmic_flop_per_launch": flop_gateup}
     else:
@@ -528,7 +559,7 @@ def run_ours(args):
         roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                     "peak_source": f"{pk_src} HBM copy bandwidth",
-                    "traffic": None if fp8 else recorded_traffic(cfg.name),
+                    "traffic": recorded_traffic(cfg.name, args.weights),
                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "algorithmic_bytes_per_launch": bytes_gateup,
                     "touched_experts": touched}
@@ -576,12 +607,15 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8" if qw else "bf16",
             "data": "synthetic (seeded normal inputs and weights, "
                     + (f"Zipf({cfg.zipf_s})-skewed router bias" if cfg.zipf_s
                        else "unbiased router")
                     + ("; routed expert weights FP8 E4M3 with 128x128 block scales, "
-                       "quantised from the same bf16 weights)" if fp8 else ")"),
+                       "quantised from the same bf16 weights)" if fp8 else
+                       f"; routed expert weights random valid GGUF {qw.upper()} blocks, "
+                       "activations quantized to 8-bit blocks on the device)" if qw else ")"),
             "config": dict(config_dict(cfg, ws), weights=args.weights),
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": int(cfg.T * cfg.H * 2),
@@ -609,8 +643,9 @@ def main():
     ap.add_argument("--config", default="prefill",
                     choices=["prefill", "decode", "large", "tiny", "combine"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
-                    help="routed expert weights: bf16, or FP8 E4M3 with 128x128 block scales")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8", "q8_0", "q4_k"],
+                    help="routed expert weights: bf16, FP8 E4M3 with 128x128 block scales, or "
+                         "keep-quant GGUF Q8_0 / Q4_K blocks")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -9,6 +9,8 @@
  *   moe_combine                        weighted top-k sum (+ optional shared term)
  *   moe_combine_gate                   combine with the shared-expert sigmoid gate
  *   shared_expert_gate                 out = sigmoid(gl) * sd
+ *   moe_quantize_act_q8, moe_grouped_gemm_q, moe_grouped_gemm_gateup_silu_q,
+ *   moe_grouped_gemm_down_q            keep-quant expert GEMMs (Q8_0 / Q4_K weights)
  *
  * Sources (vllm.cpp pages):
  *   [I3094]  issue #3094 "Row: BACKEND-ROCM-BF16-MOE": names the two grouped
@@ -24,7 +26,8 @@
  *            term), "Honest gaps" (the covered router is ungrouped softmax).
  *   [PR523]  PR #509's stacked follow-up #523, "What changed": the expert GEMM
  *            is grouped over expert ids; activation scratch is capture-safe
- *            and never reallocated during reuse.
+ *            and never reallocated during reuse; the keep-quant expert GEMMs
+ *            run on GGUF weight blocks with 8-bit activation quantizers.
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
@@ -73,7 +76,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 7 */
+int moe_abi_version(void);  /* 8 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -301,7 +304,7 @@ int moe_grouped_gemm_down_bf16_shared(const void* act_bf16, const void* w2_bf16,
  * scale per 128 x 128 block of its own rows and columns.  The GEMM uses
  *   w = bf16( f32(code) * scale )      (one f32 multiply, one RNE rounding)
  * and is then exactly the bf16 call above (same narrowing, weight, scatter,
- * tolerance); activations stay bf16.  Four converter warps per CTA turn the
+ * tolerance); activations stay bf16.  Eight converter warps per CTA turn the
  * codes into bf16 tiles in shared memory between the TMA loads and the MMA,
  * so the weights cross HBM at one byte each.
  *   w13_e4m3  uint8 [G, 2I, H] (gate rows first), w13_scale f32 [G, ceil(2I/128), ceil(H/128)]
@@ -353,6 +356,81 @@ int moe_set_gemm_pairing(int mode);
  * Process-wide, takes effect at the next launch; returns the previous
  * setting (MOE_ERR_ARG unless enable is 0 or 1). */
 int moe_set_pdl(int enable);
+
+/* ------------------------------------------------------------------------
+ * Keep-quant expert GEMMs -- kMatmulBTQuant / kMatmulBTQuantGrouped of
+ * [PR523] ("What changed"): the expert matmul reads the weights as the GGUF
+ * blocks they are stored in, grouped over the expert ids; activations are
+ * quantized to 8-bit blocks and each block's dot product is an exact integer
+ * sum ([PR523] "Evidence" checks the op at NMSE <= 5e-4 against a CPU
+ * keep-quant reference).  CUDA-core dp4a kernels: built for decode-class
+ * layers, where the weight bytes dominate.
+ *
+ * Weight formats (qfmt), little-endian blocks along each weight row:
+ *   MOE_QFMT_Q8_0  32 weights in 34 bytes: fp16 d, int8 q[32];  w = d * q
+ *   MOE_QFMT_Q4_K  256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes of
+ *                  packed 6-bit scales sc_j and mins m_j, 128 bytes of 4-bit
+ *                  codes; sub-block j (32 weights): w = d*sc_j*q - dmin*m_j
+ * A weight matrix [G, R, K] is stored as uint8 [G, R, K / block * bytes].
+ *
+ * moe_quantize_act_q8 -- the activation quantizer: for every block of 32
+ * (qfmt Q8_0: Q8_0 activations) or 256 (qfmt Q4_K: Q8_K activations) values
+ * of a bf16 row,
+ *   amax = max |x| (NaN skipped),  d = amax / 127,  id = d != 0 ? 1 / d : 0,
+ *   q = round-half-away-from-zero(x * id), NaN -> 0, clamped to [-127, 127]
+ * each a single binary32 operation; the stored scale is d rounded to fp16
+ * (Q8_0) or d itself (Q8_K).  Bit-exact.
+ *   x       bf16 [R, K], 16-byte aligned; K a multiple of the block
+ *   codes   int8 [R, K] out, 16-byte aligned
+ *   scales  f32 [R, K / block] out, 4-byte aligned
+ *
+ * moe_grouped_gemm_q -- the plain grouped op: for every group g and row r in
+ * [group_offsets[g], group_offsets[g+1]):
+ *   out[r, n] = sum over the blocks b of the row of
+ *     Q8_0: d_w[b] * d_x[b] * sum_i q_w[i] * q_x[i]
+ *     Q4_K: d_x[b] * (d * sum_j sc_j * sum_i q_ij * q_x,ij  -  dmin * sum_j m_j * sum_i q_x,ij)
+ * with exact integer block sums and f32 accumulation over the blocks.
+ *   a_codes, a_scales  quantized activations ([a_rows, K], [a_rows, K/block]),
+ *                      from moe_quantize_act_q8 with the same qfmt
+ *   a_row_gather       int32 [P] or NULL: row r reads activation row
+ *                      a_row_gather[r] / gather_div (an index outside
+ *                      [0, a_rows) reads zeros); NULL: row r reads row r
+ *   w                  uint8 [G, N, K / block * bytes], 16-byte aligned
+ *   group_offsets      int32 [G+1], read on the device, values clamped to [0, P];
+ *                      NULL allowed when G == 1
+ *   out                f32 [P, N]; rows outside every group are not written
+ *   P >= 0, N >= 1, K a multiple of 256 and at most 16384, 1 <= G <= 1024
+ *
+ * moe_grouped_gemm_gateup_silu_q -- the keep-quant gate/up: the sums above for
+ * gate rows n and up rows I + n of w13 [G, 2I, H / block * bytes], then the
+ * epilogue of moe_grouped_gemm_gateup_silu_bf16 (both narrowed to bf16 before
+ * silu(g) * u), act bf16 [P, I].  Same row gather as above.
+ *
+ * moe_grouped_gemm_down_q -- the keep-quant down projection: the sums above
+ * with w2 [G, H, I / block * bytes] and activations [P, I] in row order, then
+ * the epilogue of moe_grouped_gemm_down_bf16: one f32 multiply by
+ * pair_weight[dst] (when given), one bf16 rounding, stored at row dst =
+ * row_to_pair ? row_to_pair[r] : r of out bf16 [P, H] (a dst outside [0, P) is
+ * skipped).
+ *
+ * Errors: MOE_ERR_ARG (qfmt, sizes, NULL operands), MOE_ERR_ALIGN (alignment,
+ * K not a multiple of 256 or above 16384), MOE_ERR_CUDA.  No workspace.
+ * ---------------------------------------------------------------------- */
+enum { MOE_QFMT_Q8_0 = 1, MOE_QFMT_Q4_K = 2 };
+int moe_quantize_act_q8(const void* x_bf16, int R, int K, int qfmt, int8_t* codes, float* scales,
+                        void* stream);
+int moe_grouped_gemm_q(const int8_t* a_codes, const float* a_scales, int a_rows,
+                       const int32_t* a_row_gather, int gather_div, const uint8_t* w, int qfmt,
+                       const int32_t* group_offsets, int P, int K, int N, int G, float* out_f32,
+                       void* stream);
+int moe_grouped_gemm_gateup_silu_q(const int8_t* a_codes, const float* a_scales, int a_rows,
+                                   const int32_t* a_row_gather, int gather_div,
+                                   const uint8_t* w13, int qfmt, const int32_t* group_offsets,
+                                   int P, int H, int I, int G, void* act_bf16, void* stream);
+int moe_grouped_gemm_down_q(const int8_t* a_codes, const float* a_scales, const uint8_t* w2,
+                            int qfmt, const int32_t* group_offsets, const float* pair_weight,
+                            const int32_t* row_to_pair, int P, int I, int H, int G,
+                            void* out_bf16, void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_combine -- kMoeCombine of [PR509].  Per output element, sequentially:
@@ -429,7 +507,11 @@ enum {
   MOE_KID_SHARED_GATE = 10,
   MOE_KID_GATE_SIGMOID = 11,  /* the sigmoid pre-pass of the gate ops (workspace given) */
   MOE_KID_PERMUTE_SMALL = 12, /* count + scan + place in one block (P <= 4096) */
-  MOE_KID_COUNT = 16
+  MOE_KID_QUANT_ACT = 13,     /* moe_quantize_act_q8 */
+  MOE_KID_GEMM_Q = 14,        /* moe_grouped_gemm_q */
+  MOE_KID_GEMM_Q_GATEUP = 15, /* moe_grouped_gemm_gateup_silu_q */
+  MOE_KID_GEMM_Q_DOWN = 16,   /* moe_grouped_gemm_down_q */
+  MOE_KID_COUNT = 20
 };
 int moe_device_status(int* status_out, int clear);
 int moe_launch_counts(unsigned long long* counts, int n);

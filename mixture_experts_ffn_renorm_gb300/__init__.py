@@ -25,8 +25,10 @@ KID = {
     "route_logits": 0, "route_topk": 1, "permute_count": 2, "permute_scan": 3,
     "permute_place": 4, "permute_gather": 5, "gemm_gateup": 6, "gemm_down": 7, "combine": 8,
     "combine_gate": 9, "shared_gate": 10, "gate_sigmoid": 11, "permute_small": 12,
+    "quant_act": 13, "gemm_q": 14, "gemm_q_gateup": 15, "gemm_q_down": 16,
 }
-KID_COUNT = 16
+KID_COUNT = 20
+QFMT_Q8_0, QFMT_Q4_K = 1, 2
 
 EXPORTS = (
     "moe_last_error", "moe_abi_version", "moe_route_topk", "moe_route_topk_workspace_size",
@@ -37,6 +39,8 @@ EXPORTS = (
     "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl",
     "moe_grouped_gemm_gateup_silu_bf16_shared", "moe_grouped_gemm_down_bf16_shared",
     "moe_route_topk_ex", "moe_grouped_gemm_gateup_silu_fp8w", "moe_grouped_gemm_down_fp8w",
+    "moe_quantize_act_q8", "moe_grouped_gemm_q", "moe_grouped_gemm_gateup_silu_q",
+    "moe_grouped_gemm_down_q",
 )
 
 
@@ -75,6 +79,11 @@ _SIGS = {
                                                   _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_down_bf16_shared": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P,
                                            _I, _P, _P, _SZ, _P], _I),
+    "moe_quantize_act_q8": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_grouped_gemm_q": ([_P, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P], _I),
+    "moe_grouped_gemm_gateup_silu_q": ([_P, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P],
+                                       _I),
+    "moe_grouped_gemm_down_q": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "moe_set_gemm_pairing": ([_I], _I),
     "moe_set_pdl": ([_I], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
@@ -243,6 +252,42 @@ def moe_grouped_gemm_down_fp8w(act, w2_e4m3, w2_scale, group_offsets, pair_weigh
                                           _ptr(group_offsets), _ptr(pair_weight),
                                           _ptr(row_to_pair), P, I, H, G, _ptr(out),
                                           _ptr(workspace), ws_bytes, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_quantize_act_q8(x, R, K, qfmt, codes, scales, stream=None, check=True):
+    """8-bit activation blocks of bf16 rows (Q8_0 for qfmt Q8_0, Q8_K for Q4_K; see moe.h)."""
+    rc = lib().moe_quantize_act_q8(_ptr(x), R, K, qfmt, _ptr(codes), _ptr(scales),
+                                   _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_q(a_codes, a_scales, a_rows, a_row_gather, gather_div, w, qfmt,
+                       group_offsets, P, K, N, G, out, stream=None, check=True):
+    """Plain grouped keep-quant matmul, f32 out (see moe.h)."""
+    rc = lib().moe_grouped_gemm_q(_ptr(a_codes), _ptr(a_scales), a_rows, _ptr(a_row_gather),
+                                  gather_div, _ptr(w), qfmt, _ptr(group_offsets), P, K, N, G,
+                                  _ptr(out), _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_gateup_silu_q(a_codes, a_scales, a_rows, a_row_gather, gather_div, w13,
+                                   qfmt, group_offsets, P, H, I, G, act, stream=None,
+                                   check=True):
+    """Keep-quant gate/up GEMM + SiLU-mul (see moe.h)."""
+    rc = lib().moe_grouped_gemm_gateup_silu_q(_ptr(a_codes), _ptr(a_scales), a_rows,
+                                              _ptr(a_row_gather), gather_div, _ptr(w13), qfmt,
+                                              _ptr(group_offsets), P, H, I, G, _ptr(act),
+                                              _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_grouped_gemm_down_q(a_codes, a_scales, w2, qfmt, group_offsets, pair_weight,
+                            row_to_pair, P, I, H, G, out, stream=None, check=True):
+    """Keep-quant down GEMM with the routing weight and the scatter (see moe.h)."""
+    rc = lib().moe_grouped_gemm_down_q(_ptr(a_codes), _ptr(a_scales), _ptr(w2), qfmt,
+                                       _ptr(group_offsets), _ptr(pair_weight), _ptr(row_to_pair),
+                                       P, I, H, G, _ptr(out), _stream(stream))
     return _check(rc) if check else rc
 
 

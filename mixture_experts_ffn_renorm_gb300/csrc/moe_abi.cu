@@ -87,7 +87,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_msg; }
 
-int moe_abi_version(void) { return 7; }
+int moe_abi_version(void) { return 8; }
 
 int moe_set_pdl(int enable) {
   moe::clear_error();

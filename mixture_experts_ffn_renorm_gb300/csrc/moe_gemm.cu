@@ -140,7 +140,7 @@ struct Smem {
 //           stage then holds 4 KB of A instead of 16, so the same shared memory
 //           keeps about twice as many weight bytes in flight.
 //   kFp8B   B holds FP8 E4M3 weight codes with block scales: TMA brings A and the
-//           codes into the stage ring, four converter warps write the scaled
+//           codes into the stage ring, eight converter warps write the scaled
 //           bf16 B tiles into a second ring, and the MMA reads A and that
 template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false, int kARows = BM,
           bool kFp8B = false>

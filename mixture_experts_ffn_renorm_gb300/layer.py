@@ -13,12 +13,16 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, moe_combine, moe_combine_gate, moe_gate_workspace_size,
-               moe_grouped_gemm_down_bf16, moe_grouped_gemm_down_bf16_shared,
-               moe_grouped_gemm_down_fp8w, moe_grouped_gemm_gateup_silu_bf16,
+from . import (BF16, QFMT_Q4_K, QFMT_Q8_0, moe_combine, moe_combine_gate,
+               moe_gate_workspace_size, moe_grouped_gemm_down_bf16,
+               moe_grouped_gemm_down_bf16_shared, moe_grouped_gemm_down_fp8w,
+               moe_grouped_gemm_down_q, moe_grouped_gemm_gateup_silu_bf16,
                moe_grouped_gemm_gateup_silu_bf16_shared, moe_grouped_gemm_gateup_silu_fp8w,
-               moe_permute, moe_permute_workspace_size, moe_route_topk,
-               moe_route_topk_workspace_size)
+               moe_grouped_gemm_gateup_silu_q, moe_permute, moe_permute_workspace_size,
+               moe_quantize_act_q8, moe_route_topk, moe_route_topk_workspace_size)
+
+# keep-quant weight formats: name -> (library format id, weights per activation block)
+Q_WEIGHTS = {"q8_0": (QFMT_Q8_0, 32), "q4_k": (QFMT_Q4_K, 256)}
 
 
 def _dev_bf16(a, device):
@@ -41,11 +45,24 @@ class MoeBlock:
     ``w13_e4m3`` / ``w13_scale`` and ``w2_e4m3`` / ``w2_scale`` (codes uint8 of
     the same shapes, f32 scales per 128 x 128 block); the shared expert stays
     bf16 and runs in launches of its own.
+    qweights="q8_0" | "q4_k": keep-quant routed experts, ``w13q`` [E, 2I, H/blk*bytes]
+    and ``w2q`` [E, H, I/blk*bytes] GGUF blocks (uint8).  The token rows and the
+    act rows are quantized to 8-bit blocks on the device, the gate/up GEMM reads
+    the token rows through sorted_pair / K (no x_perm), and the shared expert
+    stays bf16 in launches of its own.
     """
 
     def __init__(self, H, I, E, K, weights, max_tokens, device="cuda", I_shared=0,
-                 routed_scale=1.0, gather=False, fuse_shared=True, fp8_weights=False):
+                 routed_scale=1.0, gather=False, fuse_shared=True, fp8_weights=False,
+                 qweights=None):
         self.H, self.I, self.E, self.K, self.Is = H, I, E, K, I_shared
+        if qweights is not None:
+            if qweights not in Q_WEIGHTS:
+                raise ValueError(f"qweights must be one of {sorted(Q_WEIGHTS)}")
+            if fp8_weights:
+                raise ValueError("qweights and fp8_weights exclude each other")
+            gather = True
+        self.qfmt, qblk = Q_WEIGHTS[qweights] if qweights is not None else (0, 0)
         self.max_tokens = max_tokens
         # gather=True: the gate/up GEMM reads each routed row straight from x
         # (through sorted_pair / K); False: permute materialises x_perm and the
@@ -54,7 +71,7 @@ class MoeBlock:
         # fuse_shared: the shared expert's GEMMs run inside the routed GEMM
         # launches (one launch each for gate/up and down); False: own launches
         self.fp8 = fp8_weights
-        self.fuse_shared = fuse_shared and not gather and not fp8_weights
+        self.fuse_shared = fuse_shared and not gather and not fp8_weights and not self.qfmt
         if fp8_weights and gather:
             raise ValueError("FP8 expert weights read x_perm rows (gather=False)")
         self.routed_scale = float(routed_scale)
@@ -68,6 +85,10 @@ class MoeBlock:
             self.w13_s = dev(weights["w13_scale"], torch.float32)
             self.w2_q = dev(weights["w2_e4m3"], torch.uint8)
             self.w2_s = dev(weights["w2_scale"], torch.float32)
+            self.w13 = self.w2 = None
+        elif self.qfmt:
+            self.w13_q = torch.as_tensor(weights["w13q"], dtype=torch.uint8).to(dv).contiguous()
+            self.w2_q = torch.as_tensor(weights["w2q"], dtype=torch.uint8).to(dv).contiguous()
             self.w13 = self.w2 = None
         else:
             self.w13 = _dev_bf16(weights["w13"], dv)
@@ -89,6 +110,12 @@ class MoeBlock:
         self.pair_to_row = torch.empty((P,), dtype=i32, device=dv)
         self.x_perm = None if gather else torch.empty((P, H), dtype=bf, device=dv)
         self.act = torch.empty((P, I), dtype=bf, device=dv)
+        if self.qfmt:
+            # 8-bit activation blocks of the token rows and of the act rows
+            self.x_q = torch.empty((T, H), dtype=torch.int8, device=dv)
+            self.x_s = torch.empty((T, H // qblk), dtype=f32, device=dv)
+            self.act_q = torch.empty((P, I), dtype=torch.int8, device=dv)
+            self.act_s = torch.empty((P, I // qblk), dtype=f32, device=dv)
         self.expert_out = torch.empty((P, H), dtype=bf, device=dv)
         self.out = torch.empty((T, H), dtype=bf, device=dv)
         if self.has_shared:
@@ -132,7 +159,13 @@ class MoeBlock:
                     self.pair_to_row, self.x_perm, ws, ws.numel(), stream)
         mark("permute")
         fused = self.has_shared and self.fuse_shared
-        if self.fp8:
+        if self.qfmt:
+            moe_quantize_act_q8(x, T, H, self.qfmt, self.x_q, self.x_s, stream)
+            mark("quant_x")
+            moe_grouped_gemm_gateup_silu_q(self.x_q, self.x_s, T, self.sorted_pair, K, self.w13_q,
+                                           self.qfmt, self.expert_offsets, P, H, I, E, self.act,
+                                           stream)
+        elif self.fp8:
             moe_grouped_gemm_gateup_silu_fp8w(self.x_perm, self.w13_q, self.w13_s,
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,
                                               stream)
@@ -149,7 +182,13 @@ class MoeBlock:
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,
                                               stream)
         mark("gemm_gateup")
-        if self.fp8:
+        if self.qfmt:
+            moe_quantize_act_q8(self.act, P, I, self.qfmt, self.act_q, self.act_s, stream)
+            mark("quant_act")
+            moe_grouped_gemm_down_q(self.act_q, self.act_s, self.w2_q, self.qfmt,
+                                    self.expert_offsets, self.topk_w, self.sorted_pair, P, I, H, E,
+                                    self.expert_out, stream)
+        elif self.fp8:
             moe_grouped_gemm_down_fp8w(self.act, self.w2_q, self.w2_s, self.expert_offsets,
                                        self.topk_w, self.sorted_pair, P, I, H, E, self.expert_out,
                                        None, 0, stream)
@@ -188,6 +227,8 @@ class MoeBlock:
             n += 1  # the combine-gate's sigmoid pass
         if self.has_shared and not self.fuse_shared:
             n += 2
+        if self.qfmt:
+            n += 2  # the two activation quantizers
         return n
 
     def capture(self, x_static):

@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_refusals_without_gpu(lib):
-    assert m.abi_version() == 7
+    assert m.abi_version() == 8
     # dtype refusals name the missing arm and return before touching the device
     rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
     assert rc == m.ERR_DTYPE and "f16" in m.last_error()
@@ -119,3 +119,35 @@ def test_newer_entry_points_refuse_without_touching_the_device(lib):
                                                None, 4, 64, 64, 1, ctypes.c_void_p(addr), None, Z,
                                                None)
     assert rc == m.ERR_ARG and "scales" in m.last_error()
+
+
+def test_keep_quant_entry_points_refuse_without_touching_the_device(lib):
+    # the keep-quant quantizer and GEMMs check format, sizes and alignment first
+    import ctypes
+    buf = (ctypes.c_uint8 * 4096)()
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    assert lib.moe_quantize_act_q8(a, 2, 64, 3, a, a, None) == m.ERR_ARG
+    assert "qfmt" in m.last_error()
+    assert lib.moe_quantize_act_q8(a, 2, 48, m.QFMT_Q8_0, a, a, None) == m.ERR_ALIGN
+    assert lib.moe_quantize_act_q8(a, 2, 64, m.QFMT_Q4_K, a, a, None) == m.ERR_ALIGN
+    assert lib.moe_quantize_act_q8(None, 0, 256, m.QFMT_Q4_K, None, None, None) == m.OK
+    # K not a multiple of 256, G out of range, NULL offsets with G > 1
+    rc = lib.moe_grouped_gemm_q(a, a, 4, None, 1, a, m.QFMT_Q8_0, None, 4, 96, 8, 1, a, None)
+    assert rc == m.ERR_ALIGN and "256" in m.last_error()
+    rc = lib.moe_grouped_gemm_q(a, a, 4, None, 1, a, m.QFMT_Q4_K, None, 4, 256, 8, 2, a, None)
+    assert rc == m.ERR_ARG and "group_offsets" in m.last_error()
+    rc = lib.moe_grouped_gemm_gateup_silu_q(a, a, 4, a, 0, a, m.QFMT_Q4_K, None, 4, 256, 8, 1, a,
+                                            None)
+    assert rc == m.ERR_ARG and "gather_div" in m.last_error()
+    rc = lib.moe_grouped_gemm_down_q(a, a, a, 0, None, None, None, 4, 256, 8, 1, a, None)
+    assert rc == m.ERR_ARG
+    rc = lib.moe_grouped_gemm_down_q(a, a, a, m.QFMT_Q8_0, None, None, None, 4, 256, 8, 1025, a,
+                                     None)
+    assert rc == m.ERR_ARG
+    # weights not 16-byte aligned
+    b = ctypes.c_void_p(a.value + 4)
+    rc = lib.moe_grouped_gemm_down_q(a, a, b, m.QFMT_Q8_0, None, None, None, 4, 256, 8, 1, a, None)
+    assert rc == m.ERR_ALIGN
+    # P = 0 is a no-op
+    assert lib.moe_grouped_gemm_q(None, None, 0, None, 1, None, m.QFMT_Q8_0, None, 0, 256, 8, 1,
+                                  None, None) == m.OK

@@ -300,3 +300,44 @@ def test_fp8_expert_weights_layer_against_the_oracle(cfg):
     rms = float(np.sqrt(np.mean(r * r)))
     worst = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), rms)))
     assert nmse <= GEMM_NMSE and worst <= GEMM_MAXREL, (nmse, worst)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("cfg", [W.DECODE, W.LayerConfig("q_T300_H512_I256_E16_K4_Is256",
+                                                           T=300, H=512, I=256, E=16, K=4,
+                                                           I_shared=256, zipf_s=1.1)],
+                         ids=lambda c: c.name)
+def test_keep_quant_layer_against_the_oracle(cfg, fmt):
+    # routed experts with keep-quant GGUF weights (both activation quantizers on
+    # the device, the gate/up GEMM gathering token rows through sorted_pair / K):
+    # the whole block against the oracle's keep-quant layer on sampled tokens,
+    # plus the quantized token rows bit for bit
+    d = W.layer_inputs(cfg, with_weights=False)
+    d.update(W.layer_q_weights(cfg, fmt))
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                   I_shared=cfg.I_shared, qweights=fmt)
+    before = launches()
+    out = to_host(blk.forward(to_dev(d["x"])))
+    assert launched_since(before, "quant_act") == 2
+    assert launched_since(before, "gemm_q_gateup") == 1
+    assert launched_since(before, "gemm_q_down") == 1
+    assert launched_since(before, "gemm_gateup") == (1 if cfg.I_shared else 0)
+    fo = O.Q8_0 if fmt == "q8_0" else O.Q4_K
+    xq, xd = O.quantize_act_q8(d["x"], fo, R=cfg.T, K=cfg.H)
+    assert np.array_equal(to_host(blk.x_q), xq)
+    assert np.array_equal(to_host(blk.x_s).view(np.uint32), xd.view(np.uint32))
+    toks = np.unique(np.concatenate([[0, cfg.T - 1],
+                                     np.random.default_rng(4).choice(cfg.T, min(cfg.T, 24),
+                                                                      replace=False)]))
+    want, ora_ids, _ = O.moe_layer_tokens_q(d["x"], d["w_router"], d["logit_bias"], d["w13q"],
+                                            d["w2q"], fo, d["w_shared_gate"], d["w13_shared"],
+                                            d["w2_shared"], H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K,
+                                            I_shared=cfg.I_shared, tokens=toks)
+    ids = to_host(blk.topk_ids)
+    same = np.all(np.sort(ora_ids, 1) == np.sort(ids[toks], 1), axis=1)
+    assert same.mean() >= 0.95
+    g, r = bf16_to_f64(out[toks][same]), bf16_to_f64(want[same])
+    nmse, _ = nmse_maxrel(g, r)
+    rms = float(np.sqrt(np.mean(r * r)))
+    worst = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), rms)))
+    assert nmse <= GEMM_NMSE and worst <= GEMM_MAXREL, (nmse, worst)
