@@ -36,10 +36,11 @@ using namespace moe;
 
 constexpr int kQWarps = 8;
 constexpr int kQThreads = 32 * kQWarps;
-constexpr int kMR = 8;                              // activation rows per unit
+constexpr int kMaxMR = 8;  // activation rows per unit: 8, or 2 for decode-class calls
 constexpr int kItemsPerUnit = 32;                   // pairs of weight rows per unit
 constexpr int kItemsPerWarp = kItemsPerUnit / kQWarps;
-constexpr int kChunkK = 2048;                       // weights of a row staged at a time
+// weights of a row staged at a time: 1024 for Q8_0 (1088 bytes), 2048 for Q4_K (1152 bytes)
+__host__ __device__ constexpr int chunk_k(int fmt) { return fmt == MOE_QFMT_Q8_0 ? 1024 : 2048; }
 constexpr int kMaxK = 16384;
 constexpr int kMaxG = 1024;
 
@@ -57,43 +58,44 @@ struct QFmt<MOE_QFMT_Q4_K> {
 };
 
 
-// Per-warp ring of weight slots.  A slot holds one K chunk of the warp's two
-// weight rows, brought in by two TMA bulk copies that complete on the slot's
-// mbarrier; each row's place is padded by 16 bytes because the Q8_0 code
-// reads take nine words and the ninth of the last block ends 4 bytes past
-// the row.  The ring gets a fixed byte budget, and the number of slots follows
-// from the slot size (2 .. kMaxSlots): long rows get few large slots, short
-// rows many small ones, so every warp keeps several KB of weights in flight.
+// Per-warp ring of weight slots.  A slot holds one K chunk of four weight
+// rows -- two items of two rows, one item per half-warp -- brought in by TMA
+// bulk copies that complete on the slot's mbarrier; each row's place is
+// padded by 16 bytes because the Q8_0 code reads take nine words and the
+// ninth of the last block ends 4 bytes past the row.  The ring gets a fixed
+// byte budget and the number of slots follows from the slot size
+// (2 .. kMaxSlots), so every warp keeps several KB of weights in flight.
 constexpr int kWarpRingBytes = 9344;
 constexpr int kMaxSlots = 8;
+constexpr int kSlotRows = 4;
 
 __host__ __device__ constexpr int align16(int n) { return (n + 15) & ~15; }
 
 __host__ __device__ inline int q_blk(int fmt) { return fmt == MOE_QFMT_Q8_0 ? 32 : 256; }
 __host__ __device__ inline int q_bytes(int fmt) { return fmt == MOE_QFMT_Q8_0 ? 34 : 144; }
-// bytes of one staged row chunk (a chunk is at most kChunkK weights)
+// bytes of one staged row chunk (a chunk is at most chunk_k(fmt) weights)
 __host__ __device__ inline int chunk_row_bytes(int fmt, int K) {
-  return ((K < kChunkK ? K : kChunkK) / q_blk(fmt)) * q_bytes(fmt);
+  return ((K < chunk_k(fmt) ? K : chunk_k(fmt)) / q_blk(fmt)) * q_bytes(fmt);
 }
 __host__ __device__ inline int slot_row_stride(int fmt, int K) {
   return align16(chunk_row_bytes(fmt, K)) + 16;
 }
 __host__ __device__ inline int ring_slots(int fmt, int K) {
-  const int n = kWarpRingBytes / (2 * slot_row_stride(fmt, K));
+  const int n = kWarpRingBytes / (kSlotRows * slot_row_stride(fmt, K));
   return n < 2 ? 2 : (n > kMaxSlots ? kMaxSlots : n);
 }
 
 // shared-memory carve-up of one CTA (host and device compute it alike)
 struct QSmem {
   int off_src, off_bars, off_codes, off_scale, off_xsum, off_ring, warp_ring, total;
-  __host__ __device__ QSmem(int fmt, int K, int G) {
+  __host__ __device__ QSmem(int fmt, int K, int G, int mr) {
     off_src = align16((G + 1) * 4);
-    off_bars = off_src + align16(kMR * 4);  // per warp kMaxSlots mbarriers, then an abort flag
+    off_bars = off_src + align16(mr * 4);  // per warp kMaxSlots mbarriers, then an abort flag
     off_codes = off_bars + align16(kQWarps * kMaxSlots * 8 + 4);
-    off_scale = off_codes + kMR * K;
-    off_xsum = off_scale + align16(kMR * (K / q_blk(fmt)) * 4);
-    off_ring = off_xsum + (fmt == MOE_QFMT_Q4_K ? align16(kMR * (K / 32) * 4) : 0);
-    warp_ring = ring_slots(fmt, K) * 2 * slot_row_stride(fmt, K);
+    off_scale = off_codes + mr * K;
+    off_xsum = off_scale + align16(mr * (K / q_blk(fmt)) * 4);
+    off_ring = off_xsum + (fmt == MOE_QFMT_Q4_K ? align16(mr * (K / 32) * 4) : 0);
+    warp_ring = ring_slots(fmt, K) * kSlotRows * slot_row_stride(fmt, K);
     total = off_ring + kQWarps * warp_ring;
   }
 };
@@ -124,32 +126,6 @@ __device__ __forceinline__ int group_lo(const int32_t* off, int g, int P) {
   return min(max(__ldg(off + g), 0), P);
 }
 
-// byte i (0..11) of the Q4_K scale field held in three words
-__device__ __forceinline__ int scale_byte(uint32_t s0, uint32_t s1, uint32_t s2, int i) {
-  const uint32_t w = i < 4 ? s0 : (i < 8 ? s1 : s2);
-  return static_cast<int>((w >> (8 * (i & 3))) & 0xFFu);
-}
-
-// 6-bit scale and min of Q4_K sub-block j: sub-blocks 0-3 keep theirs in the
-// low six bits of bytes j and j+4; sub-blocks 4-7 take the low four bits from
-// the nibbles of byte j+4 and the top two from the top bits of bytes j-4 and j
-__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j,
-                                              int& sc, int& m) {
-  if (j < 4) {
-    sc = scale_byte(s0, s1, s2, j) & 63;
-    m = scale_byte(s0, s1, s2, j + 4) & 63;
-  } else {
-    const int b = scale_byte(s0, s1, s2, j + 4);
-    sc = (b & 15) | ((scale_byte(s0, s1, s2, j - 4) >> 6) << 4);
-    m = (b >> 4) | ((scale_byte(s0, s1, s2, j) >> 6) << 4);
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, s);
-  return v;
-}
 
 // TMA bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from global to this CTA's shared memory, completing on mbarrier `bar`
@@ -183,142 +159,239 @@ __device__ __forceinline__ bool q_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
+// The 6-bit scales and mins of Q4_K sub-blocks 2c and 2c+1 (c = 0..3): the
+// two bytes 2(c&1), 2(c&1)+1 of each scale word give them at once.  Sub-blocks
+// 0-3 keep scale and min in the low six bits of bytes j (word s0) and j+4
+// (s1); sub-blocks 4-7 take the low four bits from the nibbles of byte j+4
+// (s2) and the top two from the top bits of bytes j-4 (s0) and j (s1).
+__device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32_t s2, int c,
+                                                int& sc_l, int& sc_h, int& m_l, int& m_h) {
+  const uint32_t sh = static_cast<uint32_t>(c & 1) * 16u;
+  const uint32_t w0 = s0 >> sh, w1 = s1 >> sh, w2 = s2 >> sh;
+  if (c < 2) {
+    sc_l = static_cast<int>(w0 & 63u);
+    sc_h = static_cast<int>((w0 >> 8) & 63u);
+    m_l = static_cast<int>(w1 & 63u);
+    m_h = static_cast<int>((w1 >> 8) & 63u);
+  } else {
+    sc_l = static_cast<int>((w2 & 15u) | ((w0 >> 2) & 0x30u));
+    sc_h = static_cast<int>(((w2 >> 8) & 15u) | ((w0 >> 10) & 0x30u));
+    m_l = static_cast<int>(((w2 >> 4) & 15u) | ((w1 >> 2) & 0x30u));
+    m_h = static_cast<int>(((w2 >> 12) & 15u) | ((w1 >> 10) & 0x30u));
+  }
+}
+
+__device__ __forceinline__ int dp4a8(const int (&q)[8], int4 a0, int4 a1) {
+  // two chains of four for a shorter dependency path
+  int x = __dp4a(q[0], a0.x, 0), y = __dp4a(q[4], a1.x, 0);
+  x = __dp4a(q[1], a0.y, x);
+  y = __dp4a(q[5], a1.y, y);
+  x = __dp4a(q[2], a0.z, x);
+  y = __dp4a(q[6], a1.z, y);
+  x = __dp4a(q[3], a0.w, x);
+  y = __dp4a(q[7], a1.w, y);
+  return x + y;
+}
+
 // acc[w][r] += this lane's share of  sum_k W[w][k] * A[r][k]  over one chunk
-// of K (weights k0 .. k0 + kc) for the slot's weight rows (the second at `rs`
-// bytes after the first).  The chunk is cut into tasks -- a Q8_0 block, or two
-// whole sub-blocks (64 weights, one 32-byte run of codes) of a Q4_K
-// super-block -- and the tasks of both rows are dealt to the lanes in turn.
-template <int kFmt>
+// of K (weights k0 .. k0 + kc) for an item's two weight rows (the second at
+// `rs` bytes after the first).  The 16 lanes of a half-warp share the item:
+// the chunk is cut into K tasks -- a Q8_0 block, or a 32-byte (64 weights:
+// two whole sub-blocks) or, for short rows, a 16-byte (32 weights) run of a
+// Q4_K super-block's codes -- dealt to the half's lanes (li = 0..15) in turn;
+// a lane works each of its K tasks on both rows, so the rows share the
+// activation loads and give independent dependency chains.
+template <int kFmt, int kMR>
 __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two, int k0, int kc,
                                           const int8_t* s_codes, const float* s_scale,
-                                          const int* s_xsum, int K, int m, int lane,
+                                          const int* s_xsum, int K, int m, int li,
                                           float (&acc)[2][kMR]) {
   if (kFmt == MOE_QFMT_Q8_0) {
-    const int tpr = kc / 32;  // blocks per row in this chunk
+    const int nt = kc / 32;  // blocks in this chunk
     const int nb_row = K / 32;
-#pragma unroll 1
-    for (int t = lane; t < (two ? 2 * tpr : tpr); t += 32) {
-      const int wr = t >= tpr ? 1 : 0;
-      const int b = t - wr * tpr;
+#pragma unroll
+    for (int i = 0; i < chunk_k(kFmt) / 32 / 16; ++i) {
+      const int b = li + 16 * i;
+      if (b >= nt) break;
       const int kb = k0 + 32 * b;
-      const uint8_t* row = slot + wr * rs;
-      // the 32 codes start 2 bytes into the block, 2-byte aligned: read the
-      // nine covering words and shift by 0 or 16 bits
       const int base = 34 * b + 2;
-      const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (base & ~3));
       const uint32_t sh = static_cast<uint32_t>(base & 3) * 8u;
-      uint32_t u[9];
+      int qw[2][8];
+      float dw[2];
 #pragma unroll
-      for (int i = 0; i < 9; ++i) u[i] = wp[i];
-      int qw[8];
+      for (int wr = 0; wr < 2; ++wr) {
+        // the 32 codes start 2 bytes into the block, 2-byte aligned: read the
+        // nine covering words and shift by 0 or 16 bits (a missing second row
+        // reads the ring's own bytes and is never accumulated)
+        const uint8_t* row = slot + wr * rs;
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(row + (base & ~3));
+        uint32_t u[9];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qw[i] = static_cast<int>(__funnelshift_r(u[i], u[i + 1], sh));
-      const float dw = half_bits_to_f32(*reinterpret_cast<const uint16_t*>(row + 34 * b));
+        for (int j = 0; j < 9; ++j) u[j] = wp[j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          qw[wr][j] = static_cast<int>(__funnelshift_r(u[j], u[j + 1], sh));
+        dw[wr] = half_bits_to_f32(*reinterpret_cast<const uint16_t*>(row + 34 * b));
+      }
 #pragma unroll
       for (int r = 0; r < kMR; ++r) {
         if (r >= m) break;
         const int4* ap = reinterpret_cast<const int4*>(s_codes + r * K + kb);
         const int4 a0 = ap[0], a1 = ap[1];
-        int is = __dp4a(qw[0], a0.x, 0);
-        is = __dp4a(qw[1], a0.y, is);
-        is = __dp4a(qw[2], a0.z, is);
-        is = __dp4a(qw[3], a0.w, is);
-        is = __dp4a(qw[4], a1.x, is);
-        is = __dp4a(qw[5], a1.y, is);
-        is = __dp4a(qw[6], a1.z, is);
-        is = __dp4a(qw[7], a1.w, is);
-        const float dd = __fmul_rn(dw, s_scale[r * nb_row + kb / 32]);
-        const float v = static_cast<float>(is);
-        if (wr == 0) acc[0][r] = fmaf(dd, v, acc[0][r]);
-        else acc[1][r] = fmaf(dd, v, acc[1][r]);
+        const float dx = s_scale[r * nb_row + kb / 32];
+        const int i0 = dp4a8(qw[0], a0, a1);
+        const int i1 = dp4a8(qw[1], a0, a1);
+        acc[0][r] = fmaf(__fmul_rn(dw[0], dx), static_cast<float>(i0), acc[0][r]);
+        if (two) acc[1][r] = fmaf(__fmul_rn(dw[1], dx), static_cast<float>(i1), acc[1][r]);
       }
     }
   } else {
-    const int tpr = (kc / 256) * 4;  // tasks per row: 4 per super-block
+    const int nsb = kc / 256;
     const int nsb_row = K / 256;
     const uint32_t kLo = 0x0F0F0F0Fu;
-#pragma unroll 1
-    for (int t = lane; t < (two ? 2 * tpr : tpr); t += 32) {
-      const int wr = t >= tpr ? 1 : 0;
-      const int tt = t - wr * tpr;
-      const int sb = tt >> 2, c = tt & 3;
-      const int sbg = k0 / 256 + sb;  // super-block index within the row
-      const int kb = k0 + 256 * sb + 64 * c;
-      const uint8_t* blk = slot + wr * rs + 144 * sb;
-      const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-      const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
-      const float d = half_bits_to_f32(hdr.x), dmin = half_bits_to_f32(hdr.x >> 16);
-      int sc_l, m_l, sc_h, m_h;
-      q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc_l, m_l);
-      q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc_h, m_h);
-      // 32 bytes of codes: the low nibbles are sub-block 2c, the high ones 2c+1
-      const uint32_t qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-      int ql[8], qh[8];
+    if (nsb * 4 >= 16) {
+      // wide K tasks: 32 bytes of codes, sub-blocks 2c (low nibbles) and 2c+1
+      // (high nibbles) whole, so this lane adds both min terms
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ql[i] = static_cast<int>(qv[i] & kLo);
-        qh[i] = static_cast<int>((qv[i] >> 4) & kLo);
+      for (int i = 0; i < chunk_k(kFmt) / 256 * 4 / 16; ++i) {
+        const int t = li + 16 * i;
+        if (t >= nsb * 4) break;
+        const int sb = t >> 2, c = t & 3;
+        const int sbg = k0 / 256 + sb;
+        const int kb = k0 + 256 * sb + 64 * c;
+        int ql[2][8], qh[2][8], scl[2], sch[2], ml[2], mh[2];
+        float d[2], dmin[2];
+#pragma unroll
+        for (int wr = 0; wr < 2; ++wr) {
+          const uint8_t* blk = slot + wr * rs + 144 * sb;
+          const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+          const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
+          d[wr] = half_bits_to_f32(hdr.x);
+          dmin[wr] = half_bits_to_f32(hdr.x >> 16);
+          q4k_pair_scales(hdr.y, hdr.z, hdr.w, c, scl[wr], sch[wr], ml[wr], mh[wr]);
+          const uint32_t qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            ql[wr][j] = static_cast<int>(qv[j] & kLo);
+            qh[wr][j] = static_cast<int>((qv[j] >> 4) & kLo);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kMR; ++r) {
+          if (r >= m) break;
+          const int4* ap = reinterpret_cast<const int4*>(s_codes + r * K + kb);
+          const int4 l0 = ap[0], l1 = ap[1], h0 = ap[2], h1 = ap[3];
+          const int* xs = s_xsum + r * (K / 32) + sbg * 8 + 2 * c;
+          const int x_l = xs[0], x_h = xs[1];
+          const float dx = s_scale[r * nsb_row + sbg];
+#pragma unroll
+          for (int wr = 0; wr < 2; ++wr) {
+            const int il = dp4a8(ql[wr], l0, l1);
+            const int ih = dp4a8(qh[wr], h0, h1);
+            const int s1 = scl[wr] * il + sch[wr] * ih;
+            const int s2 = ml[wr] * x_l + mh[wr] * x_h;
+            const float tv = __fsub_rn(__fmul_rn(d[wr], static_cast<float>(s1)),
+                                       __fmul_rn(dmin[wr], static_cast<float>(s2)));
+            if (wr == 0) acc[0][r] = fmaf(dx, tv, acc[0][r]);
+            else if (two) acc[1][r] = fmaf(dx, tv, acc[1][r]);
+          }
+        }
       }
+    } else {
+      // narrow K tasks for short rows: 16 bytes of codes -- weights 64c + 16h + i
+      // of sub-block 2c (low nibbles) and 64c + 32 + 16h + i of 2c+1 (high);
+      // the h = 0 lane adds the two sub-blocks' min terms
 #pragma unroll
-      for (int r = 0; r < kMR; ++r) {
-        if (r >= m) break;
-        const int4* ap = reinterpret_cast<const int4*>(s_codes + r * K + kb);
-        const int4 l0 = ap[0], l1 = ap[1], h0 = ap[2], h1 = ap[3];
-        int il = __dp4a(ql[0], l0.x, 0);
-        il = __dp4a(ql[1], l0.y, il);
-        il = __dp4a(ql[2], l0.z, il);
-        il = __dp4a(ql[3], l0.w, il);
-        il = __dp4a(ql[4], l1.x, il);
-        il = __dp4a(ql[5], l1.y, il);
-        il = __dp4a(ql[6], l1.z, il);
-        il = __dp4a(ql[7], l1.w, il);
-        int ih = __dp4a(qh[0], h0.x, 0);
-        ih = __dp4a(qh[1], h0.y, ih);
-        ih = __dp4a(qh[2], h0.z, ih);
-        ih = __dp4a(qh[3], h0.w, ih);
-        ih = __dp4a(qh[4], h1.x, ih);
-        ih = __dp4a(qh[5], h1.y, ih);
-        ih = __dp4a(qh[6], h1.z, ih);
-        ih = __dp4a(qh[7], h1.w, ih);
-        const int s1 = sc_l * il + sc_h * ih;
-        const int* xs = s_xsum + r * (K / 32) + sbg * 8 + 2 * c;
-        const int s2 = m_l * xs[0] + m_h * xs[1];
-        const float tv = __fsub_rn(__fmul_rn(d, static_cast<float>(s1)),
-                                   __fmul_rn(dmin, static_cast<float>(s2)));
-        const float dx = s_scale[r * nsb_row + sbg];
-        if (wr == 0) acc[0][r] = fmaf(dx, tv, acc[0][r]);
-        else acc[1][r] = fmaf(dx, tv, acc[1][r]);
+      for (int i = 0; i < 2; ++i) {  // at most 3 super-blocks: 24 tasks
+        const int t = li + 16 * i;
+        if (t >= nsb * 8) break;
+        const int sb = t >> 3, part = t & 7, c = part >> 1, h = part & 1;
+        const int sbg = k0 / 256 + sb;
+        const int kb = k0 + 256 * sb + 64 * c + 16 * h;
+        int ql[2][4], qh[2][4], scl[2], sch[2], ml[2], mh[2];
+        float d[2], dmin[2];
+#pragma unroll
+        for (int wr = 0; wr < 2; ++wr) {
+          const uint8_t* blk = slot + wr * rs + 144 * sb;
+          const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+          const uint4 q = *reinterpret_cast<const uint4*>(blk + 16 + 16 * part);
+          d[wr] = half_bits_to_f32(hdr.x);
+          dmin[wr] = half_bits_to_f32(hdr.x >> 16);
+          q4k_pair_scales(hdr.y, hdr.z, hdr.w, c, scl[wr], sch[wr], ml[wr], mh[wr]);
+          const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            ql[wr][j] = static_cast<int>(qv[j] & kLo);
+            qh[wr][j] = static_cast<int>((qv[j] >> 4) & kLo);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kMR; ++r) {
+          if (r >= m) break;
+          const int4 al = *reinterpret_cast<const int4*>(s_codes + r * K + kb);
+          const int4 ah = *reinterpret_cast<const int4*>(s_codes + r * K + kb + 32);
+          const int* xs = s_xsum + r * (K / 32) + sbg * 8 + 2 * c;
+          const int x_l = h == 0 ? xs[0] : 0, x_h = h == 0 ? xs[1] : 0;
+          const float dx = s_scale[r * nsb_row + sbg];
+#pragma unroll
+          for (int wr = 0; wr < 2; ++wr) {
+            int il = __dp4a(ql[wr][0], al.x, 0), ih = __dp4a(qh[wr][0], ah.x, 0);
+            il = __dp4a(ql[wr][1], al.y, il);
+            ih = __dp4a(qh[wr][1], ah.y, ih);
+            il = __dp4a(ql[wr][2], al.z, il);
+            ih = __dp4a(qh[wr][2], ah.z, ih);
+            il = __dp4a(ql[wr][3], al.w, il);
+            ih = __dp4a(qh[wr][3], ah.w, ih);
+            const int s1 = scl[wr] * il + sch[wr] * ih;
+            const int s2 = ml[wr] * x_l + mh[wr] * x_h;
+            const float tv = __fsub_rn(__fmul_rn(d[wr], static_cast<float>(s1)),
+                                       __fmul_rn(dmin[wr], static_cast<float>(s2)));
+            if (wr == 0) acc[0][r] = fmaf(dx, tv, acc[0][r]);
+            else if (two) acc[1][r] = fmaf(dx, tv, acc[1][r]);
+          }
+        }
       }
     }
   }
 }
 
+// sum over the 16 lanes of a half-warp (both halves at once)
+__device__ __forceinline__ float half_sum(float v) {
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, s);
+  return v;
+}
+
 // Each CTA takes a contiguous range of units -- (row block, column block) with
 // the column block fastest -- so consecutive units mostly share their
-// activation rows, which are then loaded once.  Each warp walks the slots of
-// its share of the range (per unit: kItemsPerWarp items, per item the K
-// chunks) through its ring: the copy of slot k + S - 1 is issued before slot
-// k is computed, so S - 1 slots stay in flight.  Two cursors walk the slot
-// sequence, one for the copies and one for the compute; each looks up its
-// unit's group once per unit.
+// activation rows, which are then loaded once.  Per unit a warp has
+// kItemsPerWarp items, worked as slots of two items (one per half-warp), each
+// slot in K chunks; the slots go through the warp's ring: the copies of slot
+// k + S - 1 start before slot k is computed, so S - 1 slots stay in flight.
+// Two cursors walk the slot sequence, one for the copies and one for the
+// compute; each finds its unit's group once per unit.
 struct QCursor {
-  int u, it, ch;   // unit, item of this warp within the unit, K chunk
-  int rb, cb, g;   // the unit's row block, column block and group
+  int u, s, ch;       // unit, slot of this warp within the unit, K chunk
+  int rb, cb, g;      // the unit's row block, column block and group
+  const uint8_t* wg;  // the group's weights
 };
 
-template <int kFmt, int kEpi>
+template <int kFmt, int kEpi, int kMR>
 __global__ void __launch_bounds__(kQThreads, 2) qgemm_kernel(QParams p) {
   using F = QFmt<kFmt>;
+  constexpr int kCK = chunk_k(kFmt);
+  constexpr int kSlotsPerUnit = kItemsPerWarp / 2;
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = p.K, G = p.G, P = p.P;
-  const QSmem L(kFmt, K, G);
+  const QSmem L(kFmt, K, G, kMR);
   int* rb_start = reinterpret_cast<int*>(smem);
   int* s_src = reinterpret_cast<int*>(smem + L.off_src);
   int8_t* s_codes = reinterpret_cast<int8_t*>(smem + L.off_codes);
   float* s_scale = reinterpret_cast<float*>(smem + L.off_scale);
   int* s_xsum = reinterpret_cast<int*>(smem + L.off_xsum);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, li = lane & 15;
   uint8_t* ring = smem + L.off_ring + warp * L.warp_ring;
   const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
   const uint32_t bars = static_cast<uint32_t>(__cvta_generic_to_shared(smem + L.off_bars)) +
@@ -373,15 +446,17 @@ __global__ void __launch_bounds__(kQThreads, 2) qgemm_kernel(QParams p) {
   const int nb_row = K / F::kBlk;
   const long long row_bytes = static_cast<long long>(nb_row) * F::kBytes;
   const long long group_bytes = (kEpi == QE_GATEUP ? 2LL * p.N : p.N) * row_bytes;
+  // the second row of an item: the up row N rows on (gate/up), else the next row
+  const long long second = kEpi == QE_GATEUP ? p.N * row_bytes : row_bytes;
   const int total = rb_start[G] * p.n_cb;  // the host bounds this below 2^31
   const int u0 = static_cast<int>(static_cast<long long>(total) * blockIdx.x / gridDim.x);
   const int u1 = static_cast<int>(static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x);
-  const int nchunk = (K + kChunkK - 1) / kChunkK;
-  const int chunk_bytes = (kChunkK / F::kBlk) * F::kBytes;
+  const int nchunk = (K + kCK - 1) / kCK;
+  constexpr int kChunkBytes = (kCK / F::kBlk) * F::kBytes;
 
   auto set_unit = [&](QCursor& c, int u) {
     c.u = u;
-    c.it = 0;
+    c.s = 0;
     c.ch = 0;
     c.rb = u / p.n_cb;
     c.cb = u - c.rb * p.n_cb;
@@ -392,52 +467,60 @@ __global__ void __launch_bounds__(kQThreads, 2) qgemm_kernel(QParams p) {
       else hi_g = mid;
     }
     c.g = lo_g;
+    c.wg = p.w + c.g * group_bytes;
   };
   auto advance = [&](QCursor& c) {
     if (++c.ch == nchunk) {
       c.ch = 0;
-      if (++c.it == kItemsPerWarp) {
+      if (++c.s == kSlotsPerUnit) {
         if (c.u + 1 < u1) set_unit(c, c.u + 1);
         else c.u = u1;  // past the end
       }
     }
   };
-  auto rows_of = [&](const QCursor& c, int& item, int& wr0, int& wr1) {
-    item = c.cb * kItemsPerUnit + c.it * kQWarps + warp;
-    if (kEpi == QE_GATEUP) {
-      wr0 = item;
-      wr1 = p.N + item;
-      return true;
-    }
-    wr0 = 2 * item;
-    wr1 = 2 * item + 1;
-    return wr1 < p.N;
+  // item of half h in the cursor's slot, its first weight row, and whether
+  // it has a second row
+  auto item_of = [&](const QCursor& c, int h, int& wr0) {
+    const int item = c.cb * kItemsPerUnit + (2 * c.s + h) * kQWarps + warp;
+    wr0 = kEpi == QE_GATEUP ? item : 2 * item;
+    return item;
   };
-  // lane 0 starts the copies of the cursor's slot into ring place `place`; the
-  // place's barrier completes when they have landed (at once for an empty slot)
+  auto has_second = [&](int wr0) { return kEpi == QE_GATEUP || wr0 + 1 < p.N; };
+  // lane 0 starts the copies of the cursor's slot into ring place `place`;
+  // the place's barrier completes when they have landed (at once when empty)
   auto issue = [&](const QCursor& c, int place) {
     if (lane != 0) return;
-    uint32_t bytes = 0;
-    const uint8_t* src0 = nullptr;
-    const uint8_t* src1 = nullptr;
-    if (c.u < u1) {
-      int item, wr0, wr1;
-      const bool two = rows_of(c, item, wr0, wr1);
+    const uint32_t bar = bars + 8 * place;
+    const uint32_t dst = ring_s + static_cast<uint32_t>(place * kSlotRows * rs);
+    ptx::fence_proxy_async_smem();  // the warp's earlier reads of this place come first
+    if (c.u >= u1) {
+      ptx::mbar_arrive_expect_tx(bar, 0);
+      return;
+    }
+    const int k0 = c.ch * kCK;
+    const uint32_t bytes =
+        static_cast<uint32_t>(((K - k0 < kCK ? K - k0 : kCK) / F::kBlk) * F::kBytes);
+    const uint8_t* base = c.wg + static_cast<long long>(c.ch) * kChunkBytes;
+    const uint8_t* src[4];
+    int n = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int wr0;
+      const int item = item_of(c, h, wr0);
+      src[2 * h] = src[2 * h + 1] = nullptr;
       if (item < p.n_items) {
-        const uint8_t* wg = p.w + c.g * group_bytes + static_cast<long long>(c.ch) * chunk_bytes;
-        const int k0 = c.ch * kChunkK;
-        bytes = static_cast<uint32_t>((((K - k0 < kChunkK) ? K - k0 : kChunkK) / F::kBlk) *
-                                      F::kBytes);
-        src0 = wg + wr0 * row_bytes;
-        if (two) src1 = wg + wr1 * row_bytes;
+        src[2 * h] = base + wr0 * row_bytes;
+        ++n;
+        if (has_second(wr0)) {
+          src[2 * h + 1] = src[2 * h] + second;
+          ++n;
+        }
       }
     }
-    const uint32_t bar = bars + 8 * place;
-    const uint32_t dst = ring_s + static_cast<uint32_t>(place * 2 * rs);
-    ptx::fence_proxy_async_smem();  // the warp's earlier reads of this place come first
-    ptx::mbar_arrive_expect_tx(bar, src1 ? 2 * bytes : bytes);
-    if (src0) bulk_copy_g2s(dst, src0, bytes, bar);
-    if (src1) bulk_copy_g2s(dst + rs, src1, bytes, bar);
+    ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * bytes);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (src[j]) bulk_copy_g2s(dst + j * rs, src[j], bytes, bar);
   };
 
   QCursor ci, cc;  // copy cursor (runs S - 1 slots ahead), compute cursor
@@ -457,12 +540,12 @@ __global__ void __launch_bounds__(kQThreads, 2) qgemm_kernel(QParams p) {
 #pragma unroll
   for (int r = 0; r < kMR; ++r) acc[0][r] = acc[1][r] = 0.0f;
 
-  int place = 0;      // ring place of the compute cursor's slot
+  int place = 0;       // ring place of the compute cursor's slot
   uint32_t round = 0;  // completed passes over the ring: the barrier phase parity
   bool alive = true;   // false after a wait gave up: the warp then only keeps step
 #pragma unroll 1
   while (cc.u < u1) {
-    if (cc.it == 0 && cc.ch == 0 && cc.rb != cur_rb) {
+    if (cc.s == 0 && cc.ch == 0 && cc.rb != cur_rb) {
       // a new row block: every warp reaches this slot together (the slot
       // sequence is the same in all warps), finishes with the old rows, and
       // the CTA loads the new activation rows
@@ -520,41 +603,53 @@ __global__ void __launch_bounds__(kQThreads, 2) qgemm_kernel(QParams p) {
     if (alive) issue(ci, place == 0 ? S - 1 : place - 1);
     if (ci.u < u1) advance(ci);
     if (alive) alive = q_wait(bars + 8 * place, round & 1u, abort_flag, p.status);
-    int item, wr0, wr1;
-    const bool two = rows_of(cc, item, wr0, wr1);
-    if (alive && item < p.n_items) {
-      const int k0 = cc.ch * kChunkK;
-      const int kc = K - k0 < kChunkK ? K - k0 : kChunkK;
-      chunk_dot<kFmt>(ring + place * 2 * rs, rs, two, k0, kc, s_codes, s_scale, s_xsum, K, m,
-                      lane, acc);
-      if (cc.ch == nchunk - 1) {
+    int wr0;
+    const int item = item_of(cc, half, wr0);
+    const bool valid = alive && item < p.n_items;
+    const bool two = has_second(wr0);
+    if (valid) {
+      const int k0 = cc.ch * kCK;
+      const int kc = K - k0 < kCK ? K - k0 : kCK;
+      chunk_dot<kFmt, kMR>(ring + (place * kSlotRows + 2 * half) * rs, rs, two, k0, kc, s_codes,
+                           s_scale, s_xsum, K, m, li, acc);
+    }
+    if (cc.ch == nchunk - 1) {
+      // reduce every row's sums over each half-warp, then lane li = r of a
+      // half finishes row r of its item: the rows' epilogues run side by side
+      float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
-        for (int r = 0; r < kMR; ++r) {
-          if (r >= m) break;
-          const float y0 = warp_sum(acc[0][r]);
-          const float y1 = warp_sum(acc[1][r]);
-          acc[0][r] = acc[1][r] = 0.0f;
-          if (lane != r) continue;
-          const int row = row0 + r;
-          if (kEpi == QE_PLAIN) {
-            float* out = static_cast<float*>(p.out) + static_cast<long long>(row) * p.N;
-            out[wr0] = y0;
-            if (two) out[wr1] = y1;
-          } else if (kEpi == QE_DOWN) {
-            const int dst = p.row_to_pair ? __ldg(p.row_to_pair + row) : row;
-            if (dst < 0 || dst >= P) continue;
+      for (int r = 0; r < kMR; ++r) {
+        if (r >= m) break;
+        const float s0 = half_sum(acc[0][r]);
+        const float s1 = half_sum(acc[1][r]);
+        acc[0][r] = acc[1][r] = 0.0f;
+        if (li == r) {
+          y0 = s0;
+          y1 = s1;
+        }
+      }
+      if (valid && li < m) {
+        const int row = row0 + li;
+        const int wr1 = kEpi == QE_GATEUP ? p.N + item : wr0 + 1;
+        if (kEpi == QE_PLAIN) {
+          float* out = static_cast<float*>(p.out) + static_cast<long long>(row) * p.N;
+          out[wr0] = y0;
+          if (two) out[wr1] = y1;
+        } else if (kEpi == QE_DOWN) {
+          const int dst = p.row_to_pair ? __ldg(p.row_to_pair + row) : row;
+          if (dst >= 0 && dst < P) {
             const float wgt = p.pair_weight ? __ldg(p.pair_weight + dst) : 1.0f;
             uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<long long>(dst) * p.N;
             out[wr0] = f32_to_bf16_bits(p.pair_weight ? __fmul_rn(y0, wgt) : y0);
             if (two) out[wr1] = f32_to_bf16_bits(p.pair_weight ? __fmul_rn(y1, wgt) : y1);
-          } else {
-            // narrowing before the activation: gate and up are rounded to bf16 first
-            const float gz = bf16_bits_to_f32(f32_to_bf16_bits(y0));
-            const float uz = bf16_bits_to_f32(f32_to_bf16_bits(y1));
-            const float sg = gz / (1.0f + __expf(-gz));
-            static_cast<uint16_t*>(p.out)[static_cast<long long>(row) * p.N + wr0] =
-                f32_to_bf16_bits(sg * uz);
           }
+        } else {
+          // narrowing before the activation: gate and up are rounded to bf16 first
+          const float gz = bf16_bits_to_f32(f32_to_bf16_bits(y0));
+          const float uz = bf16_bits_to_f32(f32_to_bf16_bits(y1));
+          const float sg = gz / (1.0f + __expf(-gz));
+          static_cast<uint16_t*>(p.out)[static_cast<long long>(row) * p.N + wr0] =
+              f32_to_bf16_bits(sg * uz);
         }
       }
     }
@@ -630,21 +725,21 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, long 
 
 int q_block(int fmt) { return fmt == MOE_QFMT_Q8_0 ? 32 : (fmt == MOE_QFMT_Q4_K ? 256 : 0); }
 
-template <int kFmt, int kEpi>
-int launch_q(const char* op, QParams& p, cudaStream_t stream) {
+template <int kFmt, int kEpi, int kMR>
+int launch_q_mr(const char* op, QParams& p, cudaStream_t stream) {
   static std::atomic<int> configured_dev{-1};
-  auto kern = qgemm_kernel<kFmt, kEpi>;
+  auto kern = qgemm_kernel<kFmt, kEpi, kMR>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return check_launch(op);
   if (configured_dev.load(std::memory_order_acquire) != dev) {
     // the attribute is raised to the largest carve-up any call can need
-    const QSmem Lmax(kFmt, kMaxK, kMaxG);
+    const QSmem Lmax(kFmt, kMaxK, kMaxG, kMR);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total) !=
         cudaSuccess)
       return check_launch(op);
     configured_dev.store(dev, std::memory_order_release);
   }
-  const QSmem Lg(kFmt, p.K, p.G);
+  const QSmem Lg(kFmt, p.K, p.G, kMR);
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQThreads, Lg.total) !=
           cudaSuccess ||
@@ -664,6 +759,15 @@ int launch_q(const char* op, QParams& p, cudaStream_t stream) {
       launch_kernel(kern, dim3(grid), dim3(kQThreads), static_cast<size_t>(Lg.total), stream,
                     nullptr, 0, p),
       op);
+}
+
+// Row blocks of 2 when the groups hold 2 rows or fewer on average (decode):
+// every unit then costs about the same, so the CTAs' equal shares of units
+// take equal time; row blocks of 8 otherwise, so that weights are re-read less.
+template <int kFmt, int kEpi>
+int launch_q(const char* op, QParams& p, cudaStream_t stream) {
+  if (static_cast<long long>(p.P) <= 2LL * p.G) return launch_q_mr<kFmt, kEpi, 2>(op, p, stream);
+  return launch_q_mr<kFmt, kEpi, kMaxMR>(op, p, stream);
 }
 
 int check_q(const char* op, int qfmt, int P, int K, int N, int G, const int32_t* group_offsets,
