@@ -181,6 +181,27 @@ __device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32
   }
 }
 
+// dp4a with the first operand's bytes unsigned (0..255) and the second's signed
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// sum over 32 bytes of (high nibble of q) * a: the nibbles are used in place
+// (q & 0xF0 = 16 * nibble), so the result is 16 times the sum, exactly
+__device__ __forceinline__ int dp4a8_hi16(const uint32_t (&q)[8], int4 a0, int4 a1) {
+  const uint32_t kHi = 0xF0F0F0F0u;
+  int x = dp4a_us(q[0] & kHi, a0.x, 0), y = dp4a_us(q[4] & kHi, a1.x, 0);
+  x = dp4a_us(q[1] & kHi, a0.y, x);
+  y = dp4a_us(q[5] & kHi, a1.y, y);
+  x = dp4a_us(q[2] & kHi, a0.z, x);
+  y = dp4a_us(q[6] & kHi, a1.z, y);
+  x = dp4a_us(q[3] & kHi, a0.w, x);
+  y = dp4a_us(q[7] & kHi, a1.w, y);
+  return x + y;
+}
+
 __device__ __forceinline__ int dp4a8(const int (&q)[8], int4 a0, int4 a1) {
   // two chains of four for a shorter dependency path
   int x = __dp4a(q[0], a0.x, 0), y = __dp4a(q[4], a1.x, 0);
@@ -259,7 +280,8 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two,
         const int sb = t >> 2, c = t & 3;
         const int sbg = k0 / 256 + sb;
         const int kb = k0 + 256 * sb + 64 * c;
-        int ql[2][8], qh[2][8], scl[2], sch[2], ml[2], mh[2];
+        int ql[2][8], scl[2], sch[2], ml[2], mh[2];
+        uint32_t qr[2][8];  // raw code words: the high nibbles are used in place
         float d[2], dmin[2];
 #pragma unroll
         for (int wr = 0; wr < 2; ++wr) {
@@ -270,12 +292,16 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two,
           d[wr] = half_bits_to_f32(hdr.x);
           dmin[wr] = half_bits_to_f32(hdr.x >> 16);
           q4k_pair_scales(hdr.y, hdr.z, hdr.w, c, scl[wr], sch[wr], ml[wr], mh[wr]);
-          const uint32_t qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          qr[wr][0] = q0.x;
+          qr[wr][1] = q0.y;
+          qr[wr][2] = q0.z;
+          qr[wr][3] = q0.w;
+          qr[wr][4] = q1.x;
+          qr[wr][5] = q1.y;
+          qr[wr][6] = q1.z;
+          qr[wr][7] = q1.w;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            ql[wr][j] = static_cast<int>(qv[j] & kLo);
-            qh[wr][j] = static_cast<int>((qv[j] >> 4) & kLo);
-          }
+          for (int j = 0; j < 8; ++j) ql[wr][j] = static_cast<int>(qr[wr][j] & kLo);
         }
 #pragma unroll
         for (int r = 0; r < kMR; ++r) {
@@ -288,7 +314,7 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two,
 #pragma unroll
           for (int wr = 0; wr < 2; ++wr) {
             const int il = dp4a8(ql[wr], l0, l1);
-            const int ih = dp4a8(qh[wr], h0, h1);
+            const int ih = dp4a8_hi16(qr[wr], h0, h1) >> 4;  // exact: a multiple of 16
             const int s1 = scl[wr] * il + sch[wr] * ih;
             const int s2 = ml[wr] * x_l + mh[wr] * x_h;
             const float tv = __fsub_rn(__fmul_rn(d[wr], static_cast<float>(s1)),
@@ -309,7 +335,8 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two,
         const int sb = t >> 3, part = t & 7, c = part >> 1, h = part & 1;
         const int sbg = k0 / 256 + sb;
         const int kb = k0 + 256 * sb + 64 * c + 16 * h;
-        int ql[2][4], qh[2][4], scl[2], sch[2], ml[2], mh[2];
+        int ql[2][4], scl[2], sch[2], ml[2], mh[2];
+        uint32_t qr[2][4];  // raw code words: the high nibbles are used in place
         float d[2], dmin[2];
 #pragma unroll
         for (int wr = 0; wr < 2; ++wr) {
@@ -319,12 +346,12 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two,
           d[wr] = half_bits_to_f32(hdr.x);
           dmin[wr] = half_bits_to_f32(hdr.x >> 16);
           q4k_pair_scales(hdr.y, hdr.z, hdr.w, c, scl[wr], sch[wr], ml[wr], mh[wr]);
-          const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+          qr[wr][0] = q.x;
+          qr[wr][1] = q.y;
+          qr[wr][2] = q.z;
+          qr[wr][3] = q.w;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            ql[wr][j] = static_cast<int>(qv[j] & kLo);
-            qh[wr][j] = static_cast<int>((qv[j] >> 4) & kLo);
-          }
+          for (int j = 0; j < 4; ++j) ql[wr][j] = static_cast<int>(qr[wr][j] & kLo);
         }
 #pragma unroll
         for (int r = 0; r < kMR; ++r) {
@@ -336,14 +363,15 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* slot, int rs, bool two,
           const float dx = s_scale[r * nsb_row + sbg];
 #pragma unroll
           for (int wr = 0; wr < 2; ++wr) {
-            int il = __dp4a(ql[wr][0], al.x, 0), ih = __dp4a(qh[wr][0], ah.x, 0);
+            const uint32_t kHi = 0xF0F0F0F0u;
+            int il = __dp4a(ql[wr][0], al.x, 0), ih = dp4a_us(qr[wr][0] & kHi, ah.x, 0);
             il = __dp4a(ql[wr][1], al.y, il);
-            ih = __dp4a(qh[wr][1], ah.y, ih);
+            ih = dp4a_us(qr[wr][1] & kHi, ah.y, ih);
             il = __dp4a(ql[wr][2], al.z, il);
-            ih = __dp4a(qh[wr][2], ah.z, ih);
+            ih = dp4a_us(qr[wr][2] & kHi, ah.z, ih);
             il = __dp4a(ql[wr][3], al.w, il);
-            ih = __dp4a(qh[wr][3], ah.w, ih);
-            const int s1 = scl[wr] * il + sch[wr] * ih;
+            ih = dp4a_us(qr[wr][3] & kHi, ah.w, ih);
+            const int s1 = scl[wr] * il + sch[wr] * (ih >> 4);  // ih is 16 x the sum
             const int s2 = ml[wr] * x_l + mh[wr] * x_h;
             const float tv = __fsub_rn(__fmul_rn(d[wr], static_cast<float>(s1)),
                                        __fmul_rn(dmin[wr], static_cast<float>(s2)));
@@ -378,7 +406,7 @@ struct QCursor {
 };
 
 template <int kFmt, int kEpi, int kMR>
-__global__ void __launch_bounds__(kQThreads, 2) qgemm_kernel(QParams p) {
+__global__ void __launch_bounds__(kQThreads, kFmt == MOE_QFMT_Q8_0 ? 3 : 2) qgemm_kernel(QParams p) {
   using F = QFmt<kFmt>;
   constexpr int kCK = chunk_k(kFmt);
   constexpr int kSlotsPerUnit = kItemsPerWarp / 2;
