@@ -65,6 +65,7 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_f32_to_f16": ([_F], ctypes.c_uint16),
         "oracle_q4k_scale_min": ([_P, _I, _P], _I),
         "oracle_dequant_q": ([_P, _I, _I64, _I, _P], _I),
+        "oracle_dequant_q_bf16": ([_P, _I, _I64, _I, _P], _I),
         "oracle_quantize_act_q8": ([_P, _I64, _I, _I, _P, _P], _I),
         "oracle_gemm_q": ([_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
         "oracle_gateup_silu_q": ([_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P], _I),
@@ -284,6 +285,15 @@ def dequant_q(w, fmt, *, rows, K):
     out = np.zeros((rows, K), np.float64)
     rc = lib().oracle_dequant_q(_ptr(np.ascontiguousarray(w, np.uint8)), fmt, rows, K, _ptr(out))
     _check(rc, "dequant_q")
+    return out
+
+
+def dequant_q_bf16(w, fmt, *, rows, K):
+    """bf16 bits [rows, K] of keep-quant weight rows (value formed in f32, rounded once)."""
+    out = np.zeros((rows, K), np.uint16)
+    rc = lib().oracle_dequant_q_bf16(_ptr(np.ascontiguousarray(w, np.uint8)), fmt, rows, K,
+                                     _ptr(out))
+    _check(rc, "dequant_q_bf16")
     return out
 
 

@@ -1089,3 +1089,35 @@ int oracle_moe_layer_tokens_q(const uint16_t* x, const uint16_t* w_router,
   }
   return ORA_OK;
 }
+
+/* Dequantisation of keep-quant weights to bf16, for running them through
+ * the bf16 expert GEMMs.  READING (the pages dequantise only implicitly, when
+ * keep-quant is off): the value is formed in binary32 and rounded to bf16 once:
+ *   Q8_0: bf16(d * q)                          (exact product)
+ *   Q4_K: bf16((d * sc_j) * q - dmin * m_j)    (exact products, one rounded
+ *                                               subtraction, then the bf16 rounding) */
+int oracle_dequant_q_bf16(const uint8_t* w, int fmt, int64_t rows, int K, uint16_t* out) {
+  const int blk = q_block(fmt), bb = q_block_bytes(fmt);
+  if (!blk || !w || !out || rows < 0 || K <= 0 || K % blk) return ORA_ERR_ARG;
+  const int64_t nb = K / blk;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* p = w + (r * nb + b) * bb;
+      uint16_t* o = out + r * K + b * blk;
+      if (fmt == ORA_Q8_0) {
+        const float d = h2f(le16(p));
+        for (int i = 0; i < 32; ++i) o[i] = f2bf(d * (float)(int8_t)p[2 + i]);
+      } else {
+        const float d = h2f(le16(p)), dmin = h2f(le16(p + 2));
+        for (int k = 0; k < 256; ++k) {
+          int sc, m;
+          q4k_scale_min(p + 4, k / 32, &sc, &m);
+          const float t1 = (d * (float)sc) * (float)q4k_code(p + 16, k);
+          const float t2 = dmin * (float)m;
+          o[k] = f2bf(t1 - t2);
+        }
+      }
+    }
+  return ORA_OK;
+}

@@ -308,3 +308,27 @@ def test_layer_q_token_by_token_equals_batch_pieces(fmt):
     sd = O.down(acts, d["w2_shared"], None, P=T, I=32, H=H, G=1)
     ref = O.combine_gate(eo.reshape(T, K, H), None, sd, gl, T=T, K=K, H=H)
     assert np.array_equal(out, ref)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_dequant_bf16_is_the_exact_value_rounded(fmt):
+    # Q8_0 and Q4_K values are formed exactly in f32 except for Q4_K's one
+    # subtraction; the bf16 result must equal the round-to-nearest-even of the
+    # exact value whenever that subtraction is exact, and be within one bf16
+    # step of it always
+    f = FMT[fmt]
+    w = W.q_weights(9, 83, 1, 6, 1024, fmt, 0.02)
+    exact = O.dequant_q(w, f, rows=6, K=1024)
+    got = O.dequant_q_bf16(w, f, rows=6, K=1024)
+    ref = O.f32_to_bf16(exact.astype(np.float32))      # exact -> f32 is exact here or one rounding
+    if fmt == "q8_0":
+        assert np.array_equal(got, ref)
+    else:
+        g = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        step = np.abs(exact) * 2.0 ** -7 + 1e-30
+        assert np.all(np.abs(g - exact) <= step)
+        assert (got == ref).mean() > 0.999
+    hand = O.dequant_q_bf16(_q4k_block(), Q4_K, rows=1, K=256)[0]
+    hv = (hand.astype(np.uint32) << 16).view(np.float32)
+    assert hv[0] == 0.25 and hv[32] == 5.5 and hv[255] == -15.75
+    assert hv[223] == 139.0      # 138.75 rounds to 139: bf16 spacing is 1 in [128, 256)
