@@ -439,12 +439,16 @@ def run_ours(args):
         d["qfmt"] = qw
     if rank > 0:  # each replica gets its own tokens of the global batch
         d["x"] = W.rank_tokens(cfg, rank)
+    # keep-quant weights on prefill-sized batches: expanded to bf16 once and run on
+    # the tensor cores (--q-dequant auto picks that above 16 rows per expert)
+    qd = bool(qw) and (args.q_dequant == "on" or
+                       (args.q_dequant == "auto" and cfg.T * cfg.K > 16 * cfg.E))
     fp8 = args.weights == "fp8"
     if fp8:
         d["w13_e4m3"], d["w13_scale"] = W.quantize_fp8_block(d["w13"])
         d["w2_e4m3"], d["w2_scale"] = W.quantize_fp8_block(d["w2"])
     blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
-                   I_shared=cfg.I_shared, fp8_weights=fp8, qweights=qw)
+                   I_shared=cfg.I_shared, fp8_weights=fp8, qweights=qw, q_dequant=qd)
     x_host = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     x_dev = x_host.to(dev)
     out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
@@ -532,7 +536,7 @@ def run_ours(args):
     wb = 1 if fp8 else 2          # bytes per expert weight (FP8 adds one f32 per 128x128 block)
     sc = 4.0 / (128 * 128) if fp8 else 0.0
     a_in = 2.0                    # bytes per activation element read by a GEMM
-    if qw:                        # GGUF blocks; 8-bit activation codes plus one f32 per block
+    if qw and not qd:             # GGUF blocks; 8-bit activation codes plus one f32 per block
         _, qblk, qbytes = Q_WEIGHTS[qw]
         wb, sc, a_in = qbytes / qblk, 0.0, 1.0 + 4.0 / qblk
     bytes_gateup = touched * 2 * cfg.I * cfg.H * (wb + sc) + P * cfg.H * a_in + P * cfg.I * 2
@@ -540,18 +544,20 @@ def run_ours(args):
     t_gu = stage_avg["gemm_gateup"] / 1000.0
     t_dn = stage_avg["gemm_down"] / 1000.0
     # the keep-quant kernels run on the CUDA cores and are reported against HBM
-    tensor_bound = (not qw and flop_gateup / (pk["bf16_tflops"] * 1e12)
+    qk = qw and not qd            # the keep-quant kernels run
+    tensor_bound = (not qk and flop_gateup / (pk["bf16_tflops"] * 1e12)
                     >= bytes_gateup / (pk["hbm_gbs"] * 1e9))
     kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
-             f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qw else
+             f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qk else
              "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)")
+    traffic_key = "bf16" if qd else args.weights
     if tensor_bound:
         achieved = flop_gateup / t_gu / 1e12
         roofline = {"kernel": kname, "bound": "tensor", "achieved": achieved,
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / pk["bf16_tflops"],
                     "peak_source": f"{pk_src} bf16 dense (burst)",
-                    "traffic": recorded_traffic(cfg.name, args.weights),
+                    "traffic": recorded_traffic(cfg.name, traffic_key),
                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "algorithmic_flop_per_launch": flop_gateup}
     else:
@@ -559,7 +565,7 @@ def run_ours(args):
         roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                     "peak_source": f"{pk_src} HBM copy bandwidth",
-                    "traffic": recorded_traffic(cfg.name, args.weights),
+                    "traffic": recorded_traffic(cfg.name, traffic_key),
                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "algorithmic_bytes_per_launch": bytes_gateup,
                     "touched_experts": touched}
@@ -608,15 +614,17 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8" if qw else "bf16",
+            "dtype": "int8" if qk else "bf16",
             "data": "synthetic (seeded normal inputs and weights, "
                     + (f"Zipf({cfg.zipf_s})-skewed router bias" if cfg.zipf_s
                        else "unbiased router")
                     + ("; routed expert weights FP8 E4M3 with 128x128 block scales, "
                        "quantised from the same bf16 weights)" if fp8 else
                        f"; routed expert weights random valid GGUF {qw.upper()} blocks, "
-                       "activations quantized to 8-bit blocks on the device)" if qw else ")"),
-            "config": dict(config_dict(cfg, ws), weights=args.weights),
+                       + ("expanded to bf16 once on the device)" if qd else
+                          "activations quantized to 8-bit blocks on the device)") if qw else ")"),
+            "config": dict(config_dict(cfg, ws), weights=args.weights,
+                           **({"q_dequant": qd} if qw else {})),
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": int(cfg.T * cfg.H * 2),
                     "d2h_bytes_per_step": int(cfg.T * cfg.H * 2)},
@@ -643,6 +651,9 @@ def main():
     ap.add_argument("--config", default="prefill",
                     choices=["prefill", "decode", "large", "tiny", "combine"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q-dequant", default="auto", choices=["auto", "on", "off"],
+                    help="keep-quant weights: expand to bf16 once and use the tensor-core GEMMs "
+                         "(auto: above 16 routed rows per expert)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8", "q8_0", "q4_k"],
                     help="routed expert weights: bf16, FP8 E4M3 with 128x128 block scales, or "
                          "keep-quant GGUF Q8_0 / Q4_K blocks")

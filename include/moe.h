@@ -11,6 +11,7 @@
  *   shared_expert_gate                 out = sigmoid(gl) * sd
  *   moe_quantize_act_q8, moe_grouped_gemm_q, moe_grouped_gemm_gateup_silu_q,
  *   moe_grouped_gemm_down_q            keep-quant expert GEMMs (Q8_0 / Q4_K weights)
+ *   moe_dequantize_q_bf16              keep-quant weights expanded to bf16
  *
  * Sources (vllm.cpp pages):
  *   [I3094]  issue #3094 "Row: BACKEND-ROCM-BF16-MOE": names the two grouped
@@ -413,6 +414,14 @@ int moe_set_pdl(int enable);
  * row_to_pair ? row_to_pair[r] : r of out bf16 [P, H] (a dst outside [0, P) is
  * skipped).
  *
+ * moe_dequantize_q_bf16 -- keep-quant weight rows expanded to bf16 [rows, K],
+ * for batches with many rows per expert, which run faster on the bf16
+ * tensor-core GEMMs: each value formed in binary32 and rounded to bf16 once,
+ *   Q8_0: bf16(d * q)        Q4_K: bf16((d * sc_j) * q - dmin * m_j)
+ * (exact products, one rounded subtraction).  Bit-exact.  w: Q4_K blocks
+ * 16-byte aligned, Q8_0 blocks 2-byte aligned; out 16-byte aligned; K a
+ * multiple of the block.
+ *
  * Errors: MOE_ERR_ARG (qfmt, sizes, NULL operands), MOE_ERR_ALIGN (alignment,
  * K not a multiple of 256 or above 16384), MOE_ERR_CUDA.  No workspace.
  * ---------------------------------------------------------------------- */
@@ -431,6 +440,8 @@ int moe_grouped_gemm_down_q(const int8_t* a_codes, const float* a_scales, const 
                             int qfmt, const int32_t* group_offsets, const float* pair_weight,
                             const int32_t* row_to_pair, int P, int I, int H, int G,
                             void* out_bf16, void* stream);
+int moe_dequantize_q_bf16(const uint8_t* w, int qfmt, long long rows, int K, void* out_bf16,
+                          void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_combine -- kMoeCombine of [PR509].  Per output element, sequentially:
@@ -511,6 +522,7 @@ enum {
   MOE_KID_GEMM_Q = 14,        /* moe_grouped_gemm_q */
   MOE_KID_GEMM_Q_GATEUP = 15, /* moe_grouped_gemm_gateup_silu_q */
   MOE_KID_GEMM_Q_DOWN = 16,   /* moe_grouped_gemm_down_q */
+  MOE_KID_DEQUANT_Q = 17,     /* moe_dequantize_q_bf16 */
   MOE_KID_COUNT = 20
 };
 int moe_device_status(int* status_out, int clear);

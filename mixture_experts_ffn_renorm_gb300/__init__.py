@@ -25,7 +25,7 @@ KID = {
     "route_logits": 0, "route_topk": 1, "permute_count": 2, "permute_scan": 3,
     "permute_place": 4, "permute_gather": 5, "gemm_gateup": 6, "gemm_down": 7, "combine": 8,
     "combine_gate": 9, "shared_gate": 10, "gate_sigmoid": 11, "permute_small": 12,
-    "quant_act": 13, "gemm_q": 14, "gemm_q_gateup": 15, "gemm_q_down": 16,
+    "quant_act": 13, "gemm_q": 14, "gemm_q_gateup": 15, "gemm_q_down": 16, "dequant_q": 17,
 }
 KID_COUNT = 20
 QFMT_Q8_0, QFMT_Q4_K = 1, 2
@@ -40,7 +40,7 @@ EXPORTS = (
     "moe_grouped_gemm_gateup_silu_bf16_shared", "moe_grouped_gemm_down_bf16_shared",
     "moe_route_topk_ex", "moe_grouped_gemm_gateup_silu_fp8w", "moe_grouped_gemm_down_fp8w",
     "moe_quantize_act_q8", "moe_grouped_gemm_q", "moe_grouped_gemm_gateup_silu_q",
-    "moe_grouped_gemm_down_q",
+    "moe_grouped_gemm_down_q", "moe_dequantize_q_bf16",
 )
 
 
@@ -84,6 +84,7 @@ _SIGS = {
     "moe_grouped_gemm_gateup_silu_q": ([_P, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P],
                                        _I),
     "moe_grouped_gemm_down_q": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "moe_dequantize_q_bf16": ([_P, _I, ctypes.c_longlong, _I, _P, _P], _I),
     "moe_set_gemm_pairing": ([_I], _I),
     "moe_set_pdl": ([_I], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
@@ -288,6 +289,12 @@ def moe_grouped_gemm_down_q(a_codes, a_scales, w2, qfmt, group_offsets, pair_wei
     rc = lib().moe_grouped_gemm_down_q(_ptr(a_codes), _ptr(a_scales), _ptr(w2), qfmt,
                                        _ptr(group_offsets), _ptr(pair_weight), _ptr(row_to_pair),
                                        P, I, H, G, _ptr(out), _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_dequantize_q_bf16(w, qfmt, rows, K, out, stream=None, check=True):
+    """Keep-quant weight rows expanded to bf16 (see moe.h)."""
+    rc = lib().moe_dequantize_q_bf16(_ptr(w), qfmt, rows, K, _ptr(out), _stream(stream))
     return _check(rc) if check else rc
 
 

@@ -18,8 +18,9 @@ from . import (BF16, QFMT_Q4_K, QFMT_Q8_0, moe_combine, moe_combine_gate,
                moe_grouped_gemm_down_bf16_shared, moe_grouped_gemm_down_fp8w,
                moe_grouped_gemm_down_q, moe_grouped_gemm_gateup_silu_bf16,
                moe_grouped_gemm_gateup_silu_bf16_shared, moe_grouped_gemm_gateup_silu_fp8w,
-               moe_grouped_gemm_gateup_silu_q, moe_permute, moe_permute_workspace_size,
-               moe_quantize_act_q8, moe_route_topk, moe_route_topk_workspace_size)
+               moe_grouped_gemm_gateup_silu_q, moe_dequantize_q_bf16, moe_permute,
+               moe_permute_workspace_size, moe_quantize_act_q8, moe_route_topk,
+               moe_route_topk_workspace_size)
 
 # keep-quant weight formats: name -> (library format id, weights per activation block)
 Q_WEIGHTS = {"q8_0": (QFMT_Q8_0, 32), "q4_k": (QFMT_Q4_K, 256)}
@@ -50,19 +51,28 @@ class MoeBlock:
     act rows are quantized to 8-bit blocks on the device, the gate/up GEMM reads
     the token rows through sorted_pair / K (no x_perm), and the shared expert
     stays bf16 in launches of its own.
+    q_dequant=True (with qweights): the GGUF blocks are expanded to bf16 once, on the
+    device, when the block is built, and the layer runs the bf16 tensor-core path --
+    the faster choice when the experts see many rows each (prefill-sized batches).
     """
 
     def __init__(self, H, I, E, K, weights, max_tokens, device="cuda", I_shared=0,
                  routed_scale=1.0, gather=False, fuse_shared=True, fp8_weights=False,
-                 qweights=None):
+                 qweights=None, q_dequant=False):
         self.H, self.I, self.E, self.K, self.Is = H, I, E, K, I_shared
         if qweights is not None:
             if qweights not in Q_WEIGHTS:
                 raise ValueError(f"qweights must be one of {sorted(Q_WEIGHTS)}")
             if fp8_weights:
                 raise ValueError("qweights and fp8_weights exclude each other")
-            gather = True
+            if not q_dequant:
+                gather = True
         self.qfmt, qblk = Q_WEIGHTS[qweights] if qweights is not None else (0, 0)
+        if q_dequant:
+            if qweights is None:
+                raise ValueError("q_dequant needs qweights")
+            weights = self._dequantized(weights, H, I, E, self.qfmt, device)
+            self.qfmt, qblk = 0, 0
         self.max_tokens = max_tokens
         # gather=True: the gate/up GEMM reads each routed row straight from x
         # (through sorted_pair / K); False: permute materialises x_perm and the
@@ -218,6 +228,19 @@ class MoeBlock:
             moe_combine(self.expert_out, BF16, None, None, BF16, self.routed_scale, T, K, H, out,
                         BF16, stream)
         mark("combine", edge=True)
+        return out
+
+    @staticmethod
+    def _dequantized(weights, H, I, E, qfmt, device):
+        """`weights` with w13 / w2 expanded from the GGUF blocks to bf16 on the device."""
+        dv = torch.device(device)
+        out = dict(weights)
+        for key, qkey, rows, Kd in (("w13", "w13q", E * 2 * I, H), ("w2", "w2q", E * H, I)):
+            q = torch.as_tensor(weights[qkey], dtype=torch.uint8).to(dv).contiguous()
+            w = torch.empty((rows, Kd), dtype=torch.bfloat16, device=dv)
+            moe_dequantize_q_bf16(q, qfmt, rows, Kd, w)
+            out[key] = w.view(E, rows // E, Kd)
+        torch.cuda.current_stream(dv).synchronize()
         return out
 
     # launches per forward (for the bench's gpu_launches claim)

@@ -341,3 +341,37 @@ def test_keep_quant_layer_against_the_oracle(cfg, fmt):
     rms = float(np.sqrt(np.mean(r * r)))
     worst = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), rms)))
     assert nmse <= GEMM_NMSE and worst <= GEMM_MAXREL, (nmse, worst)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+def test_keep_quant_weights_dequantised_layer(fmt):
+    # keep-quant weights expanded to bf16 once (q_dequant=True) and run on the
+    # bf16 tensor-core path: the whole block against the oracle's bf16 layer on
+    # the oracle's own bf16 expansion of the same blocks, on sampled tokens
+    cfg = W.LayerConfig("qd_T512_H512_I256_E16_K4_Is256", T=512, H=512, I=256, E=16, K=4,
+                        I_shared=256, zipf_s=1.1)
+    d = W.layer_inputs(cfg, with_weights=False)
+    d.update(W.layer_q_weights(cfg, fmt))
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                   I_shared=cfg.I_shared, qweights=fmt, q_dequant=True)
+    fo = O.Q8_0 if fmt == "q8_0" else O.Q4_K
+    do = dict(d)
+    do["w13"] = O.dequant_q_bf16(d["w13q"], fo, rows=cfg.E * 2 * cfg.I, K=cfg.H).reshape(
+        cfg.E, 2 * cfg.I, cfg.H)
+    do["w2"] = O.dequant_q_bf16(d["w2q"], fo, rows=cfg.E * cfg.H, K=cfg.I).reshape(
+        cfg.E, cfg.H, cfg.I)
+    assert np.array_equal(to_host(blk.w13), do["w13"]) and np.array_equal(to_host(blk.w2), do["w2"])
+    before = launches()
+    out = to_host(blk.forward(to_dev(d["x"])))
+    assert launched_since(before, "gemm_gateup") == 1 and launched_since(before, "gemm_q_gateup") == 0
+    toks = np.unique(np.concatenate([[0, cfg.T - 1],
+                                     np.random.default_rng(5).choice(cfg.T, 24, replace=False)]))
+    want, ora_ids, _ = _oracle_tokens(cfg, do, toks)
+    ids = to_host(blk.topk_ids)
+    same = np.all(np.sort(ora_ids, 1) == np.sort(ids[toks], 1), axis=1)
+    assert same.mean() >= 0.95
+    g, r = bf16_to_f64(out[toks][same]), bf16_to_f64(want[same])
+    nmse, _ = nmse_maxrel(g, r)
+    rms = float(np.sqrt(np.mean(r * r)))
+    worst = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), rms)))
+    assert nmse <= GEMM_NMSE and worst <= GEMM_MAXREL, (nmse, worst)

@@ -256,3 +256,16 @@ def test_decode_size_gemms_match_oracle(fmt):
     m.moe_grouped_gemm_down_q(to_dev(aq), to_dev(ad), to_dev(q["w2q"]), gf, to_dev(off),
                               to_dev(wts.ravel()), to_dev(sp), P, I, H, E, eo)
     assert_gemm_close(to_host(eo), eo_ref, f"decode down {fmt}")
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k"])
+@pytest.mark.parametrize("rows,K", [(1, 256), (37, 768), (300, 2048)])
+def test_dequantize_to_bf16_bit_exact(fmt, rows, K):
+    gf, fo = FMTS[fmt]
+    w = W.q_weights(rows + K, 84, 1, rows, K, fmt, 0.02).reshape(rows, -1)
+    ref = O.dequant_q_bf16(w, fo, rows=rows, K=K)
+    out = empty((rows, K), torch.bfloat16)
+    before = launches()
+    m.moe_dequantize_q_bf16(to_dev(w), gf, rows, K, out)
+    assert launched_since(before, "dequant_q") == 1
+    assert np.array_equal(to_host(out), ref)
