@@ -60,11 +60,14 @@ struct QFmt<MOE_QFMT_Q4_K> {
 
 // Per-warp ring of weight slots.  A slot holds one K chunk of four weight
 // rows -- two items of two rows, one item per half-warp -- brought in by TMA
-// bulk copies that complete on the slot's mbarrier; each row's place is
-// padded by 16 bytes because the Q8_0 code reads take nine words and the
-// ninth of the last block ends 4 bytes past the row.  The ring gets a fixed
-// byte budget and the number of slots follows from the slot size
-// (2 .. kMaxSlots), so every warp keeps several KB of weights in flight.
+// bulk copies that complete on the slot's mbarrier.  A warp's items are
+// consecutive, so when a row is a single chunk the slot's rows are two runs
+// of adjacent rows in HBM (gate/up: the two gate rows and the two up rows;
+// down: four rows) and arrive in one or two large copies: small bulk copies
+// cost the copy engine far more per byte than large ones.  The slot ends in
+// 16 spare bytes because the Q8_0 code reads take nine words and the ninth
+// of a row's last block ends 4 bytes past the row.  The ring gets a fixed
+// byte budget and the number of slots follows from the slot size.
 constexpr int kWarpRingBytes = 9344;
 constexpr int kMaxSlots = 8;
 constexpr int kSlotRows = 4;
@@ -73,15 +76,16 @@ __host__ __device__ constexpr int align16(int n) { return (n + 15) & ~15; }
 
 __host__ __device__ inline int q_blk(int fmt) { return fmt == MOE_QFMT_Q8_0 ? 32 : 256; }
 __host__ __device__ inline int q_bytes(int fmt) { return fmt == MOE_QFMT_Q8_0 ? 34 : 144; }
-// bytes of one staged row chunk (a chunk is at most chunk_k(fmt) weights)
+// bytes of one staged row chunk (a chunk is at most chunk_k(fmt) weights); a
+// multiple of 16 whenever K is a multiple of 256
 __host__ __device__ inline int chunk_row_bytes(int fmt, int K) {
   return ((K < chunk_k(fmt) ? K : chunk_k(fmt)) / q_blk(fmt)) * q_bytes(fmt);
 }
-__host__ __device__ inline int slot_row_stride(int fmt, int K) {
-  return align16(chunk_row_bytes(fmt, K)) + 16;
+__host__ __device__ inline int slot_bytes(int fmt, int K) {
+  return kSlotRows * chunk_row_bytes(fmt, K) + 16;
 }
 __host__ __device__ inline int ring_slots(int fmt, int K) {
-  const int n = kWarpRingBytes / (kSlotRows * slot_row_stride(fmt, K));
+  const int n = kWarpRingBytes / slot_bytes(fmt, K);
   return n < 2 ? 2 : (n > kMaxSlots ? kMaxSlots : n);
 }
 
@@ -95,7 +99,7 @@ struct QSmem {
     off_scale = off_codes + mr * K;
     off_xsum = off_scale + align16(mr * (K / q_blk(fmt)) * 4);
     off_ring = off_xsum + (fmt == MOE_QFMT_Q4_K ? align16(mr * (K / 32) * 4) : 0);
-    warp_ring = ring_slots(fmt, K) * kSlotRows * slot_row_stride(fmt, K);
+    warp_ring = ring_slots(fmt, K) * slot_bytes(fmt, K);
     total = off_ring + kQWarps * warp_ring;
   }
 };
@@ -426,7 +430,8 @@ __global__ void __launch_bounds__(kQThreads, kFmt == MOE_QFMT_Q8_0 ? 3 : 2) qgem
                         static_cast<uint32_t>(warp * kMaxSlots * 8);
   volatile int* abort_flag =
       reinterpret_cast<volatile int*>(smem + L.off_bars + kQWarps * kMaxSlots * 8);
-  const int rs = slot_row_stride(kFmt, K);
+  const int crb = chunk_row_bytes(kFmt, K);  // a staged row chunk
+  const int sbytes = slot_bytes(kFmt, K);
   const int S = ring_slots(kFmt, K);
 
   if (lane == 0) {
@@ -506,21 +511,22 @@ __global__ void __launch_bounds__(kQThreads, kFmt == MOE_QFMT_Q8_0 ? 3 : 2) qgem
       }
     }
   };
-  // item of half h in the cursor's slot, its first weight row, and whether
-  // it has a second row
+  // item of half h in the cursor's slot (a warp's items are consecutive), its
+  // first weight row, and whether it has a second row
   auto item_of = [&](const QCursor& c, int h, int& wr0) {
-    const int item = c.cb * kItemsPerUnit + (2 * c.s + h) * kQWarps + warp;
+    const int item = c.cb * kItemsPerUnit + warp * kItemsPerWarp + 2 * c.s + h;
     wr0 = kEpi == QE_GATEUP ? item : 2 * item;
     return item;
   };
   auto has_second = [&](int wr0) { return kEpi == QE_GATEUP || wr0 + 1 < p.N; };
-  // lane 0 starts the copies of the cursor's slot into ring place `place`;
-  // the place's barrier completes when they have landed (at once when empty)
+  // Lane 0 starts the copies of the cursor's slot into ring place `place`;
+  // the place's barrier completes when they have landed (at once when empty).
+  // Slot layout, rows of crb bytes: gate/up [gate A, gate B, up A, up B],
+  // down [A row 0, A row 1, B row 0, B row 1].
   auto issue = [&](const QCursor& c, int place) {
     if (lane != 0) return;
     const uint32_t bar = bars + 8 * place;
-    const uint32_t dst = ring_s + static_cast<uint32_t>(place * kSlotRows * rs);
-    ptx::fence_proxy_async_smem();  // the warp's earlier reads of this place come first
+    const uint32_t dst = ring_s + static_cast<uint32_t>(place * sbytes);
     if (c.u >= u1) {
       ptx::mbar_arrive_expect_tx(bar, 0);
       return;
@@ -529,26 +535,34 @@ __global__ void __launch_bounds__(kQThreads, kFmt == MOE_QFMT_Q8_0 ? 3 : 2) qgem
     const uint32_t bytes =
         static_cast<uint32_t>(((K - k0 < kCK ? K - k0 : kCK) / F::kBlk) * F::kBytes);
     const uint8_t* base = c.wg + static_cast<long long>(c.ch) * kChunkBytes;
-    const uint8_t* src[4];
-    int n = 0;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      int wr0;
-      const int item = item_of(c, h, wr0);
-      src[2 * h] = src[2 * h + 1] = nullptr;
-      if (item < p.n_items) {
-        src[2 * h] = base + wr0 * row_bytes;
-        ++n;
-        if (has_second(wr0)) {
-          src[2 * h + 1] = src[2 * h] + second;
-          ++n;
+    int wr0;
+    const int itemA = item_of(c, 0, wr0);
+    const bool one_chunk = nchunk == 1;  // then adjacent rows are adjacent in HBM too
+    if (kEpi == QE_GATEUP) {
+      const int n_it = min(2, max(0, p.n_items - itemA));  // items of the slot that exist
+      ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * n_it) * bytes);
+      if (n_it == 0) return;
+      const uint8_t* gate = base + itemA * row_bytes;
+      if (one_chunk) {
+        bulk_copy_g2s(dst, gate, n_it * bytes, bar);
+        bulk_copy_g2s(dst + 2 * crb, gate + second, n_it * bytes, bar);
+      } else {
+        for (int h = 0; h < n_it; ++h) {
+          bulk_copy_g2s(dst + h * crb, gate + h * row_bytes, bytes, bar);
+          bulk_copy_g2s(dst + (2 + h) * crb, gate + second + h * row_bytes, bytes, bar);
         }
       }
+    } else {
+      const int n_rows = min(kSlotRows, max(0, p.N - wr0));  // rows of the slot that exist
+      ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_rows) * bytes);
+      if (n_rows == 0) return;
+      const uint8_t* src = base + wr0 * row_bytes;
+      if (one_chunk) {
+        bulk_copy_g2s(dst, src, n_rows * bytes, bar);
+      } else {
+        for (int j = 0; j < n_rows; ++j) bulk_copy_g2s(dst + j * crb, src + j * row_bytes, bytes, bar);
+      }
     }
-    ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * bytes);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (src[j]) bulk_copy_g2s(dst + j * rs, src[j], bytes, bar);
   };
 
   QCursor ci, cc;  // copy cursor (runs S - 1 slots ahead), compute cursor
@@ -638,8 +652,10 @@ __global__ void __launch_bounds__(kQThreads, kFmt == MOE_QFMT_Q8_0 ? 3 : 2) qgem
     if (valid) {
       const int k0 = cc.ch * kCK;
       const int kc = K - k0 < kCK ? K - k0 : kCK;
-      chunk_dot<kFmt, kMR>(ring + (place * kSlotRows + 2 * half) * rs, rs, two, k0, kc, s_codes,
-                           s_scale, s_xsum, K, m, li, acc);
+      // the half's rows: gate/up at h and 2 + h, down at 2h and 2h + 1
+      const uint8_t* r0 = ring + place * sbytes + (kEpi == QE_GATEUP ? half : 2 * half) * crb;
+      chunk_dot<kFmt, kMR>(r0, kEpi == QE_GATEUP ? 2 * crb : crb, two, k0, kc, s_codes, s_scale,
+                           s_xsum, K, m, li, acc);
     }
     if (cc.ch == nchunk - 1) {
       // reduce every row's sums over each half-warp, then lane li = r of a
