@@ -8,12 +8,12 @@
 // GB300 has no fast 8-bit integer tensor-core path, and these ops matter where
 // the weights dominate the bytes (decode: a few rows per expert), so the dot
 // products run on the CUDA cores with dp4a.  The kernel is a persistent grid
-// over units of (up to 8 activation rows of one expert) x (32 pairs of weight
-// rows).  The unit's activation codes sit in shared memory; each warp streams
-// its weight rows, two at a time and in K chunks, from HBM into a ring of
-// shared-memory slots with cp.async (several slots in flight per warp), and
-// every lane multiplies its blocks with all of the unit's rows, so each weight
-// byte crosses HBM once per row block.
+// over units of (a row block of one expert: up to 8 activation rows, or 2 for
+// decode-class calls) x (32 pairs of weight rows).  The unit's activation codes
+// sit in shared memory; each warp streams its weight rows in K chunks, four
+// rows to a slot, from HBM into a ring of shared-memory slots with TMA bulk
+// copies, and its lanes multiply the rows with all of the unit's activation
+// rows, so each weight byte crosses HBM once per row block.
 //
 // Weight blocks (little-endian, as stored in GGUF files):
 //   Q8_0: 32 weights in 34 bytes: fp16 d, int8 q[32];          w = d*q
@@ -56,7 +56,6 @@ template <>
 struct QFmt<MOE_QFMT_Q4_K> {
   static constexpr int kBlk = 256, kBytes = 144;
 };
-
 
 // Per-warp ring of weight slots.  A slot holds one K chunk of four weight
 // rows -- two items of two rows, one item per half-warp -- brought in by TMA
@@ -129,7 +128,6 @@ __device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
 __device__ __forceinline__ int group_lo(const int32_t* off, int g, int P) {
   return min(max(__ldg(off + g), 0), P);
 }
-
 
 // TMA bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from global to this CTA's shared memory, completing on mbarrier `bar`

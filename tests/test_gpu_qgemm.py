@@ -103,6 +103,7 @@ PLAIN_CASES = [
     ([8, 8, 16, 7], 2048, 33),
     ([1, 1, 1, 1, 1, 1], 4096, 5),
     ([130, 2], 768, 1),
+    ([2, 1], 16384, 3),          # the longest rows: many K chunks, the largest shared-memory carve-up
 ]
 
 
