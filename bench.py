@@ -314,6 +314,12 @@ def combine_arms(dev, iters=20):
     return out
 
 
+def q_dequant_on(args, cfg):
+    """Whether keep-quant weights are expanded to bf16 for this run (--q-dequant)."""
+    mode = getattr(args, "q_dequant", "auto")
+    return mode == "on" or (mode == "auto" and cfg.T * cfg.K > 16 * cfg.E)
+
+
 def layer_oracle(O, cfg, d, tokens):
     """The oracle's whole block on `tokens`: keep-quant experts when `d` holds
     GGUF blocks (w13q / w2q, format d["qfmt"]), bf16 experts otherwise."""
@@ -379,7 +385,8 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_dict(cfg, 1), weights=weights),
+        "config": dict(config_dict(cfg, 1), weights=weights,
+                       **({"q_dequant": q_dequant_on(args, cfg)} if weights in Q_WEIGHTS else {})),
         "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "tokens/s",
                          "sample": f"{n} of {cfg.T} tokens per step, full block per token"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -441,8 +448,7 @@ def run_ours(args):
         d["x"] = W.rank_tokens(cfg, rank)
     # keep-quant weights on prefill-sized batches: expanded to bf16 once and run on
     # the tensor cores (--q-dequant auto picks that above 16 rows per expert)
-    qd = bool(qw) and (args.q_dequant == "on" or
-                       (args.q_dequant == "auto" and cfg.T * cfg.K > 16 * cfg.E))
+    qd = bool(qw) and q_dequant_on(args, cfg)
     fp8 = args.weights == "fp8"
     if fp8:
         d["w13_e4m3"], d["w13_scale"] = W.quantize_fp8_block(d["w13"])
