@@ -337,6 +337,10 @@ int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
  *   MOE_GEMM_SPLIT:  two launches per call -- the whole 256-row
  *                    blocks of every group on CTA pairs (no padding rows), then
  *                    the remaining rows of each group on MCAST/single tiles
+ *   MOE_GEMM_TALL:   single CTAs; the whole 256-row blocks of every group are
+ *                    256-row tiles, two M = 128 MMAs per k-step sharing each
+ *                    weight stage (a third less shared-memory fill per MMA),
+ *                    the remaining rows 128-row tiles; 256 rows or more per call
  * Results are identical up to f32 accumulation order.  On a skewed expert load
  * the single-CTA tiles are the fastest: their random mix of weight-bound and
  * tensor-bound tiles keeps both HBM and the tensor cores busy, which the
@@ -344,7 +348,8 @@ int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
  * Process-wide, takes effect at the next launch; returns the previous mode
  * (MOE_ERR_ARG for an unknown mode).  Not for use while another thread is
  * launching these GEMMs. */
-enum { MOE_GEMM_SINGLE = 0, MOE_GEMM_PAIR = 1, MOE_GEMM_MCAST = 2, MOE_GEMM_SPLIT = 3 };
+enum { MOE_GEMM_SINGLE = 0, MOE_GEMM_PAIR = 1, MOE_GEMM_MCAST = 2, MOE_GEMM_SPLIT = 3,
+       MOE_GEMM_TALL = 4 };
 int moe_set_gemm_pairing(int mode);
 
 /* moe_set_pdl -- programmatic dependent launch for every kernel of the

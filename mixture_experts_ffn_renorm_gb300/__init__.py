@@ -302,11 +302,12 @@ def moe_grouped_gemm_workspace_size(P, H, I, G) -> int:
     return lib().moe_grouped_gemm_workspace_size(P, H, I, G)
 
 
-GEMM_SINGLE, GEMM_PAIR, GEMM_MCAST, GEMM_SPLIT = 0, 1, 2, 3
+GEMM_SINGLE, GEMM_PAIR, GEMM_MCAST, GEMM_SPLIT, GEMM_TALL = 0, 1, 2, 3, 4
 
 
 def moe_set_gemm_pairing(mode: int) -> int:
-    """Tiling of the grouped GEMMs (GEMM_SINGLE / GEMM_PAIR / GEMM_MCAST / GEMM_SPLIT);
+    """Tiling of the grouped GEMMs (GEMM_SINGLE / GEMM_PAIR / GEMM_MCAST / GEMM_SPLIT /
+    GEMM_TALL);
     returns the previous mode."""
     return _check(lib().moe_set_gemm_pairing(int(mode)))
 

@@ -110,7 +110,8 @@ __host__ __device__ constexpr int stages_for_bytes(int stage_bytes) {
 // kConv > 0 (FP8 weights): the stage ring holds A and the raw weight codes
 // (kRawBytes a stage); the bf16 B tiles the MMA reads live in a second ring of
 // kConv stages, written by the converter warps.
-template <int kStages, int kBBytes, int kABytes = A_BYTES, int kConv = 0, int kRawBytes = 0>
+template <int kStages, int kBBytes, int kABytes = A_BYTES, int kConv = 0, int kRawBytes = 0,
+          int kEpiBytes = 4 * kStgBytes>
 struct Smem {
   static_assert(kStages >= 2, "stage ring too shallow");
   static constexpr int B_BYTES = kBBytes;
@@ -118,10 +119,11 @@ struct Smem {
   static constexpr int STAGE_A = 0;
   static constexpr int STAGE_RAW = kStages * kABytes;
   static constexpr int STAGE_B = STAGE_RAW + kStages * kRawBytes;
-  static constexpr int STAGE_EPI = STAGE_B + (kConv ? kConv : kStages) * B_BYTES;  // 4 staging buffers
-  static constexpr int BARS = STAGE_EPI + 4 * kStgBytes;
-  // full[kStages], empty[kStages], conv_full[kConv], conv_empty[kConv], tfull[2], tempty[2], drain
-  static constexpr int NBARS = 2 * kStages + 2 * kConv + 5;
+  static constexpr int STAGE_EPI = STAGE_B + (kConv ? kConv : kStages) * B_BYTES;  // staging buffers
+  static constexpr int BARS = STAGE_EPI + kEpiBytes;
+  // full[kStages], empty[kStages], conv_full[kConv], conv_empty[kConv], tfull[2], tempty[2],
+  // drain, tfull_tall
+  static constexpr int NBARS = 2 * kStages + 2 * kConv + 6;
   static constexpr int MISC = BARS + NBARS * 8;           // tmem slot, abort flag, scan scratch
   static constexpr int TILE_START = MISC + 64;            // int[kMaxGroups + 1]
   static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
@@ -142,14 +144,25 @@ struct Smem {
 //   kFp8B   B holds FP8 E4M3 weight codes with block scales: TMA brings A and the
 //           codes into the stage ring, eight converter warps write the scaled
 //           bf16 B tiles into a second ring, and the MMA reads A and that
+//   kTall   (single CTAs) the whole 256-row blocks of every group are tiles of 256
+//           rows: each k-step issues two M = 128 MMAs, rows 0-127 into one TMEM
+//           accumulator and rows 128-255 into the other, against the same B stage,
+//           so a stage's 32 KB of weights serve twice the rows and the per-SM
+//           shared-memory fill per MMA drops from 96 to 64 bytes a cycle.  The
+//           remaining rows of a group are 128-row tiles.  A tall tile holds both
+//           accumulators, so its epilogue runs on eight warps (one accumulator
+//           each for warps 2-5 and 6-9) to shorten the time it keeps them.
 template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false, int kARows = BM,
-          bool kFp8B = false>
+          bool kFp8B = false, bool kTall = false>
 struct Cfg {
   static_assert(kARows == BM || (!kPair && !kMcastA && !kGatherA && kARows % 8 == 0),
                 "short A tiles are single-CTA TMA tiles only");
   static_assert(!kFp8B || (!kPair && !kMcastA && !kGatherA), "FP8 weights: single-CTA tiles");
-  static constexpr int kTileM = kPair ? 2 * BM : kARows;          // product rows per tile
-  static constexpr int kABytes = kARows * BK * 2;                  // A bytes per stage
+  static_assert(!kTall || (!kPair && !kMcastA && !kGatherA && !kFp8B && kARows == BM &&
+                           kEpi != EPI_F32),
+                "tall tiles: single-CTA bf16 gate/up and down only");
+  static constexpr int kTileM = kPair ? 2 * BM : kARows;          // product rows per (short) tile
+  static constexpr int kABytes = (kTall ? 2 : 1) * kARows * BK * 2;  // A bytes per stage
   static constexpr int kBRowsCta = kPair ? kN / 2 : kN;           // B rows held per CTA
   static constexpr int kBBytes = kBRowsCta * BK * 2;
   static constexpr int kRawBytes = kFp8B ? kBRowsCta * BK : 0;    // FP8 codes per stage
@@ -161,15 +174,29 @@ struct Cfg {
   static constexpr int kBoxB = kPair ? kBRowsCta
                                      : ((kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128));
   static constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;  // output columns per tile
-  static constexpr int kThreadsT = kFp8B ? kThreadsFp8 : (kGatherA ? kThreadsGather : kThreads);
-  using S = Smem<kStages, kBBytes, kABytes, kConv, kRawBytes>;
+  static constexpr int kThreadsT =
+      kFp8B ? kThreadsFp8 : ((kGatherA || kTall) ? kThreadsGather : kThreads);
+  // epilogue: warps and the columns each stages per pass (32 rows x kEpiCols bf16)
+  static constexpr int kEpiWarps = kTall ? 8 : 4;
+  static constexpr int kEpiCols = kTall ? 32 : 64;
+  static constexpr int kStgWarp = 32 * kEpiCols * 2;
+  using S = Smem<kStages, kBBytes, kABytes, kConv, kRawBytes, kEpiWarps * kStgWarp>;
 };
 
 struct Tile {
   int g, row0, row_end, n0;
-  int pb;  // 0: the grouped problem, 1: the second (dense) problem
-  int ks;  // K range of a split-K unit (0 without split)
+  int pb;    // 0: the grouped problem, 1: the second (dense) problem
+  int ks;    // K range of a split-K unit (0 without split)
+  int tall;  // 1: a 256-row tile (kTall)
 };
+
+// M tiles of a group of `rows` rows: ceil(rows / tile_m), or with tall tiles
+// the whole 256-row blocks plus ceil(remainder / 128)
+__device__ __forceinline__ int group_m_tiles(int rows, int tile_m, bool tall) {
+  if (rows <= 0) return 0;
+  if (tall) return rows / 256 + ((rows % 256) + BM - 1) / BM;
+  return (rows + tile_m - 1) / tile_m;
+}
 
 // rows of group g this launch covers: all of them, the leading whole 256-row
 // blocks (split 1) or the remainder after them (split 2)
@@ -183,7 +210,7 @@ __device__ __forceinline__ void group_range(const int* goff, int g, int split, i
 
 __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, const int* goff,
                                             int G, int n_tiles, int bn_out, int tile_m,
-                                            int split) {
+                                            int split, bool tall = false) {
   int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -200,6 +227,18 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, con
   t.n0 = n * bn_out;
   t.pb = 0;
   t.ks = 0;
+  t.tall = 0;
+  if (tall) {  // the group's whole 256-row blocks first, then its 128-row tiles
+    const int n_tall = (r1 - r0) / 256;
+    if (m < n_tall) {
+      t.row0 = r0 + 256 * m;
+      t.row_end = t.row0 + 256;
+      t.tall = 1;
+    } else {
+      t.row0 = r0 + 256 * n_tall + BM * (m - n_tall);
+      t.row_end = min(r1, t.row0 + BM);
+    }
+  }
   return t;
 }
 
@@ -217,7 +256,7 @@ struct Sched2 {
 
 __device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const int* goff, int G,
                                             int n_tiles, int bn_out, int tile_m, int split,
-                                            const Sched2& s2) {
+                                            const Sched2& s2, bool tall = false) {
   if (s2.extra > 0 && i >= s2.routed) {
     const int q = i - s2.routed;
     const int m = q / s2.n2_tiles;
@@ -228,16 +267,19 @@ __device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const 
     t.n0 = (q - m * s2.n2_tiles) * bn_out;
     t.pb = 1;
     t.ks = 0;
+    t.tall = 0;
     return t;
   }
-  return decode_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split);
+  return decode_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split, tall);
 }
 
 // split-K units (f32 epilogue): schedule index i is K range i % ksplit of tile i / ksplit
 __device__ __forceinline__ Tile locate_unit(int i, int ksplit, const int* tile_start,
                                             const int* goff, int G, int n_tiles, int bn_out,
-                                            int tile_m, int split, const Sched2& s2) {
-  if (ksplit <= 1) return locate_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2);
+                                            int tile_m, int split, const Sched2& s2,
+                                            bool tall = false) {
+  if (ksplit <= 1)
+    return locate_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2, tall);
   const int q = i / ksplit;
   Tile t = locate_tile(q, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2);
   t.ks = i - q * ksplit;
@@ -288,14 +330,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kMcastA: a cluster of two CTAs computes the same 128 A rows against two
 // neighbouring N tiles; each CTA loads half of the A tile and multicasts it to
 // both, and each stage is released only when both MMAs are done with it.
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA, int kARows, bool kFp8B>
-__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>::kThreadsT,
-                                  1)
+// kTall: tmA2 is the A matrix with 256-row boxes (tall tiles); no second problem.
+template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA, int kARows, bool kFp8B,
+          bool kTall>
+__global__ void __launch_bounds__(
+    Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>::kThreadsT, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>;
   constexpr bool kCluster = kPair || kMcastA;
   using S = typename C::S;
   constexpr int kABytes = C::kABytes;
@@ -312,6 +356,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   constexpr int kTmemCols = 2 * kN;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPair ? 2 * BM : BM, kN);
   constexpr uint32_t kStageTx = (kGatherA ? 0 : kABytes) + (kFp8B ? S::RAW_BYTES : S::B_BYTES);
+  constexpr int kEpiCols = C::kEpiCols;
+  constexpr int kStgWarp = C::kStgWarp;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -338,6 +384,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 * kConv + a); };
   auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 2 + a); };
   const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 4);
+  // tall tiles signal their second accumulator here, not on tfull(1): warps
+  // 6-9 drain only tall tiles, and a barrier whose phases also advanced for the
+  // short tiles warps 2-5 drain from that slot would let their parity wait
+  // pass on a short tile's completion
+  const uint32_t bar_tfull_tall = ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 5);
 
   count_launch(p.launches, p.kid);
 
@@ -356,13 +407,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       ptx::mbar_init(bar_tempty(a), kPair ? 2 * BM : BM);
     }
     ptx::mbar_init(bar_drain, 1);
+    ptx::mbar_init(bar_tfull_tall, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
-    if (p.P2 > 0) {
+    if (p.P2 > 0 || kTall) {
       ptx::tma_prefetch_desc(&tmA2);
       ptx::tma_prefetch_desc(&tmB2);
     }
@@ -397,8 +449,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   for (int g = g_lo; g < g_hi; ++g) {
     int r0, r1;
     group_range(goff, g, p.split, r0, r1);
-    const int rows = r1 - r0;
-    local += rows > 0 ? ((rows + kTileM - 1) / kTileM) * n_tiles : 0;
+    local += group_m_tiles(r1 - r0, kTileM, kTall) * n_tiles;
   }
   int incl = local;
 #pragma unroll
@@ -419,8 +470,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     tile_start[g] = run;
     int r0, r1;
     group_range(goff, g, p.split, r0, r1);
-    const int rows = r1 - r0;
-    run += rows > 0 ? ((rows + kTileM - 1) / kTileM) * n_tiles : 0;
+    run += group_m_tiles(r1 - r0, kTileM, kTall) * n_tiles;
   }
   if (threadIdx.x == 0) tile_start[G] = total;
   ptx::tc_fence_before();
@@ -503,10 +553,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
         Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
-                             p.split, s2);
+                             p.split, s2, kTall);
         t.n0 += n_off;
-        const bool second = kCan2 && t.pb == 1;
-        const CUtensorMap* mA = second ? &tmA2 : &tmA;
+        const bool second = kCan2 && !kTall && t.pb == 1;
+        // tall tiles load 256 A rows through the 256-row map, short ones 128
+        const CUtensorMap* mA = (second || (kTall && t.tall)) ? &tmA2 : &tmA;
+        const uint32_t tx = (kTall && !t.tall) ? kStageTx - kABytes / 2 : kStageTx;
         const CUtensorMap* mB = second ? &tmB2 : &tmB;
         const int kb_lo = t.ks * nk_split;
         const int nk_t = second ? nk2 : min(nk, kb_lo + nk_split);
@@ -542,7 +594,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             continue;
           }
           const uint32_t fb = bar_full(stage);
-          ptx::mbar_arrive_expect_tx(fb, kStageTx);
+          ptx::mbar_arrive_expect_tx(fb, tx);
           if (kMcastA) {
             // this CTA's half of the A tile (64 rows), into both CTAs of the pair
             ptx::tma_load_2d_mcast(sa + rank * (kABytes / 2), &tmA, kb * BK,
@@ -580,12 +632,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t phase = 0;
       int cst = 0;             // FP8 weights: stage of the converted ring
       uint32_t cphase = 0;
-      int it = 0;
+      // accumulator slots: a tile takes slot `nxt` (alternating), a tall tile
+      // both; use counts per slot give the barrier phases (the epilogue keeps
+      // the same counts)
+      uint32_t uses0 = 0, uses1 = 0;
+      int nxt = 0;
       bool ok = true, any = false;
-      for (int tile = unit; ok && tile < total; tile += n_units, ++it) {
-        const int acc = it & 1;
-        const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
-        if (!wait_bar<kPair>(bar_tempty(acc), aphase ^ 1u, abort_flag, p.status)) {
+      for (int tile = unit; ok && tile < total; tile += n_units) {
+        const bool tall =
+            kTall && locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
+                                 p.split, s2, kTall).tall;
+        const int acc = nxt;
+        if (tall) {
+          if (!wait_bar(bar_tempty(0), (uses0 & 1u) ^ 1u, abort_flag, p.status) ||
+              !wait_bar(bar_tempty(1), (uses1 & 1u) ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+        } else if (!wait_bar<kPair>(bar_tempty(acc), ((acc ? uses1 : uses0) & 1u) ^ 1u,
+                                    abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -610,13 +675,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * kABytes);
           const uint64_t db = ptx::desc_kmajor_sw128(sbase + S::STAGE_B +
                                                      (kFp8B ? cst : stage) * S::B_BYTES);
+          if (tall) {
+            // rows 0-127 into slot 0, rows 128-255 (16 KB on in the stage) into slot 1
+            const uint64_t da1 =
+                ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * kABytes + kABytes / 2);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
-            if (kPair)
-              ptx::mma_bf16_pair(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
-            else
-              ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < BK / UMMA_K; ++k)
+              ptx::mma_bf16(tmem_base, da + 2ull * k, db + 2ull * k, kIdesc,
+                            (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k)
+              ptx::mma_bf16(tmem_base + static_cast<uint32_t>(kN), da1 + 2ull * k, db + 2ull * k,
+                            kIdesc, (kb | k) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
+              if (kPair)
+                ptx::mma_bf16_pair(d, da + 2ull * k, db + 2ull * k, kIdesc,
+                                   (kb | k) != 0 ? 1u : 0u);
+              else
+                ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           any = true;
           if (kPair) ptx::mma_commit_pair(bar_empty(stage), 3);
@@ -629,8 +709,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (kPair) ptx::mma_commit_pair(bar_tfull(acc), 3);
-        else ptx::mma_commit(bar_tfull(acc));
+        if (tall) {
+          ptx::mma_commit(bar_tfull(0));
+          ptx::mma_commit(bar_tfull_tall);
+          ++uses0;
+          ++uses1;
+          nxt = 0;
+        } else {
+          if (kPair) ptx::mma_commit_pair(bar_tfull(acc), 3);
+          else ptx::mma_commit(bar_tfull(acc));
+          if (acc) ++uses1;
+          else ++uses0;
+          nxt ^= 1;
+        }
       }
       if (!ok && any) {
         if (kPair) ptx::mma_commit_pair(bar_drain, 1);
@@ -638,24 +729,46 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         spin_bounded(bar_drain, 0);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + C::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
+    // kTall: warps 2-5 (group 0) and 6-9 (group 1) drain one accumulator each
+    // of a tall tile; short tiles are drained by group 0 alone
+    const int eg = kTall ? (warp - 2) >> 2 : 0;
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int r_in_tile = row_off + q * 32 + lane;
     const uint32_t tempty_leader =
         kPair ? ptx::mapa_shared(bar_tempty(0), 0) : 0u;  // + 8 * acc for buffer acc
-    int it = 0;
-    for (int tile = unit; tile < total; tile += n_units, ++it) {
+    // completions seen so far on each full barrier: slot 0 (every use), slot 1
+    // (short tiles), tall tiles' second accumulator; the slot choice mirrors the
+    // MMA issuer
+    uint32_t n0 = 0, n1 = 0, nt = 0;
+    int nxt = 0;
+    for (int tile = unit; tile < total; tile += n_units) {
       Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split,
-                           s2);
+                           s2, kTall);
       t.n0 += n_off;
       const bool second = kCan2 && t.pb == 1;
       const int n_out = second ? p.N2 : p.N;
-      const int acc = it & 1;
-      const uint32_t aphase = (static_cast<uint32_t>(it) >> 1) & 1u;
-      if (!wait_bar(bar_tfull(acc), aphase, abort_flag, p.status)) break;
+      const bool tall = kTall && t.tall;
+      const int acc = tall ? eg : nxt;
+      uint32_t fbar, aphase;
+      if (tall) {
+        fbar = eg ? bar_tfull_tall : bar_tfull(0);
+        aphase = (eg ? nt : n0) & 1u;
+        ++n0;
+        ++nt;
+        nxt = 0;
+      } else {
+        fbar = bar_tfull(acc);
+        aphase = (acc ? n1 : n0) & 1u;
+        if (acc) ++n1;
+        else ++n0;
+        nxt ^= 1;
+      }
+      if (kTall && !tall && eg == 1) continue;
+      if (!wait_bar(fbar, aphase, abort_flag, p.status)) break;
       ptx::tc_fence_after();
-      const int row = t.row0 + r_in_tile;
+      const int row = t.row0 + (tall ? eg * BM : 0) + r_in_tile;
       const bool valid = row < t.row_end;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kN);
@@ -666,7 +779,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // back so that eight lanes store one row's 128 contiguous bytes: full
         // 128-byte lines instead of 32 scattered 16-byte pieces per store.
         uint16_t* out = static_cast<uint16_t*>(second ? p.out2 : p.out);
-        const uint32_t stg = sbase + S::STAGE_EPI + static_cast<uint32_t>(warp - 2) * kStgBytes;
+        const uint32_t stg = sbase + S::STAGE_EPI + static_cast<uint32_t>(warp - 2) * kStgWarp;
+        constexpr int kH = kEpiCols / 32;        // 32-column TMEM loads per pass
+        constexpr int kPieces = kEpiCols / 8;    // 16-byte pieces of a staged row
+        constexpr int kRowsPer = 32 / kPieces;   // rows one store instruction covers
         int dst_row = row;
         float wgt = 1.0f;
         if (kEpi == EPI_DOWN && valid && !second) {
@@ -674,15 +790,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (p.pair_weight) wgt = __ldg(p.pair_weight + dst_row);
         }
 #pragma unroll 1
-        for (int c = 0; c < kBnOut / 64; ++c) {
-          uint32_t packed[32];
+        for (int c = 0; c < kBnOut / kEpiCols; ++c) {
+          uint32_t packed[kEpiCols / 2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < kH; ++h) {
             uint32_t g[32];
-            ptx::tmem_ld_32x32b_x32(taddr + c * 64 + h * 32, g);
+            ptx::tmem_ld_32x32b_x32(taddr + c * kEpiCols + h * 32, g);
             if (kEpi == EPI_GATEUP) {
               uint32_t u[32];
-              ptx::tmem_ld_32x32b_x32(taddr + kBnOut + c * 64 + h * 32, u);
+              ptx::tmem_ld_32x32b_x32(taddr + kBnOut + c * kEpiCols + h * 32, u);
               ptx::tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; j += 2) {
@@ -692,7 +808,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                   // narrowing before the activation: gate and up are rounded to bf16 first
                   const float gz = bf16_round(__uint_as_float(g[j + q2]));
                   const float uz = bf16_round(__uint_as_float(u[j + q2]));
-                  const float sl = gz / (1.0f + __expf(-gz));
+                  // SiLU is tolerance-checked, so the fast reciprocal division serves
+                  // (it gives the IEEE quotient's 0 where 1 + exp(-g) overflows)
+                  const float sl = __fdividef(gz, 1.0f + __expf(-gz));
                   a2[q2] = sl * uz;
                 }
                 packed[h * 16 + j / 2] = pack_bf16x2(a2[0], a2[1]);
@@ -710,25 +828,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               }
             }
           }
-          if (c == kBnOut / 64 - 1) {   // the accumulator is in registers: free it now
+          if (c == kBnOut / kEpiCols - 1) {  // the accumulator is in registers: free it now
             ptx::tc_fence_before();
             if (kPair && !leader) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
             else ptx::mbar_arrive(bar_tempty(acc));
           }
-          // row `lane` of the staging buffer, piece k at slot k ^ (lane & 7)
+          // row `lane` of the staging buffer, piece k at slot k ^ (lane % kPieces)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            ptx::st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4), packed[4 * k],
-                              packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+          for (int k = 0; k < kPieces; ++k)
+            ptx::st_shared_v4(stg + lane * (2 * kEpiCols) + ((k ^ (lane & (kPieces - 1))) << 4),
+                              packed[4 * k], packed[4 * k + 1], packed[4 * k + 2],
+                              packed[4 * k + 3]);
           __syncwarp();
-          const int col0 = t.n0 + c * 64;
+          const int col0 = t.n0 + c * kEpiCols;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {           // 4 rows per store instruction
-            const int r = i * 4 + (lane >> 3);     // row of the warp this lane stores
-            const int k = lane & 7;                // its 16-byte piece of that row
+          for (int i = 0; i < kPieces; ++i) {       // kRowsPer rows per store instruction
+            const int r = i * kRowsPer + lane / kPieces;  // row of the warp this lane stores
+            const int k = lane % kPieces;                 // its 16-byte piece of that row
             const int drow = __shfl_sync(0xffffffffu, dst_row, r);
             const int rvalid = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
-            const uint4 v = ptx::ld_shared_v4(stg + r * 128 + ((k ^ (r & 7)) << 4));
+            const uint4 v = ptx::ld_shared_v4(stg + r * (2 * kEpiCols) +
+                                              ((k ^ (r & (kPieces - 1))) << 4));
             const int col = col0 + k * 8;
             if (rvalid && col < n_out)
               *reinterpret_cast<uint4*>(out + static_cast<size_t>(drow) * n_out + col) = v;
@@ -920,12 +1040,12 @@ int num_sms() {
 // tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
 // grid is that many CTAs (pairs when paired), capped at the SM count
 template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
-          int kARows = BM, bool kFp8B = false>
+          int kARows = BM, bool kFp8B = false, bool kTall = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta2,
            const CUtensorMap& tb2, Params p, long long tile_bound, cudaStream_t stream) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>;
+  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>;
   constexpr bool kCluster = kPair || kMcastA;
-  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>;
   const int smem = C::S::ALLOC;
   // per instantiation and device, set once (racing threads set the same value)
   static std::atomic<int> configured_dev[64] = {};
@@ -1064,8 +1184,8 @@ extern "C" size_t moe_grouped_gemm_workspace_size(int, int, int, int) { return 0
 
 extern "C" int moe_set_gemm_pairing(int mode) {
   clear_error();
-  if (mode < MOE_GEMM_SINGLE || mode > MOE_GEMM_SPLIT)
-    return set_error(MOE_ERR_ARG, "moe_set_gemm_pairing: mode %d is not 0, 1, 2 or 3", mode);
+  if (mode < MOE_GEMM_SINGLE || mode > MOE_GEMM_TALL)
+    return set_error(MOE_ERR_ARG, "moe_set_gemm_pairing: mode %d is not 0, 1, 2, 3 or 4", mode);
   return g_pairing.exchange(mode);
 }
 
@@ -1140,6 +1260,13 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   if (narrow)
     return launch<128, EPI_GATEUP, false, false, false, kNarrowRows>(
         op, ta, tb, p, tile_bound(P, G, I, 64, kNarrowRows), s);
+  if (mode == MOE_GEMM_TALL && P >= 256) {
+    // whole 256-row blocks as tall tiles (A through 256-row boxes), the rest 128-row
+    CUtensorMap ta_tall;
+    if ((rc = make_tmap(&ta_tall, a_bf16, P, H, 2 * BM, op, "a")) != MOE_OK) return rc;
+    return launch<256, EPI_GATEUP, false, false, false, BM, false, true>(
+        op, ta, tb, ta_tall, tb, p, tile_bound(P, G, I, 128), s);
+  }
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
@@ -1196,6 +1323,12 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   if (narrow)
     return launch<256, EPI_DOWN, false, false, false, kNarrowRows>(
         op, ta, tb, p, tile_bound(P, G, H, 256, kNarrowRows), s);
+  if (mode == MOE_GEMM_TALL && P >= 256) {
+    CUtensorMap ta_tall;
+    if ((rc = make_tmap(&ta_tall, act_bf16, P, I, 2 * BM, op, "act")) != MOE_OK) return rc;
+    return launch<256, EPI_DOWN, false, false, false, BM, false, true>(
+        op, ta, tb, ta_tall, tb, p, tile_bound(P, G, H, 256), s);
+  }
   return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
 }
 

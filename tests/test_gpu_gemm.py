@@ -28,8 +28,8 @@ def _lib():
     assert m.moe_device_status() == 0
 
 
-@pytest.fixture(params=[m.GEMM_SINGLE, m.GEMM_MCAST, m.GEMM_PAIR, m.GEMM_SPLIT],
-                ids=["single", "mcast", "pair", "split"])
+@pytest.fixture(params=[m.GEMM_SINGLE, m.GEMM_MCAST, m.GEMM_PAIR, m.GEMM_SPLIT, m.GEMM_TALL],
+                ids=["single", "mcast", "pair", "split", "tall"])
 def pairing(request):
     """Every tiling of the grouped GEMMs: single CTAs (the default), A-multicast
     clusters, CTA pairs (2-SM, 256-row tiles), and whole 256-row blocks on CTA

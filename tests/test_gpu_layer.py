@@ -189,13 +189,13 @@ def test_gemm_tilings_agree_on_prefill():
     res = {}
     prev = m.moe_set_gemm_pairing(m.GEMM_SINGLE)
     try:
-        for mode in (m.GEMM_SINGLE, m.GEMM_PAIR, m.GEMM_MCAST, m.GEMM_SPLIT):
+        for mode in (m.GEMM_SINGLE, m.GEMM_PAIR, m.GEMM_MCAST, m.GEMM_SPLIT, m.GEMM_TALL):
             m.moe_set_gemm_pairing(mode)
             res[mode] = (to_host(blk.forward(x)).copy(), to_host(blk.act).copy())
     finally:
         m.moe_set_gemm_pairing(prev)
     ref_out, ref_act = res[m.GEMM_SINGLE]
-    for mode in (m.GEMM_PAIR, m.GEMM_MCAST, m.GEMM_SPLIT):
+    for mode in (m.GEMM_PAIR, m.GEMM_MCAST, m.GEMM_SPLIT, m.GEMM_TALL):
         out, act = res[mode]
         assert nmse_maxrel(bf16_to_f64(act), bf16_to_f64(ref_act))[0] <= 1e-6
         assert nmse_maxrel(bf16_to_f64(out), bf16_to_f64(ref_out))[0] <= 1e-6
