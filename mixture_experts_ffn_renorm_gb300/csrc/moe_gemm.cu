@@ -318,13 +318,10 @@ __device__ __forceinline__ void spin_bounded(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ float bf16_round(float v) {
-  return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(v)) << 16);
-}
-
+// two values rounded to bf16 (nearest even) in one conversion, lo in the low half
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(f32_to_bf16_bits(lo)) |
-         (static_cast<uint32_t>(f32_to_bf16_bits(hi)) << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // kMcastA: a cluster of two CTAs computes the same 128 A rows against two
@@ -806,8 +803,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
                   // narrowing before the activation: gate and up are rounded to bf16 first
-                  const float gz = bf16_round(__uint_as_float(g[j + q2]));
-                  const float uz = bf16_round(__uint_as_float(u[j + q2]));
+                  const uint32_t gu =
+                      pack_bf16x2(__uint_as_float(g[j + q2]), __uint_as_float(u[j + q2]));
+                  const float gz = __uint_as_float(gu << 16);
+                  const float uz = __uint_as_float(gu & 0xFFFF0000u);
                   // SiLU is tolerance-checked, so the fast reciprocal division serves
                   // (it gives the IEEE quotient's 0 where 1 + exp(-g) overflows)
                   const float sl = __fdividef(gz, 1.0f + __expf(-gz));
