@@ -217,10 +217,19 @@ def test_host_batches_pipeline_matches_eager():
         assert np.array_equal(o.view(torch.int16).numpy().view(np.uint16), w_)
 
 
-def test_graph_replay_matches_eager():
+@pytest.mark.parametrize("weights", ["bf16", "q4_k"])
+def test_graph_replay_matches_eager(weights):
+    # the forward allocates nothing, so it replays from a CUDA graph bit for bit
+    # (keep-quant experts included: their quantizers write preallocated planes)
     cfg = W.DECODE
-    d = W.layer_inputs(cfg)
-    blk = _block(cfg, d)
+    if weights == "bf16":
+        d = W.layer_inputs(cfg)
+        blk = _block(cfg, d)
+    else:
+        d = W.layer_inputs(cfg, with_weights=False)
+        d.update(W.layer_q_weights(cfg, weights))
+        blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                       I_shared=cfg.I_shared, qweights=weights)
     x = to_dev(d["x"])
     eager = to_host(blk.forward(x)).copy()
     blk.capture(x)
