@@ -103,20 +103,39 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
   float my_sel = 0.0f;
   int my_id = 0;
   if (live) {
-    // n_part K-range partial sums of each logit, added in range order, then the bias
+    // n_part K-range partial sums of each logit, added in range order, then the
+    // bias.  The loads of kQ ranges (at most 16, the largest split) are issued
+    // before their additions, so that a K split costs a few memory round trips
+    // rather than one per range.
+    constexpr int kLoads = kEx ? 16 : 32;  // loads in flight per lane
+    constexpr int kQ = kPerLane >= kLoads ? 1 : (kLoads / kPerLane > 16 ? 16 : kLoads / kPerLane);
     const float* row = logits + static_cast<size_t>(t) * E;
     const size_t slab = static_cast<size_t>(T) * E;
+    for (int q0 = 0; q0 < n_part; q0 += kQ) {
+      float part[kQ][kPerLane];
+#pragma unroll
+      for (int j = 0; j < kQ; ++j)
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+          const int e = lane + 32 * i;
+          part[j][i] = (q0 + j < n_part && e < E) ? __ldg(row + (q0 + j) * slab + e) : 0.0f;
+        }
+#pragma unroll
+      for (int j = 0; j < kQ; ++j)
+        if (q0 + j < n_part)
+#pragma unroll
+          for (int i = 0; i < kPerLane; ++i)
+            v[i] = q0 + j == 0 ? part[j][i] : __fadd_rn(v[i], part[j][i]);
+    }
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
       const int e = lane + 32 * i;
-      float a = 0.0f;
       if (e < E) {
-        a = __ldg(row + e);
-        for (int q = 1; q < n_part; ++q) a = __fadd_rn(a, __ldg(row + q * slab + e));
-        if (bias) a = __fadd_rn(a, __ldg(bias + e));
-        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = a;
+        if (bias) v[i] = __fadd_rn(v[i], __ldg(bias + e));
+        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = v[i];
+      } else {
+        v[i] = 0.0f;
       }
-      v[i] = a;
     }
     uint32_t key[kPerLane];
     float sc[kPerLane];      // what a chosen expert reports: its logit, or its sigmoid score
