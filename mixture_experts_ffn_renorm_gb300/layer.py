@@ -86,6 +86,9 @@ class MoeBlock:
             raise ValueError("FP8 expert weights read x_perm rows (gather=False)")
         self.routed_scale = float(routed_scale)
         self.device = torch.device(device)
+        if self.device.type != "cuda":
+            # every step runs in the library's CUDA kernels, which take device pointers
+            raise ValueError(f"MoeBlock needs a CUDA device, not {self.device}; there is no CPU path")
         dv = self.device
         self.w_router = _dev_bf16(weights["w_router"], dv)
         if fp8_weights:
