@@ -151,3 +151,26 @@ def test_keep_quant_entry_points_refuse_without_touching_the_device(lib):
     # P = 0 is a no-op
     assert lib.moe_grouped_gemm_q(None, None, 0, None, 1, None, m.QFMT_Q8_0, None, 0, 256, 8, 1,
                                   None, None) == m.OK
+
+
+def test_block_expansion_refuses_without_touching_the_device(lib):
+    # the bf16 expansion of keep-quant blocks checks format, sizes and alignment first
+    import ctypes
+    buf = (ctypes.c_uint8 * 4096)()
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(a.value + 1)        # 1-byte aligned
+    two = ctypes.c_void_p(a.value + 2)        # 2-byte aligned, not 16
+    assert lib.moe_dequantize_q_bf16(a, 3, 1, 256, a, None) == m.ERR_ARG
+    assert "qfmt" in m.last_error()
+    assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q8_0, -1, 32, a, None) == m.ERR_ARG
+    assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q8_0, 1, 0, a, None) == m.ERR_ARG
+    assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q8_0, 1, 48, a, None) == m.ERR_ALIGN
+    assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q4_K, 1, 128, a, None) == m.ERR_ALIGN
+    assert lib.moe_dequantize_q_bf16(None, m.QFMT_Q4_K, 1, 256, a, None) == m.ERR_ARG
+    assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q4_K, 1, 256, None, None) == m.ERR_ARG
+    # Q4_K blocks and the output want 16-byte alignment; Q8_0 blocks only 2-byte
+    assert lib.moe_dequantize_q_bf16(two, m.QFMT_Q4_K, 1, 256, a, None) == m.ERR_ALIGN
+    assert lib.moe_dequantize_q_bf16(odd, m.QFMT_Q8_0, 1, 32, a, None) == m.ERR_ALIGN
+    assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q8_0, 1, 32, two, None) == m.ERR_ALIGN
+    # no rows is a no-op, whatever the pointers
+    assert lib.moe_dequantize_q_bf16(None, m.QFMT_Q8_0, 0, 32, None, None) == m.OK
