@@ -419,16 +419,25 @@ int moe_set_pdl(int enable);
  * row_to_pair ? row_to_pair[r] : r of out bf16 [P, H] (a dst outside [0, P) is
  * skipped).
  *
- * moe_dequantize_q_bf16 -- keep-quant weight rows expanded to bf16 [rows, K],
- * for batches with many rows per expert, which run faster on the bf16
- * tensor-core GEMMs: each value formed in binary32 and rounded to bf16 once,
- *   Q8_0: bf16(d * q)        Q4_K: bf16((d * sc_j) * q - dmin * m_j)
- * (exact products, one rounded subtraction).  Bit-exact.  w: Q4_K blocks
- * 16-byte aligned, Q8_0 blocks 2-byte aligned; out 16-byte aligned; K a
- * multiple of the block.
+ * Errors of the quantizer and the three GEMMs: MOE_ERR_ARG (qfmt, sizes, NULL
+ * operands), MOE_ERR_ALIGN (alignment; quantizer K not a multiple of its
+ * block; GEMM K not a multiple of 256 or above 16384), MOE_ERR_CUDA.  No
+ * workspace.
  *
- * Errors: MOE_ERR_ARG (qfmt, sizes, NULL operands), MOE_ERR_ALIGN (alignment,
- * K not a multiple of 256 or above 16384), MOE_ERR_CUDA.  No workspace.
+ * moe_dequantize_q_bf16 -- keep-quant weight rows expanded to bf16, for
+ * batches with many rows per expert, which run faster on the bf16 tensor-core
+ * GEMMs: each value formed in binary32 and rounded to bf16 once,
+ *   Q8_0: bf16(d * q)        Q4_K: bf16((d * sc_j) * q - dmin * m_j)
+ * (exact products, one rounded subtraction).  Bit-exact.
+ *   w      uint8 [rows, K / block * bytes]: any stack of weight rows, e.g. a
+ *          whole [G, R, K] matrix as rows = G * R; Q4_K blocks 16-byte
+ *          aligned, Q8_0 blocks 2-byte aligned
+ *   qfmt   MOE_QFMT_Q8_0 or MOE_QFMT_Q4_K
+ *   rows   >= 0 (0: no-op); K >= 1, a multiple of the block (32 or 256)
+ *   out    bf16 [rows, K] out, 16-byte aligned
+ * Errors: MOE_ERR_ARG (qfmt, rows < 0, K < 1, NULL operands, more than
+ * 2^31 - 1 launch blocks), MOE_ERR_ALIGN (alignment, K not a multiple of the
+ * block), MOE_ERR_CUDA.  No workspace.
  * ---------------------------------------------------------------------- */
 enum { MOE_QFMT_Q8_0 = 1, MOE_QFMT_Q4_K = 2 };
 int moe_quantize_act_q8(const void* x_bf16, int R, int K, int qfmt, int8_t* codes, float* scales,
