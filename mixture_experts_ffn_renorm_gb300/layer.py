@@ -247,16 +247,6 @@ class MoeBlock:
         return out
 
     # launches per forward (for the bench's gpu_launches claim)
-    def kernels_per_forward(self) -> int:
-        n = 2 + (3 if self.gather else 4) + 3  # route (2), permute (3 or 4), 2 GEMMs, combine
-        if self.has_shared:
-            n += 1  # the combine-gate's sigmoid pass
-        if self.has_shared and not self.fuse_shared:
-            n += 2
-        if self.qfmt:
-            n += 2  # the two activation quantizers
-        return n
-
     def capture(self, x_static):
         """Record one forward over the fixed input buffer ``x_static`` into a CUDA graph."""
         s = torch.cuda.Stream(device=self.device)
