@@ -94,7 +94,7 @@ def test_router_gemm_logits_within_bound_and_selection_exact(T, H, E, K):
 
 
 @pytest.mark.parametrize("T,H,E", [(16, 2048, 128), (1, 4096, 256), (2048, 4096, 256),
-                                   (40, 200, 96)])
+                                   (40, 200, 96), (64, 1024, 32), (64, 320, 20)])
 def test_router_k_split_matches_unsplit_within_bound(T, H, E):
     # with a workspace the logits GEMM splits K into ranges whose partial sums
     # the selection adds in range order (then the bias); without one it runs
