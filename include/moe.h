@@ -118,6 +118,14 @@ int moe_abi_version(void);  /* 8 */
  *                selection adds them in range order, then the bias.  It uses as
  *                many ranges as the workspace holds (one: no split), so a
  *                smaller workspace only costs speed.
+ * Errors: MOE_ERR_ARG (T < 0; E outside [1, 1024]; K outside [1, min(E, 32)];
+ * renormalize not 0 or 1; NULL topk_ids or topk_w; no x or w_router without
+ * logits_in; w_shared_gate without x or gate_logit_out), MOE_ERR_ALIGN (H not a
+ * positive multiple of 8 where x is read; x, w_router, w_shared_gate or the
+ * workspace not 16-byte aligned), MOE_ERR_UNSUPPORTED (scoring != 0 or
+ * n_group != 1; the message points to moe_route_topk_ex), MOE_ERR_WORKSPACE (the
+ * logits GEMM runs with neither logits_out nor room for T*E logits),
+ * MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 int moe_route_topk(const void* x_bf16, const void* w_router_bf16, const float* logit_bias,
                    const void* w_shared_gate_bf16, const float* logits_in, int T, int H, int E,
@@ -153,6 +161,12 @@ size_t moe_route_topk_workspace_size(int T, int E, int K);
  *   K            <= topk_group * E / n_group (and the limits of moe_route_topk)
  *   the other arguments, outputs, workspace and errors as moe_route_topk;
  *   MOE_ERR_UNSUPPORTED for scoring > 1 or a select_bias with softmax.
+ * Errors: those of moe_route_topk, except that scoring 1 and n_group > 1 are
+ * accepted; MOE_ERR_UNSUPPORTED (scoring not 0 or 1; a select_bias with softmax
+ * scoring), MOE_ERR_ARG (n_group not dividing E or above 64; topk_group outside
+ * [1, n_group]; group_score not 0 or 1; two-best group scores with one expert
+ * per group; K above the experts of the eligible groups), MOE_ERR_ALIGN
+ * (select_bias not 4-byte aligned).
  * ---------------------------------------------------------------------- */
 int moe_route_topk_ex(const void* x_bf16, const void* w_router_bf16, const float* logit_bias,
                       const float* select_bias, const void* w_shared_gate_bf16,
@@ -178,6 +192,12 @@ int moe_route_topk_ex(const void* x_bf16, const void* w_router_bf16, const float
  *   x_perm         bf16 [P,H] out or NULL: x_perm[row] = x[sorted_pair[row] / K]
  *   T >= 0, 1 <= K <= 32, 1 <= E <= 1024, H multiple of 8 when x != NULL
  *   workspace      >= moe_permute_workspace_size(T, K, E) bytes
+ * Errors: MOE_ERR_ARG (T < 0; K outside [1, 32]; E outside [1, 1024]; T*K too
+ * large; NULL topk_ids, expert_offsets, sorted_pair or pair_to_row; x_perm
+ * without x or H > 0), MOE_ERR_ALIGN (x or x_perm not 16-byte aligned, H not a
+ * multiple of 8), MOE_ERR_WORKSPACE (below moe_permute_workspace_size),
+ * MOE_ERR_CUDA.  An id outside [0, E) is skipped on the device and sets
+ * MOE_STATUS_BAD_ID in the status word (moe_device_status).
  * ---------------------------------------------------------------------- */
 int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, int K, int E, int H,
                 int32_t* expert_offsets, int32_t* sorted_pair, int32_t* pair_to_row,
@@ -232,6 +252,12 @@ int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int 
  *   act          bf16 [P,I] out; rows outside every group are not written
  *   P >= 0, H > 0 and I > 0 multiples of 64, 1 <= G <= 1024
  *   workspace    >= moe_grouped_gemm_workspace_size(...) bytes (currently 0)
+ * Errors: MOE_ERR_ARG (P < 0; a non-positive dimension; G outside [1, 1024];
+ * NULL operands; NULL group_offsets with G > 1; gathering with a_rows < 1 or
+ * gather_div < 1), MOE_ERR_ALIGN (operands not 16-byte aligned; H or I not a
+ * multiple of 8), MOE_ERR_CUDA (tensor-map encoding, shared-memory reservation
+ * or launch).  A device-side wait that runs past its limit sets
+ * MOE_STATUS_TIMEOUT in the status word (moe_device_status).
  * ---------------------------------------------------------------------- */
 int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows, const int32_t* a_row_gather,
                                       int gather_div, const void* w13_bf16,
@@ -255,6 +281,7 @@ int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows, const int3
  *   row_to_pair  int32 [P] or NULL (store in row order)
  *   out          bf16 [P,H] out (pair order when row_to_pair is set, i.e. [T,K,H])
  *   P >= 0, H > 0 and I > 0 multiples of 64, 1 <= G <= 1024
+ * Errors: those of moe_grouped_gemm_gateup_silu_bf16 (no gather here).
  * ---------------------------------------------------------------------- */
 int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,
                                const int32_t* group_offsets, const float* pair_weight,
@@ -473,6 +500,10 @@ int moe_dequantize_q_bf16(const uint8_t* w, int qfmt, long long rows, int K, voi
  *   shared      [T,H] f32 or bf16 (sh_dtype) or NULL
  *   out         [T,H] f32 or bf16 (out_dtype)
  *   T >= 0, 1 <= K <= 64, H > 0 multiple of 8
+ * Errors: MOE_ERR_DTYPE (a dtype other than f32 or bf16; f16 is named),
+ * MOE_ERR_ARG (T < 0; K outside [1, 64]; H <= 0; T*H too large; NULL expert_out
+ * or out), MOE_ERR_ALIGN (H not a multiple of 8; expert_out, shared or out not
+ * 16-byte aligned), MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 int moe_combine(const void* expert_out, int eo_dtype, const float* w, const void* shared,
                 int sh_dtype, float routed_scale, int T, int K, int H, void* out, int out_dtype,
@@ -491,6 +522,9 @@ int moe_combine(const void* expert_out, int eo_dtype, const float* w, const void
  * the T sigmoids are evaluated first by a small kernel and the stream reads
  * them (faster: the sigmoid is a chain of double-precision operations); without
  * one each block evaluates the sigmoids of its tokens itself.  Same bits.
+ * Errors: those of moe_combine (sd and gl required), MOE_ERR_WORKSPACE and
+ * MOE_ERR_ALIGN for a workspace below moe_gate_workspace_size or not 16-byte
+ * aligned.
  * ---------------------------------------------------------------------- */
 int moe_combine_gate(const void* expert_out, int eo_dtype, const float* w, const void* sd,
                      int sd_dtype, const float* gl, float routed_scale, int T, int K, int H,
@@ -501,6 +535,9 @@ int moe_combine_gate(const void* expert_out, int eo_dtype, const float* w, const
  *   out[t,c] = sigmoid(gl[t]) * sd[t,c], one rounding to out_dtype.
  * Four dtype arms: sd f32/bf16 x out f32/bf16.  Bit-exact.  workspace as
  * for moe_combine_gate (NULL allowed).
+ * Errors: MOE_ERR_DTYPE, MOE_ERR_ARG (T < 0; H <= 0; NULL sd, gl or out),
+ * MOE_ERR_ALIGN (H not a multiple of 8; sd or out not 16-byte aligned; the
+ * workspace), MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 int shared_expert_gate(const void* sd, int sd_dtype, const float* gl, int T, int H, void* out,
                        int out_dtype, void* workspace, size_t ws_bytes, void* stream);
