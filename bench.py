@@ -421,6 +421,122 @@ def run_combine_only(args):
     return 0
 
 
+def timed_steps(blk, x_dev, steps, flush):
+    """Mean step time in ms over `steps` forwards on the current stream.  With a
+    flush buffer, L2 is flushed before every step and the flush is left out of
+    the time (events at each step's first and last stage); without, the steps
+    run back to back with no event between their kernels, so each kernel may
+    start under programmatic dependent launch while its predecessor drains."""
+    import torch
+
+    step_marks = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+            marks = []
+            blk.forward(x_dev, marks=marks, stages=False)
+            step_marks.append(marks)
+        else:
+            blk.forward(x_dev)
+    t_end.record()
+    torch.cuda.synchronize()
+    if flush is None:
+        return t_start.elapsed_time(t_end) / steps
+    return sum(mk[0][1].elapsed_time(mk[-1][1]) for mk in step_marks) / steps
+
+
+def stage_breakdown(blk, x_dev, steps, flush):
+    """The same steps with an event after every stage: mean ms per stage."""
+    import torch
+
+    stage_ms = {}
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        marks = []
+        blk.forward(x_dev, marks=marks)
+        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
+            stage_ms.setdefault(name, []).append((a, b))
+    torch.cuda.synchronize()
+    return {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in stage_ms.items()}
+
+
+def gemm_account(cfg, counts, stage_avg, pk, fp8=False, qw=None, qd=False):
+    """Algorithmic FLOPs and bytes of the two grouped GEMMs of one forward, their
+    rates from the per-stage times, and which roof binds the gate/up GEMM."""
+    P = cfg.T * cfg.K
+    touched = int((counts > 0).sum())
+    flop_gateup = 2.0 * P * cfg.H * 2 * cfg.I
+    flop_down = 2.0 * P * cfg.I * cfg.H
+    wb = 1 if fp8 else 2          # bytes per expert weight (FP8 adds one f32 per 128x128 block)
+    sc = 4.0 / (128 * 128) if fp8 else 0.0
+    a_in = 2.0                    # bytes per activation element read by a GEMM
+    if qw and not qd:             # GGUF blocks; 8-bit activation codes plus one f32 per block
+        _, qblk, qbytes = Q_WEIGHTS[qw]
+        wb, sc, a_in = qbytes / qblk, 0.0, 1.0 + 4.0 / qblk
+    bytes_gateup = touched * 2 * cfg.I * cfg.H * (wb + sc) + P * cfg.H * a_in + P * cfg.I * 2
+    bytes_down = touched * cfg.H * cfg.I * (wb + sc) + P * cfg.I * a_in + P * cfg.H * 2 + P * 4
+    if cfg.I_shared:              # the shared expert runs inside the same two launches
+        flop_gateup += 2.0 * cfg.T * cfg.H * 2 * cfg.I_shared
+        flop_down += 2.0 * cfg.T * cfg.I_shared * cfg.H
+        bytes_gateup += 2 * cfg.I_shared * cfg.H * 2 + cfg.T * cfg.I_shared * 2
+        bytes_down += cfg.H * cfg.I_shared * 2 + cfg.T * cfg.I_shared * 2 + cfg.T * cfg.H * 2
+    t_gu = stage_avg["gemm_gateup"] / 1000.0
+    t_dn = stage_avg["gemm_down"] / 1000.0
+    qk = bool(qw) and not qd      # the keep-quant kernels run (CUDA cores, against HBM)
+    tensor_bound = (not qk and flop_gateup / (pk["bf16_tflops"] * 1e12)
+                    >= bytes_gateup / (pk["hbm_gbs"] * 1e9))
+    return {
+        "touched": touched, "flop_gateup": flop_gateup, "flop_down": flop_down,
+        "bytes_gateup": bytes_gateup, "bytes_down": bytes_down, "t_gu": t_gu, "t_dn": t_dn,
+        "qk": qk, "tensor_bound": tensor_bound,
+        "gemm_gateup_tflops": flop_gateup / t_gu / 1e12,
+        "gemm_gateup_gbs": bytes_gateup / t_gu / 1e9,
+        "gemm_down_tflops": flop_down / t_dn / 1e12,
+        "gemm_down_gbs": bytes_down / t_dn / 1e9,
+    }
+
+
+def extra_layer(name, dev, steps, warmup, pk):
+    """One more full-size workload (decode or the large layer) timed like the
+    headline one: step time with L2 flushed between steps, per-stage times,
+    and each GEMM's rate against the roof that binds it."""
+    import torch
+
+    from mixture_experts_ffn_renorm_gb300 import workloads as W
+    from mixture_experts_ffn_renorm_gb300.layer import MoeBlock
+
+    cfg = layer_config(name)
+    d = W.layer_inputs(cfg)
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
+                   I_shared=cfg.I_shared)
+    x_dev = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        blk.forward(x_dev)
+    torch.cuda.synchronize()
+    step_ms = timed_steps(blk, x_dev, steps, flush)
+    stage_avg = stage_breakdown(blk, x_dev, steps, flush)
+    counts = np.diff(blk.expert_offsets.cpu().numpy())
+    g = gemm_account(cfg, counts, stage_avg, pk)
+    out = {"workload": cfg.name, "step_us": 1000.0 * step_ms,
+           "tokens_per_s": cfg.T / (step_ms / 1000.0),
+           "stages_us": {k: 1000.0 * v for k, v in stage_avg.items()},
+           "touched_experts": g["touched"],
+           "gemm_gateup_gbs": g["gemm_gateup_gbs"], "gemm_down_gbs": g["gemm_down_gbs"],
+           "gemm_gateup_frac_hbm": g["gemm_gateup_gbs"] / pk["hbm_gbs"],
+           "gemm_down_frac_hbm": g["gemm_down_gbs"] / pk["hbm_gbs"],
+           "gemm_gateup_tflops": g["gemm_gateup_tflops"],
+           "gemm_down_tflops": g["gemm_down_tflops"],
+           "l2": "flushed between steps (256 MB write), flush not timed"}
+    del blk, flush, x_dev, d
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -470,30 +586,13 @@ def run_ours(args):
     # between the kernels of a step, so each may start under programmatic
     # dependent launch while its predecessor drains)
     counts0 = m.moe_launch_counts()
-    step_marks = []
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev) as clk:
         barrier(ws)
         torch.cuda.synchronize()
-        t_start.record()
-        for _ in range(args.steps):
-            if flush is not None:
-                flush.zero_()
-                marks = []
-                blk.forward(x_dev, marks=marks, stages=False)
-                step_marks.append(marks)
-            else:
-                blk.forward(x_dev)
-        t_end.record()
-        torch.cuda.synchronize()
+        step_ms = timed_steps(blk, x_dev, args.steps, flush)
         barrier(ws)
     counts1 = m.moe_launch_counts()
     launches = sum(b - a for a, b in zip(counts0, counts1))
-    if flush is None:
-        step_ms = t_start.elapsed_time(t_end) / args.steps
-    else:  # the L2 flush between steps is not part of a step
-        step_ms = sum(mk[0][1].elapsed_time(mk[-1][1]) for mk in step_marks) / args.steps
     ms = max_over_ranks(step_ms, ws, dev)
     from mixture_experts_ffn_renorm_gb300 import dp
 
@@ -501,16 +600,7 @@ def run_ours(args):
 
     # ---------------- per-stage breakdown: the same steps with an event after
     # every stage (reported as components; not the headline)
-    stage_ms = {}
-    for _ in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        marks = []
-        blk.forward(x_dev, marks=marks)
-        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
-            stage_ms.setdefault(name, []).append((a, b))
-    torch.cuda.synchronize()
-    stage_avg = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in stage_ms.items()}
+    stage_avg = stage_breakdown(blk, x_dev, args.steps, flush)
 
     # ---------------- end to end through the public API with host buffers:
     # every step copies its tokens in from pinned host memory and its output
@@ -536,23 +626,11 @@ def run_ours(args):
     pk, pk_src = peaks()
     P = cfg.T * cfg.K
     counts = np.diff(blk.expert_offsets.cpu().numpy())
-    touched = int((counts > 0).sum())
-    flop_gateup = 2.0 * P * cfg.H * 2 * cfg.I
-    flop_down = 2.0 * P * cfg.I * cfg.H
-    wb = 1 if fp8 else 2          # bytes per expert weight (FP8 adds one f32 per 128x128 block)
-    sc = 4.0 / (128 * 128) if fp8 else 0.0
-    a_in = 2.0                    # bytes per activation element read by a GEMM
-    if qw and not qd:             # GGUF blocks; 8-bit activation codes plus one f32 per block
-        _, qblk, qbytes = Q_WEIGHTS[qw]
-        wb, sc, a_in = qbytes / qblk, 0.0, 1.0 + 4.0 / qblk
-    bytes_gateup = touched * 2 * cfg.I * cfg.H * (wb + sc) + P * cfg.H * a_in + P * cfg.I * 2
-    bytes_down = touched * cfg.H * cfg.I * (wb + sc) + P * cfg.I * a_in + P * cfg.H * 2 + P * 4
-    t_gu = stage_avg["gemm_gateup"] / 1000.0
-    t_dn = stage_avg["gemm_down"] / 1000.0
-    # the keep-quant kernels run on the CUDA cores and are reported against HBM
-    qk = qw and not qd            # the keep-quant kernels run
-    tensor_bound = (not qk and flop_gateup / (pk["bf16_tflops"] * 1e12)
-                    >= bytes_gateup / (pk["hbm_gbs"] * 1e9))
+    ga = gemm_account(cfg, counts, stage_avg, pk, fp8=fp8, qw=qw, qd=qd)
+    touched, qk, tensor_bound = ga["touched"], ga["qk"], ga["tensor_bound"]
+    flop_gateup, flop_down = ga["flop_gateup"], ga["flop_down"]
+    bytes_gateup, bytes_down = ga["bytes_gateup"], ga["bytes_down"]
+    t_gu, t_dn = ga["t_gu"], ga["t_dn"]
     kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
              f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qk else
              "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)")
@@ -598,6 +676,12 @@ def run_ours(args):
     components["combine_gate_workload"] = cg
     components["expert_load"] = {"max": int(counts.max()), "mean": float(counts.mean()),
                                  "min": int(counts.min()), "touched": touched}
+    if ws == 1 and args.config == "prefill" and args.weights == "bf16" and not args.no_extra_layers:
+        # the other full-size workloads, timed the same way in the same run
+        del blk
+        torch.cuda.empty_cache()
+        for name in ("decode", "large"):
+            components[name] = extra_layer(name, dev, args.steps, min(args.warmup, 5), pk)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -613,6 +697,16 @@ def run_ours(args):
         v, cores, n, dt = oracle_tokens_per_s(cfg, do, seconds=args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} of {cfg.T} tokens, whole block per token, {dt:.1f} s"}
+        import oracle as O
+
+        O.set_threads(1)
+        try:
+            v1, _, n1, dt1 = oracle_tokens_per_s(cfg, do, seconds=args.cpu_seconds / 2)
+        finally:
+            O.set_threads(cores)
+        cpu["one_core"] = {"value": v1, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                           "sample": f"{n1} of {cfg.T} tokens, whole block per token, "
+                                     f"{dt1:.1f} s"}
 
     clocks = clk.summary()
     if rank == 0:
@@ -664,6 +758,8 @@ def main():
                     help="routed expert weights: bf16, FP8 E4M3 with 128x128 block scales, or "
                          "keep-quant GGUF Q8_0 / Q4_K blocks")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extra-layers", action="store_true",
+                    help="prefill run: skip the decode and large workloads' components")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -77,7 +77,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 8 */
+int moe_abi_version(void);  /* 9 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -95,7 +95,10 @@ int moe_abi_version(void);  /* 8 */
  *            expf_cr is the binary32 rounding of a fixed double-precision
  *            evaluation (Cody-Waite reduction with ln2 split in a 32-bit head
  *            and a tail, Taylor series through r^13, scaling by 2^n); its
- *            result is the correctly rounded exp on every input tested.
+ *            result is the correctly rounded exp on every input tested.  The
+ *            kernels obtain the same bits mostly from binary32 arithmetic (a
+ *            table-driven form that declines inputs near a rounding midpoint
+ *            and hands them to the double chain): see moe_exp_sigmoid_f32.
  *   Given the same logits (logits_in), ids and weights are bit-exact.
  *
  *   x            bf16 [T,H]        (ignored when logits_in != NULL)
@@ -213,14 +216,17 @@ size_t moe_permute_workspace_size(int T, int K, int E);
  * Same arguments, outputs and bit-exact results as moe_permute, minus the
  * workspace.  The scratch is a fixed array of MOE_PERMUTE_NOALLOC_MAX_SCRATCH
  * bytes inside the library's device memory (held by every GPU that loads the
- * library until the process exits); calls whose moe_permute_workspace_size
- * exceeds it are refused with MOE_ERR_WORKSPACE (e.g. P = T*K up to 65536
- * pairs with E up to 1024, or up to 262144 pairs with E up to 256).  The call
- * allocates nothing.  The first call on each device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current, so make it
- * before any stream capture.  All calls share the array and it keeps the last
- * call's contents (no state carries over: every entry read is written first);
- * calls whose kernels may overlap on the GPU race on it.
+ * library until the process exits).  The histogram needs 4 bytes per expert
+ * for each chunk of 512 pairs, so calls are accepted for
+ *   P = T*K <= 512 * floor(2^18 / E)   (131072 pairs at E = 1024, 524288 at
+ *                                       E = 256, 1048576 at E = 128)
+ * and larger ones are refused with MOE_ERR_WORKSPACE.  The call allocates
+ * nothing.  Every call looks up the array's device address on the current
+ * device (cudaGetSymbolAddress, a host-side lookup); the first lookup on a
+ * device loads the library's device code there, so make the first call on
+ * each device before any stream capture.  All calls share the array and it
+ * keeps the last call's contents (no state carries over: every entry read is
+ * written first); calls whose kernels may overlap on the GPU race on it.
  * ---------------------------------------------------------------------- */
 #define MOE_PERMUTE_NOALLOC_MAX_SCRATCH (1 << 20)
 int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int K, int E, int H,
@@ -242,8 +248,8 @@ int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int 
  *   a_row_gather int32 [P] or NULL: row r of the product reads A row
  *                a_row_gather[r] / gather_div.  With sorted_pair and gather_div = K
  *                this reads every routed row straight from x [T,H] (no x_perm);
- *                rows are fetched by TMA tile::gather4.  An index outside
- *                [0, a_rows) reads zeros.
+ *                four producer warps copy the rows into shared memory with
+ *                16-byte cp.async.  An index outside [0, a_rows) reads zeros.
  *   gather_div   >= 1 when gathering (ignored otherwise)
  *   w13          bf16 [G, 2I, H]: gate rows first, then up rows, per group
  *   group_offsets int32 [G+1], non-decreasing, group_offsets[G] <= P;
@@ -302,9 +308,8 @@ size_t moe_grouped_gemm_workspace_size(int P, int H, int I, int G);
  * grid's round-robin schedule, so its tensor-bound work fills the ragged last
  * round of the weight-streaming routed tiles instead of a launch of its own.  Every output element
  * is computed by the same tile and K order as in the separate calls, so the
- * results are bit-identical to them.  Always single-CTA tiles (the
- * moe_set_gemm_pairing mode applies only when one half is empty, in which
- * case the call is the plain single-problem one).
+ * results are bit-identical to them.  Always single-CTA 128-row tiles (when
+ * one half is empty the call is the plain single-problem one).
  *
  *   gate/up:  xs bf16 [Ts,H], w13s bf16 [1,2Is,H] (gate rows first), acts bf16 [Ts,Is]
  *   down:     acts bf16 [Ts,Is], w2s bf16 [1,H,Is], sd bf16 [Ts,H]
@@ -352,32 +357,39 @@ int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
                                int I, int H, int G, void* out_bf16, void* workspace,
                                size_t ws_bytes, void* stream);
 
-/* moe_set_gemm_pairing -- tiling of the two grouped GEMMs above (the
- * gathered-A gate/up always runs single-CTA tiles):
- *   MOE_GEMM_SINGLE (default): one CTA per 128-row x N tile
- *   MOE_GEMM_PAIR:   CTA pairs on 256-row tiles (2-SM tcgen05.mma.cta_group::2;
- *                    each SM stages 128 A rows and half of the weight tile)
- *   MOE_GEMM_MCAST:  clusters of two CTAs on the same 128 rows and two
- *                    neighbouring N tiles; each loads half of the shared A tile
- *                    and multicasts it to both (used when the GEMM has an even
- *                    number of N tiles, otherwise single-CTA tiles)
- *   MOE_GEMM_SPLIT:  two launches per call -- the whole 256-row
- *                    blocks of every group on CTA pairs (no padding rows), then
- *                    the remaining rows of each group on MCAST/single tiles
- *   MOE_GEMM_TALL:   single CTAs; the whole 256-row blocks of every group are
- *                    256-row tiles, two M = 128 MMAs per k-step sharing each
- *                    weight stage (a third less shared-memory fill per MMA),
- *                    the remaining rows 128-row tiles; 256 rows or more per call
- * Results are identical up to f32 accumulation order.  On a skewed expert load
- * the single-CTA tiles are the fastest: their random mix of weight-bound and
- * tensor-bound tiles keeps both HBM and the tensor cores busy, which the
- * padding (PAIR) or the phase separation (SPLIT) of the others gives up.
- * Process-wide, takes effect at the next launch; returns the previous mode
- * (MOE_ERR_ARG for an unknown mode).  Not for use while another thread is
- * launching these GEMMs. */
-enum { MOE_GEMM_SINGLE = 0, MOE_GEMM_PAIR = 1, MOE_GEMM_MCAST = 2, MOE_GEMM_SPLIT = 3,
-       MOE_GEMM_TALL = 4 };
+/* moe_set_gemm_pairing -- tiling of moe_grouped_gemm_gateup_silu_bf16 (without
+ * a row gather) and moe_grouped_gemm_down_bf16:
+ *   MOE_GEMM_AUTO (default): CTA-pair tiles when P >= 1024 and the groups
+ *                    average at least 32 rows (P >= 32 G), single-CTA tiles
+ *                    otherwise
+ *   MOE_GEMM_SINGLE: one CTA per 128-row x N tile (32-row tiles when P <= 16 G)
+ *   MOE_GEMM_PAIR:   CTA-pair tiles for every such call.  A pair of SMs runs one
+ *                    tcgen05.mma.cta_group::2 with the group's weight rows on
+ *                    the M side (128 per SM) and up to 256 of its rows on the N
+ *                    side (N = their count rounded up to 16), so a group pads
+ *                    to 16 rows, and each SM stages 16 KB of weights plus at
+ *                    most 16 KB of rows per 64-wide K step
+ * Results agree up to f32 accumulation order.  The gathered gate/up, the FP8
+ * weight GEMMs and the fused shared-expert launches always use single-CTA
+ * tiles.  Values 3 and 4 (tilings measured slower and not built) are refused
+ * with MOE_ERR_UNSUPPORTED, others with MOE_ERR_ARG.  Process-wide, takes
+ * effect at the next launch; returns the previous mode.  Not for use while
+ * another thread is launching these GEMMs. */
+enum { MOE_GEMM_AUTO = 0, MOE_GEMM_SINGLE = 1, MOE_GEMM_PAIR = 2 };
 int moe_set_gemm_pairing(int mode);
+
+/* moe_set_wait_limit_ns -- limit, in nanoseconds of device time, of every
+ * pipeline wait inside the bf16 and FP8-weight grouped GEMM kernels (a role
+ * waiting for a stage to land or to be freed, or for an accumulator).
+ * Default and maximum 10^9 (one second), minimum 1000.  A wait that runs past
+ * it raises MOE_STATUS_TIMEOUT in the status word and stops its CTA: the
+ * other roles stop at their next wait, the copies and MMAs already in flight
+ * are waited for (up to one second each, whatever this limit is), the CTA's
+ * tensor memory is freed and the CTA exits, so the device stays usable and the
+ * call's output is incomplete.  A short limit lets a caller check this path
+ * without a faulty kernel.  Process-wide, takes effect at the next launch.
+ * Returns MOE_OK, or MOE_ERR_ARG outside [1000, 10^9]. */
+int moe_set_wait_limit_ns(unsigned long long ns);
 
 /* moe_set_pdl -- programmatic dependent launch for every kernel of the
  * library (enable = 1, the default) or plain stream order (0).  With it on,
@@ -520,7 +532,7 @@ int moe_combine(const void* expert_out, int eo_dtype, const float* w, const void
  * Bit-exact.  sd f32 or bf16; out f32 or bf16; gl f32 [T].
  * workspace: NULL, or >= moe_gate_workspace_size(T) bytes.  With a workspace
  * the T sigmoids are evaluated first by a small kernel and the stream reads
- * them (faster: the sigmoid is a chain of double-precision operations); without
+ * them (faster: each sigmoid is evaluated once, not once per block); without
  * one each block evaluates the sigmoids of its tokens itself.  Same bits.
  * Errors: those of moe_combine (sd and gl required), MOE_ERR_WORKSPACE and
  * MOE_ERR_ALIGN for a workspace below moe_gate_workspace_size or not 16-byte
@@ -574,10 +586,25 @@ enum {
   MOE_KID_GEMM_Q_GATEUP = 15, /* moe_grouped_gemm_gateup_silu_q */
   MOE_KID_GEMM_Q_DOWN = 16,   /* moe_grouped_gemm_down_q */
   MOE_KID_DEQUANT_Q = 17,     /* moe_dequantize_q_bf16 */
+  MOE_KID_EXP_SIGMOID = 18,   /* moe_exp_sigmoid_f32 */
   MOE_KID_COUNT = 20
 };
 int moe_device_status(int* status_out, int clear);
 int moe_launch_counts(unsigned long long* counts, int n);
+
+/* moe_exp_sigmoid_f32 -- the binary32 exp and sigmoid every bit-exact kernel
+ * of the library uses (router weights, sigmoid scoring, the shared-expert
+ * gate of [PR509], whose rework requires the gate bit-exact), evaluated on a
+ * range of bit patterns so that a caller can check them against another
+ * implementation of the same definition:
+ *   x_i = the binary32 value with bit pattern (first_bits + i) mod 2^32
+ *   exp_out[i] = expf_cr(x_i)                       (see moe_route_topk)
+ *   sigmoid_out[i] = 1 / (1 + expf_cr(-x_i))        (two binary32 operations)
+ * for i in [0, n).  Either output may be NULL; f32 arrays, 4-byte aligned.
+ * 0 <= n <= 2^32.  Errors: MOE_ERR_ARG (n outside that range; both outputs
+ * NULL), MOE_ERR_ALIGN, MOE_ERR_CUDA. */
+int moe_exp_sigmoid_f32(uint32_t first_bits, long long n, float* exp_out, float* sigmoid_out,
+                        void* stream);
 
 #ifdef __cplusplus
 }

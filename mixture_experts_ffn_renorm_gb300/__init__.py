@@ -26,6 +26,7 @@ KID = {
     "permute_place": 4, "permute_gather": 5, "gemm_gateup": 6, "gemm_down": 7, "combine": 8,
     "combine_gate": 9, "shared_gate": 10, "gate_sigmoid": 11, "permute_small": 12,
     "quant_act": 13, "gemm_q": 14, "gemm_q_gateup": 15, "gemm_q_down": 16, "dequant_q": 17,
+    "exp_sigmoid": 18,
 }
 KID_COUNT = 20
 QFMT_Q8_0, QFMT_Q4_K = 1, 2
@@ -36,11 +37,11 @@ EXPORTS = (
     "moe_grouped_gemm_gateup_silu_bf16",
     "moe_grouped_gemm_down_bf16", "moe_grouped_gemm_workspace_size", "moe_combine",
     "moe_combine_gate", "shared_expert_gate", "moe_device_status", "moe_launch_counts",
-    "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl",
+    "moe_set_gemm_pairing", "moe_gate_workspace_size", "moe_set_pdl", "moe_set_wait_limit_ns",
     "moe_grouped_gemm_gateup_silu_bf16_shared", "moe_grouped_gemm_down_bf16_shared",
     "moe_route_topk_ex", "moe_grouped_gemm_gateup_silu_fp8w", "moe_grouped_gemm_down_fp8w",
     "moe_quantize_act_q8", "moe_grouped_gemm_q", "moe_grouped_gemm_gateup_silu_q",
-    "moe_grouped_gemm_down_q", "moe_dequantize_q_bf16",
+    "moe_grouped_gemm_down_q", "moe_dequantize_q_bf16", "moe_exp_sigmoid_f32",
 )
 
 
@@ -87,11 +88,13 @@ _SIGS = {
     "moe_dequantize_q_bf16": ([_P, _I, ctypes.c_longlong, _I, _P, _P], _I),
     "moe_set_gemm_pairing": ([_I], _I),
     "moe_set_pdl": ([_I], _I),
+    "moe_set_wait_limit_ns": ([ctypes.c_ulonglong], _I),
     "moe_combine": ([_P, _I, _P, _P, _I, _F, _I, _I, _I, _P, _I, _P], _I),
     "moe_combine_gate": ([_P, _I, _P, _P, _I, _P, _F, _I, _I, _I, _P, _I, _P, _SZ, _P], _I),
     "shared_expert_gate": ([_P, _I, _P, _I, _I, _P, _I, _P, _SZ, _P], _I),
     "moe_gate_workspace_size": ([_I], _SZ),
     "moe_device_status": ([ctypes.POINTER(_I), _I], _I),
+    "moe_exp_sigmoid_f32": ([ctypes.c_uint32, ctypes.c_longlong, _P, _P, _P], _I),
     "moe_launch_counts": ([ctypes.POINTER(ctypes.c_ulonglong), _I], _I),
 }
 
@@ -302,14 +305,18 @@ def moe_grouped_gemm_workspace_size(P, H, I, G) -> int:
     return lib().moe_grouped_gemm_workspace_size(P, H, I, G)
 
 
-GEMM_SINGLE, GEMM_PAIR, GEMM_MCAST, GEMM_SPLIT, GEMM_TALL = 0, 1, 2, 3, 4
+GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR = 0, 1, 2
 
 
 def moe_set_gemm_pairing(mode: int) -> int:
-    """Tiling of the grouped GEMMs (GEMM_SINGLE / GEMM_PAIR / GEMM_MCAST / GEMM_SPLIT /
-    GEMM_TALL);
-    returns the previous mode."""
+    """Tiling of the grouped GEMMs (GEMM_AUTO / GEMM_SINGLE / GEMM_PAIR); returns the
+    previous mode."""
     return _check(lib().moe_set_gemm_pairing(int(mode)))
+
+
+def moe_set_wait_limit_ns(ns: int) -> int:
+    """Limit of the GEMM pipeline waits in nanoseconds (1000 .. 10**9, default 10**9)."""
+    return _check(lib().moe_set_wait_limit_ns(int(ns)))
 
 
 def moe_set_pdl(enable: bool) -> bool:
@@ -348,6 +355,13 @@ def moe_device_status(clear: bool = False) -> int:
     v = _I(0)
     _check(lib().moe_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def moe_exp_sigmoid_f32(first_bits, n, exp_out, sigmoid_out, stream=None, check=True):
+    """The library's binary32 exp and sigmoid on bit patterns first_bits .. + n - 1."""
+    rc = lib().moe_exp_sigmoid_f32(int(first_bits) & 0xFFFFFFFF, int(n), _ptr(exp_out),
+                                   _ptr(sigmoid_out), _stream(stream))
+    return _check(rc) if check else rc
 
 
 def moe_launch_counts() -> list[int]:

@@ -22,6 +22,24 @@ moe::DeviceDiag g_diag[kMaxDevices];
 bool g_diag_ready[kMaxDevices] = {};
 }  // namespace
 
+namespace {
+// exp and sigmoid of the bit patterns first, first + 1, ... (mod 2^32)
+__global__ void __launch_bounds__(256)
+exp_sigmoid_kernel(uint32_t first, long long n, float* __restrict__ e, float* __restrict__ s,
+                   unsigned long long* launches) {
+  moe::count_launch(launches, MOE_KID_EXP_SIGMOID);
+  moe::grid_dep_wait();
+  moe::grid_dep_launch();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const float x = __uint_as_float(first + static_cast<uint32_t>(i));
+    if (e) e[i] = moe::exp_f32(x);
+    if (s) s[i] = moe::sigmoid_f32(x);
+  }
+}
+}  // namespace
+
 namespace moe {
 
 int set_error(int code, const char* fmt, ...) {
@@ -87,7 +105,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_msg; }
 
-int moe_abi_version(void) { return 8; }
+int moe_abi_version(void) { return 9; }
 
 int moe_set_pdl(int enable) {
   moe::clear_error();
@@ -123,6 +141,26 @@ int moe_launch_counts(unsigned long long* counts, int n) {
   int m = n < MOE_KID_COUNT ? n : MOE_KID_COUNT;
   for (int i = 0; i < m; ++i) counts[i] = tmp[i];
   return m;
+}
+
+int moe_exp_sigmoid_f32(uint32_t first_bits, long long n, float* exp_out, float* sigmoid_out,
+                        void* stream) {
+  moe::clear_error();
+  const char* op = "moe_exp_sigmoid_f32";
+  if (n < 0 || n > (1ll << 32)) return moe::set_error(MOE_ERR_ARG, "%s: n=%lld outside [0, 2^32]", op, n);
+  if (!exp_out && !sigmoid_out) return moe::set_error(MOE_ERR_ARG, "%s: both outputs are NULL", op);
+  if ((reinterpret_cast<uintptr_t>(exp_out) & 3u) || (reinterpret_cast<uintptr_t>(sigmoid_out) & 3u))
+    return moe::set_error(MOE_ERR_ALIGN, "%s: outputs must be 4-byte aligned", op);
+  if (n == 0) return MOE_OK;
+  const long long blocks_needed = (n + 255) / 256;
+  const long long cap = 8ll * moe::sm_count();
+  const unsigned blocks = static_cast<unsigned>(blocks_needed < cap ? blocks_needed : cap);
+  moe::DeviceDiag diag = moe::device_diag();
+  return moe::launch_status(
+      moe::launch_kernel(exp_sigmoid_kernel, dim3(blocks), dim3(256), 0,
+                         static_cast<cudaStream_t>(stream), nullptr, 0, first_bits, n, exp_out,
+                         sigmoid_out, diag.launches),
+      op);
 }
 
 }  // extern "C"

@@ -8,9 +8,10 @@
 // token, so every expert row, shared row and output row moves as one 16-byte
 // vector per thread (two for f32) and a warp touches 512 contiguous bytes per
 // load.  All K expert vectors of a thread are in flight at once.  The sigmoid
-// of the gate is evaluated once per token per block (it costs a chain of
-// double-precision operations, which GB300 runs at a low rate); a gate block
-// streams several slices so that chain is amortised and overlaps the loads.
+// of the gate is evaluated once per token per block (about 60 binary32
+// operations, and a double-precision chain for the few inputs where the
+// binary32 form declines); a gate block streams several slices so that it is
+// amortised and overlaps the loads.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -149,12 +150,12 @@ combine_kernel(const void* __restrict__ eo, const float* __restrict__ w,
 }
 
 // kMoeCombineGate / kSharedExpertGate: a block streams kGateIters consecutive
-// slices of kThreads items, so the sigmoid of each of its tokens (a chain of
-// double-precision operations, slow on GB300) is evaluated once per block, by
-// full warps, while the first slice's loads are in flight.
+// slices of kThreads items, so the sigmoid of each of its tokens is evaluated
+// once per block, by full warps, while the first slice's loads are in flight.
 // sigma(gl[t]) for every token, one per thread, into s_out[T].  One warp per
-// block: the double-precision chain of each sigmoid is throughput-bound on an
-// SM's few FP64 units, so the tokens are spread over as many SMs as possible.
+// block, so the tokens are spread over as many SMs as possible: a warp whose
+// lanes meet an input the binary32 exp declines runs the double-precision
+// chain, which GB300's few FP64 units execute slowly.
 constexpr int kSigThreads = 32;
 __global__ void __launch_bounds__(kSigThreads)
 gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_out,
@@ -163,7 +164,7 @@ gate_sigmoid_kernel(const float* __restrict__ gl, int T, float* __restrict__ s_o
   grid_dep_wait();
   grid_dep_launch();
   const int t = blockIdx.x * kSigThreads + threadIdx.x;
-  if (t < T) s_out[t] = sigmoid_cr(__ldg(gl + t));
+  if (t < T) s_out[t] = sigmoid_f32(__ldg(gl + t));
 }
 
 // The gate ops with the sigmoids already in `sig` (gate_sigmoid_kernel): a
@@ -231,7 +232,7 @@ gate_kernel(const void* __restrict__ eo, const float* __restrict__ w,
     if (kMode == kCombineGate) routed_sum<EoT, kHasW>(eo, w, rs, t, c0, K, H, acc);
   }
   for (int r = threadIdx.x; r < n_rows; r += kThreads)
-    s_gate[r] = sigmoid_cr(__ldg(gl + t_first + r));
+    s_gate[r] = sigmoid_f32(__ldg(gl + t_first + r));
   __syncthreads();
   for (int it = 0; it < kGateIters; ++it) {
     if (it > 0) {

@@ -141,9 +141,9 @@ __device__ __forceinline__ float exp_cr(float x) {
 }
 
 // Binary32 exp from binary32 arithmetic, bit-identical to exp_cr (the defined
-// exp above) wherever it decides.  The kernels still call exp_cr; this form is
-// checked on the host against the oracle's exp ahead of its use on the device,
-// where it avoids the double-precision chain for all but a few inputs.
+// exp above) wherever it decides; exp_f32 below takes it and falls back to
+// exp_cr elsewhere, which avoids the double-precision chain for all but a few
+// inputs.
 // Table-driven reduction (P. T. P. Tang, "Table-driven implementation of the
 // exponential function in IEEE floating-point arithmetic", ACM TOMS 15(2), 1989):
 //   N = rint(x * 64/ln2), r = x - N ln2/64 (|r| <= ln2/128 plus rounding),
@@ -308,9 +308,19 @@ __host__ __device__ __forceinline__ bool exp_fast_f32(float x, float* y) {
   return true;
 }
 
-// sigma(g) = 1 / (1 + exp_cr(-g)), two separately rounded binary32 ops
-__device__ __forceinline__ float sigmoid_cr(float g) {
-  float e = exp_cr(-g);
+// The defined binary32 exp as the kernels evaluate it: the binary32 pair of
+// exp_fast_f32 where it decides, otherwise the double-precision chain exp_cr.
+// Both give exp_cr's bits, so this is exp_cr, with double precision only for
+// NaN, inputs outside [-86, 88] and about 7 in a million others.
+__device__ __forceinline__ float exp_f32(float x) {
+  float y;
+  if (exp_fast_f32(x, &y)) return y;
+  return exp_cr(x);
+}
+
+// sigma(g) = 1 / (1 + exp(-g)), two separately rounded binary32 ops after the exp
+__device__ __forceinline__ float sigmoid_f32(float g) {
+  const float e = exp_f32(-g);
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 

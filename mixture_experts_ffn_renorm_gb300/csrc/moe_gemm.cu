@@ -3,6 +3,8 @@
 // #3094 "Row: BACKEND-ROCM-BF16-MOE", which also fixes their numeric contract:
 // BF16 narrowing of the gate/up result before activation, routing weight
 // applied before the down result is stored), plus the router-logit GEMM.
+// This file holds the single-CTA tiles (one SM per 128-row x N tile); the
+// CTA-pair tiles of large batches are in moe_gemm_pair.cu.
 //
 // One persistent, warp-specialised kernel template:
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [kN x 64] bf16 per
@@ -21,10 +23,11 @@
 // ...  All tiles cost the same, so the static stride balances any skew of the
 // expert load to within one tile per CTA.  No host round trip, no scratch.
 //
-// Every wait on an mbarrier is bounded (about one second of device time); on
-// expiry the kernel raises MOE_STATUS_TIMEOUT in the library's status word,
-// every role stops, in-flight copies and MMAs are drained (again bounded) and
-// the TMEM is freed before the CTA exits.
+// Every wait on an mbarrier is bounded (one second of device time by
+// default, moe_set_wait_limit_ns); on expiry the kernel raises
+// MOE_STATUS_TIMEOUT in the library's status word, every role stops, and
+// before the CTA exits its in-flight copies and MMAs are drained (waits of
+// their own, always one second) and its TMEM is freed.
 #include <stdio.h>
 
 #include <atomic>
@@ -33,26 +36,20 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
-#include "moe_common.cuh"
-#include "sm100_ptx.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace gemm {
 
-constexpr int BM = 128;           // rows per tile (MMA M)
-constexpr int BK = 64;            // bf16 per 128-byte swizzled row: K per stage
-constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;        // producer, MMA, 4 epilogue warps
 constexpr int kThreadsGather = 320;  // + 4 warps that gather A rows
 constexpr int kConverters = 256;     // FP8 weights: 8 warps that dequantise B
 constexpr int kThreadsFp8 = kThreads + kConverters;
-constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK * 2;
 // bytes of the 227 KB per-block shared memory left for the stage ring after the
 // barriers, the schedule tables (2 x 4 KB), the epilogue staging buffers
 // (4 x 4 KB) and the 1 KB alignment slack
 constexpr int kSmemBudget = 227 * 1024 - 11 * 1024 - 16 * 1024;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr int kStgBytes = 32 * 128;  // epilogue staging: 32 rows x 64 bf16 per warp
 constexpr int kNarrowRows = 32;      // rows per tile when experts hold few rows
 
@@ -70,15 +67,14 @@ struct Params {
   int a_rows;
   const int32_t* row_gather;     // gathered A: product row r reads row row_gather[r] / gather_div
   int gather_div;
-  int split;                     // 0 whole groups; 1 their leading 256-row blocks; 2 the rest
   void* out;
   const float* pair_weight;      // down: [P] by destination row, or null
   const int32_t* row_to_pair;    // down: destination row, or null
   const float* bias;             // f32 epilogue: per output column, or null
-  // A second, dense problem in the same launch (single-CTA tiles only): rows
-  // [0, P2) of the A matrix behind the second A tensor map times the one weight
-  // matrix behind the second B map, into out2 [P2, N2] (no weight, no scatter).
-  // Its tiles come after the grouped ones in the schedule.  P2 == 0: none.
+  // A second, dense problem in the same launch: rows [0, P2) of the A matrix
+  // behind the second A tensor map times the one weight matrix behind the
+  // second B map, into out2 [P2, N2] (no weight, no scatter).  Its tiles come
+  // after the grouped ones in the schedule.  P2 == 0: none.
   int P2;
   int N2;
   int Kdim2;
@@ -94,6 +90,7 @@ struct Params {
   // each (tile, range) is a unit of its own and stores its partial sum, without
   // the bias, at out + range * P * N.  ksplit == 1: the whole K, bias added.
   int ksplit;
+  unsigned long long wait_ns;    // limit of every pipeline wait
   unsigned int* status;
   unsigned long long* launches;
   int kid;
@@ -122,8 +119,8 @@ struct Smem {
   static constexpr int STAGE_EPI = STAGE_B + (kConv ? kConv : kStages) * B_BYTES;  // staging buffers
   static constexpr int BARS = STAGE_EPI + kEpiBytes;
   // full[kStages], empty[kStages], conv_full[kConv], conv_empty[kConv], tfull[2], tempty[2],
-  // drain, tfull_tall
-  static constexpr int NBARS = 2 * kStages + 2 * kConv + 6;
+  // drain
+  static constexpr int NBARS = 2 * kStages + 2 * kConv + 5;
   static constexpr int MISC = BARS + NBARS * 8;           // tmem slot, abort flag, scan scratch
   static constexpr int TILE_START = MISC + 64;            // int[kMaxGroups + 1]
   static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
@@ -133,112 +130,64 @@ struct Smem {
 
 // Compile-time shape of one kernel instantiation.
 //   kN      MMA N (accumulator columns per tile)
-//   kPair   CTA pair (cta_group::2): M = 256 per tile, each CTA holds 128 A rows
-//           and half of B, and one thread of the even CTA issues the MMAs
-//   kARows  rows per tile and per A box (single CTAs): 128, or 32 when experts
-//           hold few rows.  The MMA is still M = 128; with 32-row tiles it reads
-//           the 96 rows after the stage's A box from whatever shared memory follows
+//   kARows  rows per tile and per A box: 128, or 32 when experts hold few
+//           rows.  The MMA is still M = 128; with 32-row tiles it reads the 96
+//           rows after the stage's A box from whatever shared memory follows
 //           (a later stage), and those accumulator rows are never stored.  A
 //           stage then holds 4 KB of A instead of 16, so the same shared memory
 //           keeps about twice as many weight bytes in flight.
 //   kFp8B   B holds FP8 E4M3 weight codes with block scales: TMA brings A and the
 //           codes into the stage ring, eight converter warps write the scaled
 //           bf16 B tiles into a second ring, and the MMA reads A and that
-//   kTall   (single CTAs) the whole 256-row blocks of every group are tiles of 256
-//           rows: each k-step issues two M = 128 MMAs, rows 0-127 into one TMEM
-//           accumulator and rows 128-255 into the other, against the same B stage,
-//           so a stage's 32 KB of weights serve twice the rows and the per-SM
-//           shared-memory fill per MMA drops from 96 to 64 bytes a cycle.  The
-//           remaining rows of a group are 128-row tiles.  A tall tile holds both
-//           accumulators, so its epilogue runs on eight warps (one accumulator
-//           each for warps 2-5 and 6-9) to shorten the time it keeps them.
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA = false, int kARows = BM,
-          bool kFp8B = false, bool kTall = false>
+template <int kN, int kEpi, bool kGatherA, int kARows = BM, bool kFp8B = false>
 struct Cfg {
-  static_assert(kARows == BM || (!kPair && !kMcastA && !kGatherA && kARows % 8 == 0),
-                "short A tiles are single-CTA TMA tiles only");
-  static_assert(!kFp8B || (!kPair && !kMcastA && !kGatherA), "FP8 weights: single-CTA tiles");
-  static_assert(!kTall || (!kPair && !kMcastA && !kGatherA && !kFp8B && kARows == BM &&
-                           kEpi != EPI_F32),
-                "tall tiles: single-CTA bf16 gate/up and down only");
-  static constexpr int kTileM = kPair ? 2 * BM : kARows;          // product rows per (short) tile
-  static constexpr int kABytes = (kTall ? 2 : 1) * kARows * BK * 2;  // A bytes per stage
-  static constexpr int kBRowsCta = kPair ? kN / 2 : kN;           // B rows held per CTA
-  static constexpr int kBBytes = kBRowsCta * BK * 2;
-  static constexpr int kRawBytes = kFp8B ? kBRowsCta * BK : 0;    // FP8 codes per stage
+  static_assert(kARows == BM || (!kGatherA && kARows % 8 == 0),
+                "short A tiles are TMA tiles only");
+  static_assert(!kFp8B || !kGatherA, "FP8 weights: TMA A tiles");
+  static constexpr int kTileM = kARows;                           // product rows per tile
+  static constexpr int kABytes = kARows * BK * 2;                 // A bytes per stage
+  static constexpr int kBBytes = kN * BK * 2;
+  static constexpr int kRawBytes = kFp8B ? kN * BK : 0;           // FP8 codes per stage
   static constexpr int kConv = kFp8B ? (kBBytes >= 32 * 1024 ? 2 : 4) : 0;
   static constexpr int kStages =
       kFp8B ? stages_for_bytes_with(kABytes + kRawBytes, kSmemBudget - kConv * kBBytes)
             : stages_for_bytes(kABytes + kBBytes);
-  // B boxes: gate/up loads its gate and up halves separately (per CTA when paired)
-  static constexpr int kBoxB = kPair ? kBRowsCta
-                                     : ((kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128));
+  // B boxes: gate/up loads its gate and up halves separately
+  static constexpr int kBoxB = (kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128);
   static constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;  // output columns per tile
-  static constexpr int kThreadsT =
-      kFp8B ? kThreadsFp8 : ((kGatherA || kTall) ? kThreadsGather : kThreads);
-  // epilogue: warps and the columns each stages per pass (32 rows x kEpiCols bf16)
-  static constexpr int kEpiWarps = kTall ? 8 : 4;
-  static constexpr int kEpiCols = kTall ? 32 : 64;
+  static constexpr int kThreadsT = kFp8B ? kThreadsFp8 : (kGatherA ? kThreadsGather : kThreads);
+  static constexpr int kEpiCols = 64;                             // columns staged per pass
   static constexpr int kStgWarp = 32 * kEpiCols * 2;
-  using S = Smem<kStages, kBBytes, kABytes, kConv, kRawBytes, kEpiWarps * kStgWarp>;
+  using S = Smem<kStages, kBBytes, kABytes, kConv, kRawBytes, 4 * kStgWarp>;
 };
 
 struct Tile {
   int g, row0, row_end, n0;
   int pb;    // 0: the grouped problem, 1: the second (dense) problem
   int ks;    // K range of a split-K unit (0 without split)
-  int tall;  // 1: a 256-row tile (kTall)
 };
 
-// M tiles of a group of `rows` rows: ceil(rows / tile_m), or with tall tiles
-// the whole 256-row blocks plus ceil(remainder / 128)
-__device__ __forceinline__ int group_m_tiles(int rows, int tile_m, bool tall) {
-  if (rows <= 0) return 0;
-  if (tall) return rows / 256 + ((rows % 256) + BM - 1) / BM;
-  return (rows + tile_m - 1) / tile_m;
-}
-
-// rows of group g this launch covers: all of them, the leading whole 256-row
-// blocks (split 1) or the remainder after them (split 2)
-__device__ __forceinline__ void group_range(const int* goff, int g, int split, int& lo, int& hi) {
-  lo = goff[g];
-  hi = goff[g + 1];
-  const int head = ((hi - lo) / 256) * 256;
-  if (split == 1) hi = lo + head;
-  else if (split == 2) lo += head;
+// M tiles of a group of `rows` rows
+__device__ __forceinline__ int group_m_tiles(int rows, int tile_m) {
+  return rows <= 0 ? 0 : (rows + tile_m - 1) / tile_m;
 }
 
 __device__ __forceinline__ Tile decode_tile(int tile, const int* tile_start, const int* goff,
-                                            int G, int n_tiles, int bn_out, int tile_m,
-                                            int split, bool tall = false) {
+                                            int G, int n_tiles, int bn_out, int tile_m) {
   int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
     if (tile_start[mid] <= tile) lo = mid; else hi = mid;
   }
-  int local = tile - tile_start[lo];
-  int m = local / n_tiles, n = local - m * n_tiles;
-  int r0, r1;
-  group_range(goff, lo, split, r0, r1);
+  const int local = tile - tile_start[lo];
+  const int m = local / n_tiles, n = local - m * n_tiles;
   Tile t;
   t.g = lo;
-  t.row0 = r0 + m * tile_m;
-  t.row_end = min(r1, t.row0 + tile_m);
+  t.row0 = goff[lo] + m * tile_m;
+  t.row_end = min(goff[lo + 1], t.row0 + tile_m);
   t.n0 = n * bn_out;
   t.pb = 0;
   t.ks = 0;
-  t.tall = 0;
-  if (tall) {  // the group's whole 256-row blocks first, then its 128-row tiles
-    const int n_tall = (r1 - r0) / 256;
-    if (m < n_tall) {
-      t.row0 = r0 + 256 * m;
-      t.row_end = t.row0 + 256;
-      t.tall = 1;
-    } else {
-      t.row0 = r0 + 256 * n_tall + BM * (m - n_tall);
-      t.row_end = min(r1, t.row0 + BM);
-    }
-  }
   return t;
 }
 
@@ -255,8 +204,8 @@ struct Sched2 {
 };
 
 __device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const int* goff, int G,
-                                            int n_tiles, int bn_out, int tile_m, int split,
-                                            const Sched2& s2, bool tall = false) {
+                                            int n_tiles, int bn_out, int tile_m,
+                                            const Sched2& s2) {
   if (s2.extra > 0 && i >= s2.routed) {
     const int q = i - s2.routed;
     const int m = q / s2.n2_tiles;
@@ -267,77 +216,29 @@ __device__ __forceinline__ Tile locate_tile(int i, const int* tile_start, const 
     t.n0 = (q - m * s2.n2_tiles) * bn_out;
     t.pb = 1;
     t.ks = 0;
-    t.tall = 0;
     return t;
   }
-  return decode_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split, tall);
+  return decode_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m);
 }
 
 // split-K units (f32 epilogue): schedule index i is K range i % ksplit of tile i / ksplit
 __device__ __forceinline__ Tile locate_unit(int i, int ksplit, const int* tile_start,
                                             const int* goff, int G, int n_tiles, int bn_out,
-                                            int tile_m, int split, const Sched2& s2,
-                                            bool tall = false) {
-  if (ksplit <= 1)
-    return locate_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2, tall);
+                                            int tile_m, const Sched2& s2) {
+  if (ksplit <= 1) return locate_tile(i, tile_start, goff, G, n_tiles, bn_out, tile_m, s2);
   const int q = i / ksplit;
-  Tile t = locate_tile(q, tile_start, goff, G, n_tiles, bn_out, tile_m, split, s2);
+  Tile t = locate_tile(q, tile_start, goff, G, n_tiles, bn_out, tile_m, s2);
   t.ks = i - q * ksplit;
   return t;
 }
 
-// Bounded mbarrier wait.  Returns false when this CTA is aborting.  kCluster:
-// acquire at cluster scope (the barrier is arrived on by the peer CTA).
-template <bool kCluster = false>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* status) {
-  auto probe = [&]() {
-    if (!kCluster) return ptx::mbar_try_wait(bar, parity);
-    if (!ptx::mbar_try_wait_cluster(bar, parity)) return false;
-    ptx::fence_acquire_cluster();
-    return true;
-  };
-  if (probe()) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 128; ++i)
-      if (probe()) return true;
-    if (*abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-      if (status) atomicOr(status, static_cast<unsigned int>(MOE_STATUS_TIMEOUT));
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void spin_bounded(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
-  }
-}
-
-// two values rounded to bf16 (nearest even) in one conversion, lo in the low half
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// kMcastA: a cluster of two CTAs computes the same 128 A rows against two
-// neighbouring N tiles; each CTA loads half of the A tile and multicasts it to
-// both, and each stage is released only when both MMAs are done with it.
-// kTall: tmA2 is the A matrix with 256-row boxes (tall tiles); no second problem.
-template <int kN, int kEpi, bool kGatherA, bool kPair, bool kMcastA, int kARows, bool kFp8B,
-          bool kTall>
-__global__ void __launch_bounds__(
-    Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>::kThreadsT, 1)
+template <int kN, int kEpi, bool kGatherA, int kARows, bool kFp8B>
+__global__ void __launch_bounds__(Cfg<kN, kEpi, kGatherA, kARows, kFp8B>::kThreadsT, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>;
-  constexpr bool kCluster = kPair || kMcastA;
+  using C = Cfg<kN, kEpi, kGatherA, kARows, kFp8B>;
   using S = typename C::S;
   constexpr int kABytes = C::kABytes;
   constexpr int kConv = C::kConv;
@@ -351,7 +252,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   // it must retire the oldest one (kDepth < kStages keeps the ring deadlock-free)
   constexpr int kDepth = kStages - 1;
   constexpr int kTmemCols = 2 * kN;
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPair ? 2 * BM : BM, kN);
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, kN);
   constexpr uint32_t kStageTx = (kGatherA ? 0 : kABytes) + (kFp8B ? S::RAW_BYTES : S::B_BYTES);
   constexpr int kEpiCols = C::kEpiCols;
   constexpr int kStgWarp = C::kStgWarp;
@@ -369,11 +270,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // pair: rank 0 (even CTA) issues the MMAs and owns the stage barriers; both load
-  const uint32_t rank = kCluster ? ptx::cluster_ctarank() : 0u;
-  const bool leader = !kPair || rank == 0;
-  const int unit = kCluster ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int n_units = kCluster ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int unit = static_cast<int>(blockIdx.x);
+  const int n_units = static_cast<int>(gridDim.x);
+  const unsigned long long wait_ns = p.wait_ns;
   auto bar_full = [&](int s) { return ptx::smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return ptx::smem_u32(bars + kStages + s); };
   auto bar_cfull = [&](int s) { return ptx::smem_u32(bars + 2 * kStages + s); };
@@ -381,11 +280,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 * kConv + a); };
   auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 2 + a); };
   const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 4);
-  // tall tiles signal their second accumulator here, not on tfull(1): warps
-  // 6-9 drain only tall tiles, and a barrier whose phases also advanced for the
-  // short tiles warps 2-5 drain from that slot would let their parity wait
-  // pass on a short tile's completion
-  const uint32_t bar_tfull_tall = ptx::smem_u32(bars + 2 * kStages + 2 * kConv + 5);
 
   count_launch(p.launches, p.kid);
 
@@ -393,7 +287,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar_full(s), kGatherA ? 1 + BM : 1);
       // FP8 weights: a stage is free once the MMA and every converter are done with it
-      ptx::mbar_init(bar_empty(s), kFp8B ? 1 + kConverters : (kMcastA ? 2 : 1));
+      ptx::mbar_init(bar_empty(s), kFp8B ? 1 + kConverters : 1);
     }
     for (int s = 0; s < kConv; ++s) {
       ptx::mbar_init(bar_cfull(s), kConverters);
@@ -401,29 +295,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_tfull(a), 1);
-      ptx::mbar_init(bar_tempty(a), kPair ? 2 * BM : BM);
+      ptx::mbar_init(bar_tempty(a), BM);
     }
     ptx::mbar_init(bar_drain, 1);
-    ptx::mbar_init(bar_tfull_tall, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
-    if (p.P2 > 0 || kTall) {
+    if (p.P2 > 0) {
       ptx::tma_prefetch_desc(&tmA2);
       ptx::tma_prefetch_desc(&tmB2);
     }
   }
   if (warp == 1) {
-    if (kPair) {
-      ptx::tmem_alloc2(ptx::smem_u32(tmem_slot), kTmemCols);
-      ptx::tmem_relinquish2();
-    } else {
-      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-      ptx::tmem_relinquish();
-    }
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
   }
 
   // the set-up above touches no global data; from here on this kernel reads
@@ -436,18 +324,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   for (int g = threadIdx.x; g <= G; g += kNThreads)
     goff[g] = p.group_offsets ? __ldg(p.group_offsets + g) : (g == 0 ? 0 : p.P);
   __syncthreads();
-  // schedule units along N: one tile, or (multicast) a pair of neighbouring tiles
-  const int n_tiles = ((p.N + kBnOut - 1) / kBnOut) / (kMcastA ? 2 : 1);
-  constexpr int kBnSched = kMcastA ? 2 * kBnOut : kBnOut;
+  const int n_tiles = (p.N + kBnOut - 1) / kBnOut;
   const int chunk = (G + kNThreads - 1) / kNThreads;
   const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
   const int g_hi = min(G, g_lo + chunk);
   int local = 0;
-  for (int g = g_lo; g < g_hi; ++g) {
-    int r0, r1;
-    group_range(goff, g, p.split, r0, r1);
-    local += group_m_tiles(r1 - r0, kTileM, kTall) * n_tiles;
-  }
+  for (int g = g_lo; g < g_hi; ++g) local += group_m_tiles(goff[g + 1] - goff[g], kTileM) * n_tiles;
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -465,18 +347,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   int run = warp_base + incl - local;
   for (int g = g_lo; g < g_hi; ++g) {
     tile_start[g] = run;
-    int r0, r1;
-    group_range(goff, g, p.split, r0, r1);
-    run += group_m_tiles(r1 - r0, kTileM, kTall) * n_tiles;
+    run += group_m_tiles(goff[g + 1] - goff[g], kTileM) * n_tiles;
   }
   if (threadIdx.x == 0) tile_start[G] = total;
   ptx::tc_fence_before();
   __syncthreads();
-  if (kCluster) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nk = (p.Kdim + BK - 1) / BK;
-  constexpr bool kCan2 = !kPair && !kMcastA && !kGatherA;
+  constexpr bool kCan2 = !kGatherA;
   const int ksplit = (kEpi == EPI_F32 && p.ksplit > 1) ? p.ksplit : 1;
   const int nk_split = (nk + ksplit - 1) / ksplit;   // k-blocks per K range
   Sched2 s2{total, 0, 1, 0};
@@ -488,8 +367,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
   total *= ksplit;
   const int nk2 = (p.Kdim2 + BK - 1) / BK;
-  const int row_off = kPair ? static_cast<int>(rank) * BM : 0;  // this CTA's A rows in a tile
-  const int n_off = kMcastA ? static_cast<int>(rank) * kBnOut : 0;  // this CTA's N tile in a unit
+
+  // state the exit drain needs: the producer's ring position and copy count,
+  // whether the MMA issuer issued anything
+  int prod_stage = 0;
+  uint32_t prod_phase = 0;
+  int prod_issued = 0;
+  bool mma_any = false;
 
   if (kGatherA && warp >= 6) {
     // ------------------------------------------------------------ A-row gatherers
@@ -504,14 +388,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int pending = 0;
     bool ok = true;
     for (int tile = unit; ok && tile < total; tile += n_units) {
-      Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split);
-      t.n0 += n_off;
-      const int r = min(t.row0 + row_off + i, p.P - 1);  // rows past the group are masked later
+      const Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
+      const int r = min(t.row0 + i, p.P - 1);  // rows past the group are masked later
       const int srow = __ldg(p.row_gather + r) / p.gather_div;
       const bool in = srow >= 0 && srow < p.a_rows;
       const uint16_t* src = p.a + static_cast<size_t>(in ? srow : 0) * p.Kdim;
       for (int kb = 0; kb < nk; ++kb) {
-        if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns)) {
+          ok = false;
+          break;
+        }
         const uint32_t dst = sbase + S::STAGE_A + stage * kABytes + i * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -542,63 +428,38 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // A box (unless gathered) and B boxes of this CTA, completion on its own barrier
+    // A box (unless gathered) and B boxes, completion on the stage's barrier
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int issued = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
-                             p.split, s2, kTall);
-        t.n0 += n_off;
-        const bool second = kCan2 && !kTall && t.pb == 1;
-        // tall tiles load 256 A rows through the 256-row map, short ones 128
-        const CUtensorMap* mA = (second || (kTall && t.tall)) ? &tmA2 : &tmA;
-        const uint32_t tx = (kTall && !t.tall) ? kStageTx - kABytes / 2 : kStageTx;
+        const Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnOut, kTileM, s2);
+        const bool second = kCan2 && t.pb == 1;
+        const CUtensorMap* mA = second ? &tmA2 : &tmA;
         const CUtensorMap* mB = second ? &tmB2 : &tmB;
         const int kb_lo = t.ks * nk_split;
         const int nk_t = second ? nk2 : min(nk, kb_lo + nk_split);
-        // B rows of this CTA: unpaired, the whole tile (gate/up: gate half, then
-        // up half); paired, rank 0 holds the first half of the N columns
-        // (gate rows) and rank 1 the second (up rows)
+        // B rows of the tile (gate/up: the gate half, then the up half)
         int brow0, brow1;
         if (second) {
           brow0 = t.n0;
           brow1 = brow0 + p.half_off2;
-        } else if (kPair) {
-          brow0 = t.g * p.b_rows_per_group + t.n0 +
-                  static_cast<int>(rank) * ((kEpi == EPI_GATEUP) ? p.half_off : kN / 2);
-          brow1 = brow0;
         } else {
           brow0 = t.g * p.b_rows_per_group + t.n0;
           brow1 = brow0 + p.half_off;
         }
         for (int kb = second ? 0 : kb_lo; kb < nk_t; ++kb) {
-          if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns)) {
+            ok = false;
+            break;
+          }
           const uint32_t sa = sbase + S::STAGE_A + stage * kABytes;
           const uint32_t sb = kFp8B ? sbase + S::STAGE_RAW + stage * S::RAW_BYTES
                                     : sbase + S::STAGE_B + stage * S::B_BYTES;
-          if (kPair) {
-            // both CTAs' boxes are counted on the even CTA's barrier, which
-            // expects the bytes of both halves
-            const uint32_t fb = ptx::mapa_shared(bar_full(stage), 0);
-            if (leader) ptx::mbar_arrive_expect_tx(bar_full(stage), 2 * kStageTx);
-            ptx::tma_load_2d_pair(sa, &tmA, kb * BK, t.row0 + row_off, fb);
-            ptx::tma_load_2d_pair(sb, &tmB, kb * BK, brow0, fb);
-            ++issued;
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
-            continue;
-          }
           const uint32_t fb = bar_full(stage);
-          ptx::mbar_arrive_expect_tx(fb, tx);
-          if (kMcastA) {
-            // this CTA's half of the A tile (64 rows), into both CTAs of the pair
-            ptx::tma_load_2d_mcast(sa + rank * (kABytes / 2), &tmA, kb * BK,
-                                   t.row0 + static_cast<int>(rank) * (BM / 2), fb, 3);
-          } else if (!kGatherA) {
-            ptx::tma_load_2d(sa, mA, kb * BK, t.row0 + row_off, fb);
-          }
+          ptx::mbar_arrive_expect_tx(fb, kStageTx);
+          if (!kGatherA) ptx::tma_load_2d(sa, mA, kb * BK, t.row0, fb);
           if (kEpi == EPI_GATEUP) {
             ptx::tma_load_2d(sb, mB, kb * BK, brow0, fb);
             ptx::tma_load_2d(sb + kBoxBytes, mB, kb * BK, brow1, fb);
@@ -607,47 +468,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int h = 0; h < kN / kBoxB; ++h)
               ptx::tma_load_2d(sb + h * kBoxBytes, mB, kb * BK, brow0 + h * kBoxB, fb);
           }
-          ++issued;
+          ++prod_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok && (!kPair || leader)) {
-        // drain: the last min(issued, kStages) copies may still be landing
-        int s = stage;
-        uint32_t ph = phase;
-        for (int i = 0; i < min(issued, kStages); ++i) {
-          if (--s < 0) { s = kStages - 1; ph ^= 1u; }
-          spin_bounded(bar_full(s), ph);
-        }
-      }
+      prod_stage = stage;
+      prod_phase = phase;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // (paired: the even CTA's thread issues for both; the odd CTA's warp 1 idles)
-    if (lane == 0 && leader) {
+    if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int cst = 0;             // FP8 weights: stage of the converted ring
       uint32_t cphase = 0;
-      // accumulator slots: a tile takes slot `nxt` (alternating), a tall tile
-      // both; use counts per slot give the barrier phases (the epilogue keeps
-      // the same counts)
-      uint32_t uses0 = 0, uses1 = 0;
-      int nxt = 0;
-      bool ok = true, any = false;
+      uint32_t uses0 = 0, uses1 = 0;  // accumulator slot uses: the barrier phases
+      int acc = 0;
+      bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        const bool tall =
-            kTall && locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
-                                 p.split, s2, kTall).tall;
-        const int acc = nxt;
-        if (tall) {
-          if (!wait_bar(bar_tempty(0), (uses0 & 1u) ^ 1u, abort_flag, p.status) ||
-              !wait_bar(bar_tempty(1), (uses1 & 1u) ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-        } else if (!wait_bar<kPair>(bar_tempty(acc), ((acc ? uses1 : uses0) & 1u) ^ 1u,
-                                    abort_flag, p.status)) {
+        if (!wait_bar(bar_tempty(acc), ((acc ? uses1 : uses0) & 1u) ^ 1u, abort_flag, p.status,
+                      wait_ns)) {
           ok = false;
           break;
         }
@@ -658,13 +498,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const int kb_lo = (tile % ksplit) * nk_split;
           nk_t = min(nk, kb_lo + nk_split) - kb_lo;
         } else if (kCan2 && s2.extra > 0 &&
-                   locate_tile(tile, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split, s2)
-                       .pb) {
+                   locate_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM, s2).pb) {
           nk_t = nk2;
         }
         for (int kb = 0; kb < nk_t; ++kb) {
-          if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
-          if (kFp8B && !wait_bar(bar_cfull(cst), cphase, abort_flag, p.status)) {
+          if (!wait_bar(bar_full(stage), phase, abort_flag, p.status, wait_ns)) {
+            ok = false;
+            break;
+          }
+          if (kFp8B && !wait_bar(bar_cfull(cst), cphase, abort_flag, p.status, wait_ns)) {
             ok = false;
             break;
           }
@@ -672,33 +514,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint64_t da = ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * kABytes);
           const uint64_t db = ptx::desc_kmajor_sw128(sbase + S::STAGE_B +
                                                      (kFp8B ? cst : stage) * S::B_BYTES);
-          if (tall) {
-            // rows 0-127 into slot 0, rows 128-255 (16 KB on in the stage) into slot 1
-            const uint64_t da1 =
-                ptx::desc_kmajor_sw128(sbase + S::STAGE_A + stage * kABytes + kABytes / 2);
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k)
-              ptx::mma_bf16(tmem_base, da + 2ull * k, db + 2ull * k, kIdesc,
-                            (kb | k) != 0 ? 1u : 0u);
-#pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k)
-              ptx::mma_bf16(tmem_base + static_cast<uint32_t>(kN), da1 + 2ull * k, db + 2ull * k,
-                            kIdesc, (kb | k) != 0 ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-              // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
-              if (kPair)
-                ptx::mma_bf16_pair(d, da + 2ull * k, db + 2ull * k, kIdesc,
-                                   (kb | k) != 0 ? 1u : 0u);
-              else
-                ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
-            }
-          }
-          any = true;
-          if (kPair) ptx::mma_commit_pair(bar_empty(stage), 3);
-          else if (kMcastA) ptx::mma_commit_mcast(bar_empty(stage), 3);  // frees it in both CTAs
-          else ptx::mma_commit(bar_empty(stage));
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            // +32 bytes along K inside the 128-byte swizzle atom: +2 in the address field
+            ptx::mma_bf16(d, da + 2ull * k, db + 2ull * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          mma_any = true;
+          ptx::mma_commit(bar_empty(stage));
           if (kFp8B) {
             ptx::mma_commit(bar_cempty(cst));
             if (++cst == kConv) { cst = 0; cphase ^= 1u; }
@@ -706,66 +527,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (tall) {
-          ptx::mma_commit(bar_tfull(0));
-          ptx::mma_commit(bar_tfull_tall);
-          ++uses0;
-          ++uses1;
-          nxt = 0;
-        } else {
-          if (kPair) ptx::mma_commit_pair(bar_tfull(acc), 3);
-          else ptx::mma_commit(bar_tfull(acc));
-          if (acc) ++uses1;
-          else ++uses0;
-          nxt ^= 1;
-        }
-      }
-      if (!ok && any) {
-        if (kPair) ptx::mma_commit_pair(bar_drain, 1);
-        else ptx::mma_commit(bar_drain);
-        spin_bounded(bar_drain, 0);
+        ptx::mma_commit(bar_tfull(acc));
+        if (acc) ++uses1;
+        else ++uses0;
+        acc ^= 1;
       }
     }
-  } else if (warp < 2 + C::kEpiWarps) {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
-    // kTall: warps 2-5 (group 0) and 6-9 (group 1) drain one accumulator each
-    // of a tall tile; short tiles are drained by group 0 alone
-    const int eg = kTall ? (warp - 2) >> 2 : 0;
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int r_in_tile = row_off + q * 32 + lane;
-    const uint32_t tempty_leader =
-        kPair ? ptx::mapa_shared(bar_tempty(0), 0) : 0u;  // + 8 * acc for buffer acc
-    // completions seen so far on each full barrier: slot 0 (every use), slot 1
-    // (short tiles), tall tiles' second accumulator; the slot choice mirrors the
-    // MMA issuer
-    uint32_t n0 = 0, n1 = 0, nt = 0;
-    int nxt = 0;
+    const int r_in_tile = q * 32 + lane;
+    uint32_t uses0 = 0, uses1 = 0;          // completions seen on each full barrier
+    int acc = 0;
     for (int tile = unit; tile < total; tile += n_units) {
-      Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM, p.split,
-                           s2, kTall);
-      t.n0 += n_off;
+      const Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnOut, kTileM, s2);
       const bool second = kCan2 && t.pb == 1;
       const int n_out = second ? p.N2 : p.N;
-      const bool tall = kTall && t.tall;
-      const int acc = tall ? eg : nxt;
-      uint32_t fbar, aphase;
-      if (tall) {
-        fbar = eg ? bar_tfull_tall : bar_tfull(0);
-        aphase = (eg ? nt : n0) & 1u;
-        ++n0;
-        ++nt;
-        nxt = 0;
-      } else {
-        fbar = bar_tfull(acc);
-        aphase = (acc ? n1 : n0) & 1u;
-        if (acc) ++n1;
-        else ++n0;
-        nxt ^= 1;
+      const uint32_t aphase = (acc ? uses1 : uses0) & 1u;
+      // every lane polls with its own clock: the warp goes on only if all of
+      // them saw the accumulator, since the TMEM loads below need the whole warp
+      const bool landed = wait_bar(bar_tfull(acc), aphase, abort_flag, p.status, wait_ns);
+      if (!__all_sync(0xffffffffu, landed)) {
+        *abort_flag = 1;
+        break;
       }
-      if (kTall && !tall && eg == 1) continue;
-      if (!wait_bar(fbar, aphase, abort_flag, p.status)) break;
       ptx::tc_fence_after();
-      const int row = t.row0 + (tall ? eg * BM : 0) + r_in_tile;
+      const int row = t.row0 + r_in_tile;
       const bool valid = row < t.row_end;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kN);
@@ -829,8 +616,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           if (c == kBnOut / kEpiCols - 1) {  // the accumulator is in registers: free it now
             ptx::tc_fence_before();
-            if (kPair && !leader) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
-            else ptx::mbar_arrive(bar_tempty(acc));
+            ptx::mbar_arrive(bar_tempty(acc));
           }
           // row `lane` of the staging buffer, piece k at slot k ^ (lane % kPieces)
 #pragma unroll
@@ -886,12 +672,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
           }
         }
-      }
-      if (!(kEpi == EPI_GATEUP || kEpi == EPI_DOWN)) {
         ptx::tc_fence_before();
-        if (kPair && !leader) ptx::mbar_arrive_remote(tempty_leader + 8u * acc);
-        else ptx::mbar_arrive(bar_tempty(acc));
+        ptx::mbar_arrive(bar_tempty(acc));
       }
+      if (acc) ++uses1;
+      else ++uses0;
+      acc ^= 1;
     }
   } else if (kFp8B) {
     // ------------------------------------------------------------ FP8 converters
@@ -905,8 +691,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
     for (int tile = unit; ok && tile < total; tile += n_units) {
-      const Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnSched, kTileM,
-                                 p.split, s2);
+      const Tile t = locate_unit(tile, ksplit, tile_start, goff, G, n_tiles, kBnOut, kTileM, s2);
       // weight rows (within the group) of tile rows [0, kN/2) and [kN/2, kN)
       const int wrow0 = t.n0;
       const int wrow1 = (kEpi == EPI_GATEUP) ? t.n0 + p.half_off : t.n0 + kN / 2;
@@ -915,8 +700,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int kb_lo = t.ks * nk_split;
       const int kb_hi = min(nk, kb_lo + nk_split);
       for (int kb = kb_lo; kb < kb_hi; ++kb) {
-        if (!wait_bar(bar_full(stage), phase, abort_flag, p.status)) { ok = false; break; }
-        if (!wait_bar(bar_cempty(cst), cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_bar(bar_full(stage), phase, abort_flag, p.status, wait_ns)) {
+          ok = false;
+          break;
+        }
+        if (!wait_bar(bar_cempty(cst), cphase ^ 1u, abort_flag, p.status, wait_ns)) {
+          ok = false;
+          break;
+        }
         const uint8_t* raw = smem + S::STAGE_RAW + stage * S::RAW_BYTES;
         const uint32_t dst = sbase + S::STAGE_B + cst * S::B_BYTES;
         const int cblk = (kb * BK) / 128;
@@ -959,11 +750,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 
   __syncthreads();
-  if (kCluster) ptx::cluster_sync();  // the peer may still use this CTA's smem or TMEM until here
+  if (*abort_flag) {
+    // A role gave up.  Copies and MMAs issued before that may still be in
+    // flight whichever role stopped first, so wait for them (bounded) before
+    // the shared memory and the TMEM they target are released.
+    if (warp == 0 && lane == 0) {
+      int s = prod_stage;
+      uint32_t ph = prod_phase;
+      for (int i = 0; i < min(prod_issued, kStages); ++i) {
+        if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+        spin_bounded(bar_full(s), ph);
+      }
+    }
+    if (warp == 1 && lane == 0 && mma_any) {
+      ptx::mma_commit(bar_drain);
+      spin_bounded(bar_drain, 0);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
-    if (kPair) ptx::tmem_dealloc2(tmem_base, kTmemCols);
-    else ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -1036,15 +843,17 @@ int num_sms() {
   return n;
 }
 
+// limit of the pipeline waits (process-wide; see moe_set_wait_limit_ns)
+std::atomic<unsigned long long> g_wait_ns{kDrainLimitNs};
+unsigned long long pipeline_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 // tile_bound: an upper bound on the number of tiles (of C::kTileM rows); the
-// grid is that many CTAs (pairs when paired), capped at the SM count
-template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
-          int kARows = BM, bool kFp8B = false, bool kTall = false>
+// grid is that many CTAs, capped at the SM count
+template <int kN, int kEpi, bool kGatherA = false, int kARows = BM, bool kFp8B = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta2,
            const CUtensorMap& tb2, Params p, long long tile_bound, cudaStream_t stream) {
-  using C = Cfg<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>;
-  constexpr bool kCluster = kPair || kMcastA;
-  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B, kTall>;
+  using C = Cfg<kN, kEpi, kGatherA, kARows, kFp8B>;
+  auto kern = grouped_gemm_kernel<kN, kEpi, kGatherA, kARows, kFp8B>;
   const int smem = C::S::ALLOC;
   // per instantiation and device, set once (racing threads set the same value)
   static std::atomic<int> configured_dev[64] = {};
@@ -1060,53 +869,26 @@ int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, const C
                        cudaGetErrorString(cudaGetLastError()));
     if (dev >= 0 && dev < 64) configured_dev[dev].store(1, std::memory_order_release);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(C::kThreadsT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // Persistent grid: as many CTAs (pairs) as can be resident at once.  A pair
-  // must sit in one GPC, so with an odd SM count per GPC fewer than SMs / 2
-  // pairs fit; launching more would leave a second, mostly idle wave.
-  static std::atomic<int> max_units_dev[64] = {};
-  int max_units = (dev >= 0 && dev < 64) ? max_units_dev[dev].load(std::memory_order_relaxed) : 0;
-  if (max_units <= 0) {
-    max_units = kCluster ? num_sms() / 2 : num_sms();
-    if (kCluster) {
-      int clusters = 0;
-      cfg.gridDim = dim3(static_cast<unsigned>(2 * max_units), 1, 1);
-      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0)
-        max_units = clusters < max_units ? clusters : max_units;
-      else
-        cudaGetLastError();
-    }
-    if (dev >= 0 && dev < 64) max_units_dev[dev].store(max_units, std::memory_order_relaxed);
-  }
+  // persistent grid: at most one CTA per SM
   long long units = tile_bound;
+  const long long max_units = num_sms();
   if (units > max_units) units = max_units;
   if (units < 1) units = 1;
   DeviceDiag diag = device_diag();
   p.status = diag.status;
   p.launches = diag.launches;
-  cfg.gridDim = dim3(static_cast<unsigned>(kCluster ? 2 * units : units), 1, 1);
-  return launch_status(launch_kernel(kern, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes,
-                                     stream, attr, 1, ta, tb, ta2, tb2, p),
+  p.wait_ns = pipeline_wait_ns();
+  return launch_status(launch_kernel(kern, dim3(static_cast<unsigned>(units), 1, 1),
+                                     dim3(C::kThreadsT, 1, 1), smem, stream, nullptr, 0, ta, tb,
+                                     ta2, tb2, p),
                        op);
 }
 
 // one grouped problem (the second-problem maps are unused copies)
-template <int kN, int kEpi, bool kGatherA = false, bool kPair = false, bool kMcastA = false,
-          int kARows = BM, bool kFp8B = false>
+template <int kN, int kEpi, bool kGatherA = false, int kARows = BM, bool kFp8B = false>
 int launch(const char* op, const CUtensorMap& ta, const CUtensorMap& tb, Params p,
            long long tile_bound, cudaStream_t stream) {
-  return launch<kN, kEpi, kGatherA, kPair, kMcastA, kARows, kFp8B>(op, ta, tb, ta, tb, p,
-                                                                  tile_bound, stream);
+  return launch<kN, kEpi, kGatherA, kARows, kFp8B>(op, ta, tb, ta, tb, p, tile_bound, stream);
 }
 
 int check_common(const char* op, int P, int Kdim, int N, int G, const void* a, const void* b,
@@ -1129,7 +911,18 @@ long long tile_bound(int P, int G, int N, int bn_out, int tile_m = BM) {
 }
 
 // tiling of the grouped GEMMs (process-wide; see moe_set_gemm_pairing)
-std::atomic<int> g_pairing{MOE_GEMM_SINGLE};
+std::atomic<int> g_pairing{MOE_GEMM_AUTO};
+
+// CTA-pair tiles (moe_gemm_pair.cu) for a bf16 grouped GEMM over x_perm-style
+// rows: forced by MOE_GEMM_PAIR; with MOE_GEMM_AUTO when the groups average at
+// least 32 rows and the call has at least 1024 (prefill-sized batches, where the
+// tensor cores bind and the pair tiles' smaller padding and shared-memory fill
+// pay); never for MOE_GEMM_SINGLE.
+bool use_pair_tiles(int P, int G) {
+  const int mode = g_pairing.load(std::memory_order_relaxed);
+  if (mode == MOE_GEMM_PAIR) return true;
+  return mode == MOE_GEMM_AUTO && P >= 1024 && static_cast<long long>(P) >= 32LL * G;
+}
 
 }  // namespace gemm
 
@@ -1183,9 +976,21 @@ extern "C" size_t moe_grouped_gemm_workspace_size(int, int, int, int) { return 0
 
 extern "C" int moe_set_gemm_pairing(int mode) {
   clear_error();
-  if (mode < MOE_GEMM_SINGLE || mode > MOE_GEMM_TALL)
-    return set_error(MOE_ERR_ARG, "moe_set_gemm_pairing: mode %d is not 0, 1, 2, 3 or 4", mode);
+  if (mode == 3 || mode == 4)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "moe_set_gemm_pairing: mode %d is not built (AUTO, SINGLE or PAIR)", mode);
+  if (mode != MOE_GEMM_AUTO && mode != MOE_GEMM_SINGLE && mode != MOE_GEMM_PAIR)
+    return set_error(MOE_ERR_ARG, "moe_set_gemm_pairing: mode %d is not 0, 1 or 2", mode);
   return g_pairing.exchange(mode);
+}
+
+extern "C" int moe_set_wait_limit_ns(unsigned long long ns) {
+  clear_error();
+  if (ns < 1000ull || ns > kDrainLimitNs)
+    return set_error(MOE_ERR_ARG, "moe_set_wait_limit_ns: %llu ns is outside [1000, %llu]", ns,
+                     kDrainLimitNs);
+  g_wait_ns.store(ns, std::memory_order_relaxed);
+  return MOE_OK;
 }
 
 extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
@@ -1205,25 +1010,24 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   if (a_row_gather && (a_rows < 1 || gather_div < 1))
     return set_error(MOE_ERR_ARG, "%s: gathering needs a_rows >= 1 and gather_div >= 1", op);
   if (P == 0) return MOE_OK;
-  const int mode = g_pairing.load(std::memory_order_relaxed);
-  const bool mcast = !a_row_gather && (mode == MOE_GEMM_MCAST || mode == MOE_GEMM_SPLIT) &&
-                     ((I + 127) / 128) % 2 == 0;
+  if (!a_row_gather && use_pair_tiles(P, G))
+    return launch_pair_gateup(op, a_bf16, w13_bf16, group_offsets, P, H, I, G, act_bf16,
+                              static_cast<cudaStream_t>(stream));
   // Few rows per expert (decode): each tile streams its weight rows from HBM
   // and the tile count decides the balance; 128-wide tiles (64 gate + 64 up
   // rows) double it, which cuts the idle tail of the last round (decode layer,
   // 82 of 128 experts touched: 127 -> 115 us).  32-row tiles load 4 KB of A per
   // stage instead of 16, so the ring keeps more weight bytes in flight.
   // Tensor-bound loads keep 128 x 256.
-  const bool narrow = !a_row_gather && mode == MOE_GEMM_SINGLE &&
-                      static_cast<long long>(P) <= 16LL * G;
+  const bool narrow = !a_row_gather && static_cast<long long>(P) <= 16LL * G;
   CUtensorMap ta, tb;
   if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, narrow ? 64 : 128, op,
                       "w13")) != MOE_OK)
     return rc;
   if (a_row_gather) {
     ta = tb;  // unused: the gatherer warps read A rows directly
-  } else if ((rc = make_tmap(&ta, a_bf16, P, H, narrow ? kNarrowRows : (mcast ? BM / 2 : BM), op,
-                             "a")) != MOE_OK) {
+  } else if ((rc = make_tmap(&ta, a_bf16, P, H, narrow ? kNarrowRows : BM, op, "a")) !=
+             MOE_OK) {
     return rc;
   }
   Params p{};
@@ -1243,29 +1047,9 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a_row_gather)
     return launch<256, EPI_GATEUP, true>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
-  if (mode == MOE_GEMM_PAIR)
-    return launch<256, EPI_GATEUP, false, true>(op, ta, tb, p, tile_bound(P, G, I, 128, 2 * BM), s);
-  if (mode == MOE_GEMM_SPLIT) {
-    // whole 256-row blocks on CTA pairs (no padding), the rest on 128-row tiles
-    CUtensorMap ta_pair;
-    if ((rc = make_tmap(&ta_pair, a_bf16, P, H, BM, op, "a")) != MOE_OK) return rc;
-    p.split = 1;
-    rc = launch<256, EPI_GATEUP, false, true>(op, ta_pair, tb, p, tile_bound(P, G, I, 128, 2 * BM), s);
-    if (rc != MOE_OK) return rc;
-    p.split = 2;
-  }
-  if (mcast)
-    return launch<256, EPI_GATEUP, false, false, true>(op, ta, tb, p, tile_bound(P, G, I, 256), s);
   if (narrow)
-    return launch<128, EPI_GATEUP, false, false, false, kNarrowRows>(
-        op, ta, tb, p, tile_bound(P, G, I, 64, kNarrowRows), s);
-  if (mode == MOE_GEMM_TALL && P >= 256) {
-    // whole 256-row blocks as tall tiles (A through 256-row boxes), the rest 128-row
-    CUtensorMap ta_tall;
-    if ((rc = make_tmap(&ta_tall, a_bf16, P, H, 2 * BM, op, "a")) != MOE_OK) return rc;
-    return launch<256, EPI_GATEUP, false, false, false, BM, false, true>(
-        op, ta, tb, ta_tall, tb, p, tile_bound(P, G, I, 128), s);
-  }
+    return launch<128, EPI_GATEUP, false, kNarrowRows>(op, ta, tb, p,
+                                                       tile_bound(P, G, I, 64, kNarrowRows), s);
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
@@ -1283,14 +1067,13 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   if (!group_offsets && G != 1)
     return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
   if (P == 0) return MOE_OK;
-  const int mode = g_pairing.load(std::memory_order_relaxed);
-  const bool mcast =
-      (mode == MOE_GEMM_MCAST || mode == MOE_GEMM_SPLIT) && ((H + 255) / 256) % 2 == 0;
+  if (use_pair_tiles(P, G))
+    return launch_pair_down(op, act_bf16, w2_bf16, group_offsets, pair_weight, row_to_pair, P, I,
+                            H, G, out_bf16, static_cast<cudaStream_t>(stream));
   // few rows per expert: 32-row tiles, as in the gate/up GEMM
-  const bool narrow = mode == MOE_GEMM_SINGLE && static_cast<long long>(P) <= 16LL * G;
+  const bool narrow = static_cast<long long>(P) <= 16LL * G;
   CUtensorMap ta, tb;
-  if ((rc = make_tmap(&ta, act_bf16, P, I, narrow ? kNarrowRows : (mcast ? BM / 2 : BM), op,
-                      "act")) != MOE_OK)
+  if ((rc = make_tmap(&ta, act_bf16, P, I, narrow ? kNarrowRows : BM, op, "act")) != MOE_OK)
     return rc;
   if ((rc = make_tmap(&tb, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) != MOE_OK)
     return rc;
@@ -1307,27 +1090,9 @@ extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_b
   p.row_to_pair = row_to_pair;
   p.kid = MOE_KID_GEMM_DOWN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mode == MOE_GEMM_PAIR)
-    return launch<256, EPI_DOWN, false, true>(op, ta, tb, p, tile_bound(P, G, H, 256, 2 * BM), s);
-  if (mode == MOE_GEMM_SPLIT) {
-    CUtensorMap ta_pair;
-    if ((rc = make_tmap(&ta_pair, act_bf16, P, I, BM, op, "act")) != MOE_OK) return rc;
-    p.split = 1;
-    rc = launch<256, EPI_DOWN, false, true>(op, ta_pair, tb, p, tile_bound(P, G, H, 256, 2 * BM), s);
-    if (rc != MOE_OK) return rc;
-    p.split = 2;
-  }
-  if (mcast)
-    return launch<256, EPI_DOWN, false, false, true>(op, ta, tb, p, tile_bound(P, G, H, 512), s);
   if (narrow)
-    return launch<256, EPI_DOWN, false, false, false, kNarrowRows>(
-        op, ta, tb, p, tile_bound(P, G, H, 256, kNarrowRows), s);
-  if (mode == MOE_GEMM_TALL && P >= 256) {
-    CUtensorMap ta_tall;
-    if ((rc = make_tmap(&ta_tall, act_bf16, P, I, 2 * BM, op, "act")) != MOE_OK) return rc;
-    return launch<256, EPI_DOWN, false, false, false, BM, false, true>(
-        op, ta, tb, ta_tall, tb, p, tile_bound(P, G, H, 256), s);
-  }
+    return launch<256, EPI_DOWN, false, kNarrowRows>(op, ta, tb, p,
+                                                     tile_bound(P, G, H, 256, kNarrowRows), s);
   return launch<256, EPI_DOWN>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
 }
 
@@ -1496,10 +1261,9 @@ extern "C" int moe_grouped_gemm_gateup_silu_fp8w(const void* a_bf16, const uint8
   p.kid = MOE_KID_GEMM_GATEUP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (narrow)
-    return launch<128, EPI_GATEUP, false, false, false, kNarrowRows, true>(
+    return launch<128, EPI_GATEUP, false, kNarrowRows, true>(
         op, ta, tb, p, tile_bound(P, G, I, 64, kNarrowRows), s);
-  return launch<256, EPI_GATEUP, false, false, false, BM, true>(op, ta, tb, p,
-                                                                tile_bound(P, G, I, 128), s);
+  return launch<256, EPI_GATEUP, false, BM, true>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
 }
 
 extern "C" int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
@@ -1540,8 +1304,7 @@ extern "C" int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w
   p.kid = MOE_KID_GEMM_DOWN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (narrow)
-    return launch<256, EPI_DOWN, false, false, false, kNarrowRows, true>(
+    return launch<256, EPI_DOWN, false, kNarrowRows, true>(
         op, ta, tb, p, tile_bound(P, G, H, 256, kNarrowRows), s);
-  return launch<256, EPI_DOWN, false, false, false, BM, true>(op, ta, tb, p,
-                                                              tile_bound(P, G, H, 256), s);
+  return launch<256, EPI_DOWN, false, BM, true>(op, ta, tb, p, tile_bound(P, G, H, 256), s);
 }

@@ -1,0 +1,628 @@
+// moe_gemm_pair.cu -- the grouped BF16 GEMMs of the MoE expert block on CTA
+// pairs, for batches with many rows per expert (prefill).  Same two ops and
+// the same numeric contract as the single-CTA tiles of moe_gemm.cu (vllm.cpp
+// issue #3094 "Row: BACKEND-ROCM-BF16-MOE": gate and up narrowed to bf16
+// before the activation; the routing weight applied once, before the down
+// result is stored).
+//
+// A tile puts weight rows (output features) on the MMA's M side and routed
+// tokens on its N side.  One tcgen05.mma.cta_group::2 with M = 256 spans the
+// two SMs of a cluster: each SM holds 128 weight rows (its half of A) and half
+// of the tile's tokens (its half of B), and its tensor memory receives its 128
+// weight rows x all N tokens.  A tile covers up to 256 consecutive rows of one
+// group, with N their count rounded up to 16, so a group is padded to 16 rows
+// rather than to a multiple of the 128 or 256 rows of a token-major tile.  Per
+// SM and 64-wide K step a stage holds 16 KB of weights and at most 16 KB of
+// tokens, against 48 KB for a 128 x 256 single-CTA tile doing the same MMA
+// work, so the shared-memory fill per MMA drops by a third.
+//
+//   warp 0      TMA producer, in both CTAs: each loads its own half of every
+//               stage, and the bytes of both halves are counted on the even
+//               CTA's stage barrier
+//   warp 1      TMEM allocation in both CTAs; in the even CTA, the one thread
+//               that issues the pair's MMAs
+//   warps 2-5   epilogue, in both CTAs: tcgen05.ld of 32 tokens of one weight
+//               row per thread, the fused op, and a transpose through shared
+//               memory into token-major output rows stored as 16-byte vectors
+//
+// gate/up: a CTA's 128 weight rows are the gate rows of 64 output features
+// followed by the up rows of the same 64, so TMEM lanes 0-63 hold gate and
+// lanes 64-127 up.  The warps that read up lanes narrow them to bf16 and pass
+// them through shared memory to the warps that read the matching gate lanes.
+//
+// The tile schedule is built on the device from the group offsets, as in
+// moe_gemm.cu: groups in order, each group's token blocks of 256, each block's
+// feature blocks; pair u takes tiles u, u + pairs, ...  Waits are bounded like
+// moe_gemm.cu's; a CTA that gives up tells its peer, the MMAs are drained, and
+// both CTAs let their in-flight copies land before they free tensor memory.
+#include <atomic>
+
+#include "gemm_common.cuh"
+
+namespace moe {
+namespace gemm {
+namespace {
+
+constexpr int kPairThreads = 192;
+constexpr int kTokBlock = 256;        // tokens per tile at most (MMA N)
+// token rows per TMA box: three tensor maps over the token rows, with boxes of
+// 32, 64 and 128 rows; a stage takes the smallest that covers its N / 2 rows
+constexpr int kTokBoxMin = 32;
+constexpr int kPStages = 6;
+constexpr int kWBytes = 128 * BK * 2; // one CTA's weight rows per stage: 16 KB
+constexpr int kTBytes = 128 * BK * 2; // one CTA's token rows per stage, at most: 16 KB
+// after a CTA gives up: how long it lets its TMA copies land before the pair
+// frees its shared and tensor memory (copies are counted on the even CTA's
+// barriers, so the odd CTA cannot wait for its own copies directly)
+constexpr unsigned long long kCopyGraceNs = 100000ull;
+
+enum PairEpi { PEPI_GATEUP = 0, PEPI_DOWN = 1 };
+
+struct PairParams {
+  const int32_t* group_offsets;  // [G+1], or null: one group [0, P)
+  int P;                         // routed rows (tokens of the product)
+  int Kdim;                      // contraction length
+  int N;                         // output columns (I for gate/up, H for down)
+  int G;
+  int w_rows_per_group;          // rows of the weight matrix per group (2I or H)
+  int half_off;                  // gate/up: offset of the up rows inside a group (I)
+  void* out;                     // bf16 [P, N] (down: rows by dst)
+  const float* pair_weight;      // down: [P] by destination row, or null
+  const int32_t* row_to_pair;    // down: destination row of each product row, or null
+  unsigned long long wait_ns;
+  unsigned int* status;
+  unsigned long long* launches;
+  int kid;
+};
+
+struct PSmem {
+  static constexpr int STAGE_W = 0;                                  // kPStages x 16 KB
+  static constexpr int STAGE_T = STAGE_W + kPStages * kWBytes;       // kPStages x 16 KB
+  static constexpr int EPI = STAGE_T + kPStages * kTBytes;           // 8 KB
+  static constexpr int META_DST = EPI + 8192;                        // int[256]
+  static constexpr int META_W = META_DST + kTokBlock * 4;            // float[256]
+  // full[kPStages], empty[kPStages], tfull[2], tempty[2], drain
+  static constexpr int BARS = META_W + kTokBlock * 4;
+  static constexpr int NBARS = 2 * kPStages + 5;
+  static constexpr int MISC = BARS + NBARS * 8;                      // tmem slot, abort flag, scan
+  static constexpr int TILE_START = MISC + 64;
+  static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
+  static constexpr int BYTES = GOFF + (kMaxGroups + 1) * 4;
+  static constexpr int ALLOC = BYTES + 1024;
+};
+static_assert(PSmem::ALLOC <= 227 * 1024, "pair GEMM shared memory");
+
+struct PTile {
+  int g, r0, n_tok, n0;
+};
+
+__device__ __forceinline__ int pair_m_tiles(int rows) {
+  return rows <= 0 ? 0 : (rows + kTokBlock - 1) / kTokBlock;
+}
+
+__device__ __forceinline__ PTile pair_tile(int tile, const int* tile_start, const int* goff, int G,
+                                           int n_fb, int fb_cols) {
+  int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  const int local = tile - tile_start[lo];
+  const int m = local / n_fb;
+  PTile t;
+  t.g = lo;
+  t.r0 = goff[lo] + m * kTokBlock;
+  t.n_tok = min(goff[lo + 1], t.r0 + kTokBlock) - t.r0;
+  t.n0 = (local - m * n_fb) * fb_cols;
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+// kEpi: PEPI_GATEUP (weights W13 [G, 2I, K], fb_cols = 128 output features per
+// tile, 64 per CTA) or PEPI_DOWN (weights W2 [G, H, K], 256 per tile, 128 per CTA)
+template <int kEpi>
+__global__ void __launch_bounds__(kPairThreads, 1)
+pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
+                 const __grid_constant__ CUtensorMap tmT64,
+                 const __grid_constant__ CUtensorMap tmT128,
+                 const __grid_constant__ CUtensorMap tmW, const PairParams p) {
+  constexpr bool kGU = kEpi == PEPI_GATEUP;
+  constexpr int kFbCols = kGU ? 128 : 256;   // output features per tile (both CTAs)
+  constexpr int kWBox = kGU ? 64 : 128;      // weight rows per TMA box
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PSmem::BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PSmem::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PSmem::MISC + 4);
+  int* scan_tmp = reinterpret_cast<int*>(smem + PSmem::MISC + 8);
+  int* tile_start = reinterpret_cast<int*>(smem + PSmem::TILE_START);
+  int* goff = reinterpret_cast<int*>(smem + PSmem::GOFF);
+  int* s_dst = reinterpret_cast<int*>(smem + PSmem::META_DST);
+  float* s_w = reinterpret_cast<float*>(smem + PSmem::META_W);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int unit = static_cast<int>(blockIdx.x >> 1);
+  const int n_units = static_cast<int>(gridDim.x >> 1);
+  const unsigned long long wait_ns = p.wait_ns;
+  auto bar_full = [&](int s) { return ptx::smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return ptx::smem_u32(bars + kPStages + s); };
+  auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kPStages + a); };
+  auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kPStages + 2 + a); };
+  const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kPStages + 4);
+
+  count_launch(p.launches, p.kid);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      ptx::mbar_init(bar_full(s), 1);    // the even CTA's expect-tx arrive
+      ptx::mbar_init(bar_empty(s), 1);   // the pair's MMA commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar_tfull(a), 1);
+      ptx::mbar_init(bar_tempty(a), 8);  // one arrive per epilogue warp of both CTAs
+    }
+    ptx::mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmT32);
+    ptx::tma_prefetch_desc(&tmT64);
+    ptx::tma_prefetch_desc(&tmT128);
+    ptx::tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc2(ptx::smem_u32(tmem_slot), 2 * kTokBlock);
+    ptx::tmem_relinquish2();
+  }
+
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // ---- device-side tile schedule (every CTA computes the same one)
+  const int G = p.G;
+  for (int g = threadIdx.x; g <= G; g += kPairThreads)
+    goff[g] = p.group_offsets ? __ldg(p.group_offsets + g) : (g == 0 ? 0 : p.P);
+  __syncthreads();
+  const int n_fb = (p.N + kFbCols - 1) / kFbCols;
+  const int chunk = (G + kPairThreads - 1) / kPairThreads;
+  const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
+  const int g_hi = min(G, g_lo + chunk);
+  int local = 0;
+  for (int g = g_lo; g < g_hi; ++g) local += pair_m_tiles(goff[g + 1] - goff[g]) * n_fb;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scan_tmp[warp] = incl;
+  __syncthreads();
+  int warp_base = 0, total = 0;
+  for (int w = 0; w < kPairThreads / 32; ++w) {
+    const int v = scan_tmp[w];
+    if (w < warp) warp_base += v;
+    total += v;
+  }
+  int run = warp_base + incl - local;
+  for (int g = g_lo; g < g_hi; ++g) {
+    tile_start[g] = run;
+    run += pair_m_tiles(goff[g + 1] - goff[g]) * n_fb;
+  }
+  if (threadIdx.x == 0) tile_start[G] = total;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the peer's barriers exist before any remote arrive or copy
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nk = (p.Kdim + BK - 1) / BK;
+
+  bool mma_any = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    // Lane 0 waits for the stage and arms the even CTA's barrier; then the
+    // stage's two or three boxes (weight rows in one or two boxes, token rows in
+    // one) are issued by lanes 0-2 as a single warp instruction.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = unit; ok && tile < total; tile += n_units) {
+      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+      const int half = ((t.n_tok + 15) & ~15) >> 1;      // tokens this CTA holds
+      const int tbox = half <= 32 ? 32 : (half <= 64 ? 64 : 128);
+      const CUtensorMap* mt = tbox == 32 ? &tmT32 : (tbox == 64 ? &tmT64 : &tmT128);
+      const uint32_t bytes = kWBytes + tbox * (BK * 2);
+      const int trow = t.r0 + static_cast<int>(rank) * half;
+      // this CTA's 128 weight rows: gate/up, 64 gate rows then the same
+      // features' 64 up rows; down, 128 consecutive output rows
+      const int wrow0 = t.g * p.w_rows_per_group + t.n0 + static_cast<int>(rank) * (kFbCols / 2);
+      const int wrow1 = wrow0 + p.half_off;
+      // this lane's box: lane 0 the (first) weight box, lane 1 the up box, lane 2 the tokens
+      const bool issues = lane == 0 || lane == 2 || (kGU && lane == 1);
+      const CUtensorMap* mbox = lane == 2 ? mt : &tmW;
+      const int ybox = lane == 0 ? wrow0 : (lane == 1 ? wrow1 : trow);
+      const uint32_t dbox = lane == 2 ? PSmem::STAGE_T : PSmem::STAGE_W + lane * (kWBox * 128);
+      const uint32_t dstep = lane == 2 ? kTBytes : kWBytes;
+      for (int kb = 0; kb < nk; ++kb) {
+        bool got = true;
+        if (lane == 0) {
+          got = wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns);
+          if (got && leader) ptx::mbar_arrive_expect_tx(bar_full(stage), 2 * bytes);
+        }
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (issues)
+          ptx::tma_load_2d_pair(sbase + dbox + stage * dstep, mbox, kb * BK, ybox,
+                                ptx::mapa_shared(bar_full(stage), 0));
+        if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t uses0 = 0, uses1 = 0;
+      int acc = 0;
+      bool ok = true;
+      for (int tile = unit; ok && tile < total; tile += n_units) {
+        const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+        const int N = (t.n_tok + 15) & ~15;
+        const uint32_t idesc = ptx::idesc_bf16_f32(256, N);
+        if (!wait_bar<true>(bar_tempty(acc), ((acc ? uses1 : uses0) & 1u) ^ 1u, abort_flag,
+                            p.status, wait_ns)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTokBlock);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bar(bar_full(stage), phase, abort_flag, p.status, wait_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t dw = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_W + stage * kWBytes);
+          const uint64_t dt = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_T + stage * kTBytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            ptx::mma_bf16_pair(d, dw + 2ull * k, dt + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_any = true;
+          ptx::mma_commit_pair(bar_empty(stage), 3);   // frees the stage in both CTAs
+          if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(bar_tfull(acc), 3);       // the accumulator is ready in both
+        if (acc) ++uses1;
+        else ++uses0;
+        acc ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = static_cast<int>(threadIdx.x) - 64;  // 0..127
+    const int q = warp & 3;                             // TMEM lane quarter of this warp
+    const bool is_up = kGU && q >= 2;
+    // feature of this thread's TMEM lane within the CTA's output columns
+    const int f = kGU ? (q & 1) * 32 + lane : q * 32 + lane;
+    const uint32_t tempty_leader = ptx::mapa_shared(bar_tempty(0), 0);  // + 8 * acc
+    const uint32_t epi = sbase + PSmem::EPI;
+    const uint32_t xch = epi;            // gate/up: up rows, 64 x 32 bf16 (4 KB)
+    const uint32_t ost = kGU ? epi + 4096 : epi;  // output staging, token-major
+    uint32_t uses0 = 0, uses1 = 0;
+    int acc = 0;
+    // down: destination rows of this thread's two token slots of the next tile,
+    // loaded one tile ahead so their latency hides behind the accumulator wait
+    auto dst_of = [&](const PTile& nt, int j) {
+      const int r = nt.r0 + j;
+      return j < nt.n_tok ? (p.row_to_pair ? __ldg(p.row_to_pair + r) : r) : -1;
+    };
+    int nd0 = -1, nd1 = -1;
+    if (!kGU && unit < total) {
+      const PTile t0 = pair_tile(unit, tile_start, goff, G, n_fb, kFbCols);
+      nd0 = dst_of(t0, et);
+      nd1 = dst_of(t0, et + 128);
+    }
+    for (int tile = unit; tile < total; tile += n_units) {
+      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+      const int col0 = t.n0 + static_cast<int>(rank) * (kFbCols / 2);  // this CTA's first column
+      int d0 = -1, d1 = -1;
+      float w0 = 1.0f, w1 = 1.0f;
+      if (!kGU) {
+        // this tile's destination rows (loaded a tile ago) and their weights;
+        // then the next tile's destination rows
+        d0 = nd0;
+        d1 = nd1;
+        if (p.pair_weight) {
+          if (d0 >= 0) w0 = __ldg(p.pair_weight + d0);
+          if (d1 >= 0) w1 = __ldg(p.pair_weight + d1);
+        }
+        if (tile + n_units < total) {
+          const PTile tn = pair_tile(tile + n_units, tile_start, goff, G, n_fb, kFbCols);
+          nd0 = dst_of(tn, et);
+          nd1 = dst_of(tn, et + 128);
+        }
+      }
+      const bool landed =
+          wait_bar(bar_tfull(acc), (acc ? uses1 : uses0) & 1u, abort_flag, p.status, wait_ns);
+      if (!kGU) {
+        // the previous tile's readers of s_dst / s_w passed its last named barrier
+        if (d0 >= 0) { s_dst[et] = d0; s_w[et] = w0; }
+        if (d1 >= 0) { s_dst[et + 128] = d1; s_w[et + 128] = w1; }
+      }
+      // one decision for the four warps (they meet at named barriers below); the
+      // barrier also publishes s_dst / s_w
+      if (!ptx::bar_and(1, 128, landed)) {
+        *abort_flag = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTokBlock);
+#pragma unroll 1
+      for (int j0 = 0; j0 < t.n_tok; j0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + j0, v);
+        ptx::tmem_ld_wait();
+        if (j0 + 32 >= t.n_tok) {  // the last TMEM read of this tile: free the accumulator
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
+        }
+        if (kGU) {
+          if (is_up) {
+            // up values narrowed to bf16, row f of the exchange buffer (16-byte
+            // pieces XOR-swizzled by (f / 2) % 4 against bank conflicts)
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ptx::st_shared_v4(xch + f * 64 + ((k ^ ((f >> 1) & 3)) << 4), pk[4 * k],
+                                pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
+          ptx::bar_sync(1, 128);
+          if (!is_up) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 u4 = ptx::ld_shared_v4(xch + f * 64 + ((k ^ ((f >> 1) & 3)) << 4));
+              const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int i = 4 * k + m;            // tokens 2i and 2i + 1
+                // narrowing before the activation: gate (here) and up (there) are bf16
+                const uint32_t gp =
+                    pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                const float g0 = __uint_as_float(gp << 16), g1 = __uint_as_float(gp & 0xFFFF0000u);
+                const float u0 = __uint_as_float(uw[m] << 16);
+                const float u1 = __uint_as_float(uw[m] & 0xFFFF0000u);
+                // SiLU is tolerance-checked: the fast reciprocal division serves
+                const float a0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+                const float a1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+                const uint32_t ap = pack_bf16x2(a0, a1);
+                const int j = 2 * i;
+                ptx::st_shared_u16(ost + j * 128 + (((f >> 3) ^ (j & 7)) << 4) + (f & 7) * 2,
+                                   static_cast<uint16_t>(ap & 0xFFFFu));
+                ptx::st_shared_u16(
+                    ost + (j + 1) * 128 + (((f >> 3) ^ ((j + 1) & 7)) << 4) + (f & 7) * 2,
+                    static_cast<uint16_t>(ap >> 16));
+              }
+            }
+          }
+          ptx::bar_sync(1, 128);
+          // 32 token rows x 64 columns: eight threads store one row's 128 bytes
+          uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int idx = et + 128 * i;
+            const int j = idx >> 3, k = idx & 7;
+            const int col = col0 + 8 * k;
+            if (j0 + j < t.n_tok && col < p.N) {
+              const uint4 val = ptx::ld_shared_v4(ost + j * 128 + ((k ^ (j & 7)) << 4));
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(t.r0 + j0 + j) * p.N + col) =
+                  val;
+            }
+          }
+          ptx::bar_sync(1, 128);
+        } else {
+          // the routing weight: one f32 multiply, then the one bf16 rounding
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = 2 * i;
+            float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+            if (p.pair_weight) {
+              a = __fmul_rn(a, s_w[min(j0 + j, kTokBlock - 1)]);
+              b = __fmul_rn(b, s_w[min(j0 + j + 1, kTokBlock - 1)]);
+            }
+            const uint32_t pk = pack_bf16x2(a, b);
+            ptx::st_shared_u16(ost + j * 256 + (((f >> 3) ^ (j & 15)) << 4) + (f & 7) * 2,
+                               static_cast<uint16_t>(pk & 0xFFFFu));
+            ptx::st_shared_u16(
+                ost + (j + 1) * 256 + (((f >> 3) ^ ((j + 1) & 15)) << 4) + (f & 7) * 2,
+                static_cast<uint16_t>(pk >> 16));
+          }
+          ptx::bar_sync(1, 128);
+          // 32 token rows x 128 columns: sixteen threads store one row's 256 bytes
+          uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = et + 128 * i;
+            const int j = idx >> 4, k = idx & 15;
+            const int col = col0 + 8 * k;
+            if (j0 + j < t.n_tok && col < p.N) {
+              const uint4 val = ptx::ld_shared_v4(ost + j * 256 + ((k ^ (j & 15)) << 4));
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(s_dst[j0 + j]) * p.N + col) =
+                  val;
+            }
+          }
+          ptx::bar_sync(1, 128);
+        }
+      }
+      if (acc) ++uses1;
+      else ++uses0;
+      acc ^= 1;
+    }
+  }
+
+  // ---- exit: if either CTA of the pair gave up, drain before freeing memory
+  __syncthreads();
+  ptx::cluster_sync();
+  const bool gave_up =
+      *abort_flag != 0 ||
+      ld_shared_cluster_u32(ptx::mapa_shared(ptx::smem_u32(const_cast<int*>(abort_flag)),
+                                             rank ^ 1u)) != 0;
+  if (gave_up) {
+    if (warp == 1 && lane == 0 && leader && mma_any) {
+      ptx::mma_commit_pair(bar_drain, 1);
+      spin_bounded(bar_drain, 0);
+    }
+    if (warp == 0 && lane == 0) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::globaltimer_ns() - t0 < kCopyGraceNs) {
+      }
+    }
+  }
+  __syncthreads();
+  ptx::cluster_sync();  // the peer may still use this CTA's shared memory or TMEM until here
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc2(tmem_base, 2 * kTokBlock);
+  }
+}
+
+}  // namespace
+
+// The pair kernels' grid: clusters of two CTAs, as many as can be resident.
+template <int kEpi>
+int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtensorMap& tw,
+                       PairParams p, long long tiles, cudaStream_t stream) {
+  auto kern = pair_gemm_kernel<kEpi>;
+  const int smem = PSmem::ALLOC;
+  static std::atomic<int> configured_dev[64] = {};
+  static std::atomic<int> max_pairs_dev[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  const bool cache = dev >= 0 && dev < 64;
+  if (!cache || !configured_dev[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "%s: cannot reserve %d bytes of shared memory: %s", op, smem,
+                       cudaGetErrorString(cudaGetLastError()));
+    if (cache) configured_dev[dev].store(1, std::memory_order_release);
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // a pair must sit in one GPC, so fewer than SMs / 2 pairs may fit at once;
+  // launching more would leave a second, mostly idle wave
+  int max_pairs = cache ? max_pairs_dev[dev].load(std::memory_order_relaxed) : 0;
+  if (max_pairs <= 0) {
+    max_pairs = num_sms() / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * max_pairs), 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0)
+      max_pairs = clusters < max_pairs ? clusters : max_pairs;
+    else
+      cudaGetLastError();
+    if (cache) max_pairs_dev[dev].store(max_pairs, std::memory_order_relaxed);
+  }
+  long long pairs = tiles < max_pairs ? tiles : max_pairs;
+  if (pairs < 1) pairs = 1;
+  DeviceDiag diag = device_diag();
+  p.status = diag.status;
+  p.launches = diag.launches;
+  p.wait_ns = pipeline_wait_ns();
+  return launch_status(launch_kernel(kern, dim3(static_cast<unsigned>(2 * pairs), 1, 1),
+                                     dim3(kPairThreads, 1, 1), smem, stream, attr, 1, tt[0], tt[1],
+                                     tt[2], tw, p),
+                       op);
+}
+
+// Upper bound on the pair tiles of a call: token blocks of 256 per group times
+// the feature blocks.
+static long long pair_tile_bound(int P, int G, int N, int fb_cols) {
+  const long long blocks = (P + kTokBlock - 1) / kTokBlock + (G < P ? G : P);
+  return blocks * ((N + fb_cols - 1) / fb_cols);
+}
+
+// the token rows [rows, cols] behind three maps with 32-, 64- and 128-row boxes
+static int make_token_maps(CUtensorMap (&tt)[3], const void* base, int rows, int cols,
+                           const char* op, const char* what) {
+  int rc;
+  for (int i = 0; i < 3; ++i)
+    if ((rc = make_tmap(&tt[i], base, rows, cols, kTokBoxMin << i, op, what)) != MOE_OK) return rc;
+  return MOE_OK;
+}
+
+int launch_pair_gateup(const char* op, const void* a_bf16, const void* w13_bf16,
+                       const int32_t* group_offsets, int P, int H, int I, int G, void* act_bf16,
+                       cudaStream_t stream) {
+  CUtensorMap tt[3], tw;
+  int rc;
+  if ((rc = make_token_maps(tt, a_bf16, P, H, op, "a")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tw, w13_bf16, static_cast<long long>(G) * 2 * I, H, 64, op, "w13")) !=
+      MOE_OK)
+    return rc;
+  PairParams p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = H;
+  p.N = I;
+  p.G = G;
+  p.w_rows_per_group = 2 * I;
+  p.half_off = I;
+  p.out = act_bf16;
+  p.kid = MOE_KID_GEMM_GATEUP;
+  return launch_pair_kernel<PEPI_GATEUP>(op, tt, tw, p, pair_tile_bound(P, G, I, 128), stream);
+}
+
+int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
+                     const int32_t* group_offsets, const float* pair_weight,
+                     const int32_t* row_to_pair, int P, int I, int H, int G, void* out_bf16,
+                     cudaStream_t stream) {
+  CUtensorMap tt[3], tw;
+  int rc;
+  if ((rc = make_token_maps(tt, act_bf16, P, I, op, "act")) != MOE_OK) return rc;
+  if ((rc = make_tmap(&tw, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) != MOE_OK)
+    return rc;
+  PairParams p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = I;
+  p.N = H;
+  p.G = G;
+  p.w_rows_per_group = H;
+  p.half_off = 0;
+  p.out = out_bf16;
+  p.pair_weight = pair_weight;
+  p.row_to_pair = row_to_pair;
+  p.kid = MOE_KID_GEMM_DOWN;
+  return launch_pair_kernel<PEPI_DOWN>(op, tt, tw, p, pair_tile_bound(P, G, H, 256), stream);
+}
+
+}  // namespace gemm
+}  // namespace moe

@@ -10,46 +10,33 @@
 //
 // The scratch is a file-scope __device__ array of MOE_PERMUTE_NOALLOC_MAX_SCRATCH
 // bytes (1 MiB).  Every GPU that loads the library holds it until the process
-// exits.  All calls share it, so two calls whose kernels overlap on the GPU
+// exits.  The permute's histogram takes 4 bytes per expert for every chunk of
+// 512 pairs, so the array serves P = T*K <= 512 * floor(2^18 / E) pairs
+// (131072 at E = 1024, 524288 at E = 256).  All calls share it, so two calls whose kernels overlap on the GPU
 // (different streams without ordering between them) race on it.  The array
 // keeps the previous call's contents; nothing needs clearing, because the count
 // kernel writes every histogram entry the later kernels read.
-#include <mutex>
-
 #include "moe_common.cuh"
 
 namespace {
 
 static __device__ __align__(256) int32_t g_permute_scratch[MOE_PERMUTE_NOALLOC_MAX_SCRATCH / 4];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// on every call, with the calling thread's current device: a cached address
+// would go stale if the caller reset the device or its primary context was
+// rebuilt, since the library's module (and the array) is then loaded anew.
 int scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess)
-    return moe::set_error(MOE_ERR_CUDA, "moe_permute_noalloc: cudaGetDevice failed: %s",
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return moe::set_error(MOE_ERR_CUDA,
+                          "moe_permute_noalloc: cudaGetSymbolAddress of the scratch failed: %s",
                           cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return moe::set_error(MOE_ERR_ARG, "moe_permute_noalloc: device %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return moe::set_error(MOE_ERR_CUDA,
-                            "moe_permute_noalloc: cudaGetSymbolAddress of the scratch failed: %s",
-                            cudaGetErrorString(e));
-    }
-    g_scratch_addr[dev] = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MOE_OK;
 }
 

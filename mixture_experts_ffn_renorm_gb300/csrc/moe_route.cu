@@ -76,11 +76,11 @@ __device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
 }
 
 // One warp selects the top-K of one token.  The weights' exps are then
-// evaluated by the whole block, one (token, rank) pair per thread, so that the
-// double-precision chain of exp_cr runs on full warps (GB300's FP64 rate is
-// low, and a warp instruction costs the same with 8 or 32 lanes active).
+// evaluated by the whole block, one (token, rank) pair per thread, so that
+// they run on full warps (a warp instruction costs the same with 8 or 32
+// lanes active).
 // kEx: the extended forms of RouteEx.  Each lane turns its logits into scores
-// (sigmoid_cr for sigmoid scoring) and keys (score + selection bias); the keys
+// (sigmoid_f32 for sigmoid scoring) and keys (score + selection bias); the keys
 // go to shared memory, where lane g scores expert group g; the warp picks the
 // topk_group best groups, and the expert choice skips experts of the others.
 template <int kPerLane, bool kEx>
@@ -159,7 +159,7 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
         sc[i] = 0.0f;
         float kv = 0.0f;
         if (e < E) {
-          sc[i] = rx.scoring == 1 ? sigmoid_cr(v[i]) : v[i];
+          sc[i] = rx.scoring == 1 ? sigmoid_f32(v[i]) : v[i];
           kv = rx.select_bias ? __fadd_rn(sc[i], __ldg(rx.select_bias + e)) : sc[i];
           s_key[e] = kv;
         }
@@ -259,8 +259,8 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
   for (int q = threadIdx.x; q < n_live * K; q += blockDim.x) {
     const int tt = q / K, j = q - tt * K;
     const float d = __fsub_rn(s_sel[tt][j], s_sel[tt][0]);
-    // rank 0: d is +0 for a finite top logit and exp_cr(+0) is exactly 1
-    s_ex[tt][j] = (j == 0 && d == 0.0f) ? 1.0f : exp_cr(d);
+    // rank 0: d is +0 for a finite top logit and exp(+0) is exactly 1
+    s_ex[tt][j] = (j == 0 && d == 0.0f) ? 1.0f : exp_f32(d);
   }
   __syncthreads();
   if (!live) return;
@@ -273,7 +273,7 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
   } else {
     float ev[kPerLane];
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) ev[i] = exp_cr(__fsub_rn(v[i], m));
+    for (int i = 0; i < kPerLane; ++i) ev[i] = exp_f32(__fsub_rn(v[i], m));
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i)
       for (int l = 0; l < 32; ++l) {

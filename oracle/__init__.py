@@ -49,6 +49,7 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_exp_f32": ([_F], _F),
         "oracle_exp_f32_array": ([_P, _P, _I64], None),
         "oracle_sigmoid_f32": ([_F], _F),
+        "oracle_sigmoid_f32_array": ([_P, _P, _I64], None),
         "oracle_route_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
         "oracle_route_topk_ex": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
         "oracle_e4m3_to_f32": ([ctypes.c_uint8], _F),
@@ -132,6 +133,13 @@ def exp_f32(x: np.ndarray) -> np.ndarray:
 
 def sigmoid_f32(g: float) -> np.float32:
     return np.float32(lib().oracle_sigmoid_f32(float(g)))
+
+
+def sigmoid_f32_array(g: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(g, np.float32)
+    out = np.empty_like(g)
+    lib().oracle_sigmoid_f32_array(_ptr(g), _ptr(out), g.size)
+    return out
 
 
 # ---------------------------------------------------------------- steps

@@ -155,6 +155,11 @@ float oracle_sigmoid_f32(float g) {
   return 1.0f / d;
 }
 
+void oracle_sigmoid_f32_array(const float* g, float* y, int64_t n) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) y[i] = oracle_sigmoid_f32(g[i]);
+}
+
 /* ------------------------------------------------------------------ */
 /* dtype-generic element access (f32 and bf16 arms; f16 is refused)    */
 /* ------------------------------------------------------------------ */

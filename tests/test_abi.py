@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_refusals_without_gpu(lib):
-    assert m.abi_version() == 8
+    assert m.abi_version() == 9
     # dtype refusals name the missing arm and return before touching the device
     rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
     assert rc == m.ERR_DTYPE and "f16" in m.last_error()
@@ -73,8 +73,17 @@ def test_process_switches(lib):
     assert prev is True                       # on by default
     assert m.moe_set_pdl(True) is False
     assert lib.moe_set_pdl(2) == m.ERR_ARG and "enable" in m.last_error()
-    assert m.moe_set_gemm_pairing(m.GEMM_SINGLE) == m.GEMM_SINGLE
+    assert m.moe_set_gemm_pairing(m.GEMM_PAIR) == m.GEMM_AUTO     # the default
+    assert m.moe_set_gemm_pairing(m.GEMM_SINGLE) == m.GEMM_PAIR
+    assert m.moe_set_gemm_pairing(m.GEMM_AUTO) == m.GEMM_SINGLE
     assert lib.moe_set_gemm_pairing(7) == m.ERR_ARG
+    # the tilings measured slower and removed are refused by name
+    for mode in (3, 4):
+        assert lib.moe_set_gemm_pairing(mode) == m.ERR_UNSUPPORTED
+    # the pipeline wait limit: 1 us .. 1 s
+    assert lib.moe_set_wait_limit_ns(999) == m.ERR_ARG and "outside" in m.last_error()
+    assert lib.moe_set_wait_limit_ns(2 * 10**9) == m.ERR_ARG
+    assert m.moe_set_wait_limit_ns(10**9) == m.OK
 
 
 def test_workspace_queries(lib):

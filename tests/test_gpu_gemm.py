@@ -15,7 +15,8 @@ import mixture_experts_ffn_renorm_gb300 as m
 import oracle as O
 from mixture_experts_ffn_renorm_gb300 import workloads as W
 
-from .gpu_util import assert_gemm_close, empty, launched_since, launches, to_dev, to_host
+from .gpu_util import (assert_gemm_close, bf16_to_f64, empty, launched_since, launches, to_dev,
+                       to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -28,12 +29,15 @@ def _lib():
     assert m.moe_device_status() == 0
 
 
-@pytest.fixture(params=[m.GEMM_SINGLE, m.GEMM_MCAST, m.GEMM_PAIR, m.GEMM_SPLIT, m.GEMM_TALL],
-                ids=["single", "mcast", "pair", "split", "tall"])
-def pairing(request):
-    """Every tiling of the grouped GEMMs: single CTAs (the default), A-multicast
-    clusters, CTA pairs (2-SM, 256-row tiles), and whole 256-row blocks on CTA
-    pairs with the rest on A-multicast clusters."""
+TILINGS = [m.GEMM_SINGLE, m.GEMM_PAIR]
+TILING_IDS = ["single", "pair"]
+
+
+@pytest.fixture(params=TILINGS, ids=TILING_IDS)
+def tiling(request):
+    """Every built tiling of the grouped GEMMs: single-CTA tiles with rows on the
+    MMA's M side, and CTA-pair tiles with weight rows on M and up to 256 rows of
+    a group on N (forced here for every shape, down to one-row groups)."""
     prev = m.moe_set_gemm_pairing(request.param)
     yield request.param
     m.moe_set_gemm_pairing(prev)
@@ -51,7 +55,7 @@ def _case(sizes, H, I, seed):
 
 
 SHAPES = [
-    # group sizes, H, I  (I / 128 and H / 256 even or odd: multicast or its fallback)
+    # group sizes, H, I
     ([4], 64, 32),
     ([3, 200, 0, 77], 512, 256),
     ([600, 5, 256, 255, 513], 256, 256),
@@ -67,7 +71,7 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("sizes,H,I", SHAPES + [([300, 0, 520], 2048, 768)])
-def test_gateup_silu(sizes, H, I, pairing):
+def test_gateup_silu(sizes, H, I, tiling):
     off, P, G, A, W13, _ = _case(sizes, H, I, sum(sizes) + H)
     want = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G)
     act = empty((P, I), torch.bfloat16)
@@ -75,7 +79,7 @@ def test_gateup_silu(sizes, H, I, pairing):
     before = launches()
     m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I, G,
                                         act)
-    assert launched_since(before, "gemm_gateup") == (2 if pairing == m.GEMM_SPLIT else 1)
+    assert launched_since(before, "gemm_gateup") == 1
     assert m.moe_device_status() == 0
     assert_gemm_close(to_host(act), want, "gate/up")
 
@@ -84,7 +88,7 @@ def test_gateup_silu(sizes, H, I, pairing):
 @pytest.mark.parametrize("K", [1, 3, 8])
 def test_gateup_silu_gathered_rows(sizes, H, I, K):
     # product row r reads x[pair[r] // K]: the routed rows come straight from the
-    # token matrix through TMA gather4 (no x_perm)
+    # token matrix, copied by the producer warps with cp.async (no x_perm)
     off, P, G, _, W13, _ = _case(sizes, H, I, sum(sizes) + 7 * H + K)
     rng = np.random.default_rng(P + K)
     T = max(1, (P + K - 1) // K) + 3
@@ -102,7 +106,7 @@ def test_gateup_silu_gathered_rows(sizes, H, I, K):
 
 
 @pytest.mark.parametrize("sizes,H,I", SHAPES + [([300, 0, 520], 2048, 768)])
-def test_down_weight_scatter(sizes, H, I, pairing):
+def test_down_weight_scatter(sizes, H, I, tiling):
     off, P, G, _, _, W2 = _case(sizes, H, I, sum(sizes) + I)
     rng = np.random.default_rng(1)
     act = W.to_bf16_bits(rng.standard_normal((P, I)).astype(np.float32))
@@ -116,7 +120,7 @@ def test_down_weight_scatter(sizes, H, I, pairing):
         m.moe_grouped_gemm_down_bf16(to_dev(act), to_dev(W2), to_dev(off),
                                      None if pw is None else to_dev(pw),
                                      None if rp is None else to_dev(rp), P, I, H, G, out)
-        assert launched_since(before, "gemm_down") == (2 if pairing == m.GEMM_SPLIT else 1)
+        assert launched_since(before, "gemm_down") == 1
         assert m.moe_device_status() == 0
         assert_gemm_close(to_host(out), want, "down")
 
@@ -272,7 +276,7 @@ def test_fp8_refusals():
     assert launches() == before
 
 
-def test_gateup_narrowing_is_visible_on_the_gpu(pairing):
+def test_gateup_narrowing_is_visible_on_the_gpu(tiling):
     # g = u = 1 + 2^-9 exactly: narrowing before the activation gives
     # bf16(silu(1) * 1) = 0x3F3B; without it the result would be 0x3F3C
     H, I = 64, 32
@@ -288,7 +292,7 @@ def test_gateup_narrowing_is_visible_on_the_gpu(pairing):
     assert np.all(to_host(act) == 0x3F3B)
 
 
-def test_single_group_without_offsets_and_rows_outside_groups(pairing):
+def test_single_group_without_offsets_and_rows_outside_groups(tiling):
     H, I, P = 128, 64, 200
     rng = np.random.default_rng(2)
     A = W.to_bf16_bits(rng.standard_normal((P, H)).astype(np.float32))
@@ -305,6 +309,76 @@ def test_single_group_without_offsets_and_rows_outside_groups(pairing):
     h = to_host(act)
     assert np.all(h[150:] == 0)
     assert_gemm_close(h[:150], want[:150], "partial group")
+
+
+def test_down_rounds_once_after_the_weight_on_the_gpu(tiling):
+    # Issue #3094: the routing weight is applied before the down result is
+    # stored, so the one bf16 rounding comes after the weight.  The dot product
+    # y = 1 + 2^-8 + 2^-10 is exact in any summation order, so the tensor-core
+    # result is fixed bit for bit: bf16(y * 0.75) = 0x3F41, where rounding y to
+    # bf16 before the weight would give 0x3F42 (worked in the oracle's pin).
+    I, H, P = 64, 256, 130
+    act = np.zeros((P, I), np.float32)
+    act[:, :3] = [1.0, 2.0**-8, 2.0**-10]
+    w2 = np.zeros((2, H, I), np.float32)
+    w2[:, :, :3] = 1.0
+    off = np.array([0, 70, P], np.int32)
+    r2p = np.random.default_rng(5).permutation(P).astype(np.int32)
+    out = empty((P, H), torch.bfloat16)
+    m.moe_grouped_gemm_down_bf16(to_dev(W.to_bf16_bits(act)), to_dev(W.to_bf16_bits(w2)),
+                                 to_dev(off), to_dev(np.full(P, 0.75, np.float32)), to_dev(r2p),
+                                 P, I, H, 2, out)
+    assert m.moe_device_status() == 0
+    assert np.all(to_host(out) == 0x3F41)
+    m.moe_grouped_gemm_down_bf16(to_dev(W.to_bf16_bits(act)), to_dev(W.to_bf16_bits(w2)),
+                                 to_dev(off), None, None, P, I, H, 2, out)
+    assert np.all(to_host(out) == 0x3F81)     # no weight: bf16(y) = 1 + 1/128
+
+
+def _zipf_sizes(G, total, s, seed):
+    rng = np.random.default_rng(seed)
+    p = 1.0 / np.arange(1, G + 1) ** s
+    sizes = rng.multinomial(total, p / p.sum())
+    return [int(v) for v in rng.permutation(sizes)]
+
+
+MULTI_ROUND = [
+    # (group sizes, H, I): tiles outnumber the 152 SMs several times over, so every
+    # persistent CTA walks several tiles and wraps its stage ring and both TMEM
+    # accumulators many times
+    (_zipf_sizes(64, 24000, 1.1, 3), 768, 384),        # 220 M-tiles x 3 N-tiles each GEMM
+    ([1 + (g % 2) for g in range(128)], 2048, 768),     # decode-like: 32-row tiles, 1536 and 1024 tiles
+]
+
+
+@pytest.mark.parametrize("sizes,H,I", MULTI_ROUND, ids=["zipf24k", "decode128"])
+def test_multi_round_schedule_every_row(sizes, H, I, tiling):
+    off, P, G, A, W13, W2 = _case(sizes, H, I, 11 + H)
+    act = empty((P, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I,
+                                        G, act)
+    assert m.moe_device_status() == 0
+    got_act = to_host(act)
+    want_act = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G)
+    assert_gemm_close(got_act, want_act, "multi-round gate/up")
+    # every row on its own too: a wrong tile leaves a row far off even when the
+    # whole-matrix NMSE is small
+    g, r = bf16_to_f64(got_act), bf16_to_f64(want_act)
+    row_err = np.sum((g - r) ** 2, 1) / np.maximum(np.sum(r * r, 1), 1e-30)
+    assert row_err.max() <= 1e-4, (int(row_err.argmax()), float(row_err.max()))
+    rng = np.random.default_rng(P)
+    wts = rng.uniform(0.05, 1.0, P).astype(np.float32)
+    r2p = rng.permutation(P).astype(np.int32)
+    out = empty((P, H), torch.bfloat16)
+    m.moe_grouped_gemm_down_bf16(act, to_dev(W2), to_dev(off), to_dev(wts), to_dev(r2p), P, I, H,
+                                 G, out)
+    assert m.moe_device_status() == 0
+    want = O.down(got_act, W2, off, P=P, I=I, H=H, G=G, pair_weight=wts, row_to_pair=r2p)
+    got = to_host(out)
+    assert_gemm_close(got, want, "multi-round down")
+    g, r = bf16_to_f64(got), bf16_to_f64(want)
+    row_err = np.sum((g - r) ** 2, 1) / np.maximum(np.sum(r * r, 1), 1e-30)
+    assert row_err.max() <= 1e-4, (int(row_err.argmax()), float(row_err.max()))
 
 
 def test_gemm_refusals_and_empty():

@@ -532,6 +532,33 @@ def test_routing_weight_applied_exactly_once():
     assert not np.array_equal(twice, out_b)
 
 
+def test_down_rounds_once_after_the_weight():
+    # Issue #3094 (numeric contract): the routing weight is applied before the
+    # down result is stored, so the store rounding comes after the weight:
+    # out = bf16(y * w), one rounding.  Here y = 1 + 2^-8 + 2^-10 exactly (a dot
+    # product of three exact terms) and w = 0.75, worked by hand:
+    #   y * w = 0.753662109375 = 2^-1 * (1 + 64.9375 / 128)  -> bf16 0x3F41 (0.75390625)
+    # A store-width rounding before the weight gives a different value:
+    #   bf16(y) = 1 + 1/128;  (1 + 1/128) * 0.75 = 2^-1 * (1 + 65.5 / 128), a tie
+    #   -> even 66 / 128  -> bf16 0x3F42 (0.7578125)
+    I, H = 8, 16
+    act = np.zeros((1, I), np.float32)
+    act[0, :3] = [1.0, 2.0**-8, 2.0**-10]
+    w2 = np.zeros((1, H, I), np.float32)
+    w2[0, :, :3] = 1.0
+    off = np.array([0, 1], np.int32)
+    out = O.down(W.to_bf16_bits(act), W.to_bf16_bits(w2), off, P=1, I=I, H=H, G=1,
+                 pair_weight=np.array([0.75], np.float32))
+    assert np.all(out == 0x3F41)
+    # the mutant that rounds y to bf16 before the weight gives 0x3F42 here
+    y_bf16 = W.to_bf16_bits(np.array([1.0 + 2.0**-8 + 2.0**-10], np.float32))
+    mutant = W.to_bf16_bits(O.bf16_to_f32(y_bf16) * np.float32(0.75))
+    assert mutant[0] == 0x3F42 and not np.any(out == mutant[0])
+    # and with no weight the one rounding is of y itself: 1 + 1/128
+    plain = O.down(W.to_bf16_bits(act), W.to_bf16_bits(w2), off, P=1, I=I, H=H, G=1)
+    assert np.all(plain == 0x3F81)
+
+
 def test_sparse_path_equals_dense_evaluation_of_every_expert():
     cfg = W.TINY
     d = W.layer_inputs(cfg)

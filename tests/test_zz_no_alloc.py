@@ -40,7 +40,12 @@ def _run(fn, ids, x, T, K, E, H, with_ws):
     return [t.cpu() for t in (off, sp, p2r, xp)]
 
 
-@pytest.mark.parametrize("T,K,E,H", [(8192, 8, 128, 64), (2048, 8, 256, 128), (37, 3, 1000, 16)])
+# every case but the last has more than 32 chunks of 512 pairs, so it runs the
+# multi-kernel permute whose histogram lives in the fixed scratch (32 chunks or
+# fewer take the one-block permute, which keeps its histogram in shared memory);
+# (16384, 8, 1024) fills the scratch to its last byte
+@pytest.mark.parametrize("T,K,E,H", [(8192, 8, 128, 64), (4100, 8, 256, 128),
+                                     (16384, 8, 1024, 16), (37, 3, 1000, 16)])
 def test_noalloc_permute_matches_workspace_permute(T, K, E, H):
     m.lib()
     ids = torch.from_numpy(_ids(T, K, E, T + E)).cuda()
@@ -54,7 +59,10 @@ def test_noalloc_permute_matches_workspace_permute(T, K, E, H):
 
 def test_noalloc_permute_refuses_sizes_beyond_its_scratch():
     m.lib()
-    T, K, E = 65536, 8, 1024      # 1024 chunks x 1024 experts x 4 B = 4 MiB > 1 MiB
+    # the limit P <= 512 * floor(2^18 / E): 16384 x 8 = 131072 pairs at E = 1024
+    # fill the scratch exactly (accepted above); one more token is refused
+    assert m.moe_permute_workspace_size(16384, 8, 1024) == m.PERMUTE_NOALLOC_MAX_SCRATCH
+    T, K, E = 16385, 8, 1024
     assert m.moe_permute_workspace_size(T, K, E) > m.PERMUTE_NOALLOC_MAX_SCRATCH
     d = torch.zeros((16,), dtype=torch.int32, device="cuda")
     with pytest.raises(m.MoeError) as ei:
