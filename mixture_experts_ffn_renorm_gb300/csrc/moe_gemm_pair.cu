@@ -21,7 +21,8 @@
 //               CTA's stage barrier
 //   warp 1      TMEM allocation in both CTAs; in the even CTA, the one thread
 //               that issues the pair's MMAs
-//   warps 2-5   epilogue, in both CTAs: tcgen05.ld of 32 tokens of one weight
+//   warps 2-9   epilogue, in both CTAs: two groups of four warps take a tile's
+//               32-token chunks in turn; tcgen05.ld of 32 tokens of one weight
 //               row per thread, the fused op, and a transpose through shared
 //               memory into token-major output rows stored as 16-byte vectors
 //
@@ -43,7 +44,7 @@ namespace moe {
 namespace gemm {
 namespace {
 
-constexpr int kPairThreads = 192;
+constexpr int kPairThreads = 320;     // producer, MMA, two groups of four epilogue warps
 constexpr int kTokBlock = 256;        // tokens per tile at most (MMA N)
 // token rows per TMA box: three tensor maps over the token rows, with boxes of
 // 32, 64 and 128 rows; a stage takes the smallest that covers its N / 2 rows
@@ -78,11 +79,11 @@ struct PairParams {
 struct PSmem {
   static constexpr int STAGE_W = 0;                                  // kPStages x 16 KB
   static constexpr int STAGE_T = STAGE_W + kPStages * kWBytes;       // kPStages x 16 KB
-  static constexpr int EPI = STAGE_T + kPStages * kTBytes;           // 8 KB
-  static constexpr int META_DST = EPI + 8192;                        // int[256]
-  static constexpr int META_W = META_DST + kTokBlock * 4;            // float[256]
+  static constexpr int EPI = STAGE_T + kPStages * kTBytes;           // 2 groups x 8 KB
+  static constexpr int META_DST = EPI + 2 * 8192;                    // int[2][256]
+  static constexpr int META_W = META_DST + 2 * kTokBlock * 4;        // float[2][256]
   // full[kPStages], empty[kPStages], tfull[2], tempty[2], drain
-  static constexpr int BARS = META_W + kTokBlock * 4;
+  static constexpr int BARS = META_W + 2 * kTokBlock * 4;
   static constexpr int NBARS = 2 * kPStages + 5;
   static constexpr int MISC = BARS + NBARS * 8;                      // tmem slot, abort flag, scan
   static constexpr int TILE_START = MISC + 64;
@@ -169,7 +170,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_tfull(a), 1);
-      ptx::mbar_init(bar_tempty(a), 8);  // one arrive per epilogue warp of both CTAs
+      ptx::mbar_init(bar_tempty(a), 16);  // one arrive per epilogue warp of both CTAs
     }
     ptx::mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -313,71 +314,78 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int et = static_cast<int>(threadIdx.x) - 64;  // 0..127
-    const int q = warp & 3;                             // TMEM lane quarter of this warp
+    // Two groups of four warps (2-5 and 6-9) take the tile's 32-token chunks in
+    // turn, each with its own staging buffers and named barrier; all eight meet
+    // once per tile (barrier 3) to decide together and to publish the tile's
+    // destination rows and weights.
+    const int eg = (warp - 2) >> 2;                              // epilogue group
+    const int et = static_cast<int>(threadIdx.x) - 64 - 128 * eg;  // 0..127 in the group
+    const int ea = static_cast<int>(threadIdx.x) - 64;           // 0..255 over both
+    const int q = warp & 3;                                      // TMEM lane quarter
     const bool is_up = kGU && q >= 2;
     // feature of this thread's TMEM lane within the CTA's output columns
     const int f = kGU ? (q & 1) * 32 + lane : q * 32 + lane;
+    const int bar_g = 1 + eg;
     const uint32_t tempty_leader = ptx::mapa_shared(bar_tempty(0), 0);  // + 8 * acc
-    const uint32_t epi = sbase + PSmem::EPI;
-    const uint32_t xch = epi;            // gate/up: up rows, 64 x 32 bf16 (4 KB)
+    const uint32_t epi = sbase + PSmem::EPI + eg * 8192;
+    const uint32_t xch = epi;                     // gate/up: up rows, 64 x 32 bf16 (4 KB)
     const uint32_t ost = kGU ? epi + 4096 : epi;  // output staging, token-major
+    // this thread's 16-bit slot in staging row j, for each j modulo the swizzle
+    // period (16-byte pieces XOR-swizzled by the row)
+    constexpr int kRowB = kGU ? 128 : 256;
+    constexpr int kSw = kRowB / 16;
+    uint32_t slot[kSw];
+#pragma unroll
+    for (int jj = 0; jj < kSw; ++jj) slot[jj] = ost + (((f >> 3) ^ jj) << 4) + (f & 7) * 2;
     uint32_t uses0 = 0, uses1 = 0;
     int acc = 0;
-    // down: destination rows of this thread's two token slots of the next tile,
-    // loaded one tile ahead so their latency hides behind the accumulator wait
-    auto dst_of = [&](const PTile& nt, int j) {
-      const int r = nt.r0 + j;
-      return j < nt.n_tok ? (p.row_to_pair ? __ldg(p.row_to_pair + r) : r) : -1;
+    // down: the destination row of this thread's token slot of the next tile,
+    // loaded a tile ahead so its latency hides behind the accumulator wait
+    auto dst_of = [&](const PTile& nt) {
+      const int r = nt.r0 + ea;
+      return ea < nt.n_tok ? (p.row_to_pair ? __ldg(p.row_to_pair + r) : r) : -1;
     };
-    int nd0 = -1, nd1 = -1;
-    if (!kGU && unit < total) {
-      const PTile t0 = pair_tile(unit, tile_start, goff, G, n_fb, kFbCols);
-      nd0 = dst_of(t0, et);
-      nd1 = dst_of(t0, et + 128);
-    }
+    int nd = -1;
+    if (!kGU && unit < total) nd = dst_of(pair_tile(unit, tile_start, goff, G, n_fb, kFbCols));
     for (int tile = unit; tile < total; tile += n_units) {
       const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
       const int col0 = t.n0 + static_cast<int>(rank) * (kFbCols / 2);  // this CTA's first column
-      int d0 = -1, d1 = -1;
-      float w0 = 1.0f, w1 = 1.0f;
+      int* dst_t = s_dst + acc * kTokBlock;     // meta of this tile (double-buffered by slot)
+      float* w_t = s_w + acc * kTokBlock;
+      int d = -1;
+      float w = 1.0f;
       if (!kGU) {
-        // this tile's destination rows (loaded a tile ago) and their weights;
-        // then the next tile's destination rows
-        d0 = nd0;
-        d1 = nd1;
-        if (p.pair_weight) {
-          if (d0 >= 0) w0 = __ldg(p.pair_weight + d0);
-          if (d1 >= 0) w1 = __ldg(p.pair_weight + d1);
-        }
-        if (tile + n_units < total) {
-          const PTile tn = pair_tile(tile + n_units, tile_start, goff, G, n_fb, kFbCols);
-          nd0 = dst_of(tn, et);
-          nd1 = dst_of(tn, et + 128);
-        }
+        d = nd;
+        if (p.pair_weight && d >= 0) w = __ldg(p.pair_weight + d);
+        if (tile + n_units < total)
+          nd = dst_of(pair_tile(tile + n_units, tile_start, goff, G, n_fb, kFbCols));
       }
       const bool landed =
           wait_bar(bar_tfull(acc), (acc ? uses1 : uses0) & 1u, abort_flag, p.status, wait_ns);
-      if (!kGU) {
-        // the previous tile's readers of s_dst / s_w passed its last named barrier
-        if (d0 >= 0) { s_dst[et] = d0; s_w[et] = w0; }
-        if (d1 >= 0) { s_dst[et + 128] = d1; s_w[et + 128] = w1; }
+      if (!kGU && d >= 0) {
+        // this buffer's last readers (two tiles ago) passed the previous tile's barrier 3
+        dst_t[ea] = d;
+        w_t[ea] = w;
       }
-      // one decision for the four warps (they meet at named barriers below); the
-      // barrier also publishes s_dst / s_w
-      if (!ptx::bar_and(1, 128, landed)) {
+      // one decision for the eight warps; the barrier also publishes dst_t / w_t
+      if (!ptx::bar_and(3, 256, landed)) {
         *abort_flag = 1;
         break;
       }
       ptx::tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTokBlock);
+      if (32 * eg >= t.n_tok) {  // no chunk for this group: its warps free the accumulator now
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
+      }
 #pragma unroll 1
-      for (int j0 = 0; j0 < t.n_tok; j0 += 32) {
+      for (int j0 = 32 * eg; j0 < t.n_tok; j0 += 64) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + j0, v);
         ptx::tmem_ld_wait();
-        if (j0 + 32 >= t.n_tok) {  // the last TMEM read of this tile: free the accumulator
+        if (j0 + 64 >= t.n_tok) {  // this warp's last TMEM read of the tile: free the accumulator
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
@@ -395,7 +403,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
               ptx::st_shared_v4(xch + f * 64 + ((k ^ ((f >> 1) & 3)) << 4), pk[4 * k],
                                 pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
           }
-          ptx::bar_sync(1, 128);
+          ptx::bar_sync(bar_g, 128);
           if (!is_up) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -415,15 +423,14 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
                 const float a1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
                 const uint32_t ap = pack_bf16x2(a0, a1);
                 const int j = 2 * i;
-                ptx::st_shared_u16(ost + j * 128 + (((f >> 3) ^ (j & 7)) << 4) + (f & 7) * 2,
+                ptx::st_shared_u16(slot[j & (kSw - 1)] + j * kRowB,
                                    static_cast<uint16_t>(ap & 0xFFFFu));
-                ptx::st_shared_u16(
-                    ost + (j + 1) * 128 + (((f >> 3) ^ ((j + 1) & 7)) << 4) + (f & 7) * 2,
-                    static_cast<uint16_t>(ap >> 16));
+                ptx::st_shared_u16(slot[(j + 1) & (kSw - 1)] + (j + 1) * kRowB,
+                                   static_cast<uint16_t>(ap >> 16));
               }
             }
           }
-          ptx::bar_sync(1, 128);
+          ptx::bar_sync(bar_g, 128);
           // 32 token rows x 64 columns: eight threads store one row's 128 bytes
           uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
@@ -437,25 +444,34 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
                   val;
             }
           }
-          ptx::bar_sync(1, 128);
+          ptx::bar_sync(bar_g, 128);
         } else {
           // the routing weight: one f32 multiply, then the one bf16 rounding
+          float wv[32];
+          if (p.pair_weight) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 w4 = ptx::ld_shared_v4(ptx::smem_u32(w_t + j0) + 16 * k);
+              wv[4 * k] = __uint_as_float(w4.x);
+              wv[4 * k + 1] = __uint_as_float(w4.y);
+              wv[4 * k + 2] = __uint_as_float(w4.z);
+              wv[4 * k + 3] = __uint_as_float(w4.w);
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int j = 2 * i;
             float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
             if (p.pair_weight) {
-              a = __fmul_rn(a, s_w[min(j0 + j, kTokBlock - 1)]);
-              b = __fmul_rn(b, s_w[min(j0 + j + 1, kTokBlock - 1)]);
+              a = __fmul_rn(a, wv[j]);
+              b = __fmul_rn(b, wv[j + 1]);
             }
             const uint32_t pk = pack_bf16x2(a, b);
-            ptx::st_shared_u16(ost + j * 256 + (((f >> 3) ^ (j & 15)) << 4) + (f & 7) * 2,
-                               static_cast<uint16_t>(pk & 0xFFFFu));
-            ptx::st_shared_u16(
-                ost + (j + 1) * 256 + (((f >> 3) ^ ((j + 1) & 15)) << 4) + (f & 7) * 2,
-                static_cast<uint16_t>(pk >> 16));
+            ptx::st_shared_u16(slot[j & (kSw - 1)] + j * kRowB, static_cast<uint16_t>(pk & 0xFFFFu));
+            ptx::st_shared_u16(slot[(j + 1) & (kSw - 1)] + (j + 1) * kRowB,
+                               static_cast<uint16_t>(pk >> 16));
           }
-          ptx::bar_sync(1, 128);
+          ptx::bar_sync(bar_g, 128);
           // 32 token rows x 128 columns: sixteen threads store one row's 256 bytes
           uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
@@ -465,11 +481,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
             const int col = col0 + 8 * k;
             if (j0 + j < t.n_tok && col < p.N) {
               const uint4 val = ptx::ld_shared_v4(ost + j * 256 + ((k ^ (j & 15)) << 4));
-              *reinterpret_cast<uint4*>(out + static_cast<size_t>(s_dst[j0 + j]) * p.N + col) =
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(dst_t[j0 + j]) * p.N + col) =
                   val;
             }
           }
-          ptx::bar_sync(1, 128);
+          ptx::bar_sync(bar_g, 128);
         }
       }
       if (acc) ++uses1;
