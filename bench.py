@@ -42,7 +42,8 @@ def recorded_traffic(workload, weights="bf16"):
     import hashlib
 
     if weights == "bf16":
-        name, srcs = "gemm_gateup_traffic.txt", ("moe_gemm.cu", "sm100_ptx.cuh")
+        name = "gemm_gateup_traffic.txt"
+        srcs = ("moe_gemm.cu", "moe_gemm_pair.cu", "gemm_common.cuh", "sm100_ptx.cuh")
     elif weights in Q_WEIGHTS:
         name, srcs = f"qgemm_gateup_{weights}_traffic.txt", ("moe_qgemm.cu", "sm100_ptx.cuh")
     else:
@@ -631,8 +632,13 @@ def run_ours(args):
     flop_gateup, flop_down = ga["flop_gateup"], ga["flop_down"]
     bytes_gateup, bytes_down = ga["bytes_gateup"], ga["bytes_down"]
     t_gu, t_dn = ga["t_gu"], ga["t_dn"]
+    # which bf16 gate/up kernel runs: the library's default tiling takes CTA-pair
+    # tiles for P >= 1024 rows averaging >= 32 per group, unless the shared expert
+    # rides in the same launch (single-CTA tiles)
+    pair = P >= 1024 and P >= 32 * cfg.E and not cfg.I_shared
     kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
              f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qk else
+             "pair_gemm_kernel<gateup> (CTA-pair gate/up GEMM + SiLU-mul)" if pair else
              "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)")
     traffic_key = "bf16" if qd else args.weights
     if tensor_bound:

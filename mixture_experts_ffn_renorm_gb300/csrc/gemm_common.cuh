@@ -51,6 +51,28 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// The same bounded wait by spinning on the non-blocking probe, for a thread
+// whose reaction time is on the critical path (a TMA producer feeding a
+// latency-bound stage ring wakes sooner than from a suspending probe); the
+// abort flag and the clock are checked every 64 probes.
+__device__ __forceinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, unsigned int* status,
+                                              unsigned long long limit_ns) {
+  if (ptx::mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_test_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      if (status) atomicOr(status, static_cast<unsigned int>(MOE_STATUS_TIMEOUT));
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // Drain wait: polls until the phase completes or kDrainLimitNs passes.
 __device__ __forceinline__ void spin_bounded(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();

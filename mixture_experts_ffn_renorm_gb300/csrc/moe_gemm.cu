@@ -450,7 +450,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           brow1 = brow0 + p.half_off;
         }
         for (int kb = second ? 0 : kb_lo; kb < nk_t; ++kb) {
-          if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns)) {
+          // spinning: the producer's reaction time is part of the ring's round trip
+          if (!wait_bar_spin(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns)) {
             ok = false;
             break;
           }

@@ -26,10 +26,15 @@
 //               row per thread, the fused op, and a transpose through shared
 //               memory into token-major output rows stored as 16-byte vectors
 //
-// gate/up: a CTA's 128 weight rows are the gate rows of 64 output features
-// followed by the up rows of the same 64, so TMEM lanes 0-63 hold gate and
-// lanes 64-127 up.  The warps that read up lanes narrow them to bf16 and pass
-// them through shared memory to the warps that read the matching gate lanes.
+// gate/up: a CTA's 128 weight rows are the up rows of 64 output features
+// followed by the gate rows of the same 64, so TMEM lanes 0-63 hold up and
+// lanes 64-127 gate.  The warps that read up lanes narrow them to bf16 and pass
+// them through shared memory to the warps that read the matching gate lanes,
+// which do the SiLU-mul.  Warp w issues on the SM's sub-partition w % 4 and
+// may read only TMEM lane quarter w % 4, so this order puts the SiLU work on
+// sub-partitions 2 and 3 and keeps 0 and 1, where the producer and the MMA
+// issuer run, for the light narrowing warps: the ring is latency-bound, and
+// every issue slot the producer waits for lengthens its round trip.
 //
 // The tile schedule is built on the device from the group offsets, as in
 // moe_gemm.cu: groups in order, each group's token blocks of 256, each block's
@@ -245,11 +250,13 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       const CUtensorMap* mt = tbox == 32 ? &tmT32 : (tbox == 64 ? &tmT64 : &tmT128);
       const uint32_t bytes = kWBytes + tbox * (BK * 2);
       const int trow = t.r0 + static_cast<int>(rank) * half;
-      // this CTA's 128 weight rows: gate/up, 64 gate rows then the same
-      // features' 64 up rows; down, 128 consecutive output rows
-      const int wrow0 = t.g * p.w_rows_per_group + t.n0 + static_cast<int>(rank) * (kFbCols / 2);
-      const int wrow1 = wrow0 + p.half_off;
-      // this lane's box: lane 0 the (first) weight box, lane 1 the up box, lane 2 the tokens
+      // this CTA's 128 weight rows: gate/up, the 64 up rows of its features
+      // then their 64 gate rows; down, 128 consecutive output rows
+      const int wrow_g = t.g * p.w_rows_per_group + t.n0 + static_cast<int>(rank) * (kFbCols / 2);
+      const int wrow0 = kGU ? wrow_g + p.half_off : wrow_g;
+      const int wrow1 = wrow_g;
+      // this lane's box: lane 0 the first weight box (up rows, or the down rows),
+      // lane 1 the gate box, lane 2 the tokens
       const bool issues = lane == 0 || lane == 2 || (kGU && lane == 1);
       const CUtensorMap* mbox = lane == 2 ? mt : &tmW;
       const int ybox = lane == 0 ? wrow0 : (lane == 1 ? wrow1 : trow);
@@ -258,7 +265,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       for (int kb = 0; kb < nk; ++kb) {
         bool got = true;
         if (lane == 0) {
-          got = wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns);
+          // spinning: the producer's reaction time is part of the ring's round trip
+          got = wait_bar_spin(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns);
           if (got && leader) ptx::mbar_arrive_expect_tx(bar_full(stage), 2 * bytes);
         }
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
@@ -322,7 +330,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     const int et = static_cast<int>(threadIdx.x) - 64 - 128 * eg;  // 0..127 in the group
     const int ea = static_cast<int>(threadIdx.x) - 64;           // 0..255 over both
     const int q = warp & 3;                                      // TMEM lane quarter
-    const bool is_up = kGU && q >= 2;
+    const bool is_up = kGU && q < 2;
     // feature of this thread's TMEM lane within the CTA's output columns
     const int f = kGU ? (q & 1) * 32 + lane : q * 32 + lane;
     const int bar_g = 1 + eg;

@@ -66,6 +66,19 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
   return ok != 0;
 }
 
+// non-blocking probe: true once the phase with this parity has completed
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // relaxed poll at cluster scope, for barriers a peer CTA arrives on remotely;
 // the caller follows a successful poll with fence_acquire_cluster() (one fence
 // per completed wait instead of an acquire on every poll)
