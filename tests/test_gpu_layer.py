@@ -80,10 +80,13 @@ def _stagewise(cfg, n_tok_sample, n_row_sample):
     rng = np.random.default_rng(99)
     toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, min(T, n_tok_sample), replace=False)]))
 
-    # router: logits (re-run with logits_out) within the bound; ids/w exact from them
+    # router: logits (re-run with logits_out, otherwise the forward's own call, so
+    # that it takes the same path) within the bound; ids/w exact from them
     ws = blk.workspace
-    m.moe_route_topk(x_dev, blk.w_router, blk.logit_bias, None, None, T, H, E, K, 1, 0, 1,
-                     blk.topk_ids, blk.topk_w, logits, None, ws, ws.numel())
+    gl_rerun = torch.empty((T,), dtype=torch.float32, device="cuda") if cfg.I_shared else None
+    m.moe_route_topk(x_dev, blk.w_router, blk.logit_bias,
+                     blk.w_shared_gate if cfg.I_shared else None, None, T, H, E, K, 1, 0, 1,
+                     blk.topk_ids, blk.topk_w, logits, gl_rerun, ws, ws.numel())
     lo = to_host(logits)
     want_ids, want_w, _, _ = O.route_topk(logits_in=lo, T=T, H=1, E=E, K=K)
     assert np.array_equal(ids, want_ids) and np.array_equal(wts.view(np.uint32), want_w.view(np.uint32))
