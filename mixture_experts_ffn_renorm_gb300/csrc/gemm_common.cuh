@@ -23,10 +23,12 @@ constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 // Bounded mbarrier wait of a pipeline role.  Returns false when this CTA is
 // aborting: another role gave up, or this wait ran past `limit_ns` of device
 // time, in which case it raises MOE_STATUS_TIMEOUT and the CTA's abort flag.
-// Each probe may suspend the thread until the phase completes, for at most
-// the limit (the probe's suspend-time hint), so a wait gives up between one
-// and two limits after it began, and the clock and the abort flag are checked
-// after every probe that comes back empty.
+// A first, non-blocking probe serves a phase that is already complete; the
+// clock starts before any probe that may suspend the thread.  Such a probe
+// suspends until the phase completes or for about the limit (its suspend-time
+// hint; the hardware may take the hint loosely), and the clock and the abort
+// flag are checked after every probe that comes back empty, so a wait gives up
+// one to two limits after it began.
 // kCluster: acquire at cluster scope (the barrier is arrived on by the peer CTA).
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -38,7 +40,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     ptx::fence_acquire_cluster();
     return true;
   };
-  if (probe()) return true;
+  if (kCluster ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_test_wait(bar, parity)) {
+    if (kCluster) ptx::fence_acquire_cluster();
+    return true;
+  }
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
     if (probe()) return true;
@@ -100,7 +105,10 @@ unsigned long long pipeline_wait_ns();
 
 // the CTA-pair kernels (moe_gemm_pair.cu): arguments already checked by the
 // entry points of moe_gemm.cu
-int launch_pair_gateup(const char* op, const void* a_bf16, const void* w13_bf16,
+// (a_row_gather non-null: routed row r is row a_row_gather[r] / gather_div of
+// a_bf16 [a_rows, H], copied by gatherer warps)
+int launch_pair_gateup(const char* op, const void* a_bf16, int a_rows,
+                       const int32_t* a_row_gather, int gather_div, const void* w13_bf16,
                        const int32_t* group_offsets, int P, int H, int I, int G, void* act_bf16,
                        cudaStream_t stream);
 int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,

@@ -1011,8 +1011,9 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   if (a_row_gather && (a_rows < 1 || gather_div < 1))
     return set_error(MOE_ERR_ARG, "%s: gathering needs a_rows >= 1 and gather_div >= 1", op);
   if (P == 0) return MOE_OK;
-  if (!a_row_gather && use_pair_tiles(P, G))
-    return launch_pair_gateup(op, a_bf16, w13_bf16, group_offsets, P, H, I, G, act_bf16,
+  if (use_pair_tiles(P, G))
+    return launch_pair_gateup(op, a_bf16, a_rows, a_row_gather, gather_div, w13_bf16,
+                              group_offsets, P, H, I, G, act_bf16,
                               static_cast<cudaStream_t>(stream));
   // Few rows per expert (decode): each tile streams its weight rows from HBM
   // and the tile count decides the balance; 128-wide tiles (64 gate + 64 up

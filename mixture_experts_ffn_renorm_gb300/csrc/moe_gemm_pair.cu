@@ -26,6 +26,15 @@
 //               row per thread, the fused op, and a transpose through shared
 //               memory into token-major output rows stored as 16-byte vectors
 //
+//   warps 10-11 (gate/up with gathered rows only) cp.async copies of the CTA's
+//               token rows straight from x: routed row r is row
+//               row_gather[r] / gather_div of x, so no permuted copy of x is
+//               needed.  The copies land in the 128-byte-swizzled layout of the
+//               TMA token box and report on an mbarrier as they complete: in the
+//               even CTA the stage's full barrier itself; in the odd CTA a
+//               barrier of its own, which warp 1 relays to the even CTA's full
+//               barrier after a proxy fence.
+//
 // gate/up: a CTA's 128 weight rows are the up rows of 64 output features
 // followed by the gate rows of the same 64, so TMEM lanes 0-63 hold up and
 // lanes 64-127 gate.  The warps that read up lanes narrow them to bf16 and pass
@@ -50,6 +59,7 @@ namespace gemm {
 namespace {
 
 constexpr int kPairThreads = 320;     // producer, MMA, two groups of four epilogue warps
+constexpr int kGatherThreads = 64;    // + two warps that gather token rows (on sub-partitions 2, 3)
 constexpr int kTokBlock = 256;        // tokens per tile at most (MMA N)
 // token rows per TMA box: three tensor maps over the token rows, with boxes of
 // 32, 64 and 128 rows; a stage takes the smallest that covers its N / 2 rows
@@ -75,6 +85,10 @@ struct PairParams {
   void* out;                     // bf16 [P, N] (down: rows by dst)
   const float* pair_weight;      // down: [P] by destination row, or null
   const int32_t* row_to_pair;    // down: destination row of each product row, or null
+  const uint16_t* a;             // gathered rows: x [a_rows, Kdim] bf16
+  int a_rows;
+  const int32_t* row_gather;     // gathered rows: routed row r is x row row_gather[r] / gather_div
+  int gather_div;
   unsigned long long wait_ns;
   unsigned int* status;
   unsigned long long* launches;
@@ -87,9 +101,9 @@ struct PSmem {
   static constexpr int EPI = STAGE_T + kPStages * kTBytes;           // 2 groups x 8 KB
   static constexpr int META_DST = EPI + 2 * 8192;                    // int[2][256]
   static constexpr int META_W = META_DST + 2 * kTokBlock * 4;        // float[2][256]
-  // full[kPStages], empty[kPStages], tfull[2], tempty[2], drain
+  // full[kPStages], empty[kPStages], tfull[2], tempty[2], drain, gathered[kPStages]
   static constexpr int BARS = META_W + 2 * kTokBlock * 4;
-  static constexpr int NBARS = 2 * kPStages + 5;
+  static constexpr int NBARS = 3 * kPStages + 5;
   static constexpr int MISC = BARS + NBARS * 8;                      // tmem slot, abort flag, scan
   static constexpr int TILE_START = MISC + 64;
   static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
@@ -130,14 +144,18 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
 }
 
 // kEpi: PEPI_GATEUP (weights W13 [G, 2I, K], fb_cols = 128 output features per
-// tile, 64 per CTA) or PEPI_DOWN (weights W2 [G, H, K], 256 per tile, 128 per CTA)
-template <int kEpi>
-__global__ void __launch_bounds__(kPairThreads, 1)
+// tile, 64 per CTA) or PEPI_DOWN (weights W2 [G, H, K], 256 per tile, 128 per CTA).
+// kGather (gate/up only): token rows copied from x by warps 10-11 instead of
+// TMA boxes of a permuted matrix.
+template <int kEpi, bool kGather>
+__global__ void __launch_bounds__(kGather ? kPairThreads + kGatherThreads : kPairThreads, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
                  const __grid_constant__ CUtensorMap tmT64,
                  const __grid_constant__ CUtensorMap tmT128,
                  const __grid_constant__ CUtensorMap tmW, const PairParams p) {
   constexpr bool kGU = kEpi == PEPI_GATEUP;
+  static_assert(kGU || !kGather, "gathered token rows: gate/up only");
+  constexpr int kNT = kGather ? kPairThreads + kGatherThreads : kPairThreads;
   constexpr int kFbCols = kGU ? 128 : 256;   // output features per tile (both CTAs)
   constexpr int kWBox = kGU ? 64 : 128;      // weight rows per TMA box
   extern __shared__ uint8_t smem_raw[];
@@ -165,13 +183,17 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
   auto bar_tfull = [&](int a) { return ptx::smem_u32(bars + 2 * kPStages + a); };
   auto bar_tempty = [&](int a) { return ptx::smem_u32(bars + 2 * kPStages + 2 + a); };
   const uint32_t bar_drain = ptx::smem_u32(bars + 2 * kPStages + 4);
+  auto bar_gath = [&](int s) { return ptx::smem_u32(bars + 2 * kPStages + 5 + s); };
 
   count_launch(p.launches, p.kid);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPStages; ++s) {
-      ptx::mbar_init(bar_full(s), 1);    // the even CTA's expect-tx arrive
+      // the even CTA's expect-tx arrive; with gathered rows also one arrive per
+      // gatherer of the even CTA and the odd CTA's relay
+      ptx::mbar_init(bar_full(s), kGather && leader ? 2 + kGatherThreads : 1);
       ptx::mbar_init(bar_empty(s), 1);   // the pair's MMA commit
+      if (kGather) ptx::mbar_init(bar_gath(s), kGatherThreads);  // this CTA's gatherers
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar_tfull(a), 1);
@@ -197,11 +219,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
 
   // ---- device-side tile schedule (every CTA computes the same one)
   const int G = p.G;
-  for (int g = threadIdx.x; g <= G; g += kPairThreads)
+  for (int g = threadIdx.x; g <= G; g += kNT)
     goff[g] = p.group_offsets ? __ldg(p.group_offsets + g) : (g == 0 ? 0 : p.P);
   __syncthreads();
   const int n_fb = (p.N + kFbCols - 1) / kFbCols;
-  const int chunk = (G + kPairThreads - 1) / kPairThreads;
+  const int chunk = (G + kNT - 1) / kNT;
   const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
   const int g_hi = min(G, g_lo + chunk);
   int local = 0;
@@ -215,7 +237,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
   if (lane == 31) scan_tmp[warp] = incl;
   __syncthreads();
   int warp_base = 0, total = 0;
-  for (int w = 0; w < kPairThreads / 32; ++w) {
+  for (int w = 0; w < kNT / 32; ++w) {
     const int v = scan_tmp[w];
     if (w < warp) warp_base += v;
     total += v;
@@ -239,7 +261,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     // ------------------------------------------------------------ TMA producer
     // Lane 0 waits for the stage and arms the even CTA's barrier; then the
     // stage's two or three boxes (weight rows in one or two boxes, token rows in
-    // one) are issued by lanes 0-2 as a single warp instruction.
+    // one unless the gatherers copy them) are issued by lanes 0-2 as a single
+    // warp instruction.
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -248,7 +271,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       const int half = ((t.n_tok + 15) & ~15) >> 1;      // tokens this CTA holds
       const int tbox = half <= 32 ? 32 : (half <= 64 ? 64 : 128);
       const CUtensorMap* mt = tbox == 32 ? &tmT32 : (tbox == 64 ? &tmT64 : &tmT128);
-      const uint32_t bytes = kWBytes + tbox * (BK * 2);
+      const uint32_t bytes = kWBytes + (kGather ? 0 : tbox * (BK * 2));
       const int trow = t.r0 + static_cast<int>(rank) * half;
       // this CTA's 128 weight rows: gate/up, the 64 up rows of its features
       // then their 64 gate rows; down, 128 consecutive output rows
@@ -257,7 +280,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       const int wrow1 = wrow_g;
       // this lane's box: lane 0 the first weight box (up rows, or the down rows),
       // lane 1 the gate box, lane 2 the tokens
-      const bool issues = lane == 0 || lane == 2 || (kGU && lane == 1);
+      const bool issues = lane == 0 || (!kGather && lane == 2) || (kGU && lane == 1);
       const CUtensorMap* mbox = lane == 2 ? mt : &tmW;
       const int ybox = lane == 0 ? wrow0 : (lane == 1 ? wrow1 : trow);
       const uint32_t dbox = lane == 2 ? PSmem::STAGE_T : PSmem::STAGE_W + lane * (kWBox * 128);
@@ -303,6 +326,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
             ok = false;
             break;
           }
+          // gathered rows: the even CTA's cp.async writes, observed through the
+          // barrier, ordered before the tensor core's reads
+          if (kGather) ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           const uint64_t dw = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_W + stage * kWBytes);
           const uint64_t dt = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_T + stage * kTBytes);
@@ -319,7 +345,86 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
         else ++uses0;
         acc ^= 1;
       }
+    } else if (kGather && lane == 0 && !leader) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      // Once this CTA's gatherers have landed a stage (observed through the
+      // barrier), fence their writes for the tensor core and arrive on the even
+      // CTA's full barrier of the stage.  The arrive is relaxed: the copies are
+      // already performed and fenced when it is made, and a release at cluster
+      // scope on every stage measured 2.6 times slower for the whole GEMM.
+      const uint32_t full_leader = ptx::mapa_shared(bar_full(0), 0);  // + 8 * stage
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = unit; ok && tile < total; tile += n_units) {
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bar_spin(bar_gath(stage), phase, abort_flag, p.status, wait_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive_remote_relaxed(full_leader + 8u * stage);
+          if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+        }
+      }
     }
+  } else if (kGather && warp >= kPairThreads / 32) {
+    // ------------------------------------------------------------ token-row gatherers
+    // Warp gw copies rows [64 gw, 64 gw + 64) of this CTA's half of the tile's
+    // tokens: each warp instruction moves four rows, lane l the 16-byte chunk
+    // l % 8 of row l / 8 (128 contiguous bytes per row), into the slot chunk
+    // c ^ (row % 8) that the 128-byte swizzle gives it.  Tokens past the tile's
+    // end, and rows outside [0, a_rows), are written as zeros.  The copies go
+    // through the SM's load/store path, which moves about two thirds of the
+    // token bytes a stage ring fed by TMA boxes of a permuted matrix takes in
+    // the same time; the gatherers spin on the stage barrier, since their
+    // reaction time adds to every stage's round trip.
+    const int gw = warp - kPairThreads / 32;
+    const int c = lane & 7;
+    const int rsub = lane >> 3;
+    const uint16_t* a = p.a;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = unit; ok && tile < total; tile += n_units) {
+      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+      const int half = ((t.n_tok + 15) & ~15) >> 1;      // rows this CTA holds (multiple of 8)
+      const int tok0 = static_cast<int>(rank) * half;    // its first token of the tile
+      const int n_m = max(0, min(16, (half - 64 * gw) >> 2));  // warp instructions per stage
+      int src[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const int tok = tok0 + 64 * gw + 4 * m + rsub;
+        int r = -1;
+        if (m < n_m && tok < t.n_tok) {
+          r = __ldg(p.row_gather + t.r0 + tok) / p.gather_div;
+          if (r >= p.a_rows) r = -1;
+        }
+        src[m] = r;
+      }
+      for (int kb = 0; kb < nk; ++kb) {
+        const bool got = wait_bar_spin(bar_empty(stage), phase ^ 1u, abort_flag, p.status, wait_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sbase + PSmem::STAGE_T + stage * kTBytes;
+        const int col = kb * BK + 8 * c;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          if (m < n_m) {
+            const int j = 64 * gw + 4 * m + rsub;
+            const bool live = src[m] >= 0 && col < p.Kdim;  // Kdim % 8 == 0: all in or out
+            ptx::cp_async_16(dst + j * 128 + ((c ^ (j & 7)) << 4),
+                             a + (live ? static_cast<size_t>(src[m]) * p.Kdim + col : 0),
+                             live ? 16u : 0u);
+          }
+        }
+        ptx::cp_async_mbar_arrive_noinc(leader ? bar_full(stage) : bar_gath(stage));
+        if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    ptx::cp_async_wait_all();   // nothing of this thread lands after the CTA's exit
   } else {
     // ------------------------------------------------------------ epilogue
     // Two groups of four warps (2-5 and 6-9) take the tile's 32-token chunks in
@@ -531,10 +636,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
 }  // namespace
 
 // The pair kernels' grid: clusters of two CTAs, as many as can be resident.
-template <int kEpi>
+template <int kEpi, bool kGather>
 int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtensorMap& tw,
                        PairParams p, long long tiles, cudaStream_t stream) {
-  auto kern = pair_gemm_kernel<kEpi>;
+  auto kern = pair_gemm_kernel<kEpi, kGather>;
+  constexpr int kNT = kGather ? kPairThreads + kGatherThreads : kPairThreads;
   const int smem = PSmem::ALLOC;
   static std::atomic<int> configured_dev[64] = {};
   static std::atomic<int> max_pairs_dev[64] = {};
@@ -563,7 +669,7 @@ int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtenso
     max_pairs = num_sms() / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * max_pairs), 1, 1);
-    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.blockDim = dim3(kNT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -581,7 +687,7 @@ int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtenso
   p.launches = diag.launches;
   p.wait_ns = pipeline_wait_ns();
   return launch_status(launch_kernel(kern, dim3(static_cast<unsigned>(2 * pairs), 1, 1),
-                                     dim3(kPairThreads, 1, 1), smem, stream, attr, 1, tt[0], tt[1],
+                                     dim3(kNT, 1, 1), smem, stream, attr, 1, tt[0], tt[1],
                                      tt[2], tw, p),
                        op);
 }
@@ -602,15 +708,20 @@ static int make_token_maps(CUtensorMap (&tt)[3], const void* base, int rows, int
   return MOE_OK;
 }
 
-int launch_pair_gateup(const char* op, const void* a_bf16, const void* w13_bf16,
+int launch_pair_gateup(const char* op, const void* a_bf16, int a_rows,
+                       const int32_t* a_row_gather, int gather_div, const void* w13_bf16,
                        const int32_t* group_offsets, int P, int H, int I, int G, void* act_bf16,
                        cudaStream_t stream) {
   CUtensorMap tt[3], tw;
   int rc;
-  if ((rc = make_token_maps(tt, a_bf16, P, H, op, "a")) != MOE_OK) return rc;
   if ((rc = make_tmap(&tw, w13_bf16, static_cast<long long>(G) * 2 * I, H, 64, op, "w13")) !=
       MOE_OK)
     return rc;
+  if (a_row_gather) {
+    for (int i = 0; i < 3; ++i) tt[i] = tw;  // unused: the gatherer warps copy the token rows
+  } else if ((rc = make_token_maps(tt, a_bf16, P, H, op, "a")) != MOE_OK) {
+    return rc;
+  }
   PairParams p{};
   p.group_offsets = group_offsets;
   p.P = P;
@@ -620,8 +731,14 @@ int launch_pair_gateup(const char* op, const void* a_bf16, const void* w13_bf16,
   p.w_rows_per_group = 2 * I;
   p.half_off = I;
   p.out = act_bf16;
+  p.a = static_cast<const uint16_t*>(a_bf16);
+  p.a_rows = a_rows;
+  p.row_gather = a_row_gather;
+  p.gather_div = gather_div;
   p.kid = MOE_KID_GEMM_GATEUP;
-  return launch_pair_kernel<PEPI_GATEUP>(op, tt, tw, p, pair_tile_bound(P, G, I, 128), stream);
+  const long long tiles = pair_tile_bound(P, G, I, 128);
+  if (a_row_gather) return launch_pair_kernel<PEPI_GATEUP, true>(op, tt, tw, p, tiles, stream);
+  return launch_pair_kernel<PEPI_GATEUP, false>(op, tt, tw, p, tiles, stream);
 }
 
 int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
@@ -645,7 +762,8 @@ int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
   p.pair_weight = pair_weight;
   p.row_to_pair = row_to_pair;
   p.kid = MOE_KID_GEMM_DOWN;
-  return launch_pair_kernel<PEPI_DOWN>(op, tt, tw, p, pair_tile_bound(P, G, H, 256), stream);
+  return launch_pair_kernel<PEPI_DOWN, false>(op, tt, tw, p, pair_tile_bound(P, G, H, 256),
+                                             stream);
 }
 
 }  // namespace gemm

@@ -78,6 +78,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// the same at cluster scope, relaxed (pair with fence_acquire_cluster)
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // relaxed poll at cluster scope, for barriers a peer CTA arrives on remotely;
 // the caller follows a successful poll with fence_acquire_cluster() (one fence
@@ -209,8 +221,19 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// orders this thread's generic-proxy shared-memory writes before later
-// async-proxy accesses (the tensor core reads its operands through the async proxy)
+// waits for every cp.async this thread issued, whether or not committed to a group
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// one arrive on this CTA's mbarrier at `bar`, made once every cp.async this
+// thread issued before has landed; with .noinc the arrive counts against the
+// barrier's expected arrival count
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// orders generic-proxy shared-memory writes before later async-proxy accesses
+// (the tensor core reads its operands through the async proxy): this thread's
+// own writes, and writes it has observed through an mbarrier wait
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

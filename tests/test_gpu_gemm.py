@@ -86,9 +86,10 @@ def test_gateup_silu(sizes, H, I, tiling):
 
 @pytest.mark.parametrize("sizes,H,I", SHAPES)
 @pytest.mark.parametrize("K", [1, 3, 8])
-def test_gateup_silu_gathered_rows(sizes, H, I, K):
+def test_gateup_silu_gathered_rows(sizes, H, I, K, tiling):
     # product row r reads x[pair[r] // K]: the routed rows come straight from the
-    # token matrix, copied by the producer warps with cp.async (no x_perm)
+    # token matrix, copied by gatherer warps with cp.async (no x_perm); on CTA
+    # pairs each CTA copies its half of a tile's tokens
     off, P, G, _, W13, _ = _case(sizes, H, I, sum(sizes) + 7 * H + K)
     rng = np.random.default_rng(P + K)
     T = max(1, (P + K - 1) // K) + 3

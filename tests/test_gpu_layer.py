@@ -182,8 +182,10 @@ def test_large_shared_layer_stagewise():
     _stagewise(W.LARGE, 32, 96)
 
 
-def test_materialised_x_perm_path_matches_gather_path():
-    cfg = W.DECODE
+@pytest.mark.parametrize("cfg", [W.DECODE, W.PREFILL], ids=["decode", "prefill"])
+def test_materialised_x_perm_path_matches_gather_path(cfg):
+    # decode runs single-CTA tiles, prefill CTA-pair tiles (gatherer warps in
+    # both CTAs, the odd CTA's copies relayed to the even CTA's barrier)
     d = W.layer_inputs(cfg)
     x = to_dev(d["x"])
     a = to_host(MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",

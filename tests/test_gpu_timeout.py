@@ -73,17 +73,27 @@ def test_wait_limit_expiry_is_reported_and_the_device_stays_usable(tiling):
     ref_act, ref_out = run()
     assert m.moe_device_status() == 0
 
-    # a 1 us limit: both launches give up, report it and end
+    # gathered rows (identity gather: row r reads A row r) take the gatherer
+    # warps' waits, and on CTA pairs the odd CTA's relay
+    ident = to_dev(np.arange(P, dtype=np.int32))
+    act_g = empty((P, I), torch.bfloat16)
+
+    def gathered():
+        return m.moe_grouped_gemm_gateup_silu_bf16(dA, P, ident, 1, dW13, doff, P, H, I, G, act_g)
+
+    # a 1 us limit: every launch gives up, reports it and ends
     m.moe_set_wait_limit_ns(1000)
-    for call in ("gateup", "down"):
+    for call in ("gateup", "gateup_gather", "down"):
         before = launches()
         if call == "gateup":
             rc = m.moe_grouped_gemm_gateup_silu_bf16(dA, P, None, 1, dW13, doff, P, H, I, G, act)
+        elif call == "gateup_gather":
+            rc = gathered()
         else:
             rc = m.moe_grouped_gemm_down_bf16(act, dW2, doff, dwts, dr2p, P, I, H, G, out)
         assert rc == m.OK                       # the launch itself was accepted
         torch.cuda.synchronize()                # and the kernel ended
-        assert launched_since(before, "gemm_" + call) == 1
+        assert launched_since(before, "gemm_" + call.replace("_gather", "")) == 1
         status = m.moe_device_status(clear=True)
         assert status & m.STATUS_TIMEOUT, f"{call}: status {status}"
         assert m.moe_device_status() == 0
@@ -91,8 +101,11 @@ def test_wait_limit_expiry_is_reported_and_the_device_stays_usable(tiling):
     # limit restored: the same process computes the same bits again
     m.moe_set_wait_limit_ns(FULL_LIMIT_NS)
     got_act, got_out = run()
+    assert gathered() == m.OK
+    torch.cuda.synchronize()
     assert m.moe_device_status() == 0
     assert np.array_equal(got_act, ref_act)
+    assert np.array_equal(to_host(act_g), ref_act)
     assert np.array_equal(got_out, ref_out)
     # and they are the oracle's, on sampled rows
     rows = np.unique(np.concatenate([off[:-1], np.random.default_rng(3).choice(P, 200, False),
