@@ -425,7 +425,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       }
     }
     ptx::cp_async_wait_all();   // nothing of this thread lands after the CTA's exit
-  } else {
+  } else if (warp < kPairThreads / 32) {
     // ------------------------------------------------------------ epilogue
     // Two groups of four warps (2-5 and 6-9) take the tile's 32-token chunks in
     // turn, each with its own staging buffers and named barrier; all eight meet
