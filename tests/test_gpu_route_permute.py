@@ -41,7 +41,8 @@ def gpu_route(x, wr, bias, wsg, logits_in, T, H, E, K, renorm=1, want_logits=Fal
             None if gl is None else to_host(gl))
 
 
-@pytest.mark.parametrize("E,K", [(8, 2), (128, 8), (256, 8), (1000, 32), (5, 5), (64, 1)])
+@pytest.mark.parametrize("E,K", [(8, 2), (128, 8), (256, 8), (1000, 32), (5, 5), (64, 1),
+                                 (96, 8), (200, 6)])
 @pytest.mark.parametrize("renorm", [1, 0])
 def test_topk_bit_exact_from_logits(E, K, renorm):
     rng = np.random.default_rng(E * 7 + K)
@@ -54,6 +55,10 @@ def test_topk_bit_exact_from_logits(E, K, renorm):
     logits[2, 0] = np.nan
     logits[3, E - 1] = np.inf
     logits[4, : E // 2] = -np.inf
+    logits[5, :] = np.nan                     # every key equal: the K lowest ids
+    logits[6, ::3] = np.nan
+    logits[7, :] = logits[7, 0]               # one value repeated: ties all the way down
+    logits[7, E - 1] = np.inf
     want_ids, want_w, _, _ = O.route_topk(logits_in=logits, T=T, H=1, E=E, K=K,
                                           renormalize=renorm)
     before = launches()
