@@ -4,8 +4,10 @@ without a faulty kernel.
 Issue #1590 "kSharedExpertGate is CPU-only" asks for failures that are named,
 not left to hang.  Every pipeline wait inside the GEMM kernels has a limit,
 which moe_set_wait_limit_ns shortens.  At 1 us a prefill-sized gate/up or down
-launch cannot finish: its epilogue waits several microseconds for the first
-accumulator.  The launch must still end, raise MOE_STATUS_TIMEOUT in the status
+launch cannot finish: with K = 2048 in both GEMMs, its epilogue waits about
+15 us for the first accumulator (a suspended probe may overrun its 1 us hint,
+so a wait of a few microseconds can still complete in time).  The launch must
+still end, raise MOE_STATUS_TIMEOUT in the status
 word, and leave the device usable: with the limit restored and the status
 cleared, the next calls in the same process give the same bits as before, and
 those match the oracle.
@@ -38,7 +40,7 @@ def _restore_limit():
 
 def _problem():
     rng = np.random.default_rng(1590)
-    G, H, I = 16, 2048, 768
+    G, H, I = 8, 2048, 2048
     sizes = rng.multinomial(8192, np.full(G, 1.0 / G))
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     P = int(off[-1])
