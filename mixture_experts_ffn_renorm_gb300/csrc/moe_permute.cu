@@ -7,8 +7,9 @@
 //   count   one warp per chunk of 512 pairs: per-chunk expert histogram in
 //           shared memory (bad ids raise MOE_STATUS_BAD_ID and are skipped)
 //   scan    one block: per expert (one warp each), exclusive scan of the chunk
-//           counts in chunk order; then the exclusive scan over experts ->
-//           expert_offsets
+//           counts in chunk order (up to 128 experts and 128 chunks: a warp's
+//           four experts loaded at once and scanned interleaved); then the
+//           exclusive scan over experts -> expert_offsets
 //   place   one warp per chunk again, 32 pairs at a time in pair order: the
 //           rank of a pair among equal experts of its step comes from one
 //           ballot per id bit, so rows inside an expert ascend with p
@@ -132,6 +133,48 @@ permute_scan(int32_t* __restrict__ hist, int E, int n_chunks, int32_t* __restric
   __shared__ int32_t warp_sum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kBatch = 8;
+  const int epw = (E + 31) >> 5;           // experts per warp
+  const int nb = (n_chunks + 31) >> 5;     // 32-chunk batches per expert
+  if (epw <= 4 && nb <= 4) {
+    // Up to 128 experts and 128 chunks (the prefill batch): all of a warp's
+    // counts are loaded at once, one round trip, and its experts' scans run
+    // interleaved, four independent shuffle chains.
+    int v[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int e = warp + 32 * a, c = 32 * b + lane;
+        v[a][b] = (a < epw && e < E && b < nb && c < n_chunks)
+                      ? hist[static_cast<size_t>(e) * n_chunks + c] : 0;
+      }
+    int carry[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      int incl[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) incl[a] = v[a][b];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int u = __shfl_up_sync(0xffffffffu, incl[a], o);
+          if (lane >= o) incl[a] += u;
+        }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int e = warp + 32 * a, c = 32 * b + lane;
+        if (a < epw && e < E && b < nb && c < n_chunks)
+          hist[static_cast<size_t>(e) * n_chunks + c] = carry[a] + incl[a] - v[a][b];
+        carry[a] += __shfl_sync(0xffffffffu, incl[a], 31);
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int e = warp + 32 * a;
+      if (lane == 0 && a < epw && e < E) tot[e] = carry[a];
+    }
+  } else {
   for (int e = warp; e < E; e += 32) {
     int32_t* row = hist + static_cast<size_t>(e) * n_chunks;
     int carry = 0;
@@ -156,6 +199,7 @@ permute_scan(int32_t* __restrict__ hist, int E, int n_chunks, int32_t* __restric
       }
     }
     if (lane == 0) tot[e] = carry;
+  }
   }
   __syncthreads();
   // block-wide exclusive scan of the per-expert totals (E <= 1024)

@@ -256,7 +256,10 @@ def _ids(T, K, E, seed, skew=False):
                                      (2048, 8, 256, 128), (77, 3, 1000, 16), (1, 1, 1, 8),
                                      (8192, 8, 128, 8), (512, 8, 128, 64), (513, 8, 128, 64),
                                      (1365, 3, 1024, 8), (2048, 8, 256, 64), (2049, 8, 256, 8),
-                                     (2048, 8, 512, 8)])
+                                     (2048, 8, 512, 8),
+                                     # the chunked scan: segments of several batches, one
+                                     # thread per expert, an expert count not a power of two
+                                     (65536, 8, 128, 8), (16384, 8, 1024, 8), (8192, 4, 300, 8)])
 def test_permute_bit_exact(T, K, E, H):
     ids = _ids(T, K, E, T + E, skew=(T >= 1000))
     rng = np.random.default_rng(5)
