@@ -77,7 +77,7 @@ enum {
 const char* moe_last_error(void);
 
 /* Library ABI version (bumped on any signature change). */
-int moe_abi_version(void);  /* 9 */
+int moe_abi_version(void);  /* 10 */
 
 /* ------------------------------------------------------------------------
  * moe_route_topk -- ungrouped softmax router ([PR509] "Honest gaps": the
@@ -275,6 +275,40 @@ int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows, const int3
                                       const int32_t* group_offsets, int P, int H, int I, int G,
                                       void* act_bf16, void* workspace, size_t ws_bytes,
                                       void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_gemm_gateup_silu_bf16_staged -- the same op as
+ * moe_grouped_gemm_gateup_silu_bf16 on the routed rows of x (kMoeGroupedGemmBf16GateUpSilu
+ * of [I3094]), with the row gather of moe_permute folded into the launch:
+ *   x_perm[r] = x[sorted_pair[r] / K]   for r in [0, P)   (zeros if that row is
+ *                                        outside [0, T))
+ *   act = the gate/up result of moe_grouped_gemm_gateup_silu_bf16 on x_perm,
+ * bit for bit.  On CTA-pair tiles (prefill-sized batches, moe_set_gemm_pairing)
+ * warps of the GEMM launch itself write x_perm, 16 rows at a time, and each tile
+ * reads its rows once their chunk is written, so the copy overlaps the GEMM;
+ * otherwise a row-gather launch runs first, then the single-CTA tiles.
+ *
+ *   x            bf16 [T,H]
+ *   sorted_pair  int32 [P]: moe_permute's sorted_pair (pair p = t*K + k)
+ *   K            >= 1: the divisor that turns a pair into its token row
+ *   x_perm       bf16 [P,H] out, 16-byte aligned (written, then read, by this call)
+ *   w13, group_offsets, P, H, I, G, act: as for moe_grouped_gemm_gateup_silu_bf16
+ *   workspace    >= moe_gateup_staged_workspace_size(P) bytes, 16-byte aligned,
+ *                device memory, zero-filled before its first use and then passed
+ *                unchanged to every later call (it carries per-chunk ready flags
+ *                and the flag value of the last launch, so no reset is needed
+ *                between calls).  Calls that may run concurrently need their own.
+ * Errors: those of moe_grouped_gemm_gateup_silu_bf16; MOE_ERR_ARG (T < 1 or K < 1,
+ * NULL sorted_pair or x_perm, with P > 0), MOE_ERR_ALIGN (x_perm), MOE_ERR_WORKSPACE.
+ * A device-side wait that runs past its limit (moe_set_wait_limit_ns), including
+ * a tile's wait for its rows, sets MOE_STATUS_TIMEOUT.
+ * ---------------------------------------------------------------------- */
+size_t moe_gateup_staged_workspace_size(int P);
+int moe_grouped_gemm_gateup_silu_bf16_staged(const void* x_bf16, int T, const int32_t* sorted_pair,
+                                             int K, void* x_perm_bf16, const void* w13_bf16,
+                                             const int32_t* group_offsets, int P, int H, int I,
+                                             int G, void* act_bf16, void* workspace,
+                                             size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_grouped_gemm_down_bf16 -- kMoeGroupedGemmBf16 of [I3094].  For every

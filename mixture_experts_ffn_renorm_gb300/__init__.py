@@ -42,6 +42,7 @@ EXPORTS = (
     "moe_route_topk_ex", "moe_grouped_gemm_gateup_silu_fp8w", "moe_grouped_gemm_down_fp8w",
     "moe_quantize_act_q8", "moe_grouped_gemm_q", "moe_grouped_gemm_gateup_silu_q",
     "moe_grouped_gemm_down_q", "moe_dequantize_q_bf16", "moe_exp_sigmoid_f32",
+    "moe_grouped_gemm_gateup_silu_bf16_staged", "moe_gateup_staged_workspace_size",
 )
 
 
@@ -71,6 +72,9 @@ _SIGS = {
     "moe_permute_noalloc": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gemm_gateup_silu_bf16": ([_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _SZ,
                                            _P], _I),
+    "moe_grouped_gemm_gateup_silu_bf16_staged": ([_P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P,
+                                                  _P, _SZ, _P], _I),
+    "moe_gateup_staged_workspace_size": ([_I], _SZ),
     "moe_grouped_gemm_down_bf16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "moe_grouped_gemm_workspace_size": ([_I, _I, _I, _I], _SZ),
     "moe_grouped_gemm_gateup_silu_fp8w": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
@@ -197,6 +201,19 @@ def moe_permute_noalloc(topk_ids, x, T, K, E, H, expert_offsets, sorted_pair, pa
     rc = lib().moe_permute_noalloc(_ptr(topk_ids), _ptr(x), T, K, E, H, _ptr(expert_offsets),
                                    _ptr(sorted_pair), _ptr(pair_to_row), _ptr(x_perm),
                                    _stream(stream))
+    return _check(rc) if check else rc
+
+
+def moe_gateup_staged_workspace_size(P) -> int:
+    return lib().moe_gateup_staged_workspace_size(P)
+
+
+def moe_grouped_gemm_gateup_silu_bf16_staged(x, T, sorted_pair, K, x_perm, w13, group_offsets, P,
+                                             H, I, G, act, workspace, ws_bytes, stream=None,
+                                             check=True):
+    rc = lib().moe_grouped_gemm_gateup_silu_bf16_staged(
+        _ptr(x), T, _ptr(sorted_pair), K, _ptr(x_perm), _ptr(w13), _ptr(group_offsets), P, H, I,
+        G, _ptr(act), _ptr(workspace), ws_bytes, _stream(stream))
     return _check(rc) if check else rc
 
 

@@ -108,6 +108,13 @@ int launch_pair_gateup(const char* op, const void* a_bf16, int a_rows,
                        const int32_t* a_row_gather, int gather_div, const void* w13_bf16,
                        const int32_t* group_offsets, int P, int H, int I, int G, void* act_bf16,
                        cudaStream_t stream);
+// (staged rows: the launch writes x_perm[r] = x[sorted_pair[r] / K] itself,
+// chunk by chunk, and its tiles read x_perm behind per-chunk ready flags)
+int launch_pair_gateup_staged(const char* op, const void* x_bf16, int T,
+                              const int32_t* sorted_pair, int K, void* x_perm_bf16,
+                              const void* w13_bf16, const int32_t* group_offsets, int P, int H,
+                              int I, int G, void* act_bf16, int32_t* stage_flags,
+                              unsigned int* stage_ctl, cudaStream_t stream);
 int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
                      const int32_t* group_offsets, const float* pair_weight,
                      const int32_t* row_to_pair, int P, int I, int H, int G, void* out_bf16,

@@ -105,7 +105,7 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_msg; }
 
-int moe_abi_version(void) { return 9; }
+int moe_abi_version(void) { return 10; }
 
 int moe_set_pdl(int enable) {
   moe::clear_error();

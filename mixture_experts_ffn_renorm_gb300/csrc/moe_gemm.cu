@@ -931,6 +931,9 @@ bool use_pair_tiles(int P, int G) {
 // K ranges for the router logits GEMM: enough (tile, range) units to give every
 // SM one when T x E alone makes few tiles (decode), at most 16, every range
 // non-empty.  ranges * T * E floats of partial sums.
+int launch_row_gather(const char* op, const void* x_bf16, int x_rows, void* x_perm_bf16,
+                      const int32_t* sorted_pair, long long P, int K, int H, cudaStream_t s);
+
 int router_splits(int T, int H, int E) {
   using namespace gemm;
   const long long tiles = static_cast<long long>((T + BM - 1) / BM) * ((E + 63) / 64);
@@ -1053,6 +1056,49 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
     return launch<128, EPI_GATEUP, false, kNarrowRows>(op, ta, tb, p,
                                                        tile_bound(P, G, I, 64, kNarrowRows), s);
   return launch<256, EPI_GATEUP>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
+}
+
+// staged rows: a 256-byte control block (the last launch's flag value, a
+// count of finished CTAs), then one flag per 16 routed rows
+extern "C" size_t moe_gateup_staged_workspace_size(int P) {
+  if (P <= 0) return 0;
+  const size_t flags = static_cast<size_t>((P + 15) / 16) * sizeof(int32_t);
+  return 256 + ((flags + 255) & ~static_cast<size_t>(255));
+}
+
+extern "C" int moe_grouped_gemm_gateup_silu_bf16_staged(
+    const void* x_bf16, int T, const int32_t* sorted_pair, int K, void* x_perm_bf16,
+    const void* w13_bf16, const int32_t* group_offsets, int P, int H, int I, int G,
+    void* act_bf16, void* workspace, size_t ws_bytes, void* stream) {
+  clear_error();
+  const char* op = "moe_grouped_gemm_gateup_silu_bf16_staged";
+  int rc;
+  if ((rc = check_common(op, P, H, I, G, x_bf16, w13_bf16, act_bf16)) != MOE_OK) return rc;
+  if (!group_offsets && G != 1)
+    return set_error(MOE_ERR_ARG, "%s: group_offsets is NULL with G=%d", op, G);
+  if (P == 0) return MOE_OK;
+  if (T < 1 || K < 1) return set_error(MOE_ERR_ARG, "%s: T=%d and K=%d must be >= 1", op, T, K);
+  if (!sorted_pair || !x_perm_bf16)
+    return set_error(MOE_ERR_ARG, "%s: sorted_pair or x_perm is NULL", op);
+  if (!aligned16(x_perm_bf16))
+    return set_error(MOE_ERR_ALIGN, "%s: x_perm must be 16-byte aligned", op);
+  const size_t need = moe_gateup_staged_workspace_size(P);
+  if (!workspace || ws_bytes < need || !aligned16(workspace))
+    return set_error(MOE_ERR_WORKSPACE, "%s: workspace of %zu bytes is smaller than %zu", op,
+                     ws_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_pair_tiles(P, G)) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return launch_pair_gateup_staged(op, x_bf16, T, sorted_pair, K, x_perm_bf16, w13_bf16,
+                                     group_offsets, P, H, I, G, act_bf16,
+                                     reinterpret_cast<int32_t*>(ws + 256),
+                                     reinterpret_cast<unsigned int*>(ws), s);
+  }
+  // single-CTA tiles: the row gather, then the tiles over x_perm
+  if ((rc = launch_row_gather(op, x_bf16, T, x_perm_bf16, sorted_pair, P, K, H, s)) != MOE_OK)
+    return rc;
+  return moe_grouped_gemm_gateup_silu_bf16(x_perm_bf16, P, nullptr, 1, w13_bf16, group_offsets, P,
+                                           H, I, G, act_bf16, nullptr, 0, stream);
 }
 
 extern "C" int moe_grouped_gemm_down_bf16(const void* act_bf16, const void* w2_bf16,

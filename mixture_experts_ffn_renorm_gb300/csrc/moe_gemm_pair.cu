@@ -34,6 +34,15 @@
 //               even CTA the stage's full barrier itself; in the odd CTA a
 //               barrier of its own, which warp 1 relays to the even CTA's full
 //               barrier after a proxy fence.
+//   warps 10-12 (gate/up with staged rows only) warps 10-11 of every CTA write
+//               x_perm rows from x, 16-row chunks in row order spread over the
+//               grid, each chunk released through a flag in global memory;
+//               warp 12 watches the flags of the chunks this CTA's tiles read and
+//               counts the ready tiles in shared memory, and the producer reads
+//               that count once per tile before it loads the tile's token boxes
+//               from x_perm.  The flags carry a value one past the last launch's
+//               (kept in the caller's workspace), so no reset is needed between
+//               calls.
 //
 // gate/up: a CTA's 128 weight rows are the up rows of 64 output features
 // followed by the gate rows of the same 64, so TMEM lanes 0-63 hold up and
@@ -60,6 +69,19 @@ namespace {
 
 constexpr int kPairThreads = 320;     // producer, MMA, two groups of four epilogue warps
 constexpr int kGatherThreads = 64;    // + two warps that gather token rows (on sub-partitions 2, 3)
+// staged rows: + two stager warps (sub-partitions 2, 3) and one watcher warp
+constexpr int kStagedThreads = 96;
+constexpr int kStageRows = 16;        // routed rows per staging chunk (one ready flag each)
+
+// Where a gate/up launch takes its token rows from: TMA boxes of a permuted
+// matrix the caller wrote (x_perm); 16-byte cp.async copies from x by gatherer
+// warps; or TMA boxes of x_perm that stager warps of the same launch write from
+// x, chunk by chunk, ahead of the tiles that read them.
+enum PairSrc { SRC_TMA = 0, SRC_GATHER = 1, SRC_STAGED = 2 };
+
+__host__ __device__ constexpr int pair_threads(int src) {
+  return kPairThreads + (src == SRC_GATHER ? kGatherThreads : src == SRC_STAGED ? kStagedThreads : 0);
+}
 constexpr int kTokBlock = 256;        // tokens per tile at most (MMA N)
 // token rows per TMA box: three tensor maps over the token rows, with boxes of
 // 32, 64 and 128 rows; a stage takes the smallest that covers its N / 2 rows
@@ -89,6 +111,9 @@ struct PairParams {
   int a_rows;
   const int32_t* row_gather;     // gathered rows: routed row r is x row row_gather[r] / gather_div
   int gather_div;
+  uint16_t* stage_out;           // staged rows: x_perm [P, Kdim], written by the stagers
+  int32_t* stage_flags;          // staged rows: [ceil(P / kStageRows)] chunk flags
+  unsigned int* stage_ctl;       // staged rows: [0] epoch of the last launch, [1] CTAs done
   unsigned long long wait_ns;
   unsigned int* status;
   unsigned long long* launches;
@@ -104,8 +129,9 @@ struct PSmem {
   // full[kPStages], empty[kPStages], tfull[2], tempty[2], drain, gathered[kPStages]
   static constexpr int BARS = META_W + 2 * kTokBlock * 4;
   static constexpr int NBARS = 3 * kPStages + 5;
-  static constexpr int MISC = BARS + NBARS * 8;                      // tmem slot, abort flag, scan
-  static constexpr int TILE_START = MISC + 64;
+  // tmem slot, abort flag, scan (one int per warp), staged rows: ready tiles, epoch
+  static constexpr int MISC = BARS + NBARS * 8;
+  static constexpr int TILE_START = MISC + 128;
   static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
   static constexpr int BYTES = GOFF + (kMaxGroups + 1) * 4;
   static constexpr int ALLOC = BYTES + 1024;
@@ -137,6 +163,44 @@ __device__ __forceinline__ PTile pair_tile(int tile, const int* tile_start, cons
   return t;
 }
 
+// staged rows: bounded wait of the producer until the watcher has published
+// more than `n` ready tiles (a shared-memory counter; acquire at CTA scope)
+__device__ __forceinline__ bool wait_ready(uint32_t s_ready, uint32_t n, volatile int* abort_flag,
+                                           unsigned int* status, unsigned long long limit_ns) {
+  if (ptx::ld_acquire_cta_shared_u32(s_ready) > n) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::ld_acquire_cta_shared_u32(s_ready) > n) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      if (status) atomicOr(status, static_cast<unsigned int>(MOE_STATUS_TIMEOUT));
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// staged rows: bounded wait of the watcher until a chunk's flag holds this
+// launch's value (set by a stager of any CTA; acquire at GPU scope)
+__device__ __forceinline__ bool wait_flag(const int32_t* flag, uint32_t want,
+                                          volatile int* abort_flag, unsigned int* status,
+                                          unsigned long long limit_ns) {
+  if (ptx::ld_acquire_gpu_u32(flag) == want) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (ptx::ld_acquire_gpu_u32(flag) == want) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      if (status) atomicOr(status, static_cast<unsigned int>(MOE_STATUS_TIMEOUT));
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
@@ -145,17 +209,19 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
 
 // kEpi: PEPI_GATEUP (weights W13 [G, 2I, K], fb_cols = 128 output features per
 // tile, 64 per CTA) or PEPI_DOWN (weights W2 [G, H, K], 256 per tile, 128 per CTA).
-// kGather (gate/up only): token rows copied from x by warps 10-11 instead of
-// TMA boxes of a permuted matrix.
-template <int kEpi, bool kGather>
-__global__ void __launch_bounds__(kGather ? kPairThreads + kGatherThreads : kPairThreads, 1)
+// kSrc (PairSrc): where the token rows come from; gathered and staged rows are
+// gate/up only.
+template <int kEpi, int kSrc>
+__global__ void __launch_bounds__(pair_threads(kSrc), 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
                  const __grid_constant__ CUtensorMap tmT64,
                  const __grid_constant__ CUtensorMap tmT128,
                  const __grid_constant__ CUtensorMap tmW, const PairParams p) {
   constexpr bool kGU = kEpi == PEPI_GATEUP;
-  static_assert(kGU || !kGather, "gathered token rows: gate/up only");
-  constexpr int kNT = kGather ? kPairThreads + kGatherThreads : kPairThreads;
+  constexpr bool kGather = kSrc == SRC_GATHER;
+  constexpr bool kStaged = kSrc == SRC_STAGED;
+  static_assert(kGU || kSrc == SRC_TMA, "gathered or staged token rows: gate/up only");
+  constexpr int kNT = pair_threads(kSrc);
   constexpr int kFbCols = kGU ? 128 : 256;   // output features per tile (both CTAs)
   constexpr int kWBox = kGU ? 64 : 128;      // weight rows per TMA box
   extern __shared__ uint8_t smem_raw[];
@@ -165,7 +231,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PSmem::BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PSmem::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PSmem::MISC + 4);
-  int* scan_tmp = reinterpret_cast<int*>(smem + PSmem::MISC + 8);
+  int* scan_tmp = reinterpret_cast<int*>(smem + PSmem::MISC + 8);   // one int per warp
+  // staged rows: how many of this CTA's tiles have their rows staged (watcher ->
+  // producer), and this launch's flag value
+  const uint32_t s_ready = ptx::smem_u32(smem + PSmem::MISC + 64);
+  volatile uint32_t* s_epoch = reinterpret_cast<volatile uint32_t*>(smem + PSmem::MISC + 68);
   int* tile_start = reinterpret_cast<int*>(smem + PSmem::TILE_START);
   int* goff = reinterpret_cast<int*>(smem + PSmem::GOFF);
   int* s_dst = reinterpret_cast<int*>(smem + PSmem::META_DST);
@@ -216,6 +286,13 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
 
   grid_dep_wait();
   grid_dep_launch();
+  // staged rows: the flag value of this launch is one past the last launch's;
+  // the last CTA of this launch records it at exit (every CTA reads it first,
+  // after the previous grid has completed)
+  if (kStaged && threadIdx.x == 0) {
+    *s_epoch = *reinterpret_cast<volatile uint32_t*>(p.stage_ctl) + 1u;
+    ptx::st_release_cta_shared_u32(s_ready, 0u);
+  }
 
   // ---- device-side tile schedule (every CTA computes the same one)
   const int G = p.G;
@@ -265,8 +342,18 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     // warp instruction.
     int stage = 0;
     uint32_t phase = 0;
+    uint32_t n_tile = 0;
     bool ok = true;
-    for (int tile = unit; ok && tile < total; tile += n_units) {
+    for (int tile = unit; ok && tile < total; tile += n_units, ++n_tile) {
+      if (kStaged) {
+        // the tile's rows of x_perm are staged (the watcher has seen their flags)
+        bool rdy = true;
+        if (lane == 0) rdy = wait_ready(s_ready, n_tile, abort_flag, p.status, wait_ns);
+        if (!__shfl_sync(0xffffffffu, rdy ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+      }
       const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
       const int half = ((t.n_tok + 15) & ~15) >> 1;      // tokens this CTA holds
       const int tbox = half <= 32 ? 32 : (half <= 64 ? 64 : 128);
@@ -302,6 +389,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
         if (++stage == kPStages) { stage = 0; phase ^= 1u; }
       }
     }
+    (void)n_tile;
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
@@ -366,6 +454,80 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
           ptx::mbar_arrive_remote_relaxed(full_leader + 8u * stage);
           if (++stage == kPStages) { stage = 0; phase ^= 1u; }
         }
+      }
+    }
+  } else if (kStaged && warp >= kPairThreads / 32 && warp < kPairThreads / 32 + 2) {
+    // ------------------------------------------------------------ stagers
+    // Warps 10 and 11 of every CTA copy routed rows of x into x_perm, one
+    // chunk of kStageRows rows at a time: stager s of the grid takes chunks
+    // s, s + stagers, ... (in row order, so the chunks the first tiles of every
+    // pair read come first).  A row is 16-byte vectors, lanes striding over it,
+    // two rows' loads in flight before their stores.  When its chunk is written
+    // each lane fences its stores for the async proxy (TMA reads them) and for
+    // the GPU, and lane 0 releases the chunk's flag with this launch's value.
+    const int gs = static_cast<int>(blockIdx.x) * 2 + (warp - kPairThreads / 32);
+    const int n_stagers = static_cast<int>(gridDim.x) * 2;
+    const int n_chunks = (p.P + kStageRows - 1) / kStageRows;
+    const int vpr = p.Kdim / 8;                   // 16-byte vectors per row
+    const uint32_t epoch = *s_epoch;
+    const uint4* x = reinterpret_cast<const uint4*>(p.a);
+    uint4* xp = reinterpret_cast<uint4*>(p.stage_out);
+    for (int c = gs; c < n_chunks && !*abort_flag; c += n_stagers) {
+      const int r0 = c * kStageRows, nr = min(kStageRows, p.P - r0);
+      int my_src = -1;                            // lane i: source row of row r0 + i
+      if (lane < nr) {
+        const int sr = __ldg(p.row_gather + r0 + lane) / p.gather_div;
+        my_src = sr >= 0 && sr < p.a_rows ? sr : -1;
+      }
+      for (int i = 0; i < nr; i += 2) {
+        const int s0 = __shfl_sync(0xffffffffu, my_src, i);
+        const int s1 = __shfl_sync(0xffffffffu, my_src, (i + 1) & 31);
+        const bool two = i + 1 < nr;
+        for (int v0 = lane; v0 < vpr; v0 += 32 * 8) {
+          uint4 a[8], b[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int v = v0 + 32 * q;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            a[q] = (v < vpr && s0 >= 0) ? __ldg(x + static_cast<size_t>(s0) * vpr + v) : z;
+            b[q] = (v < vpr && two && s1 >= 0) ? __ldg(x + static_cast<size_t>(s1) * vpr + v) : z;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int v = v0 + 32 * q;
+            if (v < vpr) {
+              xp[static_cast<size_t>(r0 + i) * vpr + v] = a[q];
+              if (two) xp[static_cast<size_t>(r0 + i + 1) * vpr + v] = b[q];
+            }
+          }
+        }
+      }
+      ptx::fence_proxy_async_global();
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) ptx::st_release_gpu_u32(p.stage_flags + c, epoch);
+    }
+  } else if (kStaged && warp == kPairThreads / 32 + 2) {
+    // ------------------------------------------------------------ watcher
+    // Lane 0 walks this CTA's tiles ahead of the producer: once every chunk
+    // holding the CTA's rows of a tile carries this launch's flag value, it
+    // fences for the async proxy and publishes the count of ready tiles.
+    if (lane == 0) {
+      const uint32_t epoch = *s_epoch;
+      uint32_t n_ready = 0;
+      bool ok = true;
+      for (int tile = unit; ok && tile < total; tile += n_units) {
+        const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+        const int half = ((t.n_tok + 15) & ~15) >> 1;
+        const int lo = t.r0 + static_cast<int>(rank) * half;        // this CTA's rows
+        const int cnt = min(half, t.n_tok - static_cast<int>(rank) * half);  // real ones
+        if (cnt > 0) {
+          for (int c = lo / kStageRows; ok && c <= (lo + cnt - 1) / kStageRows; ++c)
+            ok = wait_flag(p.stage_flags + c, epoch, abort_flag, p.status, wait_ns);
+          if (!ok) break;
+          ptx::fence_proxy_async_global();
+        }
+        ptx::st_release_cta_shared_u32(s_ready, ++n_ready);
       }
     }
   } else if (kGather && warp >= kPairThreads / 32) {
@@ -631,16 +793,27 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     ptx::tc_fence_after();
     ptx::tmem_dealloc2(tmem_base, 2 * kTokBlock);
   }
+  if (kStaged && threadIdx.x == 0) {
+    // the last CTA to finish records this launch's flag value for the next
+    // launch (its flags then mean "ready" to nobody) and resets the count
+    __threadfence();
+    const unsigned int prev = atomicAdd(p.stage_ctl + 1, 1u);
+    if (prev + 1u == gridDim.x) {
+      p.stage_ctl[1] = 0u;
+      *reinterpret_cast<volatile unsigned int*>(p.stage_ctl) = *s_epoch;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace
 
 // The pair kernels' grid: clusters of two CTAs, as many as can be resident.
-template <int kEpi, bool kGather>
+template <int kEpi, int kSrc>
 int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtensorMap& tw,
                        PairParams p, long long tiles, cudaStream_t stream) {
-  auto kern = pair_gemm_kernel<kEpi, kGather>;
-  constexpr int kNT = kGather ? kPairThreads + kGatherThreads : kPairThreads;
+  auto kern = pair_gemm_kernel<kEpi, kSrc>;
+  constexpr int kNT = pair_threads(kSrc);
   const int smem = PSmem::ALLOC;
   static std::atomic<int> configured_dev[64] = {};
   static std::atomic<int> max_pairs_dev[64] = {};
@@ -737,8 +910,40 @@ int launch_pair_gateup(const char* op, const void* a_bf16, int a_rows,
   p.gather_div = gather_div;
   p.kid = MOE_KID_GEMM_GATEUP;
   const long long tiles = pair_tile_bound(P, G, I, 128);
-  if (a_row_gather) return launch_pair_kernel<PEPI_GATEUP, true>(op, tt, tw, p, tiles, stream);
-  return launch_pair_kernel<PEPI_GATEUP, false>(op, tt, tw, p, tiles, stream);
+  if (a_row_gather) return launch_pair_kernel<PEPI_GATEUP, SRC_GATHER>(op, tt, tw, p, tiles, stream);
+  return launch_pair_kernel<PEPI_GATEUP, SRC_TMA>(op, tt, tw, p, tiles, stream);
+}
+
+int launch_pair_gateup_staged(const char* op, const void* x_bf16, int T,
+                              const int32_t* sorted_pair, int K, void* x_perm_bf16,
+                              const void* w13_bf16, const int32_t* group_offsets, int P, int H,
+                              int I, int G, void* act_bf16, int32_t* stage_flags,
+                              unsigned int* stage_ctl, cudaStream_t stream) {
+  CUtensorMap tt[3], tw;
+  int rc;
+  if ((rc = make_tmap(&tw, w13_bf16, static_cast<long long>(G) * 2 * I, H, 64, op, "w13")) !=
+      MOE_OK)
+    return rc;
+  if ((rc = make_token_maps(tt, x_perm_bf16, P, H, op, "x_perm")) != MOE_OK) return rc;
+  PairParams p{};
+  p.group_offsets = group_offsets;
+  p.P = P;
+  p.Kdim = H;
+  p.N = I;
+  p.G = G;
+  p.w_rows_per_group = 2 * I;
+  p.half_off = I;
+  p.out = act_bf16;
+  p.a = static_cast<const uint16_t*>(x_bf16);
+  p.a_rows = T;
+  p.row_gather = sorted_pair;
+  p.gather_div = K;
+  p.stage_out = static_cast<uint16_t*>(x_perm_bf16);
+  p.stage_flags = stage_flags;
+  p.stage_ctl = stage_ctl;
+  p.kid = MOE_KID_GEMM_GATEUP;
+  return launch_pair_kernel<PEPI_GATEUP, SRC_STAGED>(op, tt, tw, p, pair_tile_bound(P, G, I, 128),
+                                                      stream);
 }
 
 int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
@@ -762,7 +967,7 @@ int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
   p.pair_weight = pair_weight;
   p.row_to_pair = row_to_pair;
   p.kid = MOE_KID_GEMM_DOWN;
-  return launch_pair_kernel<PEPI_DOWN, false>(op, tt, tw, p, pair_tile_bound(P, G, H, 256),
+  return launch_pair_kernel<PEPI_DOWN, SRC_TMA>(op, tt, tw, p, pair_tile_bound(P, G, H, 256),
                                              stream);
 }
 

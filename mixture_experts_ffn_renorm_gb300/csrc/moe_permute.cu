@@ -14,6 +14,7 @@
 //           rank of a pair among equal experts of its step comes from one
 //           ballot per id bit, so rows inside an expert ascend with p
 //   gather  (optional) x_perm[row] = x[sorted_pair[row] / K], 16 bytes a thread
+//           (zeros for a row outside x)
 // Up to kSmallChunks chunks whose histograms fit in 48 KB of shared memory
 // (decode batches; the large layer's 16384 pairs over 256 experts) count, scan
 // and place run in one block (permute_small): the same steps, one launch
@@ -257,8 +258,8 @@ permute_place(const int32_t* __restrict__ ids, int P, int E, int n_chunks,
 // L2 only if the stream of x_perm writes does not push it out (with plain
 // stores x was read from DRAM about 2.8 times).
 __global__ void __launch_bounds__(256)
-permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair, int P,
-               int K, int H, uint16_t* __restrict__ x_perm, unsigned long long* launches) {
+permute_gather(const uint16_t* __restrict__ x, int x_rows, const int32_t* __restrict__ sorted_pair,
+               int P, int K, int H, uint16_t* __restrict__ x_perm, unsigned long long* launches) {
   count_launch(launches, MOE_KID_PERMUTE_GATHER);
   grid_dep_wait();
   grid_dep_launch();
@@ -267,14 +268,15 @@ permute_gather(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorte
   for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
        row < P; row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
     const int src = __ldg(sorted_pair + row) / K;
-    const uint4* s = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src) * H);
+    const bool in = src >= 0 && src < x_rows;      // a row outside x is written as zeros
+    const uint4* s = reinterpret_cast<const uint4*>(x + static_cast<size_t>(in ? src : 0) * H);
     uint4* d = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(row) * H);
     for (int v0 = 0; v0 < vpr; v0 += 32 * 8) {
       uint4 buf[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int v = v0 + i * 32 + lane;
-        if (v < vpr) buf[i] = __ldg(s + v);
+        if (v < vpr) buf[i] = in ? __ldg(s + v) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -371,20 +373,30 @@ namespace moe {
 namespace {
 
 // the optional x_perm gather after the sort
-int gather(const char* op, const void* x_bf16, void* x_perm_bf16, const int32_t* sorted_pair,
-           long long P, int K, int H, cudaStream_t s, const DeviceDiag& diag) {
+int gather(const char* op, const void* x_bf16, int x_rows, void* x_perm_bf16,
+           const int32_t* sorted_pair, long long P, int K, int H, cudaStream_t s,
+           const DeviceDiag& diag) {
   if (!x_perm_bf16) return MOE_OK;
   long long g = (P + 7) / 8;  // 8 rows (warps) per block, at most 32 blocks per SM
   const long long cap = 32LL * sm_count();
   if (g > cap) g = cap;
   return launch_status(
       launch_kernel(permute_gather, dim3(static_cast<unsigned>(g)), dim3(256), 0, s, nullptr, 0,
-                    static_cast<const uint16_t*>(x_bf16), sorted_pair, static_cast<int>(P), K, H,
+                    static_cast<const uint16_t*>(x_bf16), x_rows, sorted_pair, static_cast<int>(P), K, H,
                     static_cast<uint16_t*>(x_perm_bf16), diag.launches),
       op);
 }
 
 }  // namespace
+}  // namespace moe
+
+namespace moe {
+// x_perm[r] = x[sorted_pair[r] / K] for r < P on its own (the gate/up entry
+// with staged rows uses it for batches that take single-CTA tiles)
+int launch_row_gather(const char* op, const void* x_bf16, int x_rows, void* x_perm_bf16,
+                      const int32_t* sorted_pair, long long P, int K, int H, cudaStream_t s) {
+  return gather(op, x_bf16, x_rows, x_perm_bf16, sorted_pair, P, K, H, s, device_diag());
+}
 }  // namespace moe
 
 using namespace moe;
@@ -432,7 +444,7 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
                                          sorted_pair, pair_to_row, diag.status, diag.launches),
                            op);
     if (rc != MOE_OK) return rc;
-    return gather(op, x_bf16, x_perm_bf16, sorted_pair, P, K, H, s, diag);
+    return gather(op, x_bf16, T, x_perm_bf16, sorted_pair, P, K, H, s, diag);
   }
   if (n_chunks > 0) {
     int rc = launch_status(launch_kernel(permute_count, dim3(blocks), dim3(kWarps * 32), smem, s,
@@ -450,5 +462,5 @@ extern "C" int moe_permute(const int32_t* topk_ids, const void* x_bf16, int T, i
                                    expert_offsets, sorted_pair, pair_to_row, diag.launches),
                      op);
   if (rc != MOE_OK) return rc;
-  return gather(op, x_bf16, x_perm_bf16, sorted_pair, P, K, H, s, diag);
+  return gather(op, x_bf16, T, x_perm_bf16, sorted_pair, P, K, H, s, diag);
 }

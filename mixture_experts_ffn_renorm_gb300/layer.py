@@ -17,7 +17,8 @@ from . import (BF16, QFMT_Q4_K, QFMT_Q8_0, moe_combine, moe_combine_gate,
                moe_gate_workspace_size, moe_grouped_gemm_down_bf16,
                moe_grouped_gemm_down_bf16_shared, moe_grouped_gemm_down_fp8w,
                moe_grouped_gemm_down_q, moe_grouped_gemm_gateup_silu_bf16,
-               moe_grouped_gemm_gateup_silu_bf16_shared, moe_grouped_gemm_gateup_silu_fp8w,
+               moe_grouped_gemm_gateup_silu_bf16_shared, moe_grouped_gemm_gateup_silu_bf16_staged,
+               moe_grouped_gemm_gateup_silu_fp8w, moe_gateup_staged_workspace_size,
                moe_grouped_gemm_gateup_silu_q, moe_dequantize_q_bf16, moe_permute,
                moe_permute_workspace_size, moe_quantize_act_q8, moe_route_topk,
                moe_route_topk_workspace_size)
@@ -58,7 +59,7 @@ class MoeBlock:
 
     def __init__(self, H, I, E, K, weights, max_tokens, device="cuda", I_shared=0,
                  routed_scale=1.0, gather=False, fuse_shared=True, fp8_weights=False,
-                 qweights=None, q_dequant=False):
+                 qweights=None, q_dequant=False, staged=False):
         self.H, self.I, self.E, self.K, self.Is = H, I, E, K, I_shared
         if qweights is not None:
             if qweights not in Q_WEIGHTS:
@@ -84,6 +85,12 @@ class MoeBlock:
         self.fuse_shared = fuse_shared and not gather and not fp8_weights and not self.qfmt
         if fp8_weights and gather:
             raise ValueError("FP8 expert weights read x_perm rows (gather=False)")
+        # staged=True: permute skips its row gather and the gate/up call writes
+        # x_perm itself (on CTA pairs inside the GEMM launch); bf16 experts only
+        self.staged = staged
+        if staged and (gather or fp8_weights or self.qfmt or (I_shared > 0 and self.fuse_shared)):
+            raise ValueError("staged rows need plain bf16 experts, gather=False and no fused "
+                             "shared expert")
         self.routed_scale = float(routed_scale)
         self.device = torch.device(device)
         if self.device.type != "cuda":
@@ -122,6 +129,9 @@ class MoeBlock:
         self.sorted_pair = torch.empty((P,), dtype=i32, device=dv)
         self.pair_to_row = torch.empty((P,), dtype=i32, device=dv)
         self.x_perm = None if gather else torch.empty((P, H), dtype=bf, device=dv)
+        # zero-filled once, then passed unchanged to every staged call
+        self.ws_staged = (torch.zeros(max(16, moe_gateup_staged_workspace_size(P)),
+                                      dtype=torch.uint8, device=dv) if staged else None)
         self.act = torch.empty((P, I), dtype=bf, device=dv)
         if self.qfmt:
             # 8-bit activation blocks of the token rows and of the act rows
@@ -169,7 +179,8 @@ class MoeBlock:
                        self.gate_logit if self.has_shared else None, ws, ws.numel(), stream)
         mark("route")
         moe_permute(self.topk_ids, x, T, K, E, H, self.expert_offsets, self.sorted_pair,
-                    self.pair_to_row, self.x_perm, ws, ws.numel(), stream)
+                    self.pair_to_row, None if self.staged else self.x_perm, ws, ws.numel(),
+                    stream)
         mark("permute")
         fused = self.has_shared and self.fuse_shared
         if self.qfmt:
@@ -186,6 +197,11 @@ class MoeBlock:
             moe_grouped_gemm_gateup_silu_bf16_shared(self.x_perm, self.w13, self.expert_offsets,
                                                      P, H, I, E, self.act, x, T, self.w13_shared,
                                                      self.Is, self.act_shared, None, 0, stream)
+        elif self.staged:
+            moe_grouped_gemm_gateup_silu_bf16_staged(x, T, self.sorted_pair, K, self.x_perm,
+                                                     self.w13, self.expert_offsets, P, H, I, E,
+                                                     self.act, self.ws_staged,
+                                                     self.ws_staged.numel(), stream)
         elif self.gather:
             moe_grouped_gemm_gateup_silu_bf16(x, T, self.sorted_pair, K, self.w13,
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,

@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_refusals_without_gpu(lib):
-    assert m.abi_version() == 9
+    assert m.abi_version() == 10
     # dtype refusals name the missing arm and return before touching the device
     rc = lib.moe_combine(None, m.F16, None, None, m.BF16, 1.0, 1, 1, 8, None, m.BF16, None)
     assert rc == m.ERR_DTYPE and "f16" in m.last_error()
@@ -183,3 +183,29 @@ def test_block_expansion_refuses_without_touching_the_device(lib):
     assert lib.moe_dequantize_q_bf16(a, m.QFMT_Q8_0, 1, 32, two, None) == m.ERR_ALIGN
     # no rows is a no-op, whatever the pointers
     assert lib.moe_dequantize_q_bf16(None, m.QFMT_Q8_0, 0, 32, None, None) == m.OK
+
+
+def test_staged_gateup_checks_arguments_without_touching_the_device(lib):
+    # the gate/up entry with staged rows: workspace size, then every refusal that
+    # happens before a launch
+    import ctypes
+    buf = (ctypes.c_uint8 * 8192)()
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    odd = ctypes.c_void_p(a.value + 2)
+    # a 256-byte control block, then one flag per 16 rows padded to 256 bytes
+    assert lib.moe_gateup_staged_workspace_size(0) == 0
+    assert lib.moe_gateup_staged_workspace_size(1) == 512
+    assert lib.moe_gateup_staged_workspace_size(16 * 64) == 512
+    assert lib.moe_gateup_staged_workspace_size(16 * 64 + 1) == 768
+    f = lib.moe_grouped_gemm_gateup_silu_bf16_staged
+    # P = 0 is a no-op and needs no workspace
+    assert f(a, 1, None, 1, None, a, None, 0, 64, 64, 1, a, None, 0, None) == m.OK
+    assert f(a, 4, a, 0, a, a, None, 4, 64, 64, 1, a, a, 4096, None) == m.ERR_ARG   # K = 0
+    assert "K=0" in m.last_error()
+    assert f(a, 0, a, 1, a, a, None, 4, 64, 64, 1, a, a, 4096, None) == m.ERR_ARG   # T = 0
+    assert f(a, 4, None, 1, a, a, None, 4, 64, 64, 1, a, a, 4096, None) == m.ERR_ARG
+    assert f(a, 4, a, 1, None, a, None, 4, 64, 64, 1, a, a, 4096, None) == m.ERR_ARG
+    assert f(a, 4, a, 1, odd, a, None, 4, 64, 64, 1, a, a, 4096, None) == m.ERR_ALIGN
+    assert f(a, 4, a, 1, a, a, None, 4, 64, 64, 1, a, a, 256, None) == m.ERR_WORKSPACE
+    assert f(a, 4, a, 1, a, a, None, 4, 64, 64, 1, a, None, 4096, None) == m.ERR_WORKSPACE
+    assert f(a, 4, a, 1, a, a, None, 4, 64, 64, 2, a, a, 4096, None) == m.ERR_ARG   # G > 1, no offsets

@@ -393,3 +393,81 @@ def test_gemm_refusals_and_empty():
     before = launches()
     assert m.moe_grouped_gemm_down_bf16(act, act, None, None, None, 0, 64, 64, 1, act) == 0
     assert launches() == before
+
+
+def _staged_ws(P):
+    # zero-filled once; later calls pass it unchanged
+    return torch.zeros(max(1, m.moe_gateup_staged_workspace_size(P)), dtype=torch.uint8,
+                       device="cuda")
+
+
+def _staged(x, T, pair, K, W13, off, P, H, I, G, ws):
+    xp = empty((P, H), torch.bfloat16)
+    act = empty((P, I), torch.bfloat16)
+    before = launches()
+    m.moe_grouped_gemm_gateup_silu_bf16_staged(to_dev(x), T, to_dev(pair), K, xp, to_dev(W13),
+                                               to_dev(off), P, H, I, G, act, ws, ws.numel())
+    assert launched_since(before, "gemm_gateup") == 1
+    assert m.moe_device_status() == 0
+    return to_host(xp), to_host(act)
+
+
+@pytest.mark.parametrize("sizes,H,I", SHAPES)
+@pytest.mark.parametrize("K", [1, 8])
+def test_gateup_silu_staged_rows(sizes, H, I, K, tiling):
+    # x_perm is written by the call itself (on CTA pairs by stager warps of the
+    # GEMM launch, ahead of the tiles that read it): it must hold x[pair // K],
+    # and act must be the oracle's and bit-identical to the x_perm entry on it
+    off, P, G, _, W13, _ = _case(sizes, H, I, sum(sizes) + 5 * H + K)
+    rng = np.random.default_rng(P + 31 * K)
+    T = max(1, (P + K - 1) // K) + 2
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    pair = rng.integers(0, T * K, P).astype(np.int32)
+    ws = _staged_ws(P)
+    xp, act = _staged(x, T, pair, K, W13, off, P, H, I, G, ws)
+    assert np.array_equal(xp, x[pair // K])
+    want = O.gateup_silu(x, W13, off, P=P, H=H, I=I, G=G, a_row_gather=(pair // K).astype(np.int32))
+    assert_gemm_close(act, want, "staged gate/up")
+    ref = empty((P, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(xp), P, None, 1, to_dev(W13), to_dev(off), P, H, I,
+                                        G, ref)
+    assert np.array_equal(act, to_host(ref))
+
+
+def test_staged_rows_repeated_calls_and_out_of_range_rows(tiling):
+    # one workspace over several calls with new inputs each time: every call must
+    # wait for its own chunks (the flags of earlier launches mean nothing to it);
+    # source rows outside [0, T) are staged as zeros
+    sizes, H, I = _zipf_sizes(16, 6000, 1.1, 7), 512, 256
+    off, P, G, _, W13, _ = _case(sizes, H, I, 77)
+    K, T = 8, 6000 // 8 + 1
+    ws = _staged_ws(P)
+    for call in range(3):
+        rng = np.random.default_rng(100 + call)
+        x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+        pair = rng.integers(0, T * K, P).astype(np.int32)
+        pair[::97] = T * K + 5                        # row T: outside x
+        xp, act = _staged(x, T, pair, K, W13, off, P, H, I, G, ws)
+        src = pair // K
+        ok = src < T
+        assert np.array_equal(xp[ok], x[src[ok]])
+        assert not xp[~ok].any()
+        want = O.gateup_silu(np.concatenate([x, np.zeros((1, H), np.uint16)]), W13, off, P=P, H=H,
+                             I=I, G=G, a_row_gather=np.minimum(src, T).astype(np.int32))
+        assert_gemm_close(act, want, f"staged gate/up, call {call}")
+
+
+@pytest.mark.parametrize("sizes,H,I", MULTI_ROUND[:1], ids=["zipf24k"])
+def test_staged_rows_multi_round_every_row(sizes, H, I, tiling):
+    # several rounds of tiles per CTA, every row compared with the oracle
+    off, P, G, A, W13, _ = _case(sizes, H, I, 13 + H)
+    K = 8
+    pair = np.random.default_rng(P).integers(0, P * K, P).astype(np.int32)
+    src = pair // K                                   # rows of A, used as x (T = P)
+    xp, act = _staged(A, P, pair, K, W13, off, P, H, I, G, _staged_ws(P))
+    assert np.array_equal(xp, A[src])
+    want = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G, a_row_gather=src.astype(np.int32))
+    assert_gemm_close(act, want, "staged multi-round gate/up")
+    g, r = bf16_to_f64(act), bf16_to_f64(want)
+    row_err = np.sum((g - r) ** 2, 1) / np.maximum(np.sum(r * r, 1), 1e-30)
+    assert row_err.max() <= 1e-4, (int(row_err.argmax()), float(row_err.max()))

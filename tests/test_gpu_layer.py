@@ -197,6 +197,25 @@ def test_materialised_x_perm_path_matches_gather_path(cfg):
     assert np.array_equal(to_host(blk.x_perm), d["x"][sp // cfg.K])
 
 
+@pytest.mark.parametrize("cfg", [W.DECODE, W.PREFILL], ids=["decode", "prefill"])
+def test_staged_rows_match_the_x_perm_path(cfg):
+    # staged=True: the gate/up call writes x_perm itself (on CTA pairs inside the
+    # GEMM launch, behind per-chunk flags whose value the workspace carries from
+    # call to call); eager calls and graph replays must give the x_perm path's bits
+    d = W.layer_inputs(cfg)
+    x = to_dev(d["x"])
+    ref = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda")
+    want = to_host(ref.forward(x))
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda", staged=True)
+    for _ in range(2):
+        assert np.array_equal(to_host(blk.forward(x)), want)
+    assert np.array_equal(to_host(blk.x_perm), to_host(ref.x_perm))
+    blk.capture(x)
+    for _ in range(2):
+        assert np.array_equal(to_host(blk.replay()), want)
+    assert m.moe_device_status() == 0
+
+
 @pytest.mark.slow
 def test_gemm_tilings_agree_on_prefill():
     # single-CTA and CTA-pair tiles differ only in f32 accumulation order

@@ -83,19 +83,32 @@ def test_wait_limit_expiry_is_reported_and_the_device_stays_usable(tiling):
     def gathered():
         return m.moe_grouped_gemm_gateup_silu_bf16(dA, P, ident, 1, dW13, doff, P, H, I, G, act_g)
 
+    # staged rows (identity again): on CTA pairs the tiles also wait for the
+    # chunks that stager warps of other CTAs write; the workspace carries the
+    # flag value of the last launch across the timed-out call
+    act_s = empty((P, I), torch.bfloat16)
+    xp_s = empty((P, H), torch.bfloat16)
+    ws_s = torch.zeros(m.moe_gateup_staged_workspace_size(P), dtype=torch.uint8, device="cuda")
+
+    def staged():
+        return m.moe_grouped_gemm_gateup_silu_bf16_staged(dA, P, ident, 1, xp_s, dW13, doff, P, H,
+                                                          I, G, act_s, ws_s, ws_s.numel())
+
     # a 1 us limit: every launch gives up, reports it and ends
     m.moe_set_wait_limit_ns(1000)
-    for call in ("gateup", "gateup_gather", "down"):
+    for call in ("gateup", "gateup_gather", "gateup_staged", "down"):
         before = launches()
         if call == "gateup":
             rc = m.moe_grouped_gemm_gateup_silu_bf16(dA, P, None, 1, dW13, doff, P, H, I, G, act)
         elif call == "gateup_gather":
             rc = gathered()
+        elif call == "gateup_staged":
+            rc = staged()
         else:
             rc = m.moe_grouped_gemm_down_bf16(act, dW2, doff, dwts, dr2p, P, I, H, G, out)
         assert rc == m.OK                       # the launch itself was accepted
         torch.cuda.synchronize()                # and the kernel ended
-        assert launched_since(before, "gemm_" + call.replace("_gather", "")) == 1
+        assert launched_since(before, "gemm_" + call.split("_")[0]) == 1
         status = m.moe_device_status(clear=True)
         assert status & m.STATUS_TIMEOUT, f"{call}: status {status}"
         assert m.moe_device_status() == 0
@@ -104,10 +117,13 @@ def test_wait_limit_expiry_is_reported_and_the_device_stays_usable(tiling):
     m.moe_set_wait_limit_ns(FULL_LIMIT_NS)
     got_act, got_out = run()
     assert gathered() == m.OK
+    assert staged() == m.OK
     torch.cuda.synchronize()
     assert m.moe_device_status() == 0
     assert np.array_equal(got_act, ref_act)
     assert np.array_equal(to_host(act_g), ref_act)
+    assert np.array_equal(to_host(act_s), ref_act)
+    assert np.array_equal(to_host(xp_s), A)
     assert np.array_equal(got_out, ref_out)
     # and they are the oracle's, on sampled rows
     rows = np.unique(np.concatenate([off[:-1], np.random.default_rng(3).choice(P, 200, False),
