@@ -111,21 +111,30 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
     constexpr int kQ = kPerLane >= kLoads ? 1 : (kLoads / kPerLane > 16 ? 16 : kLoads / kPerLane);
     const float* row = logits + static_cast<size_t>(t) * E;
     const size_t slab = static_cast<size_t>(T) * E;
-    for (int q0 = 0; q0 < n_part; q0 += kQ) {
-      float part[kQ][kPerLane];
+    if (n_part == 1) {
+      // no K split (prefill-sized batches): one load per logit
 #pragma unroll
-      for (int j = 0; j < kQ; ++j)
+      for (int i = 0; i < kPerLane; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(row + e) : 0.0f;
+      }
+    } else {
+      for (int q0 = 0; q0 < n_part; q0 += kQ) {
+        float part[kQ][kPerLane];
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-          const int e = lane + 32 * i;
-          part[j][i] = (q0 + j < n_part && e < E) ? __ldg(row + (q0 + j) * slab + e) : 0.0f;
-        }
+        for (int j = 0; j < kQ; ++j)
 #pragma unroll
-      for (int j = 0; j < kQ; ++j)
-        if (q0 + j < n_part)
+          for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            part[j][i] = (q0 + j < n_part && e < E) ? __ldg(row + (q0 + j) * slab + e) : 0.0f;
+          }
 #pragma unroll
-          for (int i = 0; i < kPerLane; ++i)
-            v[i] = q0 + j == 0 ? part[j][i] : __fadd_rn(v[i], part[j][i]);
+        for (int j = 0; j < kQ; ++j)
+          if (q0 + j < n_part)
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i)
+              v[i] = q0 + j == 0 ? part[j][i] : __fadd_rn(v[i], part[j][i]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
