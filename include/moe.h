@@ -396,24 +396,26 @@ int moe_grouped_gemm_down_fp8w(const void* act_bf16, const uint8_t* w2_e4m3,
                                int I, int H, int G, void* out_bf16, void* workspace,
                                size_t ws_bytes, void* stream);
 
-/* moe_set_gemm_pairing -- tiling of moe_grouped_gemm_gateup_silu_bf16 (without
- * a row gather) and moe_grouped_gemm_down_bf16:
- *   MOE_GEMM_AUTO (default): CTA-pair tiles when P >= 1024 and the groups
- *                    average at least 32 rows (P >= 32 G), single-CTA tiles
- *                    otherwise
+/* moe_set_gemm_pairing -- tiling of moe_grouped_gemm_gateup_silu_bf16 (also
+ * with gathered or staged rows) and moe_grouped_gemm_down_bf16:
+ *   MOE_GEMM_AUTO (default): CTA-pair tiles when P >= 1024, the groups average
+ *                    at least 32 rows (P >= 32 G) and G <= 512, single-CTA
+ *                    tiles otherwise
  *   MOE_GEMM_SINGLE: one CTA per 128-row x N tile (32-row tiles when P <= 16 G)
- *   MOE_GEMM_PAIR:   CTA-pair tiles for every such call.  A pair of SMs runs one
- *                    tcgen05.mma.cta_group::2 with the group's weight rows on
- *                    the M side (128 per SM) and up to 256 of its rows on the N
- *                    side (N = their count rounded up to 16), so a group pads
- *                    to 16 rows, and each SM stages 16 KB of weights plus at
- *                    most 16 KB of rows per 64-wide K step
- * Results agree up to f32 accumulation order.  The gathered gate/up, the FP8
- * weight GEMMs and the fused shared-expert launches always use single-CTA
- * tiles.  Values 3 and 4 (tilings measured slower and not built) are refused
- * with MOE_ERR_UNSUPPORTED, others with MOE_ERR_ARG.  Process-wide, takes
- * effect at the next launch; returns the previous mode.  Not for use while
- * another thread is launching these GEMMs. */
+ *   MOE_GEMM_PAIR:   CTA-pair tiles for every such call with G <= 512.  A pair
+ *                    of SMs runs one tcgen05.mma.cta_group::2 with the group's
+ *                    weight rows on the M side (128 per SM) and up to 256 of its
+ *                    rows on the N side (N = their count rounded up to 16), so a
+ *                    group pads to 16 rows, and each SM stages 16 KB of weights
+ *                    plus at most 16 KB of rows per 64-wide K step.  In the
+ *                    gate/up GEMM a group's last block of at most 32 rows takes
+ *                    two feature blocks per tile (twice the weight rows per step)
+ * Results agree up to f32 accumulation order.  The FP8 weight GEMMs and the
+ * fused shared-expert launches always use single-CTA tiles.  Values 3 and 4
+ * (tilings measured slower and not built) are refused with
+ * MOE_ERR_UNSUPPORTED, others with MOE_ERR_ARG.  Process-wide, takes effect at
+ * the next launch; returns the previous mode.  Not for use while another
+ * thread is launching these GEMMs. */
 enum { MOE_GEMM_AUTO = 0, MOE_GEMM_SINGLE = 1, MOE_GEMM_PAIR = 2 };
 int moe_set_gemm_pairing(int mode);
 

@@ -16,6 +16,9 @@ constexpr int BM = 128;           // rows per tile on one SM (MMA M of one CTA)
 constexpr int BK = 64;            // bf16 per 128-byte swizzled row: K per stage
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int kMaxGroups = 1024;
+// groups a CTA-pair launch takes (its schedule tables in shared memory); calls
+// with more take single-CTA tiles
+constexpr int kMaxPairGroups = 512;
 // Limit of the waits that drain a CTA's own copies and MMAs before it exits
 // (always this long, whatever the pipeline limit is set to).
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;

@@ -920,6 +920,7 @@ std::atomic<int> g_pairing{MOE_GEMM_AUTO};
 // tensor cores bind and the pair tiles' smaller padding and shared-memory fill
 // pay); never for MOE_GEMM_SINGLE.
 bool use_pair_tiles(int P, int G) {
+  if (G > kMaxPairGroups) return false;
   const int mode = g_pairing.load(std::memory_order_relaxed);
   if (mode == MOE_GEMM_PAIR) return true;
   return mode == MOE_GEMM_AUTO && P >= 1024 && static_cast<long long>(P) >= 32LL * G;

@@ -86,6 +86,12 @@ constexpr int kTokBlock = 256;        // tokens per tile at most (MMA N)
 // token rows per TMA box: three tensor maps over the token rows, with boxes of
 // 32, 64 and 128 rows; a stage takes the smallest that covers its N / 2 rows
 constexpr int kTokBoxMin = 32;
+// gate/up: the last token block of a group with at most kShortTok rows is a
+// short block; its tiles take two feature blocks each (the weights of the
+// second fill the stage's token slot, its token rows a 2 KB side slot), so a
+// short block costs half the tiles and twice the weight rows per stage
+constexpr int kShortTok = 32;
+constexpr int kSideBytes = 16 * BK * 2;   // one CTA's token rows of a short tile's stage
 constexpr int kPStages = 6;
 constexpr int kWBytes = 128 * BK * 2; // one CTA's weight rows per stage: 16 KB
 constexpr int kTBytes = 128 * BK * 2; // one CTA's token rows per stage, at most: 16 KB
@@ -124,42 +130,64 @@ struct PSmem {
   static constexpr int STAGE_W = 0;                                  // kPStages x 16 KB
   static constexpr int STAGE_T = STAGE_W + kPStages * kWBytes;       // kPStages x 16 KB
   static constexpr int EPI = STAGE_T + kPStages * kTBytes;           // 2 groups x 8 KB
-  static constexpr int META_DST = EPI + 2 * 8192;                    // int[2][256]
-  static constexpr int META_W = META_DST + 2 * kTokBlock * 4;        // float[2][256]
+  static constexpr int META_DST = EPI + 2 * 8192;                    // down: int[2][256]
+  static constexpr int META_W = META_DST + 2 * kTokBlock * 4;        // down: float[2][256]
+  // gate/up short tiles: kPStages side slots of token rows (over the down's META)
+  static constexpr int SIDE = EPI + 2 * 8192;
   // full[kPStages], empty[kPStages], tfull[2], tempty[2], drain, gathered[kPStages]
-  static constexpr int BARS = META_W + 2 * kTokBlock * 4;
+  static constexpr int BARS = SIDE + kPStages * kSideBytes;
   static constexpr int NBARS = 3 * kPStages + 5;
   // tmem slot, abort flag, scan (one int per warp), staged rows: ready tiles, epoch
   static constexpr int MISC = BARS + NBARS * 8;
   static constexpr int TILE_START = MISC + 128;
-  static constexpr int GOFF = TILE_START + (kMaxGroups + 1) * 4;
-  static constexpr int BYTES = GOFF + (kMaxGroups + 1) * 4;
+  static constexpr int GOFF = TILE_START + (kMaxPairGroups + 1) * 4;
+  static constexpr int BYTES = GOFF + (kMaxPairGroups + 1) * 4;
   static constexpr int ALLOC = BYTES + 1024;
 };
+static_assert(PSmem::META_W + 2 * kTokBlock * 4 <= PSmem::BARS, "down's META inside SIDE");
+static_assert(PSmem::SIDE % 1024 == 0, "side slots on the 128-byte swizzle's 1 KB atoms");
 static_assert(PSmem::ALLOC <= 227 * 1024, "pair GEMM shared memory");
 
 struct PTile {
   int g, r0, n_tok, n0;
+  int nblk;   // feature blocks of the tile: 1, or 2 for a short block's tile
 };
 
-__device__ __forceinline__ int pair_m_tiles(int rows) {
-  return rows <= 0 ? 0 : (rows + kTokBlock - 1) / kTokBlock;
+// tiles of a group of `rows` rows: its token blocks times n_fb feature blocks,
+// the short last block (shorts) taking its feature blocks two at a time
+__device__ __forceinline__ int pair_group_tiles(int rows, int n_fb, bool shorts) {
+  if (rows <= 0) return 0;
+  const int m = (rows + kTokBlock - 1) / kTokBlock;
+  const int last = rows - (m - 1) * kTokBlock;
+  return (m - 1) * n_fb + (shorts && last <= kShortTok ? (n_fb + 1) / 2 : n_fb);
 }
 
 __device__ __forceinline__ PTile pair_tile(int tile, const int* tile_start, const int* goff, int G,
-                                           int n_fb, int fb_cols) {
+                                           int n_fb, int fb_cols, bool shorts) {
   int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (tile_start[mid] <= tile) lo = mid; else hi = mid;
   }
   const int local = tile - tile_start[lo];
-  const int m = local / n_fb;
+  const int rows = goff[lo + 1] - goff[lo];
+  const int m_last = (rows - 1) / kTokBlock;          // the group's last token block
+  const int last = rows - m_last * kTokBlock;
   PTile t;
   t.g = lo;
+  if (shorts && last <= kShortTok && local >= m_last * n_fb) {
+    const int j = local - m_last * n_fb;               // two feature blocks: 2j, 2j + 1
+    t.r0 = goff[lo] + m_last * kTokBlock;
+    t.n_tok = last;
+    t.n0 = 2 * j * fb_cols;
+    t.nblk = min(2, n_fb - 2 * j);
+    return t;
+  }
+  const int m = local / n_fb;
   t.r0 = goff[lo] + m * kTokBlock;
   t.n_tok = min(goff[lo + 1], t.r0 + kTokBlock) - t.r0;
   t.n0 = (local - m * n_fb) * fb_cols;
+  t.nblk = 1;
   return t;
 }
 
@@ -213,13 +241,16 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
 // gate/up only.
 template <int kEpi, int kSrc>
 __global__ void __launch_bounds__(pair_threads(kSrc), 1)
-pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
+pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT16,
+                 const __grid_constant__ CUtensorMap tmT32,
                  const __grid_constant__ CUtensorMap tmT64,
                  const __grid_constant__ CUtensorMap tmT128,
                  const __grid_constant__ CUtensorMap tmW, const PairParams p) {
   constexpr bool kGU = kEpi == PEPI_GATEUP;
   constexpr bool kGather = kSrc == SRC_GATHER;
   constexpr bool kStaged = kSrc == SRC_STAGED;
+  // short blocks' tiles take two feature blocks (gate/up with TMA token boxes)
+  constexpr bool kShorts = kGU && !kGather;
   static_assert(kGU || kSrc == SRC_TMA, "gathered or staged token rows: gate/up only");
   constexpr int kNT = pair_threads(kSrc);
   constexpr int kFbCols = kGU ? 128 : 256;   // output features per tile (both CTAs)
@@ -274,6 +305,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
+    if (kShorts) ptx::tma_prefetch_desc(&tmT16);
     ptx::tma_prefetch_desc(&tmT32);
     ptx::tma_prefetch_desc(&tmT64);
     ptx::tma_prefetch_desc(&tmT128);
@@ -304,7 +336,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
   const int g_lo = min(G, static_cast<int>(threadIdx.x) * chunk);
   const int g_hi = min(G, g_lo + chunk);
   int local = 0;
-  for (int g = g_lo; g < g_hi; ++g) local += pair_m_tiles(goff[g + 1] - goff[g]) * n_fb;
+  for (int g = g_lo; g < g_hi; ++g) local += pair_group_tiles(goff[g + 1] - goff[g], n_fb, kShorts);
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -322,7 +354,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
   int run = warp_base + incl - local;
   for (int g = g_lo; g < g_hi; ++g) {
     tile_start[g] = run;
-    run += pair_m_tiles(goff[g + 1] - goff[g]) * n_fb;
+    run += pair_group_tiles(goff[g + 1] - goff[g], n_fb, kShorts);
   }
   if (threadIdx.x == 0) tile_start[G] = total;
   ptx::tc_fence_before();
@@ -337,9 +369,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // Lane 0 waits for the stage and arms the even CTA's barrier; then the
-    // stage's two or three boxes (weight rows in one or two boxes, token rows in
-    // one unless the gatherers copy them) are issued by lanes 0-2 as a single
-    // warp instruction.
+    // stage's boxes (weight rows in one or two boxes, token rows in one unless
+    // the gatherers copy them; a short tile's second feature block in two more)
+    // are issued by lanes 0-4 as a single warp instruction.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t n_tile = 0;
@@ -354,24 +386,31 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
           break;
         }
       }
-      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols, kShorts);
+      const bool sh = kShorts && t.n_tok <= kShortTok;   // a short block's tile
       const int half = ((t.n_tok + 15) & ~15) >> 1;      // tokens this CTA holds
-      const int tbox = half <= 32 ? 32 : (half <= 64 ? 64 : 128);
-      const CUtensorMap* mt = tbox == 32 ? &tmT32 : (tbox == 64 ? &tmT64 : &tmT128);
-      const uint32_t bytes = kWBytes + (kGather ? 0 : tbox * (BK * 2));
+      const int tbox = sh ? 16 : (half <= 32 ? 32 : (half <= 64 ? 64 : 128));
+      const CUtensorMap* mt =
+          sh ? &tmT16 : (tbox == 32 ? &tmT32 : (tbox == 64 ? &tmT64 : &tmT128));
+      const uint32_t bytes = (sh ? t.nblk : 1) * kWBytes + (kGather ? 0 : tbox * (BK * 2));
       const int trow = t.r0 + static_cast<int>(rank) * half;
       // this CTA's 128 weight rows: gate/up, the 64 up rows of its features
       // then their 64 gate rows; down, 128 consecutive output rows
       const int wrow_g = t.g * p.w_rows_per_group + t.n0 + static_cast<int>(rank) * (kFbCols / 2);
-      const int wrow0 = kGU ? wrow_g + p.half_off : wrow_g;
-      const int wrow1 = wrow_g;
       // this lane's box: lane 0 the first weight box (up rows, or the down rows),
-      // lane 1 the gate box, lane 2 the tokens
-      const bool issues = lane == 0 || (!kGather && lane == 2) || (kGU && lane == 1);
+      // lane 1 the gate box, lane 2 the tokens (a short tile's into its side
+      // slot); lanes 3 and 4 the up and gate boxes of a short tile's second
+      // feature block, into the stage's token slot
+      const bool issues = lane == 0 || (!kGather && lane == 2) || (kGU && lane == 1) ||
+                          (sh && t.nblk == 2 && (lane == 3 || lane == 4));
+      const int wl = lane >= 3 ? lane - 3 : lane;        // box within its feature block
+      const int wrow_l = wrow_g + (lane >= 3 ? kFbCols : 0);
       const CUtensorMap* mbox = lane == 2 ? mt : &tmW;
-      const int ybox = lane == 0 ? wrow0 : (lane == 1 ? wrow1 : trow);
-      const uint32_t dbox = lane == 2 ? PSmem::STAGE_T : PSmem::STAGE_W + lane * (kWBox * 128);
-      const uint32_t dstep = lane == 2 ? kTBytes : kWBytes;
+      const int ybox = lane == 2 ? trow : (kGU && wl == 0 ? wrow_l + p.half_off : wrow_l);
+      const uint32_t dbox = lane == 2 ? (sh ? PSmem::SIDE : PSmem::STAGE_T)
+                                      : (lane >= 3 ? PSmem::STAGE_T : PSmem::STAGE_W) +
+                                            wl * (kWBox * 128);
+      const uint32_t dstep = lane == 2 ? (sh ? kSideBytes : kTBytes) : (lane >= 3 ? kTBytes : kWBytes);
       for (int kb = 0; kb < nk; ++kb) {
         bool got = true;
         if (lane == 0) {
@@ -399,7 +438,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       int acc = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+        const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols, kShorts);
+        const bool sh = kShorts && t.n_tok <= kShortTok;
+        const bool two = sh && t.nblk == 2;
         const int N = (t.n_tok + 15) & ~15;
         const uint32_t idesc = ptx::idesc_bf16_f32(256, N);
         if (!wait_bar<true>(bar_tempty(acc), ((acc ? uses1 : uses0) & 1u) ^ 1u, abort_flag,
@@ -419,10 +460,20 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
           if (kGather) ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           const uint64_t dw = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_W + stage * kWBytes);
-          const uint64_t dt = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_T + stage * kTBytes);
+          // a short tile's tokens sit in the side slot, its second feature
+          // block's weights in the token slot (accumulated 128 columns on)
+          const uint64_t dt = ptx::desc_kmajor_sw128(
+              sbase + (sh ? PSmem::SIDE + stage * kSideBytes : PSmem::STAGE_T + stage * kTBytes));
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k)
             ptx::mma_bf16_pair(d, dw + 2ull * k, dt + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          if (two) {
+            const uint64_t dw2 = ptx::desc_kmajor_sw128(sbase + PSmem::STAGE_T + stage * kTBytes);
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k)
+              ptx::mma_bf16_pair(d + 128u, dw2 + 2ull * k, dt + 2ull * k, idesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+          }
           mma_any = true;
           ptx::mma_commit_pair(bar_empty(stage), 3);   // frees the stage in both CTAs
           if (++stage == kPStages) { stage = 0; phase ^= 1u; }
@@ -517,7 +568,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       uint32_t n_ready = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < total; tile += n_units) {
-        const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+        const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols, kShorts);
         const int half = ((t.n_tok + 15) & ~15) >> 1;
         const int lo = t.r0 + static_cast<int>(rank) * half;        // this CTA's rows
         const int cnt = min(half, t.n_tok - static_cast<int>(rank) * half);  // real ones
@@ -549,7 +600,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = unit; ok && tile < total; tile += n_units) {
-      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
+      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols, kShorts);
       const int half = ((t.n_tok + 15) & ~15) >> 1;      // rows this CTA holds (multiple of 8)
       const int tok0 = static_cast<int>(rank) * half;    // its first token of the tile
       const int n_m = max(0, min(16, (half - 64 * gw) >> 2));  // warp instructions per stage
@@ -621,10 +672,19 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       return ea < nt.n_tok ? (p.row_to_pair ? __ldg(p.row_to_pair + r) : r) : -1;
     };
     int nd = -1;
-    if (!kGU && unit < total) nd = dst_of(pair_tile(unit, tile_start, goff, G, n_fb, kFbCols));
+    if (!kGU && unit < total) nd = dst_of(pair_tile(unit, tile_start, goff, G, n_fb, kFbCols, kShorts));
     for (int tile = unit; tile < total; tile += n_units) {
-      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols);
-      const int col0 = t.n0 + static_cast<int>(rank) * (kFbCols / 2);  // this CTA's first column
+      const PTile t = pair_tile(tile, tile_start, goff, G, n_fb, kFbCols, kShorts);
+      // A short tile's two feature blocks are accumulated 128 columns apart;
+      // group eg takes block eg, all its tokens in one chunk.  Otherwise the
+      // groups take the tile's 32-token chunks in turn.
+      const bool sh = kShorts && t.n_tok <= kShortTok;
+      const bool has = sh ? eg < t.nblk : 32 * eg < t.n_tok;
+      const int jbeg = sh ? 0 : 32 * eg;
+      const int jstep = sh ? kTokBlock : 64;
+      const uint32_t tcol = sh ? static_cast<uint32_t>(eg * 128) : 0u;
+      // this CTA's first output column
+      const int col0 = t.n0 + (sh ? eg * kFbCols : 0) + static_cast<int>(rank) * (kFbCols / 2);
       int* dst_t = s_dst + acc * kTokBlock;     // meta of this tile (double-buffered by slot)
       float* w_t = s_w + acc * kTokBlock;
       int d = -1;
@@ -633,7 +693,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
         d = nd;
         if (p.pair_weight && d >= 0) w = __ldg(p.pair_weight + d);
         if (tile + n_units < total)
-          nd = dst_of(pair_tile(tile + n_units, tile_start, goff, G, n_fb, kFbCols));
+          nd = dst_of(pair_tile(tile + n_units, tile_start, goff, G, n_fb, kFbCols, kShorts));
       }
       const bool landed =
           wait_bar(bar_tfull(acc), (acc ? uses1 : uses0) & 1u, abort_flag, p.status, wait_ns);
@@ -650,17 +710,17 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
       ptx::tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTokBlock);
-      if (32 * eg >= t.n_tok) {  // no chunk for this group: its warps free the accumulator now
+      if (!has) {  // no chunk for this group: its warps free the accumulator now
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
       }
 #pragma unroll 1
-      for (int j0 = 32 * eg; j0 < t.n_tok; j0 += 64) {
+      for (int j0 = jbeg; has && j0 < t.n_tok; j0 += jstep) {
         uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + j0, v);
+        ptx::tmem_ld_32x32b_x32(taddr + tcol + static_cast<uint32_t>(j0), v);
         ptx::tmem_ld_wait();
-        if (j0 + 64 >= t.n_tok) {  // this warp's last TMEM read of the tile: free the accumulator
+        if (j0 + jstep >= t.n_tok) {  // this warp's last TMEM read of the tile: free the accumulator
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive_remote_relaxed(tempty_leader + 8u * acc);
@@ -810,7 +870,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmT32,
 
 // The pair kernels' grid: clusters of two CTAs, as many as can be resident.
 template <int kEpi, int kSrc>
-int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtensorMap& tw,
+int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[4], const CUtensorMap& tw,
                        PairParams p, long long tiles, cudaStream_t stream) {
   auto kern = pair_gemm_kernel<kEpi, kSrc>;
   constexpr int kNT = pair_threads(kSrc);
@@ -861,7 +921,7 @@ int launch_pair_kernel(const char* op, const CUtensorMap (&tt)[3], const CUtenso
   p.wait_ns = pipeline_wait_ns();
   return launch_status(launch_kernel(kern, dim3(static_cast<unsigned>(2 * pairs), 1, 1),
                                      dim3(kNT, 1, 1), smem, stream, attr, 1, tt[0], tt[1],
-                                     tt[2], tw, p),
+                                     tt[2], tt[3], tw, p),
                        op);
 }
 
@@ -872,12 +932,14 @@ static long long pair_tile_bound(int P, int G, int N, int fb_cols) {
   return blocks * ((N + fb_cols - 1) / fb_cols);
 }
 
-// the token rows [rows, cols] behind three maps with 32-, 64- and 128-row boxes
-static int make_token_maps(CUtensorMap (&tt)[3], const void* base, int rows, int cols,
+// the token rows [rows, cols] behind four maps with 16-, 32-, 64- and 128-row
+// boxes (the 16-row box feeds a short tile's side slot)
+static int make_token_maps(CUtensorMap (&tt)[4], const void* base, int rows, int cols,
                            const char* op, const char* what) {
   int rc;
-  for (int i = 0; i < 3; ++i)
-    if ((rc = make_tmap(&tt[i], base, rows, cols, kTokBoxMin << i, op, what)) != MOE_OK) return rc;
+  for (int i = 0; i < 4; ++i)
+    if ((rc = make_tmap(&tt[i], base, rows, cols, (kTokBoxMin / 2) << i, op, what)) != MOE_OK)
+      return rc;
   return MOE_OK;
 }
 
@@ -885,13 +947,13 @@ int launch_pair_gateup(const char* op, const void* a_bf16, int a_rows,
                        const int32_t* a_row_gather, int gather_div, const void* w13_bf16,
                        const int32_t* group_offsets, int P, int H, int I, int G, void* act_bf16,
                        cudaStream_t stream) {
-  CUtensorMap tt[3], tw;
+  CUtensorMap tt[4], tw;
   int rc;
   if ((rc = make_tmap(&tw, w13_bf16, static_cast<long long>(G) * 2 * I, H, 64, op, "w13")) !=
       MOE_OK)
     return rc;
   if (a_row_gather) {
-    for (int i = 0; i < 3; ++i) tt[i] = tw;  // unused: the gatherer warps copy the token rows
+    for (int i = 0; i < 4; ++i) tt[i] = tw;  // unused: the gatherer warps copy the token rows
   } else if ((rc = make_token_maps(tt, a_bf16, P, H, op, "a")) != MOE_OK) {
     return rc;
   }
@@ -919,7 +981,7 @@ int launch_pair_gateup_staged(const char* op, const void* x_bf16, int T,
                               const void* w13_bf16, const int32_t* group_offsets, int P, int H,
                               int I, int G, void* act_bf16, int32_t* stage_flags,
                               unsigned int* stage_ctl, cudaStream_t stream) {
-  CUtensorMap tt[3], tw;
+  CUtensorMap tt[4], tw;
   int rc;
   if ((rc = make_tmap(&tw, w13_bf16, static_cast<long long>(G) * 2 * I, H, 64, op, "w13")) !=
       MOE_OK)
@@ -950,7 +1012,7 @@ int launch_pair_down(const char* op, const void* act_bf16, const void* w2_bf16,
                      const int32_t* group_offsets, const float* pair_weight,
                      const int32_t* row_to_pair, int P, int I, int H, int G, void* out_bf16,
                      cudaStream_t stream) {
-  CUtensorMap tt[3], tw;
+  CUtensorMap tt[4], tw;
   int rc;
   if ((rc = make_token_maps(tt, act_bf16, P, I, op, "act")) != MOE_OK) return rc;
   if ((rc = make_tmap(&tw, w2_bf16, static_cast<long long>(G) * H, I, 128, op, "w2")) != MOE_OK)
