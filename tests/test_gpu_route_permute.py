@@ -281,9 +281,9 @@ def test_permute_empty_batch_zeroes_offsets():
     assert np.array_equal(off, np.zeros(9, np.int32))
 
 
-@pytest.mark.parametrize("T", [2, 3000])
+@pytest.mark.parametrize("T", [2, 3000, 30000])
 def test_permute_flags_out_of_range_ids(T):
-    # bad ids are flagged and skipped on both the one-block and the chunked path
+    # bad ids are flagged and skipped on the one-block and the chunked paths
     K, E = 2, 4
     ids = _ids(T, K, E, 11)
     ids[1, 1] = 9
@@ -293,3 +293,37 @@ def test_permute_flags_out_of_range_ids(T):
     assert m.moe_device_status(clear=True) & m.STATUS_BAD_ID
     counts = np.bincount(ids[(ids >= 0) & (ids < E)], minlength=E)
     assert np.array_equal(np.diff(off), counts) and off[E] == T * K - 2
+
+
+def test_permute_workspace_needs_no_initialisation():
+    # the workspace's histograms start as any bytes (here all 0xFF, then what
+    # the previous call left): every call gives the same bits
+    T, K, E, H = 8192, 8, 128, 8
+    ids = _ids(T, K, E, 21, skew=True)
+    want = O.permute(ids, None, T=T, K=K, E=E, H=H)
+    P = T * K
+    wsz = m.moe_permute_workspace_size(T, K, E)
+    ws = torch.full((wsz,), 255, dtype=torch.uint8, device="cuda")
+    d_ids = to_dev(ids)
+    for _ in range(3):
+        off = empty((E + 1,), torch.int32)
+        sp, p2r = empty((P,), torch.int32), empty((P,), torch.int32)
+        m.moe_permute(d_ids, None, T, K, E, H, off, sp, p2r, None, ws, wsz)
+        for g, w_ in zip((off, sp, p2r), want[:3]):
+            assert np.array_equal(to_host(g), w_)
+    assert m.moe_device_status() == 0
+
+
+@pytest.mark.slow
+def test_permute_many_chunks():
+    # 5.6 M pairs, 10938 chunks: more chunk blocks than the GPU holds at once,
+    # and a scan of 10938 counts per expert in 32-chunk batches
+    T, K, E = 700000, 8, 128
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, E, (T, K), dtype=np.int32)
+    want = O.permute(ids, None, T=T, K=K, E=E, H=8)
+    before = launches()
+    got = gpu_permute(ids, None, T, K, E, 8)
+    assert launched_since(before, "permute_scan") == 1 and launched_since(before, "permute_place") == 1
+    for g, w_ in zip(got[:3], want[:3]):
+        assert np.array_equal(g, w_)
