@@ -381,7 +381,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     // picks the source row, and each stage copies its 64 columns (8 x 16 B)
     // with cp.async into the 128-byte-swizzled layout a TMA SWIZZLE_128B box
     // would produce (16-byte chunk c of row i lands at chunk c ^ (i % 8)).
-    // Indices outside [0, a_rows) read zeros, like a TMA out-of-bounds box.
+    // Indices outside [0, a_rows) read zeros, like a TMA out-of-bounds box, and
+    // so do the rows past the tile's group, which are never stored: at decode
+    // a tile holds one or two routed rows, and its other rows, copied from the
+    // next groups' tokens, sent every CTA's requests to the same few lines of x.
     const int i = static_cast<int>(threadIdx.x) - kThreads;
     int stage = 0;
     uint32_t phase = 0;
@@ -389,8 +392,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     bool ok = true;
     for (int tile = unit; ok && tile < total; tile += n_units) {
       const Tile t = decode_tile(tile, tile_start, goff, G, n_tiles, kBnOut, kTileM);
-      const int r = min(t.row0 + i, p.P - 1);  // rows past the group are masked later
-      const int srow = __ldg(p.row_gather + r) / p.gather_div;
+      const int srow = t.row0 + i < t.row_end ? __ldg(p.row_gather + t.row0 + i) / p.gather_div : -1;
       const bool in = srow >= 0 && srow < p.a_rows;
       const uint16_t* src = p.a + static_cast<size_t>(in ? srow : 0) * p.Kdim;
       for (int kb = 0; kb < nk; ++kb) {
