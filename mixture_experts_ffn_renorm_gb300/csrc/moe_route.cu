@@ -4,9 +4,11 @@
 //
 // Two kernels: the logits GEMM on tcgen05 tensor cores (moe_gemm.cu, f32
 // epilogue with the optional per-expert bias) and a warp-per-token selection
-// kernel.  When T x E makes few GEMM tiles (decode), the GEMM splits K into up
-// to 16 ranges that store partial sums in the workspace, and the selection
-// kernel adds them in range order (then the bias) before it selects.  Selection runs on the f32 logits themselves (softmax is monotone),
+// kernel.  When T x E makes few GEMM tiles, the GEMM splits K into up to 16
+// ranges that store partial sums in the workspace, and the selection kernel
+// adds them in range order (then the bias) before it selects.  Batches of at
+// most kSmallRouterT tokens (decode) take a CUDA-core logits kernel instead,
+// one warp per expert, which stores finished logits.  Selection runs on the f32 logits themselves (softmax is monotone),
 // so the chosen ids do not depend on exp; the weights use the bit-exact
 // binary32 exp and are summed in rank order, so they are bit-identical to the
 // sequential definition for the same logits.
@@ -66,6 +68,76 @@ __device__ __forceinline__ void shared_gate_logit(const uint16_t* __restrict__ x
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) gl_out[t] = acc;
+}
+
+// Router logits of small batches (T <= kSmallRouterT) on CUDA cores: warp w
+// owns expert w % E and the kTokWarp tokens kTokWarp (w / E), ...  Lane l owns
+// the 8-element chunks l, l + 32, ... of H.  For each block of kChunks chunks
+// the lane loads the expert's weights and the tokens' inputs all at once (one
+// memory round trip), and adds each token's products into its f32 sum by fused
+// multiply-adds in index order.  The warp adds its 32 lane sums by a
+// butterfly, and lane 0 adds the bias and stores the logits.  At these sizes
+// the tensor-core GEMM is a latency chain (a 128-row token tile, a K split
+// whose partial sums the selection adds back); here the E x T/kTokWarp warps
+// each wait for one round trip per 2048 elements of H, the router weights come
+// from L2 after their first read, and x stays in L2.
+constexpr int kSmallRouterT = 64;
+constexpr int kLogitWarps = 8;
+constexpr int kChunks = 8;     // 16-byte chunks per lane and block: 2048 of H
+constexpr int kTokWarp = 2;    // tokens per warp
+
+__global__ void __launch_bounds__(kLogitWarps * 32)
+router_logits_small(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
+                    const float* __restrict__ bias, int T, int H, int E,
+                    float* __restrict__ logits, unsigned long long* launches) {
+  count_launch(launches, MOE_KID_ROUTE_LOGITS);
+  grid_dep_wait();
+  grid_dep_launch();
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kLogitWarps + static_cast<int>(threadIdx.x >> 5);
+  const int e = w % E;
+  const int t0 = (w / E) * kTokWarp;
+  if (t0 >= T) return;
+  const int nt = min(kTokWarp, T - t0);
+  const uint16_t* wrow = wr + static_cast<size_t>(e) * H;
+  float sum[kTokWarp];
+#pragma unroll
+  for (int u = 0; u < kTokWarp; ++u) sum[u] = 0.0f;
+  for (int hb = 0; hb < H; hb += 256 * kChunks) {
+    uint4 w4[kChunks];
+    uint4 x4[kTokWarp][kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const int h = hb + 256 * c + 8 * lane;
+      w4[c] = h < H ? __ldg(reinterpret_cast<const uint4*>(wrow + h)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kTokWarp; ++u)
+        x4[u][c] = (h < H && u < nt)
+                       ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + u) * H + h))
+                       : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kTokWarp; ++u)
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t xw[4] = {x4[u][c].x, x4[u][c].y, x4[u][c].z, x4[u][c].w};
+        const uint32_t ww[4] = {w4[c].x, w4[c].y, w4[c].z, w4[c].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          sum[u] = __fmaf_rn(__uint_as_float(xw[q] << 16), __uint_as_float(ww[q] << 16), sum[u]);
+          sum[u] = __fmaf_rn(__uint_as_float(xw[q] & 0xFFFF0000u),
+                             __uint_as_float(ww[q] & 0xFFFF0000u), sum[u]);
+        }
+      }
+  }
+  const float b = bias ? __ldg(bias + e) : 0.0f;
+#pragma unroll
+  for (int u = 0; u < kTokWarp; ++u) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum[u] += __shfl_xor_sync(0xffffffffu, sum[u], o);
+    if (lane == 0 && u < nt)
+      logits[static_cast<size_t>(t0 + u) * E + e] = bias ? __fadd_rn(sum[u], b) : sum[u];
+  }
 }
 
 // Does key a (expert ia) rank above key b (expert ib): larger first, ties to
@@ -418,7 +490,9 @@ int route_impl(const char* op, const void* x_bf16, const void* w_router_bf16,
       return set_error(MOE_ERR_ALIGN, "%s: workspace must be 16-byte aligned", op);
     // K split into ranges of partial sums in the workspace, as many as it holds
     const size_t slab = static_cast<size_t>(T) * E * sizeof(float);
-    int splits = router_splits(T, H, E);
+    // small batches: finished logits from the CUDA-core kernel, no K split
+    const bool small = T <= kSmallRouterT;
+    int splits = small ? 1 : router_splits(T, H, E);
     const size_t fit = workspace ? ws_bytes / slab : 0;
     if (static_cast<size_t>(splits) > fit) splits = static_cast<int>(fit);
     float* dst = logits_out;
@@ -434,8 +508,19 @@ int route_impl(const char* op, const void* x_bf16, const void* w_router_bf16,
                          ws_bytes, logits_bytes(T, E));
       dst = static_cast<float*>(workspace);
     }
-    int rc = launch_router_logits(x_bf16, w_router_bf16, logit_bias, T, H, E, dst,
-                                  n_part, s);
+    int rc;
+    if (small) {
+      rc = launch_status(
+          launch_kernel(router_logits_small,
+                        dim3((E * ((T + kTokWarp - 1) / kTokWarp) + kLogitWarps - 1) / kLogitWarps),
+                        dim3(kLogitWarps * 32), 0, s, nullptr, 0,
+                        static_cast<const uint16_t*>(x_bf16),
+                        static_cast<const uint16_t*>(w_router_bf16), logit_bias, T, H, E, dst,
+                        device_diag().launches),
+          op);
+    } else {
+      rc = launch_router_logits(x_bf16, w_router_bf16, logit_bias, T, H, E, dst, n_part, s);
+    }
     if (rc != MOE_OK) return rc;
     logits = dst;
   } else if (logits_out && logits_out != logits_in) {

@@ -98,8 +98,10 @@ def test_router_gemm_logits_within_bound_and_selection_exact(T, H, E, K):
     assert np.array_equal(ids2, ids) and np.array_equal(w2, w)
 
 
-@pytest.mark.parametrize("T,H,E", [(16, 2048, 128), (1, 4096, 256), (2048, 4096, 256),
-                                   (40, 200, 96), (64, 1024, 32), (64, 320, 20)])
+# batches above 64 tokens (smaller ones take the CUDA-core logits kernel) that
+# make few tiles: the K split takes 16, 16, 2, 4, 16 and 5 ranges
+@pytest.mark.parametrize("T,H,E", [(65, 2048, 128), (100, 4096, 256), (2048, 4096, 256),
+                                   (96, 200, 96), (128, 1024, 32), (70, 320, 20)])
 def test_router_k_split_matches_unsplit_within_bound(T, H, E):
     # with a workspace the logits GEMM splits K into ranges whose partial sums
     # the selection adds in range order (then the bias); without one it runs
@@ -130,6 +132,30 @@ def test_router_k_split_matches_unsplit_within_bound(T, H, E):
     # the two orders round differently; the chosen sets agree except on near-ties
     same = np.all(np.sort(res[0], 1) == np.sort(res[1], 1), axis=1)
     assert same.mean() >= 0.95
+
+
+@pytest.mark.parametrize("T", [1, 5, 16, 33, 64])
+@pytest.mark.parametrize("H,E,K", [(2048, 128, 8), (4096, 256, 8), (72, 40, 3), (2048, 1000, 32)])
+def test_router_small_batch_logits_within_bound_and_selection_exact(T, H, E, K):
+    # up to 64 tokens: one CUDA-core kernel forms the finished logits (fused
+    # multiply-adds per lane in index order, a butterfly over the warp, then the
+    # bias), with or without a workspace; the selection reads them once
+    rng = np.random.default_rng(7 * T + H + E)
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = W.to_bf16_bits((0.02 * rng.standard_normal((E, H))).astype(np.float32))
+    bias = (0.5 * rng.standard_normal(E)).astype(np.float32)
+    xf, wf = bf16_to_f64(x), bf16_to_f64(wr)
+    exact = xf @ wf.T + bias
+    bound = (H + 2) * 2.0**-24 * (np.abs(xf) @ np.abs(wf).T + np.abs(bias))
+    before = launches()
+    ids, w, lo, _ = gpu_route(x, wr, bias, None, None, T, H, E, K, want_logits=True)
+    assert launched_since(before, "route_logits") == 1
+    assert np.all(np.abs(lo - exact) <= bound), float(np.max(np.abs(lo - exact) / bound))
+    want_ids, want_w, _, _ = O.route_topk(logits_in=lo, T=T, H=1, E=E, K=K)
+    assert np.array_equal(ids, want_ids)
+    assert np.array_equal(w.view(np.uint32), want_w.view(np.uint32))
+    ids2, w2, _, _ = gpu_route(x, wr, bias, None, None, T, H, E, K)
+    assert np.array_equal(ids2, ids) and np.array_equal(w2.view(np.uint32), w.view(np.uint32))
 
 
 EX_CASES = [
