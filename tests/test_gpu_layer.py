@@ -216,6 +216,49 @@ def test_staged_rows_match_the_x_perm_path(cfg):
     assert m.moe_device_status() == 0
 
 
+@pytest.mark.parametrize("cfg", [W.TINY, W.DECODE], ids=["tiny", "decode"])
+def test_host_batches_match_forward(cfg):
+    # run_host_batches: pinned host batches of different sizes go up on one
+    # stream, compute on the current one and come back on a third, with the
+    # device buffers double-buffered; every output must be the bits forward()
+    # gives for the same batch, and the tiny layer's must match the oracle
+    d = W.layer_inputs(cfg)
+    blk = _block(cfg, d)
+    rng = np.random.default_rng(11)
+    sizes = [cfg.T, max(1, cfg.T - 3), 1, cfg.T, max(1, cfg.T // 2)]
+    xs = [W.to_bf16_bits(rng.standard_normal((n, cfg.H)).astype(np.float32)) for n in sizes]
+    xs[0] = d["x"]
+    x_hosts = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in xs]
+    out_hosts = [torch.empty((n, cfg.H), dtype=torch.bfloat16).pin_memory() for n in sizes]
+    blk.run_host_batches(x_hosts, out_hosts)
+    torch.cuda.synchronize()
+    for a, o in zip(xs, out_hosts):
+        want = to_host(blk.forward(to_dev(a)))
+        assert np.array_equal(o.view(torch.int16).numpy().view(np.uint16), want)
+    if cfg is W.TINY:
+        want, _, _ = _oracle_tokens(cfg, d, range(cfg.T))
+        got = out_hosts[0].view(torch.int16).numpy().view(np.uint16)
+        nmse, _ = nmse_maxrel(bf16_to_f64(got), bf16_to_f64(want))
+        assert nmse <= GEMM_NMSE
+
+
+@pytest.mark.parametrize("cfg", [W.DECODE, W.LARGE], ids=["decode", "large"])
+def test_pdl_off_gives_the_same_bits(cfg):
+    # programmatic dependent launch only lets a kernel start its set-up early;
+    # every kernel waits for its predecessor before touching global memory, so
+    # plain stream order must give the same bits
+    d = W.layer_inputs(cfg)
+    blk = _block(cfg, d)
+    x = to_dev(d["x"])
+    on = to_host(blk.forward(x))
+    prev = m.moe_set_pdl(False)
+    try:
+        off = to_host(blk.forward(x))
+    finally:
+        m.moe_set_pdl(prev)
+    assert np.array_equal(on, off)
+
+
 @pytest.mark.slow
 def test_gemm_tilings_agree_on_prefill():
     # single-CTA and CTA-pair tiles differ only in f32 accumulation order
