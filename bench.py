@@ -513,7 +513,7 @@ def extra_layer(name, dev, steps, warmup, pk):
     cfg = layer_config(name)
     d = W.layer_inputs(cfg)
     blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
-                   I_shared=cfg.I_shared)
+                   I_shared=cfg.I_shared, gather="auto")
     x_dev = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).to(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(warmup):
@@ -576,8 +576,11 @@ def run_ours(args):
     if fp8:
         d["w13_e4m3"], d["w13_scale"] = W.quantize_fp8_block(d["w13"])
         d["w2_e4m3"], d["w2_scale"] = W.quantize_fp8_block(d["w2"])
+    # gather="auto": decode-sized calls read their routed rows of x inside the
+    # gate/up GEMM; prefill-sized ones stream x_perm
     blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device=dev,
-                   I_shared=cfg.I_shared, fp8_weights=fp8, qweights=qw, q_dequant=qd)
+                   I_shared=cfg.I_shared, fp8_weights=fp8, qweights=qw, q_dequant=qd,
+                   gather="auto")
     x_host = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     x_dev = x_host.to(dev)
     out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()

@@ -42,7 +42,8 @@ namespace moe {
 namespace gemm {
 
 constexpr int kThreads = 192;        // producer, MMA, 4 epilogue warps
-constexpr int kThreadsGather = 320;  // + 4 warps that gather A rows
+// with gathered A rows, one more thread per A row of a tile gathers it:
+// 4 more warps for 128-row tiles, 1 for 32-row tiles
 constexpr int kConverters = 256;     // FP8 weights: 8 warps that dequantise B
 constexpr int kThreadsFp8 = kThreads + kConverters;
 constexpr int A_BYTES = BM * BK * 2;
@@ -141,8 +142,8 @@ struct Smem {
 //           bf16 B tiles into a second ring, and the MMA reads A and that
 template <int kN, int kEpi, bool kGatherA, int kARows = BM, bool kFp8B = false>
 struct Cfg {
-  static_assert(kARows == BM || (!kGatherA && kARows % 8 == 0),
-                "short A tiles are TMA tiles only");
+  static_assert(kARows == BM || (kARows % 8 == 0 && (!kGatherA || kARows == 32)),
+                "short A tiles: 32 rows when gathered");
   static_assert(!kFp8B || !kGatherA, "FP8 weights: TMA A tiles");
   static constexpr int kTileM = kARows;                           // product rows per tile
   static constexpr int kABytes = kARows * BK * 2;                 // A bytes per stage
@@ -155,7 +156,7 @@ struct Cfg {
   // B boxes: gate/up loads its gate and up halves separately
   static constexpr int kBoxB = (kEpi == EPI_GATEUP) ? kN / 2 : (kN < 128 ? kN : 128);
   static constexpr int kBnOut = (kEpi == EPI_GATEUP) ? kN / 2 : kN;  // output columns per tile
-  static constexpr int kThreadsT = kFp8B ? kThreadsFp8 : (kGatherA ? kThreadsGather : kThreads);
+  static constexpr int kThreadsT = kFp8B ? kThreadsFp8 : (kGatherA ? kThreads + kARows : kThreads);
   static constexpr int kEpiCols = 64;                             // columns staged per pass
   static constexpr int kStgWarp = 32 * kEpiCols * 2;
   using S = Smem<kStages, kBBytes, kABytes, kConv, kRawBytes, 4 * kStgWarp>;
@@ -285,7 +286,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(bar_full(s), kGatherA ? 1 + BM : 1);
+      ptx::mbar_init(bar_full(s), kGatherA ? 1 + kARows : 1);
       // FP8 weights: a stage is free once the MMA and every converter are done with it
       ptx::mbar_init(bar_empty(s), kFp8B ? 1 + kConverters : 1);
     }
@@ -377,7 +378,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (kGatherA && warp >= 6) {
     // ------------------------------------------------------------ A-row gatherers
-    // Thread i owns row i of this CTA's A tile: row_gather[row] / gather_div
+    // Thread i owns row i of this CTA's A tile (128 or 32 rows): row_gather[row] / gather_div
     // picks the source row, and each stage copies its 64 columns (8 x 16 B)
     // with cp.async into the 128-byte-swizzled layout a TMA SWIZZLE_128B box
     // would produce (16-byte chunk c of row i lands at chunk c ^ (i % 8)).
@@ -1025,9 +1026,10 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   // and the tile count decides the balance; 128-wide tiles (64 gate + 64 up
   // rows) double it, which cuts the idle tail of the last round (decode layer,
   // 82 of 128 experts touched: 127 -> 115 us).  32-row tiles load 4 KB of A per
-  // stage instead of 16, so the ring keeps more weight bytes in flight.
+  // stage instead of 16 (a TMA box of x_perm, or one gatherer warp's copies of
+  // routed rows of x), so the ring keeps more weight bytes in flight.
   // Tensor-bound loads keep 128 x 256.
-  const bool narrow = !a_row_gather && static_cast<long long>(P) <= 16LL * G;
+  const bool narrow = static_cast<long long>(P) <= 16LL * G;
   CUtensorMap ta, tb;
   if ((rc = make_tmap(&tb, w13_bf16, static_cast<long long>(G) * 2 * I, H, narrow ? 64 : 128, op,
                       "w13")) != MOE_OK)
@@ -1053,6 +1055,9 @@ extern "C" int moe_grouped_gemm_gateup_silu_bf16(const void* a_bf16, int a_rows,
   p.out = act_bf16;
   p.kid = MOE_KID_GEMM_GATEUP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a_row_gather && narrow)
+    return launch<128, EPI_GATEUP, true, kNarrowRows>(op, ta, tb, p,
+                                                      tile_bound(P, G, I, 64, kNarrowRows), s);
   if (a_row_gather)
     return launch<256, EPI_GATEUP, true>(op, ta, tb, p, tile_bound(P, G, I, 128), s);
   if (narrow)

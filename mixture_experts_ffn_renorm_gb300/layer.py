@@ -52,6 +52,11 @@ class MoeBlock:
     act rows are quantized to 8-bit blocks on the device, the gate/up GEMM reads
     the token rows through sorted_pair / K (no x_perm), and the shared expert
     stays bf16 in launches of its own.
+    gather=True reads the routed rows of x inside the gate/up GEMM on every call;
+    gather="auto" does so only on calls with at most 16 routed rows per expert
+    on average (decode-sized; plain bf16 experts, no fused shared expert), where
+    the 32-row tiles gather as fast as they read x_perm and the permute's row
+    copy is saved, and materialises x_perm otherwise.
     q_dequant=True (with qweights): the GGUF blocks are expanded to bf16 once, on the
     device, when the block is built, and the layer runs the bf16 tensor-core path --
     the faster choice when the experts see many rows each (prefill-sized batches).
@@ -78,17 +83,21 @@ class MoeBlock:
         # gather=True: the gate/up GEMM reads each routed row straight from x
         # (through sorted_pair / K); False: permute materialises x_perm and the
         # GEMM streams it with tiled TMA loads
+        if gather not in (False, True, "auto"):
+            raise ValueError(f"gather must be False, True or 'auto', not {gather!r}")
         self.gather = gather
+        always = gather is True
         # fuse_shared: the shared expert's GEMMs run inside the routed GEMM
         # launches (one launch each for gate/up and down); False: own launches
         self.fp8 = fp8_weights
-        self.fuse_shared = fuse_shared and not gather and not fp8_weights and not self.qfmt
-        if fp8_weights and gather:
+        self.fuse_shared = fuse_shared and not always and not fp8_weights and not self.qfmt
+        if fp8_weights and always:
             raise ValueError("FP8 expert weights read x_perm rows (gather=False)")
         # staged=True: permute skips its row gather and the gate/up call writes
         # x_perm itself (on CTA pairs inside the GEMM launch); bf16 experts only
         self.staged = staged
-        if staged and (gather or fp8_weights or self.qfmt or (I_shared > 0 and self.fuse_shared)):
+        if staged and (gather is not False or fp8_weights or self.qfmt or
+                       (I_shared > 0 and self.fuse_shared)):
             raise ValueError("staged rows need plain bf16 experts, gather=False and no fused "
                              "shared expert")
         self.routed_scale = float(routed_scale)
@@ -128,7 +137,7 @@ class MoeBlock:
         self.expert_offsets = torch.empty((E + 1,), dtype=i32, device=dv)
         self.sorted_pair = torch.empty((P,), dtype=i32, device=dv)
         self.pair_to_row = torch.empty((P,), dtype=i32, device=dv)
-        self.x_perm = None if gather else torch.empty((P, H), dtype=bf, device=dv)
+        self.x_perm = None if always else torch.empty((P, H), dtype=bf, device=dv)
         # zero-filled once, then passed unchanged to every staged call
         self.ws_staged = (torch.zeros(max(16, moe_gateup_staged_workspace_size(P)),
                                       dtype=torch.uint8, device=dv) if staged else None)
@@ -178,11 +187,14 @@ class MoeBlock:
                        self.topk_ids, self.topk_w, None,
                        self.gate_logit if self.has_shared else None, ws, ws.numel(), stream)
         mark("route")
-        moe_permute(self.topk_ids, x, T, K, E, H, self.expert_offsets, self.sorted_pair,
-                    self.pair_to_row, None if self.staged else self.x_perm, ws, ws.numel(),
-                    stream)
-        mark("permute")
         fused = self.has_shared and self.fuse_shared
+        gathered = self.gather is True or (
+            self.gather == "auto" and P <= 16 * E and not fused and not self.staged
+            and not self.fp8 and not self.qfmt)
+        moe_permute(self.topk_ids, x, T, K, E, H, self.expert_offsets, self.sorted_pair,
+                    self.pair_to_row, None if (self.staged or gathered) else self.x_perm, ws,
+                    ws.numel(), stream)
+        mark("permute")
         if self.qfmt:
             moe_quantize_act_q8(x, T, H, self.qfmt, self.x_q, self.x_s, stream)
             mark("quant_x")
@@ -202,7 +214,7 @@ class MoeBlock:
                                                      self.w13, self.expert_offsets, P, H, I, E,
                                                      self.act, self.ws_staged,
                                                      self.ws_staged.numel(), stream)
-        elif self.gather:
+        elif gathered:
             moe_grouped_gemm_gateup_silu_bf16(x, T, self.sorted_pair, K, self.w13,
                                               self.expert_offsets, P, H, I, E, self.act, None, 0,
                                               stream)

@@ -82,3 +82,14 @@ def test_layer_refuses_a_cpu_device():
     cfg = W.TINY
     with pytest.raises(ValueError, match="CUDA device"):
         MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, {"w_router": None}, max_tokens=cfg.T, device="cpu")
+
+
+def test_layer_refuses_an_unknown_gather_mode():
+    cfg = W.TINY
+    with pytest.raises(ValueError, match="gather must be"):
+        MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, {"w_router": None}, max_tokens=cfg.T, device="cuda",
+                 gather="sometimes")
+    # "auto" with staged rows is refused like gather=True
+    with pytest.raises(ValueError, match="staged rows"):
+        MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, {"w_router": None}, max_tokens=cfg.T, device="cuda",
+                 gather="auto", staged=True)

@@ -242,6 +242,24 @@ def test_host_batches_match_forward(cfg):
         assert nmse <= GEMM_NMSE
 
 
+@pytest.mark.parametrize("cfg,gathers", [(W.DECODE, True), (W.PREFILL, False), (W.LARGE, False)],
+                         ids=["decode", "prefill", "large"])
+def test_gather_auto_picks_by_rows_per_expert(cfg, gathers):
+    # gather="auto": at most 16 routed rows per expert (decode) read x inside the
+    # gate/up GEMM and the permute copies no rows; larger batches (and the fused
+    # shared expert of the large layer) keep x_perm.  The bits are those of the
+    # x_perm path either way.
+    d = W.layer_inputs(cfg)
+    x = to_dev(d["x"])
+    want = to_host(_block(cfg, d).forward(x))
+    blk = MoeBlock(cfg.H, cfg.I, cfg.E, cfg.K, d, max_tokens=cfg.T, device="cuda",
+                   I_shared=cfg.I_shared, gather="auto")
+    before = launches()
+    got = to_host(blk.forward(x))
+    assert launched_since(before, "permute_gather") == (0 if gathers else 1)
+    assert np.array_equal(got, want)
+
+
 @pytest.mark.parametrize("cfg", [W.DECODE, W.LARGE], ids=["decode", "large"])
 def test_pdl_off_gives_the_same_bits(cfg):
     # programmatic dependent launch only lets a kernel start its set-up early;
