@@ -147,6 +147,64 @@ __device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
   return ka > kb || (ka == kb && ia < ib);
 }
 
+// The warp's top-K of one token for the plain router (at most 8 entries a lane):
+// lane j < K receives the j-th pick, its id and the value it reports.  Each
+// lane sorts its entries once by the selection order (key descending, ties to
+// the lower id); every pick then compares only the lanes' heads, and the
+// winning lane shifts its list.  Entries past E get key 0 and an id >= E, so
+// they rank below every expert (a NaN expert, also key 0, wins the tie on its
+// lower id) and are never reached, since K <= E.
+template <int kPerLane>
+__device__ __forceinline__ void select_sorted_heads(const uint32_t (&key)[kPerLane],
+                                                    const float (&sc)[kPerLane], int E, int K,
+                                                    int lane, float& my_sel, int& my_id) {
+  uint32_t hk[kPerLane];
+  uint32_t hid[kPerLane];
+  float hv[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int e = lane + 32 * i;
+    hk[i] = e < E ? key[i] : 0u;
+    hid[i] = static_cast<uint32_t>(e);
+    hv[i] = sc[i];
+  }
+  // odd-even transposition sort: kPerLane rounds of neighbour exchanges
+#pragma unroll
+  for (int r = 0; r < kPerLane; ++r)
+#pragma unroll
+    for (int i = r & 1; i + 1 < kPerLane; i += 2) {
+      const bool sw = hk[i + 1] > hk[i] || (hk[i + 1] == hk[i] && hid[i + 1] < hid[i]);
+      const uint32_t k0 = hk[i], i0 = hid[i];
+      const float v0 = hv[i];
+      hk[i] = sw ? hk[i + 1] : k0;
+      hid[i] = sw ? hid[i + 1] : i0;
+      hv[i] = sw ? hv[i + 1] : v0;
+      hk[i + 1] = sw ? k0 : hk[i + 1];
+      hid[i + 1] = sw ? i0 : hid[i + 1];
+      hv[i + 1] = sw ? v0 : hv[i + 1];
+    }
+  for (int j = 0; j < K; ++j) {
+    const uint32_t top = __reduce_max_sync(0xffffffffu, hk[0]);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, hk[0] == top ? hid[0] : 0xFFFFFFFFu);
+    const int owner = static_cast<int>(win & 31u);
+    const float wv = __shfl_sync(0xffffffffu, hv[0], owner);
+    if (owner == lane) {
+#pragma unroll
+      for (int i = 0; i + 1 < kPerLane; ++i) {
+        hk[i] = hk[i + 1];
+        hid[i] = hid[i + 1];
+        hv[i] = hv[i + 1];
+      }
+      hk[kPerLane - 1] = 0u;
+      hid[kPerLane - 1] = 0xFFFFFFFFu;
+    }
+    if (lane == j) {
+      my_sel = wv;
+      my_id = static_cast<int>(win);
+    }
+  }
+}
+
 // One warp selects the top-K of one token.  The weights' exps are then
 // evaluated by the whole block, one (token, rank) pair per thread, so that
 // they run on full warps (a warp instruction costs the same with 8 or 32
@@ -296,57 +354,7 @@ topk_kernel(const float* __restrict__ logits, int n_part, const float* __restric
       }
     }
     if (!kEx && kPerLane <= 8) {
-      // Each lane sorts its entries once by the selection order (key
-      // descending, ties to the lower id); every pick then compares only the
-      // lanes' heads, and the winning lane shifts its list.  Entries past E
-      // get key 0 and an id >= E, so they rank below every expert (a NaN
-      // expert, also key 0, wins the tie on its lower id) and are never
-      // reached, since K <= E.
-      uint32_t hk[kPerLane];
-      uint32_t hid[kPerLane];
-      float hv[kPerLane];
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        hk[i] = e < E ? key[i] : 0u;
-        hid[i] = static_cast<uint32_t>(e);
-        hv[i] = sc[i];
-      }
-      // odd-even transposition sort: kPerLane rounds of neighbour exchanges
-#pragma unroll
-      for (int r = 0; r < kPerLane; ++r)
-#pragma unroll
-        for (int i = r & 1; i + 1 < kPerLane; i += 2) {
-          const bool sw = hk[i + 1] > hk[i] || (hk[i + 1] == hk[i] && hid[i + 1] < hid[i]);
-          const uint32_t k0 = hk[i], i0 = hid[i];
-          const float v0 = hv[i];
-          hk[i] = sw ? hk[i + 1] : k0;
-          hid[i] = sw ? hid[i + 1] : i0;
-          hv[i] = sw ? hv[i + 1] : v0;
-          hk[i + 1] = sw ? k0 : hk[i + 1];
-          hid[i + 1] = sw ? i0 : hid[i + 1];
-          hv[i + 1] = sw ? v0 : hv[i + 1];
-        }
-      for (int j = 0; j < K; ++j) {
-        const uint32_t top = __reduce_max_sync(0xffffffffu, hk[0]);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, hk[0] == top ? hid[0] : 0xFFFFFFFFu);
-        const int owner = static_cast<int>(win & 31u);
-        const float wv = __shfl_sync(0xffffffffu, hv[0], owner);
-        if (owner == lane) {
-#pragma unroll
-          for (int i = 0; i + 1 < kPerLane; ++i) {
-            hk[i] = hk[i + 1];
-            hid[i] = hid[i + 1];
-            hv[i] = hv[i + 1];
-          }
-          hk[kPerLane - 1] = 0u;
-          hid[kPerLane - 1] = 0xFFFFFFFFu;
-        }
-        if (lane == j) {
-          my_sel = wv;
-          my_id = static_cast<int>(win);
-        }
-      }
+      select_sorted_heads<kPerLane>(key, sc, E, K, lane, my_sel, my_id);
     } else {
     for (int j = 0; j < K; ++j) {
       // this lane's best untaken entry (ascending id, so ties keep the lower id)

@@ -135,8 +135,10 @@ def test_router_k_split_matches_unsplit_within_bound(T, H, E):
 
 
 @pytest.mark.parametrize("T", [1, 5, 16, 33, 64])
-@pytest.mark.parametrize("H,E,K", [(2048, 128, 8), (4096, 256, 8), (72, 40, 3), (2048, 1000, 32)])
-def test_router_small_batch_logits_within_bound_and_selection_exact(T, H, E, K):
+@pytest.mark.parametrize("H,E,K", [(2048, 128, 8), (4096, 256, 8), (72, 40, 3), (2048, 1000, 32),
+                                   (64, 8, 2), (200, 300, 6)])
+@pytest.mark.parametrize("renorm", [1, 0])
+def test_router_small_batch_logits_within_bound_and_selection_exact(T, H, E, K, renorm):
     # up to 64 tokens: one CUDA-core kernel forms the finished logits (fused
     # multiply-adds per lane in index order, a butterfly over the warp, then the
     # bias), with or without a workspace; the selection reads them once
@@ -148,13 +150,13 @@ def test_router_small_batch_logits_within_bound_and_selection_exact(T, H, E, K):
     exact = xf @ wf.T + bias
     bound = (H + 2) * 2.0**-24 * (np.abs(xf) @ np.abs(wf).T + np.abs(bias))
     before = launches()
-    ids, w, lo, _ = gpu_route(x, wr, bias, None, None, T, H, E, K, want_logits=True)
+    ids, w, lo, _ = gpu_route(x, wr, bias, None, None, T, H, E, K, renorm, want_logits=True)
     assert launched_since(before, "route_logits") == 1
     assert np.all(np.abs(lo - exact) <= bound), float(np.max(np.abs(lo - exact) / bound))
-    want_ids, want_w, _, _ = O.route_topk(logits_in=lo, T=T, H=1, E=E, K=K)
+    want_ids, want_w, _, _ = O.route_topk(logits_in=lo, T=T, H=1, E=E, K=K, renormalize=renorm)
     assert np.array_equal(ids, want_ids)
     assert np.array_equal(w.view(np.uint32), want_w.view(np.uint32))
-    ids2, w2, _, _ = gpu_route(x, wr, bias, None, None, T, H, E, K)
+    ids2, w2, _, _ = gpu_route(x, wr, bias, None, None, T, H, E, K, renorm)
     assert np.array_equal(ids2, ids) and np.array_equal(w2.view(np.uint32), w.view(np.uint32))
 
 
