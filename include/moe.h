@@ -249,12 +249,15 @@ int moe_permute_noalloc(const int32_t* topk_ids, const void* x_bf16, int T, int 
  *                a_row_gather[r] / gather_div.  With sorted_pair and gather_div = K
  *                this reads every routed row straight from x [T,H] (no x_perm);
  *                extra warps copy the rows into shared memory with 16-byte
- *                cp.async (four per CTA on single-CTA tiles, two per CTA on
- *                CTA-pair tiles).  An index outside [0, a_rows) reads zeros.
- *                The result is bit-identical to passing the gathered rows as
- *                `a`; on this GPU the copies through the SMs' load path are
- *                slower than a separate x_perm pass plus tiled TMA loads, so
- *                the x_perm form is the faster one at every measured size.
+ *                cp.async (four per CTA on 128-row single-CTA tiles, one on the
+ *                32-row tiles of calls with at most 16 rows per group on
+ *                average, two per CTA on CTA-pair tiles).  An index outside
+ *                [0, a_rows) reads zeros.  The result is bit-identical to
+ *                passing the gathered rows as `a`.  On this GPU the copies
+ *                through the SMs' load path are slower than a separate x_perm
+ *                pass plus tiled TMA loads on prefill-sized calls; on decode-
+ *                sized calls (32-row tiles) the gathered form is as fast and
+ *                saves the x_perm pass.
  *   gather_div   >= 1 when gathering (ignored otherwise)
  *   w13          bf16 [G, 2I, H]: gate rows first, then up rows, per group
  *   group_offsets int32 [G+1], non-decreasing, group_offsets[G] <= P;
