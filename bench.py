@@ -42,20 +42,25 @@ def recorded_traffic(workload, weights="bf16"):
     import hashlib
 
     if weights == "bf16":
-        name = "gemm_gateup_traffic.txt"
+        names = ("gemm_gateup_traffic.txt", "gemm_gateup_traffic_large.txt")
         srcs = ("moe_gemm.cu", "moe_gemm_pair.cu", "gemm_common.cuh", "sm100_ptx.cuh")
     elif weights in Q_WEIGHTS:
-        name, srcs = f"qgemm_gateup_{weights}_traffic.txt", ("moe_qgemm.cu", "sm100_ptx.cuh")
+        names, srcs = (f"qgemm_gateup_{weights}_traffic.txt",), ("moe_qgemm.cu", "sm100_ptx.cuh")
     else:
         return None
-    path = os.path.join(ROOT, "profiles", name)
-    if not os.path.exists(path):
-        return None
     kv = {}
-    for ln in open(path):
-        if "=" in ln and not ln.startswith("#"):
-            k, v = ln.strip().split("=", 1)
-            kv[k] = v
+    for name in names:  # the record of this workload, if one is committed
+        path = os.path.join(ROOT, "profiles", name)
+        if not os.path.exists(path):
+            continue
+        rec = {}
+        for ln in open(path):
+            if "=" in ln and not ln.startswith("#"):
+                k, v = ln.strip().split("=", 1)
+                rec[k] = v
+        if rec.get("workload") == workload:
+            kv = rec
+            break
     h = hashlib.sha256()
     for f in srcs:
         with open(os.path.join(ROOT, "mixture_experts_ffn_renorm_gb300", "csrc", f), "rb") as fh:
