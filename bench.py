@@ -42,7 +42,8 @@ def recorded_traffic(workload, weights="bf16"):
     import hashlib
 
     if weights == "bf16":
-        names = ("gemm_gateup_traffic.txt", "gemm_gateup_traffic_large.txt")
+        names = ("gemm_gateup_traffic.txt", "gemm_gateup_traffic_decode.txt",
+                 "gemm_gateup_traffic_large.txt")
         srcs = ("moe_gemm.cu", "moe_gemm_pair.cu", "gemm_common.cuh", "sm100_ptx.cuh")
     elif weights in Q_WEIGHTS:
         names, srcs = (f"qgemm_gateup_{weights}_traffic.txt",), ("moe_qgemm.cu", "sm100_ptx.cuh")
