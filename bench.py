@@ -651,9 +651,14 @@ def run_ours(args):
     # tiles for P >= 1024 rows averaging >= 32 per group, unless the shared expert
     # rides in the same launch (single-CTA tiles)
     pair = P >= 1024 and P >= 32 * cfg.E and not cfg.I_shared
+    # at most 16 rows per group: 32-row, 128-wide tiles, the routed rows of x
+    # gathered inside the launch (the layer is built with gather="auto")
+    narrow = P <= 16 * cfg.E
     kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
              f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qk else
              "pair_gemm_kernel<gateup> (CTA-pair gate/up GEMM + SiLU-mul)" if pair else
+             "grouped_gemm_kernel<128,gateup,gathered,32 rows> (gate/up GEMM + SiLU-mul)"
+             if narrow and not cfg.I_shared else
              "grouped_gemm_kernel<256,gateup> (gate/up GEMM + SiLU-mul)")
     traffic_key = "bf16" if qd else args.weights
     if tensor_bound:
