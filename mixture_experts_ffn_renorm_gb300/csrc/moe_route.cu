@@ -8,10 +8,11 @@
 // ranges that store partial sums in the workspace, and the selection kernel
 // adds them in range order (then the bias) before it selects.  Batches of at
 // most kSmallRouterT tokens (decode) take a CUDA-core logits kernel instead,
-// one warp per expert, which stores finished logits.  Selection runs on the f32 logits themselves (softmax is monotone),
-// so the chosen ids do not depend on exp; the weights use the bit-exact
-// binary32 exp and are summed in rank order, so they are bit-identical to the
-// sequential definition for the same logits.
+// one warp per expert and two tokens, which stores finished logits.
+// Selection runs on the f32 logits themselves (softmax is monotone), so the
+// chosen ids do not depend on exp; the weights use the bit-exact binary32 exp
+// and are summed in rank order, so they are bit-identical to the sequential
+// definition for the same logits.
 #include <math.h>
 
 #include "moe_common.cuh"
