@@ -106,6 +106,31 @@ def test_gateup_silu_gathered_rows(sizes, H, I, K, tiling):
     assert_gemm_close(to_host(act), want, "gathered gate/up")
 
 
+@pytest.mark.parametrize("sizes,H,I", [([40, 0, 70, 1, 33] + [0] * 11, 256, 192),
+                                       ([600, 5, 256, 255, 513], 256, 256)],
+                         ids=["32-row tiles", "128-row tiles"])
+def test_gateup_silu_gathered_rows_outside_x(sizes, H, I, tiling):
+    # a gathered row whose source index lies outside [0, a_rows) reads zeros, on
+    # the decode-sized 32-row tiles (one gatherer warp) and on 128-row tiles
+    K = 4
+    off, P, G, _, W13, _ = _case(sizes, H, I, 41 + H)
+    rng = np.random.default_rng(P)
+    T = (P + K - 1) // K + 1
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    pair = rng.integers(0, T * K, P).astype(np.int32)
+    pair[::13] = T * K + 3                            # row T: outside x
+    pair[5::29] = -K                                  # row -1: outside x
+    src = pair // K
+    ok = (src >= 0) & (src < T)
+    want = O.gateup_silu(np.concatenate([x, np.zeros((1, H), np.uint16)]), W13, off, P=P, H=H,
+                         I=I, G=G, a_row_gather=np.where(ok, src, T).astype(np.int32))
+    act = empty((P, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(x), T, to_dev(pair), K, to_dev(W13), to_dev(off), P,
+                                        H, I, G, act)
+    assert m.moe_device_status() == 0
+    assert_gemm_close(to_host(act), want, "gathered gate/up, rows outside x")
+
+
 @pytest.mark.parametrize("sizes,H,I", SHAPES + [([300, 0, 520], 2048, 768)])
 def test_down_weight_scatter(sizes, H, I, tiling):
     off, P, G, _, _, W2 = _case(sizes, H, I, sum(sizes) + I)
