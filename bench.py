@@ -654,6 +654,7 @@ def run_ours(args):
     # at most 16 rows per group: 32-row, 128-wide tiles, the routed rows of x
     # gathered inside the launch (the layer is built with gather="auto")
     narrow = P <= 16 * cfg.E
+    gathered = bool(qk) or (narrow and not cfg.I_shared and not fp8)
     kname = ("grouped_gemm_kernel<gateup, FP8 weights> (gate/up GEMM + SiLU-mul)" if fp8 else
              f"qgemm_kernel<{qw}, gateup> (keep-quant gate/up + SiLU-mul, dp4a)" if qk else
              "pair_gemm_kernel<gateup> (CTA-pair gate/up GEMM + SiLU-mul)" if pair else
@@ -693,7 +694,10 @@ def run_ours(args):
         "combine_gbs": comb_bytes / (stage_avg["combine"] / 1000.0) / 1e9,
         "combine_frac_hbm": comb_bytes / (stage_avg["combine"] / 1000.0) / 1e9 / pk["hbm_gbs"],
         "route_gbs": (cfg.T * cfg.H * 2 + cfg.E * cfg.H * 2) / (stage_avg["route"] / 1000.0) / 1e9,
-        "permute_gbs": (2 * P * cfg.H * 2 + P * 16) / (stage_avg["permute"] / 1000.0) / 1e9,
+        # with gathered rows the permute writes no x_perm (indices only)
+        "permute_gbs": ((0 if gathered else 2 * P * cfg.H * 2) + P * 16)
+                       / (stage_avg["permute"] / 1000.0) / 1e9,
+        "gateup_rows": "gathered from x" if gathered else "x_perm",
         "hbm_peak_gbs": pk["hbm_gbs"],
         "stages_sum_ms": sum(stage_avg.values()),
     }
