@@ -260,6 +260,27 @@ def test_gather_auto_picks_by_rows_per_expert(cfg, gathers):
     assert np.array_equal(got, want)
 
 
+def test_two_blocks_on_two_streams_at_once():
+    # the library keeps no per-call state outside the caller's buffers: two
+    # layers enqueued on two streams without ordering between them give the
+    # bits each gives alone
+    cfgs = [W.DECODE, W.PREFILL]
+    ds = [W.layer_inputs(c) for c in cfgs]
+    blks = [_block(c, d) for c, d in zip(cfgs, ds)]
+    xs = [to_dev(d["x"]) for d in ds]
+    alone = [to_host(b.forward(x)) for b, x in zip(blks, xs)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = [None, None]
+    for rep in range(3):
+        for i in (1, 0):
+            with torch.cuda.stream(streams[i]):
+                outs[i] = blks[i].forward(xs[i], stream=streams[i].cuda_stream)
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert np.array_equal(to_host(outs[i]), alone[i]), (rep, cfgs[i].name)
+
+
 @pytest.mark.parametrize("cfg", [W.DECODE, W.LARGE], ids=["decode", "large"])
 def test_pdl_off_gives_the_same_bits(cfg):
     # programmatic dependent launch only lets a kernel start its set-up early;
