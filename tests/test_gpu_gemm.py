@@ -151,6 +151,32 @@ def test_down_weight_scatter(sizes, H, I, tiling):
         assert_gemm_close(to_host(out), want, "down")
 
 
+@pytest.mark.parametrize("G", [513, 1024])
+def test_most_groups_both_gemms(G, tiling):
+    # more groups than a CTA-pair launch takes (512): the single-CTA schedule
+    # tables at up to their 1024 groups, most groups empty or of one to three
+    # rows (32-row tiles) -- gate/up and down against the oracle
+    rng = np.random.default_rng(G)
+    sizes = [int(v) for v in rng.choice([0, 0, 1, 2, 3, 40], G)]
+    sizes[-1] = 70                                   # the last group spans three 32-row tiles
+    H, I = 128, 64
+    off, P, G_, A, W13, W2 = _case(sizes, H, I, G + 5)
+    want = O.gateup_silu(A, W13, off, P=P, H=H, I=I, G=G_)
+    act = empty((P, I), torch.bfloat16)
+    m.moe_grouped_gemm_gateup_silu_bf16(to_dev(A), P, None, 1, to_dev(W13), to_dev(off), P, H, I,
+                                        G_, act)
+    assert m.moe_device_status() == 0
+    assert_gemm_close(to_host(act), want, "gate/up, many groups")
+    wts = rng.uniform(0.05, 1.0, P).astype(np.float32)
+    r2p = rng.permutation(P).astype(np.int32)
+    want_d = O.down(want, W2, off, P=P, I=I, H=H, G=G_, pair_weight=wts, row_to_pair=r2p)
+    out = empty((P, H), torch.bfloat16)
+    m.moe_grouped_gemm_down_bf16(to_dev(want), to_dev(W2), to_dev(off), to_dev(wts), to_dev(r2p), P,
+                                 I, H, G_, out)
+    assert m.moe_device_status() == 0
+    assert_gemm_close(to_host(out), want_d, "down, many groups")
+
+
 FUSED = [
     # routed group sizes, H, I, shared rows Ts, shared I_s (ragged tiles on both sides)
     ([3, 200, 0, 77], 512, 256, 130, 192),
