@@ -40,7 +40,8 @@ ARMS = [(BF16, BF16, BF16), (F32, F32, F32), (BF16, F32, F32), (F32, BF16, BF16)
 
 
 @pytest.mark.parametrize("eo_dt,sh_dt,out_dt", ARMS)
-@pytest.mark.parametrize("T,K,H", [(1, 1, 8), (7, 3, 40), (33, 8, 264), (5, 20, 16)])
+@pytest.mark.parametrize("T,K,H", [(1, 1, 8), (7, 3, 40), (33, 8, 264), (5, 20, 16), (3, 32, 8),
+                                   (2, 64, 8)])
 @pytest.mark.parametrize("rs", [1.0, 0.7])
 def test_combine_bit_exact(eo_dt, sh_dt, out_dt, T, K, H, rs):
     rng = np.random.default_rng(T * 100 + K * 10 + H)
@@ -167,3 +168,14 @@ def test_refusals_enqueue_nothing():
     assert after == before
     # T = 0 is a legal no-op
     assert m.moe_combine(out, BF16, None, None, BF16, 1.0, 0, K, H, out, BF16) == 0
+
+
+def test_empty_batch_enqueues_nothing():
+    # T = 0: every combine and gate op returns at once, with no launch
+    d = empty((16,), torch.float32)
+    before = launches()
+    m.moe_combine(d, BF16, None, None, BF16, 1.0, 0, 8, 64, d, BF16)
+    m.moe_combine_gate(d, BF16, None, d, BF16, d, 1.0, 0, 8, 64, d, BF16)
+    m.shared_expert_gate(d, BF16, d, 0, 64, d, BF16)
+    for k in ("combine", "combine_gate", "shared_gate", "gate_sigmoid"):
+        assert launched_since(before, k) == 0, k
