@@ -202,8 +202,9 @@ def test_router_ex_bit_exact_from_logits(E, K, scoring, n_group, topk_group, gsc
 
 
 def test_router_ex_through_the_logits_gemm():
-    # DeepSeek-V3-like routing of 16 and 300 tokens: logits from the tensor-core
-    # GEMM (with the K split), ids and weights exact given those logits
+    # DeepSeek-V3-like routing of 16 and 300 tokens: logits from the CUDA-core
+    # kernel (16 tokens) and from the tensor-core GEMM with its K split (300),
+    # ids and weights exact given those logits
     E, K, H = 256, 8, 1024
     rng = np.random.default_rng(8)
     wr = W.to_bf16_bits((0.02 * rng.standard_normal((E, H))).astype(np.float32))
