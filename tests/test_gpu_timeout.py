@@ -133,3 +133,37 @@ def test_wait_limit_expiry_is_reported_and_the_device_stays_usable(tiling):
     want_out = O.down(got_act, W2, off, P=P, I=I, H=H, G=G, pair_weight=wts, row_to_pair=r2p,
                       rows=rows)
     assert_gemm_close(got_out[r2p[rows]], want_out[r2p[rows]], "down after a timeout")
+
+
+def test_wait_limit_expiry_on_decode_sized_gathered_tiles():
+    # few rows per group (P <= 16 G): 32-row tiles whose rows one gatherer warp
+    # copies from x; the 1 us limit makes every launch give up and report it,
+    # and with the limit restored the gathered call gives the x_perm call's bits
+    rng = np.random.default_rng(16)
+    G, H, I = 128, 2048, 2048
+    sizes = rng.choice([0, 1, 1, 2, 3], G)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(off[-1])
+    K = 8
+    T = (P + K - 1) // K + 1
+    x = W.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    pair = rng.permutation(T * K)[:P].astype(np.int32)
+    W13 = W.to_bf16_bits((0.02 * rng.standard_normal((G, 2 * I, H))).astype(np.float32))
+    dx, dpair, dW13, doff = to_dev(x), to_dev(pair), to_dev(W13), to_dev(off)
+    act = empty((P, I), torch.bfloat16)
+    m.moe_set_wait_limit_ns(1000)
+    before = launches()
+    assert m.moe_grouped_gemm_gateup_silu_bf16(dx, T, dpair, K, dW13, doff, P, H, I, G, act) == m.OK
+    torch.cuda.synchronize()
+    assert launched_since(before, "gemm_gateup") == 1
+    assert m.moe_device_status(clear=True) & m.STATUS_TIMEOUT
+    m.moe_set_wait_limit_ns(FULL_LIMIT_NS)
+    assert m.moe_grouped_gemm_gateup_silu_bf16(dx, T, dpair, K, dW13, doff, P, H, I, G, act) == m.OK
+    ref = empty((P, I), torch.bfloat16)
+    xp = to_dev(x[pair // K])
+    assert m.moe_grouped_gemm_gateup_silu_bf16(xp, P, None, 1, dW13, doff, P, H, I, G, ref) == m.OK
+    torch.cuda.synchronize()
+    assert m.moe_device_status() == 0
+    assert np.array_equal(to_host(act), to_host(ref))
+    want = O.gateup_silu(x, W13, off, P=P, H=H, I=I, G=G, a_row_gather=(pair // K).astype(np.int32))
+    assert_gemm_close(to_host(act), want, "gathered gate/up on 32-row tiles after a timeout")
